@@ -1,0 +1,455 @@
+"""Decode-attention benchmark of libkvq on one GB300 (or N replicas).
+
+One step = one decode step of the whole model: for every layer, append the
+new token's K/V (kvq_append) and attend over the cache (kvq_decode_attn).
+Default workload: Llama-2-7B-shaped decode, 32 layers x 32 heads, head dim
+128, batch 8, context 4096, uniform KV4 cache (K per-channel over 32-token
+groups, V per-token over 64-channel groups, 4 sink + 64 recent fp16 tokens).
+The same step on a plain fp16 cache is timed beside it.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import signal
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "llama2_7b_kv4_t4k"
+METRIC = "decode-attention µs/step and effective cache GB/s (fraction of 8 TB/s HBM) at 1 GB300"
+UNIT = "us/step"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-fp16-baseline", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ bytes
+
+def algorithmic_bytes(cfg: dict, T: int) -> int:
+    """Bytes one decode launch must move: packed codes, scales, CSR outliers
+    and fp16 sink/window tokens of every stream (each read once per KV head),
+    plus q in and out."""
+    from oracle import kvq_oracle as O  # only for the shared window rule counts
+    S, Nq, W = O.layout_counts(cfg, T)
+    d = cfg["head_dim"]
+    NS = cfg["batch"] * cfg["n_kv_heads"]
+    kb, vb = cfg["k_bits"], cfg["v_bits"]
+    per = 0
+    if kb != 16:
+        per += Nq * (d * kb // 8 + d * vb // 8)
+        if kb == 3:
+            k = cfg["outliers_per_vector"]
+            per += Nq * 4 * 2 + 2 * ((Nq + 1) * 4 + Nq * k * 3)
+        else:
+            per += (Nq // 32) * d * 4 + Nq * (d // cfg["v_group_channels"]) * 4
+    per += (S + W) * d * 2 * 2
+    qo = cfg["batch"] * cfg["n_q_heads"] * d * 2 * 2
+    return NS * per + qo
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"kvq_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.send_signal(signal.SIGTERM)
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = [r.split(",") for r in open(self.path).read().strip().splitlines() if r.count(",") >= 8]
+        os.unlink(self.path)
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]
+                          and "Not" not in r[5 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# ------------------------------------------------------------------- peaks
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def ncu_traffic(kernel_tag: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    h = source_hash()
+    for line in open(path):
+        m = re.match(r"\s*(\S+)\s+src=(\w+)\s+traffic_per_launch=(\d+)", line)
+        if m and m.group(1) == kernel_tag and m.group(2) == h:
+            return int(m.group(3))
+    return None
+
+
+def source_hash() -> str:
+    hs = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_kv_cache_07_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.startswith("kvq_decode"):
+            hs.update(open(os.path.join(csrc, f), "rb").read())
+    return hs.hexdigest()[:12]
+
+
+# --------------------------------------------------------------- the model
+
+class Model:
+    """All layers of one workload: caches filled to T-1 tokens, plus the
+    per-layer inputs of one decode step."""
+
+    def __init__(self, name: str, device, fp16: bool):
+        import torch
+        from bit_kv_cache_07_gb300 import binding, synth, workloads
+        w = workloads.WORKLOADS[name]
+        self.name, self.T = name, w["tokens"]
+        self.L = w["layers"]
+        self.cfgs, self.layers = [], []
+        self.q, self.k_new, self.v_new, self.out = [], [], [], []
+        for l in range(self.L):
+            cfg = workloads.layer_config(name, l)
+            if cfg["k_bits"] == 3:
+                cfg["k_lut"] = synth.nuq_lut(name, l, "k")
+                cfg["v_lut"] = synth.nuq_lut(name, l, "v")
+            if fp16:
+                cfg = workloads.fp16_baseline_config(cfg)
+            layer = binding.Layer(cfg, device=device)
+            K, V = synth.layer_kv(name, l, tokens=self.T - 1, device=device)
+            layer.append(0, K, V)
+            del K, V
+            self.cfgs.append(cfg)
+            self.layers.append(layer)
+            self.q.append(synth.query(name, l, device=device))
+            k, v = synth.new_token_kv(name, l, 0, device=device)
+            self.k_new.append(k)
+            self.v_new.append(v)
+            self.out.append(torch.empty_like(self.q[-1]))
+        ws_bytes = max(binding.kvq_layout_query(c).workspace_bytes for c in self.cfgs)
+        self.ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=device)
+        torch.cuda.synchronize()
+        self.binding = binding
+
+    def step(self, stream, ev=None):
+        B = self.binding
+        for l in range(self.L):
+            c = self.layers[l]
+            B.kvq_append(c.cfg, c.buf, self.T - 1, self.k_new[l], self.v_new[l], 1, stream)
+            if ev is not None:
+                ev[l][0].record(stream)
+            B.kvq_decode_attn(c.cfg, c.buf, self.T, self.q[l], self.out[l], None, self.ws, None, stream)
+            if ev is not None:
+                ev[l][1].record(stream)
+
+    def decode_bytes(self):
+        return sum(algorithmic_bytes(c, self.T) for c in self.cfgs)
+
+    def launches_per_step(self):
+        n = 0
+        for c in self.cfgs:
+            n += 1  # fp16 window copy of the appended token
+            n += 1  # decode
+        return n
+
+
+def time_steps(model, stream, steps: int, warmup: int, per_kernel=True):
+    import torch
+    for _ in range(warmup):
+        model.step(stream)
+    torch.cuda.synchronize()
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+            for _ in range(model.L)] for _ in range(steps)] if per_kernel else None
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(steps):
+        model.step(stream, evs[i] if per_kernel else None)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    total_ms = t0.elapsed_time(t1)
+    kern = None
+    if per_kernel:
+        kern = [evs[i][l][0].elapsed_time(evs[i][l][1]) for i in range(steps) for l in range(model.L)]
+    return total_ms, kern
+
+
+def time_e2e(model, stream, steps: int, warmup: int):
+    """Same step through the public API with this step's inputs copied in from
+    pinned host memory and the outputs copied back, inside the timed region."""
+    import torch
+    hq = [t.cpu().pin_memory() for t in model.q]
+    hk = [t.cpu().pin_memory() for t in model.k_new]
+    hv = [t.cpu().pin_memory() for t in model.v_new]
+    ho = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in model.out]
+    h2d = sum(t.numel() * t.element_size() for t in hq + hk + hv)
+    d2h = sum(t.numel() * t.element_size() for t in ho)
+
+    def one():
+        with torch.cuda.stream(stream):
+            for l in range(model.L):
+                model.q[l].copy_(hq[l], non_blocking=True)
+                model.k_new[l].copy_(hk[l], non_blocking=True)
+                model.v_new[l].copy_(hv[l], non_blocking=True)
+            model.step(stream)
+            for l in range(model.L):
+                ho[l].copy_(model.out[l], non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    t0.record(stream)
+    for _ in range(steps):
+        one()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    return t0.elapsed_time(t1) / steps, h2d, d2h
+
+
+# --------------------------------------------------------- distributed bits
+
+_DIST = {"on": False}
+
+
+def init_dist(n: int):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        _DIST["on"] = True
+    return rank, ws, local
+
+
+def barrier():
+    if _DIST["on"]:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float) -> float:
+    if not _DIST["on"]:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float) -> float:
+    if not _DIST["on"]:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# -------------------------------------------------------------- CPU oracle
+
+def oracle_sample(name: str, seconds: float, layer_count: int | None = None):
+    """Time the CPU oracle (single thread, as written) decoding whole streams of
+    layer 0 at the workload's context until ~seconds have passed; scale the
+    per-stream time to one full decode step (all streams of all layers)."""
+    import numpy as np
+    import torch
+    from bit_kv_cache_07_gb300 import synth, workloads
+    from oracle import kvq_oracle as O
+    w = workloads.WORKLOADS[name]
+    T = w["tokens"]
+    cfg = workloads.layer_config(name, 0)
+    if cfg["k_bits"] == 3:
+        cfg["k_lut"] = synth.nuq_lut(name, 0, "k")
+        cfg["v_lut"] = synth.nuq_lut(name, 0, "v")
+    g = w["n_q_heads"] // w["n_kv_heads"]
+    K, V = synth.layer_kv(name, 0, tokens=T, batch=1, device="cpu")
+    q = synth.query(name, 0, batch=1, device="cpu").numpy()
+    Kh, Vh = K.numpy(), V.numpy()
+    n, spent = 0, 0.0
+    while spent < seconds and n < w["n_kv_heads"]:
+        store = O.build_stream(cfg, Kh[0, n], Vh[0, n])
+        t0 = time.perf_counter()
+        O.decode_stream(cfg, T, store, q[0, n * g:(n + 1) * g])
+        spent += time.perf_counter() - t0
+        n += 1
+    streams_per_step = w["layers"] * w["batch"] * w["n_kv_heads"]
+    per_stream = spent / n
+    return {
+        "value": per_stream * streams_per_step * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "sample": f"fp64 oracle decode of {n} (batch row, KV head) streams of layer 0 at T={T}, "
+                  f"{per_stream * 1e3:.1f} ms each, scaled x{streams_per_step / n:.0f} to one "
+                  f"{w['layers']}-layer step; cache build not timed",
+    }
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from bit_kv_cache_07_gb300 import workloads
+    w = workloads.WORKLOADS[args.workload]
+    per_step = []
+    budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+    for i in range(args.warmup + args.steps):
+        r = oracle_sample(args.workload, budget)
+        if i >= args.warmup:
+            per_step.append(r["value"])
+    v = statistics.median(per_step)
+    cb = dict(r)
+    cb["value"] = v
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "layers": w["layers"], "batch": w["batch"],
+                   "q_heads": w["n_q_heads"], "kv_heads": w["n_kv_heads"], "context": w["tokens"]},
+        "cpu_baseline": cb, "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# -------------------------------------------------------------------- main
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    rank, world, local = init_dist(args.gpus)
+    import __graft_entry__
+    __graft_entry__.build()
+    from bit_kv_cache_07_gb300 import workloads
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    w = workloads.WORKLOADS[args.workload]
+
+    model = Model(args.workload, dev, fp16=False)
+    clocks = ClockSampler(local)
+    clocks.start()
+    total_ms, kern = time_steps(model, stream, args.steps, args.warmup)
+    clk = clocks.stop()
+    ms_step = max_over_ranks(total_ms / args.steps)
+    dec_bytes = model.decode_bytes()
+    kern_ms = statistics.mean(kern)
+    peak, peak_kind = measured_peaks()
+    achieved = (dec_bytes / model.L) / (kern_ms * 1e-3) / 1e9
+    e2e_ms, h2d, d2h = time_e2e(model, stream, max(3, args.steps // 2), 2)
+    e2e_ms = max_over_ranks(e2e_ms)
+    launches = model.launches_per_step() * args.steps
+    del model
+    torch.cuda.empty_cache()
+
+    fp16 = None
+    if not args.no_fp16_baseline:
+        fmodel = Model(args.workload, dev, fp16=True)
+        f_ms, f_kern = time_steps(fmodel, stream, args.steps, args.warmup)
+        f_ms = max_over_ranks(f_ms / args.steps)
+        f_bytes = fmodel.decode_bytes()
+        fp16 = {"us_per_step": f_ms * 1e3, "cache_gbs": f_bytes / (f_ms * 1e-3) / 1e9,
+                "decode_kernel_us": statistics.mean(f_kern) * 1e3,
+                "decode_kernel_gbs": (f_bytes / fmodel.L) / (statistics.mean(f_kern) * 1e-3) / 1e9,
+                "bytes_per_step": f_bytes}
+        del fmodel
+        torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_sample(args.workload, args.cpu_seconds)
+
+    value = ms_step * 1e3
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "layers": w["layers"], "batch": w["batch"],
+                   "q_heads": w["n_q_heads"], "kv_heads": w["n_kv_heads"], "head_dim": w["head_dim"],
+                   "context": w["tokens"], "cache": w["pairs"], "n_sink": w["n_sink"], "n_recent": w["n_recent"],
+                   "l2": "inputs larger than L2: %.2f GB of cache read per step" % (dec_bytes / 1e9),
+                   "step": "per layer: kvq_append of 1 token + kvq_decode_attn"},
+        "cache_gbs": sum_over_ranks(dec_bytes / (ms_step * 1e-3) / 1e9),
+        "cache_bytes_per_step": dec_bytes,
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": ncu_traffic(f"decode:{args.workload}"),
+                     "bytes_per_launch": dec_bytes / (w["layers"]),
+                     "launch_us": kern_ms * 1e3},
+        "fp16_baseline": fp16,
+        "speedup_vs_fp16": (fp16["us_per_step"] / value) if fp16 else None,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if _DIST["on"]:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,215 @@
+"""Thin ctypes binding of libkvq's C ABI (include/kvq.h).
+
+Argument marshalling only: every step of the method runs in the CUDA
+kernels of libkvq.so.  There is no fallback: if the library is missing the
+import of any entry point raises.
+
+Tensors are torch CUDA tensors (or raw device addresses as ints); the
+binding checks device, dtype, contiguity and size before calling so that a
+wrong pointer becomes a Python exception rather than a GPU fault.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+from . import build as _build
+
+KVQ_OK = 0
+STATUS = {0: "KVQ_OK", -1: "KVQ_ERR_INVALID_ARG", -2: "KVQ_ERR_UNSUPPORTED",
+          -3: "KVQ_ERR_CAPACITY", -4: "KVQ_ERR_WORKSPACE", -5: "KVQ_ERR_CUDA"}
+
+
+class KvqError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)} ({kvq_status_string(status)})")
+
+
+class kvq_config(C.Structure):
+    _fields_ = [
+        ("batch", C.c_int32), ("n_q_heads", C.c_int32), ("n_kv_heads", C.c_int32),
+        ("head_dim", C.c_int32), ("max_tokens", C.c_int32), ("k_bits", C.c_int32),
+        ("v_bits", C.c_int32), ("k_group_tokens", C.c_int32), ("v_group_channels", C.c_int32),
+        ("n_sink", C.c_int32), ("n_recent", C.c_int32), ("v_hadamard", C.c_int32),
+        ("k_pre_rope", C.c_int32), ("rope_theta", C.c_float), ("outliers_per_vector", C.c_int32),
+        ("k_lut", C.c_float * 8), ("v_lut", C.c_float * 8), ("softmax_scale", C.c_float),
+        ("split_tokens", C.c_int32),
+    ]
+
+
+class kvq_region(C.Structure):
+    _fields_ = [("offset", C.c_uint64), ("bytes", C.c_uint64)]
+
+
+REGIONS = ["k_codes", "k_scales", "v_codes", "v_scales", "k_sink", "v_sink", "k_ring", "v_ring",
+           "k_csr_rowptr", "k_csr_col", "k_csr_val", "v_csr_rowptr", "v_csr_col", "v_csr_val"]
+
+
+class kvq_layout(C.Structure):
+    _fields_ = [(n, kvq_region) for n in REGIONS] + [
+        ("layer_bytes", C.c_uint64), ("workspace_bytes", C.c_uint64), ("max_splits", C.c_int32),
+        ("ring_slots", C.c_int32), ("q_cap", C.c_int32)]
+
+
+EXPORTS = ["kvq_layout_query", "kvq_append", "kvq_decode_attn", "kvq_decode_plan",
+           "kvq_status_string"]
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded libkvq.so.  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it first (python -m bit_kv_cache_07_gb300.build)")
+        L = C.CDLL(path)
+        vp, u16p = C.c_void_p, C.c_void_p
+        L.kvq_layout_query.argtypes = [C.POINTER(kvq_config), C.POINTER(kvq_layout)]
+        L.kvq_layout_query.restype = C.c_int
+        L.kvq_append.argtypes = [C.POINTER(kvq_config), vp, C.c_int32, u16p, u16p, C.c_int32, vp]
+        L.kvq_append.restype = C.c_int
+        L.kvq_decode_attn.argtypes = [C.POINTER(kvq_config), vp, C.c_int32, u16p, u16p, vp, vp,
+                                      C.c_uint64, vp]
+        L.kvq_decode_attn.restype = C.c_int
+        L.kvq_decode_plan.argtypes = [C.POINTER(kvq_config), C.c_int32, C.POINTER(C.c_int32),
+                                      C.POINTER(C.c_int32)]
+        L.kvq_decode_plan.restype = C.c_int
+        L.kvq_status_string.argtypes = [C.c_int]
+        L.kvq_status_string.restype = C.c_char_p
+        _lib = L
+    return _lib
+
+
+def kvq_status_string(status: int) -> str:
+    return lib().kvq_status_string(int(status)).decode()
+
+
+def make_config(d: dict) -> kvq_config:
+    """kvq_config from a dict with the same field names (missing -> 0)."""
+    c = kvq_config()
+    for name, ctype in kvq_config._fields_:
+        if name in ("k_lut", "v_lut"):
+            for i, v in enumerate(d.get(name, [0.0] * 8)):
+                getattr(c, name)[i] = float(v)
+        elif name in d:
+            setattr(c, name, float(d[name]) if ctype is C.c_float else int(d[name]))
+    return c
+
+
+def _cfg(cfg) -> kvq_config:
+    return cfg if isinstance(cfg, kvq_config) else make_config(cfg)
+
+
+def _check(fn: str, st: int):
+    if st != KVQ_OK:
+        raise KvqError(fn, st)
+
+
+def kvq_layout_query(cfg) -> kvq_layout:
+    out = kvq_layout()
+    _check("kvq_layout_query", lib().kvq_layout_query(C.byref(_cfg(cfg)), C.byref(out)))
+    return out
+
+
+def kvq_decode_plan(cfg, tokens: int):
+    a, b = C.c_int32(), C.c_int32()
+    _check("kvq_decode_plan", lib().kvq_decode_plan(C.byref(_cfg(cfg)), int(tokens), C.byref(a), C.byref(b)))
+    return a.value, b.value
+
+
+def _ptr(t, what: str, dtype=None, numel: int | None = None, allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{what} is required")
+    if isinstance(t, int):
+        return t
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{what}: expected a torch tensor or a device address")
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{what} must be {dtype}, got {t.dtype}")
+    if numel is not None and t.numel() * t.element_size() < numel:
+        raise ValueError(f"{what} too small: {t.numel() * t.element_size()} < {numel} bytes")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def kvq_append(cfg, layer_buf, tokens_before: int, k_new, v_new, n_new: int, stream=None):
+    import torch
+    c = _cfg(cfg)
+    lay = kvq_layout_query(c)
+    row = c.batch * c.n_kv_heads * int(n_new) * c.head_dim * 2
+    st = lib().kvq_append(C.byref(c), _ptr(layer_buf, "layer_buf", numel=lay.layer_bytes), int(tokens_before),
+                          _ptr(k_new, "k_new", torch.float16, row), _ptr(v_new, "v_new", torch.float16, row),
+                          int(n_new), _stream(stream))
+    _check("kvq_append", st)
+
+
+def kvq_decode_attn(cfg, layer_buf, tokens: int, q, out, lse=None, workspace=None, ws_bytes=None,
+                    stream=None):
+    import torch
+    c = _cfg(cfg)
+    lay = kvq_layout_query(c)
+    nq = c.batch * c.n_q_heads * c.head_dim * 2
+    if ws_bytes is None:
+        ws_bytes = 0 if workspace is None else (
+            workspace if isinstance(workspace, int) else workspace.numel() * workspace.element_size())
+        if isinstance(workspace, int):
+            raise ValueError("ws_bytes is required with a raw workspace address")
+    st = lib().kvq_decode_attn(
+        C.byref(c), _ptr(layer_buf, "layer_buf", numel=lay.layer_bytes), int(tokens),
+        _ptr(q, "q", torch.float16, nq), _ptr(out, "out", torch.float16, nq),
+        _ptr(lse, "lse", torch.float32, c.batch * c.n_q_heads * 4, allow_none=True),
+        _ptr(workspace, "workspace", allow_none=True), int(ws_bytes), _stream(stream))
+    _check("kvq_decode_attn", st)
+
+
+# ------------------------------------------------------------ conveniences
+
+class Layer:
+    """One layer's cache: a zeroed device buffer of layer_bytes plus its
+    config.  ``append`` / ``decode`` call the C ABI."""
+
+    def __init__(self, cfg: dict, device="cuda"):
+        import torch
+        self.cfg_dict = dict(cfg)
+        self.cfg = make_config(cfg)
+        self.layout = kvq_layout_query(self.cfg)
+        self.buf = torch.zeros(self.layout.layer_bytes, dtype=torch.uint8, device=device)
+
+    def region(self, name: str):
+        r = getattr(self.layout, name)
+        return self.buf[r.offset:r.offset + r.bytes]
+
+    def append(self, tokens_before: int, k_new, v_new, stream=None):
+        kvq_append(self.cfg, self.buf, tokens_before, k_new, v_new, k_new.shape[2], stream)
+
+    def decode(self, tokens: int, q, out, lse=None, workspace=None, stream=None):
+        kvq_decode_attn(self.cfg, self.buf, tokens, q, out, lse, workspace, None, stream)
+
+
+def new_workspace(cfg, device="cuda"):
+    """A zeroed decode workspace of layout.workspace_bytes (counters at zero)."""
+    import torch
+    lay = kvq_layout_query(_cfg(cfg))
+    return torch.zeros(max(int(lay.workspace_bytes), 16), dtype=torch.uint8, device=device)

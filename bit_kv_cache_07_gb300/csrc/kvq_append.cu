@@ -1,0 +1,300 @@
+// kvq_append.cu -- cache write path: fp16 window/sink copies and the
+// quantize-and-pack kernel that flushes G_K-token groups.
+//
+// Method (page title, section):
+//  * "KVTuner" review, observation 2: K quantized per channel, asymmetric
+//    (min/scale), here over groups of G_K = 32 tokens.
+//  * InnerQ, Methodology 1-2: V grouped along the hidden dimension (G_V
+//    channels) per token, one min and one shared scale per group;
+//    Methodology 4: the most recent and the sink tokens stay fp16.
+//  * KVQuant, technical approach: non-uniform per-layer levels and
+//    per-vector dense-and-sparse outliers (~1 %), pre-RoPE K (K is written
+//    as given; RoPE happens in the decode).
+//  * Hadamard write-up, "section details": V rotated by a Hadamard matrix
+//    before the uniform quantizer.
+//
+// The fp32 quantizer is evaluated with explicitly rounded intrinsics
+// (__fsub_rn, __fdiv_rn, rintf) so that no operation is contracted or
+// approximated: codes and scales are bit-reproducible.
+#include "kvq_internal.cuh"
+
+namespace kvq {
+namespace {
+
+constexpr int kRowHalves = kHeadDim;          // 128 fp16 per token row
+constexpr int kRowVec = kRowHalves * 2 / 16;  // 16 x 16-byte chunks per row
+
+// Uniform asymmetric quantizer of one value given its group's min and the
+// fp32 scale: clamp(rint((x - min) / scale), 0, 2^b - 1); scale 0 -> 0.
+__device__ __forceinline__ uint32_t uniform_code(float x, float mn, float scale, float qmax) {
+  if (scale == 0.0f) return 0u;
+  float r = rintf(__fdiv_rn(__fsub_rn(x, mn), scale));
+  r = fminf(fmaxf(r, 0.0f), qmax);
+  return (uint32_t)r;
+}
+
+// Non-uniform (LUT) encoding of one 128-channel token vector held by a warp
+// (lane l owns channels 4l..4l+3).  The k largest |x| (ties to the lower
+// channel) become fp16 outliers with code 0; the dense rest is mapped
+// affinely onto [L0, L7] and coded by counting the level midpoints below it.
+__device__ void nuq_encode_row(const uint16_t* __restrict__ xrow, const float* lut, int k,
+                               uint8_t* __restrict__ code_row, uint32_t* minsc_out,
+                               uint8_t* col_out, uint16_t* val_out, int lane) {
+  float v[4];
+  bool is_out[4] = {false, false, false, false};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) v[q] = half_bits_to_float(xrow[4 * lane + q]);
+  int sel[kMaxOutliers];
+  for (int j = 0; j < k; ++j) {
+    float bv = -1.0f;
+    int bi = 1 << 30;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (!is_out[q]) {
+        float a = fabsf(v[q]);
+        if (a > bv) { bv = a; bi = 4 * lane + q; }
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+    }
+    sel[j] = bi;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (bi == 4 * lane + q) is_out[q] = true;
+  }
+  float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (!is_out[q]) { mn = fminf(mn, v[q]); mx = fmaxf(mx, v[q]); }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  const float s = __fdiv_rn(__fsub_rn(mx, mn), __fsub_rn(lut[7], lut[0]));
+  float tau[7];
+#pragma unroll
+  for (int i = 0; i < 7; ++i) tau[i] = __fsub_rn(__fmul_rn(__fadd_rn(lut[i], lut[i + 1]), 0.5f), lut[0]);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t c = 0;
+    if (!is_out[q] && s != 0.0f) {
+      const float u = __fdiv_rn(__fsub_rn(v[q], mn), s);
+#pragma unroll
+      for (int i = 0; i < 7; ++i) c += (u > tau[i]) ? 1u : 0u;
+    }
+    code_row[4 * lane + q] = (uint8_t)c;
+  }
+  if (lane == 0) {
+    // ascending column order for the CSR row
+    for (int a = 1; a < k; ++a) {
+      int x = sel[a], b = a - 1;
+      while (b >= 0 && sel[b] > x) { sel[b + 1] = sel[b]; --b; }
+      sel[b + 1] = x;
+    }
+    for (int j = 0; j < k; ++j) {
+      col_out[j] = (uint8_t)sel[j];
+      val_out[j] = xrow[sel[j]];
+    }
+    *minsc_out = (uint32_t)float_to_half_bits(mn) | ((uint32_t)float_to_half_bits(s) << 16);
+  }
+}
+
+// In-warp normalised Hadamard rotation of one token vector (lane l owns
+// channels 4l..4l+3): fp32 butterflies of width 1, 2, 4, ..., 64, each
+// (a, b) -> (a + b, a - b), then times fp32(1/sqrt(d)) and round to fp16.
+__device__ void hadamard_row_inplace(uint16_t* row, float c, int lane) {
+  float v[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) v[q] = half_bits_to_float(row[4 * lane + q]);
+  float a0 = __fadd_rn(v[0], v[1]), a1 = __fsub_rn(v[0], v[1]);
+  float a2 = __fadd_rn(v[2], v[3]), a3 = __fsub_rn(v[2], v[3]);
+  v[0] = __fadd_rn(a0, a2); v[2] = __fsub_rn(a0, a2);
+  v[1] = __fadd_rn(a1, a3); v[3] = __fsub_rn(a1, a3);
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[q], m);
+      v[q] = upper ? __fsub_rn(o, v[q]) : __fadd_rn(v[q], o);
+    }
+  }
+  __syncwarp();
+#pragma unroll
+  for (int q = 0; q < 4; ++q) row[4 * lane + q] = float_to_half_bits(__fmul_rn(v[q], c));
+  __syncwarp();
+}
+
+// Pack rows of 8-bit codes (one byte per channel in shared memory) into the
+// little-endian bitstream layout and store them as 32-bit words.
+__device__ void pack_rows(const uint8_t (*codes)[kHeadDim], int bits, int rows, uint8_t* dst,
+                          int row_bytes, int tid) {
+  const int words = row_bytes / 4;
+  for (int idx = tid; idx < rows * words; idx += kThreads) {
+    const int r = idx / words, wi = idx % words;
+    uint32_t word = 0;
+    if (32 % bits == 0) {
+      const int per = 32 / bits, c0 = wi * per;
+      for (int m = 0; m < per; ++m) word |= (uint32_t)codes[r][c0 + m] << (m * bits);
+    } else {
+      for (int p = 0; p < 32; ++p) {
+        const int gb = wi * 32 + p;
+        word |= (uint32_t)((codes[r][gb / bits] >> (gb % bits)) & 1) << p;
+      }
+    }
+    reinterpret_cast<uint32_t*>(dst + (size_t)r * row_bytes)[wi] = word;
+  }
+}
+
+// One CTA quantizes one G_K-token group of one stream (K and V).
+__global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_constant__ AppendParams p) {
+  const Geometry& G = p.geo;
+  const int grp = p.first_group + blockIdx.x;
+  const int s = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+
+  __shared__ __align__(16) uint16_t sK[kGroupTokens][kRowHalves];
+  __shared__ __align__(16) uint16_t sV[kGroupTokens][kRowHalves];
+  __shared__ uint8_t sCk[kGroupTokens][kHeadDim];
+  __shared__ uint8_t sCv[kGroupTokens][kHeadDim];
+
+  // fp16 sources: tokens written before this call come from the window ring,
+  // the others straight from this call's input.
+  for (int idx = tid; idx < kGroupTokens * kRowVec; idx += kThreads) {
+    const int r = idx / kRowVec, ch = idx % kRowVec;
+    const int t = G.S + grp * kGroupTokens + r;
+    const uint16_t *srck, *srcv;
+    if (t >= p.tokens_before) {
+      const size_t off = ((size_t)s * p.n_new + (t - p.tokens_before)) * kRowHalves;
+      srck = p.k_new + off;
+      srcv = p.v_new + off;
+    } else {
+      const size_t off = ((size_t)s * G.ring + (t - G.S) % G.ring) * kRowHalves;
+      srck = p.L.k_ring + off;
+      srcv = p.L.v_ring + off;
+    }
+    reinterpret_cast<uint4*>(&sK[r][0])[ch] = reinterpret_cast<const uint4*>(srck)[ch];
+    reinterpret_cast<uint4*>(&sV[r][0])[ch] = reinterpret_cast<const uint4*>(srcv)[ch];
+  }
+  __syncthreads();
+
+  const int i0 = grp * kGroupTokens;  // quantized index of the group's first token
+  const int kmax = G.nout;
+
+  // ---- K
+  if (G.kb == 3) {
+    for (int r = w; r < kGroupTokens; r += 4) {
+      const int i = i0 + r;
+      const size_t csr = (size_t)s * G.qcap * kmax + (size_t)i * kmax;
+      nuq_encode_row(sK[r], p.k_lut, kmax, sCk[r], &p.L.k_scales[(size_t)s * G.qcap + i],
+                     p.L.k_col + csr, p.L.k_val + csr, lane);
+      if (lane == 0) {
+        int32_t* rp = p.L.k_rowptr + (size_t)s * (G.qcap + 1);
+        rp[i + 1] = (i + 1) * kmax;
+        if (i == 0) rp[0] = 0;
+      }
+    }
+  } else {
+    const int c = tid;  // one channel per thread, over the group's tokens
+    float mn = half_bits_to_float(sK[0][c]), mx = mn;
+    for (int r = 1; r < kGroupTokens; ++r) {
+      const float x = half_bits_to_float(sK[r][c]);
+      mn = fminf(mn, x);
+      mx = fmaxf(mx, x);
+    }
+    const float qmax = (float)((1 << G.kb) - 1);
+    const float scale = __fdiv_rn(__fsub_rn(mx, mn), qmax);
+    for (int r = 0; r < kGroupTokens; ++r)
+      sCk[r][c] = (uint8_t)uniform_code(half_bits_to_float(sK[r][c]), mn, scale, qmax);
+    p.L.k_scales[((size_t)s * G.gcap + grp) * kHeadDim + c] =
+        (uint32_t)float_to_half_bits(mn) | ((uint32_t)float_to_half_bits(scale) << 16);
+  }
+
+  // ---- V (optionally rotated first)
+  for (int r = w; r < kGroupTokens; r += 4) {
+    const int i = i0 + r;
+    if (G.hadamard) hadamard_row_inplace(sV[r], p.hadamard_c, lane);
+    if (G.vb == 3) {
+      const size_t csr = (size_t)s * G.qcap * kmax + (size_t)i * kmax;
+      nuq_encode_row(sV[r], p.v_lut, kmax, sCv[r], &p.L.v_scales[(size_t)s * G.qcap + i],
+                     p.L.v_col + csr, p.L.v_val + csr, lane);
+      if (lane == 0) {
+        int32_t* rp = p.L.v_rowptr + (size_t)s * (G.qcap + 1);
+        rp[i + 1] = (i + 1) * kmax;
+        if (i == 0) rp[0] = 0;
+      }
+    } else {
+      float v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) v[q] = half_bits_to_float(sV[r][4 * lane + q]);
+      float mn = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
+      float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+      const int seg = G.gv / 4;  // lanes per channel group
+      for (int o = seg / 2; o > 0; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      }
+      const float qmax = (float)((1 << G.vb) - 1);
+      const float scale = __fdiv_rn(__fsub_rn(mx, mn), qmax);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) sCv[r][4 * lane + q] = (uint8_t)uniform_code(v[q], mn, scale, qmax);
+      if (lane % seg == 0)
+        p.L.v_scales[((size_t)s * G.qcap + i) * G.nvg + lane / seg] =
+            (uint32_t)float_to_half_bits(mn) | ((uint32_t)float_to_half_bits(scale) << 16);
+    }
+  }
+  __syncthreads();
+
+  pack_rows(sCk, G.kb, kGroupTokens, p.L.k_codes + ((size_t)s * G.qcap + i0) * G.krow, G.krow, tid);
+  pack_rows(sCv, G.vb, kGroupTokens, p.L.v_codes + ((size_t)s * G.qcap + i0) * G.vrow, G.vrow, tid);
+}
+
+// Copy the fp16 tokens of this call that stay fp16 (sinks and the final
+// window) into their slots.  One thread per 16-byte chunk of a K or V row.
+__global__ void __launch_bounds__(256) append_window_kernel(const __grid_constant__ AppendParams p) {
+  const Geometry& G = p.geo;
+  const size_t total = (size_t)G.NS * p.n_new * (2 * kRowVec);
+  for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (size_t)gridDim.x * blockDim.x) {
+    const int ch = (int)(idx % kRowVec);
+    const int isv = (int)((idx / kRowVec) % 2);
+    const size_t rest = idx / (2 * kRowVec);
+    const int j = (int)(rest % p.n_new);
+    const int s = (int)(rest / p.n_new);
+    const int pos = p.tokens_before + j;
+    uint16_t* dst;
+    if (G.fp16_mode) {
+      dst = (isv ? p.L.v_ring : p.L.k_ring) + ((size_t)s * G.ring + pos) * kRowHalves;
+    } else if (pos < G.S) {
+      dst = (isv ? p.L.v_sink : p.L.k_sink) + ((size_t)s * G.S + pos) * kRowHalves;
+    } else if (pos >= G.S + p.nq_after) {
+      dst = (isv ? p.L.v_ring : p.L.k_ring) + ((size_t)s * G.ring + (pos - G.S) % G.ring) * kRowHalves;
+    } else {
+      continue;  // quantized by this call
+    }
+    const uint16_t* src = (isv ? p.v_new : p.k_new) + ((size_t)s * p.n_new + j) * kRowHalves;
+    reinterpret_cast<uint4*>(dst)[ch] = reinterpret_cast<const uint4*>(src)[ch];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_append_quantize(const AppendParams& p, int n_groups, cudaStream_t st) {
+  dim3 grid(n_groups, p.geo.NS);
+  append_quantize_kernel<<<grid, kThreads, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append_window(const AppendParams& p, cudaStream_t st) {
+  const size_t total = (size_t)p.geo.NS * p.n_new * (2 * kRowVec);
+  size_t blocks = (total + 255) / 256;
+  if (blocks > 152 * 64) blocks = 152 * 64;
+  append_window_kernel<<<(unsigned)blocks, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -1,0 +1,671 @@
+// kvq_decode.cuh -- fused dequantize-and-attend decode kernel (split-K over
+// the context, last-CTA log-sum-exp merge), CUDA-core fp32 version.
+//
+// Method (page title, section):
+//  * InnerQ, Methodology 3 and 5: dequantization fused with the GEMV in one
+//    pass; a group's scale is loaded once and reused by every element of
+//    the group.  Here the per-channel K scales of a 32-token group are folded
+//    into the query once per group (q'_c = q_c * scale_c, bias = q . min),
+//    and the per-token V scales are folded into the softmax weight
+//    (p'_t = p_t * scale_t), so codes are used as plain small integers.
+//  * InnerQ, Methodology 4: fp16 sink and recent tokens attended in the
+//    same launch.
+//  * KVQuant, technical approach: pre-RoPE K -- RoPE is applied to each
+//    dequantized key at its position; non-uniform codes index a per-layer
+//    level table; per-vector fp16 outliers are added back from CSR rows.
+//  * Hadamard write-up, "section details": the quantized part of the
+//    attention sum stays in the rotated domain and is rotated back once, in
+//    the merge, after the sum.
+//
+// Work decomposition: grid = (splits per stream, NS streams), 4 warps per
+// CTA.  Splits [0, n_qsplit) each own a run of 32-token quantized groups;
+// the last split (quantized mode) owns the fp16 sinks + window.  In fp16
+// mode every split owns a run of fp16 tokens.  Inside a CTA, warp w takes
+// every 4th group/chunk.  For K, lane l computes the logits of token l of
+// the group for every query head of the GQA group (no cross-lane reduction
+// per token); for V, lane l owns channels 4l..4l+3 and accumulates over the
+// group's tokens.  Softmax is online, in base 2 (q carries log2(e)).
+#pragma once
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+template <int GQ>
+struct DecodeSmem {
+  // every member starts on a 16-byte boundary: several are read as float4
+  alignas(16) float q[GQ][kHeadDim];     // q * softmax_scale * log2(e); heads >= g are 0
+  alignas(16) float qsum[GQ];            // sum_c q[r][c]
+  alignas(16) float work[4][GQ > 2 ? GQ : 2][kHeadDim];  // per warp: folded q' / K min+scale; merge staging
+  alignas(16) float p[4][kGroupTokens][GQ];              // per warp: softmax weights of the current chunk
+  alignas(16) uint32_t vs[4][kGroupTokens][4];           // per warp: V {min, scale} words of the group
+  alignas(16) uint8_t ocol[4][kGroupTokens][kMaxOutliers];  // per warp: V outlier columns
+  alignas(16) float oval[4][kGroupTokens][kMaxOutliers];    // per warp: V outlier values
+  alignas(16) int ocnt[4][kGroupTokens];
+  alignas(16) float2 anchor[4][kHeadDim / 2];  // per warp: e^{i t0 theta_j} of the group
+  alignas(16) float ml[4][GQ][2];              // per warp (m, l)
+  alignas(16) float comb_ml[GQ][2];            // CTA-combined (m, l)
+  alignas(16) float lut_k[8];
+  alignas(16) float lut_v[8];
+  int is_last;
+};
+
+__device__ __forceinline__ float2 cmul(float2 a, float2 b) {
+  return make_float2(a.x * b.x - a.y * b.y, a.y * b.x + a.x * b.y);
+}
+
+// e^{i x} for an fp64 angle: reduce modulo 2 pi in fp64, then fp32 sincos.
+__device__ __forceinline__ float2 expi(double x) {
+  const double two_pi = 6.283185307179586476925286766559;
+  const double r = x - two_pi * rint(x / two_pi);
+  float sn, cs;
+  sincosf((float)r, &sn, &cs);
+  return make_float2(cs, sn);
+}
+
+// Online-softmax update of one warp for one 32-token chunk: z[r] is the
+// base-2 logit of this lane's token (-inf when masked).
+template <int GQ>
+__device__ __forceinline__ void softmax_update(float (&z)[GQ], float (&m)[GQ], float (&lsum)[GQ],
+                                               float (&acc)[GQ][4], float (&macc)[GQ],
+                                               float (*p_out)[GQ], int lane) {
+#pragma unroll
+  for (int r = 0; r < GQ; ++r) {
+    const float cmax = warp_max(z[r]);
+    const float mnew = fmaxf(m[r], cmax);
+    float alpha, pl;
+    if (mnew == -INFINITY) {
+      alpha = 1.0f;
+      pl = 0.0f;
+    } else {
+      alpha = exp2f(m[r] - mnew);
+      pl = exp2f(z[r] - mnew);
+    }
+    lsum[r] = lsum[r] * alpha + pl;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[r][k] *= alpha;
+    macc[r] *= alpha;
+    m[r] = mnew;
+    p_out[lane][r] = pl;
+  }
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------- K logits
+
+// Uniform per-channel K, no RoPE: z[r] = bias_r + sum_c q'_rc * code_c.
+template <int KB, int GQ>
+__device__ __forceinline__ void k_logits_uniform(const DecodeParams& p, DecodeSmem<GQ>& sm,
+                                                 int s, int grp, int lane, int w, float (&z)[GQ]) {
+  const Geometry& G = p.geo;
+  {
+    const uint4 sc = *reinterpret_cast<const uint4*>(p.L.k_scales +
+                                                     ((size_t)s * G.gcap + grp) * kHeadDim + 4 * lane);
+    const uint32_t wv[4] = {sc.x, sc.y, sc.z, sc.w};
+    float bpart[GQ];
+#pragma unroll
+    for (int r = 0; r < GQ; ++r) bpart[r] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 ms = unpack_min_scale(wv[k]);
+      const int c = 4 * lane + k;
+#pragma unroll
+      for (int r = 0; r < GQ; ++r) {
+        const float qv = sm.q[r][c];
+        sm.work[w][r][c] = qv * ms.y;
+        bpart[r] = fmaf(qv, ms.x, bpart[r]);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < GQ; ++r) z[r] = warp_sum(bpart[r]);
+  }
+  __syncwarp();
+  constexpr int KROW = kHeadDim * KB / 8;
+  constexpr int PER_WORD = 32 / KB;
+  const uint4* row = reinterpret_cast<const uint4*>(p.L.k_codes + ((size_t)s * G.qcap +
+                                                                   (size_t)grp * kGroupTokens + lane) * KROW);
+#pragma unroll
+  for (int ch = 0; ch < KROW / 16; ++ch) {
+    const uint4 u = __ldg(row + ch);
+    const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+#pragma unroll
+      for (int m0 = 0; m0 < PER_WORD; m0 += 4) {
+        const int c = (ch * 4 + wi) * PER_WORD + m0;
+        float x[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) x[k] = small_uint_to_float((wd[wi] >> ((m0 + k) * KB)) & ((1u << KB) - 1u));
+#pragma unroll
+        for (int r = 0; r < GQ; ++r) {
+          const float4 qp = *reinterpret_cast<const float4*>(&sm.work[w][r][c]);
+          z[r] = fmaf(qp.x, x[0], z[r]);
+          z[r] = fmaf(qp.y, x[1], z[r]);
+          z[r] = fmaf(qp.z, x[2], z[r]);
+          z[r] = fmaf(qp.w, x[3], z[r]);
+        }
+      }
+    }
+  }
+}
+
+// Non-uniform per-token K, no RoPE: z = min * sum(q) + s * sum_c q_c L'_code
+// plus the outlier corrections q_col * (val - min).
+template <int GQ>
+__device__ __forceinline__ void k_logits_nuq(const DecodeParams& p, DecodeSmem<GQ>& sm, int s,
+                                             int grp, int lane, float (&z)[GQ]) {
+  const Geometry& G = p.geo;
+  const size_t i = (size_t)grp * kGroupTokens + lane;
+  const float2 ms = unpack_min_scale(__ldg(p.L.k_scales + (size_t)s * G.qcap + i));
+  const uint4* row = reinterpret_cast<const uint4*>(p.L.k_codes + ((size_t)s * G.qcap + i) * 48);
+  uint32_t wd[13];
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    const uint4 u = __ldg(row + k);
+    wd[4 * k] = u.x; wd[4 * k + 1] = u.y; wd[4 * k + 2] = u.z; wd[4 * k + 3] = u.w;
+  }
+  wd[12] = 0;
+  float zl[GQ];
+#pragma unroll
+  for (int r = 0; r < GQ; ++r) zl[r] = 0.0f;
+#pragma unroll
+  for (int c = 0; c < kHeadDim; c += 4) {
+    float x[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) x[k] = sm.lut_k[code_at<3>(wd, c + k)];
+#pragma unroll
+    for (int r = 0; r < GQ; ++r) {
+      const float4 qv = *reinterpret_cast<const float4*>(&sm.q[r][c]);
+      zl[r] = fmaf(qv.x, x[0], zl[r]);
+      zl[r] = fmaf(qv.y, x[1], zl[r]);
+      zl[r] = fmaf(qv.z, x[2], zl[r]);
+      zl[r] = fmaf(qv.w, x[3], zl[r]);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < GQ; ++r) z[r] = fmaf(ms.x, sm.qsum[r], ms.y * zl[r]);
+  const int32_t* rp = p.L.k_rowptr + (size_t)s * (G.qcap + 1);
+  const int jcap = G.qcap * G.nout;  // outlier entries of a stream
+  const int j0 = max(0, __ldg(rp + i)), j1 = min(jcap, __ldg(rp + i + 1));
+  const size_t base = (size_t)s * jcap;
+  for (int j = j0; j < j1; ++j) {
+    const int col = __ldg(p.L.k_col + base + j);
+    const float dv = half_bits_to_float(__ldg(p.L.k_val + base + j)) - ms.x;
+#pragma unroll
+    for (int r = 0; r < GQ; ++r) z[r] = fmaf(sm.q[r][col], dv, z[r]);
+  }
+}
+
+// Any quantized K with RoPE after dequantization: reconstruct k^ for each
+// channel pair (j, j + 64), rotate by the angle of this lane's position
+// (anchor of the group times e^{i lane theta_j}), dot with q.
+template <int KB, int GQ>
+__device__ __forceinline__ void k_logits_rope(const DecodeParams& p, DecodeSmem<GQ>& sm,
+                                              const float2* __restrict__ rope_e, int s, int grp,
+                                              int lane, int w, float (&z)[GQ]) {
+  const Geometry& G = p.geo;
+  const int pos0 = G.S + grp * kGroupTokens;
+  // group anchor e^{i pos0 theta_j}
+  for (int j = lane; j < kHeadDim / 2; j += 32) sm.anchor[w][j] = expi((double)pos0 * p.theta[j]);
+  const size_t i = (size_t)grp * kGroupTokens + lane;
+  float nmin = 0.0f, nsc = 0.0f;
+  if (KB == 3) {
+    const float2 ms = unpack_min_scale(__ldg(p.L.k_scales + (size_t)s * G.qcap + i));
+    nmin = ms.x;
+    nsc = ms.y;
+  } else {
+    const uint4 sc = *reinterpret_cast<const uint4*>(p.L.k_scales +
+                                                     ((size_t)s * G.gcap + grp) * kHeadDim + 4 * lane);
+    const uint32_t wv[4] = {sc.x, sc.y, sc.z, sc.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 ms = unpack_min_scale(wv[k]);
+      sm.work[w][0][4 * lane + k] = ms.x;
+      sm.work[w][1][4 * lane + k] = ms.y;
+    }
+  }
+  __syncwarp();
+  constexpr int KROW = kHeadDim * KB / 8;
+  constexpr int NW = KROW / 4;
+  uint32_t wd[NW + 1];
+  const uint4* row = reinterpret_cast<const uint4*>(p.L.k_codes + ((size_t)s * G.qcap + i) * KROW);
+#pragma unroll
+  for (int k = 0; k < KROW / 16; ++k) {
+    const uint4 u = __ldg(row + k);
+    wd[4 * k] = u.x; wd[4 * k + 1] = u.y; wd[4 * k + 2] = u.z; wd[4 * k + 3] = u.w;
+  }
+  wd[NW] = 0;
+#pragma unroll
+  for (int r = 0; r < GQ; ++r) z[r] = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kHeadDim / 2; ++j) {
+    float a, b;
+    const uint32_t ca = code_at<KB>(wd, j), cb = code_at<KB>(wd, j + kHeadDim / 2);
+    if (KB == 3) {
+      a = fmaf(nsc, sm.lut_k[ca], nmin);
+      b = fmaf(nsc, sm.lut_k[cb], nmin);
+    } else {
+      a = fmaf(small_uint_to_float(ca), sm.work[w][1][j], sm.work[w][0][j]);
+      b = fmaf(small_uint_to_float(cb), sm.work[w][1][j + kHeadDim / 2], sm.work[w][0][j + kHeadDim / 2]);
+    }
+    const float2 e = cmul(sm.anchor[w][j], rope_e[lane * (kHeadDim / 2) + j]);
+    const float ra = a * e.x - b * e.y;
+    const float rb = b * e.x + a * e.y;
+#pragma unroll
+    for (int r = 0; r < GQ; ++r) z[r] = fmaf(sm.q[r][j], ra, fmaf(sm.q[r][j + kHeadDim / 2], rb, z[r]));
+  }
+  if (KB == 3) {
+    const int32_t* rp = p.L.k_rowptr + (size_t)s * (G.qcap + 1);
+    const int jcap = G.qcap * G.nout;
+    const int j0 = max(0, __ldg(rp + i)), j1 = min(jcap, __ldg(rp + i + 1));
+    const size_t base = (size_t)s * jcap;
+    for (int j = j0; j < j1; ++j) {
+      const int col = __ldg(p.L.k_col + base + j);
+      const float dv = half_bits_to_float(__ldg(p.L.k_val + base + j)) - nmin;
+      const int f = col & (kHeadDim / 2 - 1);
+      const float2 e = cmul(sm.anchor[w][f], rope_e[lane * (kHeadDim / 2) + f]);
+      // rotated unit vector of channel col, times dv, dotted with q
+#pragma unroll
+      for (int r = 0; r < GQ; ++r) {
+        const float qa = sm.q[r][f], qb = sm.q[r][f + kHeadDim / 2];
+        const float dotu = (col < kHeadDim / 2) ? (qa * e.x + qb * e.y) : (-qa * e.y + qb * e.x);
+        z[r] = fmaf(dv, dotu, z[r]);
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------ V part
+
+template <int VB, int GQ>
+__device__ __forceinline__ void v_accumulate(const DecodeParams& p, DecodeSmem<GQ>& sm, int s, int grp,
+                                             int lane, int w, float (&acc)[GQ][4], float (&macc)[GQ]) {
+  const Geometry& G = p.geo;
+  const size_t i0 = (size_t)grp * kGroupTokens;
+  // stage this group's V scales (and, for non-uniform V, its outliers)
+  if (VB == 3) {
+    const size_t i = i0 + lane;
+    sm.vs[w][lane][0] = __ldg(p.L.v_scales + (size_t)s * G.qcap + i);
+    const int32_t* rp = p.L.v_rowptr + (size_t)s * (G.qcap + 1);
+    const int jcap = G.qcap * G.nout;
+    const int j0 = max(0, __ldg(rp + i)), j1 = min(jcap, __ldg(rp + i + 1));
+    const size_t base = (size_t)s * jcap;
+    const float mn = unpack_min_scale(sm.vs[w][lane][0]).x;
+    int n = 0;
+    for (int j = j0; j < j1 && n < kMaxOutliers; ++j, ++n) {
+      sm.ocol[w][lane][n] = __ldg(p.L.v_col + base + j);
+      sm.oval[w][lane][n] = half_bits_to_float(__ldg(p.L.v_val + base + j)) - mn;
+    }
+    sm.ocnt[w][lane] = n;
+  } else {
+    const uint32_t* src = p.L.v_scales + ((size_t)s * G.qcap + i0 + lane) * G.nvg;
+    for (int k = 0; k < G.nvg; ++k) sm.vs[w][lane][k] = __ldg(src + k);
+  }
+  __syncwarp();
+  const int jg = (VB == 3) ? 0 : (4 * lane) / G.gv;
+  constexpr int VROW = kHeadDim * VB / 8;
+  const uint8_t* vbase = p.L.v_codes + ((size_t)s * G.qcap + i0) * VROW;
+#pragma unroll 4
+  for (int t = 0; t < kGroupTokens; ++t) {
+    const float2 ms = unpack_min_scale(sm.vs[w][t][jg]);
+    float cv[4];
+    if (VB == 8) {
+      const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(vbase + (size_t)t * VROW) + lane);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) cv[k] = small_uint_to_float((u >> (8 * k)) & 0xffu);
+    } else if (VB == 4) {
+      const uint32_t u = __ldg(reinterpret_cast<const uint16_t*>(vbase + (size_t)t * VROW) + lane);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) cv[k] = small_uint_to_float((u >> (4 * k)) & 0xfu);
+    } else if (VB == 2) {
+      const uint32_t u = __ldg(vbase + (size_t)t * VROW + lane);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) cv[k] = small_uint_to_float((u >> (2 * k)) & 0x3u);
+    } else {  // 3-bit: channels 4l..4l+3 at bits 12l..12l+11
+      const uint32_t* rw = reinterpret_cast<const uint32_t*>(vbase + (size_t)t * VROW);
+      const int bit = 12 * lane, wi = bit >> 5, sh = bit & 31;
+      uint32_t u = __ldg(rw + wi) >> sh;
+      if (sh > 20) u |= __ldg(rw + wi + 1) << (32 - sh);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) cv[k] = sm.lut_v[(u >> (3 * k)) & 7u];
+    }
+#pragma unroll
+    for (int r = 0; r < GQ; ++r) {
+      const float pr = sm.p[w][t][r];
+      const float pp = pr * ms.y;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[r][k] = fmaf(pp, cv[k], acc[r][k]);
+      macc[r] = fmaf(pr, ms.x, macc[r]);
+    }
+    if (VB == 3) {
+      const int n = sm.ocnt[w][t];
+      for (int j = 0; j < n; ++j) {
+        const int col = sm.ocol[w][t][j];
+        if ((col >> 2) == lane) {
+          const float dv = sm.oval[w][t][j];
+#pragma unroll
+          for (int r = 0; r < GQ; ++r) {
+            const float a = sm.p[w][t][r] * dv;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if ((col & 3) == k) acc[r][k] += a;
+          }
+        }
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// fp16 token of index k in this split's fp16 token list -> (row pointer
+// offset in halves, absolute position).
+__device__ __forceinline__ size_t fp16_row(const DecodeParams& p, int s, int k, bool* in_sink, int* pos) {
+  const Geometry& G = p.geo;
+  if (G.fp16_mode) {
+    *in_sink = false;
+    *pos = k;
+    return ((size_t)s * G.ring + k) * kHeadDim;
+  }
+  if (k < p.S_eff) {
+    *in_sink = true;
+    *pos = k;
+    return ((size_t)s * G.S + k) * kHeadDim;
+  }
+  const int ps = G.S + p.Nq + (k - p.S_eff);
+  *in_sink = false;
+  *pos = ps;
+  return ((size_t)s * G.ring + (ps - G.S) % G.ring) * kHeadDim;
+}
+
+template <int GQ>
+__device__ __forceinline__ void fp16_chunk(const DecodeParams& p, DecodeSmem<GQ>& sm, int s, int k0, int k1,
+                                           int lane, int w, float (&m)[GQ], float (&lsum)[GQ],
+                                           float (&acc)[GQ][4], float (&macc)[GQ]) {
+  const Geometry& G = p.geo;
+  float z[GQ];
+  const int k = k0 + lane;
+  if (k < k1) {
+    bool sink;
+    int pos;
+    const size_t off = fp16_row(p, s, k, &sink, &pos);
+    const uint4* krow = reinterpret_cast<const uint4*>((sink ? p.L.k_sink : p.L.k_ring) + off);
+#pragma unroll
+    for (int r = 0; r < GQ; ++r) z[r] = 0.0f;
+    if (!G.pre_rope) {
+#pragma unroll 4
+      for (int ch = 0; ch < kHeadDim / 8; ++ch) {
+        const uint4 u = __ldg(krow + ch);
+        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float2 kv = __half22float2(*reinterpret_cast<const __half2*>(&wd[h]));
+          const int c = ch * 8 + 2 * h;
+#pragma unroll
+          for (int r = 0; r < GQ; ++r) z[r] = fmaf(sm.q[r][c], kv.x, fmaf(sm.q[r][c + 1], kv.y, z[r]));
+        }
+      }
+    } else {
+      const uint16_t* kr = reinterpret_cast<const uint16_t*>(krow);
+      for (int j = 0; j < kHeadDim / 2; ++j) {
+        const float a = half_bits_to_float(kr[j]), b = half_bits_to_float(kr[j + kHeadDim / 2]);
+        const float2 e = expi((double)pos * p.theta[j]);
+        const float ra = a * e.x - b * e.y, rb = b * e.x + a * e.y;
+#pragma unroll
+        for (int r = 0; r < GQ; ++r) z[r] = fmaf(sm.q[r][j], ra, fmaf(sm.q[r][j + kHeadDim / 2], rb, z[r]));
+      }
+    }
+  } else {
+#pragma unroll
+    for (int r = 0; r < GQ; ++r) z[r] = -INFINITY;
+  }
+  softmax_update<GQ>(z, m, lsum, acc, macc, sm.p[w], lane);
+  const int n = min(32, k1 - k0);
+  for (int t = 0; t < n; ++t) {
+    bool sink;
+    int pos;
+    const size_t off = fp16_row(p, s, k0 + t, &sink, &pos);
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>((sink ? p.L.v_sink : p.L.v_ring) + off) + lane);
+    const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+#pragma unroll
+    for (int r = 0; r < GQ; ++r) {
+      const float pr = sm.p[w][t][r];
+      acc[r][0] = fmaf(pr, v01.x, acc[r][0]);
+      acc[r][1] = fmaf(pr, v01.y, acc[r][1]);
+      acc[r][2] = fmaf(pr, v23.x, acc[r][2]);
+      acc[r][3] = fmaf(pr, v23.y, acc[r][3]);
+    }
+  }
+  __syncwarp();
+}
+
+// In-warp FWHT of a 128-vector (lane l holds elements 4l..4l+3), then * c.
+__device__ __forceinline__ void warp_fwht(float (&v)[4], float c, int lane) {
+  float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+  v[0] = a0 + a2; v[2] = a0 - a2; v[1] = a1 + a3; v[3] = a1 - a3;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[q], m);
+      v[q] = upper ? (o - v[q]) : (v[q] + o);
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) v[q] *= c;
+}
+
+template <int KB, int VB, int GQ>
+__global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ DecodeParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  DecodeSmem<GQ>& sm = *reinterpret_cast<DecodeSmem<GQ>*>(smem_raw);
+  float2* rope_e = reinterpret_cast<float2*>(smem_raw + ((sizeof(DecodeSmem<GQ>) + 15) / 16) * 16);
+  const Geometry& G = p.geo;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int sp = blockIdx.x, s = blockIdx.y;
+  const int b = s / G.Hkv, hk = s % G.Hkv, g = G.g;
+
+  for (int idx = tid; idx < GQ * kHeadDim; idx += kThreads) {
+    const int r = idx / kHeadDim, c = idx % kHeadDim;
+    float v = 0.0f;
+    if (r < g) v = half_bits_to_float(p.q[((size_t)b * G.Hq + hk * g + r) * kHeadDim + c]) * p.q_scale;
+    sm.q[r][c] = v;
+  }
+  if (tid < 8) {
+    sm.lut_k[tid] = p.k_lut_off[tid];
+    sm.lut_v[tid] = p.v_lut_off[tid];
+  }
+  const bool quant_split = sp < p.n_qsplit;
+  if (G.pre_rope && quant_split) {
+    for (int idx = tid; idx < kGroupTokens * (kHeadDim / 2); idx += kThreads) {
+      const int l = idx / (kHeadDim / 2), j = idx % (kHeadDim / 2);
+      rope_e[idx] = expi((double)l * p.theta[j]);
+    }
+  }
+  __syncthreads();
+  if (tid < GQ) {
+    float a = 0.0f;
+    for (int c = 0; c < kHeadDim; ++c) a += sm.q[tid][c];
+    sm.qsum[tid] = a;
+  }
+  __syncthreads();
+
+  float m[GQ], lsum[GQ], acc[GQ][4], macc[GQ];
+#pragma unroll
+  for (int r = 0; r < GQ; ++r) {
+    m[r] = -INFINITY;
+    lsum[r] = 0.0f;
+    macc[r] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[r][k] = 0.0f;
+  }
+
+  if constexpr (KB != 16) if (quant_split) {
+    const int ngroups = p.Nq / kGroupTokens;
+    const int g0 = sp * p.gps;
+    const int g1 = min(ngroups, g0 + p.gps);
+    for (int grp = g0 + w; grp < g1; grp += 4) {
+      float z[GQ];
+      if (G.pre_rope) {
+        k_logits_rope<KB, GQ>(p, sm, rope_e, s, grp, lane, w, z);
+      } else if (KB == 3) {
+        k_logits_nuq<GQ>(p, sm, s, grp, lane, z);
+      } else {
+        k_logits_uniform<(KB == 3 ? 4 : KB), GQ>(p, sm, s, grp, lane, w, z);
+      }
+      softmax_update<GQ>(z, m, lsum, acc, macc, sm.p[w], lane);
+      v_accumulate<VB, GQ>(p, sm, s, grp, lane, w, acc, macc);
+    }
+  }
+  if (!quant_split) {
+    int k0, k1;
+    if (G.fp16_mode) {
+      k0 = sp * p.fp16_tokens_per_split;
+      k1 = min(p.T, k0 + p.fp16_tokens_per_split);
+    } else {
+      k0 = 0;
+      k1 = p.S_eff + p.W;
+    }
+    for (int c0 = k0 + 32 * w; c0 < k1; c0 += 32 * 4)
+      fp16_chunk<GQ>(p, sm, s, c0, k1, lane, w, m, lsum, acc, macc);
+  }
+
+  // ---- combine the 4 warps of this CTA
+#pragma unroll
+  for (int r = 0; r < GQ; ++r) {
+    lsum[r] = warp_sum(lsum[r]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[r][k] += macc[r];
+  }
+  __syncthreads();  // all warps are done with sm.work
+  if (lane == 0) {
+#pragma unroll
+    for (int r = 0; r < GQ; ++r) {
+      sm.ml[w][r][0] = m[r];
+      sm.ml[w][r][1] = lsum[r];
+    }
+  }
+  float (*stage)[GQ][kHeadDim] = reinterpret_cast<float (*)[GQ][kHeadDim]>(&sm.work[0][0][0]);
+  static_assert(sizeof(sm.work) >= 4 * GQ * kHeadDim * sizeof(float), "merge staging");
+#pragma unroll
+  for (int r = 0; r < GQ; ++r)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) stage[w][r][4 * lane + k] = acc[r][k];
+  __syncthreads();
+  if (tid < GQ) {
+    float M = -INFINITY;
+    for (int ww = 0; ww < 4; ++ww) M = fmaxf(M, sm.ml[ww][tid][0]);
+    float Lc = 0.0f;
+    for (int ww = 0; ww < 4; ++ww)
+      if (sm.ml[ww][tid][0] != -INFINITY) Lc += exp2f(sm.ml[ww][tid][0] - M) * sm.ml[ww][tid][1];
+    sm.comb_ml[tid][0] = M;
+    sm.comb_ml[tid][1] = Lc;
+  }
+  // combined accumulator: thread per (head, channel), written into stage[0]
+  float combined[GQ];
+#pragma unroll
+  for (int r = 0; r < GQ; ++r) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int ww = 0; ww < 4; ++ww) M = fmaxf(M, sm.ml[ww][r][0]);
+    float a = 0.0f;
+#pragma unroll
+    for (int ww = 0; ww < 4; ++ww)
+      if (sm.ml[ww][r][0] != -INFINITY) a += exp2f(sm.ml[ww][r][0] - M) * stage[ww][r][tid];
+    combined[r] = a;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < GQ; ++r) stage[0][r][tid] = combined[r];
+  __syncthreads();
+
+  const bool rotate_this = G.hadamard && quant_split;
+  if (p.n_split == 1) {
+    // single split: finish here
+    for (int r = w; r < g; r += 4) {
+      float v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] = stage[0][r][4 * lane + k];
+      if (rotate_this) warp_fwht(v, p.hadamard_c, lane);
+      const float Lc = sm.comb_ml[r][1];
+      const size_t o = ((size_t)b * G.Hq + hk * g + r) * kHeadDim + 4 * lane;
+      __half2 h0 = __floats2half2_rn(v[0] / Lc, v[1] / Lc), h1 = __floats2half2_rn(v[2] / Lc, v[3] / Lc);
+      uint2 st;
+      st.x = *reinterpret_cast<uint32_t*>(&h0);
+      st.y = *reinterpret_cast<uint32_t*>(&h1);
+      *reinterpret_cast<uint2*>(p.out + o) = st;
+      if (p.lse && lane == 0)
+        p.lse[(size_t)b * G.Hq + hk * g + r] = (sm.comb_ml[r][0] + log2f(Lc)) * 0.6931471805599453f;
+    }
+    return;
+  }
+
+  // ---- write this split's partial, take a ticket; the last CTA merges
+  {
+    const size_t base = ((size_t)s * p.n_split + sp) * g;
+    for (int r = 0; r < g; ++r) p.part_acc[(base + r) * kHeadDim + tid] = stage[0][r][tid];
+    if (tid < g) {
+      p.part_ml[(base + tid) * 2] = sm.comb_ml[tid][0];
+      p.part_ml[(base + tid) * 2 + 1] = sm.comb_ml[tid][1];
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned prev = atomicAdd(&p.counters[s], 1u);
+    sm.is_last = (prev == (unsigned)(p.n_split - 1)) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!sm.is_last) return;
+  __threadfence();
+
+  for (int r = w; r < g; r += 4) {
+    float M = -INFINITY;
+    for (int q2 = 0; q2 < p.n_split; ++q2)
+      M = fmaxf(M, __ldcg(&p.part_ml[(((size_t)s * p.n_split + q2) * g + r) * 2]));
+    float Lc = 0.0f, oq[4] = {0, 0, 0, 0}, ow[4] = {0, 0, 0, 0};
+    for (int q2 = 0; q2 < p.n_split; ++q2) {
+      const size_t base = ((size_t)s * p.n_split + q2) * g + r;
+      const float mq = __ldcg(&p.part_ml[base * 2]);
+      if (mq == -INFINITY) continue;
+      const float e = exp2f(mq - M);
+      Lc += e * __ldcg(&p.part_ml[base * 2 + 1]);
+      const float4 a = __ldcg(reinterpret_cast<const float4*>(&p.part_acc[base * kHeadDim + 4 * lane]));
+      float* dst = (q2 < p.n_qsplit) ? oq : ow;
+      dst[0] += e * a.x;
+      dst[1] += e * a.y;
+      dst[2] += e * a.z;
+      dst[3] += e * a.w;
+    }
+    if (G.hadamard) warp_fwht(oq, p.hadamard_c, lane);
+    float v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = (oq[k] + ow[k]) / Lc;
+    const size_t o = ((size_t)b * G.Hq + hk * g + r) * kHeadDim + 4 * lane;
+    __half2 h0 = __floats2half2_rn(v[0], v[1]), h1 = __floats2half2_rn(v[2], v[3]);
+    uint2 st;
+    st.x = *reinterpret_cast<uint32_t*>(&h0);
+    st.y = *reinterpret_cast<uint32_t*>(&h1);
+    *reinterpret_cast<uint2*>(p.out + o) = st;
+    if (p.lse && lane == 0) p.lse[(size_t)b * G.Hq + hk * g + r] = (M + log2f(Lc)) * 0.6931471805599453f;
+  }
+  if (tid == 0) p.counters[s] = 0u;
+}
+
+template <int KB, int VB, int GQ>
+cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t st) {
+  size_t smem = ((sizeof(DecodeSmem<GQ>) + 15) / 16) * 16;
+  if (p.geo.pre_rope) smem += sizeof(float2) * kGroupTokens * (kHeadDim / 2);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<KB, VB, GQ>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid(p.n_split, p.geo.NS);
+  decode_kernel<KB, VB, GQ><<<grid, kThreads, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

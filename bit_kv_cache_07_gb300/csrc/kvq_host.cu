@@ -1,0 +1,341 @@
+// kvq_host.cu -- the C ABI of libkvq (include/kvq.h): argument validation,
+// the byte layout of a layer buffer, the decode split plan, and launches.
+// Host code only; every step of the method runs in the kernels.
+#include <cmath>
+#include <cstring>
+
+#include "kvq_internal.cuh"
+
+using namespace kvq;
+
+namespace {
+
+constexpr uint64_t kAlign = 256;
+constexpr int kTargetCtas = 152 * 8;  // decode: aim for ~8 CTAs per SM of GB300
+
+uint64_t align_up(uint64_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool valid_lut(const float* lut) {
+  for (int i = 0; i < 8; ++i) {
+    if (!std::isfinite(lut[i])) return false;
+    if (i && !(lut[i] > lut[i - 1])) return false;
+  }
+  return true;
+}
+
+kvq_status make_geometry(const kvq_config* c, Geometry* g) {
+  if (!c || !g) return KVQ_ERR_INVALID_ARG;
+  if (c->batch < 1 || c->n_kv_heads < 1 || c->n_q_heads < 1 || c->head_dim < 1 || c->max_tokens < 1)
+    return KVQ_ERR_INVALID_ARG;
+  if (c->n_q_heads % c->n_kv_heads) return KVQ_ERR_INVALID_ARG;
+  if (c->n_sink < 0 || c->n_recent < 0 || c->split_tokens < 0) return KVQ_ERR_INVALID_ARG;
+  if ((c->v_hadamard != 0 && c->v_hadamard != 1) || (c->k_pre_rope != 0 && c->k_pre_rope != 1))
+    return KVQ_ERR_INVALID_ARG;
+  if (!(c->softmax_scale >= 0.0f) || !std::isfinite(c->softmax_scale)) return KVQ_ERR_INVALID_ARG;
+  if (c->k_pre_rope && !(c->rope_theta > 0.0f && std::isfinite(c->rope_theta))) return KVQ_ERR_INVALID_ARG;
+  if (c->head_dim != kHeadDim) return KVQ_ERR_UNSUPPORTED;
+  if (c->n_q_heads / c->n_kv_heads > kMaxGQA) return KVQ_ERR_UNSUPPORTED;
+  const int64_t ns = (int64_t)c->batch * c->n_kv_heads;
+  if (ns > 65535) return KVQ_ERR_UNSUPPORTED;
+
+  const bool fp16 = c->k_bits == 16 || c->v_bits == 16;
+  auto uni = [](int b) { return b == 2 || b == 4 || b == 8; };
+  if (fp16) {
+    if (c->k_bits != 16 || c->v_bits != 16) return KVQ_ERR_UNSUPPORTED;
+    if (c->v_hadamard) return KVQ_ERR_UNSUPPORTED;
+  } else if (c->k_bits == 3 || c->v_bits == 3) {
+    if (c->k_bits != 3 || c->v_bits != 3) return KVQ_ERR_UNSUPPORTED;
+    if (c->outliers_per_vector < 0 || c->outliers_per_vector > kMaxOutliers) return KVQ_ERR_INVALID_ARG;
+    if (!valid_lut(c->k_lut) || !valid_lut(c->v_lut)) return KVQ_ERR_INVALID_ARG;
+  } else if (!uni(c->k_bits) || !uni(c->v_bits)) {
+    return KVQ_ERR_UNSUPPORTED;
+  }
+  if (!fp16) {
+    if (c->k_group_tokens != kGroupTokens) return KVQ_ERR_UNSUPPORTED;
+    if (c->v_bits != 3 && c->v_group_channels != 32 && c->v_group_channels != 64 &&
+        c->v_group_channels != 128)
+      return KVQ_ERR_UNSUPPORTED;
+    if (c->split_tokens % kGroupTokens) return KVQ_ERR_INVALID_ARG;
+  } else if (c->split_tokens % kGroupTokens) {
+    return KVQ_ERR_INVALID_ARG;
+  }
+
+  g->B = c->batch;
+  g->Hq = c->n_q_heads;
+  g->Hkv = c->n_kv_heads;
+  g->g = c->n_q_heads / c->n_kv_heads;
+  g->NS = (int)ns;
+  g->d = c->head_dim;
+  g->fp16_mode = fp16 ? 1 : 0;
+  g->kb = c->k_bits;
+  g->vb = c->v_bits;
+  g->gk = kGroupTokens;
+  g->gv = (c->v_bits == 3 || fp16) ? kHeadDim : c->v_group_channels;
+  g->nvg = kHeadDim / g->gv;
+  g->hadamard = c->v_hadamard;
+  g->pre_rope = c->k_pre_rope;
+  g->nout = (c->k_bits == 3) ? c->outliers_per_vector : 0;
+  g->rope_theta = c->rope_theta;
+  if (fp16) {
+    g->S = 0;
+    g->R = 0;
+    g->ring = c->max_tokens;
+    g->qcap = 0;
+    g->krow = g->vrow = 0;
+  } else {
+    g->S = c->n_sink;
+    g->R = c->n_recent;
+    g->ring = c->n_recent + kGroupTokens;
+    const int64_t rest = (int64_t)c->max_tokens - c->n_sink - c->n_recent;
+    g->qcap = rest > 0 ? (int)(kGroupTokens * (rest / kGroupTokens)) : 0;
+    g->krow = kHeadDim * c->k_bits / 8;
+    g->vrow = kHeadDim * c->v_bits / 8;
+  }
+  g->gcap = g->qcap / kGroupTokens;
+  return KVQ_OK;
+}
+
+// Sink tokens present, quantized tokens and window tokens at T tokens.
+void counts(const Geometry& g, int T, int* S_eff, int* Nq, int* W) {
+  if (g.fp16_mode) {
+    *S_eff = 0;
+    *Nq = 0;
+    *W = T;
+    return;
+  }
+  *S_eff = T < g.S ? T : g.S;
+  const int rest = T - g.S - g.R;
+  *Nq = rest > 0 ? kGroupTokens * (rest / kGroupTokens) : 0;
+  *W = T - *S_eff - *Nq;
+}
+
+kvq_status build_layout(const kvq_config* c, const Geometry& g, kvq_layout* L) {
+  std::memset(L, 0, sizeof(*L));
+  uint64_t off = 0;
+  auto put = [&](kvq_region& r, uint64_t bytes) {
+    r.offset = off;
+    r.bytes = bytes;
+    off = align_up(off + bytes);
+  };
+  const uint64_t NS = (uint64_t)g.NS, Q = (uint64_t)g.qcap, d = kHeadDim;
+  put(L->k_codes, NS * Q * g.krow);
+  put(L->k_scales, g.kb == 3 ? NS * Q * 4 : NS * (uint64_t)g.gcap * d * 4);
+  put(L->v_codes, NS * Q * g.vrow);
+  put(L->v_scales, g.vb == 3 ? NS * Q * 4 : NS * Q * g.nvg * 4);
+  put(L->k_sink, NS * g.S * d * 2);
+  put(L->v_sink, NS * g.S * d * 2);
+  put(L->k_ring, NS * (uint64_t)g.ring * d * 2);
+  put(L->v_ring, NS * (uint64_t)g.ring * d * 2);
+  const uint64_t k = (uint64_t)g.nout;
+  const bool nuq = g.kb == 3;
+  put(L->k_csr_rowptr, nuq ? NS * (Q + 1) * 4 : 0);
+  put(L->k_csr_col, nuq ? NS * Q * k : 0);
+  put(L->k_csr_val, nuq ? NS * Q * k * 2 : 0);
+  put(L->v_csr_rowptr, nuq ? NS * (Q + 1) * 4 : 0);
+  put(L->v_csr_col, nuq ? NS * Q * k : 0);
+  put(L->v_csr_val, nuq ? NS * Q * k * 2 : 0);
+  L->layer_bytes = off;
+  L->max_splits = kMaxQSplits + 1;
+  L->ring_slots = g.ring;
+  L->q_cap = g.qcap;
+  const uint64_t ws = align_up(NS * 4) + align_up(NS * (uint64_t)L->max_splits * g.g * 2 * 4) +
+                      NS * (uint64_t)L->max_splits * g.g * d * 4;
+  L->workspace_bytes = ws;
+  (void)c;
+  return KVQ_OK;
+}
+
+void layer_ptrs(const kvq_layout& L, void* base, LayerPtrs* P) {
+  auto at = [&](const kvq_region& r) { return (void*)((char*)base + r.offset); };
+  P->k_codes = (uint8_t*)at(L.k_codes);
+  P->k_scales = (uint32_t*)at(L.k_scales);
+  P->v_codes = (uint8_t*)at(L.v_codes);
+  P->v_scales = (uint32_t*)at(L.v_scales);
+  P->k_sink = (uint16_t*)at(L.k_sink);
+  P->v_sink = (uint16_t*)at(L.v_sink);
+  P->k_ring = (uint16_t*)at(L.k_ring);
+  P->v_ring = (uint16_t*)at(L.v_ring);
+  P->k_rowptr = (int32_t*)at(L.k_csr_rowptr);
+  P->k_col = (uint8_t*)at(L.k_csr_col);
+  P->k_val = (uint16_t*)at(L.k_csr_val);
+  P->v_rowptr = (int32_t*)at(L.v_csr_rowptr);
+  P->v_col = (uint8_t*)at(L.v_csr_col);
+  P->v_val = (uint16_t*)at(L.v_csr_val);
+}
+
+// Split plan: how many splits cover `ngroups` 32-token groups of NS streams.
+void split_groups(int ngroups, int NS, int split_tokens, int* n_split, int* gps) {
+  if (ngroups <= 0) {
+    *n_split = 0;
+    *gps = 1;
+    return;
+  }
+  int per;
+  if (split_tokens > 0) {
+    per = split_tokens / kGroupTokens;
+  } else {
+    int want = (kTargetCtas + NS - 1) / NS;
+    if (want < 1) want = 1;
+    if (want > kMaxQSplits) want = kMaxQSplits;
+    if (want > ngroups) want = ngroups;
+    per = (ngroups + want - 1) / want;
+  }
+  if (per < 1) per = 1;
+  if ((ngroups + per - 1) / per > kMaxQSplits) per = (ngroups + kMaxQSplits - 1) / kMaxQSplits;
+  *gps = per;
+  *n_split = (ngroups + per - 1) / per;
+}
+
+struct Plan {
+  int S_eff, Nq, W, n_qsplit, n_split, gps, fp16_tps;
+};
+
+Plan make_plan(const Geometry& g, int T, int split_tokens) {
+  Plan p{};
+  counts(g, T, &p.S_eff, &p.Nq, &p.W);
+  if (g.fp16_mode) {
+    int n, per;
+    split_groups((T + kGroupTokens - 1) / kGroupTokens, g.NS, split_tokens, &n, &per);
+    p.n_qsplit = 0;
+    p.n_split = n;
+    p.gps = per;
+    p.fp16_tps = per * kGroupTokens;
+  } else {
+    int n, per;
+    split_groups(p.Nq / kGroupTokens, g.NS, split_tokens, &n, &per);
+    p.n_qsplit = n;
+    p.gps = per;
+    p.n_split = n + ((p.S_eff + p.W) > 0 ? 1 : 0);
+    p.fp16_tps = p.S_eff + p.W;
+  }
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvq_status_string(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported configuration";
+    case KVQ_ERR_CAPACITY: return "token count exceeds capacity";
+    case KVQ_ERR_WORKSPACE: return "workspace missing or too small";
+    case KVQ_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+kvq_status kvq_layout_query(const kvq_config* cfg, kvq_layout* out) {
+  if (!cfg || !out) return KVQ_ERR_INVALID_ARG;
+  Geometry g;
+  kvq_status st = make_geometry(cfg, &g);
+  if (st != KVQ_OK) return st;
+  return build_layout(cfg, g, out);
+}
+
+kvq_status kvq_decode_plan(const kvq_config* cfg, int32_t tokens, int32_t* splits_per_stream,
+                           int32_t* quantized_splits) {
+  Geometry g;
+  kvq_status st = make_geometry(cfg, &g);
+  if (st != KVQ_OK) return st;
+  if (tokens < 1) return KVQ_ERR_INVALID_ARG;
+  if (tokens > cfg->max_tokens) return KVQ_ERR_CAPACITY;
+  Plan p = make_plan(g, tokens, cfg->split_tokens);
+  if (splits_per_stream) *splits_per_stream = p.n_split;
+  if (quantized_splits) *quantized_splits = p.n_qsplit;
+  return KVQ_OK;
+}
+
+kvq_status kvq_append(const kvq_config* cfg, void* layer_buf, int32_t tokens_before,
+                      const uint16_t* k_new, const uint16_t* v_new, int32_t n_new,
+                      kvq_stream_t stream) {
+  Geometry g;
+  kvq_status st = make_geometry(cfg, &g);
+  if (st != KVQ_OK) return st;
+  if (!layer_buf || !k_new || !v_new) return KVQ_ERR_INVALID_ARG;
+  if (tokens_before < 0 || n_new < 1) return KVQ_ERR_INVALID_ARG;
+  if ((int64_t)tokens_before + n_new > cfg->max_tokens) return KVQ_ERR_CAPACITY;
+  if (((uintptr_t)k_new | (uintptr_t)v_new | (uintptr_t)layer_buf) % 16) return KVQ_ERR_INVALID_ARG;
+  kvq_layout L;
+  build_layout(cfg, g, &L);
+
+  AppendParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.geo = g;
+  layer_ptrs(L, layer_buf, &p.L);
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.tokens_before = tokens_before;
+  p.n_new = n_new;
+  int s0, w0, s1, w1;
+  counts(g, tokens_before, &s0, &p.nq_before, &w0);
+  counts(g, tokens_before + n_new, &s1, &p.nq_after, &w1);
+  p.first_group = p.nq_before / kGroupTokens;
+  p.hadamard_c = (float)(1.0 / std::sqrt((double)kHeadDim));
+  for (int i = 0; i < 8; ++i) {
+    p.k_lut[i] = cfg->k_lut[i];
+    p.v_lut[i] = cfg->v_lut[i];
+  }
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const int n_groups = (p.nq_after - p.nq_before) / kGroupTokens;
+  if (n_groups > 0) {
+    if (launch_append_quantize(p, n_groups, cs) != cudaSuccess) return KVQ_ERR_CUDA;
+  }
+  if (launch_append_window(p, cs) != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+kvq_status kvq_decode_attn(const kvq_config* cfg, const void* layer_buf, int32_t tokens,
+                           const uint16_t* q, uint16_t* out, float* lse, void* workspace,
+                           uint64_t ws_bytes, kvq_stream_t stream) {
+  Geometry g;
+  kvq_status st = make_geometry(cfg, &g);
+  if (st != KVQ_OK) return st;
+  if (!layer_buf || !q || !out) return KVQ_ERR_INVALID_ARG;
+  if (tokens < 1) return KVQ_ERR_INVALID_ARG;
+  if (tokens > cfg->max_tokens) return KVQ_ERR_CAPACITY;
+  if (((uintptr_t)layer_buf | (uintptr_t)q | (uintptr_t)out) % 16) return KVQ_ERR_INVALID_ARG;
+  kvq_layout L;
+  build_layout(cfg, g, &L);
+  Plan pl = make_plan(g, tokens, cfg->split_tokens);
+
+  DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.geo = g;
+  layer_ptrs(L, const_cast<void*>(layer_buf), &p.L);
+  p.q = q;
+  p.out = out;
+  p.lse = lse;
+  p.T = tokens;
+  p.S_eff = pl.S_eff;
+  p.Nq = pl.Nq;
+  p.W = pl.W;
+  p.n_qsplit = pl.n_qsplit;
+  p.n_split = pl.n_split;
+  p.gps = pl.gps;
+  p.fp16_tokens_per_split = pl.fp16_tps;
+  if (pl.n_split > 1) {
+    const uint64_t cnt_bytes = align_up((uint64_t)g.NS * 4);
+    const uint64_t ml_bytes = align_up((uint64_t)g.NS * pl.n_split * g.g * 2 * 4);
+    const uint64_t need = cnt_bytes + ml_bytes + (uint64_t)g.NS * pl.n_split * g.g * kHeadDim * 4;
+    if (!workspace || ws_bytes < need || ((uintptr_t)workspace % 16)) return KVQ_ERR_WORKSPACE;
+    p.counters = (uint32_t*)workspace;
+    p.part_ml = (float*)((char*)workspace + cnt_bytes);
+    p.part_acc = (float*)((char*)workspace + cnt_bytes + ml_bytes);
+  }
+  const double sm = cfg->softmax_scale > 0.0f ? (double)cfg->softmax_scale : 1.0 / std::sqrt((double)kHeadDim);
+  p.q_scale = (float)(sm * 1.4426950408889634);  // log2(e): softmax in base 2
+  p.hadamard_c = (float)(1.0 / std::sqrt((double)kHeadDim));
+  for (int i = 0; i < 8; ++i) {
+    p.k_lut_off[i] = cfg->k_lut[i] - cfg->k_lut[0];
+    p.v_lut_off[i] = cfg->v_lut[i] - cfg->v_lut[0];
+  }
+  for (int i = 0; i < kHeadDim / 2; ++i)
+    p.theta[i] = std::pow((double)cfg->rope_theta, -2.0 * i / (double)kHeadDim);
+  if (launch_decode(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+}  // extern "C"

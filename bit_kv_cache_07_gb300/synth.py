@@ -54,8 +54,10 @@ def _draw(dist: str, shape, g: torch.Generator, device) -> torch.Tensor:
     if dist == "normal":
         return torch.randn(shape, generator=g, device=device)
     if dist == "laplace":
-        u = torch.rand(shape, generator=g, device=device) - 0.5
-        return -torch.sign(u) * torch.log1p(-2.0 * u.abs())
+        # difference of two Exp(1) draws; -log1p(-r) is finite for r in [0, 1)
+        e1 = -torch.log1p(-torch.rand(shape, generator=g, device=device))
+        e2 = -torch.log1p(-torch.rand(shape, generator=g, device=device))
+        return e1 - e2
     if dist == "student_t3":
         z = torch.randn(shape, generator=g, device=device)
         chi2 = torch.randn((3,) + tuple(shape), generator=g, device=device).pow(2).sum(0)
@@ -120,3 +122,32 @@ def random_halves(shape, seed: int, scale: float = 1.0) -> np.ndarray:
     """Plain N(0, scale^2) fp16 array for small oracle-only tests."""
     rng = np.random.default_rng(seed)
     return (rng.standard_normal(shape) * scale).astype(np.float16)
+
+
+def random_kv(B: int, Hkv: int, T: int, d: int = 128, seed: int = 0, device="cpu",
+              k_outlier_channels: int = 3, k_outlier_scale: float = 8.0, v_dist: str = "laplace"):
+    """Generic fp16 K, V [B, Hkv, T, d] for parity cases of any shape:
+    K ~ N(0,1) with a few per-head outlier channels scaled up, V from v_dist."""
+    g = _gen(device, "random_kv", seed)
+    K = torch.randn((B, Hkv, T, d), generator=g, device=device)
+    if k_outlier_channels:
+        idx = torch.stack([torch.randperm(d, generator=g, device=device)[:k_outlier_channels]
+                           for _ in range(Hkv)])
+        sc = torch.ones((Hkv, d), device=device)
+        sc.scatter_(1, idx, float(k_outlier_scale))
+        K = K * sc[None, :, None, :]
+    V = _draw(v_dist, (B, Hkv, T, d), g, device)
+    return K.to(torch.float16), V.to(torch.float16)
+
+
+def random_q(B: int, Hq: int, d: int = 128, seed: int = 0, device="cpu"):
+    g = _gen(device, "random_q", seed)
+    return torch.randn((B, Hq, d), generator=g, device=device).to(torch.float16)
+
+
+def lut_from_seed(seed: int) -> list[float]:
+    """8 fp16 N(0,1) sample quantiles (see nuq_lut) from a plain seed."""
+    rng = np.random.default_rng(seed)
+    x = np.sort(rng.standard_normal(65536))
+    idx = ((np.arange(8) + 0.5) * 65536 / 8).astype(np.int64)
+    return [float(v) for v in x[idx].astype(np.float16).astype(np.float32)]

@@ -1,0 +1,220 @@
+/*
+ * kvq.h -- C ABI of libkvq: low-bit KV-cache append/quantize and fused
+ * dequantize-and-attend decode for one GPU (NVIDIA GB300, sm_103a).
+ *
+ * The method (sources, by page title and section):
+ *  - "KVTuner" review, observation 2 and "Intra-Layer KV Cache Quantization
+ *    Precision Pair Pruning" / "KV Cache quantization (Online)": K is quantized
+ *    per channel (asymmetric min/scale), each layer keeps its own static
+ *    (K bits, V bits) pair from KV8, K8V4, KV4, K4V2, KV2.
+ *  - KVQuant (arXiv 2401.18079), abstract and "technical approach": per-channel
+ *    K, pre-RoPE K (RoPE applied after dequantization), non-uniform per-layer
+ *    datatypes, per-vector dense-and-sparse outliers (~1 %), fused kernels.
+ *  - InnerQ (arXiv 2602.23200), "Methodology" 1-5: V grouped along the hidden
+ *    dimension (groups of 64 channels) with one min/scale per group, scales
+ *    loaded once and reused by every element of the group, fp16 windows for
+ *    the most recent and the sink tokens, one fused dequant + GEMV pass.
+ *  - "Hadamard rotation-based 2-bit quantization for KV cache compression",
+ *    TL;DR and "section details": V rotated by a Hadamard matrix, then uniform
+ *    2-bit; the inverse rotation is applied once after the attention sum.
+ *
+ * Conventions shared by every entry point
+ *  - All device pointers are plain CUDA device addresses; the caller owns all
+ *    memory.  The library never allocates, frees or synchronises, and keeps
+ *    no state between calls: everything is a pure function of the config and
+ *    the token counts passed in.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  Argument errors are returned before anything is
+ *    launched.  A failed launch returns KVQ_ERR_CUDA.  No C++ exception
+ *    crosses the ABI.
+ *  - fp16 is IEEE binary16 passed as 16-bit words (`uint16_t`).
+ *  - A "stream" of the cache is one (batch row b, KV head h) pair,
+ *    s = b * n_kv_heads + h.  Query head hq reads KV head hq / (Hq / Hkv).
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* the type behind cudaStream_t */
+typedef struct CUstream_st *kvq_stream_t;
+
+typedef enum kvq_status {
+    KVQ_OK = 0,
+    KVQ_ERR_INVALID_ARG = -1, /* null pointer, bad size, bad token count      */
+    KVQ_ERR_UNSUPPORTED = -2, /* valid but not built: head_dim, bits, groups  */
+    KVQ_ERR_CAPACITY = -3,    /* tokens beyond max_tokens                      */
+    KVQ_ERR_WORKSPACE = -4,   /* workspace missing or too small                */
+    KVQ_ERR_CUDA = -5         /* a CUDA launch or runtime call failed          */
+} kvq_status;
+
+/* Per-layer cache configuration.  A model with per-layer bit pairs simply
+ * uses one kvq_config per layer ("KVTuner" review, online application of
+ * the offline-chosen pairs). */
+typedef struct kvq_config {
+    int32_t batch;            /* B >= 1                                        */
+    int32_t n_q_heads;        /* Hq, a multiple of n_kv_heads                  */
+    int32_t n_kv_heads;       /* Hkv >= 1                                      */
+    int32_t head_dim;         /* d; 128 is the supported value                 */
+    int32_t max_tokens;       /* capacity of every sequence, >= 1              */
+    int32_t k_bits;           /* 2, 4, 8: uniform per-channel K; 3: non-uniform
+                                 per-token K codes; 16: plain fp16 cache (then
+                                 v_bits must be 16 too)                        */
+    int32_t v_bits;           /* 2, 4, 8: uniform per-token V over groups of
+                                 v_group_channels; 3: non-uniform; 16: fp16    */
+    int32_t k_group_tokens;   /* G_K: tokens per K group; 32 is supported      */
+    int32_t v_group_channels; /* G_V: channels per V group: 32, 64 or 128      */
+    int32_t n_sink;           /* S: first S tokens stay fp16 (attention sinks) */
+    int32_t n_recent;         /* R: at least R most recent tokens stay fp16    */
+    int32_t v_hadamard;       /* 1: rotate V by Hn = H/sqrt(d) before quantizing
+                                 (uniform or non-uniform V); the decode applies
+                                 Hn once to the summed quantized part          */
+    int32_t k_pre_rope;       /* 1: K is cached before RoPE; the decode applies
+                                 RoPE (rotate-half pairs (i, i+d/2), angle
+                                 t * rope_theta^(-2i/d) at position t) after
+                                 dequantization.  q is always passed already
+                                 rotated for its own position.                 */
+    float rope_theta;         /* RoPE base, e.g. 10000                         */
+    int32_t outliers_per_vector; /* non-uniform mode: k fp16 outliers kept per
+                                 token vector (0..8)                           */
+    float k_lut[8];           /* non-uniform K levels, strictly increasing,
+                                 fp16-representable                            */
+    float v_lut[8];           /* non-uniform V levels                          */
+    float softmax_scale;      /* 0 selects 1/sqrt(d)                           */
+    int32_t split_tokens;     /* decode: quantized tokens per split-K chunk
+                                 (multiple of G_K); 0 selects automatically    */
+} kvq_config;
+
+/* Window rule.  For a sequence holding T tokens:
+ *   positions [0, min(S, T))           sinks, fp16
+ *   positions [S, S + Nq)              quantized, Nq = G_K * floor((T-S-R)/G_K)
+ *                                      (0 when T - S - R <= 0)
+ *   positions [S + Nq, T)              fp16 recent window, W tokens, R <= W < R+G_K
+ *                                      once T >= S + R
+ * Appending tokens one at a time flushes exactly one G_K group whenever the
+ * window reaches R + G_K tokens, which gives the same Nq as one bulk append.
+ * fp16 mode (bits 16) quantizes nothing: every token is a window token. */
+
+typedef struct kvq_region {
+    uint64_t offset; /* byte offset inside the layer buffer (256-byte aligned) */
+    uint64_t bytes;  /* size in bytes (0 if the region is unused)              */
+} kvq_region;
+
+/* Byte layout of one layer buffer.  NS = batch * n_kv_heads streams,
+ * Qcap = G_K * floor(max(0, max_tokens - S - R) / G_K) quantized-token slots,
+ * Gcap = Qcap / G_K, RING = R + G_K window slots (max_tokens in fp16 mode),
+ * KROW = d * k_bits / 8, VROW = d * v_bits / 8 bytes per packed row.
+ * Quantized token index i = t - S for position t.
+ *
+ *  k_codes   [NS][Qcap][KROW] u8   packed K row of token i: code of channel c at
+ *                                  bits [b*c, b*c+b) of the row's little-endian
+ *                                  bitstream (bit 0 = LSB of byte 0)
+ *  k_scales  uniform K:  [NS][Gcap][d] {min, scale} fp16 pairs (min first), one
+ *                        per channel per G_K-token group
+ *            non-uniform K: [NS][Qcap] {min, s} fp16 pairs, one per token
+ *  v_codes   [NS][Qcap][VROW] u8   packed V row of token i (rotated domain when
+ *                                  v_hadamard)
+ *  v_scales  uniform V:  [NS][Qcap][d/G_V] {min, scale} fp16 pairs
+ *            non-uniform V: [NS][Qcap] {min, s} fp16 pairs
+ *  k_sink, v_sink [NS][S][d] fp16  sink tokens
+ *  k_ring, v_ring [NS][RING][d] fp16  window tokens; position t lives in slot
+ *                                  (t - S) mod RING (slot t in fp16 mode); V is
+ *                                  stored unrotated
+ *  k_csr_rowptr [NS][Qcap+1] i32, k_csr_col [NS][Qcap*k] u8,
+ *  k_csr_val [NS][Qcap*k] fp16     non-uniform K outliers as CSR over token rows
+ *                                  (rowptr counts from 0 per stream; columns
+ *                                  ascend within a row); same for v_csr_*
+ *
+ * Uniform quantizer (per group of n values, b bits, fp32 arithmetic, RN):
+ *   scale = (max - min) / (2^b - 1); code = clamp(rint((x - min)/scale), 0, 2^b-1);
+ *   stored min = fp16(min) (exact), scale = fp16_RN(scale); a constant group
+ *   stores scale 0 and codes 0.  Dequantized value: min + code * scale.
+ * Non-uniform quantizer (one token vector): the k largest |x| (ties -> lower
+ *   channel) are kept as fp16 outliers with code 0; over the rest,
+ *   s = (max - min)/(L7 - L0), u = (x - min)/s,
+ *   code = #{i : u > (L_i + L_{i+1})*0.5 - L0}; value = min + s*(L_code - L0).
+ * Hadamard: v' = fp16_RN(fp32(1/sqrt(d)) * FWHT_fp32(v)), butterfly stages of
+ *   width 1, 2, ..., d/2, (a, b) -> (a + b, a - b).
+ */
+typedef struct kvq_layout {
+    kvq_region k_codes, k_scales, v_codes, v_scales;
+    kvq_region k_sink, v_sink, k_ring, v_ring;
+    kvq_region k_csr_rowptr, k_csr_col, k_csr_val;
+    kvq_region v_csr_rowptr, v_csr_col, v_csr_val;
+    uint64_t layer_bytes;     /* bytes of one layer buffer                     */
+    uint64_t workspace_bytes; /* decode scratch needed for any T <= max_tokens  */
+    int32_t max_splits;       /* upper bound on decode splits per stream        */
+    int32_t ring_slots;       /* RING                                           */
+    int32_t q_cap;            /* Qcap                                           */
+} kvq_layout;
+
+/* kvq_layout_query -- host only, no CUDA call.
+ * Fills *out with the region offsets/sizes of one layer buffer, the layer
+ * buffer size and the decode workspace size for `cfg`.
+ * Returns KVQ_ERR_INVALID_ARG for null pointers or inconsistent sizes,
+ * KVQ_ERR_UNSUPPORTED for combinations the kernels are not built for. */
+kvq_status kvq_layout_query(const kvq_config *cfg, kvq_layout *out);
+
+/* kvq_append -- write n_new tokens per sequence into the cache.
+ * ("KVTuner" review, online quantization at the fixed per-layer pair;
+ *  InnerQ Methodology 1-4; KVQuant per-channel / pre-RoPE K, NUQ, outliers;
+ *  Hadamard write-up: rotate V, then quantize.)
+ *   layer_buf     device, layer_bytes, laid out as kvq_layout describes; the
+ *                 caller zero-fills it once before the first append (not
+ *                 required for correctness of quantized data, only so that
+ *                 unused bytes are defined)
+ *   tokens_before number of tokens each sequence held before this call
+ *   k_new, v_new  device fp16 [B][Hkv][n_new][d], K before RoPE when
+ *                 k_pre_rope, otherwise as the model produced it
+ *   n_new         >= 1; tokens_before + n_new <= max_tokens
+ * Tokens that fall in the sink or window regions are copied as fp16; every
+ * time the window reaches R + G_K tokens its oldest G_K tokens are quantized
+ * (for a bulk prefill, all groups at once).  Launches one quantize kernel when
+ * groups are flushed, then one copy kernel for the fp16 tokens.
+ * Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CAPACITY,
+ * KVQ_ERR_CUDA. */
+kvq_status kvq_append(const kvq_config *cfg, void *layer_buf, int32_t tokens_before,
+                      const uint16_t *k_new, const uint16_t *v_new, int32_t n_new,
+                      kvq_stream_t stream);
+
+/* kvq_decode_attn -- one decode step of attention over the cache.
+ * (KVQuant fused low-bit mat-vec kernels; InnerQ Methodology 3 and 5: fused
+ *  group dequant + GEMV with scales reused across the group; Hadamard
+ *  write-up: inverse rotation after the attention sum; KVQuant pre-RoPE K.)
+ *   layer_buf  device, as written by kvq_append
+ *   tokens     T, 1 <= T <= max_tokens: the sequence length to attend over
+ *   q          device fp16 [B][Hq][d]
+ *   out        device fp16 [B][Hq][d]: softmax(scale * q K^T) V
+ *   lse        device f32 [B][Hq] natural-log log-sum-exp of the scaled
+ *              logits, or NULL
+ *   workspace  device scratch of ws_bytes >= layout.workspace_bytes; its
+ *              first NS 32-bit words are split counters that must be zero
+ *              before the first call (zero the whole workspace once); every
+ *              call leaves them zero again.  Calls that share a workspace
+ *              must not overlap on the GPU.
+ * One kernel launch: each CTA streams its split of the packed cache once,
+ * and the last CTA of each stream merges the splits (log-sum-exp) and
+ * applies the inverse Hadamard rotation.
+ * Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CAPACITY,
+ * KVQ_ERR_WORKSPACE, KVQ_ERR_CUDA. */
+kvq_status kvq_decode_attn(const kvq_config *cfg, const void *layer_buf, int32_t tokens,
+                           const uint16_t *q, uint16_t *out, float *lse,
+                           void *workspace, uint64_t ws_bytes, kvq_stream_t stream);
+
+/* Number of CTAs (splits per stream x streams) the decode launches for
+ * `tokens`, and the splits per stream; host only.  For measurement. */
+kvq_status kvq_decode_plan(const kvq_config *cfg, int32_t tokens, int32_t *splits_per_stream,
+                           int32_t *quantized_splits);
+
+/* Static string naming a status code. */
+const char *kvq_status_string(kvq_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */
