@@ -42,17 +42,31 @@ def parse():
     ap.add_argument("--no-fp16-baseline", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: build just the first N layers (the bench line needs all)")
     return ap.parse_args()
 
 
 # ------------------------------------------------------------------ bytes
 
+def window_counts(cfg: dict, T: int):
+    """(sinks present, quantized tokens, fp16 window tokens) at T tokens: the
+    cache's window rule (sinks [0,S), Nq = 32*floor((T-S-R)/32) quantized
+    tokens, the rest fp16; an fp16 cache quantizes nothing)."""
+    if cfg["k_bits"] == 16:
+        return 0, 0, T
+    S, R = cfg["n_sink"], cfg["n_recent"]
+    rest = T - S - R
+    nq = 32 * (rest // 32) if rest > 0 else 0
+    s = min(S, T)
+    return s, nq, T - s - nq
+
+
 def algorithmic_bytes(cfg: dict, T: int) -> int:
     """Bytes one decode launch must move: packed codes, scales, CSR outliers
     and fp16 sink/window tokens of every stream (each read once per KV head),
     plus q in and out."""
-    from oracle import kvq_oracle as O  # only for the shared window rule counts
-    S, Nq, W = O.layout_counts(cfg, T)
+    S, Nq, W = window_counts(cfg, T)
     d = cfg["head_dim"]
     NS = cfg["batch"] * cfg["n_kv_heads"]
     kb, vb = cfg["k_bits"], cfg["v_bits"]
@@ -149,12 +163,12 @@ class Model:
     """All layers of one workload: caches filled to T-1 tokens, plus the
     per-layer inputs of one decode step."""
 
-    def __init__(self, name: str, device, fp16: bool):
+    def __init__(self, name: str, device, fp16: bool, layers: int = 0):
         import torch
         from bit_kv_cache_07_gb300 import binding, synth, workloads
         w = workloads.WORKLOADS[name]
         self.name, self.T = name, w["tokens"]
-        self.L = w["layers"]
+        self.L = layers if layers > 0 else w["layers"]
         self.cfgs, self.layers = [], []
         self.q, self.k_new, self.v_new, self.out = [], [], [], []
         for l in range(self.L):
@@ -328,18 +342,21 @@ def oracle_sample(name: str, seconds: float, layer_count: int | None = None):
     K, V = synth.layer_kv(name, 0, tokens=T, batch=1, device="cpu")
     q = synth.query(name, 0, batch=1, device="cpu").numpy()
     Kh, Vh = K.numpy(), V.numpy()
+    nstore = min(4, w["n_kv_heads"])
+    stores = [O.build_stream(cfg, Kh[0, h], Vh[0, h]) for h in range(nstore)]
     n, spent = 0, 0.0
-    while spent < seconds and n < w["n_kv_heads"]:
-        store = O.build_stream(cfg, Kh[0, n], Vh[0, n])
+    while spent < seconds or n < 3:
+        h = n % nstore
         t0 = time.perf_counter()
-        O.decode_stream(cfg, T, store, q[0, n * g:(n + 1) * g])
+        O.decode_stream(cfg, T, stores[h], q[0, h * g:(h + 1) * g])
         spent += time.perf_counter() - t0
         n += 1
     streams_per_step = w["layers"] * w["batch"] * w["n_kv_heads"]
     per_stream = spent / n
     return {
         "value": per_stream * streams_per_step * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
-        "sample": f"fp64 oracle decode of {n} (batch row, KV head) streams of layer 0 at T={T}, "
+        "sample": f"fp64 oracle decode of {n} (batch row, KV head) streams of layer 0 at T={T} "
+                  f"(cycling over {nstore} prebuilt streams), "
                   f"{per_stream * 1e3:.1f} ms each, scaled x{streams_per_step / n:.0f} to one "
                   f"{w['layers']}-layer step; cache build not timed",
     }
@@ -387,7 +404,7 @@ def main():
     stream = torch.cuda.Stream(device=dev)
     w = workloads.WORKLOADS[args.workload]
 
-    model = Model(args.workload, dev, fp16=False)
+    model = Model(args.workload, dev, fp16=False, layers=args.layers)
     clocks = ClockSampler(local)
     clocks.start()
     total_ms, kern = time_steps(model, stream, args.steps, args.warmup)
@@ -400,12 +417,13 @@ def main():
     e2e_ms, h2d, d2h = time_e2e(model, stream, max(3, args.steps // 2), 2)
     e2e_ms = max_over_ranks(e2e_ms)
     launches = model.launches_per_step() * args.steps
+    model_layers = model.L
     del model
     torch.cuda.empty_cache()
 
     fp16 = None
     if not args.no_fp16_baseline:
-        fmodel = Model(args.workload, dev, fp16=True)
+        fmodel = Model(args.workload, dev, fp16=True, layers=args.layers)
         f_ms, f_kern = time_steps(fmodel, stream, args.steps, args.warmup)
         f_ms = max_over_ranks(f_ms / args.steps)
         f_bytes = fmodel.decode_bytes()
@@ -425,7 +443,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": args.workload, "layers": w["layers"], "batch": w["batch"],
+        "config": {"workload": args.workload, "layers": model_layers, "batch": w["batch"],
                    "q_heads": w["n_q_heads"], "kv_heads": w["n_kv_heads"], "head_dim": w["head_dim"],
                    "context": w["tokens"], "cache": w["pairs"], "n_sink": w["n_sink"], "n_recent": w["n_recent"],
                    "l2": "inputs larger than L2: %.2f GB of cache read per step" % (dec_bytes / 1e9),
@@ -435,7 +453,7 @@ def main():
         "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": ncu_traffic(f"decode:{args.workload}"),
-                     "bytes_per_launch": dec_bytes / (w["layers"]),
+                     "bytes_per_launch": dec_bytes / model_layers,
                      "launch_us": kern_ms * 1e3},
         "fp16_baseline": fp16,
         "speedup_vs_fp16": (fp16["us_per_step"] / value) if fp16 else None,

@@ -19,9 +19,29 @@ def gpu_store(layer, s: int, T: int, counts) -> dict:
     kb, vb = cfg.k_bits, cfg.v_bits
     host = {}
 
+    import torch
+    tdt = {np.uint8: torch.uint8, np.uint16: torch.int16, np.int32: torch.int32}
+
+    class _Reg:
+        """Region viewed as [NS, ...] on the device; only stream s is copied."""
+
+        def __init__(self, name, dtype):
+            self.r = layer.region(name)
+            self.dtype = dtype
+
+        def reshape(self, *shape):
+            self.shape = shape
+            return self
+
+        def __getitem__(self, idx):
+            s_, rest = idx[0], idx[1:]
+            if self.r.numel() == 0:
+                return np.zeros(tuple(self.shape[1:]), self.dtype)[rest]
+            t = self.r.view(tdt[self.dtype]).view(*self.shape)[s_].cpu().numpy().view(self.dtype)
+            return t[rest] if rest else t
+
     def reg(name, dtype):
-        r = layer.region(name)
-        return r.cpu().numpy().view(dtype) if r.numel() else np.zeros(0, dtype)
+        return _Reg(name, dtype)
 
     qcap = lay.q_cap
     if kb == 16:
@@ -51,8 +71,8 @@ def gpu_store(layer, s: int, T: int, counts) -> dict:
     host["vsink"] = reg("v_sink", np.uint16).reshape(NS, Sc, d)[s, :S] if Sc else np.zeros((0, d), np.uint16)
     R = lay.ring_slots
     slots = [(cfg.n_sink + Nq + w - cfg.n_sink) % R for w in range(W)]
-    host["kwin"] = reg("k_ring", np.uint16).reshape(NS, R, d)[s, slots]
-    host["vwin"] = reg("v_ring", np.uint16).reshape(NS, R, d)[s, slots]
+    host["kwin"] = reg("k_ring", np.uint16).reshape(NS, R, d)[s,][slots]
+    host["vwin"] = reg("v_ring", np.uint16).reshape(NS, R, d)[s,][slots]
     return host
 
 
