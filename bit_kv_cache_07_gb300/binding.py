@@ -53,7 +53,7 @@ class kvq_layout(C.Structure):
 
 
 EXPORTS = ["kvq_layout_query", "kvq_append", "kvq_decode_attn", "kvq_decode_plan",
-           "kvq_status_string"]
+           "kvq_status_string", "kvq_decode_attn_noalloc"]
 
 _lib = None
 
@@ -81,6 +81,8 @@ def lib():
         L.kvq_decode_plan.argtypes = [C.POINTER(kvq_config), C.c_int32, C.POINTER(C.c_int32),
                                       C.POINTER(C.c_int32)]
         L.kvq_decode_plan.restype = C.c_int
+        L.kvq_decode_attn_noalloc.argtypes = [C.POINTER(kvq_config), vp, C.c_int32, u16p, u16p, vp, vp]
+        L.kvq_decode_attn_noalloc.restype = C.c_int
         L.kvq_status_string.argtypes = [C.c_int]
         L.kvq_status_string.restype = C.c_char_p
         _lib = L
@@ -182,6 +184,20 @@ def kvq_decode_attn(cfg, layer_buf, tokens: int, q, out, lse=None, workspace=Non
         _ptr(lse, "lse", torch.float32, c.batch * c.n_q_heads * 4, allow_none=True),
         _ptr(workspace, "workspace", allow_none=True), int(ws_bytes), _stream(stream))
     _check("kvq_decode_attn", st)
+
+
+def kvq_decode_attn_noalloc(cfg, layer_buf, tokens: int, q, out, lse=None, stream=None):
+    """kvq_decode_attn for callers that cannot allocate: the split-K scratch
+    is the library's own fixed 8 MiB device array (see include/kvq.h)."""
+    import torch
+    c = _cfg(cfg)
+    lay = kvq_layout_query(c)
+    nq = c.batch * c.n_q_heads * c.head_dim * 2
+    st = lib().kvq_decode_attn_noalloc(
+        C.byref(c), _ptr(layer_buf, "layer_buf", numel=lay.layer_bytes), int(tokens),
+        _ptr(q, "q", torch.float16, nq), _ptr(out, "out", torch.float16, nq),
+        _ptr(lse, "lse", torch.float32, c.batch * c.n_q_heads * 4, allow_none=True), _stream(stream))
+    _check("kvq_decode_attn_noalloc", st)
 
 
 # ------------------------------------------------------------ conveniences

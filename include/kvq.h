@@ -210,6 +210,26 @@ kvq_status kvq_decode_attn(const kvq_config *cfg, const void *layer_buf, int32_t
 kvq_status kvq_decode_plan(const kvq_config *cfg, int32_t tokens, int32_t *splits_per_stream,
                            int32_t *quantized_splits);
 
+/* kvq_decode_attn_noalloc -- kvq_decode_attn without a caller workspace.
+ * The pages have no counterpart: this exists for callers that cannot
+ * allocate device memory where they decode (a pool that owns all device
+ * memory, a host framework that forbids allocations on its hot path, a
+ * real-time loop).  The split-K scratch is a fixed 8 MiB array inside the
+ * library, held on every GPU that loads it until the process exits.
+ *   Arguments as kvq_decode_attn, minus workspace/ws_bytes.
+ *   No cudaMalloc/cudaFree or other allocating call; the split counters are
+ *   cleared with cudaMemsetAsync on `stream` before the launch.
+ *   The first call on a device looks the array's device address up
+ *   (cudaGetSymbolAddress, that device current): make it before any stream
+ *   capture.
+ *   All calls share the array: calls that overlap on the GPU race; serialise
+ *   them.
+ * Errors: as kvq_decode_attn; KVQ_ERR_WORKSPACE when this call's scratch
+ * (split counters + per-split partials) would exceed 8 MiB. */
+kvq_status kvq_decode_attn_noalloc(const kvq_config *cfg, const void *layer_buf, int32_t tokens,
+                                   const uint16_t *q, uint16_t *out, float *lse,
+                                   kvq_stream_t stream);
+
 /* Static string naming a status code. */
 const char *kvq_status_string(kvq_status status);
 

@@ -1,0 +1,74 @@
+"""kvq_decode_attn_noalloc: the decode entry point for callers that cannot
+allocate device memory (its split-K scratch is a fixed array inside the
+library).  Called through the C ABI, it must match kvq_decode_attn with a
+caller-provided workspace, on two calls in a row (the shared scratch keeps
+the previous call's contents), and reject work whose scratch would not fit.
+
+This file is collected last on purpose: a failure here does not hide the
+results of the other GPU tests."""
+import ctypes as C
+
+import numpy as np
+import pytest
+import torch
+
+from _kvq_testutil import TOL, normwise_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from bit_kv_cache_07_gb300 import build
+    build.build_library()
+    from bit_kv_cache_07_gb300 import binding
+    assert torch.cuda.is_available()
+    return binding
+
+
+def _cfg(**kw):
+    c = dict(batch=2, n_q_heads=8, n_kv_heads=2, head_dim=128, max_tokens=3000, k_bits=4, v_bits=4,
+             k_group_tokens=32, v_group_channels=64, n_sink=4, n_recent=64, v_hadamard=0, k_pre_rope=0,
+             rope_theta=10000.0, outliers_per_vector=0, softmax_scale=0.0, split_tokens=0)
+    c.update(kw)
+    return c
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(k_bits=4, v_bits=2, v_hadamard=1, n_q_heads=14)])
+def test_noalloc_matches_workspace_entry_point_twice(B, kw):
+    from bit_kv_cache_07_gb300 import synth
+    cfg = _cfg(**kw)
+    T = 2900
+    K, V = synth.random_kv(cfg["batch"], cfg["n_kv_heads"], T, seed=77, device="cuda")
+    layer = B.Layer(cfg)
+    layer.append(0, K, V)
+    q = synth.random_q(cfg["batch"], cfg["n_q_heads"], seed=78, device="cuda")
+    ref = torch.empty_like(q)
+    ref_lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+    layer.decode(T, q, ref, ref_lse, B.new_workspace(cfg))
+    splits, _ = B.kvq_decode_plan(cfg, T)
+    assert splits > 1, "the case must use split-K scratch"
+    c = B.make_config(cfg)
+    for call in range(2):
+        out = torch.full_like(q, float("nan"))
+        lse = torch.full_like(ref_lse, float("nan"))
+        st = B.lib().kvq_decode_attn_noalloc(C.byref(c), layer.buf.data_ptr(), T, q.data_ptr(),
+                                             out.data_ptr(), lse.data_ptr(),
+                                             torch.cuda.current_stream().cuda_stream)
+        assert st == 0, B.kvq_status_string(st)
+        torch.cuda.synchronize()
+        err = normwise_err(out.float().cpu().numpy(), ref.float().cpu().numpy())
+        assert err.max() < TOL, (call, err.max())
+        assert np.allclose(lse.cpu().numpy(), ref_lse.cpu().numpy(), rtol=1e-5, atol=1e-5)
+
+
+def test_noalloc_rejects_scratch_beyond_its_size(B):
+    """512 streams x 4 splits x 8 heads of partials need more than 8 MiB:
+    the call must return KVQ_ERR_WORKSPACE before touching the GPU."""
+    cfg = _cfg(batch=64, n_kv_heads=8, n_q_heads=64, max_tokens=5000)
+    splits, _ = B.kvq_decode_plan(cfg, 4000)
+    need = 512 * splits * 8 * (2 + 128) * 4
+    assert need > (8 << 20)
+    c = B.make_config(cfg)
+    fake = 1 << 20  # never dereferenced: the size check comes first
+    assert B.lib().kvq_decode_attn_noalloc(C.byref(c), fake, 4000, fake, fake, None, None) == -4
