@@ -378,13 +378,19 @@ __device__ __forceinline__ size_t fp16_row(const DecodeParams& p, int s, int k, 
   return ((size_t)s * G.ring + (ps - G.S) % G.ring) * kHeadDim;
 }
 
+// One 32-token chunk of fp16 tokens (sinks / window, or an fp16 cache) for
+// one warp: lane = token for q.k, lane = 4 channels for p.v.  sq is the
+// scaled query [GQ][d] in shared memory, pbuf this warp's [32][GQ] buffer.
 template <int GQ>
-__device__ __forceinline__ void fp16_chunk(const DecodeParams& p, DecodeSmem<GQ>& sm, int s, int k0, int k1,
-                                           int lane, int w, float (&m)[GQ], float (&lsum)[GQ],
-                                           float (&acc)[GQ][4], float (&macc)[GQ]) {
+__device__ __forceinline__ void fp16_chunk(const DecodeParams& p, const float (*sq)[kHeadDim],
+                                           float (*pbuf)[GQ], int s, int k0, int k1, int lane,
+                                           float (&m)[GQ], float (&lsum)[GQ], float (&acc)[GQ][4],
+                                           float (&macc)[GQ]) {
   const Geometry& G = p.geo;
   float z[GQ];
   const int k = k0 + lane;
+#pragma unroll
+  for (int r = 0; r < GQ; ++r) z[r] = -INFINITY;
   if (k < k1) {
     bool sink;
     int pos;
@@ -393,48 +399,82 @@ __device__ __forceinline__ void fp16_chunk(const DecodeParams& p, DecodeSmem<GQ>
 #pragma unroll
     for (int r = 0; r < GQ; ++r) z[r] = 0.0f;
     if (!G.pre_rope) {
-#pragma unroll 4
-      for (int ch = 0; ch < kHeadDim / 8; ++ch) {
-        const uint4 u = __ldg(krow + ch);
-        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+      // the row in two batches of 8 independent 16-byte loads
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const float2 kv = __half22float2(*reinterpret_cast<const __half2*>(&wd[h]));
-          const int c = ch * 8 + 2 * h;
+      for (int half = 0; half < 2; ++half) {
+        uint4 u[8];
 #pragma unroll
-          for (int r = 0; r < GQ; ++r) z[r] = fmaf(sm.q[r][c], kv.x, fmaf(sm.q[r][c + 1], kv.y, z[r]));
+        for (int i = 0; i < 8; ++i) u[i] = __ldg(krow + 8 * half + i);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t wd[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const float2 kv = __half22float2(*reinterpret_cast<const __half2*>(&wd[h]));
+            const int c = (8 * half + i) * 8 + 2 * h;
+#pragma unroll
+            for (int r = 0; r < GQ; ++r) z[r] = fmaf(sq[r][c], kv.x, fmaf(sq[r][c + 1], kv.y, z[r]));
+          }
         }
       }
     } else {
-      const uint16_t* kr = reinterpret_cast<const uint16_t*>(krow);
-      for (int j = 0; j < kHeadDim / 2; ++j) {
-        const float a = half_bits_to_float(kr[j]), b = half_bits_to_float(kr[j + kHeadDim / 2]);
-        const float2 e = expi((double)pos * p.theta[j]);
-        const float ra = a * e.x - b * e.y, rb = b * e.x + a * e.y;
+      // RoPE pairs (j, j + d/2): the row's first half holds channel j, the second j + d/2
+      uint4 ua[8], ub[8];
 #pragma unroll
-        for (int r = 0; r < GQ; ++r) z[r] = fmaf(sm.q[r][j], ra, fmaf(sm.q[r][j + kHeadDim / 2], rb, z[r]));
+      for (int i = 0; i < 8; ++i) {
+        ua[i] = __ldg(krow + i);
+        ub[i] = __ldg(krow + 8 + i);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t wa[4] = {ua[i].x, ua[i].y, ua[i].z, ua[i].w};
+        const uint32_t wb[4] = {ub[i].x, ub[i].y, ub[i].z, ub[i].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float2 a2 = __half22float2(*reinterpret_cast<const __half2*>(&wa[h]));
+          const float2 b2 = __half22float2(*reinterpret_cast<const __half2*>(&wb[h]));
+          const int j = i * 8 + 2 * h;
+          const float2 e0 = expi((double)pos * p.theta[j]);
+          const float2 e1 = expi((double)pos * p.theta[j + 1]);
+          const float ra0 = a2.x * e0.x - b2.x * e0.y, rb0 = b2.x * e0.x + a2.x * e0.y;
+          const float ra1 = a2.y * e1.x - b2.y * e1.y, rb1 = b2.y * e1.x + a2.y * e1.y;
+#pragma unroll
+          for (int r = 0; r < GQ; ++r) {
+            z[r] = fmaf(sq[r][j], ra0, fmaf(sq[r][j + kHeadDim / 2], rb0, z[r]));
+            z[r] = fmaf(sq[r][j + 1], ra1, fmaf(sq[r][j + 1 + kHeadDim / 2], rb1, z[r]));
+          }
+        }
       }
     }
-  } else {
-#pragma unroll
-    for (int r = 0; r < GQ; ++r) z[r] = -INFINITY;
   }
-  softmax_update<GQ>(z, m, lsum, acc, macc, sm.p[w], lane);
+  softmax_update<GQ>(z, m, lsum, acc, macc, pbuf, lane);
   const int n = min(32, k1 - k0);
-  for (int t = 0; t < n; ++t) {
-    bool sink;
-    int pos;
-    const size_t off = fp16_row(p, s, k0 + t, &sink, &pos);
-    const uint2 u = __ldg(reinterpret_cast<const uint2*>((sink ? p.L.v_sink : p.L.v_ring) + off) + lane);
-    const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-    const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+  // V rows in batches of 8 tokens: the loads of a batch are independent
+  for (int t0 = 0; t0 < n; t0 += 8) {
+    uint2 u[8];
 #pragma unroll
-    for (int r = 0; r < GQ; ++r) {
-      const float pr = sm.p[w][t][r];
-      acc[r][0] = fmaf(pr, v01.x, acc[r][0]);
-      acc[r][1] = fmaf(pr, v01.y, acc[r][1]);
-      acc[r][2] = fmaf(pr, v23.x, acc[r][2]);
-      acc[r][3] = fmaf(pr, v23.y, acc[r][3]);
+    for (int i = 0; i < 8; ++i) {
+      u[i] = make_uint2(0u, 0u);
+      if (t0 + i < n) {
+        bool sink;
+        int pos;
+        const size_t off = fp16_row(p, s, k0 + t0 + i, &sink, &pos);
+        u[i] = __ldg(reinterpret_cast<const uint2*>((sink ? p.L.v_sink : p.L.v_ring) + off) + lane);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (t0 + i >= n) break;
+      const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&u[i].x));
+      const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&u[i].y));
+#pragma unroll
+      for (int r = 0; r < GQ; ++r) {
+        const float pr = pbuf[t0 + i][r];
+        acc[r][0] = fmaf(pr, v01.x, acc[r][0]);
+        acc[r][1] = fmaf(pr, v01.y, acc[r][1]);
+        acc[r][2] = fmaf(pr, v23.x, acc[r][2]);
+        acc[r][3] = fmaf(pr, v23.y, acc[r][3]);
+      }
     }
   }
   __syncwarp();
@@ -529,7 +569,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
       k1 = p.S_eff + p.W;
     }
     for (int c0 = k0 + 32 * w; c0 < k1; c0 += 32 * 4)
-      fp16_chunk<GQ>(p, sm, s, c0, k1, lane, w, m, lsum, acc, macc);
+      fp16_chunk<GQ>(p, sm.q, sm.p[w], s, c0, k1, lane, m, lsum, acc, macc);
   }
 
   // ---- combine the 4 warps of this CTA

@@ -7,7 +7,6 @@ namespace kvq {
 cudaError_t launch_decode_k2(const DecodeParams& p, cudaStream_t st);
 cudaError_t launch_decode_k4(const DecodeParams& p, cudaStream_t st);
 cudaError_t launch_decode_k8(const DecodeParams& p, cudaStream_t st);
-
 template <int KB, int VB>
 static cudaError_t by_gq(const DecodeParams& p, cudaStream_t st) {
   switch (p.geo.g <= 1 ? 1 : p.geo.g <= 2 ? 2 : p.geo.g <= 4 ? 4 : 8) {

@@ -1,0 +1,72 @@
+// kvq_decode_persist_f16.cu -- the persistent decode's host side: which
+// configurations it serves, its schedule and workspace, and the dispatch;
+// plus its fp16-cache instantiations.
+#include "kvq_decode_persist.cuh"
+
+namespace kvq {
+
+cudaError_t persist_k2(const DecodeParams& p, cudaStream_t st, int* occ);
+cudaError_t persist_k4(const DecodeParams& p, cudaStream_t st, int* occ);
+cudaError_t persist_k8(const DecodeParams& p, cudaStream_t st, int* occ);
+
+static cudaError_t persist_f16(const DecodeParams& p, cudaStream_t st, int* occ) {
+  return persist::dispatch_gt<16, 16>(p, st, occ);
+}
+
+static cudaError_t dispatch(const DecodeParams& p, cudaStream_t st, int* occ) {
+  if (p.geo.fp16_mode) return persist_f16(p, st, occ);
+  switch (p.geo.kb) {
+    case 2: return persist_k2(p, st, occ);
+    case 4: return persist_k4(p, st, occ);
+    case 8: return persist_k8(p, st, occ);
+  }
+  return cudaErrorInvalidValue;
+}
+
+// Uniform K and V (2/4/8 bits) with 64-channel V groups and no RoPE, or a
+// plain fp16 cache without RoPE.  Everything else uses the split kernel.
+bool persist_eligible(const Geometry& g) {
+  if (g.pre_rope || g.g > kMaxGQA) return false;
+  if (g.fp16_mode) return true;
+  if (g.kb == 3 || g.vb == 3) return false;
+  return g.gv == 64;
+}
+
+cudaError_t plan_persist(DecodeParams& p, uint64_t* ws_need) {
+  const Geometry& G = p.geo;
+  p.ng = G.fp16_mode ? 0 : p.Nq / kGroupTokens;
+  p.nt = (p.S_eff + p.W + kGroupTokens - 1) / kGroupTokens;
+  p.n_items = p.ng + p.nt;
+  // bytes an item reads: a quantized group (codes, K scales, V scales) or 32 fp16 tokens of K and V
+  p.wq = G.fp16_mode ? 1 : (long long)kGroupTokens * (G.krow + G.vrow) + kHeadDim * 4 + kGroupTokens * G.nvg * 4;
+  p.wt = (long long)kGroupTokens * kHeadDim * 2 * 2;
+  p.wstream = (long long)p.ng * p.wq + (long long)p.nt * p.wt;
+  p.wtot = (long long)G.NS * p.wstream;
+  int dev = 0, sms = 0, occ = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = dispatch(p, nullptr, &occ);
+  if (e != cudaSuccess) return e;
+  if (occ < 1) occ = 1;
+  long long nw = (long long)sms * occ * 4;
+  const long long items = (long long)G.NS * p.n_items;
+  if (nw > items) nw = items;
+  if (nw > (long long)kMaxQSplits * G.NS) nw = (long long)kMaxQSplits * G.NS;
+  // every warp's weight range must hold at least one item start, so that the
+  // warps counted for a stream are exactly the ones that work on it
+  const long long wmax = p.ng > 0 && p.wq > p.wt ? p.wq : p.wt;
+  if (nw > p.wtot / wmax) nw = p.wtot / wmax;
+  if (nw < 1) nw = 1;
+  p.nwarps = (int)nw;
+  const uint64_t slots = (uint64_t)p.nwarps + G.NS;
+  const uint64_t cnt = ((uint64_t)G.NS * 4 + 255) / 256 * 256;
+  const uint64_t ml = (slots * G.g * 2 * 4 + 255) / 256 * 256;
+  *ws_need = cnt + ml + slots * G.g * kHeadDim * 4;
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode_persist(const DecodeParams& p, cudaStream_t st) { return dispatch(p, st, nullptr); }
+
+}  // namespace kvq

@@ -1,0 +1,9 @@
+// kvq_decode_persist_k2.cu -- persistent tensor-core decode instantiations
+// for 2-bit uniform K (V 2, 4 or 8 bits; 1, 2, 4 or 8 query heads per KV head).
+#include "kvq_decode_persist.cuh"
+
+namespace kvq {
+cudaError_t persist_k2(const DecodeParams& p, cudaStream_t st, int* occ) {
+  return persist::dispatch_vb<2>(p, st, occ);
+}
+}  // namespace kvq

@@ -11,7 +11,7 @@ using namespace kvq;
 namespace {
 
 constexpr uint64_t kAlign = 256;
-constexpr int kTargetCtas = 152 * 8;  // decode: aim for ~8 CTAs per SM of GB300
+constexpr int kTargetCtas = 152 * 6;  // decode: ~2 waves of 3 resident CTAs per SM of GB300
 
 uint64_t align_up(uint64_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -213,6 +213,89 @@ Plan make_plan(const Geometry& g, int T, int split_tokens) {
 
 }  // namespace
 
+namespace kvq {
+
+kvq_status decode_setup(const kvq_config* cfg, const void* layer_buf, int32_t tokens, const uint16_t* q,
+                        uint16_t* out, float* lse, DecodeParams* pp, bool* persistent, uint64_t* layout_ws) {
+  Geometry g;
+  kvq_status st = make_geometry(cfg, &g);
+  if (st != KVQ_OK) return st;
+  if (!layer_buf || !q || !out) return KVQ_ERR_INVALID_ARG;
+  if (tokens < 1) return KVQ_ERR_INVALID_ARG;
+  if (tokens > cfg->max_tokens) return KVQ_ERR_CAPACITY;
+  if (((uintptr_t)layer_buf | (uintptr_t)q | (uintptr_t)out) % 16) return KVQ_ERR_INVALID_ARG;
+  kvq_layout L;
+  build_layout(cfg, g, &L);
+  Plan pl = make_plan(g, tokens, cfg->split_tokens);
+  DecodeParams& p = *pp;
+  std::memset(&p, 0, sizeof(p));
+  p.geo = g;
+  layer_ptrs(L, const_cast<void*>(layer_buf), &p.L);
+  p.q = q;
+  p.out = out;
+  p.lse = lse;
+  p.T = tokens;
+  p.S_eff = pl.S_eff;
+  p.Nq = pl.Nq;
+  p.W = pl.W;
+  p.n_qsplit = pl.n_qsplit;
+  p.n_split = pl.n_split;
+  p.gps = pl.gps;
+  p.fp16_tokens_per_split = pl.fp16_tps;
+  const double sm = cfg->softmax_scale > 0.0f ? (double)cfg->softmax_scale : 1.0 / std::sqrt((double)kHeadDim);
+  p.q_scale = (float)(sm * 1.4426950408889634);  // log2(e): softmax in base 2
+  p.hadamard_c = (float)(1.0 / std::sqrt((double)kHeadDim));
+  for (int i = 0; i < 8; ++i) {
+    p.k_lut_off[i] = cfg->k_lut[i] - cfg->k_lut[0];
+    p.v_lut_off[i] = cfg->v_lut[i] - cfg->v_lut[0];
+  }
+  for (int i = 0; i < kHeadDim / 2; ++i)
+    p.theta[i] = std::pow((double)cfg->rope_theta, -2.0 * i / (double)kHeadDim);
+  *persistent = persist_eligible(g);
+  *layout_ws = L.workspace_bytes;
+  return KVQ_OK;
+}
+
+// Scratch of one decode: split counters [NS], then (m, l) and accumulators
+// of every partial result (NS x splits for the split kernel; one per
+// (warp, stream) piece for the persistent kernel).
+static uint64_t scratch_bytes(const Geometry& g, uint64_t slots, uint64_t* cnt_bytes, uint64_t* ml_bytes) {
+  *cnt_bytes = align_up((uint64_t)g.NS * 4);
+  *ml_bytes = align_up(slots * g.g * 2 * 4);
+  return *cnt_bytes + *ml_bytes + slots * g.g * kHeadDim * 4;
+}
+
+static uint64_t slots_of(const DecodeParams& p, bool persistent) {
+  return persistent ? (uint64_t)p.nwarps + p.geo.NS : (uint64_t)p.geo.NS * p.n_split;
+}
+
+kvq_status decode_plan_device(DecodeParams* p, bool persistent, uint64_t* need) {
+  *need = 0;
+  if (persistent) {
+    uint64_t ignored;
+    if (plan_persist(*p, &ignored) != cudaSuccess) return KVQ_ERR_CUDA;
+  } else if (p->n_split <= 1) {
+    return KVQ_OK;
+  }
+  uint64_t c, m;
+  *need = scratch_bytes(p->geo, slots_of(*p, persistent), &c, &m);
+  return KVQ_OK;
+}
+
+kvq_status decode_launch(DecodeParams* p, bool persistent, void* ws, cudaStream_t st) {
+  uint64_t c, m;
+  if (persistent || p->n_split > 1) {
+    scratch_bytes(p->geo, slots_of(*p, persistent), &c, &m);
+    p->counters = (uint32_t*)ws;
+    p->part_ml = (float*)((char*)ws + c);
+    p->part_acc = (float*)((char*)ws + c + m);
+  }
+  const cudaError_t e = persistent ? launch_decode_persist(*p, st) : launch_decode(*p, st);
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+}  // namespace kvq
+
 extern "C" {
 
 const char* kvq_status_string(kvq_status s) {
@@ -290,52 +373,19 @@ kvq_status kvq_append(const kvq_config* cfg, void* layer_buf, int32_t tokens_bef
 kvq_status kvq_decode_attn(const kvq_config* cfg, const void* layer_buf, int32_t tokens,
                            const uint16_t* q, uint16_t* out, float* lse, void* workspace,
                            uint64_t ws_bytes, kvq_stream_t stream) {
-  Geometry g;
-  kvq_status st = make_geometry(cfg, &g);
-  if (st != KVQ_OK) return st;
-  if (!layer_buf || !q || !out) return KVQ_ERR_INVALID_ARG;
-  if (tokens < 1) return KVQ_ERR_INVALID_ARG;
-  if (tokens > cfg->max_tokens) return KVQ_ERR_CAPACITY;
-  if (((uintptr_t)layer_buf | (uintptr_t)q | (uintptr_t)out) % 16) return KVQ_ERR_INVALID_ARG;
-  kvq_layout L;
-  build_layout(cfg, g, &L);
-  Plan pl = make_plan(g, tokens, cfg->split_tokens);
-
   DecodeParams p;
-  std::memset(&p, 0, sizeof(p));
-  p.geo = g;
-  layer_ptrs(L, const_cast<void*>(layer_buf), &p.L);
-  p.q = q;
-  p.out = out;
-  p.lse = lse;
-  p.T = tokens;
-  p.S_eff = pl.S_eff;
-  p.Nq = pl.Nq;
-  p.W = pl.W;
-  p.n_qsplit = pl.n_qsplit;
-  p.n_split = pl.n_split;
-  p.gps = pl.gps;
-  p.fp16_tokens_per_split = pl.fp16_tps;
-  if (pl.n_split > 1) {
-    const uint64_t cnt_bytes = align_up((uint64_t)g.NS * 4);
-    const uint64_t ml_bytes = align_up((uint64_t)g.NS * pl.n_split * g.g * 2 * 4);
-    const uint64_t need = cnt_bytes + ml_bytes + (uint64_t)g.NS * pl.n_split * g.g * kHeadDim * 4;
-    if (!workspace || ws_bytes < need || ((uintptr_t)workspace % 16)) return KVQ_ERR_WORKSPACE;
-    p.counters = (uint32_t*)workspace;
-    p.part_ml = (float*)((char*)workspace + cnt_bytes);
-    p.part_acc = (float*)((char*)workspace + cnt_bytes + ml_bytes);
-  }
-  const double sm = cfg->softmax_scale > 0.0f ? (double)cfg->softmax_scale : 1.0 / std::sqrt((double)kHeadDim);
-  p.q_scale = (float)(sm * 1.4426950408889634);  // log2(e): softmax in base 2
-  p.hadamard_c = (float)(1.0 / std::sqrt((double)kHeadDim));
-  for (int i = 0; i < 8; ++i) {
-    p.k_lut_off[i] = cfg->k_lut[i] - cfg->k_lut[0];
-    p.v_lut_off[i] = cfg->v_lut[i] - cfg->v_lut[0];
-  }
-  for (int i = 0; i < kHeadDim / 2; ++i)
-    p.theta[i] = std::pow((double)cfg->rope_theta, -2.0 * i / (double)kHeadDim);
-  if (launch_decode(p, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
-  return KVQ_OK;
+  bool persistent = false;
+  uint64_t layout_ws = 0;
+  kvq_status st = decode_setup(cfg, layer_buf, tokens, q, out, lse, &p, &persistent, &layout_ws);
+  if (st != KVQ_OK) return st;
+  // the persistent kernel always needs scratch; ask for the layout's bound
+  // before touching the device
+  if (persistent && (!workspace || ws_bytes < layout_ws || ((uintptr_t)workspace % 16))) return KVQ_ERR_WORKSPACE;
+  uint64_t need = 0;
+  st = decode_plan_device(&p, persistent, &need);
+  if (st != KVQ_OK) return st;
+  if (need > 0 && (!workspace || ws_bytes < need || ((uintptr_t)workspace % 16))) return KVQ_ERR_WORKSPACE;
+  return decode_launch(&p, persistent, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -83,12 +83,53 @@ struct DecodeParams {
   float k_lut_off[8];     // L_i - L_0 (fp32)
   float v_lut_off[8];
   double theta[kHeadDim / 2];  // RoPE frequencies rope_theta^(-2i/d), fp64
+  // persistent schedule (tensor-core / fp16 kernels): the streams' work items
+  // -- ng quantized 32-token groups, then nt 32-token chunks of fp16 tokens --
+  // laid end to end, weighted by their bytes, cut into nwarps equal ranges.
+  int ng, nt, n_items;
+  int nwarps;
+  long long wq, wt, wstream, wtot;
 };
+
+// Persistent-schedule arithmetic shared by host and device.
+__host__ __device__ inline long long item_pos(const DecodeParams& p, long long j) {
+  const long long s = j / p.n_items, k = j % p.n_items;
+  return s * p.wstream + (k <= p.ng ? k * p.wq : p.ng * p.wq + (k - p.ng) * p.wt);
+}
+// First item whose start weight is >= x (x in [0, wtot]).
+__host__ __device__ inline long long first_item_at(const DecodeParams& p, long long x) {
+  long long s = x / p.wstream, rem = x - s * p.wstream, k;
+  if (rem == 0) return s * p.n_items;
+  if (rem <= p.ng * p.wq) k = (rem + p.wq - 1) / p.wq;
+  else k = p.ng + (rem - p.ng * p.wq + p.wt - 1) / p.wt;
+  if (k >= p.n_items) return (s + 1) * p.n_items;
+  return s * p.n_items + k;
+}
+// Warp i covers weight [x_i, x_{i+1}), x_i = floor(i * wtot / nwarps).
+__host__ __device__ inline long long warp_x(const DecodeParams& p, long long i) {
+  return i * p.wtot / p.nwarps;
+}
+__host__ __device__ inline int owner_of(const DecodeParams& p, long long pos) {
+  return (int)(((pos + 1) * p.nwarps + p.wtot - 1) / p.wtot - 1);
+}
 
 // ------------------------------------------------------------ host hooks
 cudaError_t launch_append_quantize(const AppendParams& p, int n_groups, cudaStream_t st);
 cudaError_t launch_append_window(const AppendParams& p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st);
+// Persistent decode (uniform K/V with 64-channel V groups, no RoPE; or an fp16
+// cache).  Fills the schedule fields of p (nwarps from the device's SM count
+// and the kernel's occupancy) and reports the workspace it needs.
+bool persist_eligible(const Geometry& g);
+cudaError_t plan_persist(DecodeParams& p, uint64_t* ws_need);
+cudaError_t launch_decode_persist(const DecodeParams& p, cudaStream_t st);
+// One decode in three steps (kvq_decode_attn and the no-allocation entry
+// point share them): validate and plan on the host; size the scratch (the
+// persistent plan asks the device for its SM count and occupancy); launch.
+kvq_status decode_setup(const kvq_config* cfg, const void* layer_buf, int32_t tokens, const uint16_t* q,
+                        uint16_t* out, float* lse, DecodeParams* p, bool* persistent, uint64_t* layout_ws);
+kvq_status decode_plan_device(DecodeParams* p, bool persistent, uint64_t* need);
+kvq_status decode_launch(DecodeParams* p, bool persistent, void* ws, cudaStream_t st);
 
 // --------------------------------------------------------- device helpers
 #ifdef __CUDACC__

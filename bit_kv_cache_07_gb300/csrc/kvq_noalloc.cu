@@ -59,24 +59,20 @@ cudaError_t scratch_for_current_device(void** out) {
 extern "C" kvq_status kvq_decode_attn_noalloc(const kvq_config* cfg, const void* layer_buf, int32_t tokens,
                                               const uint16_t* q, uint16_t* out, float* lse,
                                               kvq_stream_t stream) {
-  if (!layer_buf || !q || !out) return KVQ_ERR_INVALID_ARG;
-  kvq_layout L;
-  kvq_status st = kvq_layout_query(cfg, &L);
+  kvq::DecodeParams p;
+  bool persistent = false;
+  uint64_t layout_ws = 0;
+  kvq_status st = kvq::decode_setup(cfg, layer_buf, tokens, q, out, lse, &p, &persistent, &layout_ws);
   if (st != KVQ_OK) return st;
-  int32_t n_split = 0, n_qsplit = 0;
-  st = kvq_decode_plan(cfg, tokens, &n_split, &n_qsplit);
+  uint64_t need = 0;
+  st = kvq::decode_plan_device(&p, persistent, &need);
   if (st != KVQ_OK) return st;
-  // the same scratch layout kvq_decode_attn uses: counters, (m, l), accumulators
-  const uint64_t ns = (uint64_t)cfg->batch * cfg->n_kv_heads;
-  const uint64_t g = (uint64_t)(cfg->n_q_heads / cfg->n_kv_heads);
-  const uint64_t cnt = round_up(ns * 4, 256);
-  const uint64_t need = n_split > 1
-      ? cnt + round_up(ns * n_split * g * 2 * 4, 256) + ns * n_split * g * kvq::kHeadDim * 4
-      : 0;
   if (need > kNoAllocScratchBytes) return KVQ_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (scratch_for_current_device(&scratch) != cudaSuccess) return KVQ_ERR_CUDA;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // the split counters sit at the start of the scratch and must start at zero
+  const uint64_t cnt = round_up((uint64_t)cfg->batch * cfg->n_kv_heads * 4, 256);
   if (need > 0 && cudaMemsetAsync(scratch, 0, cnt, cs) != cudaSuccess) return KVQ_ERR_CUDA;
-  return kvq_decode_attn(cfg, layer_buf, tokens, q, out, lse, scratch, kNoAllocScratchBytes, stream);
+  return kvq::decode_launch(&p, persistent, scratch, cs);
 }

@@ -1,0 +1,43 @@
+// Host-side check of the persistent decode's work schedule: every item has
+// exactly one owner warp, no warp range is empty under the launch cap, the
+// owner formula agrees with the ranges, and the (warp, stream) slots are
+// distinct and in bounds.  Built and run by test_schedule_host.py.
+#include "../bit_kv_cache_07_gb300/csrc/kvq_internal.cuh"
+#include <cstdio>
+#include <set>
+#include <vector>
+using namespace kvq;
+int main() {
+  int bad = 0, cases = 0;
+  for (int NS : {1, 2, 7, 32, 256}) for (int ng : {0, 1, 3, 31, 125}) for (int nt : {0, 1, 3}) for (long long wq : {3328LL, 5376LL, 9984LL}) {
+    if (ng + nt == 0) continue;
+    DecodeParams p{}; p.ng = ng; p.nt = nt; p.n_items = ng + nt; p.wq = wq; p.wt = 16384;
+    p.wstream = ng * wq + nt * p.wt; p.wtot = NS * p.wstream;
+    long long items = (long long)NS * p.n_items;
+    for (long long nw0 : {1LL, 5LL, 37LL, 1824LL}) {
+      long long nw = nw0; if (nw > items) nw = items; if (nw > 64LL * NS) nw = 64LL * NS;
+      long long wmax = p.ng > 0 && p.wq > p.wt ? p.wq : p.wt; if (nw > p.wtot / wmax) nw = p.wtot / wmax; if (nw < 1) nw = 1;
+      p.nwarps = (int)nw; ++cases;
+      std::vector<int> own(items, -1);
+      for (int i = 0; i < nw; ++i) {
+        long long j0 = first_item_at(p, warp_x(p, i)), j1 = first_item_at(p, warp_x(p, i + 1));
+        if (j0 >= j1) { printf("empty range NS=%d ng=%d nt=%d nw=%lld i=%d\n", NS, ng, nt, nw, i); ++bad; }
+        for (long long j = j0; j < j1; ++j) { if (own[j] != -1) ++bad; own[j] = i; }
+      }
+      std::set<long long> slots;
+      for (long long j = 0; j < items; ++j) {
+        if (own[j] < 0) { printf("unowned item\n"); ++bad; continue; }
+        if (owner_of(p, item_pos(p, j)) != own[j]) { printf("owner mismatch\n"); ++bad; }
+      }
+      for (int s = 0; s < NS; ++s) {
+        std::set<int> ws;
+        for (int k = 0; k < p.n_items; ++k) ws.insert(own[(long long)s * p.n_items + k]);
+        int wf = owner_of(p, item_pos(p, (long long)s * p.n_items)), wl = owner_of(p, item_pos(p, (long long)s * p.n_items + p.n_items - 1));
+        if ((int)ws.size() != wl - wf + 1) { printf("count mismatch s=%d\n", s); ++bad; }
+        for (int w : ws) { if (!slots.insert(w + s).second) { printf("slot clash\n"); ++bad; } if (w + s >= nw + NS) ++bad; }
+      }
+    }
+  }
+  printf("cases %d bad %d\n", cases, bad);
+  return bad != 0;
+}

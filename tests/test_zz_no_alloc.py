@@ -63,12 +63,11 @@ def test_noalloc_matches_workspace_entry_point_twice(B, kw):
 
 
 def test_noalloc_rejects_scratch_beyond_its_size(B):
-    """512 streams x 4 splits x 8 heads of partials need more than 8 MiB:
-    the call must return KVQ_ERR_WORKSPACE before touching the GPU."""
-    cfg = _cfg(batch=64, n_kv_heads=8, n_q_heads=64, max_tokens=5000)
-    splits, _ = B.kvq_decode_plan(cfg, 4000)
-    need = 512 * splits * 8 * (2 + 128) * 4
-    assert need > (8 << 20)
+    """2048 streams x 8 query heads: even one partial result per stream
+    (2048 x 8 x (2 + 128) floats) exceeds 8 MiB, so the call must return
+    KVQ_ERR_WORKSPACE before launching anything."""
+    cfg = _cfg(batch=64, n_kv_heads=32, n_q_heads=256, max_tokens=5000)
+    assert 2048 * 8 * (2 + 128) * 4 > (8 << 20)
     c = B.make_config(cfg)
     fake = 1 << 20  # never dereferenced: the size check comes first
     assert B.lib().kvq_decode_attn_noalloc(C.byref(c), fake, 4000, fake, fake, None, None) == -4
