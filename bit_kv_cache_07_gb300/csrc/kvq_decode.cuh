@@ -381,7 +381,10 @@ __device__ __forceinline__ size_t fp16_row(const DecodeParams& p, int s, int k, 
 // One 32-token chunk of fp16 tokens (sinks / window, or an fp16 cache) for
 // one warp: lane = token for q.k, lane = 4 channels for p.v.  sq is the
 // scaled query [GQ][d] in shared memory, pbuf this warp's [32][GQ] buffer.
-template <int GQ>
+// KBATCH / VBATCH: independent loads in flight per batch (K: 16-byte pieces
+// of the lane's row; V: rows), traded against registers.  ROPE = false
+// compiles the RoPE path out (callers that never see pre-RoPE keys).
+template <int GQ, int KBATCH = 8, int VBATCH = 8, bool ROPE = true>
 __device__ __forceinline__ void fp16_chunk(const DecodeParams& p, const float (*sq)[kHeadDim],
                                            float (*pbuf)[GQ], int s, int k0, int k1, int lane,
                                            float (&m)[GQ], float (&lsum)[GQ], float (&acc)[GQ][4],
@@ -398,26 +401,26 @@ __device__ __forceinline__ void fp16_chunk(const DecodeParams& p, const float (*
     const uint4* krow = reinterpret_cast<const uint4*>((sink ? p.L.k_sink : p.L.k_ring) + off);
 #pragma unroll
     for (int r = 0; r < GQ; ++r) z[r] = 0.0f;
-    if (!G.pre_rope) {
-      // the row in two batches of 8 independent 16-byte loads
+    if (!ROPE || !G.pre_rope) {
+      // the row in batches of KBATCH independent 16-byte loads
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint4 u[8];
+      for (int half = 0; half < 16 / KBATCH; ++half) {
+        uint4 u[KBATCH];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) u[i] = __ldg(krow + 8 * half + i);
+        for (int i = 0; i < KBATCH; ++i) u[i] = __ldg(krow + KBATCH * half + i);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < KBATCH; ++i) {
           const uint32_t wd[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
             const float2 kv = __half22float2(*reinterpret_cast<const __half2*>(&wd[h]));
-            const int c = (8 * half + i) * 8 + 2 * h;
+            const int c = (KBATCH * half + i) * 8 + 2 * h;
 #pragma unroll
             for (int r = 0; r < GQ; ++r) z[r] = fmaf(sq[r][c], kv.x, fmaf(sq[r][c + 1], kv.y, z[r]));
           }
         }
       }
-    } else {
+    } else if constexpr (ROPE) {
       // RoPE pairs (j, j + d/2): the row's first half holds channel j, the second j + d/2
       uint4 ua[8], ub[8];
 #pragma unroll
@@ -449,11 +452,11 @@ __device__ __forceinline__ void fp16_chunk(const DecodeParams& p, const float (*
   }
   softmax_update<GQ>(z, m, lsum, acc, macc, pbuf, lane);
   const int n = min(32, k1 - k0);
-  // V rows in batches of 8 tokens: the loads of a batch are independent
-  for (int t0 = 0; t0 < n; t0 += 8) {
-    uint2 u[8];
+  // V rows in batches of VBATCH tokens: the loads of a batch are independent
+  for (int t0 = 0; t0 < n; t0 += VBATCH) {
+    uint2 u[VBATCH];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < VBATCH; ++i) {
       u[i] = make_uint2(0u, 0u);
       if (t0 + i < n) {
         bool sink;
@@ -463,7 +466,7 @@ __device__ __forceinline__ void fp16_chunk(const DecodeParams& p, const float (*
       }
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < VBATCH; ++i) {
       if (t0 + i >= n) break;
       const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&u[i].x));
       const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&u[i].y));

@@ -113,20 +113,39 @@ __device__ __forceinline__ uint32_t ext2(uint32_t w, int i) {
 // A fragment of k-step s for one token row, from this thread's 32-channel
 // slice of the packed row (words w[]: KB=8: 8 words, KB=4: 4, KB=2: 2).
 // Returns (lo, hi): lo holds k-slots (2t, 2t+1), hi holds (2t+8, 2t+9).
+//
+// The K codes enter the mma with the magic offset left in: one lop3 (or
+// byte permute) per two codes and no fp16 fix-up.  For channel c the
+// operand is 1024 + code * u_c, u_c = 1 (8-bit), 16^(c & 1) (4-bit) or
+// 4^(c & 3) (2-bit), set by the bit field's place in its 16-bit half.  The
+// Q' operand of channel c is scaled by 2^E / u_c (exact powers of two), so
+// the mma sums 2^E (code q'_c + 1024 q'_c / u_c); the constant part,
+// 1024 * sum_c q'_c / u_c, leaves with the group's bias.
 template <int KB>
 __device__ __forceinline__ void k_frag(const uint32_t* w, int s, uint32_t& lo, uint32_t& hi) {
   if (KB == 8) {
-    lo = ext8(w[s], 0);
-    hi = ext8(w[s], 1);
+    lo = __byte_perm(w[s], 0x64646464u, 0x4240u);
+    hi = __byte_perm(w[s], 0x64646464u, 0x4341u);
   } else if (KB == 4) {
-    const int pa = (s & 1) ? 2 : 0;
-    lo = ext4(w[s >> 1], pa);
-    hi = ext4(w[s >> 1], pa + 1);
+    const uint32_t x = (s & 1) ? (w[s >> 1] >> 8) : w[s >> 1];
+    lo = lop3_or_and(x, 0x000F000Fu, 0x64006400u);  // 1024 + c
+    hi = lop3_or_and(x, 0x00F000F0u, 0x64006400u);  // 1024 + 16 c
   } else {
-    const int ia = 2 * (s & 3);
-    lo = ext2(w[s >> 2], ia);
-    hi = ext2(w[s >> 2], ia + 1);
+    const int ia = 2 * (s & 3);  // pairs ia, ia + 1 of the word: crumb places ia & 3, (ia + 1) & 3
+    const uint32_t x = (ia >= 4) ? (w[s >> 2] >> 8) : w[s >> 2];
+    lo = lop3_or_and(x, 0x00030003u << (2 * (ia & 3)), 0x64006400u);        // 1024 + 4^m c
+    hi = lop3_or_and(x, 0x00030003u << (2 * ((ia + 1) & 3)), 0x64006400u);
   }
+}
+
+// log2 of the common factor 2^E of the K-side B operand (keeps q'_c / u_c
+// and its lo part clear of fp16 subnormals).
+template <int KB>
+__device__ __forceinline__ constexpr int kq_exp() { return KB == 8 ? 0 : KB == 4 ? 4 : 6; }
+// Q' multiplier 2^E / u_c for channel c with c & 3 == k.
+template <int KB>
+__device__ __forceinline__ constexpr float kq_mult(int k) {
+  return KB == 8 ? 1.0f : KB == 4 ? ((k & 1) ? 1.0f : 16.0f) : (k == 0 ? 64.0f : k == 1 ? 16.0f : k == 2 ? 4.0f : 1.0f);
 }
 
 // Where channel offset o (0..31) of a thread's slice lands: k-step s and
@@ -157,30 +176,59 @@ __device__ __forceinline__ int v_chan(int mc, int g, int rh) {
   return 64 * (mc >> 2) + 8 * g + (mc & 3) + 4 * rh;
 }
 
+// ------------------------------------------------------------- stage layout
+// One pipeline stage holds one 32-token group: K codes, the group's K
+// {min, scale} per channel, V codes, V {min, scale} per (token, channel
+// group).  Code rows are stored unpadded; their 16-byte chunks are XOR-
+// swizzled by row (chunk ^= bits 7.. of the byte offset, masked), so that
+// the fragment reads -- 8 rows x 16 bytes per 8x8 matrix -- touch 32
+// distinct banks.
+__device__ __forceinline__ uint32_t swz(uint32_t off, uint32_t mask) { return off ^ (((off >> 7) & mask) << 4); }
+
 template <int KB, int VB>
 struct StageGeom {
   static constexpr int KROW = kHeadDim * KB / 8;
   static constexpr int VROW = kHeadDim * VB / 8;
-  static constexpr int KPITCH = KROW + (KB == 8 ? 16 : 0);
-  static constexpr int VPITCH = VROW + 16;
+  static constexpr uint32_t KSW = KB == 8 ? 7u : 0u;         // 128-byte K rows need it
+  static constexpr uint32_t VSW = (uint32_t)(VROW / 16 - 1);  // 32/64/128-byte V rows
   static constexpr int KC = 0;
-  static constexpr int KS = KC + kGroupTokens * KPITCH;
+  static constexpr int KS = KC + kGroupTokens * KROW;
   static constexpr int VC = KS + kHeadDim * 4;
-  static constexpr int VS = VC + kGroupTokens * VPITCH;
-  static constexpr int BYTES = ((VS + kGroupTokens * 4 * 4) + 127) / 128 * 128;  // V scales: up to 4 groups
+  static constexpr int VS = VC + kGroupTokens * VROW;
+  static constexpr int BYTES = ((VS + kGroupTokens * kNVG * 4) + 127) / 128 * 128;
 };
 
 // Per-warp scratch of the group processing (4 warps per CTA).
+//  bq:  each lane's B fragments of Q' (32 halves = one 64-byte row per lane,
+//       chunks swizzled like a 64-byte code row)
+//  vsc/vmn: V scale / min of the group's tokens in fp32, ordered so that
+//       the 4 tokens a lane needs sit in one 16-byte vector:
+//       vsc[j][kt][tq][4] holds tokens 16kt + 2tq + {0, 1, 8, 9} (P' build),
+//       vmn[j][gq][4]     holds tokens gq + {0, 8, 16, 24}     (softmax rows)
 template <int NT>
 struct MmaWarpSmem {
-  alignas(16) uint16_t bq[4][NT][32][40];        // each lane's 32 Q' halves per n-tile (+ pad)
-  alignas(16) float bias[4][8 * NT];             // q . kmin of the current group, per head
-  alignas(16) float vsc[4][kNVG][kGroupTokens];  // V scale of each token of the group (fp32)
-  alignas(16) float vmn[4][kNVG][kGroupTokens];  // V min of each token of the group (fp32)
+  alignas(128) uint16_t bq[4][NT][32][32];
+  alignas(16) float bias[4][8 * NT];
+  alignas(16) float vsc[4][kNVG][kGroupTokens];
+  alignas(16) float vmn[4][kNVG][kGroupTokens];
 };
 
+__device__ __forceinline__ int vsc_index(int t) {  // token -> slot in vsc[j][..]
+  const int r = t & 15;
+  return (t >> 4) * 16 + ((r & 7) >> 1) * 4 + (r & 1) + 2 * (r >> 3);
+}
+__device__ __forceinline__ int vmn_index(int t) { return (t & 7) * 4 + (t >> 3); }
+
+__device__ __forceinline__ float ex2(float x) {  // 2^x (hardware approximation; 2^-inf = 0)
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Queue the asynchronous copies of one 32-token group of stream s into the
+// stage at shared address dst.  Every lane issues its share.
 template <int KB, int VB>
-__device__ __forceinline__ void issue_group(const DecodeParams& p, int s, int grp, unsigned char* dst, int lane) {
+__device__ __forceinline__ void issue_group(const DecodeParams& p, int s, int grp, uint32_t dst, int lane) {
   using SG = StageGeom<KB, VB>;
   const Geometry& G = p.geo;
   const size_t row0 = (size_t)s * G.qcap + (size_t)grp * kGroupTokens;
@@ -188,19 +236,14 @@ __device__ __forceinline__ void issue_group(const DecodeParams& p, int s, int gr
   const uint8_t* vc = p.L.v_codes + row0 * SG::VROW;
   const uint32_t* ks = p.L.k_scales + ((size_t)s * G.gcap + grp) * kHeadDim;
   const uint32_t* vs = p.L.v_scales + row0 * kNVG;
-  const uint32_t base = smem_u32(dst);
-  constexpr int KCH = SG::KROW / 16, VCH = SG::VROW / 16;
-  for (int i = lane; i < kGroupTokens * KCH; i += 32) {
-    const int r = i / KCH, c = i % KCH;
-    cp_async16(base + SG::KC + r * SG::KPITCH + 16 * c, kc + (size_t)r * SG::KROW + 16 * c);
-  }
-  cp_async16(base + SG::KS + 16 * lane, ks + 4 * lane);  // 512 B = 32 chunks
-  for (int i = lane; i < kGroupTokens * VCH; i += 32) {
-    const int r = i / VCH, c = i % VCH;
-    cp_async16(base + SG::VC + r * SG::VPITCH + 16 * c, vc + (size_t)r * SG::VROW + 16 * c);
-  }
-  constexpr int vs_chunks = kGroupTokens * kNVG / 4;  // 16-byte chunks of V scales
-  for (int i = lane; i < vs_chunks; i += 32) cp_async16(base + SG::VS + 16 * i, vs + 4 * i);
+  constexpr int KCH = kGroupTokens * SG::KROW / 16, VCH = kGroupTokens * SG::VROW / 16;
+  static_assert(KCH % 32 == 0 && VCH % 32 == 0, "whole chunks per lane");
+#pragma unroll
+  for (int i = lane; i < KCH; i += 32) cp_async16(dst + SG::KC + swz(16 * i, SG::KSW), kc + 16 * i);
+  cp_async16(dst + SG::KS + 16 * lane, ks + 4 * lane);  // 512 B = 32 chunks
+#pragma unroll
+  for (int i = lane; i < VCH; i += 32) cp_async16(dst + SG::VC + swz(16 * i, SG::VSW), vc + 16 * i);
+  if (lane < kGroupTokens * kNVG / 4) cp_async16(dst + SG::VS + 16 * lane, vs + 4 * lane);
 }
 
 // V group (0 .. d/G_V - 1) of m-tile mc: every m-tile lies inside one group.
@@ -209,21 +252,25 @@ __device__ __forceinline__ constexpr int v_group(int mc) {
   return (VB == 8 ? 16 * mc : VB == 4 ? 32 * (mc >> 1) : 64 * (mc >> 2)) / kGV;
 }
 
+// hi (or lo) fp16 part of x, as a float: lanes with lo = 1 get x - fp16(x).
+__device__ __forceinline__ float split_part(float x, float lo) {
+  return fmaf(-lo, __half2float(__float2half_rn(x)), x);
+}
+
 // One 32-token group for one warp: Q' fragments, S = K Q' (2 m-tiles x NT
 // n-tiles), online softmax, O += V^T P' (8 m-tiles x NT).
+//  qh[k]: byte offset, inside a 64-byte fragment row, of this lane's
+//         channel 4*lane+k (hi row; the lo row's offset is qh[k] ^ 32)
 template <int KB, int VB, int NT>
-__device__ __forceinline__ void process_group(const DecodeParams& p, const float (*qw)[kHeadDim],
-                                              MmaWarpSmem<NT>& sm, const unsigned char* st,
-                                              int w, int lane, const int (&qoff)[4], float (&O)[8][NT][4],
+__device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWarpSmem<NT>& sm,
+                                              const unsigned char* st, int g, int w, int lane,
+                                              const int (&qh)[4], float (&O)[8][NT][4],
                                               float (&macc)[NT][kNVG], float (&m_used)[NT], float (&lsum)[NT]) {
   using SG = StageGeom<KB, VB>;
-  const Geometry& G = p.geo;
-  const int g = G.g;
-  constexpr int nvg = kNVG;
   const int gq = lane >> 2, tq = lane & 3;
 
-  // (a) Q' = q * scale_k (hi + lo fp16) into this warp's fragment buffer, bias = q . min_k;
-  //     V {min, scale} of this lane's token to fp32
+  // (a) Q' = q * scale_k (hi + lo fp16) into this warp's fragment rows,
+  //     bias = q . min_k; V {min, scale} of this lane's token to fp32
   {
     const uint4 sc = *reinterpret_cast<const uint4*>(st + SG::KS + 16 * lane);
     const uint32_t wv[4] = {sc.x, sc.y, sc.z, sc.w};
@@ -234,43 +281,45 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const float
 #pragma unroll
     for (int r = 0; r < 8 * NT; ++r) {
       if (r >= g) break;
-      const int nt = r >> 2, col = 2 * (r & 3);
-      uint16_t* dhi = &sm.bq[w][nt][4 * col + tsl][0];
-      uint16_t* dlo = &sm.bq[w][nt][4 * (col + 1) + tsl][0];
+      unsigned char* dhi = reinterpret_cast<unsigned char*>(&sm.bq[w][r >> 2][8 * (r & 3) + tsl][0]);
+      unsigned char* dlo = dhi + 4 * 64;
       const float4 q4 = *reinterpret_cast<const float4*>(&qw[r][4 * lane]);
       const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
-      float bp = 0.0f;
+      float bp = 0.0f, off = 0.0f;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float qp = qv[k] * ms[k].y;
+        const float qp = qv[k] * ms[k].y * kq_mult<KB>(k);  // channel 4*lane + k: c & 3 == k
         bp = fmaf(qv[k], ms[k].x, bp);
         const __half hi = __float2half_rn(qp);
         const __half lo = __float2half_rn(qp - __half2float(hi));
-        dhi[qoff[k]] = __half_as_ushort(hi);
-        dlo[qoff[k]] = __half_as_ushort(lo);
+        off += __half2float(hi) + __half2float(lo);
+        *reinterpret_cast<__half*>(dhi + qh[k]) = hi;
+        *reinterpret_cast<__half*>(dlo + (qh[k] ^ 32)) = lo;
       }
-      bp = warp_sum(bp);
+      // the mma's constant part 1024 * sum_c (hi + lo), in logit units
+      bp = warp_sum(fmaf(-1024.0f * (1.0f / (float)(1 << kq_exp<KB>())), off, bp));
       if (lane == 0) sm.bias[w][r] = bp;
     }
     const uint32_t* vsw = reinterpret_cast<const uint32_t*>(st + SG::VS);
+    const int iv = vsc_index(lane), im = vmn_index(lane);
 #pragma unroll
     for (int j = 0; j < kNVG; ++j) {
       const float2 m2 = unpack_min_scale(vsw[lane * kNVG + j]);
-      sm.vmn[w][j][lane] = m2.x;
-      sm.vsc[w][j][lane] = m2.y;
+      sm.vmn[w][j][im] = m2.x;
+      sm.vsc[w][j][iv] = m2.y;
     }
   }
   __syncwarp();
 
-  // (b) this thread's Q' fragments
+  // (b) this thread's Q' fragments (row = lane, chunks unswizzled on read)
   uint32_t bq[NT][16];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const uint4* src = reinterpret_cast<const uint4*>(&sm.bq[w][nt][lane][0]);
+    const unsigned char* row = reinterpret_cast<const unsigned char*>(&sm.bq[w][nt][lane][0]);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint4 u = src[k];
-      bq[nt][4 * k] = u.x; bq[nt][4 * k + 1] = u.y; bq[nt][4 * k + 2] = u.z; bq[nt][4 * k + 3] = u.w;
+    for (int c = 0; c < 4; ++c) {
+      const uint4 u = *reinterpret_cast<const uint4*>(row + 16 * (c ^ ((lane >> 1) & 3)));
+      bq[nt][4 * c] = u.x; bq[nt][4 * c + 1] = u.y; bq[nt][4 * c + 2] = u.z; bq[nt][4 * c + 3] = u.w;
     }
   }
 
@@ -284,19 +333,23 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const float
       for (int k = 0; k < 4; ++k) S[mt][nt][k] = 0.0f;
     constexpr int NW = SG::KROW / 16;  // words in this thread's 32-channel slice
     uint32_t w0[NW], w1[NW];
-    const unsigned char* r0 = st + SG::KC + (16 * mt + gq) * SG::KPITCH + 4 * NW * tq;
-    const unsigned char* r1 = r0 + 8 * SG::KPITCH;
+    const uint32_t o0 = (16 * mt + gq) * SG::KROW + 4 * NW * tq;
+    const uint32_t o1 = o0 + 8 * SG::KROW;
     if constexpr (NW == 8) {
-      const uint4 a = *reinterpret_cast<const uint4*>(r0), b2 = *reinterpret_cast<const uint4*>(r0 + 16);
-      const uint4 c = *reinterpret_cast<const uint4*>(r1), d2 = *reinterpret_cast<const uint4*>(r1 + 16);
+      const uint4 a = *reinterpret_cast<const uint4*>(st + SG::KC + swz(o0, SG::KSW));
+      const uint4 b2 = *reinterpret_cast<const uint4*>(st + SG::KC + swz(o0 + 16, SG::KSW));
+      const uint4 c = *reinterpret_cast<const uint4*>(st + SG::KC + swz(o1, SG::KSW));
+      const uint4 d2 = *reinterpret_cast<const uint4*>(st + SG::KC + swz(o1 + 16, SG::KSW));
       w0[0] = a.x; w0[1] = a.y; w0[2] = a.z; w0[3] = a.w; w0[4] = b2.x; w0[5] = b2.y; w0[6] = b2.z; w0[7] = b2.w;
       w1[0] = c.x; w1[1] = c.y; w1[2] = c.z; w1[3] = c.w; w1[4] = d2.x; w1[5] = d2.y; w1[6] = d2.z; w1[7] = d2.w;
     } else if constexpr (NW == 4) {
-      const uint4 a = *reinterpret_cast<const uint4*>(r0), c = *reinterpret_cast<const uint4*>(r1);
+      const uint4 a = *reinterpret_cast<const uint4*>(st + SG::KC + o0);
+      const uint4 c = *reinterpret_cast<const uint4*>(st + SG::KC + o1);
       w0[0] = a.x; w0[1] = a.y; w0[2] = a.z; w0[3] = a.w;
       w1[0] = c.x; w1[1] = c.y; w1[2] = c.z; w1[3] = c.w;
     } else {
-      const uint2 a = *reinterpret_cast<const uint2*>(r0), c = *reinterpret_cast<const uint2*>(r1);
+      const uint2 a = *reinterpret_cast<const uint2*>(st + SG::KC + o0);
+      const uint2 c = *reinterpret_cast<const uint2*>(st + SG::KC + o1);
       w0[0] = a.x; w0[1] = a.y;
       w1[0] = c.x; w1[1] = c.y;
     }
@@ -324,26 +377,30 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const float
       for (int k = 0; k < 4; ++k) S[mt][nt][k] += S2[nt][k];
   }
 
-  // (d) online softmax (base 2); this thread's heads are 4*nt + tq
+  // (d) online softmax (base 2); this thread's heads are 4*nt + tq, its
+  //     tokens gq + {0, 8, 16, 24}
   float P[NT][2][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int h = 4 * nt + tq;
-    const float bias = (h < g) ? sm.bias[w][h] : 0.0f;
-    float z[2][2];
+    const bool live = h < g;
+    const float bias = live ? sm.bias[w][h] : 0.0f;
+    float zs[2][2];
     float zm = -INFINITY;
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
       for (int rh = 0; rh < 2; ++rh) {
-        z[mt][rh] = (S[mt][nt][2 * rh] + S[mt][nt][2 * rh + 1]) + bias;
-        zm = fmaxf(zm, z[mt][rh]);
+        zs[mt][rh] = S[mt][nt][2 * rh] + S[mt][nt][2 * rh + 1];  // 2^E x (logit - bias)
+        zm = fmaxf(zm, zs[mt][rh]);
       }
     zm = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, 4));
     zm = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, 8));
     zm = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, 16));
+    constexpr float kUnscale = 1.0f / (float)(1 << kq_exp<KB>());
+    zm = live ? fmaf(zm, kUnscale, bias) : -INFINITY;
     if (zm > m_used[nt] + kLazyRescale) {
-      const float alpha = (m_used[nt] == -INFINITY) ? 0.0f : exp2f(m_used[nt] - zm);
+      const float alpha = ex2(m_used[nt] - zm);  // 0 when m_used is -inf
 #pragma unroll
       for (int mc = 0; mc < 8; ++mc)
 #pragma unroll
@@ -353,29 +410,32 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const float
       lsum[nt] *= alpha;
       m_used[nt] = zm;
     }
+    const float bm = live ? bias - m_used[nt] : -INFINITY;
     float ps = 0.0f;
+    float pv[4];
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
       for (int rh = 0; rh < 2; ++rh) {
-        const float pv = (h < g) ? exp2f(z[mt][rh] - m_used[nt]) : 0.0f;
-        P[nt][mt][rh] = pv;
-        ps += pv;
-        const int tok = 16 * mt + 8 * rh + gq;
-#pragma unroll
-        for (int j = 0; j < nvg; ++j) macc[nt][j] = fmaf(pv, sm.vmn[w][j][tok], macc[nt][j]);
+        pv[2 * mt + rh] = ex2(fmaf(zs[mt][rh], kUnscale, bm));
+        P[nt][mt][rh] = pv[2 * mt + rh];
+        ps += pv[2 * mt + rh];
       }
+#pragma unroll
+    for (int j = 0; j < kNVG; ++j) {
+      const float4 mn = *reinterpret_cast<const float4*>(&sm.vmn[w][j][4 * gq]);  // tokens gq + 8i
+      macc[nt][j] = fmaf(pv[0], mn.x, fmaf(pv[1], mn.y, fmaf(pv[2], mn.z, fmaf(pv[3], mn.w, macc[nt][j]))));
+    }
     lsum[nt] += ps;
   }
 
   // (e) O += V^T P'
+  const float lo_sel = (gq & 1) ? 1.0f : 0.0f;  // this lane's B column is a lo column
 #pragma unroll
   for (int kt = 0; kt < 2; ++kt) {
     // P' fragments per (n-tile, V group): tokens 16kt + {2tq, 2tq+1, 2tq+8, 2tq+9}, column gq
     uint32_t bp[NT][kNVG][2];
     const int src1 = 8 * tq + (gq >> 1), src2 = src1 + 4;
-    const int t0 = 16 * kt + 2 * tq;
-    const bool lo_col = (gq & 1) != 0;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const float v0 = __shfl_sync(0xffffffffu, P[nt][kt][0], src1);
@@ -383,24 +443,13 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const float
       const float v2 = __shfl_sync(0xffffffffu, P[nt][kt][1], src1);
       const float v3 = __shfl_sync(0xffffffffu, P[nt][kt][1], src2);
 #pragma unroll
-      for (int j = 0; j < nvg; ++j) {
-        const float2 sa = *reinterpret_cast<const float2*>(&sm.vsc[w][j][t0]);
-        const float2 sb = *reinterpret_cast<const float2*>(&sm.vsc[w][j][t0 + 8]);
-        float x0 = v0 * sa.x;
-        float x1 = v1 * sa.y;
-        float x2 = v2 * sb.x;
-        float x3 = v3 * sb.y;
-        if (lo_col) {
-          x0 -= __half2float(__float2half_rn(x0));
-          x1 -= __half2float(__float2half_rn(x1));
-          x2 -= __half2float(__float2half_rn(x2));
-          x3 -= __half2float(__float2half_rn(x3));
-        }
-        bp[nt][j][0] = h2_as_u32(__floats2half2_rn(x0, x1));
-        bp[nt][j][1] = h2_as_u32(__floats2half2_rn(x2, x3));
+      for (int j = 0; j < kNVG; ++j) {
+        const float4 sv = *reinterpret_cast<const float4*>(&sm.vsc[w][j][16 * kt + 4 * tq]);
+        bp[nt][j][0] = h2_as_u32(__floats2half2_rn(split_part(v0 * sv.x, lo_sel), split_part(v1 * sv.y, lo_sel)));
+        bp[nt][j][1] = h2_as_u32(__floats2half2_rn(split_part(v2 * sv.z, lo_sel), split_part(v3 * sv.w, lo_sel)));
       }
     }
-    // V code fragments via ldmatrix.trans on the packed rows
+    // V code fragments via ldmatrix.trans on the packed (swizzled) rows
     const uint32_t vbase = smem_u32(st + SG::VC);
     const int mi = lane >> 3, rr = lane & 7;
     if (VB == 4) {
@@ -408,7 +457,7 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const float
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int blk = 2 * c + (mi >> 1), th = mi & 1;
-        const uint32_t addr = vbase + (16 * kt + 8 * th + rr) * SG::VPITCH + 16 * blk;
+        const uint32_t addr = vbase + swz((16 * kt + 8 * th + rr) * SG::VROW + 16 * blk, SG::VSW);
         ldsm_x4_trans(R[2 * c][0], R[2 * c][1], R[2 * c + 1][0], R[2 * c + 1][1], addr);
       }
 #pragma unroll
@@ -425,7 +474,7 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const float
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int blk = 2 * c + (mi >> 1), th = mi & 1;
-        const uint32_t addr = vbase + (16 * kt + 8 * th + rr) * SG::VPITCH + 16 * blk;
+        const uint32_t addr = vbase + swz((16 * kt + 8 * th + rr) * SG::VROW + 16 * blk, SG::VSW);
         ldsm_x4_trans(R[2 * c][0], R[2 * c][1], R[2 * c + 1][0], R[2 * c + 1][1], addr);
       }
 #pragma unroll
@@ -440,7 +489,7 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const float
       uint32_t R[2][2];
       {
         const int blk = mi >> 1, th = mi & 1;
-        const uint32_t addr = vbase + (16 * kt + 8 * th + rr) * SG::VPITCH + 16 * blk;
+        const uint32_t addr = vbase + swz((16 * kt + 8 * th + rr) * SG::VROW + 16 * blk, SG::VSW);
         ldsm_x4_trans(R[0][0], R[0][1], R[1][0], R[1][1], addr);
       }
 #pragma unroll
@@ -452,6 +501,174 @@ __device__ __forceinline__ void process_group(const DecodeParams& p, const float
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma16816(O[mc][nt], a0, a1, a2, a3, bp[nt][j][0], bp[nt][j][1]);
       }
+    }
+  }
+}
+
+// ------------------------------------------------------------ fp16 items
+// The fp16 tokens of a stream (sinks, then the recent window; or the whole
+// cache in fp16 mode) are processed in items of kF16Tokens tokens that go
+// through the same asynchronous-copy pipeline and tensor-core path as the
+// quantized groups: K rows are the A operand of S = K Q (rows = tokens), V
+// rows (transposed by ldmatrix) the A operand of O += V^T P.  An item's K
+// and V rows (256 bytes each) sit in the stage with their 16-byte chunks
+// swizzled: K chunk c of row t at c ^ 4(t & 1) (the fragment loads of a
+// quarter warp read rows 2i, 2i+1), V chunk c at c ^ (t & 7) (ldmatrix
+// reads one chunk of 8 consecutive rows).
+constexpr int kF16Tokens = 8;
+
+struct F16Geom {
+  static constexpr int KC = 0;
+  static constexpr int VC = kF16Tokens * kHeadDim * 2;
+  static constexpr int BYTES = 2 * kF16Tokens * kHeadDim * 2;
+};
+__device__ __forceinline__ uint32_t kf16_off(int t, int c) { return t * 256 + 16 * (c ^ (4 * (t & 1))); }
+__device__ __forceinline__ uint32_t vf16_off(int t, int c) { return t * 256 + 16 * (c ^ (t & 7)); }
+
+// 16-byte asynchronous copy that writes zeros instead when !valid (the
+// source address is not read then, but stays a valid one).
+__device__ __forceinline__ void cp_async16_zfill(uint32_t smem, const void* gmem, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem), "l"(gmem), "r"(valid ? 16 : 0));
+}
+
+__device__ __forceinline__ void mma1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(b0));
+}
+
+// Queue the copies of fp16 item (stream s, first fp16 token kk0; tokens at
+// or past k1 are zero-filled).  Lanes 0-15 copy the even tokens' rows,
+// lanes 16-31 the odd ones', one 16-byte chunk of K and of V each.
+__device__ __forceinline__ void issue_f16(const DecodeParams& p, int s, int kk0, int k1, uint32_t dst, int lane) {
+  const int c = lane & 15;
+#pragma unroll
+  for (int n = 0; n < kF16Tokens / 2; ++n) {
+    const int t = 2 * n + (lane >> 4);
+    const int kk = kk0 + t;
+    const bool valid = kk < k1;
+    bool sink;
+    int pos;
+    const size_t off = fp16_row(p, s, valid ? kk : kk0, &sink, &pos);
+    const uint16_t* kr = (sink ? p.L.k_sink : p.L.k_ring) + off;
+    const uint16_t* vr = (sink ? p.L.v_sink : p.L.v_ring) + off;
+    cp_async16_zfill(dst + F16Geom::KC + kf16_off(t, c), kr + 8 * c, valid);
+    cp_async16_zfill(dst + F16Geom::VC + vf16_off(t, c), vr + 8 * c, valid);
+  }
+}
+
+// B fragments of the (unquantized) query for the fp16 items, hi + lo fp16
+// per head.  Slot order: thread tq of the k dimension owns the 16-byte K
+// chunks tq, tq+4, tq+8, tq+12 (channels 8 * chunk ..); k-step s = 2i + h
+// takes channels 8(tq + 4i) + 4h + {0, 1} (lo pair) and + {2, 3} (hi pair).
+template <int NT>
+__device__ __forceinline__ void build_bq_f16(const float (*qw)[kHeadDim], MmaWarpSmem<NT>& sm, int g, int w,
+                                             int lane) {
+  const int tqr = (lane >> 1) & 3;                 // reader thread-in-group of channels 4*lane ..
+  const int sstep = 2 * (lane >> 3) + (lane & 1);  // their k-step
+  const int xr = ((tqr >> 1) & 1) << 4;            // hi row chunk swizzle ((row >> 1) & 3) << 4
+#pragma unroll
+  for (int r = 0; r < 8 * NT; ++r) {
+    if (r >= g) break;
+    unsigned char* dhi = reinterpret_cast<unsigned char*>(&sm.bq[w][r >> 2][8 * (r & 3) + tqr][0]);
+    unsigned char* dlo = dhi + 4 * 64;
+    const float4 q4 = *reinterpret_cast<const float4*>(&qw[r][4 * lane]);
+    const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int byte = 2 * (4 * sstep + k);
+      const __half hi = __float2half_rn(qv[k]);
+      const __half lo = __float2half_rn(qv[k] - __half2float(hi));
+      *reinterpret_cast<__half*>(dhi + (byte ^ xr)) = hi;
+      *reinterpret_cast<__half*>(dlo + (byte ^ xr ^ 32)) = lo;
+    }
+  }
+}
+
+// One fp16 item for one warp: S = K Q (token rows 0..7 of the m16 tile),
+// online softmax into (m_used, lsum), O += V^T P (m16n8k8: k = the 8 tokens).
+// O here is the plain-domain accumulator (standard channel order: row gq of
+// m-tile mc is channel 16 mc + gq).
+template <int NT>
+__device__ __forceinline__ void process_f16(const MmaWarpSmem<NT>& sm, const unsigned char* st, int g, int w,
+                                            int lane, int kk0, int k1, float (&O)[8][NT][4],
+                                            float (&m_used)[NT], float (&lsum)[NT]) {
+  const int gq = lane >> 2, tq = lane & 3;
+  uint32_t bq[NT][16];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const unsigned char* row = reinterpret_cast<const unsigned char*>(&sm.bq[w][nt][lane][0]);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 u = *reinterpret_cast<const uint4*>(row + 16 * (c ^ ((lane >> 1) & 3)));
+      bq[nt][4 * c] = u.x; bq[nt][4 * c + 1] = u.y; bq[nt][4 * c + 2] = u.z; bq[nt][4 * c + 3] = u.w;
+    }
+  }
+  // S = K Q: token row gq; rows 8..15 of the tile are empty
+  float S[NT][4], S2[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) S[nt][k] = S2[nt][k] = 0.0f;
+  uint4 kw[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) kw[i] = *reinterpret_cast<const uint4*>(st + F16Geom::KC + kf16_off(gq, tq + 4 * i));
+#pragma unroll
+  for (int s_ = 0; s_ < 8; ++s_) {
+    const uint4 u = kw[s_ >> 1];
+    const uint32_t lo = (s_ & 1) ? u.z : u.x, hi = (s_ & 1) ? u.w : u.y;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      if (s_ & 1)
+        mma16816(S2[nt], lo, 0u, hi, 0u, bq[nt][2 * s_], bq[nt][2 * s_ + 1]);
+      else
+        mma16816(S[nt], lo, 0u, hi, 0u, bq[nt][2 * s_], bq[nt][2 * s_ + 1]);
+    }
+  }
+  // online softmax over the item's tokens (this thread: token gq, head 4 nt + tq)
+  const bool tok_ok = kk0 + gq < k1;
+  float P[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const bool live = 4 * nt + tq < g;
+    const float z = (S[nt][0] + S2[nt][0]) + (S[nt][1] + S2[nt][1]);
+    float zm = tok_ok ? z : -INFINITY;
+    zm = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, 4));
+    zm = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, 8));
+    zm = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, 16));
+    if (!live) zm = -INFINITY;
+    if (zm > m_used[nt] + kLazyRescale) {
+      const float alpha = ex2(m_used[nt] - zm);
+#pragma unroll
+      for (int mc = 0; mc < 8; ++mc)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) O[mc][nt][k] *= alpha;
+      lsum[nt] *= alpha;
+      m_used[nt] = zm;
+    }
+    P[nt] = (live && tok_ok) ? ex2(z - m_used[nt]) : 0.0f;
+    lsum[nt] += P[nt];
+  }
+  // O += V^T P: B = P of tokens 2tq, 2tq+1 for column gq (head gq >> 1, hi / lo)
+  const float lo_sel = (gq & 1) ? 1.0f : 0.0f;
+  const int src0 = 8 * tq + (gq >> 1);  // lane holding token 2tq, head gq >> 1
+  uint32_t bp[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const float v0 = __shfl_sync(0xffffffffu, P[nt], src0);
+    const float v1 = __shfl_sync(0xffffffffu, P[nt], src0 + 4);
+    bp[nt] = h2_as_u32(__floats2half2_rn(split_part(v0, lo_sel), split_part(v1, lo_sel)));
+  }
+  const uint32_t vbase = smem_u32(st + F16Geom::VC);
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    uint32_t a[4];
+    ldsm_x4_trans(a[0], a[1], a[2], a[3], vbase + vf16_off(lane & 7, 4 * b + (lane >> 3)));
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      mma1688(O[2 * b][nt], a[0], a[1], bp[nt]);
+      mma1688(O[2 * b + 1][nt], a[2], a[3], bp[nt]);
     }
   }
 }

@@ -3,21 +3,27 @@
 //
 // The work of a layer is a list of items, stream by stream: the stream's
 // quantized 32-token groups, then its fp16 tokens (sinks + recent window,
-// or the whole cache in fp16 mode) in 32-token chunks.  Items are weighted
-// by the bytes they read and the list is cut into as many equal ranges as
-// there are resident warps.  A warp keeps its cp.async double buffer
-// running across its whole range -- also across stream boundaries -- so the
-// memory pipeline never drains at a barrier: there is no __syncthreads after
-// the prologue.
+// or the whole cache in fp16 mode) in items of kF16Tokens tokens.  Items
+// are weighted by the bytes they read and the list is cut into as many
+// equal ranges as there are resident warps.  Every item -- quantized or
+// fp16 -- goes through the warp's asynchronous-copy pipeline (kStages
+// shared-memory stages), which runs across the warp's whole range, also
+// across stream boundaries: there is no __syncthreads after the prologue.
 //
-// When a warp leaves a stream it folds what it has into one partial result
-// (m, l, O per query head; the quantized part of O already rotated back in
-// Hadamard mode -- the rotation is linear, so rotating each partial before
-// the sum equals rotating the sum), stores it in its slot, and takes a
-// ticket; the warp that takes the stream's last ticket merges the stream's
-// partials by log-sum-exp and writes the output.  Nobody waits for anybody.
-// Slot of (warp i, stream s) = i + s: warp ranges are contiguous and
-// ordered, so these are distinct and a stream's slots are consecutive.
+// Accumulators: O (tensor-core D fragments: rows = channels, columns =
+// (head, hi/lo)), the running maximum m_used and the partial sums lsum.  The
+// quantized part of a stream accumulates codes weighted by P' = p * scale_v
+// (plus V min through macc) in the rotated domain when V is Hadamard-
+// rotated.  When the warp reaches the stream's fp16 items (or the end of
+// its piece of the stream) that part is folded into a per-warp staging
+// buffer -- rotated back there (the rotation is linear, so rotating each
+// partial before the sum equals rotating the sum) -- and O is reused for
+// the fp16 tokens.  At the end of its piece the warp combines the two,
+// stores one partial result (m, l, O per query head) in its slot and takes
+// a ticket; the warp that takes the stream's last ticket merges the
+// stream's partials by log-sum-exp and writes the output.  Nobody waits for
+// anybody.  Slot of (warp i, stream s) = i + s: warp ranges are contiguous
+// and ordered, so these are distinct and a stream's slots are consecutive.
 #pragma once
 
 #include "kvq_decode_mma.cuh"
@@ -30,29 +36,26 @@ using namespace kvq::mma;
 template <int KB, int VB, int NT, int GT>
 struct PersistLayout {
   static constexpr bool kQuant = KB != 16;
+  static constexpr int kStages = 2;  // per-warp pipeline depth (items)
   static constexpr int kFixed = (int)((sizeof(MmaWarpSmem<NT>) + 127) / 128 * 128);
-  static constexpr int kStageBytes = kQuant ? StageGeom<KB, VB>::BYTES : 0;
-  static constexpr int kPerWarpStages = 2 * kStageBytes;
+  static constexpr int kQBytes = kQuant ? StageGeom<KB, VB>::BYTES : 0;
+  static constexpr int kStageBytes = kQBytes > F16Geom::BYTES ? kQBytes : F16Geom::BYTES;
+  static constexpr int kPerWarpStages = kStages * kStageBytes;
   static constexpr int r128(int x) { return (x + 127) / 128 * 128; }
   static constexpr int kPerWarpO = r128(GT * kHeadDim * 4 + GT * 2 * 4);  // staging O[h][c] + (m, l)
-  static constexpr int kPerWarpP = r128(kGroupTokens * GT * 4);          // fp16 chunk softmax weights
   static constexpr int kPerWarpQ = r128(GT * kHeadDim * 4);              // this warp's stream's query
-  static constexpr int kPerWarp = kPerWarpStages + kPerWarpO + kPerWarpP + kPerWarpQ;
+  static constexpr int kPerWarp = kPerWarpStages + kPerWarpO + kPerWarpQ;
   static constexpr int kBytes = kFixed + 4 * kPerWarp;
 };
 
-// Fold this warp's accumulators for stream s into its slot, take a ticket,
-// and merge the stream if this was the last piece.
+// Fold the quantized accumulators into the staging buffer: sO[h][c] = the
+// (rotated back) sum of codes x P' plus the V-min term, sML[h] = (m, l).
+// O, macc and lsum restart from zero; m_used carries on.
 template <int VB, int NT, int GT>
-__device__ __forceinline__ void finalize_stream(const DecodeParams& p, int slot, int s, int wf, int count,
-                                                float* sO, float* sML, int lane, float (&O)[8][NT][4],
-                                                float (&macc)[NT][kNVG], float (&m_used)[NT], float (&lsum)[NT],
-                                                float (&m_t)[GT], float (&l_t)[GT], float (&acc_t)[GT][4],
-                                                float (&macc_t)[GT]) {
-  const Geometry& G = p.geo;
-  const int g = G.g;
+__device__ __forceinline__ void stage_quant(const DecodeParams& p, float* sO, float* sML, int g, int lane,
+                                            float (&O)[8][NT][4], float (&macc)[NT][kNVG], float (&m_used)[NT],
+                                            float (&lsum)[NT]) {
   const int gq = lane >> 2, tq = lane & 3;
-  // quantized part: reduce over the 8 row groups, stage O[h][c] and (m, l)
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -77,29 +80,81 @@ __device__ __forceinline__ void finalize_stream(const DecodeParams& p, int slot,
     }
   }
   __syncwarp();
-  // per head: rotate the quantized part back, add the fp16 part, store the slot
+  if (p.geo.hadamard) {
+#pragma unroll
+    for (int r = 0; r < GT; ++r) {
+      if (r >= g) break;
+      float* row = &sO[r * kHeadDim + 4 * lane];
+      const float4 a = *reinterpret_cast<const float4*>(row);
+      float v[4] = {a.x, a.y, a.z, a.w};
+      if (sML[2 * r] != -INFINITY) warp_fwht(v, p.hadamard_c, lane);
+      *reinterpret_cast<float4*>(row) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    __syncwarp();
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    lsum[nt] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kNVG; ++j) macc[nt][j] = 0.0f;
+#pragma unroll
+    for (int mc = 0; mc < 8; ++mc)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) O[mc][nt][k] = 0.0f;
+  }
+}
+
+// End of this warp's piece of stream s: combine the staged quantized part
+// (if any) with the fp16 part held in O (plain channel order), store the
+// slot, take a ticket, and merge the stream if this was the last piece.
+template <int NT, int GT>
+__device__ __forceinline__ void finalize_stream(const DecodeParams& p, int slot, int s, int wf, int count, float* sO,
+                                                float* sML, bool staged, int lane, const float (&O)[8][NT][4],
+                                                const float (&m_used)[NT], float (&lsum)[NT]) {
+  const Geometry& G = p.geo;
+  const int g = G.g;
+  const int gq = lane >> 2, tq = lane & 3;
+  float mqv[NT], lqv[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) lsum[nt] += __shfl_xor_sync(0xffffffffu, lsum[nt], o);
+    const int h = 4 * nt + tq;
+    mqv[nt] = (staged && h < g) ? sML[2 * h] : -INFINITY;
+    lqv[nt] = (staged && h < g) ? sML[2 * h + 1] : 0.0f;
+  }
+  __syncwarp();  // every lane has read the staged (m, l) before they are overwritten
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int h = 4 * nt + tq;
+    if (h < g) {
+      const float M = fmaxf(mqv[nt], m_used[nt]);
+      const float eq = (mqv[nt] == -INFINITY) ? 0.0f : exp2f(mqv[nt] - M);
+      const float et = (m_used[nt] == -INFINITY) ? 0.0f : exp2f(m_used[nt] - M);
+#pragma unroll
+      for (int mc = 0; mc < 8; ++mc)
+#pragma unroll
+        for (int rh = 0; rh < 2; ++rh) {
+          float* d = &sO[h * kHeadDim + 16 * mc + 8 * rh + gq];
+          const float t = et * (O[mc][nt][2 * rh] + O[mc][nt][2 * rh + 1]);
+          *d = staged ? fmaf(eq, *d, t) : t;
+        }
+      if (gq == 0) {
+        sML[2 * h] = M;
+        sML[2 * h + 1] = eq * lqv[nt] + et * lsum[nt];
+      }
+    }
+  }
+  __syncwarp();
 #pragma unroll
   for (int r = 0; r < GT; ++r) {
     if (r >= g) break;
-    float vq[4];
     const float4 a = *reinterpret_cast<const float4*>(&sO[r * kHeadDim + 4 * lane]);
-    vq[0] = a.x; vq[1] = a.y; vq[2] = a.z; vq[3] = a.w;
-    const float mq = sML[2 * r], lq = sML[2 * r + 1];
-    if (G.hadamard && mq != -INFINITY) warp_fwht(vq, p.hadamard_c, lane);
-    const float lt = warp_sum(l_t[r]);
-    const float M = fmaxf(mq, m_t[r]);
-    const float eq = (mq == -INFINITY) ? 0.0f : exp2f(mq - M);
-    const float et = (m_t[r] == -INFINITY) ? 0.0f : exp2f(m_t[r] - M);
-    float4 o;
-    o.x = eq * vq[0] + et * (acc_t[r][0] + macc_t[r]);
-    o.y = eq * vq[1] + et * (acc_t[r][1] + macc_t[r]);
-    o.z = eq * vq[2] + et * (acc_t[r][2] + macc_t[r]);
-    o.w = eq * vq[3] + et * (acc_t[r][3] + macc_t[r]);
     const size_t base = (size_t)slot * g + r;
-    *reinterpret_cast<float4*>(&p.part_acc[base * kHeadDim + 4 * lane]) = o;
+    *reinterpret_cast<float4*>(&p.part_acc[base * kHeadDim + 4 * lane]) = a;
     if (lane == 0) {
-      p.part_ml[base * 2] = M;
-      p.part_ml[base * 2 + 1] = eq * lq + et * lt;
+      p.part_ml[base * 2] = sML[2 * r];
+      p.part_ml[base * 2 + 1] = sML[2 * r + 1];
     }
   }
   __syncwarp();
@@ -140,9 +195,10 @@ __device__ __forceinline__ void finalize_stream(const DecodeParams& p, int slot,
 }
 
 template <int KB, int VB, int NT, int GT>
-__global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_persist_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, NT == 1 ? (GT == 1 ? 4 : 3) : 2)
+    decode_persist_kernel(const __grid_constant__ DecodeParams p) {
   using LY = PersistLayout<KB, VB, NT, GT>;
-  constexpr int GQ = 8 * NT;
+  constexpr int KBq = KB == 16 ? 4 : KB, VBq = VB == 16 ? 4 : VB;  // fp16 mode: quantized helpers unused
   extern __shared__ __align__(128) unsigned char smem_raw[];
   MmaWarpSmem<NT>& sm = *reinterpret_cast<MmaWarpSmem<NT>*>(smem_raw);
   const Geometry& G = p.geo;
@@ -150,11 +206,10 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_persist_kern
   const int g = G.g;
   unsigned char* mine = smem_raw + LY::kFixed + w * LY::kPerWarp;
   unsigned char* st0 = mine;
+  const uint32_t st0_s = smem_u32(st0);
   float* sO = reinterpret_cast<float*>(mine + LY::kPerWarpStages);
   float* sML = sO + GT * kHeadDim;
-  float (*pbuf)[GT] = reinterpret_cast<float (*)[GT]>(mine + LY::kPerWarpStages + LY::kPerWarpO);
-  float (*qw)[kHeadDim] =
-      reinterpret_cast<float (*)[kHeadDim]>(mine + LY::kPerWarpStages + LY::kPerWarpO + LY::kPerWarpP);
+  float (*qw)[kHeadDim] = reinterpret_cast<float (*)[kHeadDim]>(mine + LY::kPerWarpStages + LY::kPerWarpO);
 
   {
     uint32_t* z = reinterpret_cast<uint32_t*>(&sm.bq[0][0][0][0]);
@@ -168,16 +223,16 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_persist_kern
   const long long j1 = first_item_at(p, warp_x(p, gw + 1));
   if (j0 >= j1) return;
 
-  int qoff[4];
+  // byte offset of this lane's channel 4*lane+k inside its (hi) Q' fragment row
+  int qh[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     int s_, e_;
-    k_slot_of<(KB == 16 ? 4 : KB)>(4 * (lane & 7) + k, s_, e_);
-    qoff[k] = 4 * s_ + e_;
+    k_slot_of<KBq>(4 * (lane & 7) + k, s_, e_);
+    qh[k] = (2 * (4 * s_ + e_)) ^ (((lane >> 4) & 1) << 4);  // row chunk swizzle: ((row >> 1) & 3) = tsl >> 1
   }
 
   float O[8][NT][4], macc[NT][kNVG], m_used[NT], lsum[NT];
-  float m_t[GT], l_t[GT], acc_t[GT][4], macc_t[GT];
   auto reset = [&]() {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -190,90 +245,99 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2) decode_persist_kern
 #pragma unroll
         for (int k = 0; k < 4; ++k) O[mc][nt][k] = 0.0f;
     }
-#pragma unroll
-    for (int r = 0; r < GT; ++r) {
-      m_t[r] = -INFINITY;
-      l_t[r] = 0.0f;
-      macc_t[r] = 0.0f;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc_t[r][k] = 0.0f;
-    }
   };
   reset();
 
-  // next quantized item at or after j (within this warp's range), else j1
-  auto next_q = [&](long long j) -> long long {
-    if (!LY::kQuant || p.ng == 0) return j1;
-    while (j < j1) {
-      const long long k = j % p.n_items;
-      if (k < p.ng) return j;
-      j += p.n_items - k;  // first item of the next stream
+  const int n_items = p.n_items, ng = LY::kQuant ? p.ng : 0;
+  const int k1 = p.S_eff + p.W;  // fp16 tokens of a stream
+  // current item (s, k) and the next item to queue (is, ik, ij); all advance incrementally
+  int s = (int)(j0 / n_items);
+  int k = (int)(j0 - (long long)s * n_items);
+  int is = s, ik = k;
+  long long ij = j0;
+  auto issue_next = [&](int stage) {
+    if (ij < j1) {
+      const uint32_t dst = st0_s + stage * LY::kStageBytes;
+      if (LY::kQuant && ik < ng) {
+        if constexpr (LY::kQuant) issue_group<KBq, VBq>(p, is, ik, dst, lane);
+      } else {
+        issue_f16(p, is, kF16Tokens * (ik - ng), k1, dst, lane);
+      }
+      ++ij;
+      if (++ik == n_items) {
+        ik = 0;
+        ++is;
+      }
     }
-    return j1;
+    cp_async_commit();
   };
-  auto issue = [&](long long j, int stage) {
-    if constexpr (LY::kQuant) {
-      const int s = (int)(j / p.n_items), grp = (int)(j % p.n_items);
-      issue_group<(KB == 16 ? 4 : KB), (VB == 16 ? 4 : VB)>(p, s, grp, st0 + stage * LY::kStageBytes, lane);
-    }
-  };
-
-  long long qa = next_q(j0);
-  if (qa < j1) issue(qa, 0);
-  cp_async_commit();
-  long long qb = (qa < j1) ? next_q(qa + 1) : j1;
+#pragma unroll
+  for (int i = 0; i < LY::kStages - 1; ++i) issue_next(i);
   int cur = 0;
   int cur_s = -1;
+  bool has_q = false, staged = false, bq_f16 = false;
 
-  auto finish = [&](int s) {
-    const long long first = (long long)s * p.n_items;
+  auto finish = [&](int sf) {
+    if (has_q) stage_quant<VBq, NT, GT>(p, sO, sML, g, lane, O, macc, m_used, lsum);
+    staged = staged || has_q;
+    const long long first = (long long)sf * n_items;
     const int wf = owner_of(p, item_pos(p, first));
-    const int wl = owner_of(p, item_pos(p, first + p.n_items - 1));
-    finalize_stream<(VB == 16 ? 4 : VB), NT, GT>(p, gw + s, s, wf, wl - wf + 1, sO, sML, lane, O, macc, m_used,
-                                                 lsum, m_t, l_t, acc_t, macc_t);
+    const int wl = owner_of(p, item_pos(p, first + n_items - 1));
+    finalize_stream<NT, GT>(p, gw + sf, sf, wf, wl - wf + 1, sO, sML, staged, lane, O, m_used, lsum);
     reset();
+    has_q = staged = bq_f16 = false;
   };
 
   for (long long j = j0; j < j1; ++j) {
-    const int s = (int)(j / p.n_items);
-    const int k = (int)(j % p.n_items);
+    {
+      const int nxt = cur + LY::kStages - 1;
+      issue_next(nxt >= LY::kStages ? nxt - LY::kStages : nxt);
+    }
     if (s != cur_s) {
       if (cur_s >= 0) finish(cur_s);
       cur_s = s;
-      {
-        // this stream's query heads (scaled, fp32) into this warp's buffer
-        const int b = s / G.Hkv, hk = s % G.Hkv;
-        __syncwarp();
-        for (int idx = lane; idx < GT * kHeadDim / 4; idx += 32) {
-          const int r = idx / (kHeadDim / 4), c4 = idx % (kHeadDim / 4);
-          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (r < g) {
-            const uint2 u =
-                __ldg(reinterpret_cast<const uint2*>(p.q + ((size_t)b * G.Hq + hk * g + r) * kHeadDim) + c4);
-            const float2 a = __half22float2(u32_as_h2(u.x)), c2 = __half22float2(u32_as_h2(u.y));
-            v = make_float4(a.x * p.q_scale, a.y * p.q_scale, c2.x * p.q_scale, c2.y * p.q_scale);
-          }
-          *reinterpret_cast<float4*>(&qw[r][4 * c4]) = v;
+      // this stream's query heads (scaled, fp32) into this warp's buffer
+      const int b = s / G.Hkv, hk = s - b * G.Hkv;
+      __syncwarp();
+      for (int idx = lane; idx < GT * kHeadDim / 4; idx += 32) {
+        const int r = idx / (kHeadDim / 4), c4 = idx % (kHeadDim / 4);
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r < g) {
+          const uint2 u =
+              __ldg(reinterpret_cast<const uint2*>(p.q + ((size_t)b * G.Hq + hk * g + r) * kHeadDim) + c4);
+          const float2 a = __half22float2(u32_as_h2(u.x)), c2 = __half22float2(u32_as_h2(u.y));
+          v = make_float4(a.x * p.q_scale, a.y * p.q_scale, c2.x * p.q_scale, c2.y * p.q_scale);
         }
-        __syncwarp();
+        *reinterpret_cast<float4*>(&qw[r][4 * c4]) = v;
       }
+      __syncwarp();
     }
-    if (LY::kQuant && k < p.ng) {
+    cp_async_wait<LY::kStages - 1>();
+    __syncwarp();
+    const unsigned char* stc = st0 + cur * LY::kStageBytes;
+    if (LY::kQuant && k < ng) {
       if constexpr (LY::kQuant) {
-        if (qb < j1) issue(qb, cur ^ 1);
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncwarp();
-        process_group<KB, VB, NT>(p, qw, sm, st0 + cur * LY::kStageBytes, w, lane, qoff, O, macc, m_used, lsum);
-        __syncwarp();
-        cur ^= 1;
-        qa = qb;
-        qb = (qb < j1) ? next_q(qb + 1) : j1;
+        process_group<KB, VB, NT>(qw, sm, stc, g, w, lane, qh, O, macc, m_used, lsum);
+        has_q = true;
       }
     } else {
-      const int c0 = 32 * (k - p.ng);
-      const int k1 = p.S_eff + p.W;
-      fp16_chunk<GT>(p, qw, pbuf, s, c0, k1, lane, m_t, l_t, acc_t, macc_t);
+      if (!bq_f16) {
+        if (has_q) {
+          stage_quant<VBq, NT, GT>(p, sO, sML, g, lane, O, macc, m_used, lsum);
+          has_q = false;
+          staged = true;
+        }
+        build_bq_f16<NT>(qw, sm, g, w, lane);
+        bq_f16 = true;
+        __syncwarp();
+      }
+      process_f16<NT>(sm, stc, g, w, lane, kF16Tokens * (k - ng), k1, O, m_used, lsum);
+    }
+    __syncwarp();
+    cur = (cur + 1 == LY::kStages) ? 0 : cur + 1;
+    if (++k == n_items) {
+      k = 0;
+      ++s;
     }
   }
   cp_async_wait<0>();

@@ -35,11 +35,11 @@ bool persist_eligible(const Geometry& g) {
 cudaError_t plan_persist(DecodeParams& p, uint64_t* ws_need) {
   const Geometry& G = p.geo;
   p.ng = G.fp16_mode ? 0 : p.Nq / kGroupTokens;
-  p.nt = (p.S_eff + p.W + kGroupTokens - 1) / kGroupTokens;
+  p.nt = (p.S_eff + p.W + mma::kF16Tokens - 1) / mma::kF16Tokens;
   p.n_items = p.ng + p.nt;
-  // bytes an item reads: a quantized group (codes, K scales, V scales) or 32 fp16 tokens of K and V
+  // bytes an item reads: a quantized group (codes, K scales, V scales) or an fp16 item's K and V rows
   p.wq = G.fp16_mode ? 1 : (long long)kGroupTokens * (G.krow + G.vrow) + kHeadDim * 4 + kGroupTokens * G.nvg * 4;
-  p.wt = (long long)kGroupTokens * kHeadDim * 2 * 2;
+  p.wt = (long long)mma::kF16Tokens * kHeadDim * 2 * 2;
   p.wstream = (long long)p.ng * p.wq + (long long)p.nt * p.wt;
   p.wtot = (long long)G.NS * p.wstream;
   int dev = 0, sms = 0, occ = 0;

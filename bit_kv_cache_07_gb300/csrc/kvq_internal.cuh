@@ -84,7 +84,7 @@ struct DecodeParams {
   float v_lut_off[8];
   double theta[kHeadDim / 2];  // RoPE frequencies rope_theta^(-2i/d), fp64
   // persistent schedule (tensor-core / fp16 kernels): the streams' work items
-  // -- ng quantized 32-token groups, then nt 32-token chunks of fp16 tokens --
+  // -- ng quantized 32-token groups, then nt fp16 items of a few tokens each --
   // laid end to end, weighted by their bytes, cut into nwarps equal ranges.
   int ng, nt, n_items;
   int nwarps;
