@@ -76,24 +76,29 @@ __device__ __forceinline__ uint32_t lop3_or_and(uint32_t a, uint32_t mask, uint3
 __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
-// Codes to exact fp16 pairs.  The magic exponent 0x6400 makes the fp16 value
-// 1024 + x for an integer x < 1024 placed in the low mantissa bits.
+// V codes to exact fp16 pairs, centred: the value is code - 2^(b-1), so the
+// accumulated sum of codes x P' stays small and the fp32 accumulator loses
+// nothing to cancellation against the V-min term (which takes the centre:
+// min' = min + 2^(b-1) * scale).  The magic exponent 0x6400 makes the fp16
+// value 1024 + x for an integer x < 1024 placed in the low mantissa bits;
+// one half-precision subtract or multiply-add removes the offset and the
+// centre, every step exact.
 //
 // 4-bit: word w holds nibbles 0..7; pair i in 0..3 is (nibble i, nibble i+4).
 __device__ __forceinline__ uint32_t ext4(uint32_t w, int i) {
-  const __half2 k1024 = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
+  const __half2 k1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));  // 1024 + 8
   const __half2 k16th = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));  // 1/16
-  const __half2 km64 = __halves2half2(__ushort_as_half(0xD400), __ushort_as_half(0xD400));   // -64
+  const __half2 km72 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));   // -(64 + 8)
   const uint32_t x = (i >= 2) ? (w >> 8) : w;
-  if ((i & 1) == 0) return h2_as_u32(__hsub2(u32_as_h2(lop3_or_and(x, 0x000F000Fu, 0x64006400u)), k1024));
-  return h2_as_u32(__hfma2(u32_as_h2(lop3_or_and(x, 0x00F000F0u, 0x64006400u)), k16th, km64));
+  if ((i & 1) == 0) return h2_as_u32(__hsub2(u32_as_h2(lop3_or_and(x, 0x000F000Fu, 0x64006400u)), k1032));
+  return h2_as_u32(__hfma2(u32_as_h2(lop3_or_and(x, 0x00F000F0u, 0x64006400u)), k16th, km72));
 }
 
 // 8-bit: word w holds bytes 0..3; pair i in 0..1 is (byte i, byte i+2).
 __device__ __forceinline__ uint32_t ext8(uint32_t w, int i) {
-  const __half2 k1024 = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
+  const __half2 k1152 = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1024 + 128
   const uint32_t sel = (i == 0) ? 0x4240u : 0x4341u;
-  return h2_as_u32(__hsub2(u32_as_h2(__byte_perm(w, 0x64646464u, sel)), k1024));
+  return h2_as_u32(__hsub2(u32_as_h2(__byte_perm(w, 0x64646464u, sel)), k1152));
 }
 
 // 2-bit: word w holds crumbs 0..15; pair i in 0..7 is (crumb i, crumb i+8).
@@ -101,9 +106,9 @@ __device__ __forceinline__ uint32_t ext2(uint32_t w, int i) {
   const uint32_t x = (i >= 4) ? (w >> 8) : w;
   const int m = i & 3;
   const uint32_t v = lop3_or_and(x, 0x00030003u << (2 * m), 0x64006400u);  // 1024 + 4^m c
-  // (1024 + 4^m c) * 4^-m - 1024 * 4^-m = c, every step exact in fp16
+  // (1024 + 4^m c) * 4^-m - (1024 * 4^-m + 2) = c - 2, every step exact in fp16
   const uint16_t sc[4] = {0x3C00, 0x3400, 0x2C00, 0x2400};   // 1, 1/4, 1/16, 1/64
-  const uint16_t of[4] = {0xE400, 0xDC00, 0xD400, 0xCC00};   // -1024, -256, -64, -16
+  const uint16_t of[4] = {0xE402, 0xDC08, 0xD420, 0xCC80};   // -1026, -258, -66, -18
   const __half2 s = __halves2half2(__ushort_as_half(sc[m]), __ushort_as_half(sc[m]));
   const __half2 o = __halves2half2(__ushort_as_half(of[m]), __ushort_as_half(of[m]));
   return h2_as_u32(__hfma2(u32_as_h2(v), s, o));
@@ -261,7 +266,12 @@ __device__ __forceinline__ float split_part(float x, float lo) {
 // n-tiles), online softmax, O += V^T P' (8 m-tiles x NT).
 //  qh[k]: byte offset, inside a 64-byte fragment row, of this lane's
 //         channel 4*lane+k (hi row; the lo row's offset is qh[k] ^ 32)
-template <int KB, int VB, int NT>
+//
+// JC (one n-tile, at most 2 heads): the PV B operand puts the V group into
+// the columns too -- column = (head, V group, hi/lo) -- so a lane builds P'
+// for one (head, group) pair instead of one per group; an m-tile's D
+// columns of the other group are then unused (see stage_quant).
+template <int KB, int VB, int NT, bool JC>
 __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWarpSmem<NT>& sm,
                                               const unsigned char* st, int g, int w, int lane,
                                               const int (&qh)[4], float (&O)[8][NT][4],
@@ -292,7 +302,7 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
         bp = fmaf(qv[k], ms[k].x, bp);
         const __half hi = __float2half_rn(qp);
         const __half lo = __float2half_rn(qp - __half2float(hi));
-        off += __half2float(hi) + __half2float(lo);
+        off += qp;  // hi + lo = qp to ~2^-22
         *reinterpret_cast<__half*>(dhi + qh[k]) = hi;
         *reinterpret_cast<__half*>(dlo + (qh[k] ^ 32)) = lo;
       }
@@ -302,10 +312,11 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
     }
     const uint32_t* vsw = reinterpret_cast<const uint32_t*>(st + SG::VS);
     const int iv = vsc_index(lane), im = vmn_index(lane);
+    constexpr float kVCentre = (float)(1 << (VB - 1));  // the V codes enter the mma centred
 #pragma unroll
     for (int j = 0; j < kNVG; ++j) {
       const float2 m2 = unpack_min_scale(vsw[lane * kNVG + j]);
-      sm.vmn[w][j][im] = m2.x;
+      sm.vmn[w][j][im] = fmaf(kVCentre, m2.y, m2.x);
       sm.vsc[w][j][iv] = m2.y;
     }
   }
@@ -399,16 +410,29 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
     zm = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, 16));
     constexpr float kUnscale = 1.0f / (float)(1 << kq_exp<KB>());
     zm = live ? fmaf(zm, kUnscale, bias) : -INFINITY;
-    if (zm > m_used[nt] + kLazyRescale) {
-      const float alpha = ex2(m_used[nt] - zm);  // 0 when m_used is -inf
-#pragma unroll
-      for (int mc = 0; mc < 8; ++mc)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) O[mc][nt][k] *= alpha;
+    const bool resc = zm > m_used[nt] + kLazyRescale;
+    float alpha = 1.0f;
+    if (resc) {
+      alpha = ex2(m_used[nt] - zm);  // 0 when m_used is -inf
 #pragma unroll
       for (int j = 0; j < kNVG; ++j) macc[nt][j] *= alpha;
       lsum[nt] *= alpha;
       m_used[nt] = zm;
+    }
+    if constexpr (JC) {
+      // this lane's O columns belong to head tq >> 1
+      if (__any_sync(0xffffffffu, resc)) {
+        const float a_o = __shfl_sync(0xffffffffu, alpha, (lane & ~3) | (tq >> 1));
+#pragma unroll
+        for (int mc = 0; mc < 8; ++mc)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) O[mc][nt][k] *= a_o;
+      }
+    } else if (resc) {
+#pragma unroll
+      for (int mc = 0; mc < 8; ++mc)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) O[mc][nt][k] *= alpha;
     }
     const float bm = live ? bias - m_used[nt] : -INFINITY;
     float ps = 0.0f;
@@ -434,8 +458,9 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
 #pragma unroll
   for (int kt = 0; kt < 2; ++kt) {
     // P' fragments per (n-tile, V group): tokens 16kt + {2tq, 2tq+1, 2tq+8, 2tq+9}, column gq
+    // (JC: one fragment; column gq = head gq >> 2, V group (gq >> 1) & 1)
     uint32_t bp[NT][kNVG][2];
-    const int src1 = 8 * tq + (gq >> 1), src2 = src1 + 4;
+    const int src1 = 8 * tq + (JC ? (gq >> 2) : (gq >> 1)), src2 = src1 + 4;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const float v0 = __shfl_sync(0xffffffffu, P[nt][kt][0], src1);
@@ -443,8 +468,9 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
       const float v2 = __shfl_sync(0xffffffffu, P[nt][kt][1], src1);
       const float v3 = __shfl_sync(0xffffffffu, P[nt][kt][1], src2);
 #pragma unroll
-      for (int j = 0; j < kNVG; ++j) {
-        const float4 sv = *reinterpret_cast<const float4*>(&sm.vsc[w][j][16 * kt + 4 * tq]);
+      for (int j = 0; j < (JC ? 1 : kNVG); ++j) {
+        const int jv = JC ? ((gq >> 1) & 1) : j;
+        const float4 sv = *reinterpret_cast<const float4*>(&sm.vsc[w][jv][16 * kt + 4 * tq]);
         bp[nt][j][0] = h2_as_u32(__floats2half2_rn(split_part(v0 * sv.x, lo_sel), split_part(v1 * sv.y, lo_sel)));
         bp[nt][j][1] = h2_as_u32(__floats2half2_rn(split_part(v2 * sv.z, lo_sel), split_part(v3 * sv.w, lo_sel)));
       }
@@ -465,7 +491,7 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
         const int blk = mc >> 1, i = mc & 1;
         const uint32_t a0 = ext4(R[blk][0], i), a1 = ext4(R[blk][0], i + 2);
         const uint32_t a2 = ext4(R[blk][1], i), a3 = ext4(R[blk][1], i + 2);
-        const int j = v_group<VB>(mc);
+        const int j = JC ? 0 : v_group<VB>(mc);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma16816(O[mc][nt], a0, a1, a2, a3, bp[nt][j][0], bp[nt][j][1]);
       }
@@ -481,7 +507,7 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
       for (int mc = 0; mc < 8; ++mc) {
         const uint32_t a0 = ext8(R[mc][0], 0), a1 = ext8(R[mc][0], 1);
         const uint32_t a2 = ext8(R[mc][1], 0), a3 = ext8(R[mc][1], 1);
-        const int j = v_group<VB>(mc);
+        const int j = JC ? 0 : v_group<VB>(mc);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma16816(O[mc][nt], a0, a1, a2, a3, bp[nt][j][0], bp[nt][j][1]);
       }
@@ -497,7 +523,7 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
         const int blk = mc >> 2, i = mc & 3;
         const uint32_t a0 = ext2(R[blk][0], i), a1 = ext2(R[blk][0], i + 4);
         const uint32_t a2 = ext2(R[blk][1], i), a3 = ext2(R[blk][1], i + 4);
-        const int j = v_group<VB>(mc);
+        const int j = JC ? 0 : v_group<VB>(mc);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma16816(O[mc][nt], a0, a1, a2, a3, bp[nt][j][0], bp[nt][j][1]);
       }

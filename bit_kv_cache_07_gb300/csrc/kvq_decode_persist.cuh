@@ -51,7 +51,7 @@ struct PersistLayout {
 // Fold the quantized accumulators into the staging buffer: sO[h][c] = the
 // (rotated back) sum of codes x P' plus the V-min term, sML[h] = (m, l).
 // O, macc and lsum restart from zero; m_used carries on.
-template <int VB, int NT, int GT>
+template <int VB, int NT, int GT, bool JC>
 __device__ __forceinline__ void stage_quant(const DecodeParams& p, float* sO, float* sML, int g, int lane,
                                             float (&O)[8][NT][4], float (&macc)[NT][kNVG], float (&m_used)[NT],
                                             float (&lsum)[NT]) {
@@ -65,7 +65,26 @@ __device__ __forceinline__ void stage_quant(const DecodeParams& p, float* sO, fl
       for (int j = 0; j < kNVG; ++j) macc[nt][j] += __shfl_xor_sync(0xffffffffu, macc[nt][j], o);
     }
     const int h = 4 * nt + tq;
-    if (h < g) {
+    if constexpr (JC) {
+      // D columns of this lane: head tq >> 1, V group tq & 1; macc of that head from its lane
+      const int hc = tq >> 1, jj = tq & 1;
+      const float m0 = __shfl_sync(0xffffffffu, macc[0][0], (lane & ~3) | hc);
+      const float m1 = __shfl_sync(0xffffffffu, macc[0][1], (lane & ~3) | hc);
+      const float mj = jj ? m1 : m0;
+      if (hc < g) {
+#pragma unroll
+        for (int mc = 0; mc < 8; ++mc) {
+          if (v_group<VB>(mc) != jj) continue;
+#pragma unroll
+          for (int rh = 0; rh < 2; ++rh)
+            sO[hc * kHeadDim + v_chan<VB>(mc, gq, rh)] = O[mc][0][2 * rh] + O[mc][0][2 * rh + 1] + mj;
+        }
+      }
+      if (h < g && gq == 0) {
+        sML[2 * h] = m_used[nt];
+        sML[2 * h + 1] = lsum[nt];
+      }
+    } else if (h < g) {
 #pragma unroll
       for (int mc = 0; mc < 8; ++mc) {
         const float mt = macc[nt][v_group<VB>(mc)];
@@ -199,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (GT == 1 ? 4 : 3) : 2)
     decode_persist_kernel(const __grid_constant__ DecodeParams p) {
   using LY = PersistLayout<KB, VB, NT, GT>;
   constexpr int KBq = KB == 16 ? 4 : KB, VBq = VB == 16 ? 4 : VB;  // fp16 mode: quantized helpers unused
+  constexpr bool JC = NT == 1 && GT <= 2;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   MmaWarpSmem<NT>& sm = *reinterpret_cast<MmaWarpSmem<NT>*>(smem_raw);
   const Geometry& G = p.geo;
@@ -278,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (GT == 1 ? 4 : 3) : 2)
   bool has_q = false, staged = false, bq_f16 = false;
 
   auto finish = [&](int sf) {
-    if (has_q) stage_quant<VBq, NT, GT>(p, sO, sML, g, lane, O, macc, m_used, lsum);
+    if (has_q) stage_quant<VBq, NT, GT, JC>(p, sO, sML, g, lane, O, macc, m_used, lsum);
     staged = staged || has_q;
     const long long first = (long long)sf * n_items;
     const int wf = owner_of(p, item_pos(p, first));
@@ -317,13 +337,13 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (GT == 1 ? 4 : 3) : 2)
     const unsigned char* stc = st0 + cur * LY::kStageBytes;
     if (LY::kQuant && k < ng) {
       if constexpr (LY::kQuant) {
-        process_group<KB, VB, NT>(qw, sm, stc, g, w, lane, qh, O, macc, m_used, lsum);
+        process_group<KB, VB, NT, JC>(qw, sm, stc, g, w, lane, qh, O, macc, m_used, lsum);
         has_q = true;
       }
     } else {
       if (!bq_f16) {
         if (has_q) {
-          stage_quant<VBq, NT, GT>(p, sO, sML, g, lane, O, macc, m_used, lsum);
+          stage_quant<VBq, NT, GT, JC>(p, sO, sML, g, lane, O, macc, m_used, lsum);
           has_q = false;
           staged = true;
         }

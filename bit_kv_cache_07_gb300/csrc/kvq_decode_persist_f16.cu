@@ -60,6 +60,12 @@ cudaError_t plan_persist(DecodeParams& p, uint64_t* ws_need) {
   if (nw > p.wtot / wmax) nw = p.wtot / wmax;
   if (nw < 1) nw = 1;
   p.nwarps = (int)nw;
+  p.inv_n_items = 1.0 / (double)p.n_items;
+  p.inv_wq = 1.0 / (double)p.wq;
+  p.inv_wt = 1.0 / (double)p.wt;
+  p.inv_wstream = 1.0 / (double)p.wstream;
+  p.inv_wtot = 1.0 / (double)p.wtot;
+  p.inv_nwarps = 1.0 / (double)p.nwarps;
   const uint64_t slots = (uint64_t)p.nwarps + G.NS;
   const uint64_t cnt = ((uint64_t)G.NS * 4 + 255) / 256 * 256;
   const uint64_t ml = (slots * G.g * 2 * 4 + 255) / 256 * 256;

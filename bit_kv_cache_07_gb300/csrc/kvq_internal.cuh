@@ -89,28 +89,50 @@ struct DecodeParams {
   int ng, nt, n_items;
   int nwarps;
   long long wq, wt, wstream, wtot;
+  double inv_n_items, inv_wq, inv_wt, inv_wstream, inv_wtot, inv_nwarps;  // 1 / x, for idiv
 };
 
+// floor(x / d) for 0 <= x < 2^52 and d >= 1, given inv = 1.0 / d in fp64.
+// On the device one fp64 multiply and one correction step replace the long,
+// serial emulation of a 64-bit integer division (the estimate is off by at
+// most one); the host divides exactly.
+__host__ __device__ inline long long idiv_recip(long long x, long long d, double inv) {
+  long long q = (long long)((double)x * inv);
+  const long long r = x - q * d;
+  if (r < 0) --q;
+  else if (r >= d) ++q;
+  return q;
+}
+__host__ __device__ inline long long idiv(long long x, long long d, double inv) {
+#ifdef __CUDA_ARCH__
+  return idiv_recip(x, d, inv);
+#else
+  (void)inv;
+  return x / d;
+#endif
+}
+
 // Persistent-schedule arithmetic shared by host and device.
+// (Operands stay below 2^52: wtot is at most the layer's bytes, nwarps a few thousand.)
 __host__ __device__ inline long long item_pos(const DecodeParams& p, long long j) {
-  const long long s = j / p.n_items, k = j % p.n_items;
+  const long long s = idiv(j, p.n_items, p.inv_n_items), k = j - s * p.n_items;
   return s * p.wstream + (k <= p.ng ? k * p.wq : p.ng * p.wq + (k - p.ng) * p.wt);
 }
 // First item whose start weight is >= x (x in [0, wtot]).
 __host__ __device__ inline long long first_item_at(const DecodeParams& p, long long x) {
-  long long s = x / p.wstream, rem = x - s * p.wstream, k;
+  long long s = idiv(x, p.wstream, p.inv_wstream), rem = x - s * p.wstream, k;
   if (rem == 0) return s * p.n_items;
-  if (rem <= p.ng * p.wq) k = (rem + p.wq - 1) / p.wq;
-  else k = p.ng + (rem - p.ng * p.wq + p.wt - 1) / p.wt;
+  if (rem <= p.ng * p.wq) k = idiv(rem + p.wq - 1, p.wq, p.inv_wq);
+  else k = p.ng + idiv(rem - p.ng * p.wq + p.wt - 1, p.wt, p.inv_wt);
   if (k >= p.n_items) return (s + 1) * p.n_items;
   return s * p.n_items + k;
 }
 // Warp i covers weight [x_i, x_{i+1}), x_i = floor(i * wtot / nwarps).
 __host__ __device__ inline long long warp_x(const DecodeParams& p, long long i) {
-  return i * p.wtot / p.nwarps;
+  return idiv(i * p.wtot, p.nwarps, p.inv_nwarps);
 }
 __host__ __device__ inline int owner_of(const DecodeParams& p, long long pos) {
-  return (int)(((pos + 1) * p.nwarps + p.wtot - 1) / p.wtot - 1);
+  return (int)(idiv((pos + 1) * p.nwarps + p.wtot - 1, p.wtot, p.inv_wtot) - 1);
 }
 
 // ------------------------------------------------------------ host hooks

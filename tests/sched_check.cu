@@ -1,7 +1,9 @@
 // Host-side check of the persistent decode's work schedule: every item has
 // exactly one owner warp, no warp range is empty under the launch cap, the
 // owner formula agrees with the ranges, and the (warp, stream) slots are
-// distinct and in bounds.  Built and run by test_schedule_host.py.
+// distinct and in bounds.  Also checks the device's reciprocal division
+// (idiv_recip) against exact integer division.  Built and run by
+// test_schedule_host.py.
 #include "../bit_kv_cache_07_gb300/csrc/kvq_internal.cuh"
 #include <cstdio>
 #include <set>
@@ -9,9 +11,9 @@
 using namespace kvq;
 int main() {
   int bad = 0, cases = 0;
-  for (int NS : {1, 2, 7, 32, 256}) for (int ng : {0, 1, 3, 31, 125}) for (int nt : {0, 1, 3}) for (long long wq : {3328LL, 5376LL, 9984LL}) {
+  for (int NS : {1, 2, 7, 32, 256}) for (int ng : {0, 1, 3, 31, 125}) for (int nt : {0, 1, 3, 12}) for (long long wq : {3328LL, 5376LL, 9984LL}) for (long long wt : {4096LL, 16384LL}) {
     if (ng + nt == 0) continue;
-    DecodeParams p{}; p.ng = ng; p.nt = nt; p.n_items = ng + nt; p.wq = wq; p.wt = 16384;
+    DecodeParams p{}; p.ng = ng; p.nt = nt; p.n_items = ng + nt; p.wq = wq; p.wt = wt;
     p.wstream = ng * wq + nt * p.wt; p.wtot = NS * p.wstream;
     long long items = (long long)NS * p.n_items;
     for (long long nw0 : {1LL, 5LL, 37LL, 1824LL}) {
@@ -36,6 +38,20 @@ int main() {
         if ((int)ws.size() != wl - wf + 1) { printf("count mismatch s=%d\n", s); ++bad; }
         for (int w : ws) { if (!slots.insert(w + s).second) { printf("slot clash\n"); ++bad; } if (w + s >= nw + NS) ++bad; }
       }
+    }
+  }
+  // reciprocal division: exact for 0 <= x < 2^52
+  unsigned long long st = 88172645463325252ull;
+  auto rnd = [&]() { st ^= st << 13; st ^= st >> 7; st ^= st << 17; return st; };
+  for (int i = 0; i < 2000000; ++i) {
+    const long long d = (long long)(rnd() % ((i & 1) ? 5000ull : (1ull << 40))) + 1;
+    long long x = (long long)(rnd() % (1ull << 52));
+    if (i % 3 == 0) x = (x / d) * d;                      // exact multiples
+    if (i % 3 == 1 && (x / d) * d > 0) x = (x / d) * d - 1;  // just below one
+    ++cases;
+    if (idiv_recip(x, d, 1.0 / (double)d) != x / d) {
+      if (bad < 10) printf("idiv_recip(%lld, %lld) wrong\n", x, d);
+      ++bad;
     }
   }
   printf("cases %d bad %d\n", cases, bad);
