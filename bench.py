@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: build just the first N layers (the bench line needs all)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="profiling only: a shorter context than the workload's")
     return ap.parse_args()
 
 
@@ -163,16 +165,16 @@ class Model:
     """All layers of one workload: caches filled to T-1 tokens, plus the
     per-layer inputs of one decode step."""
 
-    def __init__(self, name: str, device, fp16: bool, layers: int = 0):
+    def __init__(self, name: str, device, fp16: bool, layers: int = 0, tokens: int = 0):
         import torch
         from bit_kv_cache_07_gb300 import binding, synth, workloads
         w = workloads.WORKLOADS[name]
-        self.name, self.T = name, w["tokens"]
+        self.name, self.T = name, (tokens if tokens > 0 else w["tokens"])
         self.L = layers if layers > 0 else w["layers"]
         self.cfgs, self.layers = [], []
         self.q, self.k_new, self.v_new, self.out = [], [], [], []
         for l in range(self.L):
-            cfg = workloads.layer_config(name, l)
+            cfg = workloads.layer_config(name, l, tokens=self.T)
             if cfg["k_bits"] == 3:
                 cfg["k_lut"] = synth.nuq_lut(name, l, "k")
                 cfg["v_lut"] = synth.nuq_lut(name, l, "v")
@@ -237,6 +239,38 @@ def time_steps(model, stream, steps: int, warmup: int, per_kernel=True):
     if per_kernel:
         kern = [evs[i][l][0].elapsed_time(evs[i][l][1]) for i in range(steps) for l in range(model.L)]
     return total_ms, kern
+
+
+def time_graph(model, stream, steps: int, warmup: int):
+    """One step (every layer's append + decode) captured once in a CUDA graph
+    and replayed: the per-step time without host launch gaps.  Returns
+    (ms per step, None) or (None, why) if the capture is not possible."""
+    import torch
+    try:
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            model.step(stream)
+        torch.cuda.synchronize()
+    except Exception as e:  # pragma: no cover - reported in the JSON line
+        return None, f"graph capture failed: {type(e).__name__}: {e}"
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms = t0.elapsed_time(t1) / steps
+    del g
+    return ms, None
 
 
 def time_e2e(model, stream, steps: int, warmup: int):
@@ -404,12 +438,14 @@ def main():
     stream = torch.cuda.Stream(device=dev)
     w = workloads.WORKLOADS[args.workload]
 
-    model = Model(args.workload, dev, fp16=False, layers=args.layers)
+    model = Model(args.workload, dev, fp16=False, layers=args.layers, tokens=args.tokens)
     clocks = ClockSampler(local)
     clocks.start()
     total_ms, kern = time_steps(model, stream, args.steps, args.warmup)
+    g_ms, g_err = time_graph(model, stream, args.steps, args.warmup)
     clk = clocks.stop()
-    ms_step = max_over_ranks(total_ms / args.steps)
+    eager_ms = max_over_ranks(total_ms / args.steps)
+    ms_step = max_over_ranks(g_ms) if g_ms is not None else eager_ms
     dec_bytes = model.decode_bytes()
     kern_ms = statistics.mean(kern)
     peak, peak_kind = measured_peaks()
@@ -417,15 +453,17 @@ def main():
     e2e_ms, h2d, d2h = time_e2e(model, stream, max(3, args.steps // 2), 2)
     e2e_ms = max_over_ranks(e2e_ms)
     launches = model.launches_per_step() * args.steps
-    model_layers = model.L
+    model_layers, model_T = model.L, model.T
     del model
     torch.cuda.empty_cache()
 
     fp16 = None
     if not args.no_fp16_baseline:
-        fmodel = Model(args.workload, dev, fp16=True, layers=args.layers)
+        fmodel = Model(args.workload, dev, fp16=True, layers=args.layers, tokens=args.tokens)
         f_ms, f_kern = time_steps(fmodel, stream, args.steps, args.warmup)
-        f_ms = max_over_ranks(f_ms / args.steps)
+        f_ms = f_ms / args.steps
+        fg_ms, _ = time_graph(fmodel, stream, args.steps, args.warmup)
+        f_ms = max_over_ranks(fg_ms if fg_ms is not None else f_ms)
         f_bytes = fmodel.decode_bytes()
         fp16 = {"us_per_step": f_ms * 1e3, "cache_gbs": f_bytes / (f_ms * 1e-3) / 1e9,
                 "decode_kernel_us": statistics.mean(f_kern) * 1e3,
@@ -442,15 +480,18 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f16xf16->f32 (tensor cores) on u8-packed codes", "data": "synthetic",
         "config": {"workload": args.workload, "layers": model_layers, "batch": w["batch"],
                    "q_heads": w["n_q_heads"], "kv_heads": w["n_kv_heads"], "head_dim": w["head_dim"],
-                   "context": w["tokens"], "cache": w["pairs"], "n_sink": w["n_sink"], "n_recent": w["n_recent"],
+                   "context": model_T, "cache": w["pairs"], "n_sink": w["n_sink"], "n_recent": w["n_recent"],
                    "l2": "inputs larger than L2: %.2f GB of cache read per step" % (dec_bytes / 1e9),
-                   "step": "per layer: kvq_append of 1 token + kvq_decode_attn"},
+                   "step": "per layer: kvq_append of 1 token + kvq_decode_attn",
+                   "timing": ("one step captured in a CUDA graph, replayed" if g_ms is not None else
+                              "eager launches (" + str(g_err) + ")")},
+        "ms_per_step_eager": eager_ms,
         "cache_gbs": sum_over_ranks(dec_bytes / (ms_step * 1e-3) / 1e9),
         "cache_bytes_per_step": dec_bytes,
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved, "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": "decode_persist_kernel", "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": ncu_traffic(f"decode:{args.workload}"),
                      "bytes_per_launch": dec_bytes / model_layers,

@@ -248,7 +248,7 @@ __device__ __forceinline__ void k_logits_rope(const DecodeParams& p, DecodeSmem<
       a = fmaf(small_uint_to_float(ca), sm.work[w][1][j], sm.work[w][0][j]);
       b = fmaf(small_uint_to_float(cb), sm.work[w][1][j + kHeadDim / 2], sm.work[w][0][j + kHeadDim / 2]);
     }
-    const float2 e = cmul(sm.anchor[w][j], rope_e[lane * (kHeadDim / 2) + j]);
+    const float2 e = cmul(sm.anchor[w][j], rope_e[j * kGroupTokens + lane]);
     const float ra = a * e.x - b * e.y;
     const float rb = b * e.x + a * e.y;
 #pragma unroll
@@ -263,7 +263,7 @@ __device__ __forceinline__ void k_logits_rope(const DecodeParams& p, DecodeSmem<
       const int col = __ldg(p.L.k_col + base + j);
       const float dv = half_bits_to_float(__ldg(p.L.k_val + base + j)) - nmin;
       const int f = col & (kHeadDim / 2 - 1);
-      const float2 e = cmul(sm.anchor[w][f], rope_e[lane * (kHeadDim / 2) + f]);
+      const float2 e = cmul(sm.anchor[w][f], rope_e[f * kGroupTokens + lane]);
       // rotated unit vector of channel col, times dv, dotted with q
 #pragma unroll
       for (int r = 0; r < GQ; ++r) {
@@ -522,8 +522,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   }
   const bool quant_split = sp < p.n_qsplit;
   if (G.pre_rope && quant_split) {
+    // e^{i l theta_j} at [j][l]: a warp reads one j for its 32 token offsets l,
+    // 32 consecutive entries (no bank conflicts)
     for (int idx = tid; idx < kGroupTokens * (kHeadDim / 2); idx += kThreads) {
-      const int l = idx / (kHeadDim / 2), j = idx % (kHeadDim / 2);
+      const int j = idx / kGroupTokens, l = idx % kGroupTokens;
       rope_e[idx] = expi((double)l * p.theta[j]);
     }
   }
