@@ -65,9 +65,9 @@ def window_counts(cfg: dict, T: int):
 
 
 def algorithmic_bytes(cfg: dict, T: int) -> int:
-    """Bytes one decode launch must move: packed codes, scales, CSR outliers
-    and fp16 sink/window tokens of every stream (each read once per KV head),
-    plus q in and out."""
+    """Bytes one decode launch must move: packed codes, scales, CSR outlier
+    entries and fp16 sink/window tokens of every stream (each read once per
+    KV head), plus q in and out."""
     S, Nq, W = window_counts(cfg, T)
     d = cfg["head_dim"]
     NS = cfg["batch"] * cfg["n_kv_heads"]
@@ -76,8 +76,11 @@ def algorithmic_bytes(cfg: dict, T: int) -> int:
     if kb != 16:
         per += Nq * (d * kb // 8 + d * vb // 8)
         if kb == 3:
+            # per-token {min, s} for K and V, and k CSR entries (1-byte column + fp16 value)
+            # per token vector; every row holds exactly k entries, so the decode does not
+            # need the row pointers
             k = cfg["outliers_per_vector"]
-            per += Nq * 4 * 2 + 2 * ((Nq + 1) * 4 + Nq * k * 3)
+            per += Nq * 4 * 2 + 2 * (Nq * k * 3)
         else:
             per += (Nq // 32) * d * 4 + Nq * (d // cfg["v_group_channels"]) * 4
     per += (S + W) * d * 2 * 2

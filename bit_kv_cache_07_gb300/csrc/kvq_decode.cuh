@@ -50,6 +50,24 @@ struct DecodeSmem {
   int is_last;
 };
 
+// RoPE offset table e^{i l theta_j} (or the query-folded W_{j,l}), l = token
+// offset in a 32-token group: entries of pairs 2i and 2i+1 for one l are
+// adjacent (a lane reads both with one 16-byte load), lanes l consecutive.
+__host__ __device__ __forceinline__ int rope_tab_index(int j, int l) { return (((j >> 1) * 32 + l) << 1) | (j & 1); }
+
+// 16-byte asynchronous global -> shared copies (cp.async, completion by group)
+__device__ __forceinline__ void cp_async16(uint32_t smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem), "l"(gmem));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
 __device__ __forceinline__ float2 cmul(float2 a, float2 b) {
   return make_float2(a.x * b.x - a.y * b.y, a.y * b.x + a.x * b.y);
 }
@@ -57,7 +75,8 @@ __device__ __forceinline__ float2 cmul(float2 a, float2 b) {
 // e^{i x} for an fp64 angle: reduce modulo 2 pi in fp64, then fp32 sincos.
 __device__ __forceinline__ float2 expi(double x) {
   const double two_pi = 6.283185307179586476925286766559;
-  const double r = x - two_pi * rint(x / two_pi);
+  const double inv_two_pi = 0.15915494309189533576888376337251;  // n only needs to be the nearest integer or next to it
+  const double r = x - two_pi * rint(x * inv_two_pi);
   float sn, cs;
   sincosf((float)r, &sn, &cs);
   return make_float2(cs, sn);
@@ -149,53 +168,6 @@ __device__ __forceinline__ void k_logits_uniform(const DecodeParams& p, DecodeSm
   }
 }
 
-// Non-uniform per-token K, no RoPE: z = min * sum(q) + s * sum_c q_c L'_code
-// plus the outlier corrections q_col * (val - min).
-template <int GQ>
-__device__ __forceinline__ void k_logits_nuq(const DecodeParams& p, DecodeSmem<GQ>& sm, int s,
-                                             int grp, int lane, float (&z)[GQ]) {
-  const Geometry& G = p.geo;
-  const size_t i = (size_t)grp * kGroupTokens + lane;
-  const float2 ms = unpack_min_scale(__ldg(p.L.k_scales + (size_t)s * G.qcap + i));
-  const uint4* row = reinterpret_cast<const uint4*>(p.L.k_codes + ((size_t)s * G.qcap + i) * 48);
-  uint32_t wd[13];
-#pragma unroll
-  for (int k = 0; k < 3; ++k) {
-    const uint4 u = __ldg(row + k);
-    wd[4 * k] = u.x; wd[4 * k + 1] = u.y; wd[4 * k + 2] = u.z; wd[4 * k + 3] = u.w;
-  }
-  wd[12] = 0;
-  float zl[GQ];
-#pragma unroll
-  for (int r = 0; r < GQ; ++r) zl[r] = 0.0f;
-#pragma unroll
-  for (int c = 0; c < kHeadDim; c += 4) {
-    float x[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) x[k] = sm.lut_k[code_at<3>(wd, c + k)];
-#pragma unroll
-    for (int r = 0; r < GQ; ++r) {
-      const float4 qv = *reinterpret_cast<const float4*>(&sm.q[r][c]);
-      zl[r] = fmaf(qv.x, x[0], zl[r]);
-      zl[r] = fmaf(qv.y, x[1], zl[r]);
-      zl[r] = fmaf(qv.z, x[2], zl[r]);
-      zl[r] = fmaf(qv.w, x[3], zl[r]);
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < GQ; ++r) z[r] = fmaf(ms.x, sm.qsum[r], ms.y * zl[r]);
-  const int32_t* rp = p.L.k_rowptr + (size_t)s * (G.qcap + 1);
-  const int jcap = G.qcap * G.nout;  // outlier entries of a stream
-  const int j0 = max(0, __ldg(rp + i)), j1 = min(jcap, __ldg(rp + i + 1));
-  const size_t base = (size_t)s * jcap;
-  for (int j = j0; j < j1; ++j) {
-    const int col = __ldg(p.L.k_col + base + j);
-    const float dv = half_bits_to_float(__ldg(p.L.k_val + base + j)) - ms.x;
-#pragma unroll
-    for (int r = 0; r < GQ; ++r) z[r] = fmaf(sm.q[r][col], dv, z[r]);
-  }
-}
-
 // Any quantized K with RoPE after dequantization: reconstruct k^ for each
 // channel pair (j, j + 64), rotate by the angle of this lane's position
 // (anchor of the group times e^{i lane theta_j}), dot with q.
@@ -248,7 +220,7 @@ __device__ __forceinline__ void k_logits_rope(const DecodeParams& p, DecodeSmem<
       a = fmaf(small_uint_to_float(ca), sm.work[w][1][j], sm.work[w][0][j]);
       b = fmaf(small_uint_to_float(cb), sm.work[w][1][j + kHeadDim / 2], sm.work[w][0][j + kHeadDim / 2]);
     }
-    const float2 e = cmul(sm.anchor[w][j], rope_e[j * kGroupTokens + lane]);
+    const float2 e = cmul(sm.anchor[w][j], rope_e[rope_tab_index(j, lane)]);
     const float ra = a * e.x - b * e.y;
     const float rb = b * e.x + a * e.y;
 #pragma unroll
@@ -263,7 +235,7 @@ __device__ __forceinline__ void k_logits_rope(const DecodeParams& p, DecodeSmem<
       const int col = __ldg(p.L.k_col + base + j);
       const float dv = half_bits_to_float(__ldg(p.L.k_val + base + j)) - nmin;
       const int f = col & (kHeadDim / 2 - 1);
-      const float2 e = cmul(sm.anchor[w][f], rope_e[f * kGroupTokens + lane]);
+      const float2 e = cmul(sm.anchor[w][f], rope_e[rope_tab_index(f, lane)]);
       // rotated unit vector of channel col, times dv, dotted with q
 #pragma unroll
       for (int r = 0; r < GQ; ++r) {
@@ -500,6 +472,214 @@ __device__ __forceinline__ void warp_fwht(float (&v)[4], float c, int lane) {
   for (int q = 0; q < 4; ++q) v[q] *= c;
 }
 
+// ------------------------------------------------------ staged NUQ groups
+// For the non-uniform (3-bit) cache every warp double-buffers its groups in
+// shared memory with cp.async: while it computes group i, group i + 4 (its
+// next one) streams in.  A stage holds one 32-token group of one stream:
+// K and V code rows (48 bytes each), the per-token {min, s} words, and the
+// group's CSR outlier entries -- exactly k per row (the append writes k
+// entries for every row), so a group's entries are the k*32 consecutive
+// ones starting at row * k and the row pointers are not needed here.
+struct NuqStage {
+  static constexpr int KC = 0, VC = kGroupTokens * 48, KMS = 2 * kGroupTokens * 48;
+  static constexpr int VMS = KMS + kGroupTokens * 4, CSR = VMS + kGroupTokens * 4;
+  static __host__ __device__ constexpr int kcol(int k) { return CSR; }
+  static __host__ __device__ constexpr int kval(int k) { return CSR + 32 * k; }
+  static __host__ __device__ constexpr int vcol(int k) { return CSR + 96 * k; }
+  static __host__ __device__ constexpr int vval(int k) { return CSR + 128 * k; }
+  static __host__ __device__ constexpr int bytes(int k) { return (CSR + 192 * k + 127) / 128 * 128; }
+};
+
+__device__ __forceinline__ void issue_nuq(const DecodeParams& p, int s, int grp, uint32_t dst, int lane) {
+  const Geometry& G = p.geo;
+  const int k = G.nout;
+  const size_t i0 = (size_t)s * G.qcap + (size_t)grp * kGroupTokens;  // first row of the group
+  const uint8_t* kc = p.L.k_codes + i0 * 48;
+  const uint8_t* vc = p.L.v_codes + i0 * 48;
+  for (int c = lane; c < kGroupTokens * 48 / 16; c += 32) {
+    cp_async16(dst + NuqStage::KC + 16 * c, kc + 16 * c);
+    cp_async16(dst + NuqStage::VC + 16 * c, vc + 16 * c);
+  }
+  if (lane < 8) {
+    cp_async16(dst + NuqStage::KMS + 16 * lane, p.L.k_scales + i0 + 4 * lane);
+    cp_async16(dst + NuqStage::VMS + 16 * lane, p.L.v_scales + i0 + 4 * lane);
+  }
+  // CSR: 32k column bytes and 64k value bytes per side (multiples of 16)
+  for (int c = lane; c < 2 * k; c += 32) {
+    cp_async16(dst + NuqStage::kcol(k) + 16 * c, p.L.k_col + i0 * k + 16 * c);
+    cp_async16(dst + NuqStage::vcol(k) + 16 * c, p.L.v_col + i0 * k + 16 * c);
+  }
+  for (int c = lane; c < 4 * k; c += 32) {
+    cp_async16(dst + NuqStage::kval(k) + 16 * c, reinterpret_cast<const uint8_t*>(p.L.k_val + i0 * k) + 16 * c);
+    cp_async16(dst + NuqStage::vval(k) + 16 * c, reinterpret_cast<const uint8_t*>(p.L.v_val + i0 * k) + 16 * c);
+  }
+}
+
+// 3-bit code c of a 48-byte row held in 12 (+1 zero) registers.
+__device__ __forceinline__ uint32_t code3(const uint32_t (&w)[13], int c) { return code_at<3>(w, c); }
+
+// K logits of one staged NUQ group, lane = token.
+//  no RoPE:    z = min * sum(q) + s * sum_c q_c L'_code, plus outlier terms
+//  RoPE, GQ=1: z = sum_j Re[W_{j,lane} * A_j * (k_j + i k_{j+64})], with
+//              W_{j,d} = conj(q_j + i q_{j+64}) e^{i theta_j d} (table, per
+//              CTA) and A_j = e^{i theta_j t0} (group anchor): two complex
+//              products per channel pair instead of rotating q or k
+//  RoPE, GQ>1: rotate each key pair once by A_j e^{i theta_j lane}, dot with
+//              every head
+template <int GQ>
+__device__ __forceinline__ void k_logits_nuq_st(const DecodeParams& p, DecodeSmem<GQ>& sm,
+                                                const float2* __restrict__ tab, const unsigned char* st,
+                                                int grp, int lane, int w, float (&z)[GQ]) {
+  const Geometry& G = p.geo;
+  const int k = G.nout;
+  uint32_t wd[13];
+  {
+    const uint4* row = reinterpret_cast<const uint4*>(st + NuqStage::KC + 48 * lane);
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const uint4 u = row[i];
+      wd[4 * i] = u.x; wd[4 * i + 1] = u.y; wd[4 * i + 2] = u.z; wd[4 * i + 3] = u.w;
+    }
+    wd[12] = 0;
+  }
+  const float2 ms = unpack_min_scale(reinterpret_cast<const uint32_t*>(st + NuqStage::KMS)[lane]);
+  const uint8_t* ocol = st + NuqStage::kcol(k) + k * lane;
+  const uint16_t* oval = reinterpret_cast<const uint16_t*>(st + NuqStage::kval(k)) + k * lane;
+#pragma unroll
+  for (int r = 0; r < GQ; ++r) z[r] = 0.0f;
+  if (!G.pre_rope) {
+    float zl[GQ];
+#pragma unroll
+    for (int r = 0; r < GQ; ++r) zl[r] = 0.0f;
+#pragma unroll
+    for (int c = 0; c < kHeadDim; c += 4) {
+      float x[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[e] = sm.lut_k[code3(wd, c + e)];
+#pragma unroll
+      for (int r = 0; r < GQ; ++r) {
+        const float4 qv = *reinterpret_cast<const float4*>(&sm.q[r][c]);
+        zl[r] = fmaf(qv.x, x[0], fmaf(qv.y, x[1], fmaf(qv.z, x[2], fmaf(qv.w, x[3], zl[r]))));
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < GQ; ++r) z[r] = fmaf(ms.x, sm.qsum[r], ms.y * zl[r]);
+    for (int e = 0; e < k; ++e) {
+      const int col = ocol[e];
+      const float dv = half_bits_to_float(oval[e]) - ms.x;
+#pragma unroll
+      for (int r = 0; r < GQ; ++r) z[r] = fmaf(sm.q[r][col], dv, z[r]);
+    }
+    return;
+  }
+  // group anchor e^{i t0 theta_j}
+  const int pos0 = G.S + grp * kGroupTokens;
+  for (int j = lane; j < kHeadDim / 2; j += 32) sm.anchor[w][j] = expi((double)pos0 * p.theta[j]);
+  __syncwarp();
+  if constexpr (GQ == 1) {
+    float zr = 0.0f;
+    const float4* tab4 = reinterpret_cast<const float4*>(tab);
+    const float4* anc4 = reinterpret_cast<const float4*>(&sm.anchor[w][0]);
+#pragma unroll
+    for (int j = 0; j < kHeadDim / 2; j += 2) {
+      const float4 A2 = anc4[j >> 1];                        // A_j, A_{j+1}
+      const float4 W2 = tab4[(j >> 1) * kGroupTokens + lane];  // W_{j,lane}, W_{j+1,lane}
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float a = fmaf(ms.y, sm.lut_k[code3(wd, j + h)], ms.x);
+        const float b = fmaf(ms.y, sm.lut_k[code3(wd, j + h + kHeadDim / 2)], ms.x);
+        const float ax = h ? A2.z : A2.x, ay = h ? A2.w : A2.y;
+        const float wx = h ? W2.z : W2.x, wy = h ? W2.w : W2.y;
+        const float cx = ax * a - ay * b, cy = ax * b + ay * a;  // A_j (a + i b)
+        zr = fmaf(wx, cx, fmaf(-wy, cy, zr));                    // Re[W c]
+      }
+    }
+    for (int e = 0; e < k; ++e) {
+      const int col = ocol[e];
+      const float dv = half_bits_to_float(oval[e]) - ms.x;
+      const int j = col & (kHeadDim / 2 - 1);
+      const float2 WA = cmul(tab[rope_tab_index(j, lane)], sm.anchor[w][j]);
+      zr = fmaf(dv, (col < kHeadDim / 2) ? WA.x : -WA.y, zr);  // Re[WA dv] or Re[WA i dv]
+    }
+    z[0] = zr;
+  } else {
+#pragma unroll
+    for (int j = 0; j < kHeadDim / 2; ++j) {
+      const float a = fmaf(ms.y, sm.lut_k[code3(wd, j)], ms.x);
+      const float b = fmaf(ms.y, sm.lut_k[code3(wd, j + kHeadDim / 2)], ms.x);
+      const float2 e = cmul(sm.anchor[w][j], tab[rope_tab_index(j, lane)]);
+      const float ra = a * e.x - b * e.y, rb = b * e.x + a * e.y;
+#pragma unroll
+      for (int r = 0; r < GQ; ++r) z[r] = fmaf(sm.q[r][j], ra, fmaf(sm.q[r][j + kHeadDim / 2], rb, z[r]));
+    }
+    for (int e = 0; e < k; ++e) {
+      const int col = ocol[e];
+      const float dv = half_bits_to_float(oval[e]) - ms.x;
+      const int f = col & (kHeadDim / 2 - 1);
+      const float2 ee = cmul(sm.anchor[w][f], tab[rope_tab_index(f, lane)]);
+#pragma unroll
+      for (int r = 0; r < GQ; ++r) {
+        const float qa = sm.q[r][f], qb = sm.q[r][f + kHeadDim / 2];
+        const float dotu = (col < kHeadDim / 2) ? (qa * ee.x + qb * ee.y) : (-qa * ee.y + qb * ee.x);
+        z[r] = fmaf(dv, dotu, z[r]);
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// V part of one staged NUQ group: lane = channels 4l..4l+3; the group's
+// outlier corrections go through a per-warp shared buffer (lane = entry,
+// shared-memory atomics), folded into the accumulators afterwards.
+template <int GQ>
+__device__ __forceinline__ void v_accumulate_nuq_st(const DecodeParams& p, DecodeSmem<GQ>& sm,
+                                                    const unsigned char* st, float* obuf, int lane, int w,
+                                                    float (&acc)[GQ][4], float (&macc)[GQ]) {
+  const int k = p.geo.nout;
+  const uint32_t* vms = reinterpret_cast<const uint32_t*>(st + NuqStage::VMS);
+  const int bit = 12 * lane, wi = bit >> 5, sh = bit & 31;
+#pragma unroll 4
+  for (int t = 0; t < kGroupTokens; ++t) {
+    const float2 ms = unpack_min_scale(vms[t]);
+    const uint32_t* rw = reinterpret_cast<const uint32_t*>(st + NuqStage::VC + 48 * t);
+    uint32_t u = rw[wi] >> sh;
+    if (sh > 20) u |= rw[wi + 1] << (32 - sh);
+    float cv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) cv[e] = sm.lut_v[(u >> (3 * e)) & 7u];
+#pragma unroll
+    for (int r = 0; r < GQ; ++r) {
+      const float pr = sm.p[w][t][r];
+      const float pp = pr * ms.y;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[r][e] = fmaf(pp, cv[e], acc[r][e]);
+      macc[r] = fmaf(pr, ms.x, macc[r]);
+    }
+  }
+  if (k == 0) return;
+  // outliers: entry n = lane, lane + 32, ... of the group's 32k entries
+  const uint8_t* ocol = st + NuqStage::vcol(k);
+  const uint16_t* oval = reinterpret_cast<const uint16_t*>(st + NuqStage::vval(k));
+  for (int n = lane; n < kGroupTokens * k; n += 32) {
+    const int t = n / k, col = ocol[n];
+    const float dv = half_bits_to_float(oval[n]) - unpack_min_scale(vms[t]).x;
+#pragma unroll
+    for (int r = 0; r < GQ; ++r) atomicAdd(&obuf[r * kHeadDim + col], sm.p[w][t][r] * dv);
+  }
+  __syncwarp();
+#pragma unroll
+  for (int r = 0; r < GQ; ++r) {
+    float4* b4 = reinterpret_cast<float4*>(&obuf[r * kHeadDim + 4 * lane]);
+    const float4 o = *b4;
+    acc[r][0] += o.x;
+    acc[r][1] += o.y;
+    acc[r][2] += o.z;
+    acc[r][3] += o.w;
+    *b4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  __syncwarp();
+}
+
 template <int KB, int VB, int GQ>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -526,10 +706,27 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     // 32 consecutive entries (no bank conflicts)
     for (int idx = tid; idx < kGroupTokens * (kHeadDim / 2); idx += kThreads) {
       const int j = idx / kGroupTokens, l = idx % kGroupTokens;
-      rope_e[idx] = expi((double)l * p.theta[j]);
+      rope_e[rope_tab_index(j, l)] = expi((double)l * p.theta[j]);
     }
   }
+  // NUQ: per-warp stages, then per-warp outlier buffers (zeroed)
+  unsigned char* nuq_stages = reinterpret_cast<unsigned char*>(rope_e) +
+                              (G.pre_rope ? sizeof(float2) * kGroupTokens * (kHeadDim / 2) : 0);
+  float* nuq_obuf = reinterpret_cast<float*>(nuq_stages + (KB == 3 ? 8 * NuqStage::bytes(G.nout) : 0));
+  if constexpr (KB == 3)
+    for (int idx = tid; idx < 4 * GQ * kHeadDim; idx += kThreads) nuq_obuf[idx] = 0.0f;
   __syncthreads();
+  if constexpr (KB == 3 && GQ == 1) {
+    // one query head: fold the query into the offset table, W_{j,l} = conj(q_j + i q_{j+64}) e^{i l theta_j}
+    if (G.pre_rope && quant_split) {
+      for (int idx = tid; idx < kGroupTokens * (kHeadDim / 2); idx += kThreads) {
+        const int j = idx / kGroupTokens, l = idx % kGroupTokens;
+        const int at = rope_tab_index(j, l);
+        rope_e[at] = cmul(make_float2(sm.q[0][j], -sm.q[0][j + kHeadDim / 2]), rope_e[at]);
+      }
+      __syncthreads();
+    }
+  }
   if (tid < GQ) {
     float a = 0.0f;
     for (int c = 0; c < kHeadDim; ++c) a += sm.q[tid][c];
@@ -547,7 +744,34 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     for (int k = 0; k < 4; ++k) acc[r][k] = 0.0f;
   }
 
-  if constexpr (KB != 16) if (quant_split) {
+  if constexpr (KB == 3) if (quant_split) {
+    // staged: group grp + 4 (this warp's next) streams in while grp is computed
+    const int ngroups = p.Nq / kGroupTokens;
+    const int g0 = sp * p.gps;
+    const int g1 = min(ngroups, g0 + p.gps);
+    const int sb = NuqStage::bytes(G.nout);
+    unsigned char* stw = nuq_stages + w * 2 * sb;
+    const uint32_t stw_s = smem_u32(stw);
+    float* obuf = nuq_obuf + w * GQ * kHeadDim;
+    int cur = 0;
+    if (g0 + w < g1) issue_nuq(p, s, g0 + w, stw_s, lane);
+    cp_async_commit();
+    for (int grp = g0 + w; grp < g1; grp += 4) {
+      if (grp + 4 < g1) issue_nuq(p, s, grp + 4, stw_s + (cur ^ 1) * sb, lane);
+      cp_async_commit();
+      cp_async_wait<1>();
+      __syncwarp();
+      const unsigned char* stc = stw + cur * sb;
+      float z[GQ];
+      k_logits_nuq_st<GQ>(p, sm, rope_e, stc, grp, lane, w, z);
+      softmax_update<GQ>(z, m, lsum, acc, macc, sm.p[w], lane);
+      v_accumulate_nuq_st<GQ>(p, sm, stc, obuf, lane, w, acc, macc);
+      __syncwarp();
+      cur ^= 1;
+    }
+    cp_async_wait<0>();
+  }
+  if constexpr (KB != 16 && KB != 3) if (quant_split) {
     const int ngroups = p.Nq / kGroupTokens;
     const int g0 = sp * p.gps;
     const int g1 = min(ngroups, g0 + p.gps);
@@ -555,10 +779,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
       float z[GQ];
       if (G.pre_rope) {
         k_logits_rope<KB, GQ>(p, sm, rope_e, s, grp, lane, w, z);
-      } else if (KB == 3) {
-        k_logits_nuq<GQ>(p, sm, s, grp, lane, z);
       } else {
-        k_logits_uniform<(KB == 3 ? 4 : KB), GQ>(p, sm, s, grp, lane, w, z);
+        k_logits_uniform<KB, GQ>(p, sm, s, grp, lane, w, z);
       }
       softmax_update<GQ>(z, m, lsum, acc, macc, sm.p[w], lane);
       v_accumulate<VB, GQ>(p, sm, s, grp, lane, w, acc, macc);
@@ -703,6 +925,7 @@ template <int KB, int VB, int GQ>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t st) {
   size_t smem = ((sizeof(DecodeSmem<GQ>) + 15) / 16) * 16;
   if (p.geo.pre_rope) smem += sizeof(float2) * kGroupTokens * (kHeadDim / 2);
+  if (KB == 3) smem += 8 * (size_t)NuqStage::bytes(p.geo.nout) + 4 * GQ * kHeadDim * sizeof(float);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<KB, VB, GQ>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
