@@ -453,6 +453,13 @@ def main():
     kern_ms = statistics.mean(kern)
     peak, peak_kind = measured_peaks()
     achieved = (dec_bytes / model.L) / (kern_ms * 1e-3) / 1e9
+    # per (K bits, V bits) pair when the layers differ: mean decode µs and fraction of the peak
+    by_pair = {}
+    for l, c in enumerate(model.cfgs):
+        key = f"K{c['k_bits']}V{c['v_bits']}"
+        by_pair.setdefault(key, [[], algorithmic_bytes(c, model.T)])[0].extend(kern[l::model.L])
+    pairs = {k: {"layers": len(v[0]) // args.steps, "decode_us": statistics.mean(v[0]) * 1e3,
+                 "frac": v[1] / (statistics.mean(v[0]) * 1e-3) / 1e9 / peak} for k, v in by_pair.items()}
     e2e_ms, h2d, d2h = time_e2e(model, stream, max(3, args.steps // 2), 2)
     e2e_ms = max_over_ranks(e2e_ms)
     launches = model.launches_per_step() * args.steps
@@ -499,6 +506,7 @@ def main():
                      "traffic": ncu_traffic(f"decode:{args.workload}"),
                      "bytes_per_launch": dec_bytes / model_layers,
                      "launch_us": kern_ms * 1e3},
+        "decode_by_pair": pairs if len(pairs) > 1 else None,
         "fp16_baseline": fp16,
         "speedup_vs_fp16": (fp16["us_per_step"] / value) if fp16 else None,
         "cpu_baseline": cpu,

@@ -245,59 +245,112 @@ __device__ __forceinline__ constexpr int v_group(int mc) {
   return (VB == 8 ? 16 * mc : VB == 4 ? 32 * (mc >> 1) : 64 * (mc >> 2)) / kGV;
 }
 
+// Warp reduce-scatter of NV per-lane values (NV = 1, 2, 4, 8): afterwards a
+// lane holds the warp-wide sum of value head_of_lane<NV>(lane).  Each of the
+// first log2(NV) butterfly steps halves the values a lane keeps, the rest
+// finish the sum: log2(NV) + 5 - log2(NV) rounds instead of 5 per value.
+template <int NV>
+__device__ __forceinline__ float reduce_heads(const float (&v)[NV], int lane) {
+  float a[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) a[i] = v[i];
+#pragma unroll
+  for (int n = NV, bit = 16; n > 1; n >>= 1, bit >>= 1) {
+    const bool up = (lane & bit) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float keep = up ? a[i + n / 2] : a[i];
+      const float send = up ? a[i] : a[i + n / 2];
+      a[i] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+    }
+  }
+#pragma unroll
+  for (int bit = 16 / NV; bit >= 1; bit >>= 1) a[0] += __shfl_xor_sync(0xffffffffu, a[0], bit);
+  return a[0];
+}
+template <int NV>
+__device__ __forceinline__ int head_of_lane(int lane) {
+  return NV == 8 ? (lane >> 2) & 7 : NV == 4 ? (lane >> 3) & 3 : NV == 2 ? (lane >> 4) & 1 : 0;
+}
+// lane bits not used to select the head (lanes that hold the same sum)
+template <int NV>
+__device__ __forceinline__ constexpr int rest_mask() { return 32 / NV - 1; }
+
 // hi (or lo) fp16 part of x, as a float: lanes with lo = 1 get x - fp16(x).
 __device__ __forceinline__ float split_part(float x, float lo) {
   return fmaf(-lo, __half2float(__float2half_rn(x)), x);
 }
+// The same for two values, packed: fp16x2 of (x0, x1) (lo = 0) or of their
+// remainders x - fp16(x) (lo = 1).
+__device__ __forceinline__ uint32_t split_pack(float x0, float x1, float lo) {
+  const float2 h = __half22float2(__floats2half2_rn(x0, x1));
+  return h2_as_u32(__floats2half2_rn(fmaf(-lo, h.x, x0), fmaf(-lo, h.y, x1)));
+}
+
+// Channels of this lane in the Q' build: c0, c0 + 1, c0 + D, c0 + D + 1 with
+// (c0, c0 + D) and (c0 + 1, c0 + D + 1) the two halves of the B-fragment
+// words 2s and 2s + 1 (s = lane & 7) of reader thread lane >> 3, for every
+// code width (the k-slot order of k_frag / k_slot_of).
+template <int KB>
+__device__ __forceinline__ constexpr int qb_pair_dist() { return KB == 8 ? 2 : KB == 4 ? 4 : 8; }
+template <int KB>
+__device__ __forceinline__ int qb_first_channel(int lane) {
+  return KB == 8 ? 4 * lane : KB == 4 ? 8 * (lane >> 1) + 2 * (lane & 1) : 16 * (lane >> 2) + 2 * (lane & 3);
+}
 
 // One 32-token group for one warp: Q' fragments, S = K Q' (2 m-tiles x NT
 // n-tiles), online softmax, O += V^T P' (8 m-tiles x NT).
-//  qh[k]: byte offset, inside a 64-byte fragment row, of this lane's
-//         channel 4*lane+k (hi row; the lo row's offset is qh[k] ^ 32)
 //
 // JC (one n-tile, at most 2 heads): the PV B operand puts the V group into
 // the columns too -- column = (head, V group, hi/lo) -- so a lane builds P'
 // for one (head, group) pair instead of one per group; an m-tile's D
 // columns of the other group are then unused (see stage_quant).
-template <int KB, int VB, int NT, bool JC>
+template <int KB, int VB, int NT, bool JC, int GT>
 __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWarpSmem<NT>& sm,
                                               const unsigned char* st, int g, int w, int lane,
-                                              const int (&qh)[4], float (&O)[8][NT][4],
-                                              float (&macc)[NT][kNVG], float (&m_used)[NT], float (&lsum)[NT]) {
+                                              float (&O)[8][NT][4], float (&macc)[NT][kNVG], float (&m_used)[NT],
+                                              float (&lsum)[NT]) {
   using SG = StageGeom<KB, VB>;
   const int gq = lane >> 2, tq = lane & 3;
 
   // (a) Q' = q * scale_k (hi + lo fp16) into this warp's fragment rows,
   //     bias = q . min_k; V {min, scale} of this lane's token to fp32
   {
-    const uint4 sc = *reinterpret_cast<const uint4*>(st + SG::KS + 16 * lane);
-    const uint32_t wv[4] = {sc.x, sc.y, sc.z, sc.w};
-    float2 ms[4];
+    constexpr int D = qb_pair_dist<KB>();
+    const int c0 = qb_first_channel<KB>(lane);
+    const uint2 w01 = *reinterpret_cast<const uint2*>(st + SG::KS + 4 * c0);
+    const uint2 w23 = *reinterpret_cast<const uint2*>(st + SG::KS + 4 * (c0 + D));
+    const float2 ms[4] = {unpack_min_scale(w01.x), unpack_min_scale(w01.y), unpack_min_scale(w23.x),
+                          unpack_min_scale(w23.y)};
+    // channels c0, c0 + D share the power-of-two multiplier (same c & 3 class), as do c0 + 1, c0 + D + 1
+    const float me = kq_mult<KB>(c0 & 3), mo = kq_mult<KB>((c0 + 1) & 3);
+    const float sk[4] = {ms[0].y * me, ms[1].y * mo, ms[2].y * me, ms[3].y * mo};
+    const int tsl = lane >> 3;                                        // reader thread-in-group of these channels
+    const int wofs = (8 * (lane & 7)) ^ (((tsl >> 1) & 1) << 4);      // words 2s, 2s+1 in the (swizzled) hi row
+    float bpart[GT];                                                  // this lane's share of each head's bias
 #pragma unroll
-    for (int k = 0; k < 4; ++k) ms[k] = unpack_min_scale(wv[k]);
-    const int tsl = lane >> 3;  // the reader thread-in-group owning these channels
-#pragma unroll
-    for (int r = 0; r < 8 * NT; ++r) {
-      if (r >= g) break;
+    for (int r = 0; r < GT; ++r) {
+      bpart[r] = 0.0f;
+      if (r >= g) continue;
       unsigned char* dhi = reinterpret_cast<unsigned char*>(&sm.bq[w][r >> 2][8 * (r & 3) + tsl][0]);
       unsigned char* dlo = dhi + 4 * 64;
-      const float4 q4 = *reinterpret_cast<const float4*>(&qw[r][4 * lane]);
-      const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
-      float bp = 0.0f, off = 0.0f;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float qp = qv[k] * ms[k].y * kq_mult<KB>(k);  // channel 4*lane + k: c & 3 == k
-        bp = fmaf(qv[k], ms[k].x, bp);
-        const __half hi = __float2half_rn(qp);
-        const __half lo = __float2half_rn(qp - __half2float(hi));
-        off += qp;  // hi + lo = qp to ~2^-22
-        *reinterpret_cast<__half*>(dhi + qh[k]) = hi;
-        *reinterpret_cast<__half*>(dlo + (qh[k] ^ 32)) = lo;
-      }
+      const float2 q01 = *reinterpret_cast<const float2*>(&qw[r][c0]);
+      const float2 q23 = *reinterpret_cast<const float2*>(&qw[r][c0 + D]);
+      const float qp0 = q01.x * sk[0], qp1 = q01.y * sk[1], qp2 = q23.x * sk[2], qp3 = q23.y * sk[3];
+      const __half2 hA = __floats2half2_rn(qp0, qp2), hB = __floats2half2_rn(qp1, qp3);
+      const float2 fA = __half22float2(hA), fB = __half22float2(hB);
+      const __half2 lA = __floats2half2_rn(qp0 - fA.x, qp2 - fA.y), lB = __floats2half2_rn(qp1 - fB.x, qp3 - fB.y);
+      *reinterpret_cast<uint2*>(dhi + wofs) = make_uint2(h2_as_u32(hA), h2_as_u32(hB));
+      *reinterpret_cast<uint2*>(dlo + (wofs ^ 32)) = make_uint2(h2_as_u32(lA), h2_as_u32(lB));
+      const float bp = fmaf(q01.x, ms[0].x, fmaf(q01.y, ms[1].x, fmaf(q23.x, ms[2].x, q23.y * ms[3].x)));
+      const float off = (qp0 + qp1) + (qp2 + qp3);  // hi + lo = qp to ~2^-22
       // the mma's constant part 1024 * sum_c (hi + lo), in logit units
-      bp = warp_sum(fmaf(-1024.0f * (1.0f / (float)(1 << kq_exp<KB>())), off, bp));
-      if (lane == 0) sm.bias[w][r] = bp;
+      bpart[r] = fmaf(-1024.0f * (1.0f / (float)(1 << kq_exp<KB>())), off, bp);
     }
+    // all heads' biases with one reduce-scatter over the warp
+    const float bsum = reduce_heads<GT>(bpart, lane);
+    const int hb = head_of_lane<GT>(lane);
+    if ((lane & rest_mask<GT>()) == 0 && hb < g) sm.bias[w][hb] = bsum;
     const uint32_t* vsw = reinterpret_cast<const uint32_t*>(st + SG::VS);
     const int iv = vsc_index(lane), im = vmn_index(lane);
     constexpr float kVCentre = (float)(1 << (VB - 1));  // the V codes enter the mma centred
@@ -459,8 +512,8 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
       for (int j = 0; j < (JC ? 1 : kNVG); ++j) {
         const int jv = JC ? ((gq >> 1) & 1) : j;
         const float4 sv = *reinterpret_cast<const float4*>(&sm.vsc[w][jv][16 * kt + 4 * tq]);
-        bp[nt][j][0] = h2_as_u32(__floats2half2_rn(split_part(v0 * sv.x, lo_sel), split_part(v1 * sv.y, lo_sel)));
-        bp[nt][j][1] = h2_as_u32(__floats2half2_rn(split_part(v2 * sv.z, lo_sel), split_part(v3 * sv.w, lo_sel)));
+        bp[nt][j][0] = split_pack(v0 * sv.x, v1 * sv.y, lo_sel);
+        bp[nt][j][1] = split_pack(v2 * sv.z, v3 * sv.w, lo_sel);
       }
     }
     // V code fragments via ldmatrix.trans on the packed (swizzled) rows
@@ -672,7 +725,7 @@ __device__ __forceinline__ void process_f16(const MmaWarpSmem<NT>& sm, const uns
   for (int nt = 0; nt < NT; ++nt) {
     const float v0 = __shfl_sync(0xffffffffu, P[nt], src0);
     const float v1 = __shfl_sync(0xffffffffu, P[nt], src0 + 4);
-    bp[nt] = h2_as_u32(__floats2half2_rn(split_part(v0, lo_sel), split_part(v1, lo_sel)));
+    bp[nt] = split_pack(v0, v1, lo_sel);
   }
   const uint32_t vbase = smem_u32(st + F16Geom::VC);
 #pragma unroll

@@ -243,15 +243,6 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (GT == 1 ? 4 : 3) : 2)
   const long long j1 = first_item_at(p, warp_x(p, gw + 1));
   if (j0 >= j1) return;
 
-  // byte offset of this lane's channel 4*lane+k inside its (hi) Q' fragment row
-  int qh[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    int s_, e_;
-    k_slot_of<KBq>(4 * (lane & 7) + k, s_, e_);
-    qh[k] = (2 * (4 * s_ + e_)) ^ (((lane >> 4) & 1) << 4);  // row chunk swizzle: ((row >> 1) & 3) = tsl >> 1
-  }
-
   float O[8][NT][4], macc[NT][kNVG], m_used[NT], lsum[NT];
   auto reset = [&]() {
 #pragma unroll
@@ -337,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (GT == 1 ? 4 : 3) : 2)
     const unsigned char* stc = st0 + cur * LY::kStageBytes;
     if (LY::kQuant && k < ng) {
       if constexpr (LY::kQuant) {
-        process_group<KB, VB, NT, JC>(qw, sm, stc, g, w, lane, qh, O, macc, m_used, lsum);
+        process_group<KB, VB, NT, JC, GT>(qw, sm, stc, g, w, lane, O, macc, m_used, lsum);
         has_q = true;
       }
     } else {
