@@ -223,20 +223,21 @@ __device__ __forceinline__ float ex2(float x) {  // 2^x (hardware approximation;
 template <int KB, int VB>
 __device__ __forceinline__ void issue_group(const DecodeParams& p, int s, int grp, uint32_t dst, int lane) {
   using SG = StageGeom<KB, VB>;
-  const Geometry& G = p.geo;
-  const size_t row0 = (size_t)s * G.qcap + (size_t)grp * kGroupTokens;
-  const uint8_t* kc = p.L.k_codes + row0 * SG::KROW;
-  const uint8_t* vc = p.L.v_codes + row0 * SG::VROW;
-  const uint32_t* ks = p.L.k_scales + ((size_t)s * G.gcap + grp) * kHeadDim;
-  const uint32_t* vs = p.L.v_scales + row0 * kNVG;
+  // first row of the group in the stream-major regions (< 2^31: checked on the host);
+  // the group's K scales are the 128 words at row0 * 4, its V scales the words at row0 * kNVG
+  const uint32_t row0 = (uint32_t)s * (uint32_t)p.geo.qcap + (uint32_t)grp * kGroupTokens;
+  const uint8_t* kc = p.L.k_codes + (size_t)row0 * SG::KROW + 16 * lane;
+  const uint8_t* vc = p.L.v_codes + (size_t)row0 * SG::VROW + 16 * lane;
+  const uint8_t* ks = reinterpret_cast<const uint8_t*>(p.L.k_scales) + (size_t)row0 * 16 + 16 * lane;
+  const uint8_t* vs = reinterpret_cast<const uint8_t*>(p.L.v_scales) + (size_t)row0 * (4 * kNVG) + 16 * lane;
   constexpr int KCH = kGroupTokens * SG::KROW / 16, VCH = kGroupTokens * SG::VROW / 16;
   static_assert(KCH % 32 == 0 && VCH % 32 == 0, "whole chunks per lane");
 #pragma unroll
-  for (int i = lane; i < KCH; i += 32) cp_async16(dst + SG::KC + swz(16 * i, SG::KSW), kc + 16 * i);
-  cp_async16(dst + SG::KS + 16 * lane, ks + 4 * lane);  // 512 B = 32 chunks
+  for (int n = 0; n < KCH / 32; ++n) cp_async16(dst + SG::KC + swz(16 * (lane + 32 * n), SG::KSW), kc + 512 * n);
+  cp_async16(dst + SG::KS + 16 * lane, ks);  // 512 B = 32 chunks
 #pragma unroll
-  for (int i = lane; i < VCH; i += 32) cp_async16(dst + SG::VC + swz(16 * i, SG::VSW), vc + 16 * i);
-  if (lane < kGroupTokens * kNVG / 4) cp_async16(dst + SG::VS + 16 * lane, vs + 4 * lane);
+  for (int n = 0; n < VCH / 32; ++n) cp_async16(dst + SG::VC + swz(16 * (lane + 32 * n), SG::VSW), vc + 512 * n);
+  if (lane < kGroupTokens * kNVG / 4) cp_async16(dst + SG::VS + 16 * lane, vs);
 }
 
 // V group (0 .. d/G_V - 1) of m-tile mc: every m-tile lies inside one group.

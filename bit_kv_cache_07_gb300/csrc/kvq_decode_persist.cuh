@@ -183,25 +183,48 @@ __device__ __forceinline__ void finalize_stream(const DecodeParams& p, int slot,
   prev = __shfl_sync(0xffffffffu, prev, 0);
   if (prev != (unsigned)(count - 1)) return;
   __threadfence();
-  // last piece of stream s: merge its slots wf + s .. wf + s + count - 1
+  // last piece of stream s: merge its slots wf + s .. wf + s + count - 1.
+  // The slots' (m, l) are read by one lane each (all loads in flight at
+  // once); the accumulators in batches of 4 slots.
   const int b = s / G.Hkv, hk = s % G.Hkv;
+  const size_t slot0 = (size_t)(wf + s);
   for (int r = 0; r < g; ++r) {
     float M = -INFINITY;
-    for (int q2 = 0; q2 < count; ++q2)
-      M = fmaxf(M, __ldcg(&p.part_ml[((size_t)(wf + s + q2) * g + r) * 2]));
+    for (int q0 = lane; q0 < count; q0 += 32) M = fmaxf(M, __ldcg(&p.part_ml[((slot0 + q0) * g + r) * 2]));
+    M = warp_max(M);
     float L = 0.0f, v[4] = {0, 0, 0, 0};
-    for (int q2 = 0; q2 < count; ++q2) {
-      const size_t base = (size_t)(wf + s + q2) * g + r;
-      const float mq = __ldcg(&p.part_ml[base * 2]);
-      if (mq == -INFINITY) continue;
-      const float e = exp2f(mq - M);
-      L += e * __ldcg(&p.part_ml[base * 2 + 1]);
-      const float4 a = __ldcg(reinterpret_cast<const float4*>(&p.part_acc[base * kHeadDim + 4 * lane]));
-      v[0] += e * a.x;
-      v[1] += e * a.y;
-      v[2] += e * a.z;
-      v[3] += e * a.w;
+    for (int c0 = 0; c0 < count; c0 += 32) {
+      // lane q: weight of slot c0 + q
+      float e = 0.0f;
+      if (c0 + lane < count) {
+        const size_t base = (slot0 + c0 + lane) * g + r;
+        const float mq = __ldcg(&p.part_ml[base * 2]);
+        e = (mq == -INFINITY) ? 0.0f : exp2f(mq - M);
+        L += e * __ldcg(&p.part_ml[base * 2 + 1]);
+      }
+      const int n = min(32, count - c0);
+      for (int q = 0; q < n; q += 4) {
+        float4 a[4];
+        float eq[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          eq[u] = __shfl_sync(0xffffffffu, e, (q + u) & 31);
+          a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (q + u < n)
+            a[u] = __ldcg(reinterpret_cast<const float4*>(
+                &p.part_acc[((slot0 + c0 + q + u) * g + r) * kHeadDim + 4 * lane]));
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (q + u >= n) break;
+          v[0] = fmaf(eq[u], a[u].x, v[0]);
+          v[1] = fmaf(eq[u], a[u].y, v[1]);
+          v[2] = fmaf(eq[u], a[u].z, v[2]);
+          v[3] = fmaf(eq[u], a[u].w, v[3]);
+        }
+      }
     }
+    L = warp_sum(L);
     const size_t o = ((size_t)b * G.Hq + hk * g + r) * kHeadDim + 4 * lane;
     const __half2 h0 = __floats2half2_rn(v[0] / L, v[1] / L), h1 = __floats2half2_rn(v[2] / L, v[3] / L);
     uint2 stv;

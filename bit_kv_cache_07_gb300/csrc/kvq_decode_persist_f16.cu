@@ -29,6 +29,7 @@ bool persist_eligible(const Geometry& g) {
   if (g.pre_rope || g.g > kMaxGQA) return false;
   if (g.fp16_mode) return true;
   if (g.kb == 3 || g.vb == 3) return false;
+  if ((uint64_t)g.NS * (uint64_t)g.qcap >= (1ull << 31)) return false;  // 32-bit row index in the kernel
   return g.gv == 64;
 }
 

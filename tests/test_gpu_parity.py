@@ -93,6 +93,11 @@ CASES = {
     "kv2_gqa4": (2, 2, 2, 8, 2, 1000, dict(S=4, R=128)),
     "k2v8_g2": (2, 8, 1, 4, 2, 513, dict(S=1, R=5)),
     "hadamard_g7": (4, 2, 2, 14, 2, 600, dict(S=4, R=32, had=1)),
+    # 5 to 8 heads per KV head run head-major on the tensor cores
+    "kv8_g8": (8, 8, 1, 8, 1, 700, dict(S=4, R=32)),
+    "kv4_g5": (4, 4, 2, 10, 2, 650, dict(S=2, R=40)),
+    "k2v8_g6_hadamard": (2, 8, 1, 6, 1, 500, dict(S=4, R=16, had=1)),
+    "k8v2_g8": (8, 2, 1, 16, 2, 400, dict(S=0, R=0)),
     "hadamard_kv8": (8, 8, 1, 4, 1, 400, dict(S=4, R=32, had=1)),
     "gv32": (4, 4, 1, 2, 1, 300, dict(S=2, R=16, gv=32)),
     "gv128": (4, 2, 1, 2, 1, 300, dict(S=2, R=16, gv=128)),
