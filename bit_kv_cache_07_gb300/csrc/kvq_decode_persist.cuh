@@ -42,10 +42,16 @@ struct PersistLayout {
   static constexpr int kStageBytes = kQBytes > F16Geom::BYTES ? kQBytes : F16Geom::BYTES;
   static constexpr int kPerWarpStages = kStages * kStageBytes;
   static constexpr int r128(int x) { return (x + 127) / 128 * 128; }
-  static constexpr int kPerWarpO = r128(GT * kHeadDim * 4 + GT * 2 * 4);  // staging O[h][c] + (m, l)
-  static constexpr int kPerWarpQ = r128(GT * kHeadDim * 4);              // this warp's stream's query
-  static constexpr int kPerWarp = kPerWarpStages + kPerWarpO + kPerWarpQ;
+  // this warp's stream's query; once the query is no longer needed (the
+  // stream's Q' and fp16 fragments are built) the same bytes hold the
+  // staged O[h][c], and the group-bias scratch holds the staged (m, l)
+  static constexpr int kPerWarpQ = r128(GT * kHeadDim * 4);
+  static constexpr int kPerWarp = kPerWarpStages + kPerWarpQ;
   static constexpr int kBytes = kFixed + 4 * kPerWarp;
+  // resident CTAs the registers are budgeted for: single-head groups get 4
+  // (128 registers) when 4 CTAs fit in 228 KB (1 KB reserved each); larger
+  // groups keep 168 registers (3 CTAs) -- measured faster than 4 CTAs at 128
+  static constexpr int kMinCtas = NT == 2 ? 2 : (GT == 1 && 4 * (kBytes + 1024) <= 228 * 1024 ? 4 : 3);
 };
 
 // Fold the quantized accumulators into the staging buffer: sO[h][c] = the
@@ -237,7 +243,7 @@ __device__ __forceinline__ void finalize_stream(const DecodeParams& p, int slot,
 }
 
 template <int KB, int VB, int NT, int GT>
-__global__ void __launch_bounds__(kThreads, NT == 1 ? (GT == 1 ? 4 : 3) : 2)
+__global__ void __launch_bounds__(kThreads, (PersistLayout<KB, VB, NT, GT>::kMinCtas))
     decode_persist_kernel(const __grid_constant__ DecodeParams p) {
   using LY = PersistLayout<KB, VB, NT, GT>;
   constexpr int KBq = KB == 16 ? 4 : KB, VBq = VB == 16 ? 4 : VB;  // fp16 mode: quantized helpers unused
@@ -250,9 +256,9 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (GT == 1 ? 4 : 3) : 2)
   unsigned char* mine = smem_raw + LY::kFixed + w * LY::kPerWarp;
   unsigned char* st0 = mine;
   const uint32_t st0_s = smem_u32(st0);
-  float* sO = reinterpret_cast<float*>(mine + LY::kPerWarpStages);
-  float* sML = sO + GT * kHeadDim;
-  float (*qw)[kHeadDim] = reinterpret_cast<float (*)[kHeadDim]>(mine + LY::kPerWarpStages + LY::kPerWarpO);
+  float (*qw)[kHeadDim] = reinterpret_cast<float (*)[kHeadDim]>(mine + LY::kPerWarpStages);
+  float* sO = &qw[0][0];       // staging, after the query's last use
+  float* sML = &sm.bias[w][0];  // staging (m, l): 8 * NT >= 2 * GT floats
 
   {
     uint32_t* z = reinterpret_cast<uint32_t*>(&sm.bq[0][0][0][0]);
@@ -356,14 +362,14 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (GT == 1 ? 4 : 3) : 2)
       }
     } else {
       if (!bq_f16) {
+        build_bq_f16<NT>(qw, sm, g, w, lane);  // the query's last use: sO may now overwrite it
+        bq_f16 = true;
+        __syncwarp();
         if (has_q) {
           stage_quant<VBq, NT, GT, JC>(p, sO, sML, g, lane, O, macc, m_used, lsum);
           has_q = false;
           staged = true;
         }
-        build_bq_f16<NT>(qw, sm, g, w, lane);
-        bq_f16 = true;
-        __syncwarp();
       }
       process_f16<NT>(sm, stc, g, w, lane, kF16Tokens * (k - ng), k1, O, m_used, lsum);
     }
