@@ -574,35 +574,47 @@ __device__ __forceinline__ void k_logits_nuq_st(const DecodeParams& p, DecodeSme
   }
   // group anchor e^{i t0 theta_j}
   const int pos0 = G.S + grp * kGroupTokens;
-  for (int j = lane; j < kHeadDim / 2; j += 32) sm.anchor[w][j] = expi((double)pos0 * p.theta[j]);
-  __syncwarp();
   if constexpr (GQ == 1) {
-    float zr = 0.0f;
+    // anchors of pairs 2i, 2i+1 as (x_2i, x_2i+1, y_2i, y_2i+1): fp32x2 operands without shuffling
+    float* ap = reinterpret_cast<float*>(&sm.anchor[w][0]);
+    for (int j = lane; j < kHeadDim / 2; j += 32) {
+      const float2 a = expi((double)pos0 * p.theta[j]);
+      ap[(j >> 1) * 4 + (j & 1)] = a.x;
+      ap[(j >> 1) * 4 + 2 + (j & 1)] = a.y;
+    }
+    __syncwarp();
+    // two channel pairs at a time in packed fp32x2 arithmetic (W laid out like the anchors)
     const float4* tab4 = reinterpret_cast<const float4*>(tab);
-    const float4* anc4 = reinterpret_cast<const float4*>(&sm.anchor[w][0]);
+    const float4* anc4 = reinterpret_cast<const float4*>(ap);
+    const float2 S2 = make_float2(ms.y, ms.y), M2 = make_float2(ms.x, ms.x);
+    float2 z2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < kHeadDim / 2; j += 2) {
-      const float4 A2 = anc4[j >> 1];                        // A_j, A_{j+1}
-      const float4 W2 = tab4[(j >> 1) * kGroupTokens + lane];  // W_{j,lane}, W_{j+1,lane}
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float a = fmaf(ms.y, sm.lut_k[code3(wd, j + h)], ms.x);
-        const float b = fmaf(ms.y, sm.lut_k[code3(wd, j + h + kHeadDim / 2)], ms.x);
-        const float ax = h ? A2.z : A2.x, ay = h ? A2.w : A2.y;
-        const float wx = h ? W2.z : W2.x, wy = h ? W2.w : W2.y;
-        const float cx = ax * a - ay * b, cy = ax * b + ay * a;  // A_j (a + i b)
-        zr = fmaf(wx, cx, fmaf(-wy, cy, zr));                    // Re[W c]
-      }
+      const float4 A4 = anc4[j >> 1];
+      const float4 W4 = tab4[(j >> 1) * kGroupTokens + lane];
+      const float2 Ax = make_float2(A4.x, A4.y), Ay = make_float2(A4.z, A4.w);
+      const float2 Wx = make_float2(W4.x, W4.y), Wy = make_float2(W4.z, W4.w);
+      const float2 a2 = __ffma2_rn(S2, make_float2(sm.lut_k[code3(wd, j)], sm.lut_k[code3(wd, j + 1)]), M2);
+      const float2 b2 = __ffma2_rn(
+          S2, make_float2(sm.lut_k[code3(wd, j + kHeadDim / 2)], sm.lut_k[code3(wd, j + 1 + kHeadDim / 2)]), M2);
+      const float2 cx = __ffma2_rn(Ax, a2, __fmul2_rn(make_float2(-Ay.x, -Ay.y), b2));  // ax a - ay b
+      const float2 cy = __ffma2_rn(Ax, b2, __fmul2_rn(Ay, a2));                          // ax b + ay a
+      z2 = __ffma2_rn(Wx, cx, __ffma2_rn(make_float2(-Wy.x, -Wy.y), cy, z2));           // Re[W c]
     }
+    float zr = z2.x + z2.y;
+    const float* tf = reinterpret_cast<const float*>(tab);
     for (int e = 0; e < k; ++e) {
       const int col = ocol[e];
       const float dv = half_bits_to_float(oval[e]) - ms.x;
       const int j = col & (kHeadDim / 2 - 1);
-      const float2 WA = cmul(tab[rope_tab_index(j, lane)], sm.anchor[w][j]);
+      const int wi = ((j >> 1) * kGroupTokens + lane) * 4 + (j & 1), ai = (j >> 1) * 4 + (j & 1);
+      const float2 WA = cmul(make_float2(tf[wi], tf[wi + 2]), make_float2(ap[ai], ap[ai + 2]));
       zr = fmaf(dv, (col < kHeadDim / 2) ? WA.x : -WA.y, zr);  // Re[WA dv] or Re[WA i dv]
     }
     z[0] = zr;
   } else {
+    for (int j = lane; j < kHeadDim / 2; j += 32) sm.anchor[w][j] = expi((double)pos0 * p.theta[j]);
+    __syncwarp();
 #pragma unroll
     for (int j = 0; j < kHeadDim / 2; ++j) {
       const float a = fmaf(ms.y, sm.lut_k[code3(wd, j)], ms.x);
@@ -651,8 +663,13 @@ __device__ __forceinline__ void v_accumulate_nuq_st(const DecodeParams& p, Decod
     for (int r = 0; r < GQ; ++r) {
       const float pr = sm.p[w][t][r];
       const float pp = pr * ms.y;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[r][e] = fmaf(pp, cv[e], acc[r][e]);
+      const float2 pp2 = make_float2(pp, pp);
+      const float2 a01 = __ffma2_rn(pp2, make_float2(cv[0], cv[1]), make_float2(acc[r][0], acc[r][1]));
+      const float2 a23 = __ffma2_rn(pp2, make_float2(cv[2], cv[3]), make_float2(acc[r][2], acc[r][3]));
+      acc[r][0] = a01.x;
+      acc[r][1] = a01.y;
+      acc[r][2] = a23.x;
+      acc[r][3] = a23.y;
       macc[r] = fmaf(pr, ms.x, macc[r]);
     }
   }
@@ -719,10 +736,14 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   if constexpr (KB == 3 && GQ == 1) {
     // one query head: fold the query into the offset table, W_{j,l} = conj(q_j + i q_{j+64}) e^{i l theta_j}
     if (G.pre_rope && quant_split) {
-      for (int idx = tid; idx < kGroupTokens * (kHeadDim / 2); idx += kThreads) {
-        const int j = idx / kGroupTokens, l = idx % kGroupTokens;
-        const int at = rope_tab_index(j, l);
-        rope_e[at] = cmul(make_float2(sm.q[0][j], -sm.q[0][j + kHeadDim / 2]), rope_e[at]);
+      // W of pairs 2i, 2i+1 for offset l as (x_2i, x_2i+1, y_2i, y_2i+1)
+      float4* tab4 = reinterpret_cast<float4*>(rope_e);
+      for (int idx = tid; idx < kGroupTokens * (kHeadDim / 4); idx += kThreads) {
+        const int jp = idx / kGroupTokens, l = idx % kGroupTokens, j = 2 * jp;
+        const float4 e4 = tab4[jp * kGroupTokens + l];  // E_j, E_{j+1} (rope_tab_index layout)
+        const float2 w0 = cmul(make_float2(sm.q[0][j], -sm.q[0][j + kHeadDim / 2]), make_float2(e4.x, e4.y));
+        const float2 w1 = cmul(make_float2(sm.q[0][j + 1], -sm.q[0][j + 1 + kHeadDim / 2]), make_float2(e4.z, e4.w));
+        tab4[jp * kGroupTokens + l] = make_float4(w0.x, w1.x, w0.y, w1.y);
       }
       __syncthreads();
     }
