@@ -283,9 +283,10 @@ __device__ __forceinline__ float split_part(float x, float lo) {
 }
 // The same for two values, packed: fp16x2 of (x0, x1) (lo = 0) or of their
 // remainders x - fp16(x) (lo = 1).
-__device__ __forceinline__ uint32_t split_pack(float x0, float x1, float lo) {
-  const float2 h = __half22float2(__floats2half2_rn(x0, x1));
-  return h2_as_u32(__floats2half2_rn(fmaf(-lo, h.x, x0), fmaf(-lo, h.y, x1)));
+__device__ __forceinline__ uint32_t split_pack(float2 x, float lo) {
+  const float2 h = __half22float2(__floats2half2_rn(x.x, x.y));
+  const float2 y = __ffma2_rn(make_float2(-lo, -lo), h, x);
+  return h2_as_u32(__floats2half2_rn(y.x, y.y));
 }
 
 // Channels of this lane in the Q' build: c0, c0 + 1, c0 + D, c0 + D + 1 with
@@ -447,34 +448,38 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
         zs[mt][rh] = S[mt][nt][2 * rh] + S[mt][nt][2 * rh + 1];  // 2^E x (logit - bias)
         zm = fmaxf(zm, zs[mt][rh]);
       }
-    zm = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, 4));
-    zm = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, 8));
-    zm = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, 16));
     constexpr float kUnscale = 1.0f / (float)(1 << kq_exp<KB>());
-    zm = live ? fmaf(zm, kUnscale, bias) : -INFINITY;
-    const bool resc = zm > m_used[nt] + kLazyRescale;
-    float alpha = 1.0f;
-    if (resc) {
-      alpha = ex2(m_used[nt] - zm);  // 0 when m_used is -inf
+    // The running maximum moves only when a logit exceeds it by 2^8, which is
+    // rare after a stream's first group: test this lane's 4 logits and take
+    // the group maximum (shuffles) only when some lane of the warp needs it.
+    const bool need = live && fmaf(zm, kUnscale, bias) > m_used[nt] + kLazyRescale;
+    if (__any_sync(0xffffffffu, need)) {
+      zm = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, 4));
+      zm = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, 8));
+      zm = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, 16));
+      zm = live ? fmaf(zm, kUnscale, bias) : -INFINITY;
+      const bool resc = zm > m_used[nt] + kLazyRescale;
+      float alpha = 1.0f;
+      if (resc) {
+        alpha = ex2(m_used[nt] - zm);  // 0 when m_used is -inf
 #pragma unroll
-      for (int j = 0; j < kNVG; ++j) macc[nt][j] *= alpha;
-      lsum[nt] *= alpha;
-      m_used[nt] = zm;
-    }
-    if constexpr (JC) {
-      // this lane's O columns belong to head tq >> 1
-      if (__any_sync(0xffffffffu, resc)) {
+        for (int j = 0; j < kNVG; ++j) macc[nt][j] *= alpha;
+        lsum[nt] *= alpha;
+        m_used[nt] = zm;
+      }
+      if constexpr (JC) {
+        // this lane's O columns belong to head tq >> 1
         const float a_o = __shfl_sync(0xffffffffu, alpha, (lane & ~3) | (tq >> 1));
 #pragma unroll
         for (int mc = 0; mc < 8; ++mc)
 #pragma unroll
           for (int k = 0; k < 4; ++k) O[mc][nt][k] *= a_o;
+      } else if (resc) {
+#pragma unroll
+        for (int mc = 0; mc < 8; ++mc)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) O[mc][nt][k] *= alpha;
       }
-    } else if (resc) {
-#pragma unroll
-      for (int mc = 0; mc < 8; ++mc)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) O[mc][nt][k] *= alpha;
     }
     const float bm = live ? bias - m_used[nt] : -INFINITY;
     float ps = 0.0f;
@@ -513,8 +518,8 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
       for (int j = 0; j < (JC ? 1 : kNVG); ++j) {
         const int jv = JC ? ((gq >> 1) & 1) : j;
         const float4 sv = *reinterpret_cast<const float4*>(&sm.vsc[w][jv][16 * kt + 4 * tq]);
-        bp[nt][j][0] = split_pack(v0 * sv.x, v1 * sv.y, lo_sel);
-        bp[nt][j][1] = split_pack(v2 * sv.z, v3 * sv.w, lo_sel);
+        bp[nt][j][0] = split_pack(__fmul2_rn(make_float2(v0, v1), make_float2(sv.x, sv.y)), lo_sel);
+        bp[nt][j][1] = split_pack(__fmul2_rn(make_float2(v2, v3), make_float2(sv.z, sv.w)), lo_sel);
       }
     }
     // V code fragments via ldmatrix.trans on the packed (swizzled) rows
@@ -726,7 +731,7 @@ __device__ __forceinline__ void process_f16(const MmaWarpSmem<NT>& sm, const uns
   for (int nt = 0; nt < NT; ++nt) {
     const float v0 = __shfl_sync(0xffffffffu, P[nt], src0);
     const float v1 = __shfl_sync(0xffffffffu, P[nt], src0 + 4);
-    bp[nt] = split_pack(v0, v1, lo_sel);
+    bp[nt] = split_pack(make_float2(v0, v1), lo_sel);
   }
   const uint32_t vbase = smem_u32(st + F16Geom::VC);
 #pragma unroll
