@@ -300,6 +300,25 @@ __device__ __forceinline__ int qb_first_channel(int lane) {
   return KB == 8 ? 4 * lane : KB == 4 ? 8 * (lane >> 1) + 2 * (lane & 1) : 16 * (lane >> 2) + 2 * (lane & 3);
 }
 
+// The query of a stream sits in shared memory permuted so that lane L reads
+// its four Q'-build channels (c0, c0 + D, c0 + 1, c0 + D + 1) as one float4
+// at 4L: position of channel c.
+template <int KB>
+__device__ __forceinline__ int qb_perm_pos(int c) {
+  constexpr int D = qb_pair_dist<KB>();
+  int L, c0;
+  if (KB == 8) {
+    L = c >> 2;
+  } else if (KB == 4) {
+    L = 2 * (c >> 3) + ((c >> 1) & 1);
+  } else {
+    L = 4 * (c >> 4) + ((c >> 1) & 3);
+  }
+  c0 = qb_first_channel<KB>(L);
+  const int rel = c - c0;  // 0, 1, D or D + 1
+  return 4 * L + (rel >= D ? 1 : 0) + 2 * (rel & 1);
+}
+
 // One 32-token group for one warp: Q' fragments, S = K Q' (2 m-tiles x NT
 // n-tiles), online softmax, O += V^T P' (8 m-tiles x NT).
 //
@@ -326,7 +345,9 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
                           unpack_min_scale(w23.y)};
     // channels c0, c0 + D share the power-of-two multiplier (same c & 3 class), as do c0 + 1, c0 + D + 1
     const float me = kq_mult<KB>(c0 & 3), mo = kq_mult<KB>((c0 + 1) & 3);
-    const float sk[4] = {ms[0].y * me, ms[1].y * mo, ms[2].y * me, ms[3].y * mo};
+    // pairs A = (c0, c0 + D) -> B-word 2s, B = (c0 + 1, c0 + D + 1) -> B-word 2s + 1
+    const float2 skA = make_float2(ms[0].y * me, ms[2].y * me), skB = make_float2(ms[1].y * mo, ms[3].y * mo);
+    const float2 mnA = make_float2(ms[0].x, ms[2].x), mnB = make_float2(ms[1].x, ms[3].x);
     const int tsl = lane >> 3;                                        // reader thread-in-group of these channels
     const int wofs = (8 * (lane & 7)) ^ (((tsl >> 1) & 1) << 4);      // words 2s, 2s+1 in the (swizzled) hi row
     float bpart[GT];                                                  // this lane's share of each head's bias
@@ -336,18 +357,19 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
       if (r >= g) continue;
       unsigned char* dhi = reinterpret_cast<unsigned char*>(&sm.bq[w][r >> 2][8 * (r & 3) + tsl][0]);
       unsigned char* dlo = dhi + 4 * 64;
-      const float2 q01 = *reinterpret_cast<const float2*>(&qw[r][c0]);
-      const float2 q23 = *reinterpret_cast<const float2*>(&qw[r][c0 + D]);
-      const float qp0 = q01.x * sk[0], qp1 = q01.y * sk[1], qp2 = q23.x * sk[2], qp3 = q23.y * sk[3];
-      const __half2 hA = __floats2half2_rn(qp0, qp2), hB = __floats2half2_rn(qp1, qp3);
-      const float2 fA = __half22float2(hA), fB = __half22float2(hB);
-      const __half2 lA = __floats2half2_rn(qp0 - fA.x, qp2 - fA.y), lB = __floats2half2_rn(qp1 - fB.x, qp3 - fB.y);
+      const float4 q4 = *reinterpret_cast<const float4*>(&qw[r][4 * lane]);  // (c0, c0+D, c0+1, c0+D+1)
+      const float2 qA = make_float2(q4.x, q4.y), qB = make_float2(q4.z, q4.w);
+      const float2 pA = __fmul2_rn(qA, skA), pB = __fmul2_rn(qB, skB);
+      const __half2 hA = __floats2half2_rn(pA.x, pA.y), hB = __floats2half2_rn(pB.x, pB.y);
+      const float2 m1 = make_float2(-1.0f, -1.0f);
+      const float2 rA = __ffma2_rn(m1, __half22float2(hA), pA), rB = __ffma2_rn(m1, __half22float2(hB), pB);
+      const __half2 lA = __floats2half2_rn(rA.x, rA.y), lB = __floats2half2_rn(rB.x, rB.y);
       *reinterpret_cast<uint2*>(dhi + wofs) = make_uint2(h2_as_u32(hA), h2_as_u32(hB));
       *reinterpret_cast<uint2*>(dlo + (wofs ^ 32)) = make_uint2(h2_as_u32(lA), h2_as_u32(lB));
-      const float bp = fmaf(q01.x, ms[0].x, fmaf(q01.y, ms[1].x, fmaf(q23.x, ms[2].x, q23.y * ms[3].x)));
-      const float off = (qp0 + qp1) + (qp2 + qp3);  // hi + lo = qp to ~2^-22
+      const float2 b2 = __ffma2_rn(qA, mnA, __fmul2_rn(qB, mnB));
+      const float2 o2 = __fadd2_rn(pA, pB);  // hi + lo = qp to ~2^-22
       // the mma's constant part 1024 * sum_c (hi + lo), in logit units
-      bpart[r] = fmaf(-1024.0f * (1.0f / (float)(1 << kq_exp<KB>())), off, bp);
+      bpart[r] = fmaf(-1024.0f * (1.0f / (float)(1 << kq_exp<KB>())), o2.x + o2.y, b2.x + b2.y);
     }
     // all heads' biases with one reduce-scatter over the warp
     const float bsum = reduce_heads<GT>(bpart, lane);
@@ -635,7 +657,7 @@ __device__ __forceinline__ void issue_f16(const DecodeParams& p, int s, int kk0,
 // per head.  Slot order: thread tq of the k dimension owns the 16-byte K
 // chunks tq, tq+4, tq+8, tq+12 (channels 8 * chunk ..); k-step s = 2i + h
 // takes channels 8(tq + 4i) + 4h + {0, 1} (lo pair) and + {2, 3} (hi pair).
-template <int NT>
+template <int NT, int KBQ>
 __device__ __forceinline__ void build_bq_f16(const float (*qw)[kHeadDim], MmaWarpSmem<NT>& sm, int g, int w,
                                              int lane) {
   const int tqr = (lane >> 1) & 3;                 // reader thread-in-group of channels 4*lane ..
@@ -646,8 +668,9 @@ __device__ __forceinline__ void build_bq_f16(const float (*qw)[kHeadDim], MmaWar
     if (r >= g) break;
     unsigned char* dhi = reinterpret_cast<unsigned char*>(&sm.bq[w][r >> 2][8 * (r & 3) + tqr][0]);
     unsigned char* dlo = dhi + 4 * 64;
-    const float4 q4 = *reinterpret_cast<const float4*>(&qw[r][4 * lane]);
-    const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+    float qv[4];  // channels 4*lane + k of the permuted query
+#pragma unroll
+    for (int k = 0; k < 4; ++k) qv[k] = qw[r][qb_perm_pos<KBQ>(4 * lane + k)];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int byte = 2 * (4 * sstep + k);

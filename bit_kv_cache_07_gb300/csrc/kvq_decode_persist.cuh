@@ -336,19 +336,23 @@ __global__ void __launch_bounds__(kThreads, (PersistLayout<KB, VB, NT, GT>::kMin
     if (s != cur_s) {
       if (cur_s >= 0) finish(cur_s);
       cur_s = s;
-      // this stream's query heads (scaled, fp32) into this warp's buffer
+      // this stream's query heads (scaled, fp32) into this warp's buffer, in
+      // the Q'-build order (qb_perm_pos): lane L's channels c0, c0 + D, c0 + 1,
+      // c0 + D + 1 (two adjacent pairs in global memory)
       const int b = s / G.Hkv, hk = s - b * G.Hkv;
+      constexpr int D = qb_pair_dist<KBq>();
+      const int c0 = qb_first_channel<KBq>(lane);
       __syncwarp();
-      for (int idx = lane; idx < GT * kHeadDim / 4; idx += 32) {
-        const int r = idx / (kHeadDim / 4), c4 = idx % (kHeadDim / 4);
+#pragma unroll
+      for (int r = 0; r < GT; ++r) {
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (r < g) {
-          const uint2 u =
-              __ldg(reinterpret_cast<const uint2*>(p.q + ((size_t)b * G.Hq + hk * g + r) * kHeadDim) + c4);
-          const float2 a = __half22float2(u32_as_h2(u.x)), c2 = __half22float2(u32_as_h2(u.y));
-          v = make_float4(a.x * p.q_scale, a.y * p.q_scale, c2.x * p.q_scale, c2.y * p.q_scale);
+          const uint16_t* qr = p.q + ((size_t)b * G.Hq + hk * g + r) * kHeadDim;
+          const float2 a = __half22float2(u32_as_h2(__ldg(reinterpret_cast<const uint32_t*>(qr + c0))));
+          const float2 c2 = __half22float2(u32_as_h2(__ldg(reinterpret_cast<const uint32_t*>(qr + c0 + D))));
+          v = make_float4(a.x * p.q_scale, c2.x * p.q_scale, a.y * p.q_scale, c2.y * p.q_scale);
         }
-        *reinterpret_cast<float4*>(&qw[r][4 * c4]) = v;
+        *reinterpret_cast<float4*>(&qw[r][4 * lane]) = v;
       }
       __syncwarp();
     }
@@ -362,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, (PersistLayout<KB, VB, NT, GT>::kMin
       }
     } else {
       if (!bq_f16) {
-        build_bq_f16<NT>(qw, sm, g, w, lane);  // the query's last use: sO may now overwrite it
+        build_bq_f16<NT, KBq>(qw, sm, g, w, lane);  // the query's last use: sO may now overwrite it
         bq_f16 = true;
         __syncwarp();
         if (has_q) {
