@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, (PersistLayout<KB, VB, NT, GT>::kMin
   const int n_items = p.n_items, ng = LY::kQuant ? p.ng : 0;
   const int k1 = p.S_eff + p.W;  // fp16 tokens of a stream
   // current item (s, k) and the next item to queue (is, ik, ij); all advance incrementally
-  int s = (int)(j0 / n_items);
+  int s = (int)idiv(j0, n_items, p.fd_n_items);
   int k = (int)(j0 - (long long)s * n_items);
   int is = s, ik = k;
   long long ij = j0;

@@ -61,12 +61,15 @@ cudaError_t plan_persist(DecodeParams& p, uint64_t* ws_need) {
   if (nw > p.wtot / wmax) nw = p.wtot / wmax;
   if (nw < 1) nw = 1;
   p.nwarps = (int)nw;
-  p.inv_n_items = 1.0 / (double)p.n_items;
-  p.inv_wq = 1.0 / (double)p.wq;
-  p.inv_wt = 1.0 / (double)p.wt;
-  p.inv_wstream = 1.0 / (double)p.wstream;
-  p.inv_wtot = 1.0 / (double)p.wtot;
-  p.inv_nwarps = 1.0 / (double)p.nwarps;
+  // the schedule's dividends stay below (wtot + 1) (nwarps + 1)
+  if ((unsigned __int128)(p.wtot + 1) * (unsigned __int128)(p.nwarps + 1) >= (unsigned __int128)kFastDivLimit)
+    return cudaErrorInvalidValue;
+  p.fd_n_items = make_fastdiv(p.n_items);
+  p.fd_wq = make_fastdiv(p.wq);
+  p.fd_wt = make_fastdiv(p.wt);
+  p.fd_wstream = make_fastdiv(p.wstream);
+  p.fd_wtot = make_fastdiv(p.wtot);
+  p.fd_nwarps = make_fastdiv(p.nwarps);
   const uint64_t slots = (uint64_t)p.nwarps + G.NS;
   const uint64_t cnt = ((uint64_t)G.NS * 4 + 255) / 256 * 256;
   const uint64_t ml = (slots * G.g * 2 * 4 + 255) / 256 * 256;

@@ -61,6 +61,37 @@ struct AppendParams {
   float v_lut[8];
 };
 
+// Division by a divisor that is fixed for a launch, without a hardware
+// divide: floor(x / d) = (x * m) >> sh for 0 <= x < 2^56, where
+// sh = 56 + ceil(log2 d) and m = ceil(2^sh / d) (< 2^57).  Writing
+// m = (2^sh + e) / d with 0 <= e < d <= 2^(sh - 56), the product is
+// x / d + x e / (d 2^sh) and x e < 2^sh keeps the excess below 1 / d, which
+// is less than the distance from x / d to the next integer: the floor is
+// exact.  (Round-up reciprocal multiplication, Granlund and Montgomery,
+// "Division by invariant integers using multiplication", 1994.)
+struct FastDiv {
+  unsigned long long m;
+  int sh;
+};
+inline FastDiv make_fastdiv(long long d) {  // host; d >= 1
+  int l = 0;
+  while ((1ull << l) < (unsigned long long)d) ++l;
+  const int sh = 56 + l;
+  const unsigned __int128 num = (unsigned __int128)1 << sh;
+  return FastDiv{(unsigned long long)((num + (unsigned __int128)(d - 1)) / (unsigned __int128)d), sh};
+}
+__host__ __device__ inline long long fastdiv_mulshift(long long x, const FastDiv& f) {
+  const unsigned long long ux = (unsigned long long)x;
+#ifdef __CUDA_ARCH__
+  const unsigned long long hi = __umul64hi(ux, f.m), lo = ux * f.m;
+#else
+  const unsigned __int128 pr = (unsigned __int128)ux * f.m;
+  const unsigned long long hi = (unsigned long long)(pr >> 64), lo = (unsigned long long)pr;
+#endif
+  return (long long)(f.sh >= 64 ? hi >> (f.sh - 64) : (hi << (64 - f.sh)) | (lo >> f.sh));
+}
+constexpr long long kFastDivLimit = 1ll << 56;  // dividends must stay below this
+
 struct DecodeParams {
   Geometry geo;
   LayerPtrs L;
@@ -89,50 +120,43 @@ struct DecodeParams {
   int ng, nt, n_items;
   int nwarps;
   long long wq, wt, wstream, wtot;
-  double inv_n_items, inv_wq, inv_wt, inv_wstream, inv_wtot, inv_nwarps;  // 1 / x, for idiv
+  FastDiv fd_n_items, fd_wq, fd_wt, fd_wstream, fd_wtot, fd_nwarps;  // for idiv
 };
 
-// floor(x / d) for 0 <= x < 2^52 and d >= 1, given inv = 1.0 / d in fp64.
-// On the device one fp64 multiply and one correction step replace the long,
-// serial emulation of a 64-bit integer division (the estimate is off by at
-// most one); the host divides exactly.
-__host__ __device__ inline long long idiv_recip(long long x, long long d, double inv) {
-  long long q = (long long)((double)x * inv);
-  const long long r = x - q * d;
-  if (r < 0) --q;
-  else if (r >= d) ++q;
-  return q;
-}
-__host__ __device__ inline long long idiv(long long x, long long d, double inv) {
+// floor(x / d) for 0 <= x < 2^56: the device multiplies and shifts (a
+// 64-bit integer division is a long serial emulation there, and fp64 is a
+// narrow pipe on this GPU); the host divides exactly.
+__host__ __device__ inline long long idiv(long long x, long long d, const FastDiv& f) {
 #ifdef __CUDA_ARCH__
-  return idiv_recip(x, d, inv);
+  (void)d;
+  return fastdiv_mulshift(x, f);
 #else
-  (void)inv;
+  (void)f;
   return x / d;
 #endif
 }
 
 // Persistent-schedule arithmetic shared by host and device.
-// (Operands stay below 2^52: wtot is at most the layer's bytes, nwarps a few thousand.)
+// (Dividends stay below 2^56: plan_persist checks (wtot + 1) (nwarps + 1) < 2^56.)
 __host__ __device__ inline long long item_pos(const DecodeParams& p, long long j) {
-  const long long s = idiv(j, p.n_items, p.inv_n_items), k = j - s * p.n_items;
+  const long long s = idiv(j, p.n_items, p.fd_n_items), k = j - s * p.n_items;
   return s * p.wstream + (k <= p.ng ? k * p.wq : p.ng * p.wq + (k - p.ng) * p.wt);
 }
 // First item whose start weight is >= x (x in [0, wtot]).
 __host__ __device__ inline long long first_item_at(const DecodeParams& p, long long x) {
-  long long s = idiv(x, p.wstream, p.inv_wstream), rem = x - s * p.wstream, k;
+  long long s = idiv(x, p.wstream, p.fd_wstream), rem = x - s * p.wstream, k;
   if (rem == 0) return s * p.n_items;
-  if (rem <= p.ng * p.wq) k = idiv(rem + p.wq - 1, p.wq, p.inv_wq);
-  else k = p.ng + idiv(rem - p.ng * p.wq + p.wt - 1, p.wt, p.inv_wt);
+  if (rem <= p.ng * p.wq) k = idiv(rem + p.wq - 1, p.wq, p.fd_wq);
+  else k = p.ng + idiv(rem - p.ng * p.wq + p.wt - 1, p.wt, p.fd_wt);
   if (k >= p.n_items) return (s + 1) * p.n_items;
   return s * p.n_items + k;
 }
 // Warp i covers weight [x_i, x_{i+1}), x_i = floor(i * wtot / nwarps).
 __host__ __device__ inline long long warp_x(const DecodeParams& p, long long i) {
-  return idiv(i * p.wtot, p.nwarps, p.inv_nwarps);
+  return idiv(i * p.wtot, p.nwarps, p.fd_nwarps);
 }
 __host__ __device__ inline int owner_of(const DecodeParams& p, long long pos) {
-  return (int)(idiv((pos + 1) * p.nwarps + p.wtot - 1, p.wtot, p.inv_wtot) - 1);
+  return (int)(idiv((pos + 1) * p.nwarps + p.wtot - 1, p.wtot, p.fd_wtot) - 1);
 }
 
 // ------------------------------------------------------------ host hooks

@@ -1,9 +1,9 @@
 // Host-side check of the persistent decode's work schedule: every item has
 // exactly one owner warp, no warp range is empty under the launch cap, the
 // owner formula agrees with the ranges, and the (warp, stream) slots are
-// distinct and in bounds.  Also checks the device's reciprocal division
-// (idiv_recip) against exact integer division.  Built and run by
-// test_schedule_host.py.
+// distinct and in bounds.  Also checks the device's division by a launch
+// constant (fastdiv_mulshift: multiply by a rounded-up reciprocal, shift)
+// against exact integer division.  Built and run by test_schedule_host.py.
 #include "../bit_kv_cache_07_gb300/csrc/kvq_internal.cuh"
 #include <cstdio>
 #include <set>
@@ -40,19 +40,29 @@ int main() {
       }
     }
   }
-  // reciprocal division: exact for 0 <= x < 2^52
+  // multiply-shift division: exact for 0 <= x < 2^56, any d >= 1
   unsigned long long st = 88172645463325252ull;
   auto rnd = [&]() { st ^= st << 13; st ^= st >> 7; st ^= st << 17; return st; };
-  for (int i = 0; i < 2000000; ++i) {
-    const long long d = (long long)(rnd() % ((i & 1) ? 5000ull : (1ull << 40))) + 1;
-    long long x = (long long)(rnd() % (1ull << 52));
-    if (i % 3 == 0) x = (x / d) * d;                      // exact multiples
-    if (i % 3 == 1 && (x / d) * d > 0) x = (x / d) * d - 1;  // just below one
+  auto check = [&](long long x, long long d) {
     ++cases;
-    if (idiv_recip(x, d, 1.0 / (double)d) != x / d) {
-      if (bad < 10) printf("idiv_recip(%lld, %lld) wrong\n", x, d);
+    if (fastdiv_mulshift(x, make_fastdiv(d)) != x / d) {
+      if (bad < 10) printf("fastdiv(%lld, %lld) wrong\n", x, d);
       ++bad;
     }
+  };
+  for (long long d = 1; d <= 300; ++d)  // every small divisor at the ends of the range
+    for (long long x : {0LL, 1LL, d - 1, d, d + 1, kFastDivLimit - 1, kFastDivLimit - 1 - (kFastDivLimit - 1) % d,
+                        kFastDivLimit - 2 - (kFastDivLimit - 1) % d})
+      if (x >= 0) check(x, d);
+  for (int e = 0; e < 48; ++e)  // powers of two and their neighbours
+    for (long long d : {(1LL << e) - 1, 1LL << e, (1LL << e) + 1})
+      if (d >= 1) { check(kFastDivLimit - 1, d); check((kFastDivLimit - 1) / d * d, d); check((kFastDivLimit - 1) / d * d - 1, d); }
+  for (int i = 0; i < 2000000; ++i) {
+    const long long d = (long long)(rnd() % ((i & 1) ? 5000ull : (1ull << 40))) + 1;
+    long long x = (long long)(rnd() % (unsigned long long)kFastDivLimit);
+    if (i % 3 == 0) x = (x / d) * d;                      // exact multiples
+    if (i % 3 == 1 && (x / d) * d > 0) x = (x / d) * d - 1;  // just below one
+    check(x, d);
   }
   printf("cases %d bad %d\n", cases, bad);
   return bad != 0;
