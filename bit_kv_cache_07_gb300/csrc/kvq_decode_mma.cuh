@@ -191,7 +191,7 @@ struct StageGeom {
   static constexpr int BYTES = ((VS + kGroupTokens * kNVG * 4) + 127) / 128 * 128;
 };
 
-// Per-warp scratch of the group processing (4 warps per CTA).
+// Per-warp scratch of the group processing:
 //  bq:  each lane's B fragments of Q' (32 halves = one 64-byte row per lane,
 //       chunks swizzled like a 64-byte code row)
 //  vsc/vmn: V scale / min of the group's tokens in fp32, ordered so that
@@ -200,10 +200,10 @@ struct StageGeom {
 //       vmn[j][gq][4]     holds tokens gq + {0, 8, 16, 24}     (softmax rows)
 template <int NT>
 struct MmaWarpSmem {
-  alignas(128) uint16_t bq[4][NT][32][32];
-  alignas(16) float bias[4][8 * NT];
-  alignas(16) float vsc[4][kNVG][kGroupTokens];
-  alignas(16) float vmn[4][kNVG][kGroupTokens];
+  alignas(128) uint16_t bq[NT][32][32];
+  alignas(16) float bias[8 * NT];
+  alignas(16) float vsc[kNVG][kGroupTokens];
+  alignas(16) float vmn[kNVG][kGroupTokens];
 };
 
 __device__ __forceinline__ int vsc_index(int t) {  // token -> slot in vsc[j][..]
@@ -328,7 +328,7 @@ __device__ __forceinline__ int qb_perm_pos(int c) {
 // columns of the other group are then unused (see stage_quant).
 template <int KB, int VB, int NT, bool JC, int GT>
 __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWarpSmem<NT>& sm,
-                                              const unsigned char* st, int g, int w, int lane,
+                                              const unsigned char* st, int g, int lane,
                                               float (&O)[8][NT][4], float (&macc)[NT][kNVG], float (&m_used)[NT],
                                               float (&lsum)[NT]) {
   using SG = StageGeom<KB, VB>;
@@ -355,7 +355,7 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
     for (int r = 0; r < GT; ++r) {
       bpart[r] = 0.0f;
       if (r >= g) continue;
-      unsigned char* dhi = reinterpret_cast<unsigned char*>(&sm.bq[w][r >> 2][8 * (r & 3) + tsl][0]);
+      unsigned char* dhi = reinterpret_cast<unsigned char*>(&sm.bq[r >> 2][8 * (r & 3) + tsl][0]);
       unsigned char* dlo = dhi + 4 * 64;
       const float4 q4 = *reinterpret_cast<const float4*>(&qw[r][4 * lane]);  // (c0, c0+D, c0+1, c0+D+1)
       const float2 qA = make_float2(q4.x, q4.y), qB = make_float2(q4.z, q4.w);
@@ -374,15 +374,15 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
     // all heads' biases with one reduce-scatter over the warp
     const float bsum = reduce_heads<GT>(bpart, lane);
     const int hb = head_of_lane<GT>(lane);
-    if ((lane & rest_mask<GT>()) == 0 && hb < g) sm.bias[w][hb] = bsum;
+    if ((lane & rest_mask<GT>()) == 0 && hb < g) sm.bias[hb] = bsum;
     const uint32_t* vsw = reinterpret_cast<const uint32_t*>(st + SG::VS);
     const int iv = vsc_index(lane), im = vmn_index(lane);
     constexpr float kVCentre = (float)(1 << (VB - 1));  // the V codes enter the mma centred
 #pragma unroll
     for (int j = 0; j < kNVG; ++j) {
       const float2 m2 = unpack_min_scale(vsw[lane * kNVG + j]);
-      sm.vmn[w][j][im] = fmaf(kVCentre, m2.y, m2.x);
-      sm.vsc[w][j][iv] = m2.y;
+      sm.vmn[j][im] = fmaf(kVCentre, m2.y, m2.x);
+      sm.vsc[j][iv] = m2.y;
     }
   }
   __syncwarp();
@@ -391,7 +391,7 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
   uint32_t bq[NT][16];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const unsigned char* row = reinterpret_cast<const unsigned char*>(&sm.bq[w][nt][lane][0]);
+    const unsigned char* row = reinterpret_cast<const unsigned char*>(&sm.bq[nt][lane][0]);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const uint4 u = *reinterpret_cast<const uint4*>(row + 16 * (c ^ ((lane >> 1) & 3)));
@@ -460,7 +460,7 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
   for (int nt = 0; nt < NT; ++nt) {
     const int h = 4 * nt + tq;
     const bool live = h < g;
-    const float bias = live ? sm.bias[w][h] : 0.0f;
+    const float bias = live ? sm.bias[h] : 0.0f;
     float zs[2][2];
     float zm = -INFINITY;
 #pragma unroll
@@ -516,7 +516,7 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
       }
 #pragma unroll
     for (int j = 0; j < kNVG; ++j) {
-      const float4 mn = *reinterpret_cast<const float4*>(&sm.vmn[w][j][4 * gq]);  // tokens gq + 8i
+      const float4 mn = *reinterpret_cast<const float4*>(&sm.vmn[j][4 * gq]);  // tokens gq + 8i
       macc[nt][j] = fmaf(pv[0], mn.x, fmaf(pv[1], mn.y, fmaf(pv[2], mn.z, fmaf(pv[3], mn.w, macc[nt][j]))));
     }
     lsum[nt] += ps;
@@ -539,7 +539,7 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
 #pragma unroll
       for (int j = 0; j < (JC ? 1 : kNVG); ++j) {
         const int jv = JC ? ((gq >> 1) & 1) : j;
-        const float4 sv = *reinterpret_cast<const float4*>(&sm.vsc[w][jv][16 * kt + 4 * tq]);
+        const float4 sv = *reinterpret_cast<const float4*>(&sm.vsc[jv][16 * kt + 4 * tq]);
         bp[nt][j][0] = split_pack(__fmul2_rn(make_float2(v0, v1), make_float2(sv.x, sv.y)), lo_sel);
         bp[nt][j][1] = split_pack(__fmul2_rn(make_float2(v2, v3), make_float2(sv.z, sv.w)), lo_sel);
       }
@@ -658,7 +658,7 @@ __device__ __forceinline__ void issue_f16(const DecodeParams& p, int s, int kk0,
 // chunks tq, tq+4, tq+8, tq+12 (channels 8 * chunk ..); k-step s = 2i + h
 // takes channels 8(tq + 4i) + 4h + {0, 1} (lo pair) and + {2, 3} (hi pair).
 template <int NT, int KBQ>
-__device__ __forceinline__ void build_bq_f16(const float (*qw)[kHeadDim], MmaWarpSmem<NT>& sm, int g, int w,
+__device__ __forceinline__ void build_bq_f16(const float (*qw)[kHeadDim], MmaWarpSmem<NT>& sm, int g,
                                              int lane) {
   const int tqr = (lane >> 1) & 3;                 // reader thread-in-group of channels 4*lane ..
   const int sstep = 2 * (lane >> 3) + (lane & 1);  // their k-step
@@ -666,7 +666,7 @@ __device__ __forceinline__ void build_bq_f16(const float (*qw)[kHeadDim], MmaWar
 #pragma unroll
   for (int r = 0; r < 8 * NT; ++r) {
     if (r >= g) break;
-    unsigned char* dhi = reinterpret_cast<unsigned char*>(&sm.bq[w][r >> 2][8 * (r & 3) + tqr][0]);
+    unsigned char* dhi = reinterpret_cast<unsigned char*>(&sm.bq[r >> 2][8 * (r & 3) + tqr][0]);
     unsigned char* dlo = dhi + 4 * 64;
     float qv[4];  // channels 4*lane + k of the permuted query
 #pragma unroll
@@ -687,14 +687,14 @@ __device__ __forceinline__ void build_bq_f16(const float (*qw)[kHeadDim], MmaWar
 // O here is the plain-domain accumulator (standard channel order: row gq of
 // m-tile mc is channel 16 mc + gq).
 template <int NT>
-__device__ __forceinline__ void process_f16(const MmaWarpSmem<NT>& sm, const unsigned char* st, int g, int w,
-                                            int lane, int kk0, int k1, float (&O)[8][NT][4],
+__device__ __forceinline__ void process_f16(const MmaWarpSmem<NT>& sm, const unsigned char* st, int g, int lane,
+                                            int kk0, int k1, float (&O)[8][NT][4],
                                             float (&m_used)[NT], float (&lsum)[NT]) {
   const int gq = lane >> 2, tq = lane & 3;
   uint32_t bq[NT][16];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const unsigned char* row = reinterpret_cast<const unsigned char*>(&sm.bq[w][nt][lane][0]);
+    const unsigned char* row = reinterpret_cast<const unsigned char*>(&sm.bq[nt][lane][0]);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const uint4 u = *reinterpret_cast<const uint4*>(row + 16 * (c ^ ((lane >> 1) & 3)));

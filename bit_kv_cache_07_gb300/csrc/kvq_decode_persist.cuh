@@ -37,21 +37,29 @@ template <int KB, int VB, int NT, int GT>
 struct PersistLayout {
   static constexpr bool kQuant = KB != 16;
   static constexpr int kStages = 2;  // per-warp pipeline depth (items)
-  static constexpr int kFixed = (int)((sizeof(MmaWarpSmem<NT>) + 127) / 128 * 128);
+  static constexpr int r128(int x) { return (x + 127) / 128 * 128; }
+  static constexpr int kSmem = r128((int)sizeof(MmaWarpSmem<NT>));
   static constexpr int kQBytes = kQuant ? StageGeom<KB, VB>::BYTES : 0;
   static constexpr int kStageBytes = kQBytes > F16Geom::BYTES ? kQBytes : F16Geom::BYTES;
   static constexpr int kPerWarpStages = kStages * kStageBytes;
-  static constexpr int r128(int x) { return (x + 127) / 128 * 128; }
   // this warp's stream's query; once the query is no longer needed (the
   // stream's Q' and fp16 fragments are built) the same bytes hold the
   // staged O[h][c], and the group-bias scratch holds the staged (m, l)
   static constexpr int kPerWarpQ = r128(GT * kHeadDim * 4);
-  static constexpr int kPerWarp = kPerWarpStages + kPerWarpQ;
-  static constexpr int kBytes = kFixed + 4 * kPerWarp;
-  // resident CTAs the registers are budgeted for: single-head groups get 4
-  // (128 registers) when 4 CTAs fit in 228 KB (1 KB reserved each); larger
-  // groups keep 168 registers (3 CTAs) -- measured faster than 4 CTAs at 128
-  static constexpr int kMinCtas = NT == 2 ? 2 : (GT == 1 && 4 * (kBytes + 1024) <= 228 * 1024 ? 4 : 3);
+  // a warp's region: scratch, pipeline stages, query
+  static constexpr int kPerWarp = kSmem + kPerWarpStages + kPerWarpQ;
+  // One CTA per SM holds all of the SM's warps (with several CTAs per SM the
+  // warp schedulers favour the earlier CTAs, whose warps then finish their
+  // equal shares well before the others).  Warps per SM as measured best:
+  // 16 at 128 registers for single-head groups, 12 at 168 for 2-4 heads,
+  // 8 at 255 for 5-8 heads; fewer when their shared memory would exceed a
+  // CTA's 227 KB.
+  static constexpr int kWantWarps = NT == 2 ? 8 : (GT == 1 ? 16 : 12);
+  static constexpr int kMaxCtaSmem = 227 * 1024;
+  static constexpr int kWarps = kWantWarps * kPerWarp <= kMaxCtaSmem ? kWantWarps : kMaxCtaSmem / kPerWarp;
+  static constexpr int kCtaThreads = 32 * kWarps;
+  static constexpr int kBytes = kWarps * kPerWarp;
+  static_assert(kWarps >= 1, "one warp's region must fit in a CTA");
 };
 
 // Fold the quantized accumulators into the staging buffer: sO[h][c] = the
@@ -190,43 +198,51 @@ __device__ __forceinline__ void finalize_stream(const DecodeParams& p, int slot,
   if (prev != (unsigned)(count - 1)) return;
   __threadfence();
   // last piece of stream s: merge its slots wf + s .. wf + s + count - 1.
-  // The slots' (m, l) are read by one lane each (all loads in flight at
-  // once); the accumulators in batches of 4 slots.
+  // Lane q reads slot q's (m, l); the first kMB slots' accumulators are read
+  // in the same round trip (4 channels per lane), later ones kMB at a time.
+  constexpr int kMB = 8;
   const int b = s / G.Hkv, hk = s % G.Hkv;
   const size_t slot0 = (size_t)(wf + s);
   for (int r = 0; r < g; ++r) {
-    float M = -INFINITY;
-    for (int q0 = lane; q0 < count; q0 += 32) M = fmaxf(M, __ldcg(&p.part_ml[((slot0 + q0) * g + r) * 2]));
+    auto acc_at = [&](int q) {
+      return __ldcg(reinterpret_cast<const float4*>(&p.part_acc[((slot0 + q) * g + r) * kHeadDim + 4 * lane]));
+    };
+    float mq = -INFINITY, lq = 0.0f;
+    if (lane < count) {
+      mq = __ldcg(&p.part_ml[((slot0 + lane) * g + r) * 2]);
+      lq = __ldcg(&p.part_ml[((slot0 + lane) * g + r) * 2 + 1]);
+    }
+    float4 a[kMB];
+#pragma unroll
+    for (int u = 0; u < kMB; ++u) a[u] = u < count ? acc_at(u) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float M = mq;
+    for (int q0 = lane + 32; q0 < count; q0 += 32) M = fmaxf(M, __ldcg(&p.part_ml[((slot0 + q0) * g + r) * 2]));
     M = warp_max(M);
     float L = 0.0f, v[4] = {0, 0, 0, 0};
     for (int c0 = 0; c0 < count; c0 += 32) {
       // lane q: weight of slot c0 + q
+      if (c0 > 0 && c0 + lane < count) {
+        mq = __ldcg(&p.part_ml[((slot0 + c0 + lane) * g + r) * 2]);
+        lq = __ldcg(&p.part_ml[((slot0 + c0 + lane) * g + r) * 2 + 1]);
+      }
       float e = 0.0f;
       if (c0 + lane < count) {
-        const size_t base = (slot0 + c0 + lane) * g + r;
-        const float mq = __ldcg(&p.part_ml[base * 2]);
         e = (mq == -INFINITY) ? 0.0f : exp2f(mq - M);
-        L += e * __ldcg(&p.part_ml[base * 2 + 1]);
+        L += e * lq;
       }
       const int n = min(32, count - c0);
-      for (int q = 0; q < n; q += 4) {
-        float4 a[4];
-        float eq[4];
+      for (int q = 0; q < n; q += kMB) {
+        if (c0 + q > 0) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          eq[u] = __shfl_sync(0xffffffffu, e, (q + u) & 31);
-          a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (q + u < n)
-            a[u] = __ldcg(reinterpret_cast<const float4*>(
-                &p.part_acc[((slot0 + c0 + q + u) * g + r) * kHeadDim + 4 * lane]));
+          for (int u = 0; u < kMB; ++u) a[u] = q + u < n ? acc_at(c0 + q + u) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (q + u >= n) break;
-          v[0] = fmaf(eq[u], a[u].x, v[0]);
-          v[1] = fmaf(eq[u], a[u].y, v[1]);
-          v[2] = fmaf(eq[u], a[u].z, v[2]);
-          v[3] = fmaf(eq[u], a[u].w, v[3]);
+        for (int u = 0; u < kMB; ++u) {
+          const float eq = __shfl_sync(0xffffffffu, e, (q + u) & 31);  // 0 past the last slot
+          v[0] = fmaf(eq, a[u].x, v[0]);
+          v[1] = fmaf(eq, a[u].y, v[1]);
+          v[2] = fmaf(eq, a[u].z, v[2]);
+          v[3] = fmaf(eq, a[u].w, v[3]);
         }
       }
     }
@@ -243,30 +259,24 @@ __device__ __forceinline__ void finalize_stream(const DecodeParams& p, int slot,
 }
 
 template <int KB, int VB, int NT, int GT>
-__global__ void __launch_bounds__(kThreads, (PersistLayout<KB, VB, NT, GT>::kMinCtas))
+__global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT>::kCtaThreads, 1)
     decode_persist_kernel(const __grid_constant__ DecodeParams p) {
   using LY = PersistLayout<KB, VB, NT, GT>;
   constexpr int KBq = KB == 16 ? 4 : KB, VBq = VB == 16 ? 4 : VB;  // fp16 mode: quantized helpers unused
   constexpr bool JC = NT == 1 && GT <= 2;
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  MmaWarpSmem<NT>& sm = *reinterpret_cast<MmaWarpSmem<NT>*>(smem_raw);
   const Geometry& G = p.geo;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int g = G.g;
-  unsigned char* mine = smem_raw + LY::kFixed + w * LY::kPerWarp;
-  unsigned char* st0 = mine;
+  unsigned char* mine = smem_raw + w * LY::kPerWarp;  // this warp's region; no CTA-wide sharing
+  MmaWarpSmem<NT>& sm = *reinterpret_cast<MmaWarpSmem<NT>*>(mine);
+  unsigned char* st0 = mine + LY::kSmem;
   const uint32_t st0_s = smem_u32(st0);
-  float (*qw)[kHeadDim] = reinterpret_cast<float (*)[kHeadDim]>(mine + LY::kPerWarpStages);
-  float* sO = &qw[0][0];       // staging, after the query's last use
-  float* sML = &sm.bias[w][0];  // staging (m, l): 8 * NT >= 2 * GT floats
+  float (*qw)[kHeadDim] = reinterpret_cast<float (*)[kHeadDim]>(mine + LY::kSmem + LY::kPerWarpStages);
+  float* sO = &qw[0][0];     // staging, after the query's last use
+  float* sML = &sm.bias[0];  // staging (m, l): 8 * NT >= 2 * GT floats
 
-  {
-    uint32_t* z = reinterpret_cast<uint32_t*>(&sm.bq[0][0][0][0]);
-    for (int idx = tid; idx < (int)(sizeof(sm.bq) / 4); idx += kThreads) z[idx] = 0u;
-  }
-  __syncthreads();
-
-  const int gw = blockIdx.x * 4 + w;  // global warp index
+  const int gw = blockIdx.x * LY::kWarps + w;  // global warp index
   if (gw >= p.nwarps) return;
   const long long j0 = first_item_at(p, warp_x(p, gw));
   const long long j1 = first_item_at(p, warp_x(p, gw + 1));
@@ -313,6 +323,12 @@ __global__ void __launch_bounds__(kThreads, (PersistLayout<KB, VB, NT, GT>::kMin
   };
 #pragma unroll
   for (int i = 0; i < LY::kStages - 1; ++i) issue_next(i);
+  {
+    // this warp's Q' rows start at zero (rows of absent heads stay zero)
+    uint4* z = reinterpret_cast<uint4*>(&sm.bq[0][0][0]);
+    for (int idx = lane; idx < (int)(sizeof(sm.bq) / 16); idx += 32) z[idx] = make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+  }
   int cur = 0;
   int cur_s = -1;
   bool has_q = false, staged = false, bq_f16 = false;
@@ -361,12 +377,12 @@ __global__ void __launch_bounds__(kThreads, (PersistLayout<KB, VB, NT, GT>::kMin
     const unsigned char* stc = st0 + cur * LY::kStageBytes;
     if (LY::kQuant && k < ng) {
       if constexpr (LY::kQuant) {
-        process_group<KB, VB, NT, JC, GT>(qw, sm, stc, g, w, lane, O, macc, m_used, lsum);
+        process_group<KB, VB, NT, JC, GT>(qw, sm, stc, g, lane, O, macc, m_used, lsum);
         has_q = true;
       }
     } else {
       if (!bq_f16) {
-        build_bq_f16<NT, KBq>(qw, sm, g, w, lane);  // the query's last use: sO may now overwrite it
+        build_bq_f16<NT, KBq>(qw, sm, g, lane);  // the query's last use: sO may now overwrite it
         bq_f16 = true;
         __syncwarp();
         if (has_q) {
@@ -375,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, (PersistLayout<KB, VB, NT, GT>::kMin
           staged = true;
         }
       }
-      process_f16<NT>(sm, stc, g, w, lane, kF16Tokens * (k - ng), k1, O, m_used, lsum);
+      process_f16<NT>(sm, stc, g, lane, kF16Tokens * (k - ng), k1, O, m_used, lsum);
     }
     __syncwarp();
     cur = (cur + 1 == LY::kStages) ? 0 : cur + 1;
@@ -404,14 +420,14 @@ cudaError_t launch_t(const DecodeParams& p, cudaStream_t st) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
   }
-  const int ctas = (p.nwarps + 3) / 4;
-  decode_persist_kernel<KB, VB, NT, GT><<<ctas, kThreads, smem, st>>>(p);
+  const int ctas = (p.nwarps + LY::kWarps - 1) / LY::kWarps;
+  decode_persist_kernel<KB, VB, NT, GT><<<ctas, LY::kCtaThreads, smem, st>>>(p);
   return cudaGetLastError();
 }
 
-// Resident CTAs per SM of an instantiation (for sizing the persistent grid).
+// Resident warps per SM of an instantiation (for sizing the persistent grid).
 template <int KB, int VB, int GT>
-cudaError_t occupancy_t(int* ctas_per_sm) {
+cudaError_t occupancy_t(int* warps_per_sm) {
   constexpr int NT = GT <= 4 ? 1 : 2;
   using LY = PersistLayout<KB, VB, NT, GT>;
   const int smem = LY::kBytes;
@@ -420,8 +436,11 @@ cudaError_t occupancy_t(int* ctas_per_sm) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
   }
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_persist_kernel<KB, VB, NT, GT>,
-                                                       kThreads, smem);
+  int ctas = 0;
+  const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctas, decode_persist_kernel<KB, VB, NT, GT>,
+                                                                      LY::kCtaThreads, smem);
+  *warps_per_sm = ctas * LY::kWarps;
+  return e;
 }
 
 template <int KB, int VB>

@@ -51,7 +51,7 @@ cudaError_t plan_persist(DecodeParams& p, uint64_t* ws_need) {
   e = dispatch(p, nullptr, &occ);
   if (e != cudaSuccess) return e;
   if (occ < 1) occ = 1;
-  long long nw = (long long)sms * occ * 4;
+  long long nw = (long long)sms * occ;  // occ: resident warps per SM
   const long long items = (long long)G.NS * p.n_items;
   if (nw > items) nw = items;
   if (nw > (long long)kMaxQSplits * G.NS) nw = (long long)kMaxQSplits * G.NS;
