@@ -289,6 +289,28 @@ __device__ __forceinline__ uint32_t split_pack(float2 x, float lo) {
   return h2_as_u32(__floats2half2_rn(y.x, y.y));
 }
 
+// hi and lo fp16 parts of two values, both packed: x = hi + lo to ~2^-22.
+__device__ __forceinline__ void split_hilo(float2 x, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(x.x, x.y);
+  const float2 r = __ffma2_rn(make_float2(-1.0f, -1.0f), __half22float2(h), x);
+  hi = h2_as_u32(h);
+  lo = h2_as_u32(__floats2half2_rn(r.x, r.y));
+}
+
+// Column layouts of the mma B operands (Q' and P') and of the D fragments.
+// Up to 4 heads (one n-tile, NT = 1): column = (head, hi/lo), the hi and lo
+// products summed over column pairs afterwards.  5-8 heads (NT = 2): the
+// head layout -- column = head, and the hi and lo parts go through two mma
+// into the same accumulator -- so O needs one n-tile instead of two and the
+// logits need no column sums.  A lane's two softmax slots are then heads
+// 2 tq + i (its own D columns) instead of 4 i + tq.
+template <int NT>
+__device__ __forceinline__ constexpr bool head_cols() { return NT == 2; }
+template <int NT>
+__device__ __forceinline__ constexpr int o_tiles() { return head_cols<NT>() ? 1 : NT; }
+template <int NT>
+__device__ __forceinline__ int slot_head(int i, int tq) { return head_cols<NT>() ? 2 * tq + i : 4 * i + tq; }
+
 // Channels of this lane in the Q' build: c0, c0 + 1, c0 + D, c0 + D + 1 with
 // (c0, c0 + D) and (c0 + 1, c0 + D + 1) the two halves of the B-fragment
 // words 2s and 2s + 1 (s = lane & 7) of reader thread lane >> 3, for every
@@ -320,7 +342,7 @@ __device__ __forceinline__ int qb_perm_pos(int c) {
 }
 
 // One 32-token group for one warp: Q' fragments, S = K Q' (2 m-tiles x NT
-// n-tiles), online softmax, O += V^T P' (8 m-tiles x NT).
+// n-tiles), online softmax, O += V^T P' (8 m-tiles x o_tiles<NT>()).
 //
 // JC (one n-tile, at most 2 heads): the PV B operand puts the V group into
 // the columns too -- column = (head, V group, hi/lo) -- so a lane builds P'
@@ -329,9 +351,10 @@ __device__ __forceinline__ int qb_perm_pos(int c) {
 template <int KB, int VB, int NT, bool JC, int GT>
 __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWarpSmem<NT>& sm,
                                               const unsigned char* st, int g, int lane,
-                                              float (&O)[8][NT][4], float (&macc)[NT][kNVG], float (&m_used)[NT],
-                                              float (&lsum)[NT]) {
+                                              float (&O)[8][o_tiles<NT>()][4], float (&macc)[NT][kNVG],
+                                              float (&m_used)[NT], float (&lsum)[NT]) {
   using SG = StageGeom<KB, VB>;
+  constexpr bool HC = head_cols<NT>();
   const int gq = lane >> 2, tq = lane & 3;
 
   // (a) Q' = q * scale_k (hi + lo fp16) into this warp's fragment rows,
@@ -355,8 +378,21 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
     for (int r = 0; r < GT; ++r) {
       bpart[r] = 0.0f;
       if (r >= g) continue;
-      unsigned char* dhi = reinterpret_cast<unsigned char*>(&sm.bq[r >> 2][8 * (r & 3) + tsl][0]);
-      unsigned char* dlo = dhi + 4 * 64;
+      // fragment rows (reader lanes) and byte offsets of the hi and lo words
+      unsigned char* dhi;
+      unsigned char* dlo;
+      int whi, wlo;
+      if constexpr (HC) {
+        const int R = 4 * r + tsl;  // column r in table 0 (hi) and table 1 (lo)
+        dhi = reinterpret_cast<unsigned char*>(&sm.bq[0][R][0]);
+        dlo = reinterpret_cast<unsigned char*>(&sm.bq[1][R][0]);
+        whi = wlo = (8 * (lane & 7)) ^ (((R >> 1) & 3) << 4);
+      } else {
+        dhi = reinterpret_cast<unsigned char*>(&sm.bq[r >> 2][8 * (r & 3) + tsl][0]);
+        dlo = dhi + 4 * 64;
+        whi = wofs;
+        wlo = wofs ^ 32;
+      }
       const float4 q4 = *reinterpret_cast<const float4*>(&qw[r][4 * lane]);  // (c0, c0+D, c0+1, c0+D+1)
       const float2 qA = make_float2(q4.x, q4.y), qB = make_float2(q4.z, q4.w);
       const float2 pA = __fmul2_rn(qA, skA), pB = __fmul2_rn(qB, skB);
@@ -364,8 +400,8 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
       const float2 m1 = make_float2(-1.0f, -1.0f);
       const float2 rA = __ffma2_rn(m1, __half22float2(hA), pA), rB = __ffma2_rn(m1, __half22float2(hB), pB);
       const __half2 lA = __floats2half2_rn(rA.x, rA.y), lB = __floats2half2_rn(rB.x, rB.y);
-      *reinterpret_cast<uint2*>(dhi + wofs) = make_uint2(h2_as_u32(hA), h2_as_u32(hB));
-      *reinterpret_cast<uint2*>(dlo + (wofs ^ 32)) = make_uint2(h2_as_u32(lA), h2_as_u32(lB));
+      *reinterpret_cast<uint2*>(dhi + whi) = make_uint2(h2_as_u32(hA), h2_as_u32(hB));
+      *reinterpret_cast<uint2*>(dlo + wlo) = make_uint2(h2_as_u32(lA), h2_as_u32(lB));
       const float2 b2 = __ffma2_rn(qA, mnA, __fmul2_rn(qB, mnB));
       const float2 o2 = __fadd2_rn(pA, pB);  // hi + lo = qp to ~2^-22
       // the mma's constant part 1024 * sum_c (hi + lo), in logit units
@@ -439,26 +475,37 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
       uint32_t lo0, hi0, lo1, hi1;
       k_frag<KB>(w0, s_, lo0, hi0);
       k_frag<KB>(w1, s_, lo1, hi1);
+      if constexpr (HC) {
+        // hi and lo parts: two independent chains, summed below
+        mma16816(S[mt][0], lo0, lo1, hi0, hi1, bq[0][2 * s_], bq[0][2 * s_ + 1]);
+        mma16816(S[mt][1], lo0, lo1, hi0, hi1, bq[1][2 * s_], bq[1][2 * s_ + 1]);
+      } else {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        if (s_ & 1)
-          mma16816(S2[nt], lo0, lo1, hi0, hi1, bq[nt][2 * s_], bq[nt][2 * s_ + 1]);
-        else
-          mma16816(S[mt][nt], lo0, lo1, hi0, hi1, bq[nt][2 * s_], bq[nt][2 * s_ + 1]);
+        for (int nt = 0; nt < NT; ++nt) {
+          if (s_ & 1)
+            mma16816(S2[nt], lo0, lo1, hi0, hi1, bq[nt][2 * s_], bq[nt][2 * s_ + 1]);
+          else
+            mma16816(S[mt][nt], lo0, lo1, hi0, hi1, bq[nt][2 * s_], bq[nt][2 * s_ + 1]);
+        }
       }
     }
+    if constexpr (HC) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+      for (int k = 0; k < 4; ++k) S[mt][0][k] += S[mt][1][k];
+    } else {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) S[mt][nt][k] += S2[nt][k];
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) S[mt][nt][k] += S2[nt][k];
+    }
   }
 
-  // (d) online softmax (base 2); this thread's heads are 4*nt + tq, its
+  // (d) online softmax (base 2); this thread's heads are slot_head(nt), its
   //     tokens gq + {0, 8, 16, 24}
   float P[NT][2][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const int h = 4 * nt + tq;
+    const int h = slot_head<NT>(nt, tq);
     const bool live = h < g;
     const float bias = live ? sm.bias[h] : 0.0f;
     float zs[2][2];
@@ -467,7 +514,8 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
       for (int rh = 0; rh < 2; ++rh) {
-        zs[mt][rh] = S[mt][nt][2 * rh] + S[mt][nt][2 * rh + 1];  // 2^E x (logit - bias)
+        // 2^E x (logit - bias)
+        zs[mt][rh] = HC ? S[mt][0][2 * rh + nt] : S[mt][nt][2 * rh] + S[mt][nt][2 * rh + 1];
         zm = fmaxf(zm, zs[mt][rh]);
       }
     constexpr float kUnscale = 1.0f / (float)(1 << kq_exp<KB>());
@@ -497,10 +545,19 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
 #pragma unroll
           for (int k = 0; k < 4; ++k) O[mc][nt][k] *= a_o;
       } else if (resc) {
+        if constexpr (HC) {
+          // this lane's O columns are its own two heads
 #pragma unroll
-        for (int mc = 0; mc < 8; ++mc)
+          for (int mc = 0; mc < 8; ++mc) {
+            O[mc][0][nt] *= alpha;
+            O[mc][0][2 + nt] *= alpha;
+          }
+        } else {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) O[mc][nt][k] *= alpha;
+          for (int mc = 0; mc < 8; ++mc)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) O[mc][nt][k] *= alpha;
+        }
       }
     }
     const float bm = live ? bias - m_used[nt] : -INFINITY;
@@ -526,75 +583,92 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
   const float lo_sel = (gq & 1) ? 1.0f : 0.0f;  // this lane's B column is a lo column
 #pragma unroll
   for (int kt = 0; kt < 2; ++kt) {
-    // P' fragments per (n-tile, V group): tokens 16kt + {2tq, 2tq+1, 2tq+8, 2tq+9}, column gq
-    // (JC: one fragment; column gq = head gq >> 2, V group (gq >> 1) & 1)
-    uint32_t bp[NT][kNVG][2];
-    const int src1 = 8 * tq + (JC ? (gq >> 2) : (gq >> 1)), src2 = src1 + 4;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const float v0 = __shfl_sync(0xffffffffu, P[nt][kt][0], src1);
-      const float v1 = __shfl_sync(0xffffffffu, P[nt][kt][0], src2);
-      const float v2 = __shfl_sync(0xffffffffu, P[nt][kt][1], src1);
-      const float v3 = __shfl_sync(0xffffffffu, P[nt][kt][1], src2);
-#pragma unroll
-      for (int j = 0; j < (JC ? 1 : kNVG); ++j) {
-        const int jv = JC ? ((gq >> 1) & 1) : j;
-        const float4 sv = *reinterpret_cast<const float4*>(&sm.vsc[jv][16 * kt + 4 * tq]);
-        bp[nt][j][0] = split_pack(__fmul2_rn(make_float2(v0, v1), make_float2(sv.x, sv.y)), lo_sel);
-        bp[nt][j][1] = split_pack(__fmul2_rn(make_float2(v2, v3), make_float2(sv.z, sv.w)), lo_sel);
-      }
-    }
-    // V code fragments via ldmatrix.trans on the packed (swizzled) rows
+    // V code fragments: ldmatrix.trans on the packed (swizzled) rows, then
+    // the A fragment of m-tile mc from blocks of them
     const uint32_t vbase = smem_u32(st + SG::VC);
     const int mi = lane >> 3, rr = lane & 7;
-    if (VB == 4) {
-      uint32_t R[4][2];  // [block][token half]
+    constexpr int NBLK = VB == 8 ? 8 : VB == 4 ? 4 : 2;  // 16-byte blocks of a V row
+    uint32_t R[NBLK][2];  // [block][token half]
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int blk = 2 * c + (mi >> 1), th = mi & 1;
-        const uint32_t addr = vbase + swz((16 * kt + 8 * th + rr) * SG::VROW + 16 * blk, SG::VSW);
-        ldsm_x4_trans(R[2 * c][0], R[2 * c][1], R[2 * c + 1][0], R[2 * c + 1][1], addr);
-      }
-#pragma unroll
-      for (int mc = 0; mc < 8; ++mc) {
+    for (int c = 0; c < NBLK / 2; ++c) {
+      const int blk = 2 * c + (mi >> 1), th = mi & 1;
+      const uint32_t addr = vbase + swz((16 * kt + 8 * th + rr) * SG::VROW + 16 * blk, SG::VSW);
+      ldsm_x4_trans(R[2 * c][0], R[2 * c][1], R[2 * c + 1][0], R[2 * c + 1][1], addr);
+    }
+    auto afrag = [&](int mc, uint32_t (&A)[4]) {
+      if (VB == 4) {
         const int blk = mc >> 1, i = mc & 1;
-        const uint32_t a0 = ext4(R[blk][0], i), a1 = ext4(R[blk][0], i + 2);
-        const uint32_t a2 = ext4(R[blk][1], i), a3 = ext4(R[blk][1], i + 2);
-        const int j = JC ? 0 : v_group<VB>(mc);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma16816(O[mc][nt], a0, a1, a2, a3, bp[nt][j][0], bp[nt][j][1]);
+        A[0] = ext4(R[blk][0], i); A[1] = ext4(R[blk][0], i + 2);
+        A[2] = ext4(R[blk][1], i); A[3] = ext4(R[blk][1], i + 2);
+      } else if (VB == 8) {
+        A[0] = ext8(R[mc][0], 0); A[1] = ext8(R[mc][0], 1);
+        A[2] = ext8(R[mc][1], 0); A[3] = ext8(R[mc][1], 1);
+      } else {
+        const int blk = mc >> 2, i = mc & 3;
+        A[0] = ext2(R[blk][0], i); A[1] = ext2(R[blk][0], i + 4);
+        A[2] = ext2(R[blk][1], i); A[3] = ext2(R[blk][1], i + 4);
       }
-    } else if (VB == 8) {
-      uint32_t R[8][2];
+    };
+    if constexpr (HC) {
+      // P' of tokens 16kt + 2tq + {0, 1} (+8) for head gq: held by lanes
+      // 4 (2tq + e) + (gq >> 1) in softmax slot gq & 1
+      float pv[2][2];  // [row half][token parity]
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int blk = 2 * c + (mi >> 1), th = mi & 1;
-        const uint32_t addr = vbase + swz((16 * kt + 8 * th + rr) * SG::VROW + 16 * blk, SG::VSW);
-        ldsm_x4_trans(R[2 * c][0], R[2 * c][1], R[2 * c + 1][0], R[2 * c + 1][1], addr);
+      for (int e = 0; e < 2; ++e) {
+        const int src = 4 * (2 * tq + e) + (gq >> 1);
+#pragma unroll
+        for (int rh = 0; rh < 2; ++rh) {
+          const float p0 = __shfl_sync(0xffffffffu, P[0][kt][rh], src);
+          const float p1 = __shfl_sync(0xffffffffu, P[1][kt][rh], src);
+          pv[rh][e] = (gq & 1) ? p1 : p0;
+        }
+      }
+      uint32_t bh[kNVG][2], bl[kNVG][2];
+#pragma unroll
+      for (int j = 0; j < kNVG; ++j) {
+        const float4 sv = *reinterpret_cast<const float4*>(&sm.vsc[j][16 * kt + 4 * tq]);
+        split_hilo(__fmul2_rn(make_float2(pv[0][0], pv[0][1]), make_float2(sv.x, sv.y)), bh[j][0], bl[j][0]);
+        split_hilo(__fmul2_rn(make_float2(pv[1][0], pv[1][1]), make_float2(sv.z, sv.w)), bh[j][1], bl[j][1]);
+      }
+      // hi parts over all m-tiles, then lo parts: no back-to-back accumulator dependence
+      uint32_t A[8][4];
+#pragma unroll
+      for (int mc = 0; mc < 8; ++mc) {
+        afrag(mc, A[mc]);
+        const int j = v_group<VB>(mc);
+        mma16816(O[mc][0], A[mc][0], A[mc][1], A[mc][2], A[mc][3], bh[j][0], bh[j][1]);
       }
 #pragma unroll
       for (int mc = 0; mc < 8; ++mc) {
-        const uint32_t a0 = ext8(R[mc][0], 0), a1 = ext8(R[mc][0], 1);
-        const uint32_t a2 = ext8(R[mc][1], 0), a3 = ext8(R[mc][1], 1);
-        const int j = JC ? 0 : v_group<VB>(mc);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma16816(O[mc][nt], a0, a1, a2, a3, bp[nt][j][0], bp[nt][j][1]);
+        const int j = v_group<VB>(mc);
+        mma16816(O[mc][0], A[mc][0], A[mc][1], A[mc][2], A[mc][3], bl[j][0], bl[j][1]);
       }
     } else {
-      uint32_t R[2][2];
-      {
-        const int blk = mi >> 1, th = mi & 1;
-        const uint32_t addr = vbase + swz((16 * kt + 8 * th + rr) * SG::VROW + 16 * blk, SG::VSW);
-        ldsm_x4_trans(R[0][0], R[0][1], R[1][0], R[1][1], addr);
+      // P' fragments per (n-tile, V group): tokens 16kt + {2tq, 2tq+1, 2tq+8, 2tq+9}, column gq
+      // (JC: one fragment; column gq = head gq >> 2, V group (gq >> 1) & 1)
+      uint32_t bp[NT][kNVG][2];
+      const int src1 = 8 * tq + (JC ? (gq >> 2) : (gq >> 1)), src2 = src1 + 4;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float v0 = __shfl_sync(0xffffffffu, P[nt][kt][0], src1);
+        const float v1 = __shfl_sync(0xffffffffu, P[nt][kt][0], src2);
+        const float v2 = __shfl_sync(0xffffffffu, P[nt][kt][1], src1);
+        const float v3 = __shfl_sync(0xffffffffu, P[nt][kt][1], src2);
+#pragma unroll
+        for (int j = 0; j < (JC ? 1 : kNVG); ++j) {
+          const int jv = JC ? ((gq >> 1) & 1) : j;
+          const float4 sv = *reinterpret_cast<const float4*>(&sm.vsc[jv][16 * kt + 4 * tq]);
+          bp[nt][j][0] = split_pack(__fmul2_rn(make_float2(v0, v1), make_float2(sv.x, sv.y)), lo_sel);
+          bp[nt][j][1] = split_pack(__fmul2_rn(make_float2(v2, v3), make_float2(sv.z, sv.w)), lo_sel);
+        }
       }
 #pragma unroll
       for (int mc = 0; mc < 8; ++mc) {
-        const int blk = mc >> 2, i = mc & 3;
-        const uint32_t a0 = ext2(R[blk][0], i), a1 = ext2(R[blk][0], i + 4);
-        const uint32_t a2 = ext2(R[blk][1], i), a3 = ext2(R[blk][1], i + 4);
+        uint32_t A[4];
+        afrag(mc, A);
         const int j = JC ? 0 : v_group<VB>(mc);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma16816(O[mc][nt], a0, a1, a2, a3, bp[nt][j][0], bp[nt][j][1]);
+        for (int nt = 0; nt < NT; ++nt) mma16816(O[mc][nt], A[0], A[1], A[2], A[3], bp[nt][j][0], bp[nt][j][1]);
       }
     }
   }
@@ -662,12 +736,24 @@ __device__ __forceinline__ void build_bq_f16(const float (*qw)[kHeadDim], MmaWar
                                              int lane) {
   const int tqr = (lane >> 1) & 3;                 // reader thread-in-group of channels 4*lane ..
   const int sstep = 2 * (lane >> 3) + (lane & 1);  // their k-step
-  const int xr = ((tqr >> 1) & 1) << 4;            // hi row chunk swizzle ((row >> 1) & 3) << 4
 #pragma unroll
-  for (int r = 0; r < 8 * NT; ++r) {
+  for (int r = 0; r < 4 * NT; ++r) {
     if (r >= g) break;
-    unsigned char* dhi = reinterpret_cast<unsigned char*>(&sm.bq[r >> 2][8 * (r & 3) + tqr][0]);
-    unsigned char* dlo = dhi + 4 * 64;
+    // reader row R of head r's hi (and lo) column, chunk swizzle ((R >> 1) & 3) << 4
+    unsigned char* dhi;
+    unsigned char* dlo;
+    int xr, xl;
+    if constexpr (head_cols<NT>()) {
+      const int R = 4 * r + tqr;
+      dhi = reinterpret_cast<unsigned char*>(&sm.bq[0][R][0]);
+      dlo = reinterpret_cast<unsigned char*>(&sm.bq[1][R][0]);
+      xr = xl = ((R >> 1) & 3) << 4;
+    } else {
+      dhi = reinterpret_cast<unsigned char*>(&sm.bq[r >> 2][8 * (r & 3) + tqr][0]);
+      dlo = dhi + 4 * 64;
+      xr = ((tqr >> 1) & 1) << 4;
+      xl = xr ^ 32;
+    }
     float qv[4];  // channels 4*lane + k of the permuted query
 #pragma unroll
     for (int k = 0; k < 4; ++k) qv[k] = qw[r][qb_perm_pos<KBQ>(4 * lane + k)];
@@ -677,7 +763,7 @@ __device__ __forceinline__ void build_bq_f16(const float (*qw)[kHeadDim], MmaWar
       const __half hi = __float2half_rn(qv[k]);
       const __half lo = __float2half_rn(qv[k] - __half2float(hi));
       *reinterpret_cast<__half*>(dhi + (byte ^ xr)) = hi;
-      *reinterpret_cast<__half*>(dlo + (byte ^ xr ^ 32)) = lo;
+      *reinterpret_cast<__half*>(dlo + (byte ^ xl)) = lo;
     }
   }
 }
@@ -688,8 +774,9 @@ __device__ __forceinline__ void build_bq_f16(const float (*qw)[kHeadDim], MmaWar
 // m-tile mc is channel 16 mc + gq).
 template <int NT>
 __device__ __forceinline__ void process_f16(const MmaWarpSmem<NT>& sm, const unsigned char* st, int g, int lane,
-                                            int kk0, int k1, float (&O)[8][NT][4],
+                                            int kk0, int k1, float (&O)[8][o_tiles<NT>()][4],
                                             float (&m_used)[NT], float (&lsum)[NT]) {
+  constexpr bool HC = head_cols<NT>();
   const int gq = lane >> 2, tq = lane & 3;
   uint32_t bq[NT][16];
 #pragma unroll
@@ -701,7 +788,8 @@ __device__ __forceinline__ void process_f16(const MmaWarpSmem<NT>& sm, const uns
       bq[nt][4 * c] = u.x; bq[nt][4 * c + 1] = u.y; bq[nt][4 * c + 2] = u.z; bq[nt][4 * c + 3] = u.w;
     }
   }
-  // S = K Q: token row gq; rows 8..15 of the tile are empty
+  // S = K Q: token row gq; rows 8..15 of the tile are empty.  Head columns:
+  // S holds the hi chain, S2 the lo chain; otherwise even / odd k-steps.
   float S[NT][4], S2[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
@@ -714,21 +802,26 @@ __device__ __forceinline__ void process_f16(const MmaWarpSmem<NT>& sm, const uns
   for (int s_ = 0; s_ < 8; ++s_) {
     const uint4 u = kw[s_ >> 1];
     const uint32_t lo = (s_ & 1) ? u.z : u.x, hi = (s_ & 1) ? u.w : u.y;
+    if constexpr (HC) {
+      mma16816(S[0], lo, 0u, hi, 0u, bq[0][2 * s_], bq[0][2 * s_ + 1]);
+      mma16816(S2[0], lo, 0u, hi, 0u, bq[1][2 * s_], bq[1][2 * s_ + 1]);
+    } else {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      if (s_ & 1)
-        mma16816(S2[nt], lo, 0u, hi, 0u, bq[nt][2 * s_], bq[nt][2 * s_ + 1]);
-      else
-        mma16816(S[nt], lo, 0u, hi, 0u, bq[nt][2 * s_], bq[nt][2 * s_ + 1]);
+      for (int nt = 0; nt < NT; ++nt) {
+        if (s_ & 1)
+          mma16816(S2[nt], lo, 0u, hi, 0u, bq[nt][2 * s_], bq[nt][2 * s_ + 1]);
+        else
+          mma16816(S[nt], lo, 0u, hi, 0u, bq[nt][2 * s_], bq[nt][2 * s_ + 1]);
+      }
     }
   }
-  // online softmax over the item's tokens (this thread: token gq, head 4 nt + tq)
+  // online softmax over the item's tokens (this thread: token gq, head slot_head(nt))
   const bool tok_ok = kk0 + gq < k1;
   float P[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const bool live = 4 * nt + tq < g;
-    const float z = (S[nt][0] + S2[nt][0]) + (S[nt][1] + S2[nt][1]);
+    const bool live = slot_head<NT>(nt, tq) < g;
+    const float z = HC ? S[0][nt] + S2[0][nt] : (S[nt][0] + S2[nt][0]) + (S[nt][1] + S2[nt][1]);
     float zm = tok_ok ? z : -INFINITY;
     zm = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, 4));
     zm = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, 8));
@@ -736,35 +829,67 @@ __device__ __forceinline__ void process_f16(const MmaWarpSmem<NT>& sm, const uns
     if (!live) zm = -INFINITY;
     if (zm > m_used[nt] + kLazyRescale) {
       const float alpha = ex2(m_used[nt] - zm);
+      if constexpr (HC) {
 #pragma unroll
-      for (int mc = 0; mc < 8; ++mc)
+        for (int mc = 0; mc < 8; ++mc) {
+          O[mc][0][nt] *= alpha;
+          O[mc][0][2 + nt] *= alpha;
+        }
+      } else {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) O[mc][nt][k] *= alpha;
+        for (int mc = 0; mc < 8; ++mc)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) O[mc][nt][k] *= alpha;
+      }
       lsum[nt] *= alpha;
       m_used[nt] = zm;
     }
     P[nt] = (live && tok_ok) ? ex2(z - m_used[nt]) : 0.0f;
     lsum[nt] += P[nt];
   }
-  // O += V^T P: B = P of tokens 2tq, 2tq+1 for column gq (head gq >> 1, hi / lo)
-  const float lo_sel = (gq & 1) ? 1.0f : 0.0f;
-  const int src0 = 8 * tq + (gq >> 1);  // lane holding token 2tq, head gq >> 1
-  uint32_t bp[NT];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const float v0 = __shfl_sync(0xffffffffu, P[nt], src0);
-    const float v1 = __shfl_sync(0xffffffffu, P[nt], src0 + 4);
-    bp[nt] = split_pack(make_float2(v0, v1), lo_sel);
-  }
   const uint32_t vbase = smem_u32(st + F16Geom::VC);
+  if constexpr (HC) {
+    // O += V^T P: B = P of tokens 2tq, 2tq+1 for column (head) gq, held by
+    // lanes 4 (2tq + e) + (gq >> 1) in slot gq & 1; hi and lo as two mma
+    float v[2];
 #pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    uint32_t a[4];
-    ldsm_x4_trans(a[0], a[1], a[2], a[3], vbase + vf16_off(lane & 7, 4 * b + (lane >> 3)));
+    for (int e = 0; e < 2; ++e) {
+      const int src = 4 * (2 * tq + e) + (gq >> 1);
+      const float p0 = __shfl_sync(0xffffffffu, P[0], src);
+      const float p1 = __shfl_sync(0xffffffffu, P[1], src);
+      v[e] = (gq & 1) ? p1 : p0;
+    }
+    uint32_t bh, bl;
+    split_hilo(make_float2(v[0], v[1]), bh, bl);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      uint32_t a[4];
+      ldsm_x4_trans(a[0], a[1], a[2], a[3], vbase + vf16_off(lane & 7, 4 * b + (lane >> 3)));
+      mma1688(O[2 * b][0], a[0], a[1], bh);
+      mma1688(O[2 * b + 1][0], a[2], a[3], bh);
+      mma1688(O[2 * b][0], a[0], a[1], bl);
+      mma1688(O[2 * b + 1][0], a[2], a[3], bl);
+    }
+  } else {
+    // O += V^T P: B = P of tokens 2tq, 2tq+1 for column gq (head gq >> 1, hi / lo)
+    const float lo_sel = (gq & 1) ? 1.0f : 0.0f;
+    const int src0 = 8 * tq + (gq >> 1);  // lane holding token 2tq, head gq >> 1
+    uint32_t bp[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      mma1688(O[2 * b][nt], a[0], a[1], bp[nt]);
-      mma1688(O[2 * b + 1][nt], a[2], a[3], bp[nt]);
+      const float v0 = __shfl_sync(0xffffffffu, P[nt], src0);
+      const float v1 = __shfl_sync(0xffffffffu, P[nt], src0 + 4);
+      bp[nt] = split_pack(make_float2(v0, v1), lo_sel);
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      uint32_t a[4];
+      ldsm_x4_trans(a[0], a[1], a[2], a[3], vbase + vf16_off(lane & 7, 4 * b + (lane >> 3)));
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        mma1688(O[2 * b][nt], a[0], a[1], bp[nt]);
+        mma1688(O[2 * b + 1][nt], a[2], a[3], bp[nt]);
+      }
     }
   }
 }

@@ -11,7 +11,8 @@
 // across stream boundaries: there is no __syncthreads after the prologue.
 //
 // Accumulators: O (tensor-core D fragments: rows = channels, columns =
-// (head, hi/lo)), the running maximum m_used and the partial sums lsum.  The
+// (head, hi/lo), or heads for 5-8 heads -- head_cols), the running maximum
+// m_used and the partial sums lsum.  The
 // quantized part of a stream accumulates codes weighted by P' = p * scale_v
 // (plus V min through macc) in the rotated domain when V is Hadamard-
 // rotated.  When the warp reaches the stream's fp16 items (or the end of
@@ -51,10 +52,9 @@ struct PersistLayout {
   // One CTA per SM holds all of the SM's warps (with several CTAs per SM the
   // warp schedulers favour the earlier CTAs, whose warps then finish their
   // equal shares well before the others).  Warps per SM as measured best:
-  // 16 at 128 registers for single-head groups, 12 at 168 for 2-4 heads,
-  // 8 at 255 for 5-8 heads; fewer when their shared memory would exceed a
-  // CTA's 227 KB.
-  static constexpr int kWantWarps = NT == 2 ? 8 : (GT == 1 ? 16 : 12);
+  // 16 at 128 registers for single-head groups, 12 at 168 for 2-8 heads;
+  // fewer when their shared memory would exceed a CTA's 227 KB.
+  static constexpr int kWantWarps = GT == 1 ? 16 : 12;
   static constexpr int kMaxCtaSmem = 227 * 1024;
   static constexpr int kWarps = kWantWarps * kPerWarp <= kMaxCtaSmem ? kWantWarps : kMaxCtaSmem / kPerWarp;
   static constexpr int kCtaThreads = 32 * kWarps;
@@ -67,8 +67,9 @@ struct PersistLayout {
 // O, macc and lsum restart from zero; m_used carries on.
 template <int VB, int NT, int GT, bool JC>
 __device__ __forceinline__ void stage_quant(const DecodeParams& p, float* sO, float* sML, int g, int lane,
-                                            float (&O)[8][NT][4], float (&macc)[NT][kNVG], float (&m_used)[NT],
-                                            float (&lsum)[NT]) {
+                                            float (&O)[8][o_tiles<NT>()][4], float (&macc)[NT][kNVG],
+                                            float (&m_used)[NT], float (&lsum)[NT]) {
+  constexpr bool HC = head_cols<NT>();
   const int gq = lane >> 2, tq = lane & 3;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
@@ -78,7 +79,7 @@ __device__ __forceinline__ void stage_quant(const DecodeParams& p, float* sO, fl
 #pragma unroll
       for (int j = 0; j < kNVG; ++j) macc[nt][j] += __shfl_xor_sync(0xffffffffu, macc[nt][j], o);
     }
-    const int h = 4 * nt + tq;
+    const int h = slot_head<NT>(nt, tq);
     if constexpr (JC) {
       // D columns of this lane: head tq >> 1, V group tq & 1; macc of that head from its lane
       const int hc = tq >> 1, jj = tq & 1;
@@ -104,7 +105,8 @@ __device__ __forceinline__ void stage_quant(const DecodeParams& p, float* sO, fl
         const float mt = macc[nt][v_group<VB>(mc)];
 #pragma unroll
         for (int rh = 0; rh < 2; ++rh)
-          sO[h * kHeadDim + v_chan<VB>(mc, gq, rh)] = O[mc][nt][2 * rh] + O[mc][nt][2 * rh + 1] + mt;
+          sO[h * kHeadDim + v_chan<VB>(mc, gq, rh)] =
+              (HC ? O[mc][0][2 * rh + nt] : O[mc][nt][2 * rh] + O[mc][nt][2 * rh + 1]) + mt;
       }
       if (gq == 0) {
         sML[2 * h] = m_used[nt];
@@ -130,11 +132,13 @@ __device__ __forceinline__ void stage_quant(const DecodeParams& p, float* sO, fl
     lsum[nt] = 0.0f;
 #pragma unroll
     for (int j = 0; j < kNVG; ++j) macc[nt][j] = 0.0f;
-#pragma unroll
-    for (int mc = 0; mc < 8; ++mc)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) O[mc][nt][k] = 0.0f;
   }
+#pragma unroll
+  for (int mc = 0; mc < 8; ++mc)
+#pragma unroll
+    for (int ot = 0; ot < o_tiles<NT>(); ++ot)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) O[mc][ot][k] = 0.0f;
 }
 
 // End of this warp's piece of stream s: combine the staged quantized part
@@ -142,7 +146,8 @@ __device__ __forceinline__ void stage_quant(const DecodeParams& p, float* sO, fl
 // slot, take a ticket, and merge the stream if this was the last piece.
 template <int NT, int GT>
 __device__ __forceinline__ void finalize_stream(const DecodeParams& p, int slot, int s, int wf, int count, float* sO,
-                                                float* sML, bool staged, int lane, const float (&O)[8][NT][4],
+                                                float* sML, bool staged, int lane,
+                                                const float (&O)[8][o_tiles<NT>()][4],
                                                 const float (&m_used)[NT], float (&lsum)[NT]) {
   const Geometry& G = p.geo;
   const int g = G.g;
@@ -152,14 +157,14 @@ __device__ __forceinline__ void finalize_stream(const DecodeParams& p, int slot,
   for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) lsum[nt] += __shfl_xor_sync(0xffffffffu, lsum[nt], o);
-    const int h = 4 * nt + tq;
+    const int h = slot_head<NT>(nt, tq);
     mqv[nt] = (staged && h < g) ? sML[2 * h] : -INFINITY;
     lqv[nt] = (staged && h < g) ? sML[2 * h + 1] : 0.0f;
   }
   __syncwarp();  // every lane has read the staged (m, l) before they are overwritten
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const int h = 4 * nt + tq;
+    const int h = slot_head<NT>(nt, tq);
     if (h < g) {
       const float M = fmaxf(mqv[nt], m_used[nt]);
       const float eq = (mqv[nt] == -INFINITY) ? 0.0f : exp2f(mqv[nt] - M);
@@ -169,7 +174,7 @@ __device__ __forceinline__ void finalize_stream(const DecodeParams& p, int slot,
 #pragma unroll
         for (int rh = 0; rh < 2; ++rh) {
           float* d = &sO[h * kHeadDim + 16 * mc + 8 * rh + gq];
-          const float t = et * (O[mc][nt][2 * rh] + O[mc][nt][2 * rh + 1]);
+          const float t = et * (head_cols<NT>() ? O[mc][0][2 * rh + nt] : O[mc][nt][2 * rh] + O[mc][nt][2 * rh + 1]);
           *d = staged ? fmaf(eq, *d, t) : t;
         }
       if (gq == 0) {
@@ -282,7 +287,7 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT>::kCtaThreads, 1)
   const long long j1 = first_item_at(p, warp_x(p, gw + 1));
   if (j0 >= j1) return;
 
-  float O[8][NT][4], macc[NT][kNVG], m_used[NT], lsum[NT];
+  float O[8][o_tiles<NT>()][4], macc[NT][kNVG], m_used[NT], lsum[NT];
   auto reset = [&]() {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -290,11 +295,13 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT>::kCtaThreads, 1)
       lsum[nt] = 0.0f;
 #pragma unroll
       for (int j = 0; j < kNVG; ++j) macc[nt][j] = 0.0f;
-#pragma unroll
-      for (int mc = 0; mc < 8; ++mc)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) O[mc][nt][k] = 0.0f;
     }
+#pragma unroll
+    for (int mc = 0; mc < 8; ++mc)
+#pragma unroll
+      for (int ot = 0; ot < o_tiles<NT>(); ++ot)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) O[mc][ot][k] = 0.0f;
   };
   reset();
 

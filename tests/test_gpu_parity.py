@@ -109,6 +109,7 @@ CASES = {
     "k2v2_rope_g8": (2, 2, 1, 8, 1, 300, dict(S=0, R=8, rope=1)),
     "fp16": (16, 16, 2, 8, 2, 777, dict()),
     "fp16_mha": (16, 16, 1, 3, 3, 100, dict()),
+    "fp16_g7": (16, 16, 1, 14, 2, 300, dict(S=4, R=16)),
     "fp16_rope": (16, 16, 1, 2, 1, 200, dict(rope=1)),
 }
 
