@@ -257,6 +257,8 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
 // window) into their slots.  One thread per 16-byte chunk of a K or V row.
 __global__ void __launch_bounds__(256) append_window_kernel(const __grid_constant__ AppendParams p) {
   const Geometry& G = p.geo;
+  grid_dep_wait();     // earlier kernels may still read the ring slots written here
+  grid_dep_trigger();  // the decode that follows may set up meanwhile
   const size_t total = (size_t)G.NS * p.n_new * (2 * kRowVec);
   for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (size_t)gridDim.x * blockDim.x) {
@@ -293,8 +295,7 @@ cudaError_t launch_append_window(const AppendParams& p, cudaStream_t st) {
   const size_t total = (size_t)p.geo.NS * p.n_new * (2 * kRowVec);
   size_t blocks = (total + 255) / 256;
   if (blocks > 152 * 64) blocks = 152 * 64;
-  append_window_kernel<<<(unsigned)blocks, 256, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(append_window_kernel, dim3((unsigned)blocks), dim3(256), 0, st, p);
 }
 
 }  // namespace kvq

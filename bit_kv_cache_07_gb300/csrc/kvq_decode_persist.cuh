@@ -328,14 +328,18 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT>::kCtaThreads, 1)
     }
     cp_async_commit();
   };
-#pragma unroll
-  for (int i = 0; i < LY::kStages - 1; ++i) issue_next(i);
   {
     // this warp's Q' rows start at zero (rows of absent heads stay zero)
     uint4* z = reinterpret_cast<uint4*>(&sm.bq[0][0][0]);
     for (int idx = lane; idx < (int)(sizeof(sm.bq) / 16); idx += 32) z[idx] = make_uint4(0u, 0u, 0u, 0u);
     __syncwarp();
   }
+  // everything above used only the parameters and shared memory; the cache,
+  // the query and the workspace may still be written by the previous kernel
+  grid_dep_wait();
+  grid_dep_trigger();
+#pragma unroll
+  for (int i = 0; i < LY::kStages - 1; ++i) issue_next(i);
   int cur = 0;
   int cur_s = -1;
   bool has_q = false, staged = false, bq_f16 = false;
@@ -428,8 +432,7 @@ cudaError_t launch_t(const DecodeParams& p, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   const int ctas = (p.nwarps + LY::kWarps - 1) / LY::kWarps;
-  decode_persist_kernel<KB, VB, NT, GT><<<ctas, LY::kCtaThreads, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(decode_persist_kernel<KB, VB, NT, GT>, dim3(ctas), dim3(LY::kCtaThreads), smem, st, p);
 }
 
 // Resident warps per SM of an instantiation (for sizing the persistent grid).

@@ -16,7 +16,7 @@ constexpr int kGroupTokens = 32;   // G_K supported by the kernels (one warp lan
 constexpr int kMaxQSplits = 64;    // quantized split-K chunks per stream (decode)
 constexpr int kMaxOutliers = 8;    // non-uniform outliers per vector
 constexpr int kMaxGQA = 8;         // query heads per KV head
-constexpr int kThreads = 128;      // 4 warps per CTA in every kernel
+constexpr int kThreads = 128;      // threads per CTA of the append and split-decode kernels
 
 // Geometry derived once on the host from a kvq_config.
 struct Geometry {
@@ -157,6 +157,32 @@ __host__ __device__ inline long long warp_x(const DecodeParams& p, long long i) 
 }
 __host__ __device__ inline int owner_of(const DecodeParams& p, long long pos) {
   return (int)(idiv((pos + 1) * p.nwarps + p.wtot - 1, p.wtot, p.fd_wtot) - 1);
+}
+
+// ------------------------------------------------ dependent launch (PDL)
+// Kernels launched with launch_dependent() may start while the previous
+// kernel in the stream is still running (their CTAs set up shared memory and
+// the schedule meanwhile); grid_dep_wait() returns once every earlier grid
+// has completed and its memory writes are visible, so a kernel calls it
+// before its first access to memory that earlier work writes or reads.
+// grid_dep_trigger() lets the next such kernel launch early.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" :::); }
+
+template <typename Param>
+inline cudaError_t launch_dependent(void (*kernel)(Param), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                    const Param& arg) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, arg);
 }
 
 // ------------------------------------------------------------ host hooks
