@@ -43,6 +43,8 @@ struct DecodeSmem {
   alignas(16) float oval[4][kGroupTokens][kMaxOutliers];    // per warp: V outlier values
   alignas(16) int ocnt[4][kGroupTokens];
   alignas(16) float2 anchor[4][kHeadDim / 2];  // per warp: e^{i t0 theta_j} of the group
+  alignas(16) float4 anc_v[kHeadDim / 2];      // RoPE group-anchor steps and starts (anchor_step),
+  alignas(16) float anc_c0[kHeadDim / 2];      // in shared memory: lanes index them by pair
   alignas(16) float ml[4][GQ][2];              // per warp (m, l)
   alignas(16) float comb_ml[GQ][2];            // CTA-combined (m, l)
   alignas(16) float lut_k[8];
@@ -79,6 +81,21 @@ __device__ __forceinline__ float2 expi(double x) {
   const double r = x - two_pi * rint(x * inv_two_pi);
   float sn, cs;
   sincosf((float)r, &sn, &cs);
+  return make_float2(cs, sn);
+}
+
+// Anchor e^{i theta_j (S + 32 g)} of group g without fp64 (a narrow pipe
+// on this GPU, and every lane needs two anchors per group): the angle in
+// turns from anchor_turns (a few 1e-7 turns off), reduced to [-1/2, 1/2]
+// turns, then the hardware sine and cosine (absolute error below 1e-6).
+// Groups from 2^16 on take the fp64 reduction.
+template <int GQ>
+__device__ __forceinline__ float2 anchor_expi(const DecodeParams& p, const DecodeSmem<GQ>& sm, int j, int g) {
+  if (g >= (1 << 16)) return expi((double)(p.geo.S + g * kGroupTokens) * p.theta[j]);
+  float t = anchor_turns(sm.anc_v[j], sm.anc_c0[j], g);
+  t -= rintf(t);
+  float sn, cs;
+  __sincosf(6.28318530717958648f * t, &sn, &cs);
   return make_float2(cs, sn);
 }
 
@@ -176,9 +193,8 @@ __device__ __forceinline__ void k_logits_rope(const DecodeParams& p, DecodeSmem<
                                               const float2* __restrict__ rope_e, int s, int grp,
                                               int lane, int w, float (&z)[GQ]) {
   const Geometry& G = p.geo;
-  const int pos0 = G.S + grp * kGroupTokens;
-  // group anchor e^{i pos0 theta_j}
-  for (int j = lane; j < kHeadDim / 2; j += 32) sm.anchor[w][j] = expi((double)pos0 * p.theta[j]);
+  // group anchor e^{i (S + 32 grp) theta_j}
+  for (int j = lane; j < kHeadDim / 2; j += 32) sm.anchor[w][j] = anchor_expi<GQ>(p, sm, j, grp);
   const size_t i = (size_t)grp * kGroupTokens + lane;
   float nmin = 0.0f, nsc = 0.0f;
   if (KB == 3) {
@@ -573,12 +589,11 @@ __device__ __forceinline__ void k_logits_nuq_st(const DecodeParams& p, DecodeSme
     return;
   }
   // group anchor e^{i t0 theta_j}
-  const int pos0 = G.S + grp * kGroupTokens;
   if constexpr (GQ == 1) {
     // anchors of pairs 2i, 2i+1 as (x_2i, x_2i+1, y_2i, y_2i+1): fp32x2 operands without shuffling
     float* ap = reinterpret_cast<float*>(&sm.anchor[w][0]);
     for (int j = lane; j < kHeadDim / 2; j += 32) {
-      const float2 a = expi((double)pos0 * p.theta[j]);
+      const float2 a = anchor_expi<GQ>(p, sm, j, grp);
       ap[(j >> 1) * 4 + (j & 1)] = a.x;
       ap[(j >> 1) * 4 + 2 + (j & 1)] = a.y;
     }
@@ -613,7 +628,7 @@ __device__ __forceinline__ void k_logits_nuq_st(const DecodeParams& p, DecodeSme
     }
     z[0] = zr;
   } else {
-    for (int j = lane; j < kHeadDim / 2; j += 32) sm.anchor[w][j] = expi((double)pos0 * p.theta[j]);
+    for (int j = lane; j < kHeadDim / 2; j += 32) sm.anchor[w][j] = anchor_expi<GQ>(p, sm, j, grp);
     __syncwarp();
 #pragma unroll
     for (int j = 0; j < kHeadDim / 2; ++j) {
@@ -717,6 +732,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     sm.lut_k[tid] = p.k_lut_off[tid];
     sm.lut_v[tid] = p.v_lut_off[tid];
   }
+  if (G.pre_rope)
+    for (int j = tid; j < kHeadDim / 2; j += kThreads) anchor_step(p.theta[j], G.S, &sm.anc_v[j], &sm.anc_c0[j]);
   const bool quant_split = sp < p.n_qsplit;
   if (G.pre_rope && quant_split) {
     // e^{i l theta_j} at [j][l]: a warp reads one j for its 32 token offsets l,

@@ -3,6 +3,7 @@
 // kvq_decode*.cu).  Not part of the public ABI (that is include/kvq.h).
 #pragma once
 
+#include <cmath>
 #include <cstdint>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -157,6 +158,41 @@ __host__ __device__ inline long long warp_x(const DecodeParams& p, long long i) 
 }
 __host__ __device__ inline int owner_of(const DecodeParams& p, long long pos) {
   return (int)(idiv((pos + 1) * p.nwarps + p.wtot - 1, p.wtot, p.fd_wtot) - 1);
+}
+
+// ----------------------------------------------------- RoPE group anchors
+// For RoPE frequency theta (radians per position) and S sinks: the
+// per-group angle step 32 theta / (2 pi) in turns, split into three parts of
+// at most 8 significant bits (exact products with a group index below 2^16)
+// and the rest (below 2^-21 of the step), and the anchor of group 0
+// (position S) in turns.  fp64, once per CTA on the device.
+__host__ __device__ inline void anchor_step(double theta, int S, float4* v4, float* c0) {
+  const double turns = theta / (2.0 * 3.14159265358979323846);
+  double v = turns * kGroupTokens, parts[3];
+  for (int i = 0; i < 3; ++i) {
+    parts[i] = 0.0;
+    if (v > 0.0) {
+      const double q = ldexp(1.0, ilogb(v) - 7);  // unit in the 8th significant bit
+      parts[i] = floor(v / q) * q;
+      v -= parts[i];
+    }
+  }
+  *v4 = make_float4((float)parts[0], (float)parts[1], (float)parts[2], (float)v);
+  const double a = turns * S;
+  *c0 = (float)(a - floor(a));
+}
+// The anchor angle of a channel pair (step parts v, start c0) in group
+// g (< 2^16) in turns, in [0, 1): frac(c0 + g v.x + g v.y + g v.z + g v.w) in
+// fp32; g v.x .. g v.z are exact and reduced exactly, g v.w stays below 0.2
+// turns, so the result is off by a few fp32 units of one turn (checked
+// against fp64 on the host).
+__host__ __device__ inline float anchor_turns(const float4& v, float c0, int g) {
+  const float gf = (float)g;
+  const float a = gf * v.x, b = gf * v.y, c = gf * v.z;
+  float t = (a - floorf(a)) + (b - floorf(b));
+  t = (t - floorf(t)) + (c - floorf(c));
+  t += fmaf(gf, v.w, c0);
+  return t - floorf(t);
 }
 
 // ------------------------------------------------ dependent launch (PDL)

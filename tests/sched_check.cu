@@ -3,8 +3,11 @@
 // owner formula agrees with the ranges, and the (warp, stream) slots are
 // distinct and in bounds.  Also checks the device's division by a launch
 // constant (fastdiv_mulshift: multiply by a rounded-up reciprocal, shift)
-// against exact integer division.  Built and run by test_schedule_host.py.
+// against exact integer division, and the fp32 RoPE group anchors
+// (anchor_turns) against the fp64 angle.  Built and run by
+// test_schedule_host.py.
 #include "../bit_kv_cache_07_gb300/csrc/kvq_internal.cuh"
+#include <cmath>
 #include <cstdio>
 #include <set>
 #include <vector>
@@ -64,6 +67,30 @@ int main() {
     if (i % 3 == 1 && (x / d) * d > 0) x = (x / d) * d - 1;  // just below one
     check(x, d);
   }
+  // RoPE group anchors in fp32 (anchor_turns) against the fp64 angle
+  double worst = 0.0;
+  for (double base : {10000.0, 500000.0, 1e6}) for (int S : {0, 4, 128}) {
+    DecodeParams p{};
+    for (int i = 0; i < kHeadDim / 2; ++i) p.theta[i] = std::pow(base, -2.0 * i / (double)kHeadDim);
+    float4 av[kHeadDim / 2];
+    float ac[kHeadDim / 2];
+    for (int j = 0; j < kHeadDim / 2; ++j) anchor_step(p.theta[j], S, &av[j], &ac[j]);
+    for (int j = 0; j < kHeadDim / 2; ++j)
+      for (int g : {0, 1, 2, 3, 31, 32, 33, 255, 256, 4095, 4096, 32767, 32768, 65534, 65535})
+        for (int dg = 0; dg < 3; ++dg) {
+          const int gg = g - dg * 7919 >= 0 ? g - dg * 7919 : g;
+          const double exact = (double)(S + 32 * gg) * p.theta[j] / (2.0 * 3.14159265358979323846);
+          double d = (double)anchor_turns(av[j], ac[j], gg) - (exact - std::floor(exact));
+          d -= std::round(d);  // circular distance in turns
+          ++cases;
+          if (std::fabs(d) > worst) worst = std::fabs(d);
+          if (std::fabs(d) > 1e-6) {
+            if (bad < 10) printf("anchor j=%d g=%d S=%d base=%g off by %g turns\n", j, gg, S, base, d);
+            ++bad;
+          }
+        }
+  }
+  printf("anchor worst %.3g turns\n", worst);
   printf("cases %d bad %d\n", cases, bad);
   return bad != 0;
 }
