@@ -27,6 +27,8 @@
 // group's tokens.  Softmax is online, in base 2 (q carries log2(e)).
 #pragma once
 
+#include <cstddef>
+
 #include "kvq_internal.cuh"
 
 namespace kvq {
@@ -36,12 +38,7 @@ struct DecodeSmem {
   // every member starts on a 16-byte boundary: several are read as float4
   alignas(16) float q[GQ][kHeadDim];     // q * softmax_scale * log2(e); heads >= g are 0
   alignas(16) float qsum[GQ];            // sum_c q[r][c]
-  alignas(16) float work[4][GQ > 2 ? GQ : 2][kHeadDim];  // per warp: folded q' / K min+scale; merge staging
   alignas(16) float p[4][kGroupTokens][GQ];              // per warp: softmax weights of the current chunk
-  alignas(16) uint32_t vs[4][kGroupTokens][4];           // per warp: V {min, scale} words of the group
-  alignas(16) uint8_t ocol[4][kGroupTokens][kMaxOutliers];  // per warp: V outlier columns
-  alignas(16) float oval[4][kGroupTokens][kMaxOutliers];    // per warp: V outlier values
-  alignas(16) int ocnt[4][kGroupTokens];
   alignas(16) float2 anchor[4][kHeadDim / 2];  // per warp: e^{i t0 theta_j} of the group
   alignas(16) float4 anc_v[kHeadDim / 2];      // RoPE group-anchor steps and starts (anchor_step),
   alignas(16) float anc_c0[kHeadDim / 2];      // in shared memory: lanes index them by pair
@@ -50,7 +47,21 @@ struct DecodeSmem {
   alignas(16) float lut_k[8];
   alignas(16) float lut_v[8];
   int is_last;
+  // used by the uniform-code paths only (a non-uniform launch leaves them out
+  // of its shared memory: decode_smem_fixed)
+  alignas(16) float work[4][GQ > 2 ? GQ : 2][kHeadDim];  // per warp: folded q' / K min+scale; merge staging
+  alignas(16) uint32_t vs[4][kGroupTokens][4];           // per warp: V {min, scale} words of the group
+  alignas(16) uint8_t ocol[4][kGroupTokens][kMaxOutliers];  // per warp: V outlier columns
+  alignas(16) float oval[4][kGroupTokens][kMaxOutliers];    // per warp: V outlier values
+  alignas(16) int ocnt[4][kGroupTokens];
 };
+
+// Bytes of DecodeSmem a launch uses: the non-uniform (KB = 3) kernel stops
+// before `work` (its merge staging goes to its free NUQ stages instead).
+template <int KB, int GQ>
+__host__ __device__ constexpr size_t decode_smem_fixed() {
+  return ((KB == 3 ? offsetof(DecodeSmem<GQ>, work) : sizeof(DecodeSmem<GQ>)) + 15) / 16 * 16;
+}
 
 // RoPE offset table e^{i l theta_j} (or the query-folded W_{j,l}), l = token
 // offset in a 32-token group: entries of pairs 2i and 2i+1 for one l are
@@ -716,7 +727,7 @@ template <int KB, int VB, int GQ>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   DecodeSmem<GQ>& sm = *reinterpret_cast<DecodeSmem<GQ>*>(smem_raw);
-  float2* rope_e = reinterpret_cast<float2*>(smem_raw + ((sizeof(DecodeSmem<GQ>) + 15) / 16) * 16);
+  float2* rope_e = reinterpret_cast<float2*>(smem_raw + decode_smem_fixed<KB, GQ>());
   const Geometry& G = p.geo;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int sp = blockIdx.x, s = blockIdx.y;
@@ -852,8 +863,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
       sm.ml[w][r][1] = lsum[r];
     }
   }
-  float (*stage)[GQ][kHeadDim] = reinterpret_cast<float (*)[GQ][kHeadDim]>(&sm.work[0][0][0]);
+  // merge staging: `work`, or the (now idle) NUQ stages of a non-uniform launch
+  float (*stage)[GQ][kHeadDim] = reinterpret_cast<float (*)[GQ][kHeadDim]>(
+      KB == 3 ? reinterpret_cast<float*>(nuq_stages) : &sm.work[0][0][0]);
   static_assert(sizeof(sm.work) >= 4 * GQ * kHeadDim * sizeof(float), "merge staging");
+  static_assert(KB != 3 || 8 * NuqStage::bytes(0) >= 4 * GQ * kHeadDim * (int)sizeof(float), "merge staging");
 #pragma unroll
   for (int r = 0; r < GQ; ++r)
 #pragma unroll
@@ -961,7 +975,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
 
 template <int KB, int VB, int GQ>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t st) {
-  size_t smem = ((sizeof(DecodeSmem<GQ>) + 15) / 16) * 16;
+  size_t smem = decode_smem_fixed<KB, GQ>();
   if (p.geo.pre_rope) smem += sizeof(float2) * kGroupTokens * (kHeadDim / 2);
   if (KB == 3) smem += 8 * (size_t)NuqStage::bytes(p.geo.nout) + 4 * GQ * kHeadDim * sizeof(float);
   if (smem > 48 * 1024) {
