@@ -39,6 +39,7 @@ struct DecodeSmem {
   alignas(16) float q[GQ][kHeadDim];     // q * softmax_scale * log2(e); heads >= g are 0
   alignas(16) float qsum[GQ];            // sum_c q[r][c]
   alignas(16) float p[4][kGroupTokens][GQ];              // per warp: softmax weights of the current chunk
+  alignas(16) float pv[4][kGroupTokens][GQ];             // per warp: NUQ weights times the token's V scale
   alignas(16) float2 anchor[4][kHeadDim / 2];  // per warp: e^{i t0 theta_j} of the group
   alignas(16) float4 anc_v[kHeadDim / 2];      // RoPE group-anchor steps and starts (anchor_step),
   alignas(16) float anc_c0[kHeadDim / 2];      // in shared memory: lanes index them by pair
@@ -676,9 +677,20 @@ __device__ __forceinline__ void v_accumulate_nuq_st(const DecodeParams& p, Decod
   const int k = p.geo.nout;
   const uint32_t* vms = reinterpret_cast<const uint32_t*>(st + NuqStage::VMS);
   const int bit = 12 * lane, wi = bit >> 5, sh = bit & 31;
+  {
+    // this lane's token: p * scale for the loop below; the V-min term
+    // sum_t p_t min_t once for the warp
+    const float2 ms = unpack_min_scale(vms[lane]);
+#pragma unroll
+    for (int r = 0; r < GQ; ++r) {
+      const float pr = sm.p[w][lane][r];
+      sm.pv[w][lane][r] = pr * ms.y;
+      macc[r] += warp_sum(pr * ms.x);
+    }
+    __syncwarp();
+  }
 #pragma unroll 4
   for (int t = 0; t < kGroupTokens; ++t) {
-    const float2 ms = unpack_min_scale(vms[t]);
     const uint32_t* rw = reinterpret_cast<const uint32_t*>(st + NuqStage::VC + 48 * t);
     uint32_t u = rw[wi] >> sh;
     if (sh > 20) u |= rw[wi + 1] << (32 - sh);
@@ -687,8 +699,7 @@ __device__ __forceinline__ void v_accumulate_nuq_st(const DecodeParams& p, Decod
     for (int e = 0; e < 4; ++e) cv[e] = sm.lut_v[(u >> (3 * e)) & 7u];
 #pragma unroll
     for (int r = 0; r < GQ; ++r) {
-      const float pr = sm.p[w][t][r];
-      const float pp = pr * ms.y;
+      const float pp = sm.pv[w][t][r];
       const float2 pp2 = make_float2(pp, pp);
       const float2 a01 = __ffma2_rn(pp2, make_float2(cv[0], cv[1]), make_float2(acc[r][0], acc[r][1]));
       const float2 a23 = __ffma2_rn(pp2, make_float2(cv[2], cv[3]), make_float2(acc[r][2], acc[r][3]));
@@ -696,7 +707,6 @@ __device__ __forceinline__ void v_accumulate_nuq_st(const DecodeParams& p, Decod
       acc[r][1] = a01.y;
       acc[r][2] = a23.x;
       acc[r][3] = a23.y;
-      macc[r] = fmaf(pr, ms.x, macc[r]);
     }
   }
   if (k == 0) return;
