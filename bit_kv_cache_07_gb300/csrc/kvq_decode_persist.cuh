@@ -205,7 +205,9 @@ __device__ __forceinline__ void finalize_stream(const DecodeParams& p, int slot,
   // last piece of stream s: merge its slots wf + s .. wf + s + count - 1.
   // Lane q reads slot q's (m, l); the first kMB slots' accumulators are read
   // in the same round trip (4 channels per lane), later ones kMB at a time.
-  constexpr int kMB = 8;
+  // Single-head streams have ~10 slots and registers to spare at this point
+  // (measured: 16 at a time is faster there, 8 for larger groups).
+  constexpr int kMB = GT == 1 ? 16 : 8;
   const int b = s / G.Hkv, hk = s % G.Hkv;
   const size_t slot0 = (size_t)(wf + s);
   for (int r = 0; r < g; ++r) {
