@@ -276,6 +276,75 @@ def time_graph(model, stream, steps: int, warmup: int):
     return ms, None
 
 
+def time_append(name: str, dev, T: int, stream, reps: int = 20):
+    """Append through the C ABI on layer 0 of the workload (reported beside the
+    decode step): a bulk prefill of T - 1 tokens into an empty cache, a 1-token
+    append that only copies the token into the fp16 window, and a 1-token
+    append that also flushes (quantizes) one 32-token group.  The 1-token
+    calls are captured reps at a time in a CUDA graph (no host time in the
+    number); CUDA events on the launching stream."""
+    import torch
+    from bit_kv_cache_07_gb300 import binding, synth, workloads
+    cfg = workloads.layer_config(name, 0, tokens=T)
+    if cfg["k_bits"] == 3:
+        cfg["k_lut"] = synth.nuq_lut(name, 0, "k")
+        cfg["v_lut"] = synth.nuq_lut(name, 0, "v")
+    layer = binding.Layer(cfg, device=dev)
+    K, V = synth.layer_kv(name, 0, tokens=T - 1, device=dev)
+    k1, v1 = synth.new_token_kv(name, 0, 0, device=dev)
+
+    def events_us(fn, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / n
+
+    def prefill():
+        binding.kvq_append(cfg, layer.buf, 0, K, V, T - 1, stream)
+
+    for _ in range(2):
+        prefill()
+    pre_us = events_us(prefill, 3)
+
+    def one_token_us(t):
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            for _ in range(reps):
+                binding.kvq_append(cfg, layer.buf, t, k1, v1, 1, stream)
+        with torch.cuda.stream(stream):
+            g.replay()
+            us = events_us(g.replay, 3) / reps
+        del g
+        return us
+
+    def nq(t):
+        return window_counts(cfg, t)[1]
+    t_copy = next((t for t in range(T - 2, 0, -1) if nq(t + 1) == nq(t)), None)
+    t_flush = next((t for t in range(T - 2, 0, -1) if nq(t + 1) > nq(t)), None)
+    copy_us = one_token_us(t_copy) if t_copy is not None else None
+    flush_us = one_token_us(t_flush) if t_flush is not None else None
+    d, NS = cfg["head_dim"], cfg["batch"] * cfg["n_kv_heads"]
+    qo = cfg["batch"] * cfg["n_q_heads"] * d * 2 * 2
+    pre_bytes = 2 * NS * (T - 1) * d * 2 + (algorithmic_bytes(cfg, T - 1) - qo)
+    amort = None
+    if copy_us is not None and flush_us is not None:
+        amort = (31 * copy_us + flush_us) / 32
+    del layer, K, V
+    torch.cuda.empty_cache()
+    return {
+        "layer": 0, "prefill_tokens": T - 1, "prefill_us": pre_us,
+        "prefill_bytes": pre_bytes, "prefill_gbs": pre_bytes / (pre_us * 1e-6) / 1e9,
+        "token_us": copy_us, "flush_token_us": flush_us, "amortised_token_us": amort,
+        "note": "prefill bytes = fp16 K/V read + packed codes, scales and fp16 sink/window written; "
+                "1-token appends: one flush (a 32-token group quantized) every 32 tokens",
+    }
+
+
 def time_e2e(model, stream, steps: int, warmup: int):
     """Same step through the public API with this step's inputs copied in from
     pinned host memory and the outputs copied back, inside the timed region."""
@@ -466,6 +535,7 @@ def main():
     model_layers, model_T = model.L, model.T
     del model
     torch.cuda.empty_cache()
+    append = time_append(args.workload, dev, model_T, stream)
 
     fp16 = None
     if not args.no_fp16_baseline:
@@ -507,6 +577,7 @@ def main():
                      "bytes_per_launch": dec_bytes / model_layers,
                      "launch_us": kern_ms * 1e3},
         "decode_by_pair": pairs if len(pairs) > 1 else None,
+        "append": append,
         "fp16_baseline": fp16,
         "speedup_vs_fp16": (fp16["us_per_step"] / value) if fp16 else None,
         "cpu_baseline": cpu,
