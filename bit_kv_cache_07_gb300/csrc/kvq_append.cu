@@ -130,16 +130,40 @@ __device__ void hadamard_row_inplace(uint16_t* row, float c, int lane) {
 }
 
 // Pack rows of 8-bit codes (one byte per channel in shared memory) into the
-// little-endian bitstream layout and store them as 32-bit words.
+// little-endian bitstream layout and store them as 32-bit words.  Uniform
+// widths gather a word's codes with one shared load and merge the fields
+// with shifts and byte permutes; 3-bit words take 12 codes (36 bits cover
+// the word's 32 plus its 0-2 bit offset) into a 64-bit accumulator.
+__device__ __forceinline__ uint32_t pack4x8(uint32_t x) {  // 4 byte codes < 16 -> 16 bits
+  const uint32_t t = x | (x >> 4);                           // byte 0: c0 | c1 << 4, byte 2: c2 | c3 << 4
+  return __byte_perm(t, 0u, 0x4420) & 0xFFFFu;
+}
+__device__ __forceinline__ uint32_t pack2x4(uint32_t x) {  // 4 byte codes < 4 -> 8 bits
+  uint32_t t = x | (x >> 6);  // bits 0-3: c0 | c1 << 2; bits 16-19: c2 | c3 << 2
+  t |= t >> 12;               // bits 4-7: c2 | c3 << 2
+  return t & 0xFFu;
+}
 __device__ void pack_rows(const uint8_t (*codes)[kHeadDim], int bits, int rows, uint8_t* dst,
                           int row_bytes, int tid) {
   const int words = row_bytes / 4;
   for (int idx = tid; idx < rows * words; idx += kThreads) {
     const int r = idx / words, wi = idx % words;
     uint32_t word = 0;
-    if (32 % bits == 0) {
-      const int per = 32 / bits, c0 = wi * per;
-      for (int m = 0; m < per; ++m) word |= (uint32_t)codes[r][c0 + m] << (m * bits);
+    if (bits == 8) {
+      word = *reinterpret_cast<const uint32_t*>(&codes[r][4 * wi]);
+    } else if (bits == 4) {
+      const uint2 x = *reinterpret_cast<const uint2*>(&codes[r][8 * wi]);
+      word = pack4x8(x.x) | (pack4x8(x.y) << 16);
+    } else if (bits == 2) {
+      const uint4 x = *reinterpret_cast<const uint4*>(&codes[r][16 * wi]);
+      word = pack2x4(x.x) | (pack2x4(x.y) << 8) | (pack2x4(x.z) << 16) | (pack2x4(x.w) << 24);
+    } else if (bits == 3) {
+      const int c0 = (32 * wi) / 3, off = 32 * wi - 3 * c0;
+      unsigned long long acc = 0;
+#pragma unroll
+      for (int m = 0; m < 12; ++m)
+        if (c0 + m < kHeadDim) acc |= (unsigned long long)(codes[r][c0 + m] & 7u) << (3 * m);
+      word = (uint32_t)(acc >> off);
     } else {
       for (int p = 0; p < 32; ++p) {
         const int gb = wi * 32 + p;
@@ -159,26 +183,41 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
 
   __shared__ __align__(16) uint16_t sK[kGroupTokens][kRowHalves];
   __shared__ __align__(16) uint16_t sV[kGroupTokens][kRowHalves];
-  __shared__ uint8_t sCk[kGroupTokens][kHeadDim];
-  __shared__ uint8_t sCv[kGroupTokens][kHeadDim];
+  __shared__ __align__(16) uint8_t sCk[kGroupTokens][kHeadDim];
+  __shared__ __align__(16) uint8_t sCv[kGroupTokens][kHeadDim];
 
   // fp16 sources: tokens written before this call come from the window ring,
-  // the others straight from this call's input.
-  for (int idx = tid; idx < kGroupTokens * kRowVec; idx += kThreads) {
-    const int r = idx / kRowVec, ch = idx % kRowVec;
-    const int t = G.S + grp * kGroupTokens + r;
-    const uint16_t *srck, *srcv;
-    if (t >= p.tokens_before) {
-      const size_t off = ((size_t)s * p.n_new + (t - p.tokens_before)) * kRowHalves;
-      srck = p.k_new + off;
-      srcv = p.v_new + off;
-    } else {
-      const size_t off = ((size_t)s * G.ring + (t - G.S) % G.ring) * kRowHalves;
-      srck = p.L.k_ring + off;
-      srcv = p.L.v_ring + off;
+  // the others straight from this call's input.  All of a thread's loads are
+  // issued before the first shared store.
+  {
+    constexpr int kPer = kGroupTokens * kRowVec / kThreads;
+    static_assert(kPer * kThreads == kGroupTokens * kRowVec, "whole chunks per thread");
+    uint4 kx[kPer], vx[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int idx = tid + u * kThreads;
+      const int r = idx / kRowVec, ch = idx % kRowVec;
+      const int t = G.S + grp * kGroupTokens + r;
+      const uint16_t *srck, *srcv;
+      if (t >= p.tokens_before) {
+        const size_t off = ((size_t)s * p.n_new + (t - p.tokens_before)) * kRowHalves;
+        srck = p.k_new + off;
+        srcv = p.v_new + off;
+      } else {
+        const size_t off = ((size_t)s * G.ring + (t - G.S) % G.ring) * kRowHalves;
+        srck = p.L.k_ring + off;
+        srcv = p.L.v_ring + off;
+      }
+      kx[u] = reinterpret_cast<const uint4*>(srck)[ch];
+      vx[u] = reinterpret_cast<const uint4*>(srcv)[ch];
     }
-    reinterpret_cast<uint4*>(&sK[r][0])[ch] = reinterpret_cast<const uint4*>(srck)[ch];
-    reinterpret_cast<uint4*>(&sV[r][0])[ch] = reinterpret_cast<const uint4*>(srcv)[ch];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int idx = tid + u * kThreads;
+      const int r = idx / kRowVec, ch = idx % kRowVec;
+      reinterpret_cast<uint4*>(&sK[r][0])[ch] = kx[u];
+      reinterpret_cast<uint4*>(&sV[r][0])[ch] = vx[u];
+    }
   }
   __syncthreads();
 
