@@ -26,9 +26,18 @@ constexpr int kRowVec = kRowHalves * 2 / 16;  // 16 x 16-byte chunks per row
 
 // Uniform asymmetric quantizer of one value given its group's min and the
 // fp32 scale: clamp(rint((x - min) / scale), 0, 2^b - 1); scale 0 -> 0.
-__device__ __forceinline__ uint32_t uniform_code(float x, float mn, float scale, float qmax) {
+// code = clamp(rint(RN((x - mn) / scale)), 0, qmax) without a division per
+// element: rs = RN(1 / scale) is shared by the group, and qa = RN(d * rs)
+// differs from the quotient by at most 2^-23 relative (< 3.1e-5 for
+// quotients below 256) while RN(d / scale) is within half an ulp (< 7.7e-6)
+// of it, so both round to the same integer unless qa lies within 1e-4 of a
+// half-integer; there the IEEE division decides.
+__device__ __forceinline__ uint32_t uniform_code(float x, float mn, float scale, float rs, float qmax) {
   if (scale == 0.0f) return 0u;
-  float r = rintf(__fdiv_rn(__fsub_rn(x, mn), scale));
+  const float d = __fsub_rn(x, mn);
+  const float qa = __fmul_rn(d, rs);
+  float r = rintf(qa);
+  if (fabsf(__fsub_rn(__fsub_rn(qa, truncf(qa)), 0.5f)) < 1e-4f) r = rintf(__fdiv_rn(d, scale));
   r = fminf(fmaxf(r, 0.0f), qmax);
   return (uint32_t)r;
 }
@@ -247,8 +256,10 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
     }
     const float qmax = (float)((1 << G.kb) - 1);
     const float scale = __fdiv_rn(__fsub_rn(mx, mn), qmax);
+    const float rs = scale == 0.0f ? 0.0f : __frcp_rn(scale);
+#pragma unroll 8
     for (int r = 0; r < kGroupTokens; ++r)
-      sCk[r][c] = (uint8_t)uniform_code(half_bits_to_float(sK[r][c]), mn, scale, qmax);
+      sCk[r][c] = (uint8_t)uniform_code(half_bits_to_float(sK[r][c]), mn, scale, rs, qmax);
     p.L.k_scales[((size_t)s * G.gcap + grp) * kHeadDim + c] =
         (uint32_t)float_to_half_bits(mn) | ((uint32_t)float_to_half_bits(scale) << 16);
   }
@@ -279,8 +290,9 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
       }
       const float qmax = (float)((1 << G.vb) - 1);
       const float scale = __fdiv_rn(__fsub_rn(mx, mn), qmax);
+      const float rs = scale == 0.0f ? 0.0f : __frcp_rn(scale);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) sCv[r][4 * lane + q] = (uint8_t)uniform_code(v[q], mn, scale, qmax);
+      for (int q = 0; q < 4; ++q) sCv[r][4 * lane + q] = (uint8_t)uniform_code(v[q], mn, scale, rs, qmax);
       if (lane % seg == 0)
         p.L.v_scales[((size_t)s * G.qcap + i) * G.nvg + lane / seg] =
             (uint32_t)float_to_half_bits(mn) | ((uint32_t)float_to_half_bits(scale) << 16);

@@ -1,0 +1,58 @@
+"""The append kernel's uniform code without a division per element.
+
+The kernel computes code = clamp(rint(RN((x - mn) / scale)), 0, 2^b - 1) as
+rint(RN(d * RN(1 / scale))) and falls back to the IEEE division only when
+that product lies within 1e-4 of a half-integer.  This checks, in float32
+arithmetic on the host (the same correctly rounded operations the kernel
+uses), that the shortcut and the division give the same code everywhere
+outside the guard band, over random groups and over quotients placed right
+next to half-integers."""
+import numpy as np
+import pytest
+
+
+def codes_both(x, mn, scale, qmax):
+    f = np.float32
+    d = (x - mn).astype(f)
+    rs = (f(1.0) / scale).astype(f)
+    qa = (d * rs).astype(f)
+    exact = np.rint((d / scale).astype(f))
+    fast = np.rint(qa)
+    guard = np.abs((qa - np.trunc(qa)).astype(f) - f(0.5)) < f(1e-4)
+    fast = np.where(guard, exact, fast)
+    clip = lambda r: np.clip(r, 0, qmax)
+    return clip(fast), clip(exact), guard
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
+def test_shortcut_equals_division_on_random_groups(bits):
+    rng = np.random.default_rng(bits)
+    qmax = np.float32(2 ** bits - 1)
+    for _ in range(200):
+        scale_mag = 10.0 ** rng.uniform(-4, 2)
+        x = (rng.standard_normal(4096) * scale_mag).astype(np.float16).astype(np.float32)
+        mn, mx = x.min(), x.max()
+        scale = ((mx - mn) / qmax).astype(np.float32)
+        if scale == 0:
+            continue
+        fast, exact, _ = codes_both(x, mn, scale, qmax)
+        assert np.array_equal(fast, exact)
+
+
+def test_shortcut_near_half_integers():
+    # quotients pinned within a few ulps of k + 1/2 for every k: the guard
+    # must catch all of them
+    rng = np.random.default_rng(7)
+    f = np.float32
+    for bits in (2, 4, 8):
+        qmax = f(2 ** bits - 1)
+        for _ in range(2000):
+            scale = f(10.0 ** rng.uniform(-3, 1))
+            k = rng.integers(0, int(qmax))
+            target = (f(k) + f(0.5)) * scale
+            d = np.nextafter(target, np.inf if rng.random() < 0.5 else -np.inf).astype(f)
+            for step in range(rng.integers(0, 4)):
+                d = np.nextafter(d, f(np.inf)).astype(f)
+            x = np.array([d], dtype=f)
+            fast, exact, guard = codes_both(x, f(0.0), scale, qmax)
+            assert fast[0] == exact[0]
