@@ -42,11 +42,21 @@ __device__ __forceinline__ uint32_t uniform_code(float x, float mn, float scale,
   return (uint32_t)r;
 }
 
+// Level midpoints tau_i = (L_i + L_(i+1)) / 2 - L_0 of a LUT, in fp32 as the
+// encoder compares them (computed once per CTA).
+__device__ __forceinline__ void nuq_midpoints(const float* lut, float (&tau)[7]) {
+#pragma unroll
+  for (int i = 0; i < 7; ++i) tau[i] = __fsub_rn(__fmul_rn(__fadd_rn(lut[i], lut[i + 1]), 0.5f), lut[0]);
+}
+
 // Non-uniform (LUT) encoding of one 128-channel token vector held by a warp
 // (lane l owns channels 4l..4l+3).  The k largest |x| (ties to the lower
 // channel) become fp16 outliers with code 0; the dense rest is mapped
-// affinely onto [L0, L7] and coded by counting the level midpoints below it.
-__device__ void nuq_encode_row(const uint16_t* __restrict__ xrow, const float* lut, int k,
+// affinely onto [L0, L7] and coded by counting the level midpoints below
+// u = RN((x - mn) / s).  u comes from RN(d * RN(1 / s)), which is within
+// 3 * 2^-24 relative of it; only when that product lies within 2^-21
+// relative of a midpoint does the IEEE division decide.
+__device__ void nuq_encode_row(const uint16_t* __restrict__ xrow, const float* lut, const float (&tau)[7], int k,
                                uint8_t* __restrict__ code_row, uint32_t* minsc_out,
                                uint8_t* col_out, uint16_t* val_out, int lane) {
   float v[4];
@@ -54,7 +64,10 @@ __device__ void nuq_encode_row(const uint16_t* __restrict__ xrow, const float* l
 #pragma unroll
   for (int q = 0; q < 4; ++q) v[q] = half_bits_to_float(xrow[4 * lane + q]);
   int sel[kMaxOutliers];
-  for (int j = 0; j < k; ++j) {
+#pragma unroll
+  for (int j = 0; j < kMaxOutliers; ++j) {
+    sel[j] = 1 << 30;  // past k: sorts last, never written
+    if (j >= k) continue;
     float bv = -1.0f;
     int bi = 1 << 30;
 #pragma unroll
@@ -84,27 +97,40 @@ __device__ void nuq_encode_row(const uint16_t* __restrict__ xrow, const float* l
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   }
   const float s = __fdiv_rn(__fsub_rn(mx, mn), __fsub_rn(lut[7], lut[0]));
-  float tau[7];
-#pragma unroll
-  for (int i = 0; i < 7; ++i) tau[i] = __fsub_rn(__fmul_rn(__fadd_rn(lut[i], lut[i + 1]), 0.5f), lut[0]);
+  const float rs = s != 0.0f ? __frcp_rn(s) : 0.0f;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint32_t c = 0;
     if (!is_out[q] && s != 0.0f) {
-      const float u = __fdiv_rn(__fsub_rn(v[q], mn), s);
+      const float d = __fsub_rn(v[q], mn);
+      float u = __fmul_rn(d, rs);
+      const float band = u * 0x1p-21f;
+      bool near = false;
+#pragma unroll
+      for (int i = 0; i < 7; ++i) near |= fabsf(__fsub_rn(u, tau[i])) <= band;
+      if (near) u = __fdiv_rn(d, s);
 #pragma unroll
       for (int i = 0; i < 7; ++i) c += (u > tau[i]) ? 1u : 0u;
     }
     code_row[4 * lane + q] = (uint8_t)c;
   }
   if (lane == 0) {
-    // ascending column order for the CSR row
-    for (int a = 1; a < k; ++a) {
-      int x = sel[a], b = a - 1;
-      while (b >= 0 && sel[b] > x) { sel[b + 1] = sel[b]; --b; }
-      sel[b + 1] = x;
+    // ascending column order for the CSR row: an odd-even transposition
+    // sort, k passes over the first k slots
+#pragma unroll
+    for (int pass = 0; pass < kMaxOutliers; ++pass) {
+      if (pass >= k) break;
+#pragma unroll
+      for (int a = pass & 1; a + 1 < kMaxOutliers; a += 2)
+        if (a + 1 < k && sel[a] > sel[a + 1]) {
+          const int t = sel[a];
+          sel[a] = sel[a + 1];
+          sel[a + 1] = t;
+        }
     }
-    for (int j = 0; j < k; ++j) {
+#pragma unroll
+    for (int j = 0; j < kMaxOutliers; ++j) {
+      if (j >= k) break;
       col_out[j] = (uint8_t)sel[j];
       val_out[j] = xrow[sel[j]];
     }
@@ -232,13 +258,16 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
 
   const int i0 = grp * kGroupTokens;  // quantized index of the group's first token
   const int kmax = G.nout;
+  float tau_k[7], tau_v[7];  // NUQ level midpoints
+  nuq_midpoints(p.k_lut, tau_k);
+  nuq_midpoints(p.v_lut, tau_v);
 
   // ---- K
   if (G.kb == 3) {
     for (int r = w; r < kGroupTokens; r += 4) {
       const int i = i0 + r;
       const size_t csr = (size_t)s * G.qcap * kmax + (size_t)i * kmax;
-      nuq_encode_row(sK[r], p.k_lut, kmax, sCk[r], &p.L.k_scales[(size_t)s * G.qcap + i],
+      nuq_encode_row(sK[r], p.k_lut, tau_k, kmax, sCk[r], &p.L.k_scales[(size_t)s * G.qcap + i],
                      p.L.k_col + csr, p.L.k_val + csr, lane);
       if (lane == 0) {
         int32_t* rp = p.L.k_rowptr + (size_t)s * (G.qcap + 1);
@@ -270,7 +299,7 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
     if (G.hadamard) hadamard_row_inplace(sV[r], p.hadamard_c, lane);
     if (G.vb == 3) {
       const size_t csr = (size_t)s * G.qcap * kmax + (size_t)i * kmax;
-      nuq_encode_row(sV[r], p.v_lut, kmax, sCv[r], &p.L.v_scales[(size_t)s * G.qcap + i],
+      nuq_encode_row(sV[r], p.v_lut, tau_v, kmax, sCv[r], &p.L.v_scales[(size_t)s * G.qcap + i],
                      p.L.v_col + csr, p.L.v_val + csr, lane);
       if (lane == 0) {
         int32_t* rp = p.L.v_rowptr + (size_t)s * (G.qcap + 1);

@@ -6,7 +6,9 @@ that product lies within 1e-4 of a half-integer.  This checks, in float32
 arithmetic on the host (the same correctly rounded operations the kernel
 uses), that the shortcut and the division give the same code everywhere
 outside the guard band, over random groups and over quotients placed right
-next to half-integers."""
+next to half-integers.  The non-uniform encoder's comparisons of
+u = RN(d / s) with the level midpoints use the same product and fall back to
+the division within 2^-21 relative of a midpoint; checked the same way."""
 import numpy as np
 import pytest
 
@@ -56,3 +58,44 @@ def test_shortcut_near_half_integers():
             x = np.array([d], dtype=f)
             fast, exact, guard = codes_both(x, f(0.0), scale, qmax)
             assert fast[0] == exact[0]
+
+
+def nuq_codes_both(x, mn, s, tau):
+    """Code = #{i : u > tau_i}, u = RN(d / s): the kernel's product with the
+    shared reciprocal and a relative guard band of 2^-21, against the
+    division."""
+    f = np.float32
+    d = (x - mn).astype(f)
+    rs = (f(1.0) / s).astype(f)
+    uf = (d * rs).astype(f)
+    ue = (d / s).astype(f)
+    band = (uf * f(2.0 ** -21)).astype(f)
+    near = (np.abs((uf[:, None] - tau[None, :]).astype(f)) <= band[:, None]).any(axis=1)
+    u = np.where(near, ue, uf)
+    fast = (u[:, None] > tau[None, :]).sum(axis=1)
+    exact = (ue[:, None] > tau[None, :]).sum(axis=1)
+    return fast, exact
+
+
+def test_nuq_shortcut_equals_division():
+    f = np.float32
+    rng = np.random.default_rng(11)
+    for trial in range(300):
+        lut = np.sort(rng.standard_normal(8) * rng.uniform(0.5, 20)).astype(np.float16).astype(f)
+        if np.any(np.diff(lut) <= 0):
+            continue
+        tau = ((lut[:-1] + lut[1:]).astype(f) * f(0.5) - lut[0]).astype(f)
+        x = (rng.standard_normal(2048) * 10.0 ** rng.uniform(-3, 2)).astype(np.float16).astype(f)
+        mn, mx = x.min(), x.max()
+        s = ((mx - mn) / (lut[7] - lut[0])).astype(f)
+        if s == 0:
+            continue
+        # also quotients placed within a few ulps of every midpoint
+        near = []
+        for t in tau:
+            d0 = (t * s).astype(f)
+            for k in range(-3, 4):
+                near.append(mn + np.nextafter(d0, f(np.inf) if k > 0 else f(-np.inf)) if k else mn + d0)
+        xs = np.concatenate([x, np.array(near, dtype=f)]).astype(f)
+        fast, exact = nuq_codes_both(xs, mn, s, tau)
+        assert np.array_equal(fast, exact), trial
