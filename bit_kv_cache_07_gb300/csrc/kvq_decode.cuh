@@ -984,7 +984,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
 }
 
 template <int KB, int VB, int GQ>
-cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t st) {
+cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t st, int* occ) {
   size_t smem = decode_smem_fixed<KB, GQ>();
   if (p.geo.pre_rope) smem += sizeof(float2) * kGroupTokens * (kHeadDim / 2);
   if (KB == 3) smem += 8 * (size_t)NuqStage::bytes(p.geo.nout) + 4 * GQ * kHeadDim * sizeof(float);
@@ -993,6 +993,8 @@ cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t st) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
+  if (occ)  // resident CTAs per SM, for sizing the grid; no launch
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, decode_kernel<KB, VB, GQ>, kThreads, (int)smem);
   dim3 grid(p.n_split, p.geo.NS);
   decode_kernel<KB, VB, GQ><<<grid, kThreads, smem, st>>>(p);
   return cudaGetLastError();

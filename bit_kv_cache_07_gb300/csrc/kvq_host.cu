@@ -240,6 +240,7 @@ kvq_status decode_setup(const kvq_config* cfg, const void* layer_buf, int32_t to
   p.W = pl.W;
   p.n_qsplit = pl.n_qsplit;
   p.n_split = pl.n_split;
+  p.auto_split = cfg->split_tokens <= 0 ? 1 : 0;
   p.gps = pl.gps;
   p.fp16_tokens_per_split = pl.fp16_tps;
   const double sm = cfg->softmax_scale > 0.0f ? (double)cfg->softmax_scale : 1.0 / std::sqrt((double)kHeadDim);
@@ -269,13 +270,42 @@ static uint64_t slots_of(const DecodeParams& p, bool persistent) {
   return persistent ? (uint64_t)p.nwarps + p.geo.NS : (uint64_t)p.geo.NS * p.n_split;
 }
 
-kvq_status decode_plan_device(DecodeParams* p, bool persistent, uint64_t* need) {
+// Split kernel: with the split count left to the library, raise the
+// quantized splits so that the grid (NS x splits CTAs) fills whole waves of
+// the kernel's resident CTAs -- a grid of 1.5 waves leaves half the GPU idle
+// during its last wave, and every CTA streams the same number of groups.
+static cudaError_t fill_waves(DecodeParams* p) {
+  if (!p->auto_split || p->n_qsplit <= 0) return cudaSuccess;
+  int dev = 0, sms = 0, occ = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = launch_decode(*p, nullptr, &occ);
+  if (e != cudaSuccess) return e;
+  if (occ < 1) return cudaSuccess;
+  const long long resident = (long long)sms * occ, NS = p->geo.NS;
+  const int fp16_split = p->n_split - p->n_qsplit;
+  const long long waves = (NS * p->n_split + resident - 1) / resident;
+  const int ngroups = p->Nq / kGroupTokens;
+  long long q = waves * resident / NS - fp16_split;
+  if (q > kMaxQSplits) q = kMaxQSplits;
+  if (q > ngroups) q = ngroups;
+  if (q <= p->n_qsplit) return cudaSuccess;
+  p->gps = (ngroups + (int)q - 1) / (int)q;
+  p->n_qsplit = (ngroups + p->gps - 1) / p->gps;
+  p->n_split = p->n_qsplit + fp16_split;
+  return cudaSuccess;
+}
+
+kvq_status decode_plan_device(DecodeParams* p, bool persistent, uint64_t* need, bool widen) {
   *need = 0;
   if (persistent) {
     uint64_t ignored;
     if (plan_persist(*p, &ignored) != cudaSuccess) return KVQ_ERR_CUDA;
-  } else if (p->n_split <= 1) {
-    return KVQ_OK;
+  } else {
+    if (widen && fill_waves(p) != cudaSuccess) return KVQ_ERR_CUDA;
+    if (p->n_split <= 1) return KVQ_OK;
   }
   uint64_t c, m;
   *need = scratch_bytes(p->geo, slots_of(*p, persistent), &c, &m);

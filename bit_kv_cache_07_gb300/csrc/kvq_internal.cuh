@@ -109,6 +109,7 @@ struct DecodeParams {
   int n_qsplit;           // splits over quantized groups
   int n_split;            // total splits per stream (quantized + fp16)
   int gps;                // quantized groups per split
+  int auto_split;         // 1: split count chosen by the library (config split_tokens = 0)
   int fp16_tokens_per_split;
   float q_scale;          // softmax_scale * log2(e)
   float hadamard_c;       // fp32(1/sqrt(d))
@@ -224,7 +225,9 @@ inline cudaError_t launch_dependent(void (*kernel)(Param), dim3 grid, dim3 block
 // ------------------------------------------------------------ host hooks
 cudaError_t launch_append_quantize(const AppendParams& p, int n_groups, cudaStream_t st);
 cudaError_t launch_append_window(const AppendParams& p, cudaStream_t st);
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st);
+// Split-K decode; with occ != nullptr it only reports the kernel's resident
+// CTAs per SM (for sizing the grid) and launches nothing.
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, int* occ = nullptr);
 // Persistent decode (uniform K/V with 64-channel V groups, no RoPE; or an fp16
 // cache).  Fills the schedule fields of p (nwarps from the device's SM count
 // and the kernel's occupancy) and reports the workspace it needs.
@@ -236,7 +239,10 @@ cudaError_t launch_decode_persist(const DecodeParams& p, cudaStream_t st);
 // persistent plan asks the device for its SM count and occupancy); launch.
 kvq_status decode_setup(const kvq_config* cfg, const void* layer_buf, int32_t tokens, const uint16_t* q,
                         uint16_t* out, float* lse, DecodeParams* p, bool* persistent, uint64_t* layout_ws);
-kvq_status decode_plan_device(DecodeParams* p, bool persistent, uint64_t* need);
+// widen: with automatic splits, raise the split kernel's split count so its
+// grid fills whole waves of resident CTAs (more scratch; the fixed-scratch
+// entry point passes false).
+kvq_status decode_plan_device(DecodeParams* p, bool persistent, uint64_t* need, bool widen = true);
 kvq_status decode_launch(DecodeParams* p, bool persistent, void* ws, cudaStream_t st);
 
 // --------------------------------------------------------- device helpers

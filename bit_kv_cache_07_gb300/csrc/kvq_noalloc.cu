@@ -65,7 +65,7 @@ extern "C" kvq_status kvq_decode_attn_noalloc(const kvq_config* cfg, const void*
   kvq_status st = kvq::decode_setup(cfg, layer_buf, tokens, q, out, lse, &p, &persistent, &layout_ws);
   if (st != KVQ_OK) return st;
   uint64_t need = 0;
-  st = kvq::decode_plan_device(&p, persistent, &need);
+  st = kvq::decode_plan_device(&p, persistent, &need, /*widen=*/false);
   if (st != KVQ_OK) return st;
   if (need > kNoAllocScratchBytes) return KVQ_ERR_WORKSPACE;
   void* scratch = nullptr;

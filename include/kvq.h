@@ -205,8 +205,11 @@ kvq_status kvq_decode_attn(const kvq_config *cfg, const void *layer_buf, int32_t
                            const uint16_t *q, uint16_t *out, float *lse,
                            void *workspace, uint64_t ws_bytes, kvq_stream_t stream);
 
-/* Number of CTAs (splits per stream x streams) the decode launches for
- * `tokens`, and the splits per stream; host only.  For measurement. */
+/* The split-kernel plan for `tokens` on the host: splits per stream (CTAs
+ * per stream of the split-K kernel) and how many of them cover quantized
+ * groups; host only, for measurement.  With split_tokens = 0 the decode
+ * itself may raise the quantized splits (up to 64) so that its grid fills
+ * whole waves of the kernel's resident CTAs on the device it runs on. */
 kvq_status kvq_decode_plan(const kvq_config *cfg, int32_t tokens, int32_t *splits_per_stream,
                            int32_t *quantized_splits);
 
