@@ -988,13 +988,11 @@ cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t st, int* occ) {
   size_t smem = decode_smem_fixed<KB, GQ>();
   if (p.geo.pre_rope) smem += sizeof(float2) * kGroupTokens * (kHeadDim / 2);
   if (KB == 3) smem += 8 * (size_t)NuqStage::bytes(p.geo.nout) + 4 * GQ * kHeadDim * sizeof(float);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<KB, VB, GQ>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  static std::atomic<long long> smem_memo[kMemoDevices], occ_memo[kMemoDevices];
+  const cudaError_t e = ensure_smem_limit(decode_kernel<KB, VB, GQ>, smem_memo, (int)smem);
+  if (e != cudaSuccess) return e;
   if (occ)  // resident CTAs per SM, for sizing the grid; no launch
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, decode_kernel<KB, VB, GQ>, kThreads, (int)smem);
+    return occupancy_memo(decode_kernel<KB, VB, GQ>, occ_memo, kThreads, (int)smem, occ);
   dim3 grid(p.n_split, p.geo.NS);
   decode_kernel<KB, VB, GQ><<<grid, kThreads, smem, st>>>(p);
   return cudaGetLastError();

@@ -428,11 +428,9 @@ cudaError_t launch_t(const DecodeParams& p, cudaStream_t st) {
   constexpr int NT = GT <= 4 ? 1 : 2;
   using LY = PersistLayout<KB, VB, NT, GT>;
   const int smem = LY::kBytes;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(decode_persist_kernel<KB, VB, NT, GT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-  }
+  static std::atomic<long long> smem_memo[kMemoDevices];
+  cudaError_t e = ensure_smem_limit(decode_persist_kernel<KB, VB, NT, GT>, smem_memo, smem);
+  if (e != cudaSuccess) return e;
   const int ctas = (p.nwarps + LY::kWarps - 1) / LY::kWarps;
   return launch_dependent(decode_persist_kernel<KB, VB, NT, GT>, dim3(ctas), dim3(LY::kCtaThreads), smem, st, p);
 }
@@ -443,14 +441,11 @@ cudaError_t occupancy_t(int* warps_per_sm) {
   constexpr int NT = GT <= 4 ? 1 : 2;
   using LY = PersistLayout<KB, VB, NT, GT>;
   const int smem = LY::kBytes;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(decode_persist_kernel<KB, VB, NT, GT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-  }
+  static std::atomic<long long> smem_memo[kMemoDevices], occ_memo[kMemoDevices];
+  cudaError_t e = ensure_smem_limit(decode_persist_kernel<KB, VB, NT, GT>, smem_memo, smem);
+  if (e != cudaSuccess) return e;
   int ctas = 0;
-  const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctas, decode_persist_kernel<KB, VB, NT, GT>,
-                                                                      LY::kCtaThreads, smem);
+  e = occupancy_memo(decode_persist_kernel<KB, VB, NT, GT>, occ_memo, LY::kCtaThreads, smem, &ctas);
   *warps_per_sm = ctas * LY::kWarps;
   return e;
 }

@@ -43,10 +43,8 @@ cudaError_t plan_persist(DecodeParams& p, uint64_t* ws_need) {
   p.wt = (long long)mma::kF16Tokens * kHeadDim * 2 * 2;
   p.wstream = (long long)p.ng * p.wq + (long long)p.nt * p.wt;
   p.wtot = (long long)G.NS * p.wstream;
-  int dev = 0, sms = 0, occ = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int sms = 0, occ = 0;
+  cudaError_t e = device_sm_count(&sms);
   if (e != cudaSuccess) return e;
   e = dispatch(p, nullptr, &occ);
   if (e != cudaSuccess) return e;

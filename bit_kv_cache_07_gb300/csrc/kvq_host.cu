@@ -250,8 +250,9 @@ kvq_status decode_setup(const kvq_config* cfg, const void* layer_buf, int32_t to
     p.k_lut_off[i] = cfg->k_lut[i] - cfg->k_lut[0];
     p.v_lut_off[i] = cfg->v_lut[i] - cfg->v_lut[0];
   }
-  for (int i = 0; i < kHeadDim / 2; ++i)
-    p.theta[i] = std::pow((double)cfg->rope_theta, -2.0 * i / (double)kHeadDim);
+  if (g.pre_rope)  // RoPE frequencies (only the pre-RoPE paths read them)
+    for (int i = 0; i < kHeadDim / 2; ++i)
+      p.theta[i] = std::pow((double)cfg->rope_theta, -2.0 * i / (double)kHeadDim);
   *persistent = persist_eligible(g);
   *layout_ws = L.workspace_bytes;
   return KVQ_OK;
@@ -276,10 +277,8 @@ static uint64_t slots_of(const DecodeParams& p, bool persistent) {
 // during its last wave, and every CTA streams the same number of groups.
 static cudaError_t fill_waves(DecodeParams* p) {
   if (!p->auto_split || p->n_qsplit <= 0) return cudaSuccess;
-  int dev = 0, sms = 0, occ = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int sms = 0, occ = 0;
+  cudaError_t e = device_sm_count(&sms);
   if (e != cudaSuccess) return e;
   e = launch_decode(*p, nullptr, &occ);
   if (e != cudaSuccess) return e;

@@ -3,6 +3,7 @@
 // kvq_decode*.cu).  Not part of the public ABI (that is include/kvq.h).
 #pragma once
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cuda_fp16.h>
@@ -220,6 +221,71 @@ inline cudaError_t launch_dependent(void (*kernel)(Param), dim3 grid, dim3 block
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, arg);
+}
+
+// ----------------------------------------------- per-device launch memos
+// Facts that do not change within a process -- a device's SM count, a
+// kernel's raised shared-memory limit, its resident CTAs at a shared-memory
+// size -- are remembered per device (0 = not known yet; a race only repeats
+// a query), so that a decode call does not pay the runtime queries each time.
+constexpr int kMemoDevices = 64;
+
+inline int memo_slot() {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMemoDevices) return -1;
+  return d;
+}
+
+inline cudaError_t device_sm_count(int* sms) {
+  static std::atomic<long long> memo[kMemoDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool slot = dev >= 0 && dev < kMemoDevices;
+  if (slot) {
+    const long long v = memo[dev].load(std::memory_order_relaxed);
+    if (v > 0) {
+      *sms = (int)v;
+      return cudaSuccess;
+    }
+  }
+  e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess && slot) memo[dev].store(*sms, std::memory_order_relaxed);
+  return e;
+}
+
+// Raise a kernel's dynamic shared-memory limit to at least smem (memo: the
+// largest limit set per device).
+template <typename Kernel>
+inline cudaError_t ensure_smem_limit(Kernel kernel, std::atomic<long long>* memo, int smem) {
+  if (smem <= 48 * 1024) return cudaSuccess;
+  const int d = memo_slot();
+  if (d >= 0 && memo[d].load(std::memory_order_relaxed) >= smem) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess && d >= 0) {
+    long long cur = memo[d].load(std::memory_order_relaxed);
+    while (cur < smem && !memo[d].compare_exchange_weak(cur, smem, std::memory_order_relaxed)) {
+    }
+  }
+  return e;
+}
+
+// Resident CTAs per SM of a kernel at (threads, smem) (memo: the last size
+// asked per device; call after ensure_smem_limit).
+template <typename Kernel>
+inline cudaError_t occupancy_memo(Kernel kernel, std::atomic<long long>* memo, int threads, int smem, int* ctas) {
+  const int d = memo_slot();
+  if (d >= 0) {
+    const long long v = memo[d].load(std::memory_order_relaxed);
+    if (v > 0 && (v >> 16) == smem) {
+      *ctas = (int)(v & 0xFFFF) - 1;
+      return cudaSuccess;
+    }
+  }
+  const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kernel, threads, smem);
+  if (e == cudaSuccess && d >= 0 && *ctas >= 0 && *ctas < 0xFFFF)
+    memo[d].store(((long long)smem << 16) | (*ctas + 1), std::memory_order_relaxed);
+  return e;
 }
 
 // ------------------------------------------------------------ host hooks
