@@ -103,7 +103,7 @@ __device__ __forceinline__ float2 expi(double x) {
 // Groups from 2^16 on take the fp64 reduction.
 template <int GQ>
 __device__ __forceinline__ float2 anchor_expi(const DecodeParams& p, const DecodeSmem<GQ>& sm, int j, int g) {
-  if (g >= (1 << 16)) return expi((double)(p.geo.S + g * kGroupTokens) * p.theta[j]);
+  if (g >= (1 << 16)) return expi(((double)p.geo.S + (double)g * kGroupTokens) * p.theta[j]);
   float t = anchor_turns(sm.anc_v[j], sm.anc_c0[j], g);
   t -= rintf(t);
   float sn, cs;
