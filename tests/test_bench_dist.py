@@ -75,3 +75,12 @@ def test_reference_arm_runs_on_rank0_only(world):
         mp.spawn(_ref_rank_main, args=(world, out), nprocs=world, join=True)
         got = dict(out)
     assert got[0] >= 1 and all(got[r] == 0 for r in range(1, world))
+
+
+def test_all_cores_oracle_timing_runs_workers():
+    """The all-cores CPU baseline: spawned oracle workers, one stream each;
+    the reported step time is positive and names the process count."""
+    import bench
+    r = bench.oracle_sample_all_cores("toy_k4v2_t1k", 0.2, procs=2)
+    assert r is not None and "unavailable" not in r, r
+    assert r["cores"] == 2 and r["kind"] == "oracle" and r["value"] > 0
