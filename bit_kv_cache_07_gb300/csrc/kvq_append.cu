@@ -32,13 +32,16 @@ constexpr int kRowVec = kRowHalves * 2 / 16;  // 16 x 16-byte chunks per row
 // quotients below 256) while RN(d / scale) is within half an ulp (< 7.7e-6)
 // of it, so both round to the same integer unless qa lies within 1e-4 of a
 // half-integer; there the IEEE division decides.
-__device__ __forceinline__ uint32_t uniform_code(float x, float mn, float scale, float rs, float qmax) {
+// (0 <= x - mn <= max - mn, so the quotient lies in [0, qmax (1 + 2^-23)]
+// and its rounding in [0, qmax]: the clamp of the definition never binds;
+// qa - rint(qa) is exact, and its magnitude exceeds 0.4999 exactly when qa
+// lies within 1e-4 of a half-integer.)
+__device__ __forceinline__ uint32_t uniform_code(float x, float mn, float scale, float rs) {
   if (scale == 0.0f) return 0u;
   const float d = __fsub_rn(x, mn);
   const float qa = __fmul_rn(d, rs);
   float r = rintf(qa);
-  if (fabsf(__fsub_rn(__fsub_rn(qa, truncf(qa)), 0.5f)) < 1e-4f) r = rintf(__fdiv_rn(d, scale));
-  r = fminf(fmaxf(r, 0.0f), qmax);
+  if (fabsf(__fsub_rn(qa, r)) > 0.4999f) r = rintf(__fdiv_rn(d, scale));
   return (uint32_t)r;
 }
 
@@ -276,19 +279,21 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
       }
     }
   } else {
-    const int c = tid;  // one channel per thread, over the group's tokens
-    float mn = half_bits_to_float(sK[0][c]), mx = mn;
+    const int c = tid;  // one channel per thread, over the group's tokens (held in registers)
+    float xk[kGroupTokens];
+#pragma unroll
+    for (int r = 0; r < kGroupTokens; ++r) xk[r] = half_bits_to_float(sK[r][c]);
+    float mn = xk[0], mx = xk[0];
+#pragma unroll
     for (int r = 1; r < kGroupTokens; ++r) {
-      const float x = half_bits_to_float(sK[r][c]);
-      mn = fminf(mn, x);
-      mx = fmaxf(mx, x);
+      mn = fminf(mn, xk[r]);
+      mx = fmaxf(mx, xk[r]);
     }
     const float qmax = (float)((1 << G.kb) - 1);
     const float scale = __fdiv_rn(__fsub_rn(mx, mn), qmax);
     const float rs = scale == 0.0f ? 0.0f : __frcp_rn(scale);
-#pragma unroll 8
-    for (int r = 0; r < kGroupTokens; ++r)
-      sCk[r][c] = (uint8_t)uniform_code(half_bits_to_float(sK[r][c]), mn, scale, rs, qmax);
+#pragma unroll
+    for (int r = 0; r < kGroupTokens; ++r) sCk[r][c] = (uint8_t)uniform_code(xk[r], mn, scale, rs);
     p.L.k_scales[((size_t)s * G.gcap + grp) * kHeadDim + c] =
         (uint32_t)float_to_half_bits(mn) | ((uint32_t)float_to_half_bits(scale) << 16);
   }
@@ -321,7 +326,7 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
       const float scale = __fdiv_rn(__fsub_rn(mx, mn), qmax);
       const float rs = scale == 0.0f ? 0.0f : __frcp_rn(scale);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) sCv[r][4 * lane + q] = (uint8_t)uniform_code(v[q], mn, scale, rs, qmax);
+      for (int q = 0; q < 4; ++q) sCv[r][4 * lane + q] = (uint8_t)uniform_code(v[q], mn, scale, rs);
       if (lane % seg == 0)
         p.L.v_scales[((size_t)s * G.qcap + i) * G.nvg + lane / seg] =
             (uint32_t)float_to_half_bits(mn) | ((uint32_t)float_to_half_bits(scale) << 16);

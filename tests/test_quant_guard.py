@@ -2,7 +2,8 @@
 
 The kernel computes code = clamp(rint(RN((x - mn) / scale)), 0, 2^b - 1) as
 rint(RN(d * RN(1 / scale))) and falls back to the IEEE division only when
-that product lies within 1e-4 of a half-integer.  This checks, in float32
+that product lies within 1e-4 of a half-integer (|qa - rint(qa)| > 0.4999);
+it drops the clamp, which never binds for x in [mn, mx].  This checks, in float32
 arithmetic on the host (the same correctly rounded operations the kernel
 uses), that the shortcut and the division give the same code everywhere
 outside the guard band, over random groups and over quotients placed right
@@ -18,12 +19,11 @@ def codes_both(x, mn, scale, qmax):
     d = (x - mn).astype(f)
     rs = (f(1.0) / scale).astype(f)
     qa = (d * rs).astype(f)
-    exact = np.rint((d / scale).astype(f))
+    exact = np.clip(np.rint((d / scale).astype(f)), 0, qmax)  # the definition, clamped
     fast = np.rint(qa)
-    guard = np.abs((qa - np.trunc(qa)).astype(f) - f(0.5)) < f(1e-4)
-    fast = np.where(guard, exact, fast)
-    clip = lambda r: np.clip(r, 0, qmax)
-    return clip(fast), clip(exact), guard
+    guard = np.abs((qa - fast).astype(f)) > f(0.4999)        # within 1e-4 of a half-integer
+    fast = np.where(guard, np.rint((d / scale).astype(f)), fast)  # the kernel: no clamp
+    return fast, exact, guard
 
 
 @pytest.mark.parametrize("bits", [2, 3, 4, 8])
