@@ -283,17 +283,8 @@ static cudaError_t fill_waves(DecodeParams* p) {
   e = launch_decode(*p, nullptr, &occ);
   if (e != cudaSuccess) return e;
   if (occ < 1) return cudaSuccess;
-  const long long resident = (long long)sms * occ, NS = p->geo.NS;
-  const int fp16_split = p->n_split - p->n_qsplit;
-  const long long waves = (NS * p->n_split + resident - 1) / resident;
-  const int ngroups = p->Nq / kGroupTokens;
-  long long q = waves * resident / NS - fp16_split;
-  if (q > kMaxQSplits) q = kMaxQSplits;
-  if (q > ngroups) q = ngroups;
-  if (q <= p->n_qsplit) return cudaSuccess;
-  p->gps = (ngroups + (int)q - 1) / (int)q;
-  p->n_qsplit = (ngroups + p->gps - 1) / p->gps;
-  p->n_split = p->n_qsplit + fp16_split;
+  p->gps = fill_waves_plan(p->geo.NS, (long long)sms * occ, p->Nq / kGroupTokens, p->gps, &p->n_qsplit,
+                           &p->n_split);
   return cudaSuccess;
 }
 

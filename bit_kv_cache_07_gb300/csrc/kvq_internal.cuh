@@ -223,6 +223,25 @@ inline cudaError_t launch_dependent(void (*kernel)(Param), dim3 grid, dim3 block
   return cudaLaunchKernelEx(&cfg, kernel, arg);
 }
 
+// Split kernel: raise the quantized splits (n_qsplit of n_split per stream,
+// the rest covering the fp16 tokens) so that NS x splits CTAs fill whole
+// waves of `resident` CTAs, at most kMaxQSplits and one group per split.
+// Returns the new groups per split (or the old one when nothing changes)
+// and updates the split counts.
+inline int fill_waves_plan(long long NS, long long resident, int ngroups, int gps, int* n_qsplit, int* n_split) {
+  if (*n_qsplit <= 0 || resident < 1) return gps;
+  const int fp16_split = *n_split - *n_qsplit;
+  const long long waves = (NS * *n_split + resident - 1) / resident;
+  long long q = waves * resident / NS - fp16_split;
+  if (q > kMaxQSplits) q = kMaxQSplits;
+  if (q > ngroups) q = ngroups;
+  if (q <= *n_qsplit) return gps;
+  const int per = (ngroups + (int)q - 1) / (int)q;
+  *n_qsplit = (ngroups + per - 1) / per;
+  *n_split = *n_qsplit + fp16_split;
+  return per;
+}
+
 // ----------------------------------------------- per-device launch memos
 // Facts that do not change within a process -- a device's SM count, a
 // kernel's raised shared-memory limit, its resident CTAs at a shared-memory

@@ -91,6 +91,31 @@ int main() {
         }
   }
   printf("anchor worst %.3g turns\n", worst);
+  // split-kernel grid widened to whole waves: the 1M-token NUQ layer's case,
+  // then every combination of a small grid of shapes
+  {
+    int nq = 29, ns = 29;
+    const int per = fill_waves_plan(32, 608, 32768, 1130, &nq, &ns);
+    ++cases;
+    if (nq != 38 || ns != 38 || per != 863) { printf("fill_waves 1M: %d %d %d\n", nq, ns, per); ++bad; }
+  }
+  for (int NS : {1, 8, 32, 200, 1024}) for (int ngroups : {1, 7, 64, 1000, 32768}) for (int f : {0, 1})
+    for (long long resident : {152LL, 456LL, 608LL}) for (int q0 : {1, 5, 29, 64}) {
+      if (q0 > ngroups) continue;
+      const int gps0 = (ngroups + q0 - 1) / q0;
+      int nq = (ngroups + gps0 - 1) / gps0, ns = nq + f;
+      const int nq0 = nq;
+      const int per = fill_waves_plan(NS, resident, ngroups, gps0, &nq, &ns);
+      ++cases;
+      // splits never drop, never exceed the cap or the groups, cover every group exactly once,
+      // and a widened grid is no larger than the whole waves the old one started
+      const long long waves = ((long long)NS * (nq0 + f) + resident - 1) / resident;
+      if (nq < nq0 || nq > kMaxQSplits || nq > ngroups || ns != nq + f || (long long)per * nq < ngroups ||
+          (long long)per * (nq - 1) >= ngroups || (nq > nq0 && (long long)NS * ns > waves * resident)) {
+        printf("fill_waves NS=%d ngroups=%d f=%d res=%lld q0=%d -> %d\n", NS, ngroups, f, resident, q0, nq);
+        ++bad;
+      }
+    }
   printf("cases %d bad %d\n", cases, bad);
   return bad != 0;
 }
