@@ -195,3 +195,48 @@ def test_quantization_error_ordering():
         errs[b] = np.max(_normwise(out, ref))
     assert errs[8] < 1e-2
     assert errs[4] > 8 * errs[8]
+
+
+def _fp16_stream(T, rng, V=None):
+    K = rng.standard_normal((T, D)).astype(np.float16)
+    if V is None:
+        V = rng.standard_normal((T, D)).astype(np.float16)
+    return K, V
+
+
+def test_softmax_weights_sum_to_one():
+    """A V that is the same vector for every token must come back exactly:
+    the weights sum to 1 (fp16 cache, and a quantized cache whose V rows
+    sit on the grid)."""
+    rng = np.random.default_rng(41)
+    # on the 4-bit grid of every 64-channel group: min -1, scale 1/8, codes 0 and 15 present
+    codes = rng.integers(0, 16, D)
+    codes[0], codes[1], codes[64], codes[65] = 0, 15, 0, 15
+    c = (-1.0 + codes / 8.0).astype(np.float16)
+    for cfg, T in [(make_cfg(16, 16), 300), (make_cfg(4, 4, S=4, R=32), 300)]:
+        K, _ = _fp16_stream(T, rng)
+        V = np.tile(c, (T, 1))
+        store = O.build_stream(cfg, K, V)
+        q = rng.standard_normal((2, D)).astype(np.float16)
+        out, _ = O.decode_stream(cfg, T, store, q)
+        assert np.allclose(out, c.astype(np.float64)[None, :], rtol=0, atol=1e-12)
+
+
+def test_split_lse_merge_equals_single_pass():
+    """Attention over a prefix and over the rest, merged by log-sum-exp with
+    the returned lse, equals the single pass over all tokens -- the merge the
+    split kernels perform, and the meaning of lse (natural log of the sum of
+    exp of the scaled logits)."""
+    rng = np.random.default_rng(43)
+    cfg = make_cfg(16, 16)
+    T, T1 = 500, 173
+    K, V = _fp16_stream(T, rng)
+    q = rng.standard_normal((3, D)).astype(np.float16)
+    full, lse = O.decode_stream(cfg, T, O.build_stream(cfg, K, V), q)
+    oa, la = O.decode_stream(cfg, T1, O.build_stream(cfg, K[:T1], V[:T1]), q)
+    ob, lb = O.decode_stream(cfg, T - T1, O.build_stream(cfg, K[T1:], V[T1:]), q)
+    m = np.maximum(la, lb)
+    wa, wb = np.exp(la - m), np.exp(lb - m)
+    merged = (wa[:, None] * oa + wb[:, None] * ob) / (wa + wb)[:, None]
+    assert np.allclose(merged, full, rtol=0, atol=1e-12)
+    assert np.allclose(m + np.log(wa + wb), lse, rtol=0, atol=1e-12)
