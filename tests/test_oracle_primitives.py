@@ -282,6 +282,14 @@ def test_rope_invariants():
         a = O.rope_apply(q, m, 1e4) @ O.rope_apply(k, n, 1e4)
         b = q @ O.rope_apply(k, n - m, 1e4)
         assert np.isclose(a, b, rtol=1e-9, atol=1e-9)
+    # at the million-token positions of the long-context layer the fp64
+    # angles still keep the relative-position property (rounding of
+    # pos * theta_i is ~1e-10 rad there)
+    for m, n in [(1_000_000, 1_048_575), (1_048_575, 1_048_575)]:
+        a = O.rope_apply(q, m, 1e4) @ O.rope_apply(k, n, 1e4)
+        b = q @ O.rope_apply(k, n - m, 1e4)
+        assert np.isclose(a, b, rtol=1e-8, atol=1e-8)
+        assert np.isclose(np.linalg.norm(O.rope_apply(k, n, 1e4)), np.linalg.norm(k))
 
 
 def test_nuq_golden():
