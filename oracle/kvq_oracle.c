@@ -25,9 +25,9 @@
  *  - "Hadamard rotation-based 2-bit quantization for KV cache compression":
  *    rotate V with a Hadamard matrix, quantize uniformly to 2 bits, apply the
  *    inverse after the attention sum.
- * The fp32 quantizer formula scale=(max-min)/(2^b-1),
- * code=clamp(rint((x-min)/scale),0,2^b-1) is fixed by the benchmark spec
- * of the method; fp64 is used for attention.
+ * The uniform quantizer (min/max per group, one shared scale) computes
+ * scale=(max-min)/(2^b-1) and code=clamp(rint((x-min)/scale),0,2^b-1) in
+ * fp32, correctly rounded step by step; attention is computed in fp64.
  *
  * Build: gcc -O2 -std=c11 -fPIC -shared -ffp-contract=off -fno-fast-math.
  * -ffp-contract=off matters: the fp32 quantizer must not fuse into FMA.
