@@ -111,6 +111,15 @@ CASES = {
     "fp16_mha": (16, 16, 1, 3, 3, 100, dict()),
     "fp16_g7": (16, 16, 1, 14, 2, 300, dict(S=4, R=16)),
     "fp16_rope": (16, 16, 1, 2, 1, 200, dict(rope=1)),
+    # 3 query heads per KV head fill 3 of the 4 head slots (one padded slot)
+    # in both kernels
+    "kv4_g3": (4, 4, 1, 6, 2, 500, dict(S=4, R=32)),
+    "k2v4_g3_hadamard": (2, 4, 2, 3, 1, 333, dict(S=2, R=16, had=1)),
+    "fp16_g3": (16, 16, 1, 3, 1, 150, dict()),
+    "nuq_rope_g3": (3, 3, 1, 3, 1, 300, dict(rope=1, nout=2)),
+    "k4v2_gv32_g3": (4, 2, 1, 6, 2, 300, dict(S=2, R=16, gv=32)),
+    # the cache filled to its capacity
+    "kv8_full_capacity": (8, 8, 1, 4, 2, 417, dict(S=4, R=64, max_tokens=417)),
 }
 
 
