@@ -196,9 +196,13 @@ kvq_status kvq_append(const kvq_config *cfg, void *layer_buf, int32_t tokens_bef
  *              before the first call (zero the whole workspace once); every
  *              call leaves them zero again.  Calls that share a workspace
  *              must not overlap on the GPU.
- * One kernel launch: each CTA streams its split of the packed cache once,
- * and the last CTA of each stream merges the splits (log-sum-exp) and
- * applies the inverse Hadamard rotation.
+ * One kernel launch.  The cache is cut into pieces that are each streamed
+ * once: contiguous ranges of 32-token groups and fp16 tokens per warp in the
+ * persistent tensor-core kernel (uniform K/V with 64-channel V groups, or
+ * the fp16 cache), or per-CTA splits in the split kernel (NUQ, pre-RoPE K,
+ * other V group sizes).  Whichever piece of a stream finishes last merges
+ * the stream's partial results by log-sum-exp and applies the inverse
+ * Hadamard rotation to the quantized part.
  * Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CAPACITY,
  * KVQ_ERR_WORKSPACE, KVQ_ERR_CUDA. */
 kvq_status kvq_decode_attn(const kvq_config *cfg, const void *layer_buf, int32_t tokens,
