@@ -2,10 +2,19 @@
 
 One step = one decode step of the whole model: for every layer, append the
 new token's K/V (kvq_append) and attend over the cache (kvq_decode_attn).
-Default workload: Llama-2-7B-shaped decode, 32 layers x 32 heads, head dim
-128, batch 8, context 4096, uniform KV4 cache (K per-channel over 32-token
-groups, V per-token over 64-channel groups, 4 sink + 64 recent fp16 tokens).
-The same step on a plain fp16 cache is timed beside it.
+Default workload: Llama-3-8B-shaped GQA decode, 32 layers x 32 query heads /
+8 KV heads, head dim 128, batch 16, context 32768, with a per-layer (K, V)
+bit pair drawn by seed from KV8, K8V4, KV4, K4V2, KV2 (layers 0, 1 and 31
+KV8); K per channel over 32-token groups, V per token over 64-channel
+groups, 4 sink + 128 recent fp16 tokens.  The same step on a plain fp16
+cache is timed beside it.
+
+The step time is the median of several timed rounds of exactly --steps
+CUDA-graph replays (the rounds repeat until at least 1.5 s has been timed,
+so that the clock sampler sees the timed region).  Each layer's decode
+kernel is timed separately inside a second captured copy of the step, with
+external CUDA events recorded around every decode launch; the roofline
+fraction comes from those in-graph durations.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
 instead, on a bounded sample of the same workload.
@@ -27,7 +36,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-WORKLOAD = "llama2_7b_kv4_t4k"
+WORKLOAD = "llama3_8b_mixed_t32k"
+HBM_NOMINAL_GBS = 8000.0  # the 8 TB/s HBM figure the metric names
 METRIC = "decode-attention µs/step and effective cache GB/s (fraction of 8 TB/s HBM) at 1 GB300"
 UNIT = "us/step"
 
@@ -35,8 +45,10 @@ UNIT = "us/step"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--min-timed-seconds", type=float, default=1.5,
+                    help="repeat rounds of exactly --steps graph replays until this much was timed")
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-fp16-baseline", action="store_true")
@@ -105,7 +117,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
@@ -139,16 +151,17 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def ncu_traffic(kernel_tag: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current decode kernel source (else None)."""
+def ncu_traffic(tag: str):
+    """DRAM bytes per decode launch (dram__bytes_read.sum + dram__bytes_write.sum)
+    from the committed ncu record for `tag` (decode:<workload>:<pair>), if it
+    was taken on the current decode kernel sources (else None)."""
     path = os.path.join(ROOT, "profiles", "decode_traffic.txt")
     if not os.path.exists(path):
         return None
     h = source_hash()
     for line in open(path):
         m = re.match(r"\s*(\S+)\s+src=(\w+)\s+traffic_per_launch=(\d+)", line)
-        if m and m.group(1) == kernel_tag and m.group(2) == h:
+        if m and m.group(1) == tag and m.group(2) == h:
             return int(m.group(3))
     return None
 
@@ -214,11 +227,19 @@ class Model:
         return sum(algorithmic_bytes(c, self.T) for c in self.cfgs)
 
     def launches_per_step(self):
+        """Kernel launches of one step: per layer the 1-token append's window
+        copy (plus a quantize launch when the append flushes a group) and the
+        decode."""
         n = 0
         for c in self.cfgs:
             n += 1  # fp16 window copy of the appended token
+            if window_counts(c, self.T)[1] > window_counts(c, self.T - 1)[1]:
+                n += 1  # the append flushes one 32-token group
             n += 1  # decode
         return n
+
+    def kernel_names(self):
+        return [self.binding.decode_kernel_name(c, self.T) for c in self.cfgs]
 
 
 def time_steps(model, stream, steps: int, warmup: int, per_kernel=True):
@@ -244,10 +265,13 @@ def time_steps(model, stream, steps: int, warmup: int, per_kernel=True):
     return total_ms, kern
 
 
-def time_graph(model, stream, steps: int, warmup: int):
+def time_graph(model, stream, steps: int, warmup: int, min_seconds: float = 1.5, max_rounds: int = 200):
     """One step (every layer's append + decode) captured once in a CUDA graph
-    and replayed: the per-step time without host launch gaps.  Returns
-    (ms per step, None) or (None, why) if the capture is not possible."""
+    and replayed: the per-step time without host launch gaps.  Rounds of
+    exactly `steps` replays are timed back to back (CUDA events on the
+    launching stream, one pair per round) until at least `min_seconds` of
+    GPU time has been timed; returns (median ms per step over the rounds,
+    rounds, None) or (None, 0, why) if the capture is not possible."""
     import torch
     try:
         g = torch.cuda.CUDAGraph()
@@ -256,24 +280,72 @@ def time_graph(model, stream, steps: int, warmup: int):
             model.step(stream)
         torch.cuda.synchronize()
     except Exception as e:  # pragma: no cover - reported in the JSON line
-        return None, f"graph capture failed: {type(e).__name__}: {e}"
+        return None, 0, f"graph capture failed: {type(e).__name__}: {e}"
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             g.replay()
     torch.cuda.synchronize()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # size the rounds from one untimed probe round
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        p0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        p1.record(stream)
+    torch.cuda.synchronize()
+    round_s = max(p0.elapsed_time(p1) * 1e-3, 1e-6)
+    rounds = max(1, min(max_rounds, int(min_seconds / round_s + 0.999)))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(rounds)]
     barrier()
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
-        t0.record(stream)
-        for _ in range(steps):
-            g.replay()
-        t1.record(stream)
+        for e0, e1 in evs:
+            e0.record(stream)
+            for _ in range(steps):
+                g.replay()
+            e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    ms = t0.elapsed_time(t1) / steps
+    per_round = [e0.elapsed_time(e1) / steps for e0, e1 in evs]
     del g
-    return ms, None
+    return statistics.median(per_round), rounds, None
+
+
+def _timing_event():
+    """A CUDA timing event that, recorded during stream capture, becomes an
+    event record node of the graph (so it is timed at every replay)."""
+    import torch
+    return torch.cuda.Event(enable_timing=True, external=True)
+
+
+def time_decode_in_graph(model, stream, steps: int, warmup: int):
+    """Each layer's decode kernel timed inside a replayed CUDA graph: the step
+    is captured with an external event recorded right before and right after
+    every decode launch, replayed `steps` times, and the per-layer durations
+    averaged.  Returns (per-layer mean ms, None) or (None, why)."""
+    import torch
+    try:
+        evs = [[_timing_event(), _timing_event()] for _ in range(model.L)]
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            model.step(stream, evs)
+        torch.cuda.synchronize()
+    except Exception as e:  # pragma: no cover - reported in the JSON line
+        return None, f"in-graph decode timing failed: {type(e).__name__}: {e}"
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    acc = [0.0] * model.L
+    for _ in range(steps):
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        for l in range(model.L):
+            acc[l] += evs[l][0].elapsed_time(evs[l][1])
+    del g
+    return [a / steps for a in acc], None
 
 
 def time_append(name: str, dev, T: int, stream, reps: int = 20):
@@ -460,6 +532,7 @@ def oracle_sample(name: str, seconds: float, layer_count: int | None = None):
     streams_per_step = w["layers"] * w["batch"] * w["n_kv_heads"]
     per_stream = spent / n
     return {
+        "streams": n, "seconds": spent,
         "value": per_stream * streams_per_step * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
         "sample": f"fp64 oracle decode of {n} (batch row, KV head) streams of layer 0 at T={T} "
                   f"(cycling over {nstore} prebuilt streams), "
@@ -524,19 +597,29 @@ def oracle_sample_all_cores(name: str, seconds: float, procs: int | None = None)
 
 
 def run_reference(args):
+    """The reference arm: the CPU oracle as written (one host core, fp64),
+    on the same workload.  Each of the warmup + steps "steps" times whole
+    single-stream decodes of layer 0 for a bounded wall-clock budget and
+    scales them to one full model step (every stream of every layer); the
+    line states how many stream decodes were timed and the scale factor."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     from bit_kv_cache_07_gb300 import workloads
     w = workloads.WORKLOADS[args.workload]
-    per_step = []
+    per_step, timed_streams, timed_s = [], 0, 0.0
     budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+    t_start = time.perf_counter()
     for i in range(args.warmup + args.steps):
         r = oracle_sample(args.workload, budget)
         if i >= args.warmup:
             per_step.append(r["value"])
+            timed_streams += r["streams"]
+            timed_s += r["seconds"]
+    wall = time.perf_counter() - t_start
     v = statistics.median(per_step)
-    cb = dict(r)
+    streams_per_step = w["layers"] * w["batch"] * w["n_kv_heads"]
+    cb = {k: r[k] for k in ("unit", "cores", "kind", "sample")}
     cb["value"] = v
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 0,
@@ -544,11 +627,62 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "layers": w["layers"], "batch": w["batch"],
                    "q_heads": w["n_q_heads"], "kv_heads": w["n_kv_heads"], "context": w["tokens"]},
+        "sampled": {
+            "what": "each step is a bounded sample, not a whole model step: single-stream oracle decodes "
+                    "of layer 0 at the full context, scaled to the step's streams",
+            "stream_decodes_timed": timed_streams, "seconds_timed": timed_s, "wall_seconds": wall,
+            "streams_per_model_step": streams_per_step,
+            "extrapolation_per_step": streams_per_step / max(1, timed_streams / max(1, args.steps)),
+        },
         "cpu_baseline": cb, "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
 
 # -------------------------------------------------------------------- main
+
+def _pair_name(c: dict) -> str:
+    if c["k_bits"] == 16:
+        return "FP16"
+    if c["k_bits"] == 3:
+        return "NUQ3"
+    return f"K{c['k_bits']}V{c['v_bits']}"
+
+
+def decode_roofline(model, per_layer_ms, peak, peak_kind, workload):
+    """Roofline object of the decode launches of one step (in-graph times),
+    plus a per-(K, V)-pair breakdown when the layers differ."""
+    names = model.kernel_names()
+    layer_bytes = [algorithmic_bytes(c, model.T) for c in model.cfgs]
+    total_b, total_ms = sum(layer_bytes), sum(per_layer_ms)
+    achieved = total_b / (total_ms * 1e-3) / 1e9
+    traffic = [ncu_traffic(f"decode:{workload}:{_pair_name(c)}") for c in model.cfgs]
+    by_pair = {}
+    for l, c in enumerate(model.cfgs):
+        e = by_pair.setdefault(_pair_name(c), {"kernel": names[l], "layers": 0, "ms": [], "bytes": layer_bytes[l],
+                                               "traffic": traffic[l]})
+        e["layers"] += 1
+        e["ms"].append(per_layer_ms[l])
+    pairs = {}
+    for k, e in by_pair.items():
+        us = statistics.mean(e["ms"]) * 1e3
+        gbs = e["bytes"] / (us * 1e-6) / 1e9
+        pairs[k] = {"kernel": e["kernel"], "layers": e["layers"], "decode_us": us, "bytes_per_launch": e["bytes"],
+                    "achieved_gbs": gbs, "frac": gbs / peak, "frac_of_8tbs": gbs / HBM_NOMINAL_GBS,
+                    "traffic": e["traffic"]}
+    kinds = sorted(set(names))
+    roof = {
+        "bound": "hbm",
+        "kernel": kinds[0] if len(kinds) == 1 else f"{len(kinds)} instantiations: " + "; ".join(kinds),
+        "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+        "frac": achieved / peak, "frac_of_8tbs": achieved / HBM_NOMINAL_GBS,
+        "traffic": (sum(traffic) / len(traffic)) if all(t is not None for t in traffic) else None,
+        "bytes_per_launch": total_b / len(layer_bytes),
+        "launch_us": total_ms * 1e3 / len(layer_bytes),
+        "timing": "mean in-graph decode duration per layer: external CUDA events recorded around each "
+                  "decode launch inside a captured step, replayed",
+    }
+    return roof, (pairs if len(pairs) > 1 else None)
+
 
 def main():
     args = parse()
@@ -568,23 +702,19 @@ def main():
     model = Model(args.workload, dev, fp16=False, layers=args.layers, tokens=args.tokens)
     clocks = ClockSampler(local)
     clocks.start()
-    total_ms, kern = time_steps(model, stream, args.steps, args.warmup)
-    g_ms, g_err = time_graph(model, stream, args.steps, args.warmup)
+    total_ms, _ = time_steps(model, stream, args.steps, args.warmup, per_kernel=False)
+    g_ms, rounds, g_err = time_graph(model, stream, args.steps, args.warmup, args.min_timed_seconds)
+    layer_ms, t_err = time_decode_in_graph(model, stream, args.steps, args.warmup)
     clk = clocks.stop()
     eager_ms = max_over_ranks(total_ms / args.steps)
     ms_step = max_over_ranks(g_ms) if g_ms is not None else eager_ms
+    if layer_ms is None:  # fall back to eager per-kernel events
+        _, kern = time_steps(model, stream, args.steps, 1, per_kernel=True)
+        layer_ms = [statistics.mean(kern[l::model.L]) for l in range(model.L)]
     dec_bytes = model.decode_bytes()
-    kern_ms = statistics.mean(kern)
     peak, peak_kind = measured_peaks()
-    achieved = (dec_bytes / model.L) / (kern_ms * 1e-3) / 1e9
-    # per (K bits, V bits) pair when the layers differ: mean decode µs and fraction of the peak
-    by_pair = {}
-    for l, c in enumerate(model.cfgs):
-        key = f"K{c['k_bits']}V{c['v_bits']}"
-        by_pair.setdefault(key, [[], algorithmic_bytes(c, model.T)])[0].extend(kern[l::model.L])
-    pairs = {k: {"layers": len(v[0]) // args.steps, "decode_us": statistics.mean(v[0]) * 1e3,
-                 "frac": v[1] / (statistics.mean(v[0]) * 1e-3) / 1e9 / peak} for k, v in by_pair.items()}
-    e2e_ms, h2d, d2h = time_e2e(model, stream, max(3, args.steps // 2), 2)
+    roof, pairs = decode_roofline(model, layer_ms, peak, peak_kind, args.workload)
+    e2e_ms, h2d, d2h = time_e2e(model, stream, max(3, args.steps), 2)
     e2e_ms = max_over_ranks(e2e_ms)
     launches = model.launches_per_step() * args.steps
     model_layers, model_T = model.L, model.T
@@ -595,21 +725,27 @@ def main():
     fp16 = None
     if not args.no_fp16_baseline:
         fmodel = Model(args.workload, dev, fp16=True, layers=args.layers, tokens=args.tokens)
-        f_ms, f_kern = time_steps(fmodel, stream, args.steps, args.warmup)
-        f_ms = f_ms / args.steps
-        fg_ms, _ = time_graph(fmodel, stream, args.steps, args.warmup)
-        f_ms = max_over_ranks(fg_ms if fg_ms is not None else f_ms)
+        fg_ms, _, _ = time_graph(fmodel, stream, args.steps, args.warmup, 0.0)
+        if fg_ms is None:
+            f_total, _ = time_steps(fmodel, stream, args.steps, args.warmup, per_kernel=False)
+            fg_ms = f_total / args.steps
+        f_ms = max_over_ranks(fg_ms)
+        f_layer_ms, _ = time_decode_in_graph(fmodel, stream, args.steps, args.warmup)
         f_bytes = fmodel.decode_bytes()
         fp16 = {"us_per_step": f_ms * 1e3, "cache_gbs": f_bytes / (f_ms * 1e-3) / 1e9,
-                "decode_kernel_us": statistics.mean(f_kern) * 1e3,
-                "decode_kernel_gbs": (f_bytes / fmodel.L) / (statistics.mean(f_kern) * 1e-3) / 1e9,
-                "bytes_per_step": f_bytes}
+                "bytes_per_step": f_bytes, "kernel": fmodel.kernel_names()[0]}
+        if f_layer_ms is not None:
+            f_dec = statistics.mean(f_layer_ms)
+            fp16.update(decode_kernel_us=f_dec * 1e3,
+                        decode_kernel_gbs=(f_bytes / fmodel.L) / (f_dec * 1e-3) / 1e9,
+                        decode_frac=(f_bytes / fmodel.L) / (f_dec * 1e-3) / 1e9 / peak)
         del fmodel
         torch.cuda.empty_cache()
 
     cpu = cpu_all = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_sample(args.workload, args.cpu_seconds)
+        cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
         cpu_all = oracle_sample_all_cores(args.workload, args.cpu_seconds)
 
     value = ms_step * 1e3
@@ -622,26 +758,29 @@ def main():
                    "context": model_T, "cache": w["pairs"], "n_sink": w["n_sink"], "n_recent": w["n_recent"],
                    "l2": "inputs larger than L2: %.2f GB of cache read per step" % (dec_bytes / 1e9),
                    "step": "per layer: kvq_append of 1 token + kvq_decode_attn",
-                   "timing": ("one step captured in a CUDA graph, replayed" if g_ms is not None else
+                   "timing": (f"one step captured in a CUDA graph; median over {rounds} timed rounds of "
+                              f"exactly {args.steps} replays" if g_ms is not None else
                               "eager launches (" + str(g_err) + ")")},
         "ms_per_step_eager": eager_ms,
         "cache_gbs": sum_over_ranks(dec_bytes / (ms_step * 1e-3) / 1e9),
+        "cache_frac_of_8tbs": dec_bytes / (ms_step * 1e-3) / 1e9 / HBM_NOMINAL_GBS,
         "cache_bytes_per_step": dec_bytes,
-        "roofline": {"bound": "hbm", "kernel": "decode_persist_kernel", "achieved": achieved, "peak": peak,
-                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": ncu_traffic(f"decode:{args.workload}"),
-                     "bytes_per_launch": dec_bytes / model_layers,
-                     "launch_us": kern_ms * 1e3},
-        "decode_by_pair": pairs if len(pairs) > 1 else None,
+        "roofline": roof,
+        "decode_by_pair": pairs,
         "append": append,
         "fp16_baseline": fp16,
         "speedup_vs_fp16": (fp16["us_per_step"] / value) if fp16 else None,
+        "byte_ratio_vs_fp16": (fp16["bytes_per_step"] / dec_bytes) if fp16 else None,
         "cpu_baseline": cpu,
         "cpu_baseline_all_cores": cpu_all,
-        "e2e": {"value": e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "how": "eager calls of the public C ABI per layer; this step's q and new K/V copied in from "
+                       "pinned host memory and every layer's output copied back, inside the timed region"},
         "gpu_launches": launches,
         "clocks": clk,
     }
+    if t_err:
+        line["roofline"]["timing_note"] = t_err
     if rank == 0:
         print(json.dumps(line), flush=True)
     if _DIST["on"]:

@@ -53,7 +53,7 @@ class kvq_layout(C.Structure):
 
 
 EXPORTS = ["kvq_layout_query", "kvq_append", "kvq_decode_attn", "kvq_decode_plan",
-           "kvq_status_string", "kvq_decode_attn_noalloc"]
+           "kvq_decode_path", "kvq_status_string", "kvq_decode_attn_noalloc"]
 
 _lib = None
 
@@ -81,6 +81,9 @@ def lib():
         L.kvq_decode_plan.argtypes = [C.POINTER(kvq_config), C.c_int32, C.POINTER(C.c_int32),
                                       C.POINTER(C.c_int32)]
         L.kvq_decode_plan.restype = C.c_int
+        L.kvq_decode_path.argtypes = [C.POINTER(kvq_config), C.c_int32, C.POINTER(C.c_int32),
+                                      C.POINTER(C.c_int32)]
+        L.kvq_decode_path.restype = C.c_int
         L.kvq_decode_attn_noalloc.argtypes = [C.POINTER(kvq_config), vp, C.c_int32, u16p, u16p, vp, vp]
         L.kvq_decode_attn_noalloc.restype = C.c_int
         L.kvq_status_string.argtypes = [C.c_int]
@@ -124,6 +127,24 @@ def kvq_decode_plan(cfg, tokens: int):
     a, b = C.c_int32(), C.c_int32()
     _check("kvq_decode_plan", lib().kvq_decode_plan(C.byref(_cfg(cfg)), int(tokens), C.byref(a), C.byref(b)))
     return a.value, b.value
+
+
+def kvq_decode_path(cfg, tokens: int):
+    """(persistent, gq_slots): whether the decode of `tokens` runs the persistent
+    tensor-core kernel (else the split-K kernel), and its head-slot count."""
+    a, b = C.c_int32(), C.c_int32()
+    _check("kvq_decode_path", lib().kvq_decode_path(C.byref(_cfg(cfg)), int(tokens), C.byref(a), C.byref(b)))
+    return bool(a.value), b.value
+
+
+def decode_kernel_name(cfg, tokens: int) -> str:
+    """Name of the kernel instantiation a decode launches (as ncu lists it)."""
+    c = _cfg(cfg)
+    persistent, gt = kvq_decode_path(c, tokens)
+    if persistent:
+        nt = 1 if gt <= 4 else 2
+        return f"decode_persist_kernel<{c.k_bits}, {c.v_bits}, {nt}, {gt}>"
+    return f"decode_kernel<{c.k_bits}, {c.v_bits}, {gt}>"
 
 
 def _ptr(t, what: str, dtype=None, numel: int | None = None, allow_none=False):

@@ -351,6 +351,17 @@ kvq_status kvq_decode_plan(const kvq_config* cfg, int32_t tokens, int32_t* split
   return KVQ_OK;
 }
 
+kvq_status kvq_decode_path(const kvq_config* cfg, int32_t tokens, int32_t* persistent, int32_t* gq_slots) {
+  Geometry g;
+  kvq_status st = make_geometry(cfg, &g);
+  if (st != KVQ_OK) return st;
+  if (tokens < 1) return KVQ_ERR_INVALID_ARG;
+  if (tokens > cfg->max_tokens) return KVQ_ERR_CAPACITY;
+  if (persistent) *persistent = persist_eligible(g) ? 1 : 0;
+  if (gq_slots) *gq_slots = g.g <= 1 ? 1 : g.g <= 2 ? 2 : g.g <= 4 ? 4 : 8;
+  return KVQ_OK;
+}
+
 kvq_status kvq_append(const kvq_config* cfg, void* layer_buf, int32_t tokens_before,
                       const uint16_t* k_new, const uint16_t* v_new, int32_t n_new,
                       kvq_stream_t stream) {

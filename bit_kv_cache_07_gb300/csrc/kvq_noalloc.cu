@@ -18,9 +18,12 @@
 //
 // Host code cannot use the array's name as a device address (in host code it
 // names a host-side stand-in), so the device address is fetched with
-// cudaGetSymbolAddress once per device, with that device current, the first
-// time this entry point runs on it.  Make that first call before any stream
-// capture begins.
+// cudaGetSymbolAddress, with the device current: on the first call on a
+// device, and again on every call whose stream is not being captured (after
+// a cudaDeviceReset the library's module is loaded anew and the array may sit
+// elsewhere).  A call made during stream capture reuses the address of the
+// last call outside capture, so make one call on each device before any
+// stream capture begins (and again after a device reset).
 #include <mutex>
 
 #include "kvq_internal.cuh"
@@ -37,14 +40,18 @@ void* g_scratch_ptr[kMaxDevices] = {};
 
 uint64_t round_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
-// Device address of the scratch array on the current device (looked up once).
-cudaError_t scratch_for_current_device(void** out) {
+// Device address of the scratch array on the current device: looked up
+// whenever `st` is not capturing, remembered for calls made during capture.
+cudaError_t scratch_for_current_device(cudaStream_t st, void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(st, &cap);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (!g_scratch_ptr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone || !g_scratch_ptr[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
@@ -68,9 +75,9 @@ extern "C" kvq_status kvq_decode_attn_noalloc(const kvq_config* cfg, const void*
   st = kvq::decode_plan_device(&p, persistent, &need, /*widen=*/false);
   if (st != KVQ_OK) return st;
   if (need > kNoAllocScratchBytes) return KVQ_ERR_WORKSPACE;
-  void* scratch = nullptr;
-  if (scratch_for_current_device(&scratch) != cudaSuccess) return KVQ_ERR_CUDA;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  void* scratch = nullptr;
+  if (scratch_for_current_device(cs, &scratch) != cudaSuccess) return KVQ_ERR_CUDA;
   // the split counters sit at the start of the scratch and must start at zero
   const uint64_t cnt = round_up((uint64_t)cfg->batch * cfg->n_kv_heads * 4, 256);
   if (need > 0 && cudaMemsetAsync(scratch, 0, cnt, cs) != cudaSuccess) return KVQ_ERR_CUDA;

@@ -217,6 +217,15 @@ kvq_status kvq_decode_attn(const kvq_config *cfg, const void *layer_buf, int32_t
 kvq_status kvq_decode_plan(const kvq_config *cfg, int32_t tokens, int32_t *splits_per_stream,
                            int32_t *quantized_splits);
 
+/* Which decode kernel kvq_decode_attn launches for `tokens` (host only, for
+ * measurement and tests): *persistent = 1 for the persistent tensor-core
+ * kernel (uniform 2/4/8-bit K and V with 64-channel V groups and no pre-RoPE
+ * K, or the fp16 cache), 0 for the split-K kernel (non-uniform codes,
+ * pre-RoPE K, 32- or 128-channel V groups).  *gq_slots = query-head slots per
+ * KV head the kernel is instantiated for (1, 2, 4 or 8).
+ * Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CAPACITY. */
+kvq_status kvq_decode_path(const kvq_config *cfg, int32_t tokens, int32_t *persistent, int32_t *gq_slots);
+
 /* kvq_decode_attn_noalloc -- kvq_decode_attn without a caller workspace.
  * The pages have no counterpart: this exists for callers that cannot
  * allocate device memory where they decode (a pool that owns all device
@@ -226,9 +235,11 @@ kvq_status kvq_decode_plan(const kvq_config *cfg, int32_t tokens, int32_t *split
  *   Arguments as kvq_decode_attn, minus workspace/ws_bytes.
  *   No cudaMalloc/cudaFree or other allocating call; the split counters are
  *   cleared with cudaMemsetAsync on `stream` before the launch.
- *   The first call on a device looks the array's device address up
- *   (cudaGetSymbolAddress, that device current): make it before any stream
- *   capture.
+ *   The array's device address is looked up (cudaGetSymbolAddress, that
+ *   device current) on every call whose stream is not being captured; a call
+ *   during stream capture reuses the last address looked up on its device.
+ *   So make one call on each device before any stream capture (and again
+ *   after a cudaDeviceReset, which may move the array).
  *   All calls share the array: calls that overlap on the GPU race; serialise
  *   them.
  * Errors: as kvq_decode_attn; KVQ_ERR_WORKSPACE when this call's scratch

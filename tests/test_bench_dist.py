@@ -63,7 +63,8 @@ def _ref_rank_main(rank: int, world: int, out):
 
     called = []
     bench.oracle_sample = lambda *a, **k: called.append(1) or {"value": 1.0, "unit": "us/step", "cores": 1,
-                                                                 "kind": "oracle", "sample": "stub"}
+                                                                 "kind": "oracle", "sample": "stub",
+                                                                 "streams": 3, "seconds": 0.1}
     bench.run_reference(Args())
     out[rank] = len(called)
 

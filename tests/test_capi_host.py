@@ -116,3 +116,19 @@ def test_decode_plan(B):
     assert qs == 64 and spl == 64
     L = B.kvq_layout_query(big)
     assert spl <= L.max_splits
+
+
+def test_decode_path(B):
+    """Which decode kernel a configuration takes (host only): the persistent
+    tensor-core kernel for uniform 2/4/8-bit K and V with 64-channel V groups
+    and no pre-RoPE K, or the fp16 cache; the split kernel otherwise."""
+    assert B.kvq_decode_path(base(), 900) == (True, 4)
+    assert B.kvq_decode_path(base(v_group_channels=32), 900) == (False, 4)
+    assert B.kvq_decode_path(base(k_pre_rope=1), 900)[0] is False
+    assert B.kvq_decode_path(base(k_bits=16, v_bits=16), 900) == (True, 4)
+    assert B.kvq_decode_path(base(n_q_heads=14), 900) == (True, 8)
+    assert B.decode_kernel_name(base(), 900) == "decode_persist_kernel<4, 2, 1, 4>"
+    assert B.decode_kernel_name(base(n_q_heads=2), 900) == "decode_persist_kernel<4, 2, 1, 1>"
+    assert B.decode_kernel_name(base(k_pre_rope=1), 900) == "decode_kernel<4, 2, 4>"
+    with pytest.raises(B.KvqError):
+        B.kvq_decode_path(base(), 1001)

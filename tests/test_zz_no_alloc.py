@@ -34,11 +34,29 @@ def _cfg(**kw):
     return c
 
 
-@pytest.mark.parametrize("kw", [dict(), dict(k_bits=4, v_bits=2, v_hadamard=1, n_q_heads=14)])
-def test_noalloc_matches_workspace_entry_point_twice(B, kw):
+_LUT_K = [-1.53, -0.88, -0.49, -0.16, 0.16, 0.49, 0.88, 1.53]
+_LUT_V = [-1.5, -0.9, -0.5, -0.15, 0.15, 0.5, 0.9, 1.5]
+
+# (config changes, kernel expected: True = persistent, False = split-K)
+CASES = {
+    "persistent_kv4_g4": (dict(), True),
+    "persistent_k4v2_hadamard_g7": (dict(k_bits=4, v_bits=2, v_hadamard=1, n_q_heads=14), True),
+    # the split-K kernel: its partials live in the fixed scratch, sized by the
+    # host plan (the fixed-scratch entry point does not widen the grid)
+    "split_nuq3_rope": (dict(k_bits=3, v_bits=3, k_pre_rope=1, outliers_per_vector=2, n_sink=0, n_recent=0,
+                             k_lut=_LUT_K, v_lut=_LUT_V), False),
+    "split_k4v4_gv32": (dict(v_group_channels=32), False),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_noalloc_matches_workspace_entry_point_twice(B, name):
     from bit_kv_cache_07_gb300 import synth
+    kw, want_persistent = CASES[name]
     cfg = _cfg(**kw)
     T = 2900
+    persistent, _ = B.kvq_decode_path(cfg, T)
+    assert persistent == want_persistent, "the case must exercise the intended decode kernel"
     K, V = synth.random_kv(cfg["batch"], cfg["n_kv_heads"], T, seed=77, device="cuda")
     layer = B.Layer(cfg)
     layer.append(0, K, V)
@@ -46,8 +64,9 @@ def test_noalloc_matches_workspace_entry_point_twice(B, kw):
     ref = torch.empty_like(q)
     ref_lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
     layer.decode(T, q, ref, ref_lse, B.new_workspace(cfg))
-    splits, _ = B.kvq_decode_plan(cfg, T)
-    assert splits > 1, "the case must use split-K scratch"
+    if not persistent:
+        splits, _ = B.kvq_decode_plan(cfg, T)
+        assert splits > 1, "the split-K case must use more than one split (scratch partials)"
     c = B.make_config(cfg)
     for call in range(2):
         out = torch.full_like(q, float("nan"))
