@@ -12,9 +12,9 @@ cache is timed beside it.
 The step time is the median of several timed rounds of exactly --steps
 CUDA-graph replays (the rounds repeat until at least 1.5 s has been timed,
 so that the clock sampler sees the timed region).  Each layer's decode
-kernel is timed separately inside a second captured copy of the step, with
-external CUDA events recorded around every decode launch; the roofline
-fraction comes from those in-graph durations.
+kernel time comes from decode-only CUDA graphs (one per (K, V) pair, its
+layers' decode launches back to back, replayed between two events); the
+roofline fraction comes from those in-graph durations.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
 instead, on a bounded sample of the same workload.
@@ -223,6 +223,10 @@ class Model:
             if ev is not None:
                 ev[l][1].record(stream)
 
+    def decode(self, l: int, stream):
+        c = self.layers[l]
+        self.binding.kvq_decode_attn(c.cfg, c.buf, self.T, self.q[l], self.out[l], None, self.ws, None, stream)
+
     def decode_bytes(self):
         return sum(algorithmic_bytes(c, self.T) for c in self.cfgs)
 
@@ -311,41 +315,44 @@ def time_graph(model, stream, steps: int, warmup: int, min_seconds: float = 1.5,
     return statistics.median(per_round), rounds, None
 
 
-def _timing_event():
-    """A CUDA timing event that, recorded during stream capture, becomes an
-    event record node of the graph (so it is timed at every replay)."""
+def time_decode_only(model, stream, steps: int, warmup: int):
+    """Each layer's decode kernel time, measured inside replayed CUDA graphs:
+    for every (K, V) pair, the decode launches of that pair's layers are
+    captured back to back in one graph (no appends, nothing between them), the
+    graph is replayed `steps` times between two CUDA events on the launching
+    stream, and the time is divided by the launches.  Every layer gets the
+    mean of its pair.  Returns (per-layer ms, None) or (None, why)."""
     import torch
-    return torch.cuda.Event(enable_timing=True, external=True)
-
-
-def time_decode_in_graph(model, stream, steps: int, warmup: int):
-    """Each layer's decode kernel timed inside a replayed CUDA graph: the step
-    is captured with an external event recorded right before and right after
-    every decode launch, replayed `steps` times, and the per-layer durations
-    averaged.  Returns (per-layer mean ms, None) or (None, why)."""
-    import torch
-    try:
-        evs = [[_timing_event(), _timing_event()] for _ in range(model.L)]
-        g = torch.cuda.CUDAGraph()
-        torch.cuda.synchronize()
-        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
-            model.step(stream, evs)
-        torch.cuda.synchronize()
-    except Exception as e:  # pragma: no cover - reported in the JSON line
-        return None, f"in-graph decode timing failed: {type(e).__name__}: {e}"
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            g.replay()
-    torch.cuda.synchronize()
-    acc = [0.0] * model.L
-    for _ in range(steps):
+    groups = {}
+    for l, c in enumerate(model.cfgs):
+        groups.setdefault(_pair_name(c), []).append(l)
+    per_layer = [0.0] * model.L
+    for pair, layers in groups.items():
+        try:
+            g = torch.cuda.CUDAGraph()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                for l in layers:
+                    model.decode(l, stream)
+            torch.cuda.synchronize()
+        except Exception as e:  # pragma: no cover - reported in the JSON line
+            return None, f"decode-only graph capture failed: {type(e).__name__}: {e}"
         with torch.cuda.stream(stream):
-            g.replay()
+            for _ in range(warmup):
+                g.replay()
         torch.cuda.synchronize()
-        for l in range(model.L):
-            acc[l] += evs[l][0].elapsed_time(evs[l][1])
-    del g
-    return [a / steps for a in acc], None
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / (steps * len(layers))
+        for l in layers:
+            per_layer[l] = ms
+        del g
+    return per_layer, None
 
 
 def time_append(name: str, dev, T: int, stream, reps: int = 20):
@@ -502,26 +509,40 @@ def sum_over_ranks(x: float) -> float:
 
 # -------------------------------------------------------------- CPU oracle
 
+_ORACLE_STREAMS = {}
+
+
+def _oracle_streams(name: str):
+    """Up to 4 prebuilt oracle streams of layer 0 of a workload at its full
+    context, with their queries (built once per process; not timed)."""
+    if name not in _ORACLE_STREAMS:
+        from bit_kv_cache_07_gb300 import synth, workloads
+        from oracle import kvq_oracle as O
+        w = workloads.WORKLOADS[name]
+        T = w["tokens"]
+        cfg = workloads.layer_config(name, 0)
+        if cfg["k_bits"] == 3:
+            cfg["k_lut"] = synth.nuq_lut(name, 0, "k")
+            cfg["v_lut"] = synth.nuq_lut(name, 0, "v")
+        g = w["n_q_heads"] // w["n_kv_heads"]
+        K, V = synth.layer_kv(name, 0, tokens=T, batch=1, device="cpu")
+        q = synth.query(name, 0, batch=1, device="cpu").numpy()
+        Kh, Vh = K.numpy(), V.numpy()
+        nstore = min(4, w["n_kv_heads"])
+        stores = [O.build_stream(cfg, Kh[0, h], Vh[0, h]) for h in range(nstore)]
+        _ORACLE_STREAMS[name] = (cfg, T, g, q, stores)
+    return _ORACLE_STREAMS[name]
+
+
 def oracle_sample(name: str, seconds: float, layer_count: int | None = None):
     """Time the CPU oracle (single thread, as written) decoding whole streams of
     layer 0 at the workload's context until ~seconds have passed; scale the
     per-stream time to one full decode step (all streams of all layers)."""
-    import numpy as np
-    import torch
-    from bit_kv_cache_07_gb300 import synth, workloads
+    from bit_kv_cache_07_gb300 import workloads
     from oracle import kvq_oracle as O
     w = workloads.WORKLOADS[name]
-    T = w["tokens"]
-    cfg = workloads.layer_config(name, 0)
-    if cfg["k_bits"] == 3:
-        cfg["k_lut"] = synth.nuq_lut(name, 0, "k")
-        cfg["v_lut"] = synth.nuq_lut(name, 0, "v")
-    g = w["n_q_heads"] // w["n_kv_heads"]
-    K, V = synth.layer_kv(name, 0, tokens=T, batch=1, device="cpu")
-    q = synth.query(name, 0, batch=1, device="cpu").numpy()
-    Kh, Vh = K.numpy(), V.numpy()
-    nstore = min(4, w["n_kv_heads"])
-    stores = [O.build_stream(cfg, Kh[0, h], Vh[0, h]) for h in range(nstore)]
+    cfg, T, g, q, stores = _oracle_streams(name)
+    nstore = len(stores)
     n, spent = 0, 0.0
     while spent < seconds or n < 3:
         h = n % nstore
@@ -678,8 +699,8 @@ def decode_roofline(model, per_layer_ms, peak, peak_kind, workload):
         "traffic": (sum(traffic) / len(traffic)) if all(t is not None for t in traffic) else None,
         "bytes_per_launch": total_b / len(layer_bytes),
         "launch_us": total_ms * 1e3 / len(layer_bytes),
-        "timing": "mean in-graph decode duration per layer: external CUDA events recorded around each "
-                  "decode launch inside a captured step, replayed",
+        "timing": "mean decode duration per layer: each (K, V) pair's decode launches captured back to "
+                  "back in a CUDA graph, replayed between two CUDA events, divided by the launches",
     }
     return roof, (pairs if len(pairs) > 1 else None)
 
@@ -704,7 +725,7 @@ def main():
     clocks.start()
     total_ms, _ = time_steps(model, stream, args.steps, args.warmup, per_kernel=False)
     g_ms, rounds, g_err = time_graph(model, stream, args.steps, args.warmup, args.min_timed_seconds)
-    layer_ms, t_err = time_decode_in_graph(model, stream, args.steps, args.warmup)
+    layer_ms, t_err = time_decode_only(model, stream, args.steps, args.warmup)
     clk = clocks.stop()
     eager_ms = max_over_ranks(total_ms / args.steps)
     ms_step = max_over_ranks(g_ms) if g_ms is not None else eager_ms
@@ -730,7 +751,7 @@ def main():
             f_total, _ = time_steps(fmodel, stream, args.steps, args.warmup, per_kernel=False)
             fg_ms = f_total / args.steps
         f_ms = max_over_ranks(fg_ms)
-        f_layer_ms, _ = time_decode_in_graph(fmodel, stream, args.steps, args.warmup)
+        f_layer_ms, _ = time_decode_only(fmodel, stream, args.steps, args.warmup)
         f_bytes = fmodel.decode_bytes()
         fp16 = {"us_per_step": f_ms * 1e3, "cache_gbs": f_bytes / (f_ms * 1e-3) / 1e9,
                 "bytes_per_step": f_bytes, "kernel": fmodel.kernel_names()[0]}

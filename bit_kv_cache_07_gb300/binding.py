@@ -34,7 +34,7 @@ class kvq_config(C.Structure):
         ("n_sink", C.c_int32), ("n_recent", C.c_int32), ("v_hadamard", C.c_int32),
         ("k_pre_rope", C.c_int32), ("rope_theta", C.c_float), ("outliers_per_vector", C.c_int32),
         ("k_lut", C.c_float * 8), ("v_lut", C.c_float * 8), ("softmax_scale", C.c_float),
-        ("split_tokens", C.c_int32),
+        ("split_tokens", C.c_int32), ("position_offset", C.c_int32),
     ]
 
 
@@ -53,7 +53,8 @@ class kvq_layout(C.Structure):
 
 
 EXPORTS = ["kvq_layout_query", "kvq_append", "kvq_decode_attn", "kvq_decode_plan",
-           "kvq_decode_path", "kvq_status_string", "kvq_decode_attn_noalloc"]
+           "kvq_decode_path", "kvq_status_string", "kvq_decode_attn_noalloc", "kvq_context_shard",
+           "kvq_merge_attn"]
 
 _lib = None
 
@@ -84,6 +85,11 @@ def lib():
         L.kvq_decode_path.argtypes = [C.POINTER(kvq_config), C.c_int32, C.POINTER(C.c_int32),
                                       C.POINTER(C.c_int32)]
         L.kvq_decode_path.restype = C.c_int
+        L.kvq_context_shard.argtypes = [C.POINTER(kvq_config), C.c_int32, C.c_int32, C.c_int32,
+                                        C.POINTER(kvq_config), C.POINTER(C.c_int32), C.POINTER(C.c_int32)]
+        L.kvq_context_shard.restype = C.c_int
+        L.kvq_merge_attn.argtypes = [C.c_int32, C.c_int64, C.c_int32, vp, vp, vp, vp, vp]
+        L.kvq_merge_attn.restype = C.c_int
         L.kvq_decode_attn_noalloc.argtypes = [C.POINTER(kvq_config), vp, C.c_int32, u16p, u16p, vp, vp]
         L.kvq_decode_attn_noalloc.restype = C.c_int
         L.kvq_status_string.argtypes = [C.c_int]
@@ -219,6 +225,40 @@ def kvq_decode_attn_noalloc(cfg, layer_buf, tokens: int, q, out, lse=None, strea
         _ptr(q, "q", torch.float16, nq), _ptr(out, "out", torch.float16, nq),
         _ptr(lse, "lse", torch.float32, c.batch * c.n_q_heads * 4, allow_none=True), _stream(stream))
     _check("kvq_decode_attn_noalloc", st)
+
+
+def config_dict(c: kvq_config) -> dict:
+    """The fields of a kvq_config as a dict (the inverse of make_config)."""
+    d = {}
+    for name, _ in kvq_config._fields_:
+        v = getattr(c, name)
+        d[name] = [float(x) for x in v] if name in ("k_lut", "v_lut") else v
+    return d
+
+
+def kvq_context_shard(cfg, tokens: int, n_shards: int, shard: int):
+    """(shard config dict, first token, tokens) of one shard of a context of
+    `tokens` tokens cut into n_shards (host only; see include/kvq.h)."""
+    out = kvq_config()
+    a, n = C.c_int32(), C.c_int32()
+    _check("kvq_context_shard", lib().kvq_context_shard(C.byref(_cfg(cfg)), int(tokens), int(n_shards), int(shard),
+                                                        C.byref(out), C.byref(a), C.byref(n)))
+    return config_dict(out), a.value, n.value
+
+
+def kvq_merge_attn(outs, lses, out, lse_out=None, stream=None):
+    """Merge n parts' outputs [n, rows.., 128] fp16 and lse [n, rows..] f32
+    into out [rows.., 128] fp16 (and lse_out), by log-sum-exp."""
+    import torch
+    n = outs.shape[0]
+    rows = outs[0].numel() // outs.shape[-1]
+    if lses.shape[0] != n or lses[0].numel() != rows:
+        raise ValueError("lses must be [n_parts, rows]")
+    st = lib().kvq_merge_attn(
+        n, rows, int(outs.shape[-1]), _ptr(outs, "outs", torch.float16, n * rows * 256),
+        _ptr(lses, "lses", torch.float32, n * rows * 4), _ptr(out, "out", torch.float16, rows * 256),
+        _ptr(lse_out, "lse_out", torch.float32, rows * 4, allow_none=True), _stream(stream))
+    _check("kvq_merge_attn", st)
 
 
 # ------------------------------------------------------------ conveniences

@@ -103,7 +103,8 @@ __device__ __forceinline__ float2 expi(double x) {
 // Groups from 2^16 on take the fp64 reduction.
 template <int GQ>
 __device__ __forceinline__ float2 anchor_expi(const DecodeParams& p, const DecodeSmem<GQ>& sm, int j, int g) {
-  if (g >= (1 << 16)) return expi(((double)p.geo.S + (double)g * kGroupTokens) * p.theta[j]);
+  if (g >= (1 << 16))
+    return expi(((double)p.geo.pos_offset + (double)p.geo.S + (double)g * kGroupTokens) * p.theta[j]);
   float t = anchor_turns(sm.anc_v[j], sm.anc_c0[j], g);
   t -= rintf(t);
   float sn, cs;
@@ -437,8 +438,9 @@ __device__ __forceinline__ void fp16_chunk(const DecodeParams& p, const float (*
           const float2 a2 = __half22float2(*reinterpret_cast<const __half2*>(&wa[h]));
           const float2 b2 = __half22float2(*reinterpret_cast<const __half2*>(&wb[h]));
           const int j = i * 8 + 2 * h;
-          const float2 e0 = expi((double)pos * p.theta[j]);
-          const float2 e1 = expi((double)pos * p.theta[j + 1]);
+          const double apos = (double)G.pos_offset + (double)pos;  // absolute position
+          const float2 e0 = expi(apos * p.theta[j]);
+          const float2 e1 = expi(apos * p.theta[j + 1]);
           const float ra0 = a2.x * e0.x - b2.x * e0.y, rb0 = b2.x * e0.x + a2.x * e0.y;
           const float ra1 = a2.y * e1.x - b2.y * e1.y, rb1 = b2.y * e1.x + a2.y * e1.y;
 #pragma unroll
@@ -754,7 +756,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     sm.lut_v[tid] = p.v_lut_off[tid];
   }
   if (G.pre_rope)
-    for (int j = tid; j < kHeadDim / 2; j += kThreads) anchor_step(p.theta[j], G.S, &sm.anc_v[j], &sm.anc_c0[j]);
+    for (int j = tid; j < kHeadDim / 2; j += kThreads)
+      anchor_step(p.theta[j], (long long)G.pos_offset + G.S, &sm.anc_v[j], &sm.anc_c0[j]);
   const bool quant_split = sp < p.n_qsplit;
   if (G.pre_rope && quant_split) {
     // e^{i l theta_j} at [j][l]: a warp reads one j for its 32 token offsets l,

@@ -33,6 +33,8 @@ kvq_status make_geometry(const kvq_config* c, Geometry* g) {
     return KVQ_ERR_INVALID_ARG;
   if (!(c->softmax_scale >= 0.0f) || !std::isfinite(c->softmax_scale)) return KVQ_ERR_INVALID_ARG;
   if (c->k_pre_rope && !(c->rope_theta > 0.0f && std::isfinite(c->rope_theta))) return KVQ_ERR_INVALID_ARG;
+  if (c->position_offset < 0 || (int64_t)c->position_offset + c->max_tokens >= (int64_t)1 << 31)
+    return KVQ_ERR_INVALID_ARG;
   if (c->head_dim != kHeadDim) return KVQ_ERR_UNSUPPORTED;
   if (c->n_q_heads / c->n_kv_heads > kMaxGQA) return KVQ_ERR_UNSUPPORTED;
   const int64_t ns = (int64_t)c->batch * c->n_kv_heads;
@@ -76,6 +78,7 @@ kvq_status make_geometry(const kvq_config* c, Geometry* g) {
   g->pre_rope = c->k_pre_rope;
   g->nout = (c->k_bits == 3) ? c->outliers_per_vector : 0;
   g->rope_theta = c->rope_theta;
+  g->pos_offset = c->position_offset;
   if (fp16) {
     g->S = 0;
     g->R = 0;
@@ -360,6 +363,51 @@ kvq_status kvq_decode_path(const kvq_config* cfg, int32_t tokens, int32_t* persi
   if (persistent) *persistent = persist_eligible(g) ? 1 : 0;
   if (gq_slots) *gq_slots = g.g <= 1 ? 1 : g.g <= 2 ? 2 : g.g <= 4 ? 4 : 8;
   return KVQ_OK;
+}
+
+kvq_status kvq_context_shard(const kvq_config* cfg, int32_t tokens, int32_t n_shards, int32_t shard,
+                             kvq_config* shard_cfg, int32_t* first_token, int32_t* shard_tokens) {
+  Geometry g;
+  kvq_status st = make_geometry(cfg, &g);
+  if (st != KVQ_OK) return st;
+  if (!shard_cfg || !first_token || !shard_tokens) return KVQ_ERR_INVALID_ARG;
+  if (n_shards < 1 || n_shards > 65536 || shard < 0 || shard >= n_shards || tokens < 1) return KVQ_ERR_INVALID_ARG;
+  if (tokens > cfg->max_tokens) return KVQ_ERR_CAPACITY;
+  // shard r starts at the quantized-group boundary S + 32 floor(r ng / n)
+  // (fp16 cache: the 32-token block boundary), shard 0 at token 0
+  int S_eff, Nq, W;
+  counts(g, tokens, &S_eff, &Nq, &W);
+  const int64_t ng = g.fp16_mode ? tokens / kGroupTokens : Nq / kGroupTokens;
+  const int64_t base = g.fp16_mode ? 0 : g.S;
+  auto bound = [&](int64_t r) -> int64_t {
+    if (r <= 0) return 0;
+    if (r >= n_shards) return tokens;
+    const int64_t b = base + kGroupTokens * (r * ng / n_shards);
+    return b < tokens ? b : tokens;
+  };
+  const int64_t a = bound(shard), b = bound(shard + 1);
+  const bool last = shard == n_shards - 1;
+  *shard_cfg = *cfg;
+  shard_cfg->n_sink = shard == 0 ? cfg->n_sink : 0;
+  shard_cfg->n_recent = last ? cfg->n_recent : 0;
+  shard_cfg->position_offset = cfg->position_offset + (int32_t)a;
+  const int64_t cap = last ? (int64_t)cfg->max_tokens - a : b - a;
+  shard_cfg->max_tokens = (int32_t)(cap > 0 ? cap : 1);
+  *first_token = (int32_t)a;
+  *shard_tokens = (int32_t)(b - a);
+  return KVQ_OK;
+}
+
+kvq_status kvq_merge_attn(int32_t n_parts, int64_t rows, int32_t head_dim, const uint16_t* outs,
+                          const float* lses, uint16_t* out, float* lse_out, kvq_stream_t stream) {
+  if (n_parts < 1 || rows < 0) return KVQ_ERR_INVALID_ARG;
+  if (head_dim != kHeadDim) return KVQ_ERR_UNSUPPORTED;
+  if (rows == 0) return KVQ_OK;
+  if (!outs || !lses || !out) return KVQ_ERR_INVALID_ARG;
+  if (((uintptr_t)outs | (uintptr_t)out) % 8 || ((uintptr_t)lses | (uintptr_t)lse_out) % 4) return KVQ_ERR_INVALID_ARG;
+  const cudaError_t e =
+      launch_merge_attn(n_parts, rows, outs, lses, out, lse_out, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
 kvq_status kvq_append(const kvq_config* cfg, void* layer_buf, int32_t tokens_before,

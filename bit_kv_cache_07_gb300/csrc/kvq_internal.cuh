@@ -27,6 +27,7 @@ struct Geometry {
   int S, R, ring, qcap, gcap;
   int krow, vrow;
   int hadamard, pre_rope, nout, fp16_mode;
+  int pos_offset;  // absolute position of the cache's first token (RoPE)
   float rope_theta;
 };
 
@@ -163,12 +164,13 @@ __host__ __device__ inline int owner_of(const DecodeParams& p, long long pos) {
 }
 
 // ----------------------------------------------------- RoPE group anchors
-// For RoPE frequency theta (radians per position) and S sinks: the
-// per-group angle step 32 theta / (2 pi) in turns, split into three parts of
-// at most 8 significant bits (exact products with a group index below 2^16)
-// and the rest (below 2^-21 of the step), and the anchor of group 0
-// (position S) in turns.  fp64, once per CTA on the device.
-__host__ __device__ inline void anchor_step(double theta, int S, float4* v4, float* c0) {
+// For RoPE frequency theta (radians per position) and the absolute position
+// S of the first quantized token: the per-group angle step 32 theta / (2 pi)
+// in turns, split into three parts of at most 8 significant bits (exact
+// products with a group index below 2^16) and the rest (below 2^-21 of the
+// step), and the anchor of group 0 (position S) in turns.  fp64, once per
+// CTA on the device.
+__host__ __device__ inline void anchor_step(double theta, long long S, float4* v4, float* c0) {
   const double turns = theta / (2.0 * 3.14159265358979323846);
   double v = turns * kGroupTokens, parts[3];
   for (int i = 0; i < 3; ++i) {
@@ -180,7 +182,7 @@ __host__ __device__ inline void anchor_step(double theta, int S, float4* v4, flo
     }
   }
   *v4 = make_float4((float)parts[0], (float)parts[1], (float)parts[2], (float)v);
-  const double a = turns * S;
+  const double a = turns * (double)S;
   *c0 = (float)(a - floor(a));
 }
 // The anchor angle of a channel pair (step parts v, start c0) in group
@@ -308,6 +310,8 @@ inline cudaError_t occupancy_memo(Kernel kernel, std::atomic<long long>* memo, i
 }
 
 // ------------------------------------------------------------ host hooks
+cudaError_t launch_merge_attn(int n_parts, long long rows, const uint16_t* outs, const float* lses,
+                              uint16_t* out, float* lse_out, cudaStream_t st);
 cudaError_t launch_append_quantize(const AppendParams& p, int n_groups, cudaStream_t st);
 cudaError_t launch_append_window(const AppendParams& p, cudaStream_t st);
 // Split-K decode; with occ != nullptr it only reports the kernel's resident

@@ -21,7 +21,7 @@ PAIR_ORDER = ["KV8", "K8V4", "KV4", "K4V2", "KV2"]
 
 _BASE = dict(head_dim=128, k_group_tokens=32, v_group_channels=64, n_sink=0, n_recent=0,
              v_hadamard=0, k_pre_rope=0, rope_theta=10000.0, outliers_per_vector=0,
-             softmax_scale=0.0, split_tokens=0)
+             softmax_scale=0.0, split_tokens=0, position_offset=0)
 
 WORKLOADS = {
     "toy_k4v2_t1k": dict(

@@ -87,6 +87,12 @@ typedef struct kvq_config {
     float softmax_scale;      /* 0 selects 1/sqrt(d)                           */
     int32_t split_tokens;     /* decode: quantized tokens per split-K chunk
                                  (multiple of G_K); 0 selects automatically    */
+    int32_t position_offset;  /* absolute position of the cache's first token
+                                 (0 for a whole context; the first token of a
+                                 context shard, see kvq_context_shard): RoPE
+                                 after dequantization rotates the key at
+                                 position_offset + t.  >= 0, and
+                                 position_offset + max_tokens < 2^31           */
 } kvq_config;
 
 /* Window rule.  For a sequence holding T tokens:
@@ -247,6 +253,45 @@ kvq_status kvq_decode_path(const kvq_config *cfg, int32_t tokens, int32_t *persi
 kvq_status kvq_decode_attn_noalloc(const kvq_config *cfg, const void *layer_buf, int32_t tokens,
                                    const uint16_t *q, uint16_t *out, float *lse,
                                    kvq_stream_t stream);
+
+/* Context-parallel decode (KVQuant summary, abstract and main results: a
+ * 10M-token context on an 8-GPU system).  The context of every sequence is
+ * cut into n_shards contiguous shards at quantized-group boundaries, each
+ * held by its own cache (one per GPU): shard 0 keeps the S sink tokens, the
+ * last shard the fp16 recent window, every shard an equal share (+-1) of
+ * the Nq / G_K quantized groups (fp16 cache: of the 32-token blocks).  The
+ * union of the shards' caches holds exactly the groups, scales, sinks and
+ * window of one cache of the whole context, so decoding every shard with
+ * the same query and merging the results by log-sum-exp (kvq_merge_attn)
+ * gives the attention over the whole context.  Appended tokens go to the
+ * last shard.
+ *
+ * kvq_context_shard -- host only.  For a context of `tokens` tokens (at the
+ * time the shards are filled), fills *shard_cfg (cfg with n_sink = S on
+ * shard 0 and 0 elsewhere, n_recent = R on the last shard and 0 elsewhere,
+ * position_offset = cfg->position_offset + *first_token, max_tokens = the
+ * shard's tokens, or what is left of cfg->max_tokens on the last shard),
+ * *first_token and *shard_tokens (0 for a shard that holds no token: it
+ * takes part in the merge as an empty part, lse = -inf, and is not decoded).
+ * Errors: KVQ_ERR_INVALID_ARG (n_shards < 1 or > 65536, shard out of range,
+ * tokens < 1), KVQ_ERR_CAPACITY, and the config errors of kvq_layout_query. */
+kvq_status kvq_context_shard(const kvq_config *cfg, int32_t tokens, int32_t n_shards, int32_t shard,
+                             kvq_config *shard_cfg, int32_t *first_token, int32_t *shard_tokens);
+
+/* kvq_merge_attn -- attention over the union of n_parts disjoint parts of a
+ * context from each part's normalised output and log-sum-exp (the decode's
+ * out and lse):  lse = log sum_r exp(lse_r),  out = sum_r exp(lse_r - lse) out_r.
+ * (The same merge the decode applies to its own split partials.)
+ *   outs     device fp16 [n_parts][rows][head_dim]
+ *   lses     device f32  [n_parts][rows], natural log; -inf marks an empty part
+ *   out      device fp16 [rows][head_dim] (may not alias outs)
+ *   lse_out  device f32  [rows] or NULL (-inf where every part is empty; out
+ *            is then 0)
+ * rows = batch * n_q_heads; head_dim = 128.  One launch, fp32 arithmetic.
+ * Errors: KVQ_ERR_INVALID_ARG (n_parts < 1, rows < 0, null or misaligned
+ * pointers), KVQ_ERR_UNSUPPORTED (head_dim), KVQ_ERR_CUDA. */
+kvq_status kvq_merge_attn(int32_t n_parts, int64_t rows, int32_t head_dim, const uint16_t *outs,
+                          const float *lses, uint16_t *out, float *lse_out, kvq_stream_t stream);
 
 /* Static string naming a status code. */
 const char *kvq_status_string(kvq_status status);

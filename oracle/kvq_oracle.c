@@ -307,6 +307,9 @@ typedef struct orc_cfg {
     double sm_scale;      /* softmax scale (1/sqrt(d) when 0) */
     float k_lut[8];
     float v_lut[8];
+    int32_t pos_offset;   /* absolute position of the stream's first token (a
+                             context shard that starts later); RoPE angles use
+                             pos_offset + t */
 } orc_cfg;
 
 /* Sinks are positions [0, S).  The quantized tokens are the
@@ -467,7 +470,7 @@ static void token_k(const orc_cfg *c, const orc_store *st, int S, int Nq, int t,
         }
     }
     if (c->k_pre_rope)
-        orc_rope_apply(kr, d, (double)t, c->rope_theta);
+        orc_rope_apply(kr, d, (double)c->pos_offset + (double)t, c->rope_theta);
 }
 
 /* V of token t as stored, in fp64: dequantized (still in the rotated domain
@@ -562,4 +565,41 @@ void orc_decode_stream(const orc_cfg *c, int T, int g, const uint16_t *q,
         lse[h] = mx[h] + log(L[h]);
     }
     free(qv); free(logit); free(mx); free(L); free(oq); free(ow);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Merge of attention results over disjoint parts of one context.           */
+/* ------------------------------------------------------------------------ */
+
+/* n parts of the same query rows (rows of d channels each): part r has the
+ * normalised output o_r = sum_{t in r} p_t v_t / sum_{t in r} p_t and
+ * lse_r = log sum_{t in r} exp(logit_t) (-inf for an empty part).  The
+ * attention over the union is
+ *   lse = log sum_r exp(lse_r),   o = sum_r exp(lse_r - lse) o_r.
+ * outs [n][rows][d], lses [n][rows]; out [rows][d], lse [rows]; fp64.  The
+ * largest lse_r is subtracted before exponentiating (an exact identity). */
+void orc_merge_parts(int n, int rows, int d, const double *outs, const double *lses,
+                     double *out, double *lse)
+{
+    for (int i = 0; i < rows; i++) {
+        double m = -INFINITY;
+        for (int r = 0; r < n; r++)
+            if (lses[(size_t)r * rows + i] > m) m = lses[(size_t)r * rows + i];
+        double L = 0.0;
+        for (int ch = 0; ch < d; ch++) out[(size_t)i * d + ch] = 0.0;
+        if (m == -INFINITY) {   /* every part empty */
+            lse[i] = -INFINITY;
+            continue;
+        }
+        for (int r = 0; r < n; r++) {
+            double lr = lses[(size_t)r * rows + i];
+            if (lr == -INFINITY) continue;
+            double w = exp(lr - m);
+            L += w;
+            for (int ch = 0; ch < d; ch++)
+                out[(size_t)i * d + ch] += w * outs[((size_t)r * rows + i) * d + ch];
+        }
+        for (int ch = 0; ch < d; ch++) out[(size_t)i * d + ch] /= L;
+        lse[i] = m + log(L);
+    }
 }

@@ -43,7 +43,7 @@ class _Cfg(C.Structure):
         ("gk", C.c_int32), ("gv", C.c_int32), ("n_sink", C.c_int32),
         ("n_recent", C.c_int32), ("v_hadamard", C.c_int32), ("k_pre_rope", C.c_int32),
         ("outliers", C.c_int32), ("rope_theta", C.c_double), ("sm_scale", C.c_double),
-        ("k_lut", C.c_float * 8), ("v_lut", C.c_float * 8),
+        ("k_lut", C.c_float * 8), ("v_lut", C.c_float * 8), ("pos_offset", C.c_int32),
     ]
 
 
@@ -78,6 +78,7 @@ def lib():
         L.orc_build_stream.argtypes = [C.POINTER(_Cfg), C.c_int, u16, u16,
                                        u8, u16, u8, u16, u16, u16, u16, u16,
                                        i32, u8, u16, i32, u8, u16]
+        L.orc_merge_parts.argtypes = [C.c_int, C.c_int, C.c_int, f64, f64, f64, f64]
         L.orc_decode_stream.argtypes = [C.POINTER(_Cfg), C.c_int, C.c_int, u16,
                                         u8, u16, u8, u16, u16, u16, u16, u16,
                                         i32, u8, u16, i32, u8, u16, f64, f64]
@@ -188,6 +189,7 @@ def _cfg(cfg: dict) -> _Cfg:
     c.outliers = cfg.get("outliers_per_vector", 0)
     c.rope_theta = cfg.get("rope_theta", 10000.0)
     c.sm_scale = cfg.get("softmax_scale", 0.0)
+    c.pos_offset = cfg.get("position_offset", 0)
     for i, v in enumerate(cfg.get("k_lut", [0.0] * 8)):
         c.k_lut[i] = v
     for i, v in enumerate(cfg.get("v_lut", [0.0] * 8)):
@@ -293,4 +295,20 @@ def decode_layer(cfg: dict, T: int, stores: list, q, streams=None):
         o, l = decode_stream(cfg, T, stores[s], q[b, h * g:(h + 1) * g])
         out[b, h * g:(h + 1) * g] = o
         lse[b, h * g:(h + 1) * g] = l
+    return out, lse
+
+
+def merge_parts(outs, lses):
+    """Attention over the union of n disjoint context parts from each part's
+    normalised output and log-sum-exp: outs [n, ..., d], lses [n, ...]
+    (fp64; -inf marks an empty part) -> (out [..., d], lse [...])."""
+    outs = np.ascontiguousarray(outs, np.float64)
+    lses = np.ascontiguousarray(lses, np.float64)
+    n, d = outs.shape[0], outs.shape[-1]
+    rows = int(np.prod(outs.shape[1:-1])) if outs.ndim > 2 else 1
+    assert lses.shape == outs.shape[:-1]
+    out = np.zeros(outs.shape[1:], np.float64)
+    lse = np.zeros(lses.shape[1:], np.float64)
+    lib().orc_merge_parts(n, rows, d, _P(outs, C.c_double), _P(lses, C.c_double),
+                          _P(out, C.c_double), _P(lse, C.c_double))
     return out, lse

@@ -28,12 +28,12 @@ def B():
 
 
 def cfg_dict(kb, vb, Bt, Hq, Hkv, T, S=0, R=0, gv=64, had=0, rope=0, nout=0, max_tokens=None, split=0,
-             lut_seed=None):
+             lut_seed=None, offset=0):
     c = dict(batch=Bt, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=128,
              max_tokens=T + 40 if max_tokens is None else max_tokens, k_bits=kb, v_bits=vb,
              k_group_tokens=32, v_group_channels=gv, n_sink=S, n_recent=R, v_hadamard=had,
              k_pre_rope=rope, rope_theta=10000.0, outliers_per_vector=nout, softmax_scale=0.0,
-             split_tokens=split, k_lut=[0.0] * 8, v_lut=[0.0] * 8)
+             split_tokens=split, position_offset=offset, k_lut=[0.0] * 8, v_lut=[0.0] * 8)
     if kb == 3:
         from bit_kv_cache_07_gb300 import synth
         c["k_lut"] = synth.lut_from_seed(1000 + (lut_seed or 0))
@@ -118,6 +118,11 @@ CASES = {
     "fp16_g3": (16, 16, 1, 3, 1, 150, dict()),
     "nuq_rope_g3": (3, 3, 1, 3, 1, 300, dict(rope=1, nout=2)),
     "k4v2_gv32_g3": (4, 2, 1, 6, 2, 300, dict(S=2, R=16, gv=32)),
+    # RoPE at absolute positions that start far from 0 (a later context shard):
+    # the group anchors, the fp64 fallback past 2^16 groups and the fp16 tokens
+    "nuq_rope_offset": (3, 3, 1, 2, 2, 700, dict(rope=1, nout=2, offset=2_000_003)),
+    "k4v4_rope_offset_sinks": (4, 4, 1, 4, 1, 500, dict(S=4, R=16, rope=1, offset=123_456)),
+    "fp16_rope_offset": (16, 16, 1, 2, 1, 200, dict(rope=1, offset=999_999)),
     # the cache filled to its capacity
     "kv8_full_capacity": (8, 8, 1, 4, 2, 417, dict(S=4, R=64, max_tokens=417)),
 }

@@ -15,13 +15,15 @@ D = 128
 
 
 def dense_attention(cfg, q, K, V):
-    """q [B,Hq,d], K,V [B,Hkv,T,d] (fp64) -> out [B,Hq,d], lse [B,Hq]."""
+    """q [B,Hq,d], K,V [B,Hkv,T,d] (fp64) -> out [B,Hq,d], lse [B,Hq].
+    Token t sits at position position_offset + t."""
     B, Hq, d = q.shape
     Hkv, T = K.shape[1], K.shape[2]
     K = K.copy()
     if cfg.get("k_pre_rope"):
         th = cfg["rope_theta"] ** (-2.0 * np.arange(d // 2) / d)
-        z = (K[..., : d // 2] + 1j * K[..., d // 2:]) * np.exp(1j * np.arange(T)[:, None] * th)
+        pos = cfg.get("position_offset", 0) + np.arange(T)
+        z = (K[..., : d // 2] + 1j * K[..., d // 2:]) * np.exp(1j * pos[:, None] * th)
         K = np.concatenate([z.real, z.imag], -1)
     Kx = np.repeat(K, Hq // Hkv, axis=1)
     Vx = np.repeat(V, Hq // Hkv, axis=1)
@@ -240,3 +242,85 @@ def test_split_lse_merge_equals_single_pass():
     merged = (wa[:, None] * oa + wb[:, None] * ob) / (wa + wb)[:, None]
     assert np.allclose(merged, full, rtol=0, atol=1e-12)
     assert np.allclose(m + np.log(wa + wb), lse, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("kb", [3, 4])
+def test_pre_rope_position_offset_equals_dense(kb):
+    """A stream whose first token sits at absolute position 1_000_003 (a
+    later context shard): RoPE after dequantization uses that position."""
+    kw = dict(k_pre_rope=1, position_offset=1_000_003)
+    if kb == 3:
+        kw.update(outliers_per_vector=2, k_lut=list(_lut(5)), v_lut=list(_lut(6)))
+        cfg = make_cfg(3, 3, **kw)
+    else:
+        cfg = make_cfg(4, 4, S=2, R=16, **kw)
+    out, lse, ref, rlse = run_layer(cfg, 1, 4, 2, 200, seed=51)
+    assert np.allclose(out, ref, rtol=0, atol=1e-10)
+    assert np.allclose(lse, rlse, rtol=0, atol=1e-10)
+    cfg0 = dict(cfg, position_offset=0)
+    out0, _, _, _ = run_layer(cfg0, 1, 4, 2, 200, seed=51)
+    assert np.abs(out0 - out).max() > 1e-3  # the offset changes the result
+
+
+def _parts_by_hand(cfg, T, cuts):
+    """Context parts at the quantized-group boundaries S + 32 * c for c in
+    cuts: part 0 keeps the sinks, the last part the fp16 window; every other
+    part is quantized groups only.  Returns [(first token, tokens, part cfg)]."""
+    S, R = cfg["n_sink"], cfg["n_recent"]
+    bounds = [0] + [S + 32 * c for c in cuts] + [T]
+    parts = []
+    for r in range(len(bounds) - 1):
+        a, b = bounds[r], bounds[r + 1]
+        pc = dict(cfg, position_offset=a, n_sink=S if r == 0 else 0,
+                  n_recent=R if r == len(bounds) - 2 else 0)
+        parts.append((a, b - a, pc))
+    return parts
+
+
+@pytest.mark.parametrize("kind", ["kv4_sinks_window", "nuq_rope", "hadamard_k4v2", "fp16"])
+def test_merge_parts_equals_single_pass(kind):
+    """The context cut into parts at group boundaries, each part stored and
+    decoded on its own (sinks in the first, the window in the last, RoPE at
+    absolute positions), then merged by log-sum-exp, equals the decode of
+    the whole context: same quantized groups, same softmax.  An empty part
+    (lse = -inf) contributes nothing."""
+    rng = np.random.default_rng(61)
+    T = 900
+    if kind == "kv4_sinks_window":
+        cfg = make_cfg(4, 4, S=4, R=64)
+    elif kind == "nuq_rope":
+        cfg = make_cfg(3, 3, k_pre_rope=1, outliers_per_vector=2, k_lut=list(_lut(7)), v_lut=list(_lut(8)))
+    elif kind == "hadamard_k4v2":
+        cfg = make_cfg(4, 2, S=2, R=32, v_hadamard=1)
+    else:
+        cfg = make_cfg(16, 16)
+    K = rng.standard_normal((T, D)).astype(np.float16)
+    V = rng.laplace(size=(T, D)).astype(np.float16)
+    q = rng.standard_normal((4, D)).astype(np.float16)
+    full, flse = O.decode_stream(cfg, T, O.build_stream(cfg, K, V), q)
+    _, Nq, _ = O.layout_counts(cfg, T)
+    ng = Nq // 32 if cfg["k_bits"] != 16 else T // 32
+    cuts = [ng // 3, ng // 3, (2 * ng) // 3]  # the second part is empty
+    outs, lses = [], []
+    for a, n, pc in _parts_by_hand(cfg, T, cuts):
+        if n == 0:
+            outs.append(np.zeros((4, D)))
+            lses.append(np.full(4, -np.inf))
+            continue
+        o, l = O.decode_stream(pc, n, O.build_stream(pc, K[a:a + n], V[a:a + n]), q)
+        outs.append(o)
+        lses.append(l)
+    merged, mlse = O.merge_parts(np.stack(outs), np.stack(lses))
+    assert np.allclose(merged, full, rtol=0, atol=1e-12)
+    assert np.allclose(mlse, flse, rtol=0, atol=1e-12)
+
+
+def test_merge_parts_closed_form():
+    """Two parts with known lse: weights e^lse_r / sum; all parts empty gives
+    lse -inf and a zero output."""
+    o = np.array([[[1.0, 0.0]], [[0.0, 1.0]]])
+    out, lse = O.merge_parts(o, np.array([[np.log(3.0)], [np.log(1.0)]]))
+    assert np.allclose(out, [[0.75, 0.25]], rtol=0, atol=1e-15)
+    assert np.allclose(lse, [np.log(4.0)], rtol=0, atol=1e-15)
+    out, lse = O.merge_parts(o, np.full((2, 1), -np.inf))
+    assert lse[0] == -np.inf and not out.any()
