@@ -192,8 +192,8 @@ class Model:
         for l in range(self.L):
             cfg = workloads.layer_config(name, l, tokens=self.T)
             if cfg["k_bits"] == 3:
-                cfg["k_lut"] = synth.nuq_lut(name, l, "k")
-                cfg["v_lut"] = synth.nuq_lut(name, l, "v")
+                from bit_kv_cache_07_gb300 import calibrate
+                cfg["k_lut"], cfg["v_lut"] = calibrate.nuq_tables(name, l, device=device)
             if fp16:
                 cfg = workloads.fp16_baseline_config(cfg)
             layer = binding.Layer(cfg, device=device)
@@ -366,8 +366,8 @@ def time_append(name: str, dev, T: int, stream, reps: int = 20):
     from bit_kv_cache_07_gb300 import binding, synth, workloads
     cfg = workloads.layer_config(name, 0, tokens=T)
     if cfg["k_bits"] == 3:
-        cfg["k_lut"] = synth.nuq_lut(name, 0, "k")
-        cfg["v_lut"] = synth.nuq_lut(name, 0, "v")
+        from bit_kv_cache_07_gb300 import calibrate
+        cfg["k_lut"], cfg["v_lut"] = calibrate.nuq_tables(name, 0, device=dev)
     layer = binding.Layer(cfg, device=dev)
     K, V = synth.layer_kv(name, 0, tokens=T - 1, device=dev)
     k1, v1 = synth.new_token_kv(name, 0, 0, device=dev)
@@ -512,6 +512,20 @@ def sum_over_ranks(x: float) -> float:
 _ORACLE_STREAMS = {}
 
 
+def _oracle_tables(name: str, layer: int):
+    """The CPU-baseline leg's level tables: a fitted workload's tables are
+    fitted by the oracle on CPU-drawn calibration tokens (nothing here comes
+    from the CUDA path); otherwise the seeded quantile tables."""
+    from bit_kv_cache_07_gb300 import synth, workloads
+    from oracle import kvq_oracle as O
+    w = workloads.WORKLOADS[name]
+    if w.get("lut") != "fitted":
+        return synth.nuq_lut(name, layer, "k"), synth.nuq_lut(name, layer, "v")
+    K, V = synth.layer_kv(name, layer, tokens=w["lut_calib_tokens"], batch=1, device="cpu")
+    k = w["outliers_per_vector"]
+    return O.nuq_fit_lut(K.numpy(), k)[0], O.nuq_fit_lut(V.numpy(), k, w["v_hadamard"])[0]
+
+
 def _oracle_streams(name: str):
     """Up to 4 prebuilt oracle streams of layer 0 of a workload at its full
     context, with their queries (built once per process; not timed)."""
@@ -522,8 +536,7 @@ def _oracle_streams(name: str):
         T = w["tokens"]
         cfg = workloads.layer_config(name, 0)
         if cfg["k_bits"] == 3:
-            cfg["k_lut"] = synth.nuq_lut(name, 0, "k")
-            cfg["v_lut"] = synth.nuq_lut(name, 0, "v")
+            cfg["k_lut"], cfg["v_lut"] = _oracle_tables(name, 0)
         g = w["n_q_heads"] // w["n_kv_heads"]
         K, V = synth.layer_kv(name, 0, tokens=T, batch=1, device="cpu")
         q = synth.query(name, 0, batch=1, device="cpu").numpy()
@@ -571,8 +584,7 @@ def _oracle_worker(name: str, head: int, seconds: float):
     T = w["tokens"]
     cfg = workloads.layer_config(name, 0)
     if cfg["k_bits"] == 3:
-        cfg["k_lut"] = synth.nuq_lut(name, 0, "k")
-        cfg["v_lut"] = synth.nuq_lut(name, 0, "v")
+        cfg["k_lut"], cfg["v_lut"] = _oracle_tables(name, 0)
     g = w["n_q_heads"] // w["n_kv_heads"]
     K, V = synth.layer_kv(name, 0, tokens=T, batch=1, device="cpu")
     q = synth.query(name, 0, batch=1, device="cpu").numpy()

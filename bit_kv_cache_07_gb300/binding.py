@@ -54,7 +54,8 @@ class kvq_layout(C.Structure):
 
 EXPORTS = ["kvq_layout_query", "kvq_append", "kvq_decode_attn", "kvq_decode_plan",
            "kvq_decode_path", "kvq_status_string", "kvq_decode_attn_noalloc", "kvq_context_shard",
-           "kvq_merge_attn"]
+           "kvq_merge_attn", "kvq_fit_nuq_lut"]
+NUQ_FIT_WORKSPACE_BYTES = 3 * 65538 * 8
 
 _lib = None
 
@@ -90,6 +91,9 @@ def lib():
         L.kvq_context_shard.restype = C.c_int
         L.kvq_merge_attn.argtypes = [C.c_int32, C.c_int64, C.c_int32, vp, vp, vp, vp, vp]
         L.kvq_merge_attn.restype = C.c_int
+        L.kvq_fit_nuq_lut.argtypes = [vp, C.c_int64, C.c_int32, C.c_int32, C.c_int32, C.c_int32, vp, C.c_uint64,
+                                      vp, vp, vp]
+        L.kvq_fit_nuq_lut.restype = C.c_int
         L.kvq_decode_attn_noalloc.argtypes = [C.POINTER(kvq_config), vp, C.c_int32, u16p, u16p, vp, vp]
         L.kvq_decode_attn_noalloc.restype = C.c_int
         L.kvq_status_string.argtypes = [C.c_int]
@@ -244,6 +248,28 @@ def kvq_context_shard(cfg, tokens: int, n_shards: int, shard: int):
     _check("kvq_context_shard", lib().kvq_context_shard(C.byref(_cfg(cfg)), int(tokens), int(n_shards), int(shard),
                                                         C.byref(out), C.byref(a), C.byref(n)))
     return config_dict(out), a.value, n.value
+
+
+def kvq_fit_nuq_lut(x, outliers: int, hadamard: int = 0, max_iters: int = 100, workspace=None, stream=None):
+    """Fit a non-uniform level table to the vectors x [..., 128] (fp16, on
+    the GPU).  Returns (lut as a list of 8 floats, updates made or -1); the
+    call synchronises `stream` to read the result."""
+    import torch
+    d = x.shape[-1]
+    n = x.numel() // d
+    if workspace is None:
+        workspace = torch.empty(NUQ_FIT_WORKSPACE_BYTES, dtype=torch.uint8, device=x.device)
+    lut = torch.empty(8, dtype=torch.float32, device=x.device)
+    info = torch.empty(1, dtype=torch.int32, device=x.device)
+    st = lib().kvq_fit_nuq_lut(_ptr(x, "x", torch.float16, n * d * 2), n, d, int(outliers), int(hadamard),
+                               int(max_iters), _ptr(workspace, "workspace", numel=NUQ_FIT_WORKSPACE_BYTES),
+                               NUQ_FIT_WORKSPACE_BYTES, lut.data_ptr(), info.data_ptr(), _stream(stream))
+    _check("kvq_fit_nuq_lut", st)
+    if stream is not None and not isinstance(stream, int):
+        stream.synchronize()
+    else:
+        torch.cuda.synchronize(x.device)
+    return [float(v) for v in lut.cpu()], int(info.item())
 
 
 def kvq_merge_attn(outs, lses, out, lse_out=None, stream=None):

@@ -52,21 +52,14 @@ __device__ __forceinline__ void nuq_midpoints(const float* lut, float (&tau)[7])
   for (int i = 0; i < 7; ++i) tau[i] = __fsub_rn(__fmul_rn(__fadd_rn(lut[i], lut[i + 1]), 0.5f), lut[0]);
 }
 
-// Non-uniform (LUT) encoding of one 128-channel token vector held by a warp
-// (lane l owns channels 4l..4l+3).  The k largest |x| (ties to the lower
-// channel) become fp16 outliers with code 0; the dense rest is mapped
-// affinely onto [L0, L7] and coded by counting the level midpoints below
-// u = RN((x - mn) / s).  u comes from RN(d * RN(1 / s)), which is within
-// 3 * 2^-24 relative of it; only when that product lies within 2^-21
-// relative of a midpoint does the IEEE division decide.
-__device__ void nuq_encode_row(const uint16_t* __restrict__ xrow, const float* lut, const float (&tau)[7], int k,
-                               uint8_t* __restrict__ code_row, uint32_t* minsc_out,
-                               uint8_t* col_out, uint16_t* val_out, int lane) {
-  float v[4];
-  bool is_out[4] = {false, false, false, false};
+// The k largest |v| of a token vector held by a warp (lane l: channels
+// 4l..4l+3), ties to the lower channel: is_out marks this lane's outliers,
+// sel[j] is the channel of the j-th largest (past k: a value that sorts
+// last).  The dense min and max of the rest come back in mn, mx.
+__device__ __forceinline__ void nuq_outliers(const float (&v)[4], int k, int lane, bool (&is_out)[4],
+                                             int (&sel)[kMaxOutliers], float& mn, float& mx) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) v[q] = half_bits_to_float(xrow[4 * lane + q]);
-  int sel[kMaxOutliers];
+  for (int q = 0; q < 4; ++q) is_out[q] = false;
 #pragma unroll
   for (int j = 0; j < kMaxOutliers; ++j) {
     sel[j] = 1 << 30;  // past k: sorts last, never written
@@ -90,7 +83,8 @@ __device__ void nuq_encode_row(const uint16_t* __restrict__ xrow, const float* l
     for (int q = 0; q < 4; ++q)
       if (bi == 4 * lane + q) is_out[q] = true;
   }
-  float mn = INFINITY, mx = -INFINITY;
+  mn = INFINITY;
+  mx = -INFINITY;
 #pragma unroll
   for (int q = 0; q < 4; ++q)
     if (!is_out[q]) { mn = fminf(mn, v[q]); mx = fmaxf(mx, v[q]); }
@@ -99,6 +93,25 @@ __device__ void nuq_encode_row(const uint16_t* __restrict__ xrow, const float* l
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   }
+}
+
+// Non-uniform (LUT) encoding of one 128-channel token vector held by a warp
+// (lane l owns channels 4l..4l+3).  The k largest |x| (ties to the lower
+// channel) become fp16 outliers with code 0; the dense rest is mapped
+// affinely onto [L0, L7] and coded by counting the level midpoints below
+// u = RN((x - mn) / s).  u comes from RN(d * RN(1 / s)), which is within
+// 3 * 2^-24 relative of it; only when that product lies within 2^-21
+// relative of a midpoint does the IEEE division decide.
+__device__ void nuq_encode_row(const uint16_t* __restrict__ xrow, const float* lut, const float (&tau)[7], int k,
+                               uint8_t* __restrict__ code_row, uint32_t* minsc_out,
+                               uint8_t* col_out, uint16_t* val_out, int lane) {
+  float v[4];
+  bool is_out[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) v[q] = half_bits_to_float(xrow[4 * lane + q]);
+  int sel[kMaxOutliers];
+  float mn, mx;
+  nuq_outliers(v, k, lane, is_out, sel, mn, mx);
   const float s = __fdiv_rn(__fsub_rn(mx, mn), __fsub_rn(lut[7], lut[0]));
   const float rs = s != 0.0f ? __frcp_rn(s) : 0.0f;
 #pragma unroll
@@ -144,10 +157,7 @@ __device__ void nuq_encode_row(const uint16_t* __restrict__ xrow, const float* l
 // In-warp normalised Hadamard rotation of one token vector (lane l owns
 // channels 4l..4l+3): fp32 butterflies of width 1, 2, 4, ..., 64, each
 // (a, b) -> (a + b, a - b), then times fp32(1/sqrt(d)) and round to fp16.
-__device__ void hadamard_row_inplace(uint16_t* row, float c, int lane) {
-  float v[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) v[q] = half_bits_to_float(row[4 * lane + q]);
+__device__ __forceinline__ void hadamard_vals(float (&v)[4], float c, int lane) {
   float a0 = __fadd_rn(v[0], v[1]), a1 = __fsub_rn(v[0], v[1]);
   float a2 = __fadd_rn(v[2], v[3]), a3 = __fsub_rn(v[2], v[3]);
   v[0] = __fadd_rn(a0, a2); v[2] = __fsub_rn(a0, a2);
@@ -161,9 +171,18 @@ __device__ void hadamard_row_inplace(uint16_t* row, float c, int lane) {
       v[q] = upper ? __fsub_rn(o, v[q]) : __fadd_rn(v[q], o);
     }
   }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) v[q] = half_bits_to_float(float_to_half_bits(__fmul_rn(v[q], c)));
+}
+
+__device__ void hadamard_row_inplace(uint16_t* row, float c, int lane) {
+  float v[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) v[q] = half_bits_to_float(row[4 * lane + q]);
+  hadamard_vals(v, c, lane);
   __syncwarp();
 #pragma unroll
-  for (int q = 0; q < 4; ++q) row[4 * lane + q] = float_to_half_bits(__fmul_rn(v[q], c));
+  for (int q = 0; q < 4; ++q) row[4 * lane + q] = float_to_half_bits(v[q]);
   __syncwarp();
 }
 
@@ -368,7 +387,173 @@ __global__ void __launch_bounds__(256) append_window_kernel(const __grid_constan
   }
 }
 
+// ------------------------------------------------ level-table fitting
+// Unweighted per-layer Lloyd fit of the 8 non-uniform levels (KVQuant:
+// per-layer datatypes computed offline; the sensitivity weights need a
+// model's gradients and are left out).  Every dense value of a calibration
+// vector is placed in its vector's dense range exactly as the encoder maps
+// it -- outliers removed by the same selection, u = RN((x - mn) / (mx - mn))
+// -- on a grid of 2^-16: p = rint(u 2^16), an integer in [0, 2^16].  The
+// first kernel counts the positions (a histogram of 2^16 + 1 bins); the
+// second takes prefix sums of the counts and of position x count and runs
+// Lloyd's iterations on them with the end levels held at 0 and 2^16 (every
+// vector's min and max sit there).  All sums are exact integers and every
+// level an fp64 quotient of two of them, so the fit does not depend on the
+// order in which values are counted.
+constexpr int kFitGrid = 1 << 16;
+constexpr int kFitWarps = 8;
+
+__global__ void __launch_bounds__(32 * kFitWarps)
+    nuq_fit_hist_kernel(const uint16_t* __restrict__ x, long long nvec, int k, int hadamard, float hc,
+                        unsigned long long* __restrict__ hist) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * kFitWarps;
+  unsigned long long n_lo = 0, n_hi = 0;  // positions 0 and 2^16 (each vector's min and max): once per warp
+  for (long long v = (long long)blockIdx.x * kFitWarps + (threadIdx.x >> 5); v < nvec; v += warps) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(x + (size_t)v * kHeadDim) + lane);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    float val[4] = {a.x, a.y, b.x, b.y};
+    if (hadamard) hadamard_vals(val, hc, lane);
+    bool is_out[4];
+    int sel[kMaxOutliers];
+    float mn, mx;
+    nuq_outliers(val, k, lane, is_out, sel, mn, mx);
+    if (!(mx > mn)) continue;  // a constant dense part: no positions (warp-uniform)
+    const float span = __fsub_rn(mx, mn);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (is_out[q]) continue;
+      const int pos = (int)rintf(__fmul_rn(__fdiv_rn(__fsub_rn(val[q], mn), span), (float)kFitGrid));
+      if (pos == 0) ++n_lo;
+      else if (pos == kFitGrid) ++n_hi;
+      else atomicAdd(&hist[pos], 1ull);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    n_lo += __shfl_xor_sync(0xffffffffu, n_lo, o);
+    n_hi += __shfl_xor_sync(0xffffffffu, n_hi, o);
+  }
+  if (lane == 0) {
+    if (n_lo) atomicAdd(&hist[0], n_lo);
+    if (n_hi) atomicAdd(&hist[kFitGrid], n_hi);
+  }
+}
+
+// One CTA: exclusive prefix sums pc[i] = sum_{b<i} hist[b] and
+// ps[i] = sum_{b<i} b hist[b] (i = 0 .. 2^16 + 1), then Lloyd in one thread:
+// the positions of level i's cell, (t_{i-1}, t_i] with t the midpoints, are
+// the integers floor(t_{i-1}) + 1 .. floor(t_i), so a cell's count and sum
+// are two differences of prefix sums.
+__global__ void __launch_bounds__(1024)
+    nuq_fit_lloyd_kernel(const unsigned long long* __restrict__ hist, unsigned long long* __restrict__ pc,
+                         unsigned long long* __restrict__ ps, int max_iters, float* __restrict__ lut_out,
+                         int* __restrict__ info_out) {
+  constexpr int kBins = kFitGrid + 1;
+  constexpr int kPer = (kBins + 1023) / 1024;
+  __shared__ unsigned long long wc[32], wsum[32];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int b0 = tid * kPer, b1 = min(kBins, b0 + kPer);
+  unsigned long long c = 0, sx = 0;
+  for (int b = b0; b < b1; ++b) {
+    const unsigned long long h = hist[b];
+    c += h;
+    sx += (unsigned long long)b * h;
+  }
+  // block-wide exclusive scan of (c, sx)
+  unsigned long long ic = c, is = sx;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long tc = __shfl_up_sync(0xffffffffu, ic, o), ts = __shfl_up_sync(0xffffffffu, is, o);
+    if (lane >= o) {
+      ic += tc;
+      is += ts;
+    }
+  }
+  if (lane == 31) {
+    wc[w] = ic;
+    wsum[w] = is;
+  }
+  __syncthreads();
+  if (w == 0) {
+    unsigned long long vc = wc[lane], vs = wsum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long tc = __shfl_up_sync(0xffffffffu, vc, o), ts = __shfl_up_sync(0xffffffffu, vs, o);
+      if (lane >= o) {
+        vc += tc;
+        vs += ts;
+      }
+    }
+    wc[lane] = vc - wc[lane];  // exclusive over warps
+    wsum[lane] = vs - wsum[lane];
+  }
+  __syncthreads();
+  unsigned long long rc = wc[w] + ic - c, rs = wsum[w] + is - sx;
+  for (int b = b0; b < b1; ++b) {
+    pc[b] = rc;
+    ps[b] = rs;
+    const unsigned long long h = hist[b];
+    rc += h;
+    rs += (unsigned long long)b * h;
+  }
+  if (b1 == kBins && b0 < b1) {
+    pc[kBins] = rc;
+    ps[kBins] = rs;
+  }
+  __syncthreads();
+  if (tid != 0) return;
+  double l[8];
+  for (int i = 0; i < 8; ++i) l[i] = (double)i * (double)kFitGrid / 7.0;
+  int it = 0;
+  while (it < max_iters) {
+    double t[7];
+    for (int i = 0; i < 7; ++i) t[i] = (l[i] + l[i + 1]) / 2.0;
+    ++it;
+    bool changed = false;
+    for (int i = 1; i < 7; ++i) {
+      const long long lo = (long long)floor(t[i - 1]) + 1, hi = (long long)floor(t[i]);
+      if (hi < lo) continue;
+      const unsigned long long n = pc[hi + 1] - pc[lo];
+      if (n == 0) continue;
+      const double nl = (double)(ps[hi + 1] - ps[lo]) / (double)n;
+      if (nl != l[i]) changed = true;
+      l[i] = nl;
+    }
+    if (!changed) break;
+  }
+  float lut[8];
+  bool ok = true;
+  for (int i = 0; i < 8; ++i) {
+    lut[i] = __half2float(__float2half_rn((float)(l[i] / (double)kFitGrid)));
+    if (i && !(lut[i] > lut[i - 1])) ok = false;
+    lut_out[i] = lut[i];
+  }
+  if (info_out) *info_out = ok ? it : -1;
+}
+
 }  // namespace
+
+cudaError_t launch_nuq_fit(const uint16_t* x, long long nvec, int k, int hadamard, int max_iters, void* ws,
+                           float* lut_out, int* info_out, cudaStream_t st) {
+  unsigned long long* hist = reinterpret_cast<unsigned long long*>(ws);
+  unsigned long long* pc = hist + (kFitGrid + 2);
+  unsigned long long* ps = pc + (kFitGrid + 2);
+  cudaError_t e = cudaMemsetAsync(hist, 0, sizeof(unsigned long long) * (kFitGrid + 1), st);
+  if (e != cudaSuccess) return e;
+  int sms = 0;
+  e = device_sm_count(&sms);
+  if (e != cudaSuccess) return e;
+  long long blocks = (nvec + kFitWarps - 1) / kFitWarps;
+  if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
+  nuq_fit_hist_kernel<<<(unsigned)blocks, 32 * kFitWarps, 0, st>>>(x, nvec, k, hadamard,
+                                                                    (float)(1.0 / std::sqrt((double)kHeadDim)), hist);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  nuq_fit_lloyd_kernel<<<1, 1024, 0, st>>>(hist, pc, ps, max_iters, lut_out, info_out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_append_quantize(const AppendParams& p, int n_groups, cudaStream_t st) {
   dim3 grid(n_groups, p.geo.NS);

@@ -398,6 +398,20 @@ kvq_status kvq_context_shard(const kvq_config* cfg, int32_t tokens, int32_t n_sh
   return KVQ_OK;
 }
 
+kvq_status kvq_fit_nuq_lut(const uint16_t* x, int64_t n_vectors, int32_t head_dim, int32_t outliers,
+                           int32_t hadamard, int32_t max_iters, void* workspace, uint64_t ws_bytes, float* lut_out,
+                           int32_t* info_out, kvq_stream_t stream) {
+  if (head_dim != kHeadDim) return KVQ_ERR_UNSUPPORTED;
+  if (!x || !lut_out || n_vectors < 1 || outliers < 0 || outliers > kMaxOutliers || (hadamard != 0 && hadamard != 1) ||
+      max_iters < 1 || max_iters > 1000000)
+    return KVQ_ERR_INVALID_ARG;
+  if (((uintptr_t)x % 8) || ((uintptr_t)lut_out % 4) || ((uintptr_t)info_out % 4)) return KVQ_ERR_INVALID_ARG;
+  if (!workspace || ws_bytes < KVQ_NUQ_FIT_WORKSPACE_BYTES || ((uintptr_t)workspace % 8)) return KVQ_ERR_WORKSPACE;
+  const cudaError_t e = launch_nuq_fit(x, n_vectors, outliers, hadamard, max_iters, workspace, lut_out, info_out,
+                                       reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
 kvq_status kvq_merge_attn(int32_t n_parts, int64_t rows, int32_t head_dim, const uint16_t* outs,
                           const float* lses, uint16_t* out, float* lse_out, kvq_stream_t stream) {
   if (n_parts < 1 || rows < 0) return KVQ_ERR_INVALID_ARG;

@@ -310,6 +310,8 @@ inline cudaError_t occupancy_memo(Kernel kernel, std::atomic<long long>* memo, i
 }
 
 // ------------------------------------------------------------ host hooks
+cudaError_t launch_nuq_fit(const uint16_t* x, long long nvec, int k, int hadamard, int max_iters, void* ws,
+                           float* lut_out, int* info_out, cudaStream_t st);
 cudaError_t launch_merge_attn(int n_parts, long long rows, const uint16_t* outs, const float* lses,
                               uint16_t* out, float* lse_out, cudaStream_t st);
 cudaError_t launch_append_quantize(const AppendParams& p, int n_groups, cudaStream_t st);

@@ -8,7 +8,9 @@ that ``synth`` draws from.  Nothing here computes any part of the method.
 Shapes follow the pages' workloads: a toy single head at 1k context, a
 Llama-2-7B MHA decode at 4k, a Llama-3-8B GQA decode at 32k with per-layer
 (K, V) bit pairs, a Qwen-like GQA decode with Hadamard-rotated 2-bit V, and
-a LLaMA-7B layer at 1M context with pre-RoPE 3-bit non-uniform codes.
+a LLaMA-7B layer at 1M context with pre-RoPE 3-bit non-uniform codes whose
+level tables are fitted per layer on the layer's first 2048 tokens
+(``lut="fitted"``; see calibrate.py).
 """
 from __future__ import annotations
 
@@ -42,7 +44,7 @@ WORKLOADS = {
         k_dist="normal", k_outlier_channels="random3", k_outlier_scale=8.0, v_dist="student_t3"),
     "llama7b_nuq3_t1m": dict(
         _BASE, layers=1, batch=1, n_q_heads=32, n_kv_heads=32, tokens=1048576,
-        pairs="NUQ3", k_pre_rope=1, outliers_per_vector=2,
+        pairs="NUQ3", k_pre_rope=1, outliers_per_vector=2, lut="fitted", lut_calib_tokens=2048,
         k_dist="normal", k_outlier_channels="random3", k_outlier_scale=8.0, v_dist="laplace"),
 }
 

@@ -254,6 +254,40 @@ kvq_status kvq_decode_attn_noalloc(const kvq_config *cfg, const void *layer_buf,
                                    const uint16_t *q, uint16_t *out, float *lse,
                                    kvq_stream_t stream);
 
+/* kvq_fit_nuq_lut -- fit the 8 levels of a non-uniform (3-bit) table to
+ * calibration vectors: unweighted Lloyd iterations (KVQuant summary,
+ * "technical approach": non-uniform per-layer datatypes computed offline;
+ * the sensitivity weighting needs a model's gradients and is not done).
+ * Every dense value of a vector is placed in its vector's dense range as the
+ * encoder maps it -- the `outliers` largest |x| removed (ties to the lower
+ * channel), u = RN((x - min) / (max - min)) in fp32 -- on a grid of 2^-16,
+ * p = rint(u * 2^16) in [0, 2^16]; a vector with a constant dense part gives
+ * no value.  Lloyd starts from l_i = i * 2^16 / 7, holds l_0 = 0 and
+ * l_7 = 2^16 (every vector's min and max sit there), assigns every p to the
+ * level it is nearest to (p > (l_i + l_{i+1}) / 2 moves it up; a tie stays
+ * down, as in the encoder) and moves l_1..l_6 to the mean of their values
+ * (exact integer sums, one fp64 division; an empty level stays), until an
+ * update changes nothing or max_iters updates were made.  The table is
+ * lut_out[i] = fp16_RN(l_i / 2^16) in [0, 1] (the encoder is invariant to
+ * an affine map of the table).
+ *   x          device fp16 [n_vectors][head_dim], 8-byte aligned (head_dim 128)
+ *   outliers   0..8: per-vector outliers left out, as kvq_config's
+ *              outliers_per_vector
+ *   hadamard   1: rotate each vector by Hn first, as the encoder does for a
+ *              Hadamard-rotated V
+ *   workspace  device scratch of >= KVQ_NUQ_FIT_WORKSPACE_BYTES, 8-byte
+ *              aligned (its contents need not be zero)
+ *   lut_out    device f32 [8]
+ *   info_out   device int32 [1] or NULL: the updates made, or -1 when the
+ *              rounded levels are not strictly increasing (the table is then
+ *              not usable)
+ * Three launches on `stream` (a memset and two kernels).  Errors:
+ * KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_WORKSPACE, KVQ_ERR_CUDA. */
+#define KVQ_NUQ_FIT_WORKSPACE_BYTES (3ull * 65538ull * 8ull)
+kvq_status kvq_fit_nuq_lut(const uint16_t *x, int64_t n_vectors, int32_t head_dim, int32_t outliers,
+                           int32_t hadamard, int32_t max_iters, void *workspace, uint64_t ws_bytes,
+                           float *lut_out, int32_t *info_out, kvq_stream_t stream);
+
 /* Context-parallel decode (KVQuant summary, abstract and main results: a
  * 10M-token context on an 8-GPU system).  The context of every sequence is
  * cut into n_shards contiguous shards at quantized-group boundaries, each

@@ -603,3 +603,124 @@ void orc_merge_parts(int n, int rows, int d, const double *outs, const double *l
         lse[i] = m + log(L);
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Fitting a non-uniform level table (unweighted per-layer Lloyd).          */
+/* ------------------------------------------------------------------------ */
+
+/* The position of every dense value of a vector inside its dense range, on
+ * the grid of 2^-16: outliers removed as orc_nuq_encode removes them (the k
+ * largest |x|, ties to the lower channel), mn / mx the dense min / max
+ * (fp32), u = (x - mn) / (mx - mn) (fp32, RN), position = rint(u * 2^16),
+ * an integer in [0, 2^16].  The encoder maps mn to L0 and mx to L7 by the
+ * same affine map, so a table fitted on these positions (scaled to [0, 1])
+ * is one the encoder can use directly.  A vector whose dense part is
+ * constant (mx == mn) gives no positions (the encoder codes it all 0).  With
+ * `hadamard`, the vector is first rotated as orc_hadamard_rotate does.
+ * Writes the positions of vector x (n channels) to pos and returns how many. */
+static int nuq_fit_positions(const uint16_t *xin, int n, int k, int hadamard, int32_t *pos)
+{
+    uint16_t rot[1024];
+    const uint16_t *x = xin;
+    if (hadamard) {
+        orc_hadamard_rotate(xin, n, rot);
+        x = rot;
+    }
+    unsigned char is_out[1024];
+    memset(is_out, 0, sizeof is_out);
+    for (int j = 0; j < k; j++) {
+        int best = -1;
+        float bv = -1.0f;
+        for (int i = 0; i < n; i++) {
+            if (is_out[i]) continue;
+            float a = fabsf(orc_half_to_float(x[i]));
+            if (a > bv) { bv = a; best = i; }
+        }
+        is_out[best] = 1;
+    }
+    float mn = INFINITY, mx = -INFINITY;
+    for (int i = 0; i < n; i++) {
+        if (is_out[i]) continue;
+        float v = orc_half_to_float(x[i]);
+        if (v < mn) mn = v;
+        if (v > mx) mx = v;
+    }
+    if (!(mx > mn)) return 0;
+    float span = mx - mn;
+    int m = 0;
+    for (int i = 0; i < n; i++) {
+        if (is_out[i]) continue;
+        float u = (orc_half_to_float(x[i]) - mn) / span;
+        pos[m++] = (int32_t)rintf(u * 65536.0f);
+    }
+    return m;
+}
+
+/* Lloyd's algorithm for 8 levels on the positions of all dense values of
+ * nvec vectors x [nvec][n] (fp16), with the two end levels held at 0 and
+ * 2^16 (every vector's dense min and max sit there):
+ *   start        l_i = i * 2^16 / 7                              (fp64)
+ *   assignment   a position p belongs to level #{i < 7 : p > (l_i + l_{i+1}) / 2}
+ *                (the encoder's rule: an exact tie goes down)
+ *   update       l_i = (sum of its positions) / (their count) for i = 1..6
+ *                (exact integer sums, one fp64 division; an empty level
+ *                keeps its value)
+ * repeated until an update changes no level or max_iters updates were made.
+ * lut[i] = fp16_RN(l_i / 2^16) as fp32; levels (if not NULL) gets the l_i
+ * (fp64, positions).  Returns the number of updates made, or -1 if the
+ * rounded levels are not strictly increasing. */
+int orc_nuq_fit_lut(const uint16_t *x, long nvec, int n, int k, int hadamard, int max_iters, float *lut,
+                    double *levels)
+{
+    int32_t *pos = malloc(sizeof(int32_t) * (size_t)nvec * (size_t)n);
+    long np = 0;
+    for (long v = 0; v < nvec; v++)
+        np += nuq_fit_positions(x + (size_t)v * n, n, k, hadamard, pos + np);
+    double l[8];
+    for (int i = 0; i < 8; i++) l[i] = (double)i * 65536.0 / 7.0;
+    int it = 0;
+    while (it < max_iters) {
+        double t[7];
+        for (int i = 0; i < 7; i++) t[i] = (l[i] + l[i + 1]) / 2.0;
+        long long cnt[8] = {0}, sum[8] = {0};
+        for (long j = 0; j < np; j++) {
+            int c = 0;
+            for (int i = 0; i < 7; i++)
+                if ((double)pos[j] > t[i]) c++;
+            cnt[c] += 1;
+            sum[c] += pos[j];
+        }
+        it++;
+        int changed = 0;
+        for (int i = 1; i < 7; i++) {
+            if (cnt[i] == 0) continue;
+            double nl = (double)sum[i] / (double)cnt[i];
+            if (nl != l[i]) changed = 1;
+            l[i] = nl;
+        }
+        if (!changed) break;
+    }
+    free(pos);
+    if (levels)
+        for (int i = 0; i < 8; i++) levels[i] = l[i];
+    for (int i = 0; i < 8; i++) lut[i] = orc_half_to_float(orc_float_to_half((float)(l[i] / 65536.0)));
+    for (int i = 1; i < 8; i++)
+        if (!(lut[i] > lut[i - 1])) return -1;
+    return it;
+}
+
+/* The positions of nvec vectors (as orc_nuq_fit_lut sees them), for tests:
+ * writes at most cap positions, returns how many there are. */
+long orc_nuq_fit_positions(const uint16_t *x, long nvec, int n, int k, int hadamard, int32_t *pos, long cap)
+{
+    int32_t tmp[1024];
+    long np = 0;
+    for (long v = 0; v < nvec; v++) {
+        int m = nuq_fit_positions(x + (size_t)v * n, n, k, hadamard, tmp);
+        for (int i = 0; i < m; i++) {
+            if (np < cap) pos[np] = tmp[i];
+            np++;
+        }
+    }
+    return np;
+}

@@ -78,6 +78,11 @@ def lib():
         L.orc_build_stream.argtypes = [C.POINTER(_Cfg), C.c_int, u16, u16,
                                        u8, u16, u8, u16, u16, u16, u16, u16,
                                        i32, u8, u16, i32, u8, u16]
+        L.orc_nuq_fit_lut.argtypes = [u16, C.c_long, C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(C.c_float),
+                                      f64]
+        L.orc_nuq_fit_lut.restype = C.c_int
+        L.orc_nuq_fit_positions.argtypes = [u16, C.c_long, C.c_int, C.c_int, C.c_int, i32, C.c_long]
+        L.orc_nuq_fit_positions.restype = C.c_long
         L.orc_merge_parts.argtypes = [C.c_int, C.c_int, C.c_int, f64, f64, f64, f64]
         L.orc_decode_stream.argtypes = [C.POINTER(_Cfg), C.c_int, C.c_int, u16,
                                         u8, u16, u8, u16, u16, u16, u16, u16,
@@ -312,3 +317,33 @@ def merge_parts(outs, lses):
     lib().orc_merge_parts(n, rows, d, _P(outs, C.c_double), _P(lses, C.c_double),
                           _P(out, C.c_double), _P(lse, C.c_double))
     return out, lse
+
+
+def nuq_fit_lut(x, k: int, hadamard: int = 0, max_iters: int = 100, levels: bool = False):
+    """Fit 8 non-uniform levels to the vectors x [..., d] (fp16): unweighted
+    Lloyd on the dense values' positions in their vector's [min, max] range,
+    end levels held at 0 and 1.  Returns (lut list of 8 floats, updates made
+    or -1 if the fp16-rounded levels are not strictly increasing), plus the
+    unrounded levels in grid units (fp64 array) when levels=True."""
+    x = _u16(x)
+    d = x.shape[-1]
+    nvec = x.size // d
+    lut = (C.c_float * 8)()
+    lv = np.zeros(8, np.float64)
+    it = lib().orc_nuq_fit_lut(_P(np.ascontiguousarray(x.reshape(nvec, d)), C.c_uint16), nvec, d, k,
+                               hadamard, max_iters, lut, _P(lv, C.c_double))
+    if levels:
+        return [float(v) for v in lut], it, lv
+    return [float(v) for v in lut], it
+
+
+def nuq_fit_positions(x, k: int, hadamard: int = 0) -> np.ndarray:
+    """The grid positions (0 .. 2^16) of the dense values the fit sees."""
+    x = _u16(x)
+    d = x.shape[-1]
+    nvec = x.size // d
+    xs = np.ascontiguousarray(x.reshape(nvec, d))
+    cap = nvec * d
+    pos = np.zeros(max(cap, 1), np.int32)
+    n = lib().orc_nuq_fit_positions(_P(xs, C.c_uint16), nvec, d, k, hadamard, _P(pos, C.c_int32), cap)
+    return pos[:n]

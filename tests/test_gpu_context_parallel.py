@@ -127,7 +127,7 @@ def test_serving_loop_appends_to_the_last_shard(B):
     """Prefill 3 shards, then append tokens one at a time to the last shard
     (its window flushes groups as a single cache's would) and decode."""
     from bit_kv_cache_07_gb300 import synth
-    cfg = _cfg(4, 2, Hq=4, Hkv=1, T=900, n_sink=4, n_recent=32, v_hadamard=1)
+    cfg = _cfg(4, 2, Bt=1, Hq=4, Hkv=1, T=900, n_sink=4, n_recent=32, v_hadamard=1)
     T0, steps = 700, 70
     K, V = synth.random_kv(1, 1, T0 + steps, seed=95, device="cuda", v_dist="student_t3")
     q = synth.random_q(1, 4, seed=96, device="cuda")

@@ -28,8 +28,14 @@ def run_layer(binding, name, layer_idx, sample_streams):
     T = w["tokens"]
     cfg = workloads.layer_config(name, layer_idx)
     if cfg["k_bits"] == 3:
-        cfg["k_lut"] = synth.nuq_lut(name, layer_idx, "k")
-        cfg["v_lut"] = synth.nuq_lut(name, layer_idx, "v")
+        from bit_kv_cache_07_gb300 import calibrate
+        cfg["k_lut"], cfg["v_lut"] = calibrate.nuq_tables(name, layer_idx)
+        if w.get("lut") == "fitted":
+            # the library's fit against the oracle's on the same calibration tokens
+            Kc, Vc = calibrate.calibration_kv(name, layer_idx)
+            k = w["outliers_per_vector"]
+            assert O.nuq_fit_lut(Kc.cpu().numpy(), k)[0] == cfg["k_lut"]
+            assert O.nuq_fit_lut(Vc.cpu().numpy(), k, w["v_hadamard"])[0] == cfg["v_lut"]
     K, V = synth.layer_kv(name, layer_idx, tokens=T, device="cuda")
     assert torch.isfinite(K).all() and torch.isfinite(V).all()
     layer = binding.Layer(cfg)
