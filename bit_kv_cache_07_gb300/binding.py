@@ -35,6 +35,7 @@ class kvq_config(C.Structure):
         ("k_pre_rope", C.c_int32), ("rope_theta", C.c_float), ("outliers_per_vector", C.c_int32),
         ("k_lut", C.c_float * 8), ("v_lut", C.c_float * 8), ("softmax_scale", C.c_float),
         ("split_tokens", C.c_int32), ("position_offset", C.c_int32),
+        ("k_group_channels", C.c_int32), ("hybrid_groups", C.c_int32), ("k_channel_norm", C.c_int32),
     ]
 
 
@@ -42,14 +43,15 @@ class kvq_region(C.Structure):
     _fields_ = [("offset", C.c_uint64), ("bytes", C.c_uint64)]
 
 
-REGIONS = ["k_codes", "k_scales", "v_codes", "v_scales", "k_sink", "v_sink", "k_ring", "v_ring",
-           "k_csr_rowptr", "k_csr_col", "k_csr_val", "v_csr_rowptr", "v_csr_col", "v_csr_val"]
+_REGIONS_HEAD = ["k_codes", "k_scales", "v_codes", "v_scales", "k_sink", "v_sink", "k_ring", "v_ring",
+                 "k_csr_rowptr", "k_csr_col", "k_csr_val", "v_csr_rowptr", "v_csr_col", "v_csr_val"]
+REGIONS = _REGIONS_HEAD + ["k_norm"]
 
 
 class kvq_layout(C.Structure):
-    _fields_ = [(n, kvq_region) for n in REGIONS] + [
+    _fields_ = [(n, kvq_region) for n in _REGIONS_HEAD] + [
         ("layer_bytes", C.c_uint64), ("workspace_bytes", C.c_uint64), ("max_splits", C.c_int32),
-        ("ring_slots", C.c_int32), ("q_cap", C.c_int32)]
+        ("ring_slots", C.c_int32), ("q_cap", C.c_int32), ("k_norm", kvq_region)]
 
 
 EXPORTS = ["kvq_layout_query", "kvq_append", "kvq_decode_attn", "kvq_decode_plan",

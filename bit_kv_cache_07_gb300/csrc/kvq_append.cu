@@ -45,6 +45,60 @@ __device__ __forceinline__ uint32_t uniform_code(float x, float mn, float scale,
   return (uint32_t)r;
 }
 
+// Parameters of one uniform group from its min, max and exact fp64 sum
+// (InnerQ, Methodology 2: the group picks a symmetric or an asymmetric grid
+// from its own statistics).  Symmetric when `hybrid`, mx > mn and the mean
+// lies within half an asymmetric step of zero, |mean| 2^(b+1) <= mx - mn:
+// scale = max(|mn|, |mx|) / (2^(b-1) - 1), stored min = -2^(b-1) fp16(scale)
+// (falls back to asymmetric if that overflows fp16).  Asymmetric otherwise:
+// scale = (mx - mn) / (2^b - 1), stored min = fp16(mn).  The inputs are fp16
+// values (or fp16 values divided by powers of two up to 2^16), so the fp64
+// sum of at most 128 of them is exact in any order.
+struct GroupQ {
+  float mn, scale, rs;  // asymmetric origin, fp32 scale and its reciprocal
+  int sym;              // 1: symmetric codes
+  uint32_t word;        // stored {min, scale} fp16 pair
+};
+__device__ __forceinline__ GroupQ group_params(float mn, float mx, double sum, int n, int bits, int hybrid) {
+  GroupQ g;
+  g.sym = 0;
+  if (hybrid && mx > mn && fabs(sum / (double)n) * (double)(1 << (bits + 1)) <= (double)mx - (double)mn) {
+    const float a = fmaxf(fabsf(mn), fabsf(mx));
+    const float scale = __fdiv_rn(a, (float)((1 << (bits - 1)) - 1));
+    const uint16_t sh = float_to_half_bits(scale);
+    const uint16_t mh = float_to_half_bits(__fmul_rn(-(float)(1 << (bits - 1)), half_bits_to_float(sh)));
+    if (!isinf(half_bits_to_float(mh))) {
+      g.sym = 1;
+      g.mn = 0.0f;
+      g.scale = scale;
+      g.rs = __frcp_rn(scale);
+      g.word = (uint32_t)mh | ((uint32_t)sh << 16);
+      return g;
+    }
+  }
+  g.mn = mn;
+  g.scale = __fdiv_rn(__fsub_rn(mx, mn), (float)((1 << bits) - 1));
+  g.rs = g.scale == 0.0f ? 0.0f : __frcp_rn(g.scale);
+  g.word = (uint32_t)float_to_half_bits(mn) | ((uint32_t)float_to_half_bits(g.scale) << 16);
+  return g;
+}
+
+// Symmetric code clamp(rint(x / scale), -qs, qs) + 2^(b-1), qs = 2^(b-1) - 1
+// (|x| <= qs scale up to rounding: the quotient's magnitude stays below 256,
+// so the reciprocal shortcut of uniform_code applies unchanged).
+__device__ __forceinline__ uint32_t sym_code(float x, float scale, float rs, int bits) {
+  const float qa = __fmul_rn(x, rs);
+  float r = rintf(qa);
+  if (fabsf(__fsub_rn(qa, r)) > 0.4999f) r = rintf(__fdiv_rn(x, scale));
+  const float qs = (float)((1 << (bits - 1)) - 1);
+  r = fminf(fmaxf(r, -qs), qs);
+  return (uint32_t)((int)r + (1 << (bits - 1)));
+}
+
+__device__ __forceinline__ uint32_t group_code(float x, const GroupQ& g, int bits) {
+  return g.sym ? sym_code(x, g.scale, g.rs, bits) : uniform_code(x, g.mn, g.scale, g.rs);
+}
+
 // Level midpoints tau_i = (L_i + L_(i+1)) / 2 - L_0 of a LUT, in fp32 as the
 // encoder compares them (computed once per CTA).
 __device__ __forceinline__ void nuq_midpoints(const float* lut, float (&tau)[7]) {
@@ -297,6 +351,30 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
         if (i == 0) rp[0] = 0;
       }
     }
+  } else if (G.gkc) {
+    // InnerQ: per token, groups of 64 channels along the hidden dimension
+    // (16 lanes per group), on the keys divided by the channel normalisation
+    for (int r = w; r < kGroupTokens; r += 4) {
+      const int i = i0 + r;
+      float v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        v[q] = half_bits_to_float(sK[r][4 * lane + q]);
+        if (G.knorm) v[q] = __fdiv_rn(v[q], p.L.k_norm[(size_t)s * kHeadDim + 4 * lane + q]);  // exact: 2^e
+      }
+      float mn = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
+      float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+      double sum = ((double)v[0] + (double)v[1]) + ((double)v[2] + (double)v[3]);
+      for (int o = 8; o > 0; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      }
+      const GroupQ gq = group_params(mn, mx, sum, 64, G.kb, G.hybrid);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) sCk[r][4 * lane + q] = (uint8_t)group_code(v[q], gq, G.kb);
+      if ((lane & 15) == 0) p.L.k_scales[((size_t)s * G.qcap + i) * G.nkg + (lane >> 4)] = gq.word;
+    }
   } else {
     const int c = tid;  // one channel per thread, over the group's tokens (held in registers)
     float xk[kGroupTokens];
@@ -308,13 +386,13 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
       mn = fminf(mn, xk[r]);
       mx = fmaxf(mx, xk[r]);
     }
-    const float qmax = (float)((1 << G.kb) - 1);
-    const float scale = __fdiv_rn(__fsub_rn(mx, mn), qmax);
-    const float rs = scale == 0.0f ? 0.0f : __frcp_rn(scale);
+    double sum = 0.0;
+    if (G.hybrid)
+      for (int r = 0; r < kGroupTokens; ++r) sum += (double)xk[r];
+    const GroupQ gq = group_params(mn, mx, sum, kGroupTokens, G.kb, G.hybrid);
 #pragma unroll
-    for (int r = 0; r < kGroupTokens; ++r) sCk[r][c] = (uint8_t)uniform_code(xk[r], mn, scale, rs);
-    p.L.k_scales[((size_t)s * G.gcap + grp) * kHeadDim + c] =
-        (uint32_t)float_to_half_bits(mn) | ((uint32_t)float_to_half_bits(scale) << 16);
+    for (int r = 0; r < kGroupTokens; ++r) sCk[r][c] = (uint8_t)group_code(xk[r], gq, G.kb);
+    p.L.k_scales[((size_t)s * G.gcap + grp) * kHeadDim + c] = gq.word;
   }
 
   // ---- V (optionally rotated first)
@@ -336,25 +414,42 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
       for (int q = 0; q < 4; ++q) v[q] = half_bits_to_float(sV[r][4 * lane + q]);
       float mn = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
       float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+      double sum = ((double)v[0] + (double)v[1]) + ((double)v[2] + (double)v[3]);
       const int seg = G.gv / 4;  // lanes per channel group
       for (int o = seg / 2; o > 0; o >>= 1) {
         mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (G.hybrid) sum += __shfl_xor_sync(0xffffffffu, sum, o);
       }
-      const float qmax = (float)((1 << G.vb) - 1);
-      const float scale = __fdiv_rn(__fsub_rn(mx, mn), qmax);
-      const float rs = scale == 0.0f ? 0.0f : __frcp_rn(scale);
+      const GroupQ gq = group_params(mn, mx, sum, G.gv, G.vb, G.hybrid);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) sCv[r][4 * lane + q] = (uint8_t)uniform_code(v[q], mn, scale, rs);
-      if (lane % seg == 0)
-        p.L.v_scales[((size_t)s * G.qcap + i) * G.nvg + lane / seg] =
-            (uint32_t)float_to_half_bits(mn) | ((uint32_t)float_to_half_bits(scale) << 16);
+      for (int q = 0; q < 4; ++q) sCv[r][4 * lane + q] = (uint8_t)group_code(v[q], gq, G.vb);
+      if (lane % seg == 0) p.L.v_scales[((size_t)s * G.qcap + i) * G.nvg + lane / seg] = gq.word;
     }
   }
   __syncthreads();
 
   pack_rows(sCk, G.kb, kGroupTokens, p.L.k_codes + ((size_t)s * G.qcap + i0) * G.krow, G.krow, tid);
   pack_rows(sCv, G.vb, kGroupTokens, p.L.v_codes + ((size_t)s * G.qcap + i0) * G.vrow, G.vrow, tid);
+}
+
+// InnerQ per-channel key normalisation of an empty cache's first append:
+// n_c = the smallest power of two >= max |K_c| over the call's tokens (1 for
+// an all-zero channel), per stream.  One CTA per stream, one thread per
+// channel (threads of a warp read consecutive channels of a token row).
+__global__ void __launch_bounds__(kHeadDim) key_norm_kernel(const __grid_constant__ AppendParams p) {
+  const int s = blockIdx.x, c = threadIdx.x;
+  const uint16_t* k = p.k_new + (size_t)s * p.n_new * kRowHalves + c;
+  float m = 0.0f;
+  for (int t = 0; t < p.n_new; ++t) m = fmaxf(m, fabsf(half_bits_to_float(k[(size_t)t * kRowHalves])));
+  float n = 1.0f;
+  if (m > 0.0f) {
+    int e;
+    frexpf(m, &e);  // m = f 2^e, f in [0.5, 1): 2^(e-1) <= m < 2^e
+    n = ldexpf(1.0f, e);
+    if (ldexpf(1.0f, e - 1) >= m) n = ldexpf(1.0f, e - 1);  // m itself a power of two
+  }
+  p.L.k_norm[(size_t)s * kHeadDim + c] = n;
 }
 
 // Copy the fp16 tokens of this call that stay fp16 (sinks and the final
@@ -558,6 +653,11 @@ cudaError_t launch_nuq_fit(const uint16_t* x, long long nvec, int k, int hadamar
 cudaError_t launch_append_quantize(const AppendParams& p, int n_groups, cudaStream_t st) {
   dim3 grid(n_groups, p.geo.NS);
   append_quantize_kernel<<<grid, kThreads, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_key_norm(const AppendParams& p, cudaStream_t st) {
+  key_norm_kernel<<<p.geo.NS, kHeadDim, 0, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -144,7 +144,7 @@ __device__ __forceinline__ constexpr float kq_mult(int k) {
 // Where channel offset o (0..31) of a thread's slice lands: k-step s and
 // element e (0,1: the lo register's halves; 2,3: the hi register's).
 template <int KB>
-__device__ __forceinline__ void k_slot_of(int o, int& s, int& e) {
+__host__ __device__ __forceinline__ void k_slot_of(int o, int& s, int& e) {
   if (KB == 8) {
     const int n = o & 3;
     s = o >> 2;
@@ -178,7 +178,12 @@ __device__ __forceinline__ int v_chan(int mc, int g, int rh) {
 // distinct banks.
 __device__ __forceinline__ uint32_t swz(uint32_t off, uint32_t mask) { return off ^ (((off >> 7) & mask) << 4); }
 
-template <int KB, int VB>
+//
+// InnerQ keys (IQ: per-token groups of 64 channels) keep a group's per-token
+// K {min, scale} words (2 per token, 256 bytes) where the per-channel words
+// would be, and their code rows use a different swizzle (iq_kswz): a thread
+// reads the two halves of its key channels from the two 64-channel groups.
+template <int KB, int VB, bool IQ = false>
 struct StageGeom {
   static constexpr int KROW = kHeadDim * KB / 8;
   static constexpr int VROW = kHeadDim * VB / 8;
@@ -186,7 +191,8 @@ struct StageGeom {
   static constexpr uint32_t VSW = (uint32_t)(VROW / 16 - 1);  // 32/64/128-byte V rows
   static constexpr int KC = 0;
   static constexpr int KS = KC + kGroupTokens * KROW;
-  static constexpr int VC = KS + kHeadDim * 4;
+  static constexpr int KSB = IQ ? kGroupTokens * 8 : kHeadDim * 4;  // K scale bytes of a group
+  static constexpr int VC = KS + KSB;
   static constexpr int VS = VC + kGroupTokens * VROW;
   static constexpr int BYTES = ((VS + kGroupTokens * kNVG * 4) + 127) / 128 * 128;
 };
@@ -218,23 +224,41 @@ __device__ __forceinline__ float ex2(float x) {  // 2^x (hardware approximation;
   return y;
 }
 
+// InnerQ key rows: thread tq of a quad reads bytes [NB tq, NB tq + NB) of
+// its row (channels 16 tq .. 16 tq + 15 of group 0) and the same bytes of the
+// row's second half (group 1), NB = KROW / 8.  Rows r and r + 128 / KROW (the
+// same banks) would collide, so rows with bit 7 of their byte offset set swap
+// 16-byte chunks by XOR with KROW / 2 (chunk-granular: the 16-byte copies stay
+// aligned): the quad's reads of 8 (KB 2), 4 (KB 4) or 2 (KB 8) rows then hit
+// distinct banks.
+template <int KB>
+__host__ __device__ __forceinline__ uint32_t iq_kswz(uint32_t off) {
+  constexpr uint32_t half_row = kHeadDim * KB / 16;
+  return off ^ (((off >> 7) & 1u) * half_row);
+}
+
 // Queue the asynchronous copies of one 32-token group of stream s into the
 // stage at shared address dst.  Every lane issues its share.
-template <int KB, int VB>
+template <int KB, int VB, bool IQ = false>
 __device__ __forceinline__ void issue_group(const DecodeParams& p, int s, int grp, uint32_t dst, int lane) {
-  using SG = StageGeom<KB, VB>;
+  using SG = StageGeom<KB, VB, IQ>;
   // first row of the group in the stream-major regions (< 2^31: checked on the host);
   // the group's K scales are the 128 words at row0 * 4, its V scales the words at row0 * kNVG
   const uint32_t row0 = (uint32_t)s * (uint32_t)p.geo.qcap + (uint32_t)grp * kGroupTokens;
   const uint8_t* kc = p.L.k_codes + (size_t)row0 * SG::KROW + 16 * lane;
   const uint8_t* vc = p.L.v_codes + (size_t)row0 * SG::VROW + 16 * lane;
-  const uint8_t* ks = reinterpret_cast<const uint8_t*>(p.L.k_scales) + (size_t)row0 * 16 + 16 * lane;
+  // per-channel K: the group's 128 {min, scale} words at row0 * 4; InnerQ K:
+  // 2 words per token at row0 * 2
+  const uint8_t* ks = reinterpret_cast<const uint8_t*>(p.L.k_scales) + (size_t)row0 * (IQ ? 8 : 16) + 16 * lane;
   const uint8_t* vs = reinterpret_cast<const uint8_t*>(p.L.v_scales) + (size_t)row0 * (4 * kNVG) + 16 * lane;
   constexpr int KCH = kGroupTokens * SG::KROW / 16, VCH = kGroupTokens * SG::VROW / 16;
   static_assert(KCH % 32 == 0 && VCH % 32 == 0, "whole chunks per lane");
 #pragma unroll
-  for (int n = 0; n < KCH / 32; ++n) cp_async16(dst + SG::KC + swz(16 * (lane + 32 * n), SG::KSW), kc + 512 * n);
-  cp_async16(dst + SG::KS + 16 * lane, ks);  // 512 B = 32 chunks
+  for (int n = 0; n < KCH / 32; ++n) {
+    const uint32_t off = 16 * (lane + 32 * n);
+    cp_async16(dst + SG::KC + (IQ ? iq_kswz<KB>(off) : swz(off, SG::KSW)), kc + 512 * n);
+  }
+  if (!IQ || lane < SG::KSB / 16) cp_async16(dst + SG::KS + 16 * lane, ks);  // 512 B or 256 B of K scales
 #pragma unroll
   for (int n = 0; n < VCH / 32; ++n) cp_async16(dst + SG::VC + swz(16 * (lane + 32 * n), SG::VSW), vc + 512 * n);
   if (lane < kGroupTokens * kNVG / 4) cp_async16(dst + SG::VS + 16 * lane, vs);
@@ -341,6 +365,96 @@ __device__ __forceinline__ int qb_perm_pos(int c) {
   return 4 * L + (rel >= D ? 1 : 0) + 2 * (rel & 1);
 }
 
+// ------------------------------------------------------------- InnerQ keys
+// Per-warp scratch of the InnerQ key path: the group's per-token K scale and
+// min for its two 64-channel groups (ordered like vmn: the 4 tokens gq + 8i a
+// lane needs sit in one 16-byte vector), and per query head of the stream
+// the constants {Ohat_0, Ohat_1, Q_0, Q_1} of its two groups (see build_bq_iq).
+struct IqWarpSmem {
+  alignas(16) float ksc[2][kGroupTokens];
+  alignas(16) float kmn[2][kGroupTokens];
+  alignas(16) float iqc[kMaxGQA][4];
+};
+
+// The inverse of k_slot_of: the channel offset o (0..31) of a thread's slice
+// that k-step s, element e takes.
+template <int KB>
+__host__ __device__ __forceinline__ constexpr int k_offset_of(int s, int e) {
+  return KB == 8 ? 4 * s + ((e >> 1) | ((e & 1) << 1))
+         : KB == 4 ? 8 * (s >> 1) + (((e & 1) << 2) | ((s & 1) << 1) | (e >> 1))
+                   : 16 * (s >> 2) + (((e & 1) << 3) | ((s & 3) << 1) | (e >> 1));
+}
+// InnerQ: the key channel of slice offset o of thread tq (half from each group)
+__host__ __device__ __forceinline__ constexpr int iq_channel(int tq, int o) {
+  return o < 16 ? 16 * tq + o : kHeadDim / 2 + 16 * tq + (o - 16);
+}
+
+// The Q' fragments of an InnerQ stream, built once per stream: with keys
+// grouped per token, K's scales no longer enter q (they multiply each group's
+// partial product after the mma), so Q' = q * n_c (the channel's key
+// normalisation) * 2^E / u_c, split into hi + lo fp16, is constant over the
+// stream.  Each lane writes its own fragment row (the layout process_group's
+// step (b) reads).  Per head h and group j it also stores
+//   Ohat_j = 2^-E * 1024 * sum_{c in j} (hi + lo)_c   (the magic offset the
+//            mma adds: the group's code product is S_j 2^-E - Ohat_j)
+//   Q_j    = sum_{c in j} q_c n_c                        (for the K min term)
+// in logit units.  qw holds q * softmax scale in the qb_perm_pos<KB> order.
+template <int KB, int NT>
+__device__ __forceinline__ void build_bq_iq(const float (*qw)[kHeadDim], const float* __restrict__ knorm,
+                                            MmaWarpSmem<NT>& sm, IqWarpSmem& iq, int g, int lane) {
+  constexpr bool HC = head_cols<NT>();
+  constexpr float kE = (float)(1 << kq_exp<KB>());
+  const int gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int h = HC ? gq : 4 * nt + (gq >> 1);
+    const bool lo = HC ? (nt == 1) : ((gq & 1) != 0);
+    uint32_t reg[16];
+#pragma unroll
+    for (int ri = 0; ri < 16; ++ri) {
+      uint32_t hv[2];
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int c = iq_channel(tq, k_offset_of<KB>(ri >> 1, 2 * (ri & 1) + x));
+        float v = 0.0f;
+        if (h < g) v = qw[h][qb_perm_pos<KB>(c)] * (knorm ? __ldg(knorm + c) : 1.0f) * (kE / kq_mult<KB>(c & 3));
+        const __half hi = __float2half_rn(v);
+        hv[x] = __half_as_ushort(lo ? __float2half_rn(v - __half2float(hi)) : hi);
+      }
+      reg[ri] = hv[0] | (hv[1] << 16);
+    }
+    unsigned char* row = reinterpret_cast<unsigned char*>(&sm.bq[nt][lane][0]);
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4)
+      *reinterpret_cast<uint4*>(row + 16 * (c4 ^ ((lane >> 1) & 3))) =
+          make_uint4(reg[4 * c4], reg[4 * c4 + 1], reg[4 * c4 + 2], reg[4 * c4 + 3]);
+  }
+  // the constants: lane L sums channels 4L..4L+3 (all in group L / 16)
+  for (int h = 0; h < g; ++h) {
+    float oh = 0.0f, qs = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int c = 4 * lane + k;
+      const float qn = qw[h][qb_perm_pos<KB>(c)] * (knorm ? __ldg(knorm + c) : 1.0f);
+      const float v = qn * (kE / kq_mult<KB>(c & 3));
+      const __half hi = __float2half_rn(v);
+      const float lo = __half2float(__float2half_rn(v - __half2float(hi)));
+      oh += (__half2float(hi) + lo) * (1024.0f / kE);
+      qs += qn;
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {
+      oh += __shfl_xor_sync(0xffffffffu, oh, o);
+      qs += __shfl_xor_sync(0xffffffffu, qs, o);
+    }
+    if ((lane & 15) == 0) {
+      iq.iqc[h][lane >> 4] = oh;
+      iq.iqc[h][2 + (lane >> 4)] = qs;
+    }
+  }
+  __syncwarp();
+}
+
 // One 32-token group for one warp: Q' fragments, S = K Q' (2 m-tiles x NT
 // n-tiles), online softmax, O += V^T P' (8 m-tiles x o_tiles<NT>()).
 //
@@ -348,18 +462,35 @@ __device__ __forceinline__ int qb_perm_pos(int c) {
 // the columns too -- column = (head, V group, hi/lo) -- so a lane builds P'
 // for one (head, group) pair instead of one per group; an m-tile's D
 // columns of the other group are then unused (see stage_quant).
-template <int KB, int VB, int NT, bool JC, int GT>
-__device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWarpSmem<NT>& sm,
+//
+// IQ (InnerQ keys, per-token 64-channel groups): Q' is the stream's (built by
+// build_bq_iq), step (a) only stages the group's per-token K {min, scale};
+// in (c) k-steps 0-3 cover key group 0 and 4-7 group 1 in separate
+// accumulators, and the logit of token t is
+//   sum_j scale_tj (S_tj 2^-E - Ohat_j) + min_tj Q_j.
+template <int KB, int VB, int NT, bool JC, int GT, bool IQ = false>
+__device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWarpSmem<NT>& sm, IqWarpSmem* iq,
                                               const unsigned char* st, int g, int lane,
                                               float (&O)[8][o_tiles<NT>()][4], float (&macc)[NT][kNVG],
                                               float (&m_used)[NT], float (&lsum)[NT]) {
-  using SG = StageGeom<KB, VB>;
+  using SG = StageGeom<KB, VB, IQ>;
   constexpr bool HC = head_cols<NT>();
   const int gq = lane >> 2, tq = lane & 3;
 
   // (a) Q' = q * scale_k (hi + lo fp16) into this warp's fragment rows,
   //     bias = q . min_k; V {min, scale} of this lane's token to fp32
+  //     (InnerQ keys: this lane's token's K {min, scale} per group instead)
+  if constexpr (IQ) {
+    const uint2 kw = *reinterpret_cast<const uint2*>(st + SG::KS + 8 * lane);
+    const float2 k0 = unpack_min_scale(kw.x), k1 = unpack_min_scale(kw.y);
+    const int im = vmn_index(lane);
+    iq->kmn[0][im] = k0.x;
+    iq->ksc[0][im] = k0.y;
+    iq->kmn[1][im] = k1.x;
+    iq->ksc[1][im] = k1.y;
+  }
   {
+    if constexpr (!IQ) {
     constexpr int D = qb_pair_dist<KB>();
     const int c0 = qb_first_channel<KB>(lane);
     const uint2 w01 = *reinterpret_cast<const uint2*>(st + SG::KS + 4 * c0);
@@ -411,6 +542,7 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
     const float bsum = reduce_heads<GT>(bpart, lane);
     const int hb = head_of_lane<GT>(lane);
     if ((lane & rest_mask<GT>()) == 0 && hb < g) sm.bias[hb] = bsum;
+    }
     const uint32_t* vsw = reinterpret_cast<const uint32_t*>(st + SG::VS);
     const int iv = vsc_index(lane), im = vmn_index(lane);
     constexpr float kVCentre = (float)(1 << (VB - 1));  // the V codes enter the mma centred
@@ -437,6 +569,14 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
 
   // (c) S = K Q'
   float S[2][NT][4];
+  float Z[2][NT][2];  // InnerQ keys: the logits (base 2) of this lane's tokens and head slots
+  float4 iks0, iks1, ikm0, ikm1;  // InnerQ keys: scale / min of tokens gq + 8i, groups 0 and 1
+  if constexpr (IQ) {
+    iks0 = *reinterpret_cast<const float4*>(&iq->ksc[0][4 * gq]);
+    iks1 = *reinterpret_cast<const float4*>(&iq->ksc[1][4 * gq]);
+    ikm0 = *reinterpret_cast<const float4*>(&iq->kmn[0][4 * gq]);
+    ikm1 = *reinterpret_cast<const float4*>(&iq->kmn[1][4 * gq]);
+  }
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt) {
 #pragma unroll
@@ -447,7 +587,32 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
     uint32_t w0[NW], w1[NW];
     const uint32_t o0 = (16 * mt + gq) * SG::KROW + 4 * NW * tq;
     const uint32_t o1 = o0 + 8 * SG::KROW;
-    if constexpr (NW == 8) {
+    if constexpr (IQ) {
+      // half of the slice from each 64-channel group: bytes NB tq .. of both row halves
+      constexpr int NB = SG::KROW / 8;
+      const uint32_t r0 = (16 * mt + gq) * SG::KROW + NB * tq, r1 = r0 + 8 * SG::KROW;
+      const unsigned char* kc = st + SG::KC;
+      if constexpr (NW == 8) {
+        const uint4 a = *reinterpret_cast<const uint4*>(kc + iq_kswz<KB>(r0));
+        const uint4 b2 = *reinterpret_cast<const uint4*>(kc + iq_kswz<KB>(r0 + SG::KROW / 2));
+        const uint4 c = *reinterpret_cast<const uint4*>(kc + iq_kswz<KB>(r1));
+        const uint4 d2 = *reinterpret_cast<const uint4*>(kc + iq_kswz<KB>(r1 + SG::KROW / 2));
+        w0[0] = a.x; w0[1] = a.y; w0[2] = a.z; w0[3] = a.w; w0[4] = b2.x; w0[5] = b2.y; w0[6] = b2.z; w0[7] = b2.w;
+        w1[0] = c.x; w1[1] = c.y; w1[2] = c.z; w1[3] = c.w; w1[4] = d2.x; w1[5] = d2.y; w1[6] = d2.z; w1[7] = d2.w;
+      } else if constexpr (NW == 4) {
+        const uint2 a = *reinterpret_cast<const uint2*>(kc + iq_kswz<KB>(r0));
+        const uint2 b2 = *reinterpret_cast<const uint2*>(kc + iq_kswz<KB>(r0 + SG::KROW / 2));
+        const uint2 c = *reinterpret_cast<const uint2*>(kc + iq_kswz<KB>(r1));
+        const uint2 d2 = *reinterpret_cast<const uint2*>(kc + iq_kswz<KB>(r1 + SG::KROW / 2));
+        w0[0] = a.x; w0[1] = a.y; w0[2] = b2.x; w0[3] = b2.y;
+        w1[0] = c.x; w1[1] = c.y; w1[2] = d2.x; w1[3] = d2.y;
+      } else {
+        w0[0] = *reinterpret_cast<const uint32_t*>(kc + iq_kswz<KB>(r0));
+        w0[1] = *reinterpret_cast<const uint32_t*>(kc + iq_kswz<KB>(r0 + SG::KROW / 2));
+        w1[0] = *reinterpret_cast<const uint32_t*>(kc + iq_kswz<KB>(r1));
+        w1[1] = *reinterpret_cast<const uint32_t*>(kc + iq_kswz<KB>(r1 + SG::KROW / 2));
+      }
+    } else if constexpr (NW == 8) {
       const uint4 a = *reinterpret_cast<const uint4*>(st + SG::KC + swz(o0, SG::KSW));
       const uint4 b2 = *reinterpret_cast<const uint4*>(st + SG::KC + swz(o0 + 16, SG::KSW));
       const uint4 c = *reinterpret_cast<const uint4*>(st + SG::KC + swz(o1, SG::KSW));
@@ -475,7 +640,14 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
       uint32_t lo0, hi0, lo1, hi1;
       k_frag<KB>(w0, s_, lo0, hi0);
       k_frag<KB>(w1, s_, lo1, hi1);
-      if constexpr (HC) {
+      if constexpr (IQ) {
+        // key group 0 (k-steps 0-3) into S, group 1 (4-7) into S2; head columns:
+        // [0] hi and [1] lo tables
+        float (*acc)[4] = s_ < 4 ? S[mt] : S2;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          mma16816(acc[nt], lo0, lo1, hi0, hi1, bq[nt][2 * s_], bq[nt][2 * s_ + 1]);
+      } else if constexpr (HC) {
         // hi and lo parts: two independent chains, summed below
         mma16816(S[mt][0], lo0, lo1, hi0, hi1, bq[0][2 * s_], bq[0][2 * s_ + 1]);
         mma16816(S[mt][1], lo0, lo1, hi0, hi1, bq[1][2 * s_], bq[1][2 * s_ + 1]);
@@ -489,7 +661,28 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
         }
       }
     }
-    if constexpr (HC) {
+    if constexpr (IQ) {
+      // logit = sum_j scale_tj (S_tj 2^-E - Ohat_j) + min_tj Q_j, tokens gq + 8 (2 mt + rh)
+      constexpr float kUn = 1.0f / (float)(1 << kq_exp<KB>());
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int h = slot_head<NT>(nt, tq);
+        const float4 cst = *reinterpret_cast<const float4*>(&iq->iqc[h < g ? h : 0][0]);
+#pragma unroll
+        for (int rh = 0; rh < 2; ++rh) {
+          const int i = 2 * mt + rh;
+          const float a = HC ? S[mt][0][2 * rh + nt] + S[mt][1][2 * rh + nt] : S[mt][nt][2 * rh] + S[mt][nt][2 * rh + 1];
+          const float b = HC ? S2[0][2 * rh + nt] + S2[1][2 * rh + nt] : S2[nt][2 * rh] + S2[nt][2 * rh + 1];
+          const float s0 = i == 0 ? iks0.x : i == 1 ? iks0.y : i == 2 ? iks0.z : iks0.w;
+          const float s1 = i == 0 ? iks1.x : i == 1 ? iks1.y : i == 2 ? iks1.z : iks1.w;
+          const float m0 = i == 0 ? ikm0.x : i == 1 ? ikm0.y : i == 2 ? ikm0.z : ikm0.w;
+          const float m1 = i == 0 ? ikm1.x : i == 1 ? ikm1.y : i == 2 ? ikm1.z : ikm1.w;
+          float z = fmaf(s0, fmaf(a, kUn, -cst.x), m0 * cst.z);
+          z = fmaf(s1, fmaf(b, kUn, -cst.y), fmaf(m1, cst.w, z));
+          Z[mt][nt][rh] = z;
+        }
+      }
+    } else if constexpr (HC) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) S[mt][0][k] += S[mt][1][k];
     } else {
@@ -507,18 +700,18 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
   for (int nt = 0; nt < NT; ++nt) {
     const int h = slot_head<NT>(nt, tq);
     const bool live = h < g;
-    const float bias = live ? sm.bias[h] : 0.0f;
+    const float bias = (IQ || !live) ? 0.0f : sm.bias[h];
     float zs[2][2];
     float zm = -INFINITY;
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
       for (int rh = 0; rh < 2; ++rh) {
-        // 2^E x (logit - bias)
-        zs[mt][rh] = HC ? S[mt][0][2 * rh + nt] : S[mt][nt][2 * rh] + S[mt][nt][2 * rh + 1];
+        // 2^E x (logit - bias); InnerQ keys: the logit
+        zs[mt][rh] = IQ ? Z[mt][nt][rh] : HC ? S[mt][0][2 * rh + nt] : S[mt][nt][2 * rh] + S[mt][nt][2 * rh + 1];
         zm = fmaxf(zm, zs[mt][rh]);
       }
-    constexpr float kUnscale = 1.0f / (float)(1 << kq_exp<KB>());
+    constexpr float kUnscale = IQ ? 1.0f : 1.0f / (float)(1 << kq_exp<KB>());
     // The running maximum moves only when a logit exceeds it by 2^8, which is
     // rare after a stream's first group: test this lane's 4 logits and take
     // the group maximum (shuffles) only when some lane of the warp needs it.

@@ -34,13 +34,15 @@ namespace persist {
 
 using namespace kvq::mma;
 
-template <int KB, int VB, int NT, int GT>
+template <int KB, int VB, int NT, int GT, bool IQ = false>
 struct PersistLayout {
   static constexpr bool kQuant = KB != 16;
   static constexpr int kStages = 2;  // per-warp pipeline depth (items)
   static constexpr int r128(int x) { return (x + 127) / 128 * 128; }
-  static constexpr int kSmem = r128((int)sizeof(MmaWarpSmem<NT>));
-  static constexpr int kQBytes = kQuant ? StageGeom<KB, VB>::BYTES : 0;
+  // the warp's group scratch (InnerQ keys: plus the per-token K scales and the
+  // stream's per-head constants)
+  static constexpr int kSmem = r128((int)sizeof(MmaWarpSmem<NT>) + (IQ ? (int)sizeof(IqWarpSmem) : 0));
+  static constexpr int kQBytes = kQuant ? StageGeom<KB, VB, IQ>::BYTES : 0;
   static constexpr int kStageBytes = kQBytes > F16Geom::BYTES ? kQBytes : F16Geom::BYTES;
   static constexpr int kPerWarpStages = kStages * kStageBytes;
   // this warp's stream's query; once the query is no longer needed (the
@@ -265,10 +267,10 @@ __device__ __forceinline__ void finalize_stream(const DecodeParams& p, int slot,
   if (lane == 0) p.counters[s] = 0u;
 }
 
-template <int KB, int VB, int NT, int GT>
-__global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT>::kCtaThreads, 1)
+template <int KB, int VB, int NT, int GT, bool IQ = false>
+__global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT, IQ>::kCtaThreads, 1)
     decode_persist_kernel(const __grid_constant__ DecodeParams p) {
-  using LY = PersistLayout<KB, VB, NT, GT>;
+  using LY = PersistLayout<KB, VB, NT, GT, IQ>;
   constexpr int KBq = KB == 16 ? 4 : KB, VBq = VB == 16 ? 4 : VB;  // fp16 mode: quantized helpers unused
   constexpr bool JC = NT == 1 && GT <= 2;
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -277,6 +279,7 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT>::kCtaThreads, 1)
   const int g = G.g;
   unsigned char* mine = smem_raw + w * LY::kPerWarp;  // this warp's region; no CTA-wide sharing
   MmaWarpSmem<NT>& sm = *reinterpret_cast<MmaWarpSmem<NT>*>(mine);
+  IqWarpSmem* iq = IQ ? reinterpret_cast<IqWarpSmem*>(mine + sizeof(MmaWarpSmem<NT>)) : nullptr;
   unsigned char* st0 = mine + LY::kSmem;
   const uint32_t st0_s = smem_u32(st0);
   float (*qw)[kHeadDim] = reinterpret_cast<float (*)[kHeadDim]>(mine + LY::kSmem + LY::kPerWarpStages);
@@ -318,7 +321,7 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT>::kCtaThreads, 1)
     if (ij < j1) {
       const uint32_t dst = st0_s + stage * LY::kStageBytes;
       if (LY::kQuant && ik < ng) {
-        if constexpr (LY::kQuant) issue_group<KBq, VBq>(p, is, ik, dst, lane);
+        if constexpr (LY::kQuant) issue_group<KBq, VBq, IQ>(p, is, ik, dst, lane);
       } else {
         issue_f16(p, is, kF16Tokens * (ik - ng), k1, dst, lane);
       }
@@ -384,13 +387,16 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT>::kCtaThreads, 1)
         *reinterpret_cast<float4*>(&qw[r][4 * lane]) = v;
       }
       __syncwarp();
+      // InnerQ keys: the stream's Q' fragments and per-head constants, once
+      if constexpr (IQ && LY::kQuant)
+        build_bq_iq<KBq, NT>(qw, G.knorm ? p.L.k_norm + (size_t)s * kHeadDim : nullptr, sm, *iq, g, lane);
     }
     cp_async_wait<LY::kStages - 1>();
     __syncwarp();
     const unsigned char* stc = st0 + cur * LY::kStageBytes;
     if (LY::kQuant && k < ng) {
       if constexpr (LY::kQuant) {
-        process_group<KB, VB, NT, JC, GT>(qw, sm, stc, g, lane, O, macc, m_used, lsum);
+        process_group<KB, VB, NT, JC, GT, IQ>(qw, sm, iq, stc, g, lane, O, macc, m_used, lsum);
         has_q = true;
       }
     } else {
@@ -423,54 +429,55 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT>::kCtaThreads, 1)
 namespace kvq {
 namespace persist {
 
-template <int KB, int VB, int GT>
+template <int KB, int VB, int GT, bool IQ>
 cudaError_t launch_t(const DecodeParams& p, cudaStream_t st) {
   constexpr int NT = GT <= 4 ? 1 : 2;
-  using LY = PersistLayout<KB, VB, NT, GT>;
+  using LY = PersistLayout<KB, VB, NT, GT, IQ>;
   const int smem = LY::kBytes;
   static std::atomic<long long> smem_memo[kMemoDevices];
-  cudaError_t e = ensure_smem_limit(decode_persist_kernel<KB, VB, NT, GT>, smem_memo, smem);
+  cudaError_t e = ensure_smem_limit(decode_persist_kernel<KB, VB, NT, GT, IQ>, smem_memo, smem);
   if (e != cudaSuccess) return e;
   const int ctas = (p.nwarps + LY::kWarps - 1) / LY::kWarps;
-  return launch_dependent(decode_persist_kernel<KB, VB, NT, GT>, dim3(ctas), dim3(LY::kCtaThreads), smem, st, p);
+  return launch_dependent(decode_persist_kernel<KB, VB, NT, GT, IQ>, dim3(ctas), dim3(LY::kCtaThreads), smem, st,
+                          p);
 }
 
 // Resident warps per SM of an instantiation (for sizing the persistent grid).
-template <int KB, int VB, int GT>
+template <int KB, int VB, int GT, bool IQ>
 cudaError_t occupancy_t(int* warps_per_sm) {
   constexpr int NT = GT <= 4 ? 1 : 2;
-  using LY = PersistLayout<KB, VB, NT, GT>;
+  using LY = PersistLayout<KB, VB, NT, GT, IQ>;
   const int smem = LY::kBytes;
   static std::atomic<long long> smem_memo[kMemoDevices], occ_memo[kMemoDevices];
-  cudaError_t e = ensure_smem_limit(decode_persist_kernel<KB, VB, NT, GT>, smem_memo, smem);
+  cudaError_t e = ensure_smem_limit(decode_persist_kernel<KB, VB, NT, GT, IQ>, smem_memo, smem);
   if (e != cudaSuccess) return e;
   int ctas = 0;
-  e = occupancy_memo(decode_persist_kernel<KB, VB, NT, GT>, occ_memo, LY::kCtaThreads, smem, &ctas);
+  e = occupancy_memo(decode_persist_kernel<KB, VB, NT, GT, IQ>, occ_memo, LY::kCtaThreads, smem, &ctas);
   *warps_per_sm = ctas * LY::kWarps;
   return e;
 }
 
-template <int KB, int VB>
+template <int KB, int VB, bool IQ = false>
 cudaError_t dispatch_gt(const DecodeParams& p, cudaStream_t st, int* occ) {
   const int g = p.geo.g;
   if (occ) {
-    if (g <= 1) return occupancy_t<KB, VB, 1>(occ);
-    if (g <= 2) return occupancy_t<KB, VB, 2>(occ);
-    if (g <= 4) return occupancy_t<KB, VB, 4>(occ);
-    return occupancy_t<KB, VB, 8>(occ);
+    if (g <= 1) return occupancy_t<KB, VB, 1, IQ>(occ);
+    if (g <= 2) return occupancy_t<KB, VB, 2, IQ>(occ);
+    if (g <= 4) return occupancy_t<KB, VB, 4, IQ>(occ);
+    return occupancy_t<KB, VB, 8, IQ>(occ);
   }
-  if (g <= 1) return launch_t<KB, VB, 1>(p, st);
-  if (g <= 2) return launch_t<KB, VB, 2>(p, st);
-  if (g <= 4) return launch_t<KB, VB, 4>(p, st);
-  return launch_t<KB, VB, 8>(p, st);
+  if (g <= 1) return launch_t<KB, VB, 1, IQ>(p, st);
+  if (g <= 2) return launch_t<KB, VB, 2, IQ>(p, st);
+  if (g <= 4) return launch_t<KB, VB, 4, IQ>(p, st);
+  return launch_t<KB, VB, 8, IQ>(p, st);
 }
 
-template <int KB>
+template <int KB, bool IQ = false>
 cudaError_t dispatch_vb(const DecodeParams& p, cudaStream_t st, int* occ) {
   switch (p.geo.vb) {
-    case 2: return dispatch_gt<KB, 2>(p, st, occ);
-    case 4: return dispatch_gt<KB, 4>(p, st, occ);
-    case 8: return dispatch_gt<KB, 8>(p, st, occ);
+    case 2: return dispatch_gt<KB, 2, IQ>(p, st, occ);
+    case 4: return dispatch_gt<KB, 4, IQ>(p, st, occ);
+    case 8: return dispatch_gt<KB, 8, IQ>(p, st, occ);
   }
   return cudaErrorInvalidValue;
 }

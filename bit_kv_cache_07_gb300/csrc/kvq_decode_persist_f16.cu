@@ -8,6 +8,9 @@ namespace kvq {
 cudaError_t persist_k2(const DecodeParams& p, cudaStream_t st, int* occ);
 cudaError_t persist_k4(const DecodeParams& p, cudaStream_t st, int* occ);
 cudaError_t persist_k8(const DecodeParams& p, cudaStream_t st, int* occ);
+cudaError_t persist_iq_k2(const DecodeParams& p, cudaStream_t st, int* occ);
+cudaError_t persist_iq_k4(const DecodeParams& p, cudaStream_t st, int* occ);
+cudaError_t persist_iq_k8(const DecodeParams& p, cudaStream_t st, int* occ);
 
 static cudaError_t persist_f16(const DecodeParams& p, cudaStream_t st, int* occ) {
   return persist::dispatch_gt<16, 16>(p, st, occ);
@@ -15,6 +18,14 @@ static cudaError_t persist_f16(const DecodeParams& p, cudaStream_t st, int* occ)
 
 static cudaError_t dispatch(const DecodeParams& p, cudaStream_t st, int* occ) {
   if (p.geo.fp16_mode) return persist_f16(p, st, occ);
+  if (p.geo.gkc) {  // InnerQ keys
+    switch (p.geo.kb) {
+      case 2: return persist_iq_k2(p, st, occ);
+      case 4: return persist_iq_k4(p, st, occ);
+      case 8: return persist_iq_k8(p, st, occ);
+    }
+    return cudaErrorInvalidValue;
+  }
   switch (p.geo.kb) {
     case 2: return persist_k2(p, st, occ);
     case 4: return persist_k4(p, st, occ);
@@ -39,7 +50,9 @@ cudaError_t plan_persist(DecodeParams& p, uint64_t* ws_need) {
   p.nt = (p.S_eff + p.W + mma::kF16Tokens - 1) / mma::kF16Tokens;
   p.n_items = p.ng + p.nt;
   // bytes an item reads: a quantized group (codes, K scales, V scales) or an fp16 item's K and V rows
-  p.wq = G.fp16_mode ? 1 : (long long)kGroupTokens * (G.krow + G.vrow) + kHeadDim * 4 + kGroupTokens * G.nvg * 4;
+  p.wq = G.fp16_mode ? 1
+                     : (long long)kGroupTokens * (G.krow + G.vrow) + (G.gkc ? kGroupTokens * G.nkg * 4 : kHeadDim * 4) +
+                           kGroupTokens * G.nvg * 4;
   p.wt = (long long)mma::kF16Tokens * kHeadDim * 2 * 2;
   p.wstream = (long long)p.ng * p.wq + (long long)p.nt * p.wt;
   p.wtot = (long long)G.NS * p.wstream;

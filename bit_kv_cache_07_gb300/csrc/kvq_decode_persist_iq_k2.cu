@@ -1,0 +1,10 @@
+// kvq_decode_persist_iq_k2.cu -- persistent tensor-core decode instantiations
+// for InnerQ keys (per-token 64-channel groups) at 2 bits (V 2, 4 or 8 bits;
+// 1, 2, 4 or 8 query heads per KV head).
+#include "kvq_decode_persist.cuh"
+
+namespace kvq {
+cudaError_t persist_iq_k2(const DecodeParams& p, cudaStream_t st, int* occ) {
+  return persist::dispatch_vb<2, true>(p, st, occ);
+}
+}  // namespace kvq

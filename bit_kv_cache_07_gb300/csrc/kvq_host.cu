@@ -35,6 +35,10 @@ kvq_status make_geometry(const kvq_config* c, Geometry* g) {
   if (c->k_pre_rope && !(c->rope_theta > 0.0f && std::isfinite(c->rope_theta))) return KVQ_ERR_INVALID_ARG;
   if (c->position_offset < 0 || (int64_t)c->position_offset + c->max_tokens >= (int64_t)1 << 31)
     return KVQ_ERR_INVALID_ARG;
+  if ((c->hybrid_groups != 0 && c->hybrid_groups != 1) || (c->k_channel_norm != 0 && c->k_channel_norm != 1) ||
+      c->k_group_channels < 0)
+    return KVQ_ERR_INVALID_ARG;
+  if (c->k_channel_norm && !c->k_group_channels) return KVQ_ERR_INVALID_ARG;
   if (c->head_dim != kHeadDim) return KVQ_ERR_UNSUPPORTED;
   if (c->n_q_heads / c->n_kv_heads > kMaxGQA) return KVQ_ERR_UNSUPPORTED;
   const int64_t ns = (int64_t)c->batch * c->n_kv_heads;
@@ -51,6 +55,13 @@ kvq_status make_geometry(const kvq_config* c, Geometry* g) {
     if (!valid_lut(c->k_lut) || !valid_lut(c->v_lut)) return KVQ_ERR_INVALID_ARG;
   } else if (!uni(c->k_bits) || !uni(c->v_bits)) {
     return KVQ_ERR_UNSUPPORTED;
+  }
+  const bool uniform = !fp16 && c->k_bits != 3;
+  if (c->hybrid_groups && !uniform) return KVQ_ERR_UNSUPPORTED;
+  if (c->k_group_channels) {
+    // InnerQ K: 64-channel per-token groups, served by the persistent decode
+    if (c->k_group_channels != 64 || !uniform || c->v_group_channels != 64 || c->k_pre_rope)
+      return KVQ_ERR_UNSUPPORTED;
   }
   if (!fp16) {
     if (c->k_group_tokens != kGroupTokens) return KVQ_ERR_UNSUPPORTED;
@@ -79,6 +90,10 @@ kvq_status make_geometry(const kvq_config* c, Geometry* g) {
   g->nout = (c->k_bits == 3) ? c->outliers_per_vector : 0;
   g->rope_theta = c->rope_theta;
   g->pos_offset = c->position_offset;
+  g->gkc = c->k_group_channels;
+  g->nkg = c->k_group_channels ? kHeadDim / c->k_group_channels : 0;
+  g->hybrid = c->hybrid_groups;
+  g->knorm = c->k_channel_norm;
   if (fp16) {
     g->S = 0;
     g->R = 0;
@@ -122,7 +137,7 @@ kvq_status build_layout(const kvq_config* c, const Geometry& g, kvq_layout* L) {
   };
   const uint64_t NS = (uint64_t)g.NS, Q = (uint64_t)g.qcap, d = kHeadDim;
   put(L->k_codes, NS * Q * g.krow);
-  put(L->k_scales, g.kb == 3 ? NS * Q * 4 : NS * (uint64_t)g.gcap * d * 4);
+  put(L->k_scales, g.kb == 3 ? NS * Q * 4 : g.gkc ? NS * Q * g.nkg * 4 : NS * (uint64_t)g.gcap * d * 4);
   put(L->v_codes, NS * Q * g.vrow);
   put(L->v_scales, g.vb == 3 ? NS * Q * 4 : NS * Q * g.nvg * 4);
   put(L->k_sink, NS * g.S * d * 2);
@@ -137,6 +152,7 @@ kvq_status build_layout(const kvq_config* c, const Geometry& g, kvq_layout* L) {
   put(L->v_csr_rowptr, nuq ? NS * (Q + 1) * 4 : 0);
   put(L->v_csr_col, nuq ? NS * Q * k : 0);
   put(L->v_csr_val, nuq ? NS * Q * k * 2 : 0);
+  put(L->k_norm, g.knorm ? NS * d * 4 : 0);
   L->layer_bytes = off;
   L->max_splits = kMaxQSplits + 1;
   L->ring_slots = g.ring;
@@ -164,6 +180,7 @@ void layer_ptrs(const kvq_layout& L, void* base, LayerPtrs* P) {
   P->v_rowptr = (int32_t*)at(L.v_csr_rowptr);
   P->v_col = (uint8_t*)at(L.v_csr_col);
   P->v_val = (uint16_t*)at(L.v_csr_val);
+  P->k_norm = (float*)at(L.k_norm);
 }
 
 // Split plan: how many splits cover `ngroups` 32-token groups of NS streams.
@@ -455,6 +472,8 @@ kvq_status kvq_append(const kvq_config* cfg, void* layer_buf, int32_t tokens_bef
     p.v_lut[i] = cfg->v_lut[i];
   }
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // InnerQ key normalisation: fixed by the first append into an empty cache
+  if (g.knorm && tokens_before == 0 && launch_key_norm(p, cs) != cudaSuccess) return KVQ_ERR_CUDA;
   const int n_groups = (p.nq_after - p.nq_before) / kGroupTokens;
   if (n_groups > 0) {
     if (launch_append_quantize(p, n_groups, cs) != cudaSuccess) return KVQ_ERR_CUDA;

@@ -28,6 +28,9 @@ struct Geometry {
   int krow, vrow;
   int hadamard, pre_rope, nout, fp16_mode;
   int pos_offset;  // absolute position of the cache's first token (RoPE)
+  int gkc, nkg;    // InnerQ K: channels per per-token K group (0: per-channel K), groups per token
+  int hybrid;      // InnerQ: symmetric / asymmetric choice per uniform group
+  int knorm;       // InnerQ: per-channel key normalisation
   float rope_theta;
 };
 
@@ -47,6 +50,7 @@ struct LayerPtrs {
   int32_t* v_rowptr;
   uint8_t* v_col;
   uint16_t* v_val;
+  float* k_norm;        // [NS][d] InnerQ key normalisation
 };
 
 struct AppendParams {
@@ -315,6 +319,7 @@ cudaError_t launch_nuq_fit(const uint16_t* x, long long nvec, int k, int hadamar
 cudaError_t launch_merge_attn(int n_parts, long long rows, const uint16_t* outs, const float* lses,
                               uint16_t* out, float* lse_out, cudaStream_t st);
 cudaError_t launch_append_quantize(const AppendParams& p, int n_groups, cudaStream_t st);
+cudaError_t launch_key_norm(const AppendParams& p, cudaStream_t st);
 cudaError_t launch_append_window(const AppendParams& p, cudaStream_t st);
 // Split-K decode; with occ != nullptr it only reports the kernel's resident
 // CTAs per SM (for sizing the grid) and launches nothing.

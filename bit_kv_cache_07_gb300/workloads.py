@@ -23,7 +23,8 @@ PAIR_ORDER = ["KV8", "K8V4", "KV4", "K4V2", "KV2"]
 
 _BASE = dict(head_dim=128, k_group_tokens=32, v_group_channels=64, n_sink=0, n_recent=0,
              v_hadamard=0, k_pre_rope=0, rope_theta=10000.0, outliers_per_vector=0,
-             softmax_scale=0.0, split_tokens=0, position_offset=0)
+             softmax_scale=0.0, split_tokens=0, position_offset=0, k_group_channels=0, hybrid_groups=0,
+             k_channel_norm=0)
 
 WORKLOADS = {
     "toy_k4v2_t1k": dict(
@@ -42,6 +43,13 @@ WORKLOADS = {
         _BASE, layers=28, batch=64, n_q_heads=28, n_kv_heads=4, tokens=8192,
         pairs="K4V2", v_hadamard=1, n_sink=4, n_recent=32,
         k_dist="normal", k_outlier_channels="random3", k_outlier_scale=8.0, v_dist="student_t3"),
+    # InnerQ: keys grouped per token along the hidden dimension (64 channels),
+    # hybrid symmetric / asymmetric groups, per-channel key normalisation, at
+    # the Llama-3-8B shape with the pages' 4-bit example and 32 recent tokens
+    "llama3_8b_innerq_kv4_t32k": dict(
+        _BASE, layers=32, batch=16, n_q_heads=32, n_kv_heads=8, tokens=32768,
+        pairs="KV4", n_sink=4, n_recent=32, k_group_channels=64, hybrid_groups=1, k_channel_norm=1,
+        k_dist="normal", k_outlier_channels="random3", k_outlier_scale=8.0, v_dist="laplace"),
     "llama7b_nuq3_t1m": dict(
         _BASE, layers=1, batch=1, n_q_heads=32, n_kv_heads=32, tokens=1048576,
         pairs="NUQ3", k_pre_rope=1, outliers_per_vector=2, lut="fitted", lut_calib_tokens=2048,
@@ -50,7 +58,7 @@ WORKLOADS = {
 
 # order of the workloads as listed with the method's benchmark
 WORKLOAD_ORDER = ["toy_k4v2_t1k", "llama2_7b_kv4_t4k", "llama3_8b_mixed_t32k",
-                  "qwen_gqa_hadamard_t8k", "llama7b_nuq3_t1m"]
+                  "qwen_gqa_hadamard_t8k", "llama7b_nuq3_t1m", "llama3_8b_innerq_kv4_t32k"]
 
 
 def layer_pairs(name: str) -> list[str]:
@@ -93,7 +101,7 @@ def fp16_baseline_config(cfg: dict) -> dict:
     """The same shape as an all-fp16 cache (the baseline decode)."""
     c = dict(cfg)
     c.update(k_bits=16, v_bits=16, n_sink=0, n_recent=0, v_hadamard=0, k_pre_rope=0,
-             outliers_per_vector=0)
+             outliers_per_vector=0, k_group_channels=0, hybrid_groups=0, k_channel_norm=0)
     return c
 
 

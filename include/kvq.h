@@ -93,6 +93,27 @@ typedef struct kvq_config {
                                  after dequantization rotates the key at
                                  position_offset + t.  >= 0, and
                                  position_offset + max_tokens < 2^31           */
+    /* InnerQ (InnerQ summary, "Key Contributions" and "Methodology" 1-4): */
+    int32_t k_group_channels; /* 0: K per channel over k_group_tokens tokens;
+                                 64: K per token in groups of 64 channels along
+                                 the hidden dimension (uniform 2/4/8-bit K,
+                                 64-channel V groups, no pre-RoPE K)           */
+    int32_t hybrid_groups;    /* 1: every uniform K and V group codes itself
+                                 symmetrically when its mean lies within half an
+                                 asymmetric step of zero,
+                                 |mean| * 2^(b+1) <= max - min (mean in exact
+                                 fp64): scale = max|x| / (2^(b-1) - 1), code =
+                                 clamp(rint(x / scale), -(2^(b-1)-1), 2^(b-1)-1)
+                                 + 2^(b-1), stored min = -2^(b-1) * fp16(scale)
+                                 (so dequantization is unchanged); otherwise
+                                 asymmetric.  0: always asymmetric.            */
+    int32_t k_channel_norm;   /* 1 (with k_group_channels 64): per-channel key
+                                 normalisation: the first append into an empty
+                                 cache sets n_c = the smallest power of two
+                                 >= max |K_c| over its tokens (1 for a zero
+                                 channel); quantized keys are coded as K / n_c
+                                 and the decode multiplies q by n_c.  Sinks and
+                                 the fp16 window stay raw.                     */
 } kvq_config;
 
 /* Window rule.  For a sequence holding T tokens:
@@ -121,6 +142,8 @@ typedef struct kvq_region {
  *                                  bitstream (bit 0 = LSB of byte 0)
  *  k_scales  uniform K:  [NS][Gcap][d] {min, scale} fp16 pairs (min first), one
  *                        per channel per G_K-token group
+ *            InnerQ K (k_group_channels 64): [NS][Qcap][d/64] {min, scale}, one
+ *                        per token per 64-channel group
  *            non-uniform K: [NS][Qcap] {min, s} fp16 pairs, one per token
  *  v_codes   [NS][Qcap][VROW] u8   packed V row of token i (rotated domain when
  *                                  v_hadamard)
@@ -130,6 +153,7 @@ typedef struct kvq_region {
  *  k_ring, v_ring [NS][RING][d] fp16  window tokens; position t lives in slot
  *                                  (t - S) mod RING (slot t in fp16 mode); V is
  *                                  stored unrotated
+ *  k_norm   [NS][d] f32            InnerQ key normalisation n_c (k_channel_norm)
  *  k_csr_rowptr [NS][Qcap+1] i32, k_csr_col [NS][Qcap*k] u8,
  *  k_csr_val [NS][Qcap*k] fp16     non-uniform K outliers as CSR over token rows
  *                                  (rowptr counts from 0 per stream; columns
@@ -156,6 +180,7 @@ typedef struct kvq_layout {
     int32_t max_splits;       /* upper bound on decode splits per stream        */
     int32_t ring_slots;       /* RING                                           */
     int32_t q_cap;            /* Qcap                                           */
+    kvq_region k_norm;        /* InnerQ key normalisation (0 bytes if unused)   */
 } kvq_layout;
 
 /* kvq_layout_query -- host only, no CUDA call.

@@ -123,6 +123,93 @@ void orc_quantize_uniform(const uint16_t *x, int n, int stride, int bits,
     *scale_h = orc_float_to_half(scale);
 }
 
+/* The InnerQ per-group quantizer on fp32 inputs x[i*stride] (i < n), b bits.
+ *   mn, mx   : min / max
+ *   mean     : (sum of x) / n in fp64 (exact: see below)
+ *   symmetric when `hybrid`, mx > mn and |mean| * 2^(b+1) <= mx - mn (the
+ *   mean lies within half an asymmetric step of zero: the group is centred):
+ *     a       = max(|mn|, |mx|), qs = 2^(b-1) - 1
+ *     scale32 = a / qs                                   (fp32 RN)
+ *     code    = clamp(rint(x / scale32), -qs, qs) + 2^(b-1)   (fp32, RN-even)
+ *     stored  : scale_h = fp16_RN(scale32), min_h = fp16(-2^(b-1) * scale_h),
+ *               so that min_h + code * scale_h = (code - 2^(b-1)) * scale_h
+ *     (if 2^(b-1) * scale_h overflows fp16 the group falls back to asymmetric)
+ *   otherwise asymmetric, as orc_quantize_uniform: scale32 = (mx - mn) / (2^b - 1),
+ *     code = clamp(rint((x - mn) / scale32), 0, 2^b - 1), min_h = fp16_RN(mn),
+ *     scale_h = fp16_RN(scale32); a constant group stores scale 0, codes 0.
+ * The inputs are fp16 values, or fp16 values divided by powers of two up to
+ * 2^16 (the key normalisation), so each is an integer multiple of 2^-40 below
+ * 2^16 in magnitude and the fp64 sum of n <= 128 of them is exact. */
+void orc_quantize_group(const float *x, int n, int stride, int bits, int hybrid,
+                        uint8_t *code, int code_stride, uint16_t *min_h, uint16_t *scale_h)
+{
+    float mn = x[0], mx = x[0];
+    double sum = 0.0;
+    for (int i = 0; i < n; i++) {
+        float v = x[(long)i * stride];
+        if (v < mn) mn = v;
+        if (v > mx) mx = v;
+        sum += (double)v;
+    }
+    double mean = sum / (double)n;
+    if (hybrid && mx > mn && fabs(mean) * (double)(1 << (bits + 1)) <= (double)mx - (double)mn) {
+        float a = fabsf(mn) > fabsf(mx) ? fabsf(mn) : fabsf(mx);
+        float qs = (float)((1 << (bits - 1)) - 1);
+        float scale = a / qs;
+        uint16_t sh = orc_float_to_half(scale);
+        float mf = -(float)(1 << (bits - 1)) * orc_half_to_float(sh);
+        uint16_t mh = orc_float_to_half(mf);
+        if (isfinite(orc_half_to_float(mh))) {
+            for (int i = 0; i < n; i++) {
+                float r = rintf(x[(long)i * stride] / scale);
+                if (r < -qs) r = -qs;
+                if (r > qs) r = qs;
+                code[(long)i * code_stride] = (uint8_t)((int)r + (1 << (bits - 1)));
+            }
+            *min_h = mh;
+            *scale_h = sh;
+            return;
+        }
+    }
+    float qmax = (float)((1 << bits) - 1);
+    float scale = (mx - mn) / qmax;
+    for (int i = 0; i < n; i++) {
+        int c = 0;
+        if (scale != 0.0f) {
+            float r = rintf((x[(long)i * stride] - mn) / scale);
+            if (r < 0.0f) r = 0.0f;
+            if (r > qmax) r = qmax;
+            c = (int)r;
+        }
+        code[(long)i * code_stride] = (uint8_t)c;
+    }
+    *min_h = orc_float_to_half(mn);
+    *scale_h = orc_float_to_half(scale);
+}
+
+/* InnerQ per-channel key normalisation: for each channel c, n_c = 2^e with e
+ * the smallest integer such that max_t |K_tc| <= 2^e over the given tokens
+ * (1 for an all-zero channel).  A power of two, so K / n_c and q * n_c are
+ * exact; |K / n_c| <= 1 on those tokens. */
+void orc_key_norm(const uint16_t *K, int T, int d, float *norm)
+{
+    for (int c = 0; c < d; c++) {
+        float m = 0.0f;
+        for (int t = 0; t < T; t++) {
+            float a = fabsf(orc_half_to_float(K[(size_t)t * d + c]));
+            if (a > m) m = a;
+        }
+        float n = 1.0f;
+        if (m > 0.0f) {
+            int e;
+            frexpf(m, &e);            /* m = f * 2^e, f in [0.5, 1) */
+            n = ldexpf(1.0f, e);      /* 2^e >= m */
+            if (ldexpf(1.0f, e - 1) >= m) n = ldexpf(1.0f, e - 1);  /* m a power of two */
+        }
+        norm[c] = n;
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Bit packing: code i of a row occupies bits [b*i, b*i + b) of the row's    */
 /* little-endian bitstream (bit 0 = least significant bit of byte 0).       */
@@ -310,6 +397,15 @@ typedef struct orc_cfg {
     int32_t pos_offset;   /* absolute position of the stream's first token (a
                              context shard that starts later); RoPE angles use
                              pos_offset + t */
+    int32_t gkc;          /* InnerQ K layout: per token, groups of gkc channels
+                             along the hidden dimension (0: per channel over gk
+                             tokens) */
+    int32_t hybrid;       /* InnerQ: every uniform group picks a symmetric or an
+                             asymmetric grid from its own statistics */
+    int32_t k_norm;       /* InnerQ: per-channel key normalisation (InnerQ K
+                             layout only) */
+    int32_t norm_tokens;  /* the first norm_tokens tokens (the prefill) fix the
+                             normalisation (<= 0: all T tokens) */
 } orc_cfg;
 
 /* Sinks are positions [0, S).  The quantized tokens are the
@@ -350,12 +446,15 @@ static int row_bytes(int bits, int d) { return d * bits / 8; }
  *  kwin,  vwin  [W][d]           fp16 copies of the window tokens (position order)
  *  k_rowptr [Nq+1], k_cols [Nq*k], k_vals [Nq*k]  (NUQ K outliers, CSR)
  *  v_rowptr, v_cols, v_vals                        (NUQ V outliers, CSR)
+ *  kn    [d]                     InnerQ key normalisation n_c (fp32 powers of two)
+ *  With the InnerQ K layout (gkc > 0), ks is [Nq][d/gkc][2] (min, scale) per
+ *  token per channel group, of the keys divided by n_c when k_norm is set.
  * V window tokens are stored unrotated even when V is Hadamard-rotated. */
 void orc_build_stream(const orc_cfg *c, int T, const uint16_t *K, const uint16_t *V,
                       uint8_t *kc, uint16_t *ks, uint8_t *vc, uint16_t *vs,
                       uint16_t *ksink, uint16_t *vsink, uint16_t *kwin, uint16_t *vwin,
                       int32_t *k_rowptr, uint8_t *k_cols, uint16_t *k_vals,
-                      int32_t *v_rowptr, uint8_t *v_cols, uint16_t *v_vals)
+                      int32_t *v_rowptr, uint8_t *v_cols, uint16_t *v_vals, float *kn)
 {
     int d = c->d, S, Nq, W;
     orc_layout_counts(c, T, &S, &Nq, &W);
@@ -379,7 +478,27 @@ void orc_build_stream(const orc_cfg *c, int T, const uint16_t *K, const uint16_t
 
     /* K */
     int krow = row_bytes(c->k_bits, d);
-    if (c->k_bits == 3) {
+    if (c->k_norm) {
+        int P = (c->norm_tokens > 0 && c->norm_tokens < T) ? c->norm_tokens : T;
+        orc_key_norm(K, P, d, kn);
+    }
+    if (c->gkc > 0) {
+        /* InnerQ: per token, groups of gkc channels along the hidden dimension,
+         * on the normalised keys K / n_c */
+        float xn[1024];
+        int ng = d / c->gkc;
+        for (int i = 0; i < Nq; i++) {
+            const uint16_t *x = K + (size_t)(S + i) * d;
+            for (int ch = 0; ch < d; ch++)
+                xn[ch] = orc_half_to_float(x[ch]) / (c->k_norm ? kn[ch] : 1.0f);
+            for (int j = 0; j < ng; j++) {
+                uint16_t *e = ks + ((size_t)i * ng + j) * 2;
+                orc_quantize_group(xn + j * c->gkc, c->gkc, 1, c->k_bits, c->hybrid,
+                                   codes + j * c->gkc, 1, &e[0], &e[1]);
+            }
+            orc_pack_bits(codes, d, c->k_bits, kc + (size_t)i * krow);
+        }
+    } else if (c->k_bits == 3) {
         k_rowptr[0] = 0;
         for (int i = 0; i < Nq; i++) {
             const uint16_t *x = K + (size_t)(S + i) * d;
@@ -391,19 +510,25 @@ void orc_build_stream(const orc_cfg *c, int T, const uint16_t *K, const uint16_t
     } else {
         /* per channel, over groups of gk consecutive quantized tokens */
         uint8_t *gcodes = malloc((size_t)c->gk * d);
+        float *gx = malloc(sizeof(float) * (size_t)c->gk * d);
         int ngrp = Nq / c->gk;
         for (int g = 0; g < ngrp; g++) {
             const uint16_t *base = K + (size_t)(S + g * c->gk) * d;
+            for (size_t e = 0; e < (size_t)c->gk * d; e++) gx[e] = orc_half_to_float(base[e]);
             for (int ch = 0; ch < d; ch++) {
                 uint16_t *e = ks + ((size_t)g * d + ch) * 2;
-                orc_quantize_uniform(base + ch, c->gk, d, c->k_bits,
-                                     gcodes + ch, d, &e[0], &e[1]);
+                if (c->hybrid)
+                    orc_quantize_group(gx + ch, c->gk, d, c->k_bits, 1, gcodes + ch, d, &e[0], &e[1]);
+                else
+                    orc_quantize_uniform(base + ch, c->gk, d, c->k_bits,
+                                         gcodes + ch, d, &e[0], &e[1]);
             }
             for (int r = 0; r < c->gk; r++)
                 orc_pack_bits(gcodes + (size_t)r * d, d, c->k_bits,
                               kc + (size_t)(g * c->gk + r) * krow);
         }
         free(gcodes);
+        free(gx);
     }
 
     /* V */
@@ -421,10 +546,16 @@ void orc_build_stream(const orc_cfg *c, int T, const uint16_t *K, const uint16_t
             v_rowptr[i + 1] = v_rowptr[i] + c->outliers;
         } else {
             int ng = d / c->gv;
+            float xf[1024];
+            for (int ch = 0; ch < d; ch++) xf[ch] = orc_half_to_float(x[ch]);
             for (int j = 0; j < ng; j++) {
                 uint16_t *e = vs + ((size_t)i * ng + j) * 2;
-                orc_quantize_uniform(x + j * c->gv, c->gv, 1, c->v_bits,
-                                     codes + j * c->gv, 1, &e[0], &e[1]);
+                if (c->hybrid)
+                    orc_quantize_group(xf + j * c->gv, c->gv, 1, c->v_bits, 1,
+                                       codes + j * c->gv, 1, &e[0], &e[1]);
+                else
+                    orc_quantize_uniform(x + j * c->gv, c->gv, 1, c->v_bits,
+                                         codes + j * c->gv, 1, &e[0], &e[1]);
             }
         }
         orc_pack_bits(codes, d, c->v_bits, vc + (size_t)i * vrow);
@@ -440,6 +571,7 @@ typedef struct orc_store {
     const uint16_t *ksink, *vsink, *kwin, *vwin;
     const int32_t *k_rowptr; const uint8_t *k_cols; const uint16_t *k_vals;
     const int32_t *v_rowptr; const uint8_t *v_cols; const uint16_t *v_vals;
+    const float *kn;
 } orc_store;
 
 /* K of token t as stored, reconstructed in fp64 (dequantized, or the fp16
@@ -456,7 +588,15 @@ static void token_k(const orc_cfg *c, const orc_store *st, int S, int Nq, int t,
     } else {
         int i = t - S;
         orc_unpack_bits(st->kc + (size_t)i * row_bytes(c->k_bits, d), d, c->k_bits, codes);
-        if (c->k_bits == 3) {
+        if (c->gkc > 0) {
+            int ng = d / c->gkc;
+            for (int ch = 0; ch < d; ch++) {
+                const uint16_t *e = st->ks + ((size_t)i * ng + ch / c->gkc) * 2;
+                double v = (double)orc_half_to_float(e[0]) +
+                           (double)codes[ch] * (double)orc_half_to_float(e[1]);
+                kr[ch] = c->k_norm ? v * (double)st->kn[ch] : v;
+            }
+        } else if (c->k_bits == 3) {
             orc_nuq_decode(codes, d, st->ks[2 * i], st->ks[2 * i + 1], c->k_lut,
                            st->k_rowptr[i + 1] - st->k_rowptr[i], st->k_cols + st->k_rowptr[i],
                            st->k_vals + st->k_rowptr[i], kr);
@@ -517,12 +657,12 @@ void orc_decode_stream(const orc_cfg *c, int T, int g, const uint16_t *q,
                        const uint16_t *kwin, const uint16_t *vwin,
                        const int32_t *k_rowptr, const uint8_t *k_cols, const uint16_t *k_vals,
                        const int32_t *v_rowptr, const uint8_t *v_cols, const uint16_t *v_vals,
-                       double *out, double *lse)
+                       const float *kn, double *out, double *lse)
 {
     int d = c->d, S, Nq, W;
     orc_layout_counts(c, T, &S, &Nq, &W);
     orc_store st = { kc, ks, vc, vs, ksink, vsink, kwin, vwin,
-                     k_rowptr, k_cols, k_vals, v_rowptr, v_cols, v_vals };
+                     k_rowptr, k_cols, k_vals, v_rowptr, v_cols, v_vals, kn };
     double sm = c->sm_scale != 0.0 ? c->sm_scale : 1.0 / sqrt((double)d);
 
     double *qv = malloc(sizeof(double) * (size_t)g * d);

@@ -44,6 +44,7 @@ class _Cfg(C.Structure):
         ("n_recent", C.c_int32), ("v_hadamard", C.c_int32), ("k_pre_rope", C.c_int32),
         ("outliers", C.c_int32), ("rope_theta", C.c_double), ("sm_scale", C.c_double),
         ("k_lut", C.c_float * 8), ("v_lut", C.c_float * 8), ("pos_offset", C.c_int32),
+        ("gkc", C.c_int32), ("hybrid", C.c_int32), ("k_norm", C.c_int32), ("norm_tokens", C.c_int32),
     ]
 
 
@@ -75,9 +76,12 @@ def lib():
         L.orc_rope_apply.argtypes = [f64, C.c_int, C.c_double, C.c_double]
         L.orc_layout_counts.argtypes = [C.POINTER(_Cfg), C.c_int, C.POINTER(C.c_int),
                                         C.POINTER(C.c_int), C.POINTER(C.c_int)]
+        f32 = C.POINTER(C.c_float)
         L.orc_build_stream.argtypes = [C.POINTER(_Cfg), C.c_int, u16, u16,
                                        u8, u16, u8, u16, u16, u16, u16, u16,
-                                       i32, u8, u16, i32, u8, u16]
+                                       i32, u8, u16, i32, u8, u16, f32]
+        L.orc_quantize_group.argtypes = [f32, C.c_int, C.c_int, C.c_int, C.c_int, u8, C.c_int, u16, u16]
+        L.orc_key_norm.argtypes = [u16, C.c_int, C.c_int, f32]
         L.orc_nuq_fit_lut.argtypes = [u16, C.c_long, C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(C.c_float),
                                       f64]
         L.orc_nuq_fit_lut.restype = C.c_int
@@ -86,7 +90,7 @@ def lib():
         L.orc_merge_parts.argtypes = [C.c_int, C.c_int, C.c_int, f64, f64, f64, f64]
         L.orc_decode_stream.argtypes = [C.POINTER(_Cfg), C.c_int, C.c_int, u16,
                                         u8, u16, u8, u16, u16, u16, u16, u16,
-                                        i32, u8, u16, i32, u8, u16, f64, f64]
+                                        i32, u8, u16, i32, u8, u16, f32, f64, f64]
     return _lib
 
 
@@ -195,6 +199,10 @@ def _cfg(cfg: dict) -> _Cfg:
     c.rope_theta = cfg.get("rope_theta", 10000.0)
     c.sm_scale = cfg.get("softmax_scale", 0.0)
     c.pos_offset = cfg.get("position_offset", 0)
+    c.gkc = cfg.get("k_group_channels", 0)
+    c.hybrid = cfg.get("hybrid_groups", 0)
+    c.k_norm = cfg.get("k_channel_norm", 0)
+    c.norm_tokens = cfg.get("norm_tokens", 0)
     for i, v in enumerate(cfg.get("k_lut", [0.0] * 8)):
         c.k_lut[i] = v
     for i, v in enumerate(cfg.get("v_lut", [0.0] * 8)):
@@ -217,9 +225,11 @@ def _store_shapes(cfg: dict, T: int):
     k = cfg.get("outliers_per_vector", 0)
     gk = cfg.get("k_group_tokens", 32)
     gv = cfg.get("v_group_channels", 64)
+    gkc = cfg.get("k_group_channels", 0)
     shapes = {
         "kc": ((Nq, d * kb // 8 if kb != 16 else 0), np.uint8),
-        "ks": (((Nq, 2) if kb == 3 else (Nq // gk if kb != 16 else 0, d, 2)), np.uint16),
+        "ks": (((Nq, 2) if kb == 3 else (Nq, d // gkc, 2) if gkc else (Nq // gk if kb != 16 else 0, d, 2)),
+               np.uint16),
         "vc": ((Nq, d * vb // 8 if vb != 16 else 0), np.uint8),
         "vs": (((Nq, 2) if vb == 3 else (Nq, d // gv if vb != 16 else 0, 2)), np.uint16),
         "ksink": ((S, d), np.uint16), "vsink": ((S, d), np.uint16),
@@ -230,13 +240,14 @@ def _store_shapes(cfg: dict, T: int):
         "v_rowptr": ((Nq + 1 if vb == 3 else 0,), np.int32),
         "v_cols": ((Nq * k if vb == 3 else 0,), np.uint8),
         "v_vals": ((Nq * k if vb == 3 else 0,), np.uint16),
+        "kn": ((d if cfg.get("k_channel_norm", 0) else 0,), np.float32),
     }
     return shapes
 
 
 _ORDER = ["kc", "ks", "vc", "vs", "ksink", "vsink", "kwin", "vwin",
-          "k_rowptr", "k_cols", "k_vals", "v_rowptr", "v_cols", "v_vals"]
-_CT = {np.uint8: C.c_uint8, np.uint16: C.c_uint16, np.int32: C.c_int32}
+          "k_rowptr", "k_cols", "k_vals", "v_rowptr", "v_cols", "v_vals", "kn"]
+_CT = {np.uint8: C.c_uint8, np.uint16: C.c_uint16, np.int32: C.c_int32, np.float32: C.c_float}
 
 
 def _ptrs(store):
@@ -347,3 +358,22 @@ def nuq_fit_positions(x, k: int, hadamard: int = 0) -> np.ndarray:
     pos = np.zeros(max(cap, 1), np.int32)
     n = lib().orc_nuq_fit_positions(_P(xs, C.c_uint16), nvec, d, k, hadamard, _P(pos, C.c_int32), cap)
     return pos[:n]
+
+
+def quantize_group(x, bits: int, hybrid: int):
+    """InnerQ group quantizer on fp32 values -> (codes u8, min_h u16, scale_h u16)."""
+    x = np.ascontiguousarray(x, np.float32).ravel()
+    codes = np.zeros(x.size, np.uint8)
+    mn, sc = C.c_uint16(), C.c_uint16()
+    lib().orc_quantize_group(_P(x, C.c_float), x.size, 1, bits, hybrid, _P(codes, C.c_uint8), 1,
+                             C.byref(mn), C.byref(sc))
+    return codes, mn.value, sc.value
+
+
+def key_norm(K) -> np.ndarray:
+    """Per-channel key normalisation (powers of two) of fp16 K [T, d]."""
+    K = _u16(K)
+    T, d = K.shape
+    out = np.zeros(d, np.float32)
+    lib().orc_key_norm(_P(K, C.c_uint16), T, d, _P(out, C.c_float))
+    return out

@@ -20,7 +20,7 @@ def gpu_store(layer, s: int, T: int, counts) -> dict:
     host = {}
 
     import torch
-    tdt = {np.uint8: torch.uint8, np.uint16: torch.int16, np.int32: torch.int32}
+    tdt = {np.uint8: torch.uint8, np.uint16: torch.int16, np.int32: torch.int32, np.float32: torch.float32}
 
     class _Reg:
         """Region viewed as [NS, ...] on the device; only stream s is copied."""
@@ -63,8 +63,14 @@ def gpu_store(layer, s: int, T: int, counts) -> dict:
     else:
         gcap = qcap // 32
         nvg = d // cfg.v_group_channels
-        host["ks"] = reg("k_scales", np.uint16).reshape(NS, gcap, d, 2)[s, :Nq // 32]
+        if cfg.k_group_channels:  # InnerQ keys: per token, per 64-channel group
+            nkg = d // cfg.k_group_channels
+            host["ks"] = reg("k_scales", np.uint16).reshape(NS, qcap, nkg, 2)[s, :Nq]
+        else:
+            host["ks"] = reg("k_scales", np.uint16).reshape(NS, gcap, d, 2)[s, :Nq // 32]
         host["vs"] = reg("v_scales", np.uint16).reshape(NS, qcap, nvg, 2)[s, :Nq]
+        if cfg.k_channel_norm:
+            host["kn"] = reg("k_norm", np.float32).reshape(NS, d)[s]
     host["vc"] = reg("v_codes", np.uint8).reshape(NS, qcap, vrow)[s, :Nq]
     Sc = cfg.n_sink
     host["ksink"] = reg("k_sink", np.uint16).reshape(NS, Sc, d)[s, :S] if Sc else np.zeros((0, d), np.uint16)
