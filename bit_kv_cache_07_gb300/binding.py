@@ -36,6 +36,7 @@ class kvq_config(C.Structure):
         ("k_lut", C.c_float * 8), ("v_lut", C.c_float * 8), ("softmax_scale", C.c_float),
         ("split_tokens", C.c_int32), ("position_offset", C.c_int32),
         ("k_group_channels", C.c_int32), ("hybrid_groups", C.c_int32), ("k_channel_norm", C.c_int32),
+        ("kv_heads_total", C.c_int32), ("kv_head_index", C.c_void_p),
     ]
 
 
@@ -56,7 +57,7 @@ class kvq_layout(C.Structure):
 
 EXPORTS = ["kvq_layout_query", "kvq_append", "kvq_decode_attn", "kvq_decode_plan",
            "kvq_decode_path", "kvq_status_string", "kvq_decode_attn_noalloc", "kvq_context_shard",
-           "kvq_merge_attn", "kvq_fit_nuq_lut"]
+           "kvq_merge_attn", "kvq_fit_nuq_lut", "kvq_measure_distortion", "kvq_rate_allocate"]
 NUQ_FIT_WORKSPACE_BYTES = 3 * 65538 * 8
 
 _lib = None
@@ -96,6 +97,12 @@ def lib():
         L.kvq_fit_nuq_lut.argtypes = [vp, C.c_int64, C.c_int32, C.c_int32, C.c_int32, C.c_int32, vp, C.c_uint64,
                                       vp, vp, vp]
         L.kvq_fit_nuq_lut.restype = C.c_int
+        L.kvq_measure_distortion.argtypes = [C.POINTER(kvq_config), vp, vp, C.c_int32, C.c_int32, vp, C.c_uint64,
+                                             vp, vp]
+        L.kvq_measure_distortion.restype = C.c_int
+        f64p = C.POINTER(C.c_double)
+        L.kvq_rate_allocate.argtypes = [C.c_int32, f64p, f64p, C.c_int32, C.POINTER(C.c_int32), f64p, f64p, f64p]
+        L.kvq_rate_allocate.restype = C.c_int
         L.kvq_decode_attn_noalloc.argtypes = [C.POINTER(kvq_config), vp, C.c_int32, u16p, u16p, vp, vp]
         L.kvq_decode_attn_noalloc.restype = C.c_int
         L.kvq_status_string.argtypes = [C.c_int]
@@ -109,15 +116,31 @@ def kvq_status_string(status: int) -> str:
 
 
 def make_config(d: dict) -> kvq_config:
-    """kvq_config from a dict with the same field names (missing -> 0)."""
+    """kvq_config from a dict with the same field names (missing -> 0).  A
+    kv_head_index given as a list of ints becomes a host array kept alive by
+    the returned struct."""
     c = kvq_config()
     for name, ctype in kvq_config._fields_:
         if name in ("k_lut", "v_lut"):
             for i, v in enumerate(d.get(name, [0.0] * 8)):
                 getattr(c, name)[i] = float(v)
+        elif name == "kv_head_index":
+            idx = d.get(name)
+            if isinstance(idx, (list, tuple)):
+                arr = (C.c_int32 * len(idx))(*[int(v) for v in idx])
+                c._kv_head_index_keep = arr
+                c.kv_head_index = C.cast(arr, C.c_void_p)
+            elif idx:
+                c.kv_head_index = int(idx)
         elif name in d:
             setattr(c, name, float(d[name]) if ctype is C.c_float else int(d[name]))
     return c
+
+
+def _totals(c: kvq_config):
+    """(KV heads, query heads) of the whole layer the cache belongs to."""
+    hkv = c.kv_heads_total or c.n_kv_heads
+    return hkv, hkv * (c.n_q_heads // c.n_kv_heads)
 
 
 def _cfg(cfg) -> kvq_config:
@@ -193,7 +216,7 @@ def kvq_append(cfg, layer_buf, tokens_before: int, k_new, v_new, n_new: int, str
     import torch
     c = _cfg(cfg)
     lay = kvq_layout_query(c)
-    row = c.batch * c.n_kv_heads * int(n_new) * c.head_dim * 2
+    row = c.batch * _totals(c)[0] * int(n_new) * c.head_dim * 2
     st = lib().kvq_append(C.byref(c), _ptr(layer_buf, "layer_buf", numel=lay.layer_bytes), int(tokens_before),
                           _ptr(k_new, "k_new", torch.float16, row), _ptr(v_new, "v_new", torch.float16, row),
                           int(n_new), _stream(stream))
@@ -205,7 +228,8 @@ def kvq_decode_attn(cfg, layer_buf, tokens: int, q, out, lse=None, workspace=Non
     import torch
     c = _cfg(cfg)
     lay = kvq_layout_query(c)
-    nq = c.batch * c.n_q_heads * c.head_dim * 2
+    hq = _totals(c)[1]
+    nq = c.batch * hq * c.head_dim * 2
     if ws_bytes is None:
         ws_bytes = 0 if workspace is None else (
             workspace if isinstance(workspace, int) else workspace.numel() * workspace.element_size())
@@ -214,7 +238,7 @@ def kvq_decode_attn(cfg, layer_buf, tokens: int, q, out, lse=None, workspace=Non
     st = lib().kvq_decode_attn(
         C.byref(c), _ptr(layer_buf, "layer_buf", numel=lay.layer_bytes), int(tokens),
         _ptr(q, "q", torch.float16, nq), _ptr(out, "out", torch.float16, nq),
-        _ptr(lse, "lse", torch.float32, c.batch * c.n_q_heads * 4, allow_none=True),
+        _ptr(lse, "lse", torch.float32, c.batch * hq * 4, allow_none=True),
         _ptr(workspace, "workspace", allow_none=True), int(ws_bytes), _stream(stream))
     _check("kvq_decode_attn", st)
 
@@ -225,11 +249,12 @@ def kvq_decode_attn_noalloc(cfg, layer_buf, tokens: int, q, out, lse=None, strea
     import torch
     c = _cfg(cfg)
     lay = kvq_layout_query(c)
-    nq = c.batch * c.n_q_heads * c.head_dim * 2
+    hq = _totals(c)[1]
+    nq = c.batch * hq * c.head_dim * 2
     st = lib().kvq_decode_attn_noalloc(
         C.byref(c), _ptr(layer_buf, "layer_buf", numel=lay.layer_bytes), int(tokens),
         _ptr(q, "q", torch.float16, nq), _ptr(out, "out", torch.float16, nq),
-        _ptr(lse, "lse", torch.float32, c.batch * c.n_q_heads * 4, allow_none=True), _stream(stream))
+        _ptr(lse, "lse", torch.float32, c.batch * hq * 4, allow_none=True), _stream(stream))
     _check("kvq_decode_attn_noalloc", st)
 
 
@@ -272,6 +297,40 @@ def kvq_fit_nuq_lut(x, outliers: int, hadamard: int = 0, max_iters: int = 100, w
     else:
         torch.cuda.synchronize(x.device)
     return [float(v) for v in lut.cpu()], int(info.item())
+
+
+def kvq_measure_distortion(cfg, k, v, bits: int, stream=None):
+    """{D_K, D_V} per layer KV head ([Hkv_total, 2] float64 tensor on the GPU)
+    of this cache's quantizers at `bits` on calibration tokens k, v
+    [B, Hkv_total, n, 128] fp16."""
+    import torch
+    c = _cfg(cfg)
+    hkv = _totals(c)[0]
+    n = k.shape[2]
+    ws = torch.empty(max(16, c.batch * c.n_kv_heads * 128 * 4), dtype=torch.uint8, device=k.device)
+    out = torch.empty((hkv, 2), dtype=torch.float64, device=k.device)
+    nb = c.batch * hkv * n * 256
+    st = lib().kvq_measure_distortion(C.byref(c), _ptr(k, "k", torch.float16, nb), _ptr(v, "v", torch.float16, nb),
+                                      int(n), int(bits), ws.data_ptr(), ws.numel(), out.data_ptr(), _stream(stream))
+    _check("kvq_measure_distortion", st)
+    return out
+
+
+def kvq_rate_allocate(distortion, total_bits: int, weights=None):
+    """Greedy per-component bits (2/4/8) from distortions [n, 3] at 2, 4, 8
+    bits; returns (bits, alpha, beta, continuous water-filling bits)."""
+    import numpy as np
+    D = np.ascontiguousarray(distortion, np.float64)
+    n = D.shape[0]
+    w = None if weights is None else np.ascontiguousarray(weights, np.float64)
+    bits = np.zeros(n, np.int32)
+    a, b, wf = np.zeros(n), np.zeros(n), np.zeros(n)
+    f64p = C.POINTER(C.c_double)
+    st = lib().kvq_rate_allocate(n, D.ctypes.data_as(f64p), None if w is None else w.ctypes.data_as(f64p),
+                                 int(total_bits), bits.ctypes.data_as(C.POINTER(C.c_int32)), a.ctypes.data_as(f64p),
+                                 b.ctypes.data_as(f64p), wf.ctypes.data_as(f64p))
+    _check("kvq_rate_allocate", st)
+    return bits, a, b, wf
 
 
 def kvq_merge_attn(outs, lses, out, lse_out=None, stream=None):

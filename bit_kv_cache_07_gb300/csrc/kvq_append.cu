@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
       const int t = G.S + grp * kGroupTokens + r;
       const uint16_t *srck, *srcv;
       if (t >= p.tokens_before) {
-        const size_t off = ((size_t)s * p.n_new + (t - p.tokens_before)) * kRowHalves;
+        const size_t off = (in_stream(G, s) * p.n_new + (t - p.tokens_before)) * kRowHalves;
         srck = p.k_new + off;
         srcv = p.v_new + off;
       } else {
@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
 // channel (threads of a warp read consecutive channels of a token row).
 __global__ void __launch_bounds__(kHeadDim) key_norm_kernel(const __grid_constant__ AppendParams p) {
   const int s = blockIdx.x, c = threadIdx.x;
-  const uint16_t* k = p.k_new + (size_t)s * p.n_new * kRowHalves + c;
+  const uint16_t* k = p.k_new + in_stream(p.geo, s) * p.n_new * kRowHalves + c;
   float m = 0.0f;
   for (int t = 0; t < p.n_new; ++t) m = fmaxf(m, fabsf(half_bits_to_float(k[(size_t)t * kRowHalves])));
   float n = 1.0f;
@@ -477,7 +477,7 @@ __global__ void __launch_bounds__(256) append_window_kernel(const __grid_constan
     } else {
       continue;  // quantized by this call
     }
-    const uint16_t* src = (isv ? p.v_new : p.k_new) + ((size_t)s * p.n_new + j) * kRowHalves;
+    const uint16_t* src = (isv ? p.v_new : p.k_new) + (in_stream(G, s) * p.n_new + j) * kRowHalves;
     reinterpret_cast<uint4*>(dst)[ch] = reinterpret_cast<const uint4*>(src)[ch];
   }
 }
@@ -628,7 +628,173 @@ __global__ void __launch_bounds__(1024)
   if (info_out) *info_out = ok ? it : -1;
 }
 
+// --------------------------------------------------- distortion per head
+// Mean squared error of the cache's uniform quantizers at `bits` on
+// calibration tokens (RateQuant, "Methodology" 1 and 3: the distortion-rate
+// curve of this quantizer, fitted per head, K and V separately).  One CTA
+// per (32-token block, stream): K per channel over the block when it is
+// whole (or, InnerQ keys, per token over 64-channel groups of the normalised
+// keys), V per token over its channel groups (rotated first with Hadamard
+// V); x^ = min + code scale from the stored fp16 pair, errors squared and
+// summed in fp64 into sse[layer head][K, V].
+__global__ void __launch_bounds__(kThreads)
+    distortion_kernel(const __grid_constant__ AppendParams p, int n_tokens, int bits, const float* __restrict__ knorm,
+                      double* __restrict__ sse) {
+  const Geometry& G = p.geo;
+  const int blk = blockIdx.x, s = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  __shared__ __align__(16) uint16_t sK[kGroupTokens][kRowHalves];
+  __shared__ __align__(16) uint16_t sV[kGroupTokens][kRowHalves];
+  __shared__ double red[2][kThreads / 32];
+  const int t0 = blk * kGroupTokens, nt = min(kGroupTokens, n_tokens - t0);
+  for (int idx = tid; idx < kGroupTokens * kRowVec; idx += kThreads) {
+    const int r = idx / kRowVec, ch = idx % kRowVec;
+    uint4 kx = make_uint4(0, 0, 0, 0), vx = kx;
+    if (r < nt) {
+      const size_t off = (in_stream(G, s) * n_tokens + t0 + r) * kRowHalves;
+      kx = reinterpret_cast<const uint4*>(p.k_new + off)[ch];
+      vx = reinterpret_cast<const uint4*>(p.v_new + off)[ch];
+    }
+    reinterpret_cast<uint4*>(&sK[r][0])[ch] = kx;
+    reinterpret_cast<uint4*>(&sV[r][0])[ch] = vx;
+  }
+  __syncthreads();
+  double ek = 0.0, ev = 0.0;
+  if (!G.gkc) {
+    if (nt == kGroupTokens) {  // per channel over the whole block
+      const int c = tid;
+      float x[kGroupTokens];
+      float mn = INFINITY, mx = -INFINITY;
+      double sum = 0.0;
+#pragma unroll
+      for (int r = 0; r < kGroupTokens; ++r) {
+        x[r] = half_bits_to_float(sK[r][c]);
+        mn = fminf(mn, x[r]);
+        mx = fmaxf(mx, x[r]);
+        sum += (double)x[r];
+      }
+      const GroupQ gq = group_params(mn, mx, sum, kGroupTokens, bits, G.hybrid);
+      const double m = half_bits_to_float((uint16_t)(gq.word & 0xffffu)), sc = half_bits_to_float((uint16_t)(gq.word >> 16));
+#pragma unroll
+      for (int r = 0; r < kGroupTokens; ++r) {
+        const double e = (double)x[r] - (m + (double)group_code(x[r], gq, bits) * sc);
+        ek += e * e;
+      }
+    }
+  } else {
+    for (int r = w; r < nt; r += 4) {  // InnerQ keys: per token, 64-channel groups
+      float v[4], n4[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        n4[q] = G.knorm ? knorm[(size_t)s * kHeadDim + 4 * lane + q] : 1.0f;
+        v[q] = __fdiv_rn(half_bits_to_float(sK[r][4 * lane + q]), n4[q]);
+      }
+      float mn = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
+      float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+      double sum = ((double)v[0] + (double)v[1]) + ((double)v[2] + (double)v[3]);
+      for (int o = 8; o > 0; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      }
+      const GroupQ gq = group_params(mn, mx, sum, 64, bits, G.hybrid);
+      const double m = half_bits_to_float((uint16_t)(gq.word & 0xffffu)), sc = half_bits_to_float((uint16_t)(gq.word >> 16));
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const double e = ((double)v[q] - (m + (double)group_code(v[q], gq, bits) * sc)) * (double)n4[q];
+        ek += e * e;
+      }
+    }
+  }
+  for (int r = w; r < nt; r += 4) {  // V per token over its channel groups
+    float v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = half_bits_to_float(sV[r][4 * lane + q]);
+    if (G.hadamard) hadamard_vals(v, p.hadamard_c, lane);
+    float mn = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
+    float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+    double sum = ((double)v[0] + (double)v[1]) + ((double)v[2] + (double)v[3]);
+    const int seg = G.gv / 4;
+    for (int o = seg / 2; o > 0; o >>= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    }
+    const GroupQ gq = group_params(mn, mx, sum, G.gv, bits, G.hybrid);
+    const double m = half_bits_to_float((uint16_t)(gq.word & 0xffffu)), sc = half_bits_to_float((uint16_t)(gq.word >> 16));
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const double e = (double)v[q] - (m + (double)group_code(v[q], gq, bits) * sc);
+      ev += e * e;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ek += __shfl_xor_sync(0xffffffffu, ek, o);
+    ev += __shfl_xor_sync(0xffffffffu, ev, o);
+  }
+  if (lane == 0) {
+    red[0][w] = ek;
+    red[1][w] = ev;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    double a = 0.0, b = 0.0;
+    for (int i = 0; i < kThreads / 32; ++i) {
+      a += red[0][i];
+      b += red[1][i];
+    }
+    const int h = layer_head(G, s % G.Hkv);
+    atomicAdd(&sse[2 * h], a);
+    atomicAdd(&sse[2 * h + 1], b);
+  }
+}
+
+// The per-stream key normalisation of the calibration tokens (InnerQ keys).
+__global__ void __launch_bounds__(kHeadDim) calib_norm_kernel(const __grid_constant__ AppendParams p, int n_tokens,
+                                                               float* __restrict__ knorm) {
+  const int s = blockIdx.x, c = threadIdx.x;
+  const uint16_t* k = p.k_new + in_stream(p.geo, s) * n_tokens * kRowHalves + c;
+  float m = 0.0f;
+  for (int t = 0; t < n_tokens; ++t) m = fmaxf(m, fabsf(half_bits_to_float(k[(size_t)t * kRowHalves])));
+  float n = 1.0f;
+  if (m > 0.0f) {
+    int e;
+    frexpf(m, &e);
+    n = ldexpf(1.0f, e);
+    if (ldexpf(1.0f, e - 1) >= m) n = ldexpf(1.0f, e - 1);
+  }
+  knorm[(size_t)s * kHeadDim + c] = n;
+}
+
+// sse[h][j] /= count[j]: the mean squared errors.
+__global__ void mse_finish_kernel(double* sse, int heads, double nk, double nv) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < 2 * heads) sse[i] = (i & 1) ? (nv > 0 ? sse[i] / nv : 0.0) : (nk > 0 ? sse[i] / nk : 0.0);
+}
+
 }  // namespace
+
+cudaError_t launch_distortion(const AppendParams& p, int n_tokens, int bits, float* knorm, double* mse,
+                              cudaStream_t st) {
+  const Geometry& G = p.geo;
+  cudaError_t e = cudaMemsetAsync(mse, 0, sizeof(double) * 2 * G.Hkv_tot, st);
+  if (e != cudaSuccess) return e;
+  if (G.knorm) {
+    calib_norm_kernel<<<G.NS, kHeadDim, 0, st>>>(p, n_tokens, knorm);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  dim3 grid((n_tokens + kGroupTokens - 1) / kGroupTokens, G.NS);
+  distortion_kernel<<<grid, kThreads, 0, st>>>(p, n_tokens, bits, knorm, mse);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // values per layer head: every batch row's keys (whole 32-token blocks per
+  // channel, or every token) and values
+  const double rows = (double)G.B;
+  const double nk = rows * (G.gkc ? (double)n_tokens : (double)(n_tokens / kGroupTokens * kGroupTokens)) * kHeadDim;
+  const double nv = rows * (double)n_tokens * kHeadDim;
+  mse_finish_kernel<<<(2 * G.Hkv_tot + 127) / 128, 128, 0, st>>>(mse, G.Hkv_tot, nk, nv);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_nuq_fit(const uint16_t* x, long long nvec, int k, int hadamard, int max_iters, void* ws,
                            float* lut_out, int* info_out, cudaStream_t st) {

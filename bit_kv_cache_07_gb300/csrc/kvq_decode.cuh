@@ -748,7 +748,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   for (int idx = tid; idx < GQ * kHeadDim; idx += kThreads) {
     const int r = idx / kHeadDim, c = idx % kHeadDim;
     float v = 0.0f;
-    if (r < g) v = half_bits_to_float(p.q[((size_t)b * G.Hq + hk * g + r) * kHeadDim + c]) * p.q_scale;
+    if (r < g) v = half_bits_to_float(p.q[q_row(G, b, hk, r) * kHeadDim + c]) * p.q_scale;
     sm.q[r][c] = v;
   }
   if (tid < 8) {
@@ -922,14 +922,14 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
       for (int k = 0; k < 4; ++k) v[k] = stage[0][r][4 * lane + k];
       if (rotate_this) warp_fwht(v, p.hadamard_c, lane);
       const float Lc = sm.comb_ml[r][1];
-      const size_t o = ((size_t)b * G.Hq + hk * g + r) * kHeadDim + 4 * lane;
+      const size_t o = q_row(G, b, hk, r) * kHeadDim + 4 * lane;
       __half2 h0 = __floats2half2_rn(v[0] / Lc, v[1] / Lc), h1 = __floats2half2_rn(v[2] / Lc, v[3] / Lc);
       uint2 st;
       st.x = *reinterpret_cast<uint32_t*>(&h0);
       st.y = *reinterpret_cast<uint32_t*>(&h1);
       *reinterpret_cast<uint2*>(p.out + o) = st;
       if (p.lse && lane == 0)
-        p.lse[(size_t)b * G.Hq + hk * g + r] = (sm.comb_ml[r][0] + log2f(Lc)) * 0.6931471805599453f;
+        p.lse[q_row(G, b, hk, r)] = (sm.comb_ml[r][0] + log2f(Lc)) * 0.6931471805599453f;
     }
     return;
   }
@@ -975,13 +975,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     float v[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) v[k] = (oq[k] + ow[k]) / Lc;
-    const size_t o = ((size_t)b * G.Hq + hk * g + r) * kHeadDim + 4 * lane;
+    const size_t o = q_row(G, b, hk, r) * kHeadDim + 4 * lane;
     __half2 h0 = __floats2half2_rn(v[0], v[1]), h1 = __floats2half2_rn(v[2], v[3]);
     uint2 st;
     st.x = *reinterpret_cast<uint32_t*>(&h0);
     st.y = *reinterpret_cast<uint32_t*>(&h1);
     *reinterpret_cast<uint2*>(p.out + o) = st;
-    if (p.lse && lane == 0) p.lse[(size_t)b * G.Hq + hk * g + r] = (M + log2f(Lc)) * 0.6931471805599453f;
+    if (p.lse && lane == 0) p.lse[q_row(G, b, hk, r)] = (M + log2f(Lc)) * 0.6931471805599453f;
   }
   if (tid == 0) p.counters[s] = 0u;
 }

@@ -256,13 +256,13 @@ __device__ __forceinline__ void finalize_stream(const DecodeParams& p, int slot,
       }
     }
     L = warp_sum(L);
-    const size_t o = ((size_t)b * G.Hq + hk * g + r) * kHeadDim + 4 * lane;
+    const size_t o = q_row(G, b, hk, r) * kHeadDim + 4 * lane;
     const __half2 h0 = __floats2half2_rn(v[0] / L, v[1] / L), h1 = __floats2half2_rn(v[2] / L, v[3] / L);
     uint2 stv;
     stv.x = h2_as_u32(h0);
     stv.y = h2_as_u32(h1);
     *reinterpret_cast<uint2*>(p.out + o) = stv;
-    if (p.lse && lane == 0) p.lse[(size_t)b * G.Hq + hk * g + r] = (M + log2f(L)) * 0.6931471805599453f;
+    if (p.lse && lane == 0) p.lse[q_row(G, b, hk, r)] = (M + log2f(L)) * 0.6931471805599453f;
   }
   if (lane == 0) p.counters[s] = 0u;
 }
@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT, IQ>::kCtaThreads
       for (int r = 0; r < GT; ++r) {
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (r < g) {
-          const uint16_t* qr = p.q + ((size_t)b * G.Hq + hk * g + r) * kHeadDim;
+          const uint16_t* qr = p.q + q_row(G, b, hk, r) * kHeadDim;
           const float2 a = __half22float2(u32_as_h2(__ldg(reinterpret_cast<const uint32_t*>(qr + c0))));
           const float2 c2 = __half22float2(u32_as_h2(__ldg(reinterpret_cast<const uint32_t*>(qr + c0 + D))));
           v = make_float4(a.x * p.q_scale, c2.x * p.q_scale, a.y * p.q_scale, c2.y * p.q_scale);

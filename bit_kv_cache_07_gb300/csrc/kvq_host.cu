@@ -73,6 +73,21 @@ kvq_status make_geometry(const kvq_config* c, Geometry* g) {
     return KVQ_ERR_INVALID_ARG;
   }
 
+  const int32_t tot = c->kv_heads_total ? c->kv_heads_total : c->n_kv_heads;
+  if (tot < c->n_kv_heads || (int64_t)c->batch * tot > 65535) return KVQ_ERR_INVALID_ARG;
+  if (c->kv_head_index) {
+    if (c->n_kv_heads > 256) return KVQ_ERR_UNSUPPORTED;
+    for (int i = 0; i < c->n_kv_heads; ++i) {
+      const int32_t h = c->kv_head_index[i];
+      if (h < 0 || h >= tot) return KVQ_ERR_INVALID_ARG;
+      for (int j = 0; j < i; ++j)
+        if (c->kv_head_index[j] == h) return KVQ_ERR_INVALID_ARG;
+    }
+  }
+  g->Hkv_tot = tot;
+  g->Hq_tot = tot * (c->n_q_heads / c->n_kv_heads);
+  g->has_map = c->kv_head_index ? 1 : 0;
+  for (int i = 0; i < 256; ++i) g->kvmap[i] = (int16_t)(c->kv_head_index && i < c->n_kv_heads ? c->kv_head_index[i] : i);
   g->B = c->batch;
   g->Hq = c->n_q_heads;
   g->Hkv = c->n_kv_heads;
@@ -234,6 +249,8 @@ Plan make_plan(const Geometry& g, int T, int split_tokens) {
 }  // namespace
 
 namespace kvq {
+
+kvq_status make_geometry_for(const kvq_config* cfg, Geometry* g) { return make_geometry(cfg, g); }
 
 kvq_status decode_setup(const kvq_config* cfg, const void* layer_buf, int32_t tokens, const uint16_t* q,
                         uint16_t* out, float* lse, DecodeParams* pp, bool* persistent, uint64_t* layout_ws) {

@@ -32,7 +32,23 @@ struct Geometry {
   int hybrid;      // InnerQ: symmetric / asymmetric choice per uniform group
   int knorm;       // InnerQ: per-channel key normalisation
   float rope_theta;
+  // per-head pairs: this cache holds Hkv of the layer's Hkv_tot KV heads
+  // (kvmap[h] = the layer head of cache head h when has_map)
+  int Hkv_tot, Hq_tot, has_map;
+  int16_t kvmap[256];
 };
+
+// The layer's KV head of this cache's head h.
+__host__ __device__ inline int layer_head(const Geometry& G, int h) { return G.has_map ? G.kvmap[h] : h; }
+// Row block of cache stream s in the layer's [B][Hkv_tot] inputs (k_new, v_new).
+__host__ __device__ inline size_t in_stream(const Geometry& G, int s) {
+  const int b = s / G.Hkv, h = s - b * G.Hkv;
+  return (size_t)b * G.Hkv_tot + layer_head(G, h);
+}
+// Row of query head r of cache KV head hk, batch row b, in q / out / lse.
+__host__ __device__ inline size_t q_row(const Geometry& G, int b, int hk, int r) {
+  return (size_t)b * G.Hq_tot + (size_t)layer_head(G, hk) * G.g + r;
+}
 
 // Typed pointers into one layer buffer.
 struct LayerPtrs {
@@ -314,6 +330,8 @@ inline cudaError_t occupancy_memo(Kernel kernel, std::atomic<long long>* memo, i
 }
 
 // ------------------------------------------------------------ host hooks
+cudaError_t launch_distortion(const AppendParams& p, int n_tokens, int bits, float* knorm, double* mse,
+                              cudaStream_t st);
 cudaError_t launch_nuq_fit(const uint16_t* x, long long nvec, int k, int hadamard, int max_iters, void* ws,
                            float* lut_out, int* info_out, cudaStream_t st);
 cudaError_t launch_merge_attn(int n_parts, long long rows, const uint16_t* outs, const float* lses,
@@ -330,6 +348,8 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, int* occ = nul
 bool persist_eligible(const Geometry& g);
 cudaError_t plan_persist(DecodeParams& p, uint64_t* ws_need);
 cudaError_t launch_decode_persist(const DecodeParams& p, cudaStream_t st);
+// Geometry of a config (validation included), for the other host units.
+kvq_status make_geometry_for(const kvq_config* cfg, Geometry* g);
 // One decode in three steps (kvq_decode_attn and the no-allocation entry
 // point share them): validate and plan on the host; size the scratch (the
 // persistent plan asks the device for its SM count and occupancy); launch.

@@ -1,0 +1,71 @@
+"""Per-head (K, V) bits (RateQuant summary, "Methodology" 1-4).
+
+A layer whose KV heads use different (K bits, V bits) pairs is held as one
+libkvq cache per distinct pair, each covering its subset of the layer's
+heads through the config's head map (``kv_heads_total``,
+``kv_head_index``): every append reads the layer's whole K/V tensors and
+every decode the whole q and out, so no data is gathered or scattered.  A
+decode step launches one decode kernel per distinct pair.
+
+``allocate_pairs`` chooses the pairs: the distortion of the cache's
+quantizer is measured per head on calibration tokens at 2, 4 and 8 bits
+(``kvq_measure_distortion``, on the GPU), and ``kvq_rate_allocate`` fits
+D(b) = alpha beta^-b per component (K and V of every head: the page's K/V
+separation) and spends the bit budget greedily.  This module only groups,
+calls and keeps the sub-caches.
+"""
+from __future__ import annotations
+
+from . import binding
+
+LADDER = (2, 4, 8)
+
+
+def allocate_pairs(cfg: dict, K, V, avg_bits: float, weights=None):
+    """Per-head (K bits, V bits) for a layer shaped like cfg, from calibration
+    tokens K, V [B, Hkv, n, d] (fp16, GPU), with an average of avg_bits per
+    component (total = round(avg_bits * 2 * Hkv)).  Returns (pairs, report)."""
+    import numpy as np
+    base = dict(cfg)
+    base.update(k_bits=4, v_bits=4)
+    hkv = cfg["n_kv_heads"]
+    D = np.stack([binding.kvq_measure_distortion(base, K, V, b).cpu().numpy() for b in LADDER], -1)  # [Hkv, 2, 3]
+    comps = D.reshape(2 * hkv, 3)  # component 2h = K of head h, 2h + 1 = V of head h
+    total = int(round(avg_bits * 2 * hkv))
+    bits, alpha, beta, wf = binding.kvq_rate_allocate(comps, total, weights)
+    pairs = [(int(bits[2 * h]), int(bits[2 * h + 1])) for h in range(hkv)]
+    return pairs, {"distortion": comps.tolist(), "alpha": alpha.tolist(), "beta": beta.tolist(),
+                   "waterfill_bits": wf.tolist(), "bits": bits.tolist(), "total_bits": total}
+
+
+class MixedLayer:
+    """One layer's cache with per-KV-head (K bits, V bits) pairs: a
+    binding.Layer per distinct pair over its heads."""
+
+    def __init__(self, cfg: dict, pairs, device="cuda"):
+        hkv = cfg["n_kv_heads"]
+        if len(pairs) != hkv:
+            raise ValueError("one (K bits, V bits) pair per KV head")
+        g = cfg["n_q_heads"] // hkv
+        self.cfg = dict(cfg)
+        self.pairs = [tuple(p) for p in pairs]
+        self.parts = []
+        for pair in sorted(set(self.pairs)):
+            heads = [h for h in range(hkv) if self.pairs[h] == pair]
+            sub = dict(cfg, k_bits=pair[0], v_bits=pair[1], n_kv_heads=len(heads), n_q_heads=g * len(heads),
+                       kv_heads_total=hkv, kv_head_index=heads)
+            self.parts.append((pair, heads, binding.Layer(sub, device=device)))
+
+    def append(self, tokens_before: int, k_new, v_new, stream=None):
+        for _, _, layer in self.parts:
+            layer.append(tokens_before, k_new, v_new, stream)
+
+    def decode(self, tokens: int, q, out, lse=None, workspace=None, stream=None):
+        for _, _, layer in self.parts:
+            layer.decode(tokens, q, out, lse, workspace, stream)
+
+    def workspace_bytes(self) -> int:
+        return max(layer.layout.workspace_bytes for _, _, layer in self.parts)
+
+    def layer_bytes(self) -> int:
+        return sum(layer.layout.layer_bytes for _, _, layer in self.parts)

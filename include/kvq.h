@@ -114,6 +114,20 @@ typedef struct kvq_config {
                                  channel); quantized keys are coded as K / n_c
                                  and the decode multiplies q by n_c.  Sinks and
                                  the fp16 window stay raw.                     */
+    /* Per-head (K, V) bits (RateQuant summary, "Methodology" 3-4: per-head
+     * allocation, K and V separate): a layer whose KV heads use different
+     * pairs is held as one cache per distinct pair, each covering a subset
+     * of the layer's heads; n_kv_heads / n_q_heads are the subset's counts. */
+    int32_t kv_heads_total;   /* the layer's KV heads (0: n_kv_heads).  k_new,
+                                 v_new are [B][kv_heads_total][n_new][d]; q,
+                                 out and lse are [B][kv_heads_total *
+                                 (n_q_heads / n_kv_heads)][...]; only this
+                                 cache's heads are read and written            */
+    const int32_t *kv_head_index; /* host array of n_kv_heads distinct layer
+                                 KV-head indices (< kv_heads_total, at most 256
+                                 entries) that this cache holds, in its stream
+                                 order; NULL: heads 0 .. n_kv_heads - 1.  Read
+                                 during each call only.                        */
 } kvq_config;
 
 /* Window rule.  For a sequence holding T tokens:
@@ -312,6 +326,47 @@ kvq_status kvq_decode_attn_noalloc(const kvq_config *cfg, const void *layer_buf,
 kvq_status kvq_fit_nuq_lut(const uint16_t *x, int64_t n_vectors, int32_t head_dim, int32_t outliers,
                            int32_t hadamard, int32_t max_iters, void *workspace, uint64_t ws_bytes,
                            float *lut_out, int32_t *info_out, kvq_stream_t stream);
+
+/* Per-head (K, V) bit allocation (RateQuant summary, "Methodology" 1-4).
+ *
+ * kvq_measure_distortion -- the mean squared error of this cache's uniform
+ * quantizers at `bits` (2, 4 or 8, for K and V alike) on calibration tokens,
+ * per KV head of the layer, K and V separately (the "distortion
+ * calibration" of RateQuant, here of this quantizer):
+ *   k, v      device fp16 [B][kv_heads_total][n_tokens][d], 16-byte aligned
+ *   K         per channel over the whole 32-token blocks of the n_tokens (or,
+ *             with k_group_channels 64, per token over 64-channel groups of
+ *             the keys divided by the per-channel normalisation of these
+ *             tokens when k_channel_norm is set); V per token over
+ *             v_group_channels groups, rotated first when v_hadamard; the
+ *             config's hybrid_groups; x^ = min + code * scale from the stored
+ *             fp16 pair; errors in fp64 (the normalised keys' errors scaled
+ *             back by n_c)
+ *   workspace device, >= B * n_kv_heads * d * 4 bytes when k_channel_norm
+ *             (else may be NULL)
+ *   mse_out   device f64 [kv_heads_total][2]: {D_K, D_V} averaged over the
+ *             batch rows and tokens
+ * cfg's k_bits / v_bits are ignored (bits applies); non-uniform and fp16
+ * configs are not supported.  Errors: KVQ_ERR_INVALID_ARG,
+ * KVQ_ERR_UNSUPPORTED, KVQ_ERR_WORKSPACE, KVQ_ERR_CUDA. */
+kvq_status kvq_measure_distortion(const kvq_config *cfg, const uint16_t *k, const uint16_t *v, int32_t n_tokens,
+                                  int32_t bits, void *workspace, uint64_t ws_bytes, double *mse_out,
+                                  kvq_stream_t stream);
+
+/* kvq_rate_allocate -- host only.  For n components (typically 2 per KV
+ * head: K and V) with measured distortions distortion[i][0..2] at 2, 4 and
+ * 8 bits (all > 0, falling), fits D_i(b) = alpha_i * beta_i^-b by least
+ * squares in ln D (beta_i must exceed 1), and allocates total_bits bits
+ * (>= 2 n) by the greedy marginal-gain rule on the ladder 2 -> 4 -> 8:
+ * every component starts at 2 bits, and while a step fits the remaining
+ * budget the one with the largest w_i (D_i(b) - D_i(b')) / (b' - b) is taken
+ * (ties to the lower index).  weights (sensitivities w_i) may be NULL (all
+ * 1).  bits_out[n] gets 2, 4 or 8; alpha_out, beta_out and waterfill_out
+ * (the continuous reverse water-filling optimum b_i with sum b_i =
+ * total_bits, from w_i alpha_i ln(beta_i) beta_i^-b_i equal for all i) may
+ * be NULL.  Errors: KVQ_ERR_INVALID_ARG. */
+kvq_status kvq_rate_allocate(int32_t n, const double *distortion, const double *weights, int32_t total_bits,
+                             int32_t *bits_out, double *alpha_out, double *beta_out, double *waterfill_out);
 
 /* Context-parallel decode (KVQuant summary, abstract and main results: a
  * 10M-token context on an 8-GPU system).  The context of every sequence is

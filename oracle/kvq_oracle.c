@@ -864,3 +864,160 @@ long orc_nuq_fit_positions(const uint16_t *x, long nvec, int n, int k, int hadam
     }
     return np;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Per-head bit allocation (RateQuant): distortion-rate fit and allocation.  */
+/* ------------------------------------------------------------------------ */
+
+/* Mean squared error of the cache's uniform quantizers on one stream's T
+ * calibration tokens (fp16 K, V [T][d]) at `bits`: K per channel over the
+ * floor(T / gk) whole groups of gk tokens (or, with the InnerQ layout, per
+ * token over gkc-channel groups of the normalised keys), V per token over
+ * gv-channel groups (rotated first when v_hadamard; the error is measured
+ * where the quantizer works).  x^ = min_h + code * scale_h in fp64; hybrid
+ * groups as configured.  dk, dv: sum of squared errors / number of values. */
+void orc_quant_distortion(const orc_cfg *c, int T, const uint16_t *K, const uint16_t *V, int bits,
+                          double *dk, double *dv)
+{
+    int d = c->d;
+    uint8_t codes[1024];
+    float xf[1024];
+    uint16_t rot[1024];
+    double sk = 0.0, sv = 0.0;
+    long nk = 0, nv = 0;
+    if (c->gkc > 0) {
+        float kn[1024];
+        if (c->k_norm) orc_key_norm(K, T, d, kn);
+        for (int t = 0; t < T; t++) {
+            for (int ch = 0; ch < d; ch++)
+                xf[ch] = orc_half_to_float(K[(size_t)t * d + ch]) / (c->k_norm ? kn[ch] : 1.0f);
+            for (int j = 0; j < d / c->gkc; j++) {
+                uint16_t mh, sh;
+                orc_quantize_group(xf + j * c->gkc, c->gkc, 1, bits, c->hybrid, codes, 1, &mh, &sh);
+                for (int i = 0; i < c->gkc; i++) {
+                    double xh = (double)orc_half_to_float(mh) + (double)codes[i] * (double)orc_half_to_float(sh);
+                    double e = ((double)xf[j * c->gkc + i] - xh) * (c->k_norm ? (double)kn[j * c->gkc + i] : 1.0);
+                    sk += e * e;
+                    nk++;
+                }
+            }
+        }
+    } else {
+        int ng = T / c->gk;
+        float *gx = malloc(sizeof(float) * (size_t)c->gk);
+        for (int g = 0; g < ng; g++)
+            for (int ch = 0; ch < d; ch++) {
+                uint16_t mh, sh;
+                for (int i = 0; i < c->gk; i++)
+                    gx[i] = orc_half_to_float(K[(size_t)(g * c->gk + i) * d + ch]);
+                orc_quantize_group(gx, c->gk, 1, bits, c->hybrid, codes, 1, &mh, &sh);
+                for (int i = 0; i < c->gk; i++) {
+                    double e = (double)gx[i] -
+                               ((double)orc_half_to_float(mh) + (double)codes[i] * (double)orc_half_to_float(sh));
+                    sk += e * e;
+                    nk++;
+                }
+            }
+        free(gx);
+    }
+    for (int t = 0; t < T; t++) {
+        const uint16_t *x = V + (size_t)t * d;
+        if (c->v_hadamard) {
+            orc_hadamard_rotate(x, d, rot);
+            x = rot;
+        }
+        for (int ch = 0; ch < d; ch++) xf[ch] = orc_half_to_float(x[ch]);
+        for (int j = 0; j < d / c->gv; j++) {
+            uint16_t mh, sh;
+            orc_quantize_group(xf + j * c->gv, c->gv, 1, bits, c->hybrid, codes, 1, &mh, &sh);
+            for (int i = 0; i < c->gv; i++) {
+                double e = (double)xf[j * c->gv + i] -
+                           ((double)orc_half_to_float(mh) + (double)codes[i] * (double)orc_half_to_float(sh));
+                sv += e * e;
+                nv++;
+            }
+        }
+    }
+    *dk = nk ? sk / (double)nk : 0.0;
+    *dv = nv ? sv / (double)nv : 0.0;
+}
+
+/* Fit D(b) = alpha * beta^-b to n points (b_i, D_i > 0): least squares of
+ * ln D = ln alpha - b ln beta (RateQuant, "Methodology" 1 and the
+ * distortion calibration of 3). */
+void orc_fit_rd(int n, const double *b, const double *D, double *alpha, double *beta)
+{
+    double sb = 0, sy = 0, sbb = 0, sby = 0;
+    for (int i = 0; i < n; i++) {
+        double y = log(D[i]);
+        sb += b[i];
+        sy += y;
+        sbb += b[i] * b[i];
+        sby += b[i] * y;
+    }
+    double slope = (n * sby - sb * sy) / (n * sbb - sb * sb);  /* = -ln beta */
+    double icpt = (sy - slope * sb) / n;                        /* = ln alpha */
+    *alpha = exp(icpt);
+    *beta = exp(-slope);
+}
+
+/* Reverse water-filling (RateQuant "Methodology" 1, per-component beta):
+ * minimise sum_i w_i alpha_i beta_i^-b_i subject to sum_i b_i = B over real
+ * b_i.  Stationarity: w_i alpha_i ln(beta_i) beta_i^-b_i = lambda, i.e.
+ * b_i = (ln(w_i alpha_i ln beta_i) - ln lambda) / ln beta_i; ln lambda is
+ * found by bisection so that the b_i sum to B.  (With a common beta this is
+ * b_i = B/n + (ln w_i - ln wbar) / ln beta, wbar the geometric mean of
+ * w_i alpha_i.)  Components need beta_i > 1. */
+void orc_rate_waterfill(int n, const double *alpha, const double *beta, const double *w, double B, double *b)
+{
+    double lo = -1e3, hi = 1e3;
+    for (int it = 0; it < 400; it++) {
+        double mid = 0.5 * (lo + hi), sum = 0;
+        for (int i = 0; i < n; i++) {
+            double wi = w ? w[i] : 1.0;
+            sum += (log(wi * alpha[i] * log(beta[i])) - mid) / log(beta[i]);
+        }
+        if (sum > B) lo = mid; else hi = mid;
+    }
+    double ll = 0.5 * (lo + hi);
+    for (int i = 0; i < n; i++) {
+        double wi = w ? w[i] : 1.0;
+        b[i] = (log(wi * alpha[i] * log(beta[i])) - ll) / log(beta[i]);
+    }
+}
+
+/* Greedy marginal-gain allocation (RateQuant "Methodology" 3, Alg. 1) on the
+ * bit widths the cache supports, the ladder 2 -> 4 -> 8: every component
+ * starts at 2 bits; while some next step fits the remaining budget
+ * (total - sum of bits), take the step with the largest weighted distortion
+ * reduction per added bit, w_i (D_i(b) - D_i(b')) / (b' - b) with the fitted
+ * D_i; ties go to the lower component index.  bits_out[i] in {2, 4, 8}.
+ * Returns the bits used (-1 if the budget is below 2 bits per component). */
+int orc_rate_greedy(int n, const double *alpha, const double *beta, const double *w, int total, int *bits_out)
+{
+    int used = 2 * n;
+    if (total < used) return -1;
+    for (int i = 0; i < n; i++) bits_out[i] = 2;
+    for (;;) {
+        int best = -1;
+        double bg = 0.0;
+        for (int i = 0; i < n; i++) {
+            int b0 = bits_out[i];
+            if (b0 >= 8) continue;
+            int b1 = b0 == 2 ? 4 : 8;
+            if (used + (b1 - b0) > total) continue;
+            double wi = w ? w[i] : 1.0;
+            double gain = wi * (alpha[i] * pow(beta[i], -b0) - alpha[i] * pow(beta[i], -b1)) / (double)(b1 - b0);
+            if (best < 0 || gain > bg) {
+                best = i;
+                bg = gain;
+            }
+        }
+        if (best < 0) break;
+        int b0 = bits_out[best];
+        int b1 = b0 == 2 ? 4 : 8;
+        used += b1 - b0;
+        bits_out[best] = b1;
+    }
+    return used;
+}

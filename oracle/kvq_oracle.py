@@ -87,6 +87,11 @@ def lib():
         L.orc_nuq_fit_lut.restype = C.c_int
         L.orc_nuq_fit_positions.argtypes = [u16, C.c_long, C.c_int, C.c_int, C.c_int, i32, C.c_long]
         L.orc_nuq_fit_positions.restype = C.c_long
+        L.orc_quant_distortion.argtypes = [C.POINTER(_Cfg), C.c_int, u16, u16, C.c_int, f64, f64]
+        L.orc_fit_rd.argtypes = [C.c_int, f64, f64, f64, f64]
+        L.orc_rate_waterfill.argtypes = [C.c_int, f64, f64, f64, C.c_double, f64]
+        L.orc_rate_greedy.argtypes = [C.c_int, f64, f64, f64, C.c_int, i32]
+        L.orc_rate_greedy.restype = C.c_int
         L.orc_merge_parts.argtypes = [C.c_int, C.c_int, C.c_int, f64, f64, f64, f64]
         L.orc_decode_stream.argtypes = [C.POINTER(_Cfg), C.c_int, C.c_int, u16,
                                         u8, u16, u8, u16, u16, u16, u16, u16,
@@ -377,3 +382,43 @@ def key_norm(K) -> np.ndarray:
     out = np.zeros(d, np.float32)
     lib().orc_key_norm(_P(K, C.c_uint16), T, d, _P(out, C.c_float))
     return out
+
+
+def quant_distortion(cfg: dict, K, V, bits: int):
+    """(D_K, D_V): mean squared error of the cache's quantizers on one
+    stream's calibration tokens K, V [T, d] at `bits`."""
+    K, V = _u16(K), _u16(V)
+    dk, dv = C.c_double(), C.c_double()
+    c = _cfg(cfg)
+    lib().orc_quant_distortion(C.byref(c), K.shape[0], _P(K, C.c_uint16), _P(V, C.c_uint16), bits,
+                               C.byref(dk), C.byref(dv))
+    return dk.value, dv.value
+
+
+def _f64(a):
+    return None if a is None else np.ascontiguousarray(a, np.float64)
+
+
+def fit_rd(bits, D):
+    """(alpha, beta) of D(b) = alpha beta^-b, least squares in ln D."""
+    b, D = _f64(bits), _f64(D)
+    a, be = C.c_double(), C.c_double()
+    lib().orc_fit_rd(b.size, _P(b, C.c_double), _P(D, C.c_double), C.byref(a), C.byref(be))
+    return a.value, be.value
+
+
+def rate_waterfill(alpha, beta, B: float, w=None):
+    alpha, beta, w = _f64(alpha), _f64(beta), _f64(w)
+    out = np.zeros(alpha.size)
+    lib().orc_rate_waterfill(alpha.size, _P(alpha, C.c_double), _P(beta, C.c_double),
+                             _P(w, C.c_double) if w is not None else None, float(B), _P(out, C.c_double))
+    return out
+
+
+def rate_greedy(alpha, beta, total: int, w=None):
+    """Greedy bits in {2, 4, 8} per component under a total budget; (bits, used)."""
+    alpha, beta, w = _f64(alpha), _f64(beta), _f64(w)
+    out = np.zeros(alpha.size, np.int32)
+    used = lib().orc_rate_greedy(alpha.size, _P(alpha, C.c_double), _P(beta, C.c_double),
+                                 _P(w, C.c_double) if w is not None else None, int(total), _P(out, C.c_int32))
+    return out, used

@@ -70,7 +70,7 @@ def gpu_store(layer, s: int, T: int, counts) -> dict:
             host["ks"] = reg("k_scales", np.uint16).reshape(NS, gcap, d, 2)[s, :Nq // 32]
         host["vs"] = reg("v_scales", np.uint16).reshape(NS, qcap, nvg, 2)[s, :Nq]
         if cfg.k_channel_norm:
-            host["kn"] = reg("k_norm", np.float32).reshape(NS, d)[s]
+            host["kn"] = reg("k_norm", np.float32).reshape(NS, d)[s, :]
     host["vc"] = reg("v_codes", np.uint8).reshape(NS, qcap, vrow)[s, :Nq]
     Sc = cfg.n_sink
     host["ksink"] = reg("k_sink", np.uint16).reshape(NS, Sc, d)[s, :S] if Sc else np.zeros((0, d), np.uint16)
