@@ -179,16 +179,20 @@ def source_hash() -> str:
 
 class Model:
     """All layers of one workload: caches filled to T-1 tokens, plus the
-    per-layer inputs of one decode step."""
+    per-layer inputs of one decode step.  A layer is one or more decode
+    units: one cache per layer, or with per-head (K, V) bits one cache per
+    distinct pair over its KV heads (their head maps address the layer's
+    whole K/V, q and out)."""
 
     def __init__(self, name: str, device, fp16: bool, layers: int = 0, tokens: int = 0):
         import torch
-        from bit_kv_cache_07_gb300 import binding, synth, workloads
+        from bit_kv_cache_07_gb300 import binding, mixed, synth, workloads
         w = workloads.WORKLOADS[name]
         self.name, self.T = name, (tokens if tokens > 0 else w["tokens"])
         self.L = layers if layers > 0 else w["layers"]
-        self.cfgs, self.layers = [], []
+        self.cfgs, self.units, self.unit_layer = [], [], []
         self.q, self.k_new, self.v_new, self.out = [], [], [], []
+        self.head_pairs = []
         for l in range(self.L):
             cfg = workloads.layer_config(name, l, tokens=self.T)
             if cfg["k_bits"] == 3:
@@ -196,44 +200,53 @@ class Model:
                 cfg["k_lut"], cfg["v_lut"] = calibrate.nuq_tables(name, l, device=device)
             if fp16:
                 cfg = workloads.fp16_baseline_config(cfg)
-            layer = binding.Layer(cfg, device=device)
             K, V = synth.layer_kv(name, l, tokens=self.T - 1, device=device)
-            layer.append(0, K, V)
+            if w["pairs"] == "rateq" and not fp16:
+                Kc, Vc = synth.layer_kv(name, l, tokens=w["rateq_calib_tokens"], batch=1, device=device)
+                pairs, _ = mixed.allocate_pairs(cfg, Kc, Vc, w["rateq_avg_bits"])
+                del Kc, Vc
+                ml = mixed.MixedLayer(cfg, pairs, device=device)
+                ml.append(0, K, V)
+                self.head_pairs.append(pairs)
+                parts = [sub for _, _, sub in ml.parts]
+            else:
+                layer = binding.Layer(cfg, device=device)
+                layer.append(0, K, V)
+                parts = [layer]
             del K, V
-            self.cfgs.append(cfg)
-            self.layers.append(layer)
+            for sub in parts:
+                self.cfgs.append(sub.cfg_dict)
+                self.units.append(sub)
+                self.unit_layer.append(l)
             self.q.append(synth.query(name, l, device=device))
             k, v = synth.new_token_kv(name, l, 0, device=device)
             self.k_new.append(k)
             self.v_new.append(v)
             self.out.append(torch.empty_like(self.q[-1]))
-        ws_bytes = max(binding.kvq_layout_query(c).workspace_bytes for c in self.cfgs)
+        ws_bytes = max(u.layout.workspace_bytes for u in self.units)
         self.ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=device)
         torch.cuda.synchronize()
         self.binding = binding
 
-    def step(self, stream, ev=None):
+    def step(self, stream):
         B = self.binding
-        for l in range(self.L):
-            c = self.layers[l]
-            B.kvq_append(c.cfg, c.buf, self.T - 1, self.k_new[l], self.v_new[l], 1, stream)
-            if ev is not None:
-                ev[l][0].record(stream)
-            B.kvq_decode_attn(c.cfg, c.buf, self.T, self.q[l], self.out[l], None, self.ws, None, stream)
-            if ev is not None:
-                ev[l][1].record(stream)
+        for i, u in enumerate(self.units):
+            l = self.unit_layer[i]
+            B.kvq_append(u.cfg, u.buf, self.T - 1, self.k_new[l], self.v_new[l], 1, stream)
+        for i in range(len(self.units)):
+            self.decode(i, stream)
 
-    def decode(self, l: int, stream):
-        c = self.layers[l]
-        self.binding.kvq_decode_attn(c.cfg, c.buf, self.T, self.q[l], self.out[l], None, self.ws, None, stream)
+    def decode(self, i: int, stream):
+        u, l = self.units[i], self.unit_layer[i]
+        self.binding.kvq_decode_attn(u.cfg, u.buf, self.T, self.q[l], self.out[l], None, self.ws, None, stream)
 
     def decode_bytes(self):
         return sum(algorithmic_bytes(c, self.T) for c in self.cfgs)
 
     def launches_per_step(self):
-        """Kernel launches of one step: per layer the 1-token append's window
-        copy (plus a quantize launch when the append flushes a group) and the
-        decode."""
+        """Kernel launches of one step: per decode unit the 1-token append's
+        window copy (plus a quantize launch when the append flushes a group)
+        and the decode."""
         n = 0
         for c in self.cfgs:
             n += 1  # fp16 window copy of the appended token
@@ -246,27 +259,22 @@ class Model:
         return [self.binding.decode_kernel_name(c, self.T) for c in self.cfgs]
 
 
-def time_steps(model, stream, steps: int, warmup: int, per_kernel=True):
+def time_steps(model, stream, steps: int, warmup: int):
+    """Eager steps (host launches every call) timed with CUDA events: ms total."""
     import torch
     for _ in range(warmup):
         model.step(stream)
     torch.cuda.synchronize()
-    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-            for _ in range(model.L)] for _ in range(steps)] if per_kernel else None
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     t0.record(stream)
     for i in range(steps):
-        model.step(stream, evs[i] if per_kernel else None)
+        model.step(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    total_ms = t0.elapsed_time(t1)
-    kern = None
-    if per_kernel:
-        kern = [evs[i][l][0].elapsed_time(evs[i][l][1]) for i in range(steps) for l in range(model.L)]
-    return total_ms, kern
+    return t0.elapsed_time(t1)
 
 
 def time_graph(model, stream, steps: int, warmup: int, min_seconds: float = 1.5, max_rounds: int = 200):
@@ -316,17 +324,17 @@ def time_graph(model, stream, steps: int, warmup: int, min_seconds: float = 1.5,
 
 
 def time_decode_only(model, stream, steps: int, warmup: int):
-    """Each layer's decode kernel time, measured inside replayed CUDA graphs:
-    for every (K, V) pair, the decode launches of that pair's layers are
+    """Each decode unit's kernel time, measured inside replayed CUDA graphs:
+    for every (K, V) pair, the decode launches of that pair's units are
     captured back to back in one graph (no appends, nothing between them), the
     graph is replayed `steps` times between two CUDA events on the launching
-    stream, and the time is divided by the launches.  Every layer gets the
-    mean of its pair.  Returns (per-layer ms, None) or (None, why)."""
+    stream, and the time is divided by the launches.  Every unit gets the
+    mean of its pair.  Returns (per-unit ms, None) or (None, why)."""
     import torch
     groups = {}
     for l, c in enumerate(model.cfgs):
         groups.setdefault(_pair_name(c), []).append(l)
-    per_layer = [0.0] * model.L
+    per_layer = [0.0] * len(model.cfgs)
     for pair, layers in groups.items():
         try:
             g = torch.cuda.CUDAGraph()
@@ -735,15 +743,14 @@ def main():
     model = Model(args.workload, dev, fp16=False, layers=args.layers, tokens=args.tokens)
     clocks = ClockSampler(local)
     clocks.start()
-    total_ms, _ = time_steps(model, stream, args.steps, args.warmup, per_kernel=False)
+    total_ms = time_steps(model, stream, args.steps, args.warmup)
     g_ms, rounds, g_err = time_graph(model, stream, args.steps, args.warmup, args.min_timed_seconds)
     layer_ms, t_err = time_decode_only(model, stream, args.steps, args.warmup)
     clk = clocks.stop()
     eager_ms = max_over_ranks(total_ms / args.steps)
     ms_step = max_over_ranks(g_ms) if g_ms is not None else eager_ms
-    if layer_ms is None:  # fall back to eager per-kernel events
-        _, kern = time_steps(model, stream, args.steps, 1, per_kernel=True)
-        layer_ms = [statistics.mean(kern[l::model.L]) for l in range(model.L)]
+    if layer_ms is None:
+        raise RuntimeError(t_err)
     dec_bytes = model.decode_bytes()
     peak, peak_kind = measured_peaks()
     roof, pairs = decode_roofline(model, layer_ms, peak, peak_kind, args.workload)
@@ -751,6 +758,7 @@ def main():
     e2e_ms = max_over_ranks(e2e_ms)
     launches = model.launches_per_step() * args.steps
     model_layers, model_T = model.L, model.T
+    head_pairs = model.head_pairs or None
     del model
     torch.cuda.empty_cache()
     append = time_append(args.workload, dev, model_T, stream)
@@ -760,7 +768,7 @@ def main():
         fmodel = Model(args.workload, dev, fp16=True, layers=args.layers, tokens=args.tokens)
         fg_ms, _, _ = time_graph(fmodel, stream, args.steps, args.warmup, 0.0)
         if fg_ms is None:
-            f_total, _ = time_steps(fmodel, stream, args.steps, args.warmup, per_kernel=False)
+            f_total = time_steps(fmodel, stream, args.steps, args.warmup)
             fg_ms = f_total / args.steps
         f_ms = max_over_ranks(fg_ms)
         f_layer_ms, _ = time_decode_only(fmodel, stream, args.steps, args.warmup)
@@ -769,9 +777,10 @@ def main():
                 "bytes_per_step": f_bytes, "kernel": fmodel.kernel_names()[0]}
         if f_layer_ms is not None:
             f_dec = statistics.mean(f_layer_ms)
+            nu = len(fmodel.cfgs)
             fp16.update(decode_kernel_us=f_dec * 1e3,
-                        decode_kernel_gbs=(f_bytes / fmodel.L) / (f_dec * 1e-3) / 1e9,
-                        decode_frac=(f_bytes / fmodel.L) / (f_dec * 1e-3) / 1e9 / peak)
+                        decode_kernel_gbs=(f_bytes / nu) / (f_dec * 1e-3) / 1e9,
+                        decode_frac=(f_bytes / nu) / (f_dec * 1e-3) / 1e9 / peak)
         del fmodel
         torch.cuda.empty_cache()
 
@@ -800,6 +809,7 @@ def main():
         "cache_bytes_per_step": dec_bytes,
         "roofline": roof,
         "decode_by_pair": pairs,
+        "head_pairs": head_pairs,
         "append": append,
         "fp16_baseline": fp16,
         "speedup_vs_fp16": (fp16["us_per_step"] / value) if fp16 else None,

@@ -417,7 +417,7 @@ __device__ __forceinline__ void build_bq_iq(const float (*qw)[kHeadDim], const f
       for (int x = 0; x < 2; ++x) {
         const int c = iq_channel(tq, k_offset_of<KB>(ri >> 1, 2 * (ri & 1) + x));
         float v = 0.0f;
-        if (h < g) v = qw[h][qb_perm_pos<KB>(c)] * (knorm ? __ldg(knorm + c) : 1.0f) * (kE / kq_mult<KB>(c & 3));
+        if (h < g) v = qw[h][qb_perm_pos<KB>(c)] * (knorm ? __ldg(knorm + c) : 1.0f) * kq_mult<KB>(c & 3);
         const __half hi = __float2half_rn(v);
         hv[x] = __half_as_ushort(lo ? __float2half_rn(v - __half2float(hi)) : hi);
       }
@@ -436,7 +436,7 @@ __device__ __forceinline__ void build_bq_iq(const float (*qw)[kHeadDim], const f
     for (int k = 0; k < 4; ++k) {
       const int c = 4 * lane + k;
       const float qn = qw[h][qb_perm_pos<KB>(c)] * (knorm ? __ldg(knorm + c) : 1.0f);
-      const float v = qn * (kE / kq_mult<KB>(c & 3));
+      const float v = qn * kq_mult<KB>(c & 3);
       const __half hi = __float2half_rn(v);
       const float lo = __half2float(__float2half_rn(v - __half2float(hi)));
       oh += (__half2float(hi) + lo) * (1024.0f / kE);

@@ -27,7 +27,7 @@ def allocate_pairs(cfg: dict, K, V, avg_bits: float, weights=None):
     component (total = round(avg_bits * 2 * Hkv)).  Returns (pairs, report)."""
     import numpy as np
     base = dict(cfg)
-    base.update(k_bits=4, v_bits=4)
+    base.update(k_bits=4, v_bits=4, batch=K.shape[0])
     hkv = cfg["n_kv_heads"]
     D = np.stack([binding.kvq_measure_distortion(base, K, V, b).cpu().numpy() for b in LADDER], -1)  # [Hkv, 2, 3]
     comps = D.reshape(2 * hkv, 3)  # component 2h = K of head h, 2h + 1 = V of head h

@@ -50,6 +50,13 @@ WORKLOADS = {
         _BASE, layers=32, batch=16, n_q_heads=32, n_kv_heads=8, tokens=32768,
         pairs="KV4", n_sink=4, n_recent=32, k_group_channels=64, hybrid_groups=1, k_channel_norm=1,
         k_dist="normal", k_outlier_channels="random3", k_outlier_scale=8.0, v_dist="laplace"),
+    # RateQuant: per-head (K, V) bits allocated per layer from the measured
+    # distortion of the cache's quantizer on the layer's first 2048 tokens, an
+    # average of 4 bits per K or V component, at the Llama-3-8B shape
+    "llama3_8b_rateq_t32k": dict(
+        _BASE, layers=32, batch=16, n_q_heads=32, n_kv_heads=8, tokens=32768,
+        pairs="rateq", rateq_avg_bits=4.0, rateq_calib_tokens=2048, n_sink=4, n_recent=128,
+        k_dist="normal", k_outlier_channels="random3", k_outlier_scale=8.0, v_dist="laplace"),
     "llama7b_nuq3_t1m": dict(
         _BASE, layers=1, batch=1, n_q_heads=32, n_kv_heads=32, tokens=1048576,
         pairs="NUQ3", k_pre_rope=1, outliers_per_vector=2, lut="fitted", lut_calib_tokens=2048,
@@ -58,7 +65,8 @@ WORKLOADS = {
 
 # order of the workloads as listed with the method's benchmark
 WORKLOAD_ORDER = ["toy_k4v2_t1k", "llama2_7b_kv4_t4k", "llama3_8b_mixed_t32k",
-                  "qwen_gqa_hadamard_t8k", "llama7b_nuq3_t1m", "llama3_8b_innerq_kv4_t32k"]
+                  "qwen_gqa_hadamard_t8k", "llama7b_nuq3_t1m", "llama3_8b_innerq_kv4_t32k",
+                  "llama3_8b_rateq_t32k"]
 
 
 def layer_pairs(name: str) -> list[str]:
@@ -66,6 +74,8 @@ def layer_pairs(name: str) -> list[str]:
     pair index from numpy default_rng(0).integers(0, 5, layers) over
     PAIR_ORDER and forces layers 0, 1 and the last to KV8."""
     w = WORKLOADS[name]
+    if w["pairs"] == "rateq":  # per-head pairs are allocated at run time (mixed.py); KV4 is the layer's base
+        return ["KV4"] * w["layers"]
     if w["pairs"] != "seeded":
         return [w["pairs"]] * w["layers"]
     idx = np.random.default_rng(0).integers(0, 5, w["layers"])
