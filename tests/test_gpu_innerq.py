@@ -35,8 +35,10 @@ def cfg_iq(kb, vb, Bt, Hq, Hkv, T, S=4, R=32, hybrid=1, norm=1, had=0, gkc=64):
 def run_case(B, cfg, T, seed, chunks=None, v_dist="laplace", centred_k=False):
     from bit_kv_cache_07_gb300 import synth
     K, V = synth.random_kv(cfg["batch"], cfg["n_kv_heads"], T, seed=seed, device="cuda", v_dist=v_dist)
-    if centred_k:  # keys whose groups are mostly centred: the symmetric grid is taken often
-        K = (K.float() - K.float().mean(-1, keepdim=True)).half()
+    if centred_k:  # every 64-channel group's mean exactly 0 (channel c + 32 = -channel c): symmetric groups
+        K = K.clone()
+        K[..., 32:64] = -K[..., 0:32]
+        K[..., 96:128] = -K[..., 64:96]
     layer = B.Layer(cfg)
     chunks = chunks or [T]
     t = 0
@@ -104,7 +106,7 @@ def test_innerq_centred_keys_take_symmetric_groups(B, bits):
             if kc[i, 64 * j:64 * j + 64].min() >= 1 and \
                     O.half_to_float(int(ks[i, j, 0])) == -(1 << (bits - 1)) * O.half_to_float(int(ks[i, j, 1])):
                 sym += 1
-    assert sym > kc.shape[0] // 2
+    assert sym == 2 * kc.shape[0]  # every group of every quantized token
 
 
 def test_innerq_chunked_append_normalisation_from_first_chunk(B):
