@@ -45,24 +45,34 @@ __device__ __forceinline__ uint32_t uniform_code(float x, float mn, float scale,
   return (uint32_t)r;
 }
 
-// Parameters of one uniform group from its min, max and exact fp64 sum
+// Parameters of one uniform group from its min, max and exact sum
 // (InnerQ, Methodology 2: the group picks a symmetric or an asymmetric grid
 // from its own statistics).  Symmetric when `hybrid`, mx > mn and the mean
 // lies within half an asymmetric step of zero, |mean| 2^(b+1) <= mx - mn:
 // scale = max(|mn|, |mx|) / (2^(b-1) - 1), stored min = -2^(b-1) fp16(scale)
 // (falls back to asymmetric if that overflows fp16).  Asymmetric otherwise:
-// scale = (mx - mn) / (2^b - 1), stored min = fp16(mn).  The inputs are fp16
-// values (or fp16 values divided by powers of two up to 2^16), so the fp64
-// sum of at most 128 of them is exact in any order.
+// scale = (mx - mn) / (2^b - 1), stored min = fp16(mn).
+// The inputs are fp16 values (units of 2^-24, |x| < 2^16), or fp16 values
+// divided by the key normalisation (|x| <= 1, units of 2^-40), so every one
+// is an integer in units 2^-sh (sh = 24 or 40) and the sum is computed
+// exactly in 64-bit integers (fixed()), in any order; the comparison
+// |S| 2^(b+1) <= n (MX - MN), all in those units, is then exact too (the
+// same real-number test the oracle makes with its exact fp64 mean).  At most
+// 128 values: |S| <= 2^47 and the products stay below 2^57.
+__device__ __forceinline__ long long fixed(float x, int sh) {
+  return __float2ll_rz(__fmul_rn(x, sh == 40 ? 1099511627776.0f : 16777216.0f));  // exact: a power-of-two scaling
+}
 struct GroupQ {
   float mn, scale, rs;  // asymmetric origin, fp32 scale and its reciprocal
   int sym;              // 1: symmetric codes
   uint32_t word;        // stored {min, scale} fp16 pair
 };
-__device__ __forceinline__ GroupQ group_params(float mn, float mx, double sum, int n, int bits, int hybrid) {
+__device__ __forceinline__ GroupQ group_params(float mn, float mx, long long sum, int sh, int n, int bits,
+                                               int hybrid) {
   GroupQ g;
   g.sym = 0;
-  if (hybrid && mx > mn && fabs(sum / (double)n) * (double)(1 << (bits + 1)) <= (double)mx - (double)mn) {
+  long long S = sum < 0 ? -sum : sum;
+  if (hybrid && mx > mn && (S << (bits + 1)) <= (long long)n * (fixed(mx, sh) - fixed(mn, sh))) {
     const float a = fmaxf(fabsf(mn), fabsf(mx));
     const float scale = __fdiv_rn(a, (float)((1 << (bits - 1)) - 1));
     const uint16_t sh = float_to_half_bits(scale);
@@ -364,13 +374,15 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
       }
       float mn = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
       float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
-      double sum = ((double)v[0] + (double)v[1]) + ((double)v[2] + (double)v[3]);
+      const int sh = G.knorm ? 40 : 24;
+      long long sum = 0;
+      if (G.hybrid) sum = (fixed(v[0], sh) + fixed(v[1], sh)) + (fixed(v[2], sh) + fixed(v[3], sh));
       for (int o = 8; o > 0; o >>= 1) {
         mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (G.hybrid) sum += __shfl_xor_sync(0xffffffffu, sum, o);
       }
-      const GroupQ gq = group_params(mn, mx, sum, 64, G.kb, G.hybrid);
+      const GroupQ gq = group_params(mn, mx, sum, sh, 64, G.kb, G.hybrid);
 #pragma unroll
       for (int q = 0; q < 4; ++q) sCk[r][4 * lane + q] = (uint8_t)group_code(v[q], gq, G.kb);
       if ((lane & 15) == 0) p.L.k_scales[((size_t)s * G.qcap + i) * G.nkg + (lane >> 4)] = gq.word;
@@ -386,10 +398,10 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
       mn = fminf(mn, xk[r]);
       mx = fmaxf(mx, xk[r]);
     }
-    double sum = 0.0;
+    long long sum = 0;
     if (G.hybrid)
-      for (int r = 0; r < kGroupTokens; ++r) sum += (double)xk[r];
-    const GroupQ gq = group_params(mn, mx, sum, kGroupTokens, G.kb, G.hybrid);
+      for (int r = 0; r < kGroupTokens; ++r) sum += fixed(xk[r], 24);
+    const GroupQ gq = group_params(mn, mx, sum, 24, kGroupTokens, G.kb, G.hybrid);
 #pragma unroll
     for (int r = 0; r < kGroupTokens; ++r) sCk[r][c] = (uint8_t)group_code(xk[r], gq, G.kb);
     p.L.k_scales[((size_t)s * G.gcap + grp) * kHeadDim + c] = gq.word;
@@ -414,14 +426,15 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
       for (int q = 0; q < 4; ++q) v[q] = half_bits_to_float(sV[r][4 * lane + q]);
       float mn = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
       float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
-      double sum = ((double)v[0] + (double)v[1]) + ((double)v[2] + (double)v[3]);
+      long long sum = 0;
+      if (G.hybrid) sum = (fixed(v[0], 24) + fixed(v[1], 24)) + (fixed(v[2], 24) + fixed(v[3], 24));
       const int seg = G.gv / 4;  // lanes per channel group
       for (int o = seg / 2; o > 0; o >>= 1) {
         mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         if (G.hybrid) sum += __shfl_xor_sync(0xffffffffu, sum, o);
       }
-      const GroupQ gq = group_params(mn, mx, sum, G.gv, G.vb, G.hybrid);
+      const GroupQ gq = group_params(mn, mx, sum, 24, G.gv, G.vb, G.hybrid);
 #pragma unroll
       for (int q = 0; q < 4; ++q) sCv[r][4 * lane + q] = (uint8_t)group_code(v[q], gq, G.vb);
       if (lane % seg == 0) p.L.v_scales[((size_t)s * G.qcap + i) * G.nvg + lane / seg] = gq.word;
@@ -435,13 +448,23 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
 
 // InnerQ per-channel key normalisation of an empty cache's first append:
 // n_c = the smallest power of two >= max |K_c| over the call's tokens (1 for
-// an all-zero channel), per stream.  One CTA per stream, one thread per
-// channel (threads of a warp read consecutive channels of a token row).
-__global__ void __launch_bounds__(kHeadDim) key_norm_kernel(const __grid_constant__ AppendParams p) {
-  const int s = blockIdx.x, c = threadIdx.x;
+// an all-zero channel), per stream.  Two passes: CTAs over (token block,
+// stream) fold the block's max |K_c| into the stream's slot with an integer
+// atomic max (non-negative floats order like their bit patterns: the max is
+// exact in any order), then one thread per (stream, channel) turns the max
+// into the power of two, in place.  The slots start at zero (memset).
+constexpr int kNormTokens = 256;  // tokens per CTA of the max pass
+__global__ void __launch_bounds__(kHeadDim) key_norm_max_kernel(const __grid_constant__ AppendParams p) {
+  const int s = blockIdx.y, c = threadIdx.x;
+  const int t0 = blockIdx.x * kNormTokens, t1 = min(p.n_new, t0 + kNormTokens);
   const uint16_t* k = p.k_new + in_stream(p.geo, s) * p.n_new * kRowHalves + c;
   float m = 0.0f;
-  for (int t = 0; t < p.n_new; ++t) m = fmaxf(m, fabsf(half_bits_to_float(k[(size_t)t * kRowHalves])));
+  for (int t = t0; t < t1; ++t) m = fmaxf(m, fabsf(half_bits_to_float(k[(size_t)t * kRowHalves])));
+  atomicMax(reinterpret_cast<unsigned int*>(&p.L.k_norm[(size_t)s * kHeadDim + c]), __float_as_uint(m));
+}
+__global__ void __launch_bounds__(kHeadDim) key_norm_pow2_kernel(const __grid_constant__ AppendParams p) {
+  float* slot = &p.L.k_norm[(size_t)blockIdx.x * kHeadDim + threadIdx.x];
+  const float m = *slot;
   float n = 1.0f;
   if (m > 0.0f) {
     int e;
@@ -449,7 +472,7 @@ __global__ void __launch_bounds__(kHeadDim) key_norm_kernel(const __grid_constan
     n = ldexpf(1.0f, e);
     if (ldexpf(1.0f, e - 1) >= m) n = ldexpf(1.0f, e - 1);  // m itself a power of two
   }
-  p.L.k_norm[(size_t)s * kHeadDim + c] = n;
+  *slot = n;
 }
 
 // Copy the fp16 tokens of this call that stay fp16 (sinks and the final
@@ -665,15 +688,15 @@ __global__ void __launch_bounds__(kThreads)
       const int c = tid;
       float x[kGroupTokens];
       float mn = INFINITY, mx = -INFINITY;
-      double sum = 0.0;
+      long long sum = 0;
 #pragma unroll
       for (int r = 0; r < kGroupTokens; ++r) {
         x[r] = half_bits_to_float(sK[r][c]);
         mn = fminf(mn, x[r]);
         mx = fmaxf(mx, x[r]);
-        sum += (double)x[r];
+        sum += fixed(x[r], 24);
       }
-      const GroupQ gq = group_params(mn, mx, sum, kGroupTokens, bits, G.hybrid);
+      const GroupQ gq = group_params(mn, mx, sum, 24, kGroupTokens, bits, G.hybrid);
       const double m = half_bits_to_float((uint16_t)(gq.word & 0xffffu)), sc = half_bits_to_float((uint16_t)(gq.word >> 16));
 #pragma unroll
       for (int r = 0; r < kGroupTokens; ++r) {
@@ -691,13 +714,14 @@ __global__ void __launch_bounds__(kThreads)
       }
       float mn = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
       float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
-      double sum = ((double)v[0] + (double)v[1]) + ((double)v[2] + (double)v[3]);
+      const int sh = G.knorm ? 40 : 24;
+      long long sum = (fixed(v[0], sh) + fixed(v[1], sh)) + (fixed(v[2], sh) + fixed(v[3], sh));
       for (int o = 8; o > 0; o >>= 1) {
         mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         sum += __shfl_xor_sync(0xffffffffu, sum, o);
       }
-      const GroupQ gq = group_params(mn, mx, sum, 64, bits, G.hybrid);
+      const GroupQ gq = group_params(mn, mx, sum, sh, 64, bits, G.hybrid);
       const double m = half_bits_to_float((uint16_t)(gq.word & 0xffffu)), sc = half_bits_to_float((uint16_t)(gq.word >> 16));
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -713,14 +737,14 @@ __global__ void __launch_bounds__(kThreads)
     if (G.hadamard) hadamard_vals(v, p.hadamard_c, lane);
     float mn = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
     float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
-    double sum = ((double)v[0] + (double)v[1]) + ((double)v[2] + (double)v[3]);
+    long long sum = (fixed(v[0], 24) + fixed(v[1], 24)) + (fixed(v[2], 24) + fixed(v[3], 24));
     const int seg = G.gv / 4;
     for (int o = seg / 2; o > 0; o >>= 1) {
       mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       sum += __shfl_xor_sync(0xffffffffu, sum, o);
     }
-    const GroupQ gq = group_params(mn, mx, sum, G.gv, bits, G.hybrid);
+    const GroupQ gq = group_params(mn, mx, sum, 24, G.gv, bits, G.hybrid);
     const double m = half_bits_to_float((uint16_t)(gq.word & 0xffffu)), sc = half_bits_to_float((uint16_t)(gq.word >> 16));
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -823,7 +847,11 @@ cudaError_t launch_append_quantize(const AppendParams& p, int n_groups, cudaStre
 }
 
 cudaError_t launch_key_norm(const AppendParams& p, cudaStream_t st) {
-  key_norm_kernel<<<p.geo.NS, kHeadDim, 0, st>>>(p);
+  cudaError_t e = cudaMemsetAsync(p.L.k_norm, 0, sizeof(float) * (size_t)p.geo.NS * kHeadDim, st);
+  if (e != cudaSuccess) return e;
+  key_norm_max_kernel<<<dim3((p.n_new + kNormTokens - 1) / kNormTokens, p.geo.NS), kHeadDim, 0, st>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  key_norm_pow2_kernel<<<p.geo.NS, kHeadDim, 0, st>>>(p);
   return cudaGetLastError();
 }
 
