@@ -266,9 +266,11 @@ __device__ __forceinline__ uint32_t pack2x4(uint32_t x) {  // 4 byte codes < 4 -
 }
 __device__ void pack_rows(const uint8_t (*codes)[kHeadDim], int bits, int rows, uint8_t* dst,
                           int row_bytes, int tid) {
-  const int words = row_bytes / 4;
+  const int words = row_bytes / 4;  // 8, 16, 32 (2/4/8 bits) or 12 (3 bits)
+  const int lw = __ffs(words) - 1;   // log2 of a power-of-two word count
   for (int idx = tid; idx < rows * words; idx += kThreads) {
-    const int r = idx / words, wi = idx % words;
+    const int r = bits == 3 ? idx / 12 : idx >> lw;
+    const int wi = idx - r * words;
     uint32_t word = 0;
     if (bits == 8) {
       word = *reinterpret_cast<const uint32_t*>(&codes[r][4 * wi]);

@@ -12,6 +12,8 @@ Recipe (per layer):
        drawn per layer, x8 for the others) -- K outliers are channel-wise
        ("KVTuner" review, observation 2; KVQuant per-channel keys);
   V  ~ N(0, 1), Laplace(0, 1) or Student-t(nu=3) per workload;
+  per-head spread (the per-head bit workload): K and V of each KV head
+       scaled by factors log-uniform in [1/4, 4], drawn per layer;
   q  ~ N(0, 1);
   NUQ level tables: 8 quantiles of 65,536 seeded N(0, 1) samples, rounded
   to fp16 (a stand-in for the per-layer offline datatype of KVQuant).
@@ -65,6 +67,13 @@ def _draw(dist: str, shape, g: torch.Generator, device) -> torch.Tensor:
     raise ValueError(dist)
 
 
+def head_scales(name: str, layer: int, n_kv_heads: int, spread: float):
+    """Per-KV-head K and V scale factors, log-uniform in [1/spread, spread]
+    (seeded per layer): heads whose values differ in spread."""
+    rng = np.random.default_rng(seed_of(name, layer, "head_scales"))
+    return (spread ** rng.uniform(-1, 1, n_kv_heads), spread ** rng.uniform(-1, 1, n_kv_heads))
+
+
 def layer_kv(name: str, layer: int, tokens: int | None = None, batch: int | None = None,
              device="cpu", t0: int = 0):
     """fp16 K, V of one layer: [B, Hkv, tokens, d], token positions [t0, t0 + tokens)."""
@@ -77,6 +86,11 @@ def layer_kv(name: str, layer: int, tokens: int | None = None, batch: int | None
     och = torch.as_tensor(k_outlier_channels(name, layer, H, d), device=device)
     kscale = torch.ones((H, d), device=device)
     kscale.scatter_(1, och, float(w["k_outlier_scale"]))
+    vscale = torch.ones((H, 1), device=device)
+    if w.get("head_spread"):  # heads of different spread: K and V scales per head, log-uniform in [1/s, s]
+        hk, hv = head_scales(name, layer, H, w["head_spread"])
+        kscale = kscale * torch.as_tensor(hk, dtype=torch.float32, device=device)[:, None]
+        vscale = torch.as_tensor(hv, dtype=torch.float32, device=device)[:, None]
     first, last = t0 // CHUNK, (t0 + T - 1) // CHUNK
     for c in range(first, last + 1):
         a, b = max(t0, c * CHUNK), min(t0 + T, (c + 1) * CHUNK)
@@ -84,6 +98,7 @@ def layer_kv(name: str, layer: int, tokens: int | None = None, batch: int | None
         kc = _draw(w["k_dist"], shape, _gen(device, name, layer, "K", c), device)
         vc = _draw(w["v_dist"], shape, _gen(device, name, layer, "V", c), device)
         kc = kc * kscale[None, :, None, :]
+        vc = vc * vscale[None, :, :, None]
         lo, hi = a - c * CHUNK, b - c * CHUNK
         K[:, :, a - t0:b - t0] = kc[:, :, lo:hi].to(torch.float16)
         V[:, :, a - t0:b - t0] = vc[:, :, lo:hi].to(torch.float16)

@@ -52,10 +52,11 @@ WORKLOADS = {
         k_dist="normal", k_outlier_channels="random3", k_outlier_scale=8.0, v_dist="laplace"),
     # RateQuant: per-head (K, V) bits allocated per layer from the measured
     # distortion of the cache's quantizer on the layer's first 2048 tokens, an
-    # average of 4 bits per K or V component, at the Llama-3-8B shape
+    # average of 4 bits per K or V component, at the Llama-3-8B shape, with
+    # heads of different spread (K and V scales per head in [1/4, 4])
     "llama3_8b_rateq_t32k": dict(
         _BASE, layers=32, batch=16, n_q_heads=32, n_kv_heads=8, tokens=32768,
-        pairs="rateq", rateq_avg_bits=4.0, rateq_calib_tokens=2048, n_sink=4, n_recent=128,
+        pairs="rateq", rateq_avg_bits=4.0, rateq_calib_tokens=2048, n_sink=4, n_recent=128, head_spread=4.0,
         k_dist="normal", k_outlier_channels="random3", k_outlier_scale=8.0, v_dist="laplace"),
     "llama7b_nuq3_t1m": dict(
         _BASE, layers=1, batch=1, n_q_heads=32, n_kv_heads=32, tokens=1048576,

@@ -96,7 +96,7 @@ def test_allocation_pipeline_matches_the_oracle(B):
     """GPU distortions -> library fit + greedy, against oracle distortions ->
     oracle fit + greedy: the same per-head pairs."""
     from bit_kv_cache_07_gb300 import mixed, synth, workloads
-    name = "llama3_8b_mixed_t32k"
+    name = "llama3_8b_rateq_t32k"  # heads of different spread: the allocation mixes pairs
     cfg = workloads.layer_config(name, 0)
     K, V = synth.layer_kv(name, 0, tokens=512, batch=1, device="cuda")
     pairs, rep = mixed.allocate_pairs(cfg, K, V, 4.0)
@@ -113,3 +113,4 @@ def test_allocation_pipeline_matches_the_oracle(B):
     assert rep["bits"] == bits.tolist()
     assert pairs == [(int(bits[2 * h]), int(bits[2 * h + 1])) for h in range(cfg["n_kv_heads"])]
     assert sum(rep["bits"]) <= rep["total_bits"]
+    assert len(set(pairs)) > 1
