@@ -192,7 +192,7 @@ class Model:
         self.L = layers if layers > 0 else w["layers"]
         self.cfgs, self.units, self.unit_layer = [], [], []
         self.q, self.k_new, self.v_new, self.out = [], [], [], []
-        self.head_pairs = []
+        self.head_pairs, self.mixed = [], [None] * self.L
         for l in range(self.L):
             cfg = workloads.layer_config(name, l, tokens=self.T)
             if cfg["k_bits"] == 3:
@@ -208,6 +208,7 @@ class Model:
                 ml = mixed.MixedLayer(cfg, pairs, device=device)
                 ml.append(0, K, V)
                 self.head_pairs.append(pairs)
+                self.mixed[l] = ml
                 parts = [sub for _, _, sub in ml.parts]
             else:
                 layer = binding.Layer(cfg, device=device)
@@ -233,12 +234,20 @@ class Model:
         for i, u in enumerate(self.units):
             l = self.unit_layer[i]
             B.kvq_append(u.cfg, u.buf, self.T - 1, self.k_new[l], self.v_new[l], 1, stream)
-        for i in range(len(self.units)):
-            self.decode(i, stream)
+        for l in range(self.L):
+            self.decode_layer(l, stream)
 
     def decode(self, i: int, stream):
         u, l = self.units[i], self.unit_layer[i]
         self.binding.kvq_decode_attn(u.cfg, u.buf, self.T, self.q[l], self.out[l], None, self.ws, None, stream)
+
+    def decode_layer(self, l: int, stream):
+        if self.mixed[l] is not None:  # its pairs' caches side by side (fork / join on side streams)
+            self.mixed[l].decode(self.T, self.q[l], self.out[l], None, None, stream)
+            return
+        for i, ul in enumerate(self.unit_layer):
+            if ul == l:
+                self.decode(i, stream)
 
     def decode_bytes(self):
         return sum(algorithmic_bytes(c, self.T) for c in self.cfgs)
@@ -331,6 +340,8 @@ def time_decode_only(model, stream, steps: int, warmup: int):
     stream, and the time is divided by the launches.  Every unit gets the
     mean of its pair.  Returns (per-unit ms, None) or (None, why)."""
     import torch
+    if any(m is not None for m in model.mixed):
+        return _time_mixed_layers(model, stream, steps, warmup)
     groups = {}
     for l, c in enumerate(model.cfgs):
         groups.setdefault(_pair_name(c), []).append(l)
@@ -361,6 +372,37 @@ def time_decode_only(model, stream, steps: int, warmup: int):
             per_layer[l] = ms
         del g
     return per_layer, None
+
+
+def _time_mixed_layers(model, stream, steps: int, warmup: int):
+    """Per-head pairs: every layer's decode (its pairs' caches side by side)
+    captured back to back in one graph, replayed between two events; each
+    layer's time is split over its decode units by their bytes."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+        for l in range(model.L):
+            model.decode_layer(l, stream)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    layer_ms = e0.elapsed_time(e1) / (steps * model.L)
+    b = [algorithmic_bytes(c, model.T) for c in model.cfgs]
+    lb = [0] * model.L
+    for i, l in enumerate(model.unit_layer):
+        lb[l] += b[i]
+    del g
+    return [layer_ms * b[i] / lb[model.unit_layer[i]] for i in range(len(b))], None
 
 
 def time_append(name: str, dev, T: int, stream, reps: int = 20):
@@ -754,6 +796,13 @@ def main():
     dec_bytes = model.decode_bytes()
     peak, peak_kind = measured_peaks()
     roof, pairs = decode_roofline(model, layer_ms, peak, peak_kind, args.workload)
+    if any(m is not None for m in model.mixed):
+        pairs = None  # the parts of a layer run side by side: only the layer's time is measured
+        roof["launch_us"] = sum(layer_ms) * 1e3 / model.L
+        roof["bytes_per_launch"] = model.decode_bytes() / model.L
+        roof["timing"] = ("mean decode time per layer (its per-pair caches decoded side by side on forked "
+                          "streams, each on a byte-proportional share of the SMs): every layer's decode captured "
+                          "back to back in a CUDA graph, replayed between two CUDA events")
     e2e_ms, h2d, d2h = time_e2e(model, stream, max(3, args.steps), 2)
     e2e_ms = max_over_ranks(e2e_ms)
     launches = model.launches_per_step() * args.steps

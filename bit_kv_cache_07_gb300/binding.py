@@ -36,7 +36,7 @@ class kvq_config(C.Structure):
         ("k_lut", C.c_float * 8), ("v_lut", C.c_float * 8), ("softmax_scale", C.c_float),
         ("split_tokens", C.c_int32), ("position_offset", C.c_int32),
         ("k_group_channels", C.c_int32), ("hybrid_groups", C.c_int32), ("k_channel_norm", C.c_int32),
-        ("kv_heads_total", C.c_int32), ("kv_head_index", C.c_void_p),
+        ("kv_heads_total", C.c_int32), ("kv_head_index", C.c_void_p), ("sm_budget", C.c_int32),
     ]
 
 

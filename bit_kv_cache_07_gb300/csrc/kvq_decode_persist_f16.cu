@@ -59,6 +59,7 @@ cudaError_t plan_persist(DecodeParams& p, uint64_t* ws_need) {
   int sms = 0, occ = 0;
   cudaError_t e = device_sm_count(&sms);
   if (e != cudaSuccess) return e;
+  if (G.sm_budget > 0 && G.sm_budget < sms) sms = G.sm_budget;  // a share of the GPU
   e = dispatch(p, nullptr, &occ);
   if (e != cudaSuccess) return e;
   if (occ < 1) occ = 1;

@@ -84,6 +84,8 @@ kvq_status make_geometry(const kvq_config* c, Geometry* g) {
         if (c->kv_head_index[j] == h) return KVQ_ERR_INVALID_ARG;
     }
   }
+  if (c->sm_budget < 0) return KVQ_ERR_INVALID_ARG;
+  g->sm_budget = c->sm_budget;
   g->Hkv_tot = tot;
   g->Hq_tot = tot * (c->n_q_heads / c->n_kv_heads);
   g->has_map = c->kv_head_index ? 1 : 0;
@@ -317,6 +319,7 @@ static cudaError_t fill_waves(DecodeParams* p) {
   int sms = 0, occ = 0;
   cudaError_t e = device_sm_count(&sms);
   if (e != cudaSuccess) return e;
+  if (p->geo.sm_budget > 0 && p->geo.sm_budget < sms) sms = p->geo.sm_budget;
   e = launch_decode(*p, nullptr, &occ);
   if (e != cudaSuccess) return e;
   if (occ < 1) return cudaSuccess;

@@ -36,6 +36,7 @@ struct Geometry {
   // (kvmap[h] = the layer head of cache head h when has_map)
   int Hkv_tot, Hq_tot, has_map;
   int16_t kvmap[256];
+  int sm_budget;  // decode: SMs this cache's work may use (0: all)
 };
 
 // The layer's KV head of this cache's head h.

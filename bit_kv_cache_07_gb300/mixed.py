@@ -40,29 +40,60 @@ def allocate_pairs(cfg: dict, K, V, avg_bits: float, weights=None):
 
 class MixedLayer:
     """One layer's cache with per-KV-head (K bits, V bits) pairs: a
-    binding.Layer per distinct pair over its heads."""
+    binding.Layer per distinct pair over its heads.  A decode runs the parts
+    side by side: each gets a share of the SMs proportional to its cache
+    bytes (the config's sm_budget) and its own workspace, the first on the
+    caller's stream and the others on side streams that fork from it and
+    join back into it (CUDA-graph capturable)."""
 
     def __init__(self, cfg: dict, pairs, device="cuda"):
+        import torch
         hkv = cfg["n_kv_heads"]
         if len(pairs) != hkv:
             raise ValueError("one (K bits, V bits) pair per KV head")
         g = cfg["n_q_heads"] // hkv
         self.cfg = dict(cfg)
         self.pairs = [tuple(p) for p in pairs]
-        self.parts = []
-        for pair in sorted(set(self.pairs)):
-            heads = [h for h in range(hkv) if self.pairs[h] == pair]
-            sub = dict(cfg, k_bits=pair[0], v_bits=pair[1], n_kv_heads=len(heads), n_q_heads=g * len(heads),
-                       kv_heads_total=hkv, kv_head_index=heads)
-            self.parts.append((pair, heads, binding.Layer(sub, device=device)))
+        groups = [(pair, [h for h in range(hkv) if self.pairs[h] == pair]) for pair in sorted(set(self.pairs))]
+        subs = [dict(cfg, k_bits=pair[0], v_bits=pair[1], n_kv_heads=len(heads), n_q_heads=g * len(heads),
+                     kv_heads_total=hkv, kv_head_index=heads) for pair, heads in groups]
+        sms = torch.cuda.get_device_properties(torch.device(device)).multi_processor_count
+        size = [binding.kvq_layout_query(c).layer_bytes for c in subs]
+        share = [max(1, int(sms * b / sum(size))) for b in size] if len(subs) > 1 else [0]
+        self.parts, self.ws, self.side = [], [], []
+        for (pair, heads), sub, sm in zip(groups, subs, share):
+            sub["sm_budget"] = sm
+            layer = binding.Layer(sub, device=device)
+            self.parts.append((pair, heads, layer))
+            self.ws.append(torch.zeros(max(16, layer.layout.workspace_bytes), dtype=torch.uint8, device=device))
+        self.side = [torch.cuda.Stream(device=device) for _ in self.parts[1:]]
 
     def append(self, tokens_before: int, k_new, v_new, stream=None):
         for _, _, layer in self.parts:
             layer.append(tokens_before, k_new, v_new, stream)
 
     def decode(self, tokens: int, q, out, lse=None, workspace=None, stream=None):
-        for _, _, layer in self.parts:
-            layer.decode(tokens, q, out, lse, workspace, stream)
+        """Attention over the layer's cache into out (all heads); each part
+        uses its own workspace (`workspace` is not used)."""
+        import torch
+        main = stream if stream is not None else torch.cuda.current_stream()
+        if len(self.parts) == 1:
+            self.parts[0][2].decode(tokens, q, out, lse, self.ws[0], main)
+            return
+        fork = torch.cuda.Event()
+        fork.record(main)
+        joins = []
+        for i, (_, _, layer) in enumerate(self.parts):
+            s = main if i == 0 else self.side[i - 1]
+            if i:
+                s.wait_event(fork)
+            layer.decode(tokens, q, out, lse, self.ws[i], s)
+            if i:
+                e = torch.cuda.Event()
+                e.record(s)
+                joins.append(e)
+        for e in joins:
+            main.wait_event(e)
 
     def workspace_bytes(self) -> int:
         return max(layer.layout.workspace_bytes for _, _, layer in self.parts)

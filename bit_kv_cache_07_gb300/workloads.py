@@ -50,6 +50,12 @@ WORKLOADS = {
         _BASE, layers=32, batch=16, n_q_heads=32, n_kv_heads=8, tokens=32768,
         pairs="KV4", n_sink=4, n_recent=32, k_group_channels=64, hybrid_groups=1, k_channel_norm=1,
         k_dist="normal", k_outlier_channels="random3", k_outlier_scale=8.0, v_dist="laplace"),
+    # the Llama-3-8B per-layer pairs of the mixed workload with InnerQ keys
+    # (per-token 64-channel groups, hybrid groups, key normalisation)
+    "llama3_8b_mixed_innerq_t32k": dict(
+        _BASE, layers=32, batch=16, n_q_heads=32, n_kv_heads=8, tokens=32768,
+        pairs="seeded", n_sink=4, n_recent=128, k_group_channels=64, hybrid_groups=1, k_channel_norm=1,
+        k_dist="normal", k_outlier_channels="random3", k_outlier_scale=8.0, v_dist="laplace"),
     # RateQuant: per-head (K, V) bits allocated per layer from the measured
     # distortion of the cache's quantizer on the layer's first 2048 tokens, an
     # average of 4 bits per K or V component, at the Llama-3-8B shape, with
@@ -67,7 +73,7 @@ WORKLOADS = {
 # order of the workloads as listed with the method's benchmark
 WORKLOAD_ORDER = ["toy_k4v2_t1k", "llama2_7b_kv4_t4k", "llama3_8b_mixed_t32k",
                   "qwen_gqa_hadamard_t8k", "llama7b_nuq3_t1m", "llama3_8b_innerq_kv4_t32k",
-                  "llama3_8b_rateq_t32k"]
+                  "llama3_8b_rateq_t32k", "llama3_8b_mixed_innerq_t32k"]
 
 
 def layer_pairs(name: str) -> list[str]:

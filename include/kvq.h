@@ -128,6 +128,11 @@ typedef struct kvq_config {
                                  entries) that this cache holds, in its stream
                                  order; NULL: heads 0 .. n_kv_heads - 1.  Read
                                  during each call only.                        */
+    int32_t sm_budget;        /* decode: spread this cache's work over at most
+                                 this many SMs (0: all).  The caches of one
+                                 layer's distinct pairs, each given a share,
+                                 can then be decoded side by side on separate
+                                 CUDA streams (each with its own workspace).   */
 } kvq_config;
 
 /* Window rule.  For a sequence holding T tokens:
