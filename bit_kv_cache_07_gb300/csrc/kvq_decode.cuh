@@ -556,10 +556,21 @@ __device__ __forceinline__ uint32_t code3(const uint32_t (&w)[13], int c) { retu
 //              products per channel pair instead of rotating q or k
 //  RoPE, GQ>1: rotate each key pair once by A_j e^{i theta_j lane}, dot with
 //              every head
+// Group anchors of a warp that visits groups g, g + 4, g + 8, ...: lane j
+// keeps pairs j and j + 32; the anchor moves by e^{i theta_j 128} per visit
+// (`step`, from an fp64 angle) and is recomputed exactly (anchor_expi) every
+// kAnchorEvery visits, so fp32 rounding of the products stays within that
+// many complex multiplications.
+constexpr int kAnchorEvery = 16;
+struct AnchorWalk {
+  float2 a[2], step[2];
+  int left;  // visits before the next exact anchor
+};
+
 template <int GQ>
 __device__ __forceinline__ void k_logits_nuq_st(const DecodeParams& p, DecodeSmem<GQ>& sm,
                                                 const float2* __restrict__ tab, const unsigned char* st,
-                                                int grp, int lane, int w, float (&z)[GQ]) {
+                                                int grp, int lane, int w, float (&z)[GQ], AnchorWalk& aw) {
   const Geometry& G = p.geo;
   const int k = G.nout;
   uint32_t wd[13];
@@ -606,11 +617,19 @@ __device__ __forceinline__ void k_logits_nuq_st(const DecodeParams& p, DecodeSme
   if constexpr (GQ == 1) {
     // anchors of pairs 2i, 2i+1 as (x_2i, x_2i+1, y_2i, y_2i+1): fp32x2 operands without shuffling
     float* ap = reinterpret_cast<float*>(&sm.anchor[w][0]);
-    for (int j = lane; j < kHeadDim / 2; j += 32) {
-      const float2 a = anchor_expi<GQ>(p, sm, j, grp);
-      ap[(j >> 1) * 4 + (j & 1)] = a.x;
-      ap[(j >> 1) * 4 + 2 + (j & 1)] = a.y;
+    if (aw.left == 0) {
+      aw.a[0] = anchor_expi<GQ>(p, sm, lane, grp);
+      aw.a[1] = anchor_expi<GQ>(p, sm, lane + 32, grp);
+      aw.left = kAnchorEvery;
     }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = lane + 32 * h;
+      ap[(j >> 1) * 4 + (j & 1)] = aw.a[h].x;
+      ap[(j >> 1) * 4 + 2 + (j & 1)] = aw.a[h].y;
+      aw.a[h] = cmul(aw.a[h], aw.step[h]);  // the anchor of this warp's next group
+    }
+    --aw.left;
     __syncwarp();
     // two channel pairs at a time in packed fp32x2 arithmetic (W laid out like the anchors)
     const float4* tab4 = reinterpret_cast<const float4*>(tab);
@@ -631,13 +650,18 @@ __device__ __forceinline__ void k_logits_nuq_st(const DecodeParams& p, DecodeSme
       z2 = __ffma2_rn(Wx, cx, __ffma2_rn(make_float2(-Wy.x, -Wy.y), cy, z2));           // Re[W c]
     }
     float zr = z2.x + z2.y;
-    const float* tf = reinterpret_cast<const float*>(tab);
     for (int e = 0; e < k; ++e) {
       const int col = ocol[e];
       const float dv = half_bits_to_float(oval[e]) - ms.x;
       const int j = col & (kHeadDim / 2 - 1);
-      const int wi = ((j >> 1) * kGroupTokens + lane) * 4 + (j & 1), ai = (j >> 1) * 4 + (j & 1);
-      const float2 WA = cmul(make_float2(tf[wi], tf[wi + 2]), make_float2(ap[ai], ap[ai + 2]));
+      // W and the anchor of pair j as 16-byte loads: the W rows of a lane are
+      // 16 bytes apart from its neighbours' whatever their columns (no bank
+      // conflicts); pick the pair's components
+      const float4 W4 = tab4[(j >> 1) * kGroupTokens + lane];
+      const float4 A4 = anc4[j >> 1];
+      const bool odd = (j & 1) != 0;
+      const float2 WA = cmul(make_float2(odd ? W4.y : W4.x, odd ? W4.w : W4.z),
+                             make_float2(odd ? A4.y : A4.x, odd ? A4.w : A4.z));
       zr = fmaf(dv, (col < kHeadDim / 2) ? WA.x : -WA.y, zr);  // Re[WA dv] or Re[WA i dv]
     }
     z[0] = zr;
@@ -712,14 +736,16 @@ __device__ __forceinline__ void v_accumulate_nuq_st(const DecodeParams& p, Decod
     }
   }
   if (k == 0) return;
-  // outliers: entry n = lane, lane + 32, ... of the group's 32k entries
-  const uint8_t* ocol = st + NuqStage::vcol(k);
-  const uint16_t* oval = reinterpret_cast<const uint16_t*>(st + NuqStage::vval(k));
-  for (int n = lane; n < kGroupTokens * k; n += 32) {
-    const int t = n / k, col = ocol[n];
-    const float dv = half_bits_to_float(oval[n]) - unpack_min_scale(vms[t]).x;
+  // outliers: lane t adds its own token's k entries (rows hold exactly k,
+  // at entries t k .. t k + k - 1); columns of different tokens may meet
+  const uint8_t* ocol = st + NuqStage::vcol(k) + k * lane;
+  const uint16_t* oval = reinterpret_cast<const uint16_t*>(st + NuqStage::vval(k)) + k * lane;
+  const float vmin = unpack_min_scale(vms[lane]).x;
+  for (int e = 0; e < k; ++e) {
+    const int col = ocol[e];
+    const float dv = half_bits_to_float(oval[e]) - vmin;
 #pragma unroll
-    for (int r = 0; r < GQ; ++r) atomicAdd(&obuf[r * kHeadDim + col], sm.p[w][t][r] * dv);
+    for (int r = 0; r < GQ; ++r) atomicAdd(&obuf[r * kHeadDim + col], sm.p[w][lane][r] * dv);
   }
   __syncwarp();
 #pragma unroll
@@ -816,6 +842,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     const uint32_t stw_s = smem_u32(stw);
     float* obuf = nuq_obuf + w * GQ * kHeadDim;
     int cur = 0;
+    AnchorWalk aw;
+    aw.left = 0;
+    if (G.pre_rope) {
+      // e^{i theta_j 4 G_K}: a warp's consecutive groups are 4 apart
+#pragma unroll
+      for (int h = 0; h < 2; ++h) aw.step[h] = expi(4.0 * kGroupTokens * p.theta[lane + 32 * h]);
+    }
     if (g0 + w < g1) issue_nuq(p, s, g0 + w, stw_s, lane);
     cp_async_commit();
     for (int grp = g0 + w; grp < g1; grp += 4) {
@@ -825,7 +858,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
       __syncwarp();
       const unsigned char* stc = stw + cur * sb;
       float z[GQ];
-      k_logits_nuq_st<GQ>(p, sm, rope_e, stc, grp, lane, w, z);
+      k_logits_nuq_st<GQ>(p, sm, rope_e, stc, grp, lane, w, z, aw);
       softmax_update<GQ>(z, m, lsum, acc, macc, sm.p[w], lane);
       v_accumulate_nuq_st<GQ>(p, sm, stc, obuf, lane, w, acc, macc);
       __syncwarp();

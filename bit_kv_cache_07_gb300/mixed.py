@@ -58,8 +58,16 @@ class MixedLayer:
         subs = [dict(cfg, k_bits=pair[0], v_bits=pair[1], n_kv_heads=len(heads), n_q_heads=g * len(heads),
                      kv_heads_total=hkv, kv_head_index=heads) for pair, heads in groups]
         sms = torch.cuda.get_device_properties(torch.device(device)).multi_processor_count
-        size = [binding.kvq_layout_query(c).layer_bytes for c in subs]
-        share = [max(1, int(sms * b / sum(size))) for b in size] if len(subs) > 1 else [0]
+        # SM shares proportional to each part's expected decode time: the larger
+        # of its bytes over the copy bandwidth and its 32-token groups times the
+        # per-group arithmetic (the low-bit parts are bound by the latter:
+        # about the same instructions per group whatever the bit width)
+        est = []
+        for c in subs:
+            lay = binding.kvq_layout_query(c)
+            groups = c["batch"] * c["n_kv_heads"] * (lay.q_cap // 32)
+            est.append(max(lay.layer_bytes / 6.0e12, groups * 1.05e-9))
+        share = [max(1, int(sms * e / sum(est))) for e in est] if len(subs) > 1 else [0]
         self.parts, self.ws, self.side = [], [], []
         for (pair, heads), sub, sm in zip(groups, subs, share):
             sub["sm_budget"] = sm
