@@ -65,8 +65,8 @@ class MixedLayer:
         est = []
         for c in subs:
             lay = binding.kvq_layout_query(c)
-            groups = c["batch"] * c["n_kv_heads"] * (lay.q_cap // 32)
-            est.append(max(lay.layer_bytes / 6.0e12, groups * 1.05e-9))
+            n_groups = c["batch"] * c["n_kv_heads"] * (lay.q_cap // 32)
+            est.append(max(lay.layer_bytes / 6.0e12, n_groups * 1.05e-9))
         share = [max(1, int(sms * e / sum(est))) for e in est] if len(subs) > 1 else [0]
         self.parts, self.ws, self.side = [], [], []
         for (pair, heads), sub, sm in zip(groups, subs, share):
