@@ -94,7 +94,14 @@ def algorithmic_bytes(cfg: dict, T: int) -> int:
             k = cfg["outliers_per_vector"]
             per += Nq * 4 * 2 + 2 * (Nq * k * 3)
         else:
-            per += (Nq // 32) * d * 4 + Nq * (d // cfg["v_group_channels"]) * 4
+            gkc = cfg.get("k_group_channels", 0)
+            if gkc:  # InnerQ keys: {scale, min} per token and 64-channel group
+                per += Nq * (d // gkc) * 4
+            else:  # per-channel keys: {scale, min} per channel and 32-token group
+                per += (Nq // 32) * d * 4
+            per += Nq * (d // cfg["v_group_channels"]) * 4
+        if cfg.get("k_channel_norm", 0):
+            per += d * 4  # the stream's per-channel key normalisation (fp32)
     per += (S + W) * d * 2 * 2
     qo = cfg["batch"] * cfg["n_q_heads"] * d * 2 * 2
     return NS * per + qo
@@ -224,10 +231,32 @@ class Model:
             self.k_new.append(k)
             self.v_new.append(v)
             self.out.append(torch.empty_like(self.q[-1]))
+        # a step's inputs (every layer's q and new K/V) and outputs (every
+        # layer's attention) each in one contiguous buffer, the per-layer
+        # tensors views into it: a step moves them with one copy each way
+        self.inputs = self._gather(self.q + self.k_new + self.v_new)
+        self.outputs = self._gather(self.out)
+        self.q = self._views(self.inputs, self.q)
+        self.k_new = self._views(self.inputs[sum(t.numel() for t in self.q):], self.k_new)
+        self.v_new = self._views(self.inputs[sum(t.numel() for t in self.q + self.k_new):], self.v_new)
+        self.out = self._views(self.outputs, self.out)
         ws_bytes = max(u.layout.workspace_bytes for u in self.units)
         self.ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=device)
         torch.cuda.synchronize()
         self.binding = binding
+
+    @staticmethod
+    def _gather(ts):
+        import torch
+        return torch.cat([t.reshape(-1) for t in ts])
+
+    @staticmethod
+    def _views(flat, ts):
+        out, o = [], 0
+        for t in ts:
+            out.append(flat[o:o + t.numel()].view(t.shape))
+            o += t.numel()
+        return out
 
     def step(self, stream):
         B = self.binding
@@ -478,22 +507,16 @@ def time_e2e(model, stream, steps: int, warmup: int):
     """Same step through the public API with this step's inputs copied in from
     pinned host memory and the outputs copied back, inside the timed region."""
     import torch
-    hq = [t.cpu().pin_memory() for t in model.q]
-    hk = [t.cpu().pin_memory() for t in model.k_new]
-    hv = [t.cpu().pin_memory() for t in model.v_new]
-    ho = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in model.out]
-    h2d = sum(t.numel() * t.element_size() for t in hq + hk + hv)
-    d2h = sum(t.numel() * t.element_size() for t in ho)
+    h_in = model.inputs.cpu().pin_memory()  # every layer's q and new K/V of the step
+    h_out = torch.empty(model.outputs.shape, dtype=model.outputs.dtype).pin_memory()
+    h2d = h_in.numel() * h_in.element_size()
+    d2h = h_out.numel() * h_out.element_size()
 
     def one():
         with torch.cuda.stream(stream):
-            for l in range(model.L):
-                model.q[l].copy_(hq[l], non_blocking=True)
-                model.k_new[l].copy_(hk[l], non_blocking=True)
-                model.v_new[l].copy_(hv[l], non_blocking=True)
+            model.inputs.copy_(h_in, non_blocking=True)
             model.step(stream)
-            for l in range(model.L):
-                ho[l].copy_(model.out[l], non_blocking=True)
+            h_out.copy_(model.outputs, non_blocking=True)
 
     for _ in range(warmup):
         one()
@@ -866,8 +889,9 @@ def main():
         "cpu_baseline": cpu,
         "cpu_baseline_all_cores": cpu_all,
         "e2e": {"value": e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "how": "eager calls of the public C ABI per layer; this step's q and new K/V copied in from "
-                       "pinned host memory and every layer's output copied back, inside the timed region"},
+                "how": "eager calls of the public C ABI per layer; this step's q and new K/V of every layer "
+                       "copied in from pinned host memory (one copy) and every layer's output copied back "
+                       "(one copy), inside the timed region"},
         "gpu_launches": launches,
         "clocks": clk,
     }

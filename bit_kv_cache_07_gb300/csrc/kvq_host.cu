@@ -11,7 +11,11 @@ using namespace kvq;
 namespace {
 
 constexpr uint64_t kAlign = 256;
-constexpr int kTargetCtas = 152 * 6;  // decode: ~2 waves of 3 resident CTAs per SM of GB300
+// The host-only split plan (kvq_layout_query / kvq_decode_plan run without a
+// device) aims at this many CTAs, about two waves of 3 resident CTAs on 152
+// SMs; a decode then widens it to the SM count and occupancy of the device
+// it runs on (fill_waves below).
+constexpr int kTargetCtas = 152 * 6;
 
 uint64_t align_up(uint64_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 

@@ -358,7 +358,7 @@ kvq_status decode_setup(const kvq_config* cfg, const void* layer_buf, int32_t to
                         uint16_t* out, float* lse, DecodeParams* p, bool* persistent, uint64_t* layout_ws);
 // widen: with automatic splits, raise the split kernel's split count so its
 // grid fills whole waves of resident CTAs (more scratch; the fixed-scratch
-// entry point passes false).
+// entry point passes false when the widened plan would not fit its array).
 kvq_status decode_plan_device(DecodeParams* p, bool persistent, uint64_t* need, bool widen = true);
 kvq_status decode_launch(DecodeParams* p, bool persistent, void* ws, cudaStream_t st);
 

@@ -71,9 +71,17 @@ extern "C" kvq_status kvq_decode_attn_noalloc(const kvq_config* cfg, const void*
   uint64_t layout_ws = 0;
   kvq_status st = kvq::decode_setup(cfg, layer_buf, tokens, q, out, lse, &p, &persistent, &layout_ws);
   if (st != KVQ_OK) return st;
+  // the split plan widened to this device's SMs, as kvq_decode_attn uses it,
+  // when its partials fit the scratch; else the narrower host plan
+  kvq::DecodeParams host_plan = p;
   uint64_t need = 0;
-  st = kvq::decode_plan_device(&p, persistent, &need, /*widen=*/false);
+  st = kvq::decode_plan_device(&p, persistent, &need, /*widen=*/true);
   if (st != KVQ_OK) return st;
+  if (need > kNoAllocScratchBytes) {
+    p = host_plan;
+    st = kvq::decode_plan_device(&p, persistent, &need, /*widen=*/false);
+    if (st != KVQ_OK) return st;
+  }
   if (need > kNoAllocScratchBytes) return KVQ_ERR_WORKSPACE;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   void* scratch = nullptr;

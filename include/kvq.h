@@ -292,6 +292,9 @@ kvq_status kvq_decode_path(const kvq_config *cfg, int32_t tokens, int32_t *persi
  *   after a cudaDeviceReset, which may move the array).
  *   All calls share the array: calls that overlap on the GPU race; serialise
  *   them.
+ *   The split kernel's splits are widened to the device's SMs as in
+ *   kvq_decode_attn when the partials fit the array, else the host plan
+ *   (kvq_decode_plan) is used as is.
  * Errors: as kvq_decode_attn; KVQ_ERR_WORKSPACE when this call's scratch
  * (split counters + per-split partials) would exceed 8 MiB. */
 kvq_status kvq_decode_attn_noalloc(const kvq_config *cfg, const void *layer_buf, int32_t tokens,
