@@ -59,8 +59,17 @@ __device__ __forceinline__ uint32_t uniform_code(float x, float mn, float scale,
 // |S| 2^(b+1) <= n (MX - MN), all in those units, is then exact too (the
 // same real-number test the oracle makes with its exact fp64 mean).  At most
 // 128 values: |S| <= 2^47 and the products stay below 2^57.
+// x 2^sh as an integer, from the bits of x (no 64-bit conversion
+// instruction): |m| 2^(e - 150 + sh) with m the 24-bit significand and e
+// the biased exponent (1 for subnormals); a negative shift only drops zero
+// bits, because x 2^sh is an integer.
 __device__ __forceinline__ long long fixed(float x, int sh) {
-  return __float2ll_rz(__fmul_rn(x, sh == 40 ? 1099511627776.0f : 16777216.0f));  // exact: a power-of-two scaling
+  const uint32_t b = __float_as_uint(x);
+  const int e = (int)((b >> 23) & 0xFFu);
+  const long long m = (long long)((b & 0x7FFFFFu) | (e ? 0x800000u : 0u));
+  const int shift = (e ? e : 1) - 150 + sh;
+  const long long a = shift >= 0 ? (m << shift) : (m >> -shift);
+  return (b >> 31) ? -a : a;
 }
 struct GroupQ {
   float mn, scale, rs;  // asymmetric origin, fp32 scale and its reciprocal
@@ -264,23 +273,24 @@ __device__ __forceinline__ uint32_t pack2x4(uint32_t x) {  // 4 byte codes < 4 -
   t |= t >> 12;               // bits 4-7: c2 | c3 << 2
   return t & 0xFFu;
 }
-__device__ void pack_rows(const uint8_t (*codes)[kHeadDim], int bits, int rows, uint8_t* dst,
-                          int row_bytes, int tid) {
+template <int bits>
+__device__ __forceinline__ void pack_rows(const uint8_t (*codes)[kHeadDim], int rows, uint8_t* dst, int row_bytes,
+                                          int tid) {
   const int words = row_bytes / 4;  // 8, 16, 32 (2/4/8 bits) or 12 (3 bits)
   const int lw = __ffs(words) - 1;   // log2 of a power-of-two word count
   for (int idx = tid; idx < rows * words; idx += kThreads) {
     const int r = bits == 3 ? idx / 12 : idx >> lw;
     const int wi = idx - r * words;
     uint32_t word = 0;
-    if (bits == 8) {
+    if constexpr (bits == 8) {
       word = *reinterpret_cast<const uint32_t*>(&codes[r][4 * wi]);
-    } else if (bits == 4) {
+    } else if constexpr (bits == 4) {
       const uint2 x = *reinterpret_cast<const uint2*>(&codes[r][8 * wi]);
       word = pack4x8(x.x) | (pack4x8(x.y) << 16);
-    } else if (bits == 2) {
+    } else if constexpr (bits == 2) {
       const uint4 x = *reinterpret_cast<const uint4*>(&codes[r][16 * wi]);
       word = pack2x4(x.x) | (pack2x4(x.y) << 8) | (pack2x4(x.z) << 16) | (pack2x4(x.w) << 24);
-    } else if (bits == 3) {
+    } else if constexpr (bits == 3) {
       const int c0 = (32 * wi) / 3, off = 32 * wi - 3 * c0;
       unsigned long long acc = 0;
 #pragma unroll
@@ -297,7 +307,11 @@ __device__ void pack_rows(const uint8_t (*codes)[kHeadDim], int bits, int rows, 
   }
 }
 
-// One CTA quantizes one G_K-token group of one stream (K and V).
+// One CTA quantizes one G_K-token group of one stream (K and V).  One
+// instantiation per key mode and bit widths -- KM = 0: uniform K per channel,
+// 1: uniform InnerQ K (per token, 64-channel groups), 2: non-uniform codes
+// (KB = VB = 3) -- so that each holds only its own path.
+template <int KM, int KB, int VB>
 __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_constant__ AppendParams p) {
   const Geometry& G = p.geo;
   const int grp = p.first_group + blockIdx.x;
@@ -351,7 +365,7 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
   nuq_midpoints(p.v_lut, tau_v);
 
   // ---- K
-  if (G.kb == 3) {
+  if constexpr (KM == 2) {
     for (int r = w; r < kGroupTokens; r += 4) {
       const int i = i0 + r;
       const size_t csr = (size_t)s * G.qcap * kmax + (size_t)i * kmax;
@@ -363,16 +377,26 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
         if (i == 0) rp[0] = 0;
       }
     }
-  } else if (G.gkc) {
+  } else if constexpr (KM == 1) {
     // InnerQ: per token, groups of 64 channels along the hidden dimension
     // (16 lanes per group), on the keys divided by the channel normalisation
+    // the normalisation is a power of two 2^e (|e| <= 24): dividing by it is
+    // exactly multiplying by 2^-e, and neither result can be subnormal
+    float inv[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+    if (G.knorm) {
+      const float4 n4 = *reinterpret_cast<const float4*>(&p.L.k_norm[(size_t)s * kHeadDim + 4 * lane]);
+      inv[0] = __frcp_rn(n4.x);
+      inv[1] = __frcp_rn(n4.y);
+      inv[2] = __frcp_rn(n4.z);
+      inv[3] = __frcp_rn(n4.w);
+    }
     for (int r = w; r < kGroupTokens; r += 4) {
       const int i = i0 + r;
       float v[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         v[q] = half_bits_to_float(sK[r][4 * lane + q]);
-        if (G.knorm) v[q] = __fdiv_rn(v[q], p.L.k_norm[(size_t)s * kHeadDim + 4 * lane + q]);  // exact: 2^e
+        if (G.knorm) v[q] = __fmul_rn(v[q], inv[q]);
       }
       float mn = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
       float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
@@ -384,9 +408,9 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         if (G.hybrid) sum += __shfl_xor_sync(0xffffffffu, sum, o);
       }
-      const GroupQ gq = group_params(mn, mx, sum, sh, 64, G.kb, G.hybrid);
+      const GroupQ gq = group_params(mn, mx, sum, sh, 64, KB, G.hybrid);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) sCk[r][4 * lane + q] = (uint8_t)group_code(v[q], gq, G.kb);
+      for (int q = 0; q < 4; ++q) sCk[r][4 * lane + q] = (uint8_t)group_code(v[q], gq, KB);
       if ((lane & 15) == 0) p.L.k_scales[((size_t)s * G.qcap + i) * G.nkg + (lane >> 4)] = gq.word;
     }
   } else {
@@ -403,9 +427,9 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
     long long sum = 0;
     if (G.hybrid)
       for (int r = 0; r < kGroupTokens; ++r) sum += fixed(xk[r], 24);
-    const GroupQ gq = group_params(mn, mx, sum, 24, kGroupTokens, G.kb, G.hybrid);
+    const GroupQ gq = group_params(mn, mx, sum, 24, kGroupTokens, KB, G.hybrid);
 #pragma unroll
-    for (int r = 0; r < kGroupTokens; ++r) sCk[r][c] = (uint8_t)group_code(xk[r], gq, G.kb);
+    for (int r = 0; r < kGroupTokens; ++r) sCk[r][c] = (uint8_t)group_code(xk[r], gq, KB);
     p.L.k_scales[((size_t)s * G.gcap + grp) * kHeadDim + c] = gq.word;
   }
 
@@ -413,7 +437,7 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
   for (int r = w; r < kGroupTokens; r += 4) {
     const int i = i0 + r;
     if (G.hadamard) hadamard_row_inplace(sV[r], p.hadamard_c, lane);
-    if (G.vb == 3) {
+    if constexpr (VB == 3) {
       const size_t csr = (size_t)s * G.qcap * kmax + (size_t)i * kmax;
       nuq_encode_row(sV[r], p.v_lut, tau_v, kmax, sCv[r], &p.L.v_scales[(size_t)s * G.qcap + i],
                      p.L.v_col + csr, p.L.v_val + csr, lane);
@@ -436,16 +460,16 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         if (G.hybrid) sum += __shfl_xor_sync(0xffffffffu, sum, o);
       }
-      const GroupQ gq = group_params(mn, mx, sum, 24, G.gv, G.vb, G.hybrid);
+      const GroupQ gq = group_params(mn, mx, sum, 24, G.gv, VB, G.hybrid);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) sCv[r][4 * lane + q] = (uint8_t)group_code(v[q], gq, G.vb);
+      for (int q = 0; q < 4; ++q) sCv[r][4 * lane + q] = (uint8_t)group_code(v[q], gq, VB);
       if (lane % seg == 0) p.L.v_scales[((size_t)s * G.qcap + i) * G.nvg + lane / seg] = gq.word;
     }
   }
   __syncthreads();
 
-  pack_rows(sCk, G.kb, kGroupTokens, p.L.k_codes + ((size_t)s * G.qcap + i0) * G.krow, G.krow, tid);
-  pack_rows(sCv, G.vb, kGroupTokens, p.L.v_codes + ((size_t)s * G.qcap + i0) * G.vrow, G.vrow, tid);
+  pack_rows<KB>(sCk, kGroupTokens, p.L.k_codes + ((size_t)s * G.qcap + i0) * G.krow, G.krow, tid);
+  pack_rows<VB>(sCv, kGroupTokens, p.L.v_codes + ((size_t)s * G.qcap + i0) * G.vrow, G.vrow, tid);
 }
 
 // InnerQ per-channel key normalisation of an empty cache's first append:
@@ -455,14 +479,39 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
 // atomic max (non-negative floats order like their bit patterns: the max is
 // exact in any order), then one thread per (stream, channel) turns the max
 // into the power of two, in place.  The slots start at zero (memset).
+__device__ __forceinline__ __half2 u32_as_half2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// In the max pass thread t reads 16-byte pieces (channels 8 (t mod 16) ..
+// + 7) of every 8th row from row t / 16 on, keeps the maxima of |x| as fp16
+// pairs (exact), and the 8 row slots of a channel meet in shared memory.
 constexpr int kNormTokens = 256;  // tokens per CTA of the max pass
 __global__ void __launch_bounds__(kHeadDim) key_norm_max_kernel(const __grid_constant__ AppendParams p) {
-  const int s = blockIdx.y, c = threadIdx.x;
+  __shared__ float part[8][kHeadDim];
+  const int s = blockIdx.y, tid = threadIdx.x, piece = tid & 15, row = tid >> 4;
   const int t0 = blockIdx.x * kNormTokens, t1 = min(p.n_new, t0 + kNormTokens);
-  const uint16_t* k = p.k_new + in_stream(p.geo, s) * p.n_new * kRowHalves + c;
-  float m = 0.0f;
-  for (int t = t0; t < t1; ++t) m = fmaxf(m, fabsf(half_bits_to_float(k[(size_t)t * kRowHalves])));
-  atomicMax(reinterpret_cast<unsigned int*>(&p.L.k_norm[(size_t)s * kHeadDim + c]), __float_as_uint(m));
+  const uint4* k = reinterpret_cast<const uint4*>(p.k_new + in_stream(p.geo, s) * p.n_new * kRowHalves) + piece;
+  __half2 m[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m[i] = __float2half2_rn(0.0f);
+#pragma unroll 4
+  for (int t = t0 + row; t < t1; t += 8) {
+    const uint4 x = k[(size_t)t * (kRowHalves / 8)];
+    m[0] = __hmax2(m[0], __habs2(u32_as_half2(x.x)));
+    m[1] = __hmax2(m[1], __habs2(u32_as_half2(x.y)));
+    m[2] = __hmax2(m[2], __habs2(u32_as_half2(x.z)));
+    m[3] = __hmax2(m[3], __habs2(u32_as_half2(x.w)));
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(m[i]);
+    part[row][8 * piece + 2 * i] = f.x;
+    part[row][8 * piece + 2 * i + 1] = f.y;
+  }
+  __syncthreads();
+  float mc = part[0][tid];
+#pragma unroll
+  for (int r = 1; r < 8; ++r) mc = fmaxf(mc, part[r][tid]);
+  atomicMax(reinterpret_cast<unsigned int*>(&p.L.k_norm[(size_t)s * kHeadDim + tid]), __float_as_uint(mc));
 }
 __global__ void __launch_bounds__(kHeadDim) key_norm_pow2_kernel(const __grid_constant__ AppendParams p) {
   float* slot = &p.L.k_norm[(size_t)blockIdx.x * kHeadDim + threadIdx.x];
@@ -478,29 +527,43 @@ __global__ void __launch_bounds__(kHeadDim) key_norm_pow2_kernel(const __grid_co
 }
 
 // Copy the fp16 tokens of this call that stay fp16 (sinks and the final
-// window) into their slots.  One thread per 16-byte chunk of a K or V row.
+// window) into their slots.  One thread per 16-byte chunk of a K or V row,
+// over those tokens only: the call's tokens j < a (sinks; every token of an
+// fp16 cache) and j >= b (past the quantized part).
+__host__ __device__ __forceinline__ void window_split(const AppendParams& p, int* a, int* b) {
+  const Geometry& G = p.geo;
+  if (G.fp16_mode) {
+    *a = *b = p.n_new;
+    return;
+  }
+  auto clamp = [](int x, int lo, int hi) { return x < lo ? lo : x > hi ? hi : x; };
+  *a = clamp(G.S - p.tokens_before, 0, p.n_new);
+  *b = clamp(G.S + p.nq_after - p.tokens_before, *a, p.n_new);
+}
 __global__ void __launch_bounds__(256) append_window_kernel(const __grid_constant__ AppendParams p) {
   const Geometry& G = p.geo;
   grid_dep_wait();     // earlier kernels may still read the ring slots written here
   grid_dep_trigger();  // the decode that follows may set up meanwhile
-  const size_t total = (size_t)G.NS * p.n_new * (2 * kRowVec);
+  int a, b;
+  window_split(p, &a, &b);
+  const int ncopy = a + (p.n_new - b);
+  const size_t total = (size_t)G.NS * ncopy * (2 * kRowVec);
   for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (size_t)gridDim.x * blockDim.x) {
     const int ch = (int)(idx % kRowVec);
     const int isv = (int)((idx / kRowVec) % 2);
     const size_t rest = idx / (2 * kRowVec);
-    const int j = (int)(rest % p.n_new);
-    const int s = (int)(rest / p.n_new);
+    const int jc = (int)(rest % ncopy);
+    const int s = (int)(rest / ncopy);
+    const int j = jc < a ? jc : b + (jc - a);
     const int pos = p.tokens_before + j;
     uint16_t* dst;
     if (G.fp16_mode) {
       dst = (isv ? p.L.v_ring : p.L.k_ring) + ((size_t)s * G.ring + pos) * kRowHalves;
     } else if (pos < G.S) {
       dst = (isv ? p.L.v_sink : p.L.k_sink) + ((size_t)s * G.S + pos) * kRowHalves;
-    } else if (pos >= G.S + p.nq_after) {
-      dst = (isv ? p.L.v_ring : p.L.k_ring) + ((size_t)s * G.ring + (pos - G.S) % G.ring) * kRowHalves;
     } else {
-      continue;  // quantized by this call
+      dst = (isv ? p.L.v_ring : p.L.k_ring) + ((size_t)s * G.ring + (pos - G.S) % G.ring) * kRowHalves;
     }
     const uint16_t* src = (isv ? p.v_new : p.k_new) + (in_stream(G, s) * p.n_new + j) * kRowHalves;
     reinterpret_cast<uint4*>(dst)[ch] = reinterpret_cast<const uint4*>(src)[ch];
@@ -844,8 +907,20 @@ cudaError_t launch_nuq_fit(const uint16_t* x, long long nvec, int k, int hadamar
 
 cudaError_t launch_append_quantize(const AppendParams& p, int n_groups, cudaStream_t st) {
   dim3 grid(n_groups, p.geo.NS);
-  append_quantize_kernel<<<grid, kThreads, 0, st>>>(p);
-  return cudaGetLastError();
+  const int kb = p.geo.kb, vb = p.geo.vb, km = kb == 3 ? 2 : p.geo.gkc ? 1 : 0;
+  bool done = false;
+  auto go = [&](auto kernel) {
+    kernel<<<grid, kThreads, 0, st>>>(p);
+    done = true;
+  };
+  if (km == 2) go(append_quantize_kernel<2, 3, 3>);
+#define KVQ_APPEND(K, V)                                          \
+  if (km == 0 && kb == K && vb == V) go(append_quantize_kernel<0, K, V>); \
+  if (km == 1 && kb == K && vb == V) go(append_quantize_kernel<1, K, V>);
+  KVQ_APPEND(2, 2) KVQ_APPEND(2, 4) KVQ_APPEND(2, 8) KVQ_APPEND(4, 2) KVQ_APPEND(4, 4) KVQ_APPEND(4, 8)
+  KVQ_APPEND(8, 2) KVQ_APPEND(8, 4) KVQ_APPEND(8, 8)
+#undef KVQ_APPEND
+  return done ? cudaGetLastError() : cudaErrorInvalidValue;
 }
 
 cudaError_t launch_key_norm(const AppendParams& p, cudaStream_t st) {
@@ -858,9 +933,12 @@ cudaError_t launch_key_norm(const AppendParams& p, cudaStream_t st) {
 }
 
 cudaError_t launch_append_window(const AppendParams& p, cudaStream_t st) {
-  const size_t total = (size_t)p.geo.NS * p.n_new * (2 * kRowVec);
+  int a, b;
+  window_split(p, &a, &b);
+  const size_t total = (size_t)p.geo.NS * (a + (p.n_new - b)) * (2 * kRowVec);
   size_t blocks = (total + 255) / 256;
   if (blocks > 152 * 64) blocks = 152 * 64;
+  if (blocks < 1) blocks = 1;  // nothing to copy: the launch still keeps the dependent-launch chain
   return launch_dependent(append_window_kernel, dim3((unsigned)blocks), dim3(256), 0, st, p);
 }
 

@@ -249,3 +249,40 @@ def test_negative_control_corrupted_byte_is_detected(B):
     layer.decode(T, q, bad, None, B.new_workspace(cfg))
     torch.cuda.synchronize()
     assert not torch.equal(bad, clean)
+
+
+def _tie_values(rng, shape, qmax):
+    """fp16 values on a grid of step 2^-4 from an offset of 1: the group's
+    extremes 1 and 1 + qmax/16 are planted at the first two positions of
+    every group, every other value is 1 + (k + 0.5)/16 (an exact tie of the
+    quantizer's quotient, which must round half to even) or 1 + k/16."""
+    k = rng.integers(0, qmax, shape)
+    half = rng.integers(0, 2, shape)
+    return 1.0 + (k + 0.5 * half) / 16.0
+
+
+@pytest.mark.parametrize("kb,vb,iq", [(2, 2, 0), (4, 4, 0), (8, 8, 0), (4, 2, 0), (4, 4, 1), (8, 2, 1)])
+def test_exact_ties_round_half_even(B, kb, vb, iq):
+    """Groups whose quotients (x - min) / scale sit exactly on half-integers:
+    the kernel's reciprocal shortcut flags them and the IEEE division rounds
+    them half to even, byte for byte as the oracle."""
+    rng = np.random.default_rng(kb * 10 + vb + 100 * iq)
+    Bt, Hkv, T = 1, 2, 96
+    cfg = cfg_dict(kb, vb, Bt, 2 * Hkv, Hkv, T)
+    if iq:
+        cfg.update(k_group_channels=64)
+    qk, qv = (1 << kb) - 1, (1 << vb) - 1
+    K = _tie_values(rng, (Bt, Hkv, T, 128), qk)
+    V = _tie_values(rng, (Bt, Hkv, T, 128), qv)
+    if iq:  # per token, channel groups of 64: extremes at channels 0, 1 and 64, 65
+        K[..., 0], K[..., 1], K[..., 64], K[..., 65] = 1.0, 1.0 + qk / 16, 1.0, 1.0 + qk / 16
+    else:  # per channel over 32-token groups: extremes at tokens 32 g and 32 g + 1
+        K[:, :, 0::32, :], K[:, :, 1::32, :] = 1.0, 1.0 + qk / 16
+    V[..., 0], V[..., 1], V[..., 64], V[..., 65] = 1.0, 1.0 + qv / 16, 1.0, 1.0 + qv / 16
+    K, V = K.astype(np.float16), V.astype(np.float16)
+    assert np.all(K.astype(np.float64) == 1.0 + np.round((K.astype(np.float64) - 1.0) * 32) / 32)
+    layer = B.Layer(cfg)
+    layer.append(0, torch.from_numpy(K).cuda(), torch.from_numpy(V).cuda())
+    torch.cuda.synchronize()
+    refs = check_store(layer, cfg, T, K, V)
+    check_decode(B, layer, cfg, T, refs, seed=3)
