@@ -470,6 +470,12 @@ void orc_build_stream(const orc_cfg *c, int T, const uint16_t *K, const uint16_t
         memcpy(kwin + (size_t)w * d, K + (size_t)t * d, (size_t)d * 2);
         memcpy(vwin + (size_t)w * d, V + (size_t)t * d, (size_t)d * 2);
     }
+    /* InnerQ key normalisation: fixed by the first norm_tokens tokens (the
+     * prefill), whether or not any of them is quantized yet */
+    if (c->k_norm) {
+        int P = (c->norm_tokens > 0 && c->norm_tokens < T) ? c->norm_tokens : T;
+        orc_key_norm(K, P, d, kn);
+    }
     if (Nq == 0) {
         if (c->k_bits == 3) k_rowptr[0] = 0;
         if (c->v_bits == 3) v_rowptr[0] = 0;
@@ -478,10 +484,6 @@ void orc_build_stream(const orc_cfg *c, int T, const uint16_t *K, const uint16_t
 
     /* K */
     int krow = row_bytes(c->k_bits, d);
-    if (c->k_norm) {
-        int P = (c->norm_tokens > 0 && c->norm_tokens < T) ? c->norm_tokens : T;
-        orc_key_norm(K, P, d, kn);
-    }
     if (c->gkc > 0) {
         /* InnerQ: per token, groups of gkc channels along the hidden dimension,
          * on the normalised keys K / n_c */
