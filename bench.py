@@ -76,10 +76,15 @@ def window_counts(cfg: dict, T: int):
     return s, nq, T - s - nq
 
 
-def algorithmic_bytes(cfg: dict, T: int) -> int:
+def algorithmic_bytes(cfg: dict, T: int, rows=None) -> int:
     """Bytes one decode launch must move: packed codes, scales, CSR outlier
     entries and fp16 sink/window tokens of every stream (each read once per
-    KV head), plus q in and out."""
+    KV head), plus q in and out.  With per-row lengths `rows` (a ragged
+    batch) every row's streams count at their own length."""
+    if rows is not None:
+        one = dict(cfg, batch=1)
+        qo1 = cfg["n_q_heads"] * cfg["head_dim"] * 2 * 2
+        return sum(algorithmic_bytes(one, t) - qo1 for t in rows) + cfg["batch"] * qo1
     S, Nq, W = window_counts(cfg, T)
     d = cfg["head_dim"]
     NS = cfg["batch"] * cfg["n_kv_heads"]
@@ -196,6 +201,7 @@ class Model:
         from bit_kv_cache_07_gb300 import binding, mixed, synth, workloads
         w = workloads.WORKLOADS[name]
         self.name, self.T = name, (tokens if tokens > 0 else w["tokens"])
+        self.rows = workloads.row_tokens(name, self.T)  # per batch row lengths (ragged), or None
         self.L = layers if layers > 0 else w["layers"]
         self.cfgs, self.units, self.unit_layer = [], [], []
         self.q, self.k_new, self.v_new, self.out = [], [], [], []
@@ -219,7 +225,10 @@ class Model:
                 parts = [sub for _, _, sub in ml.parts]
             else:
                 layer = binding.Layer(cfg, device=device)
-                layer.append(0, K, V)
+                if self.rows is not None:
+                    layer.append_ragged([0] * cfg["batch"], [t - 1 for t in self.rows], K, V)
+                else:
+                    layer.append(0, K, V)
                 parts = [layer]
             del K, V
             for sub in parts:
@@ -262,13 +271,24 @@ class Model:
         B = self.binding
         for i, u in enumerate(self.units):
             l = self.unit_layer[i]
-            B.kvq_append(u.cfg, u.buf, self.T - 1, self.k_new[l], self.v_new[l], 1, stream)
+            if self.rows is not None:
+                B.kvq_append_ragged(u.cfg, u.buf, [t - 1 for t in self.rows], [1] * len(self.rows),
+                                    self.k_new[l], self.v_new[l], stream)
+            else:
+                B.kvq_append(u.cfg, u.buf, self.T - 1, self.k_new[l], self.v_new[l], 1, stream)
         for l in range(self.L):
             self.decode_layer(l, stream)
 
     def decode(self, i: int, stream):
         u, l = self.units[i], self.unit_layer[i]
+        if self.rows is not None:
+            self.binding.kvq_decode_attn_ragged(u.cfg, u.buf, self.rows, self.q[l], self.out[l], None, self.ws,
+                                                None, stream)
+            return
         self.binding.kvq_decode_attn(u.cfg, u.buf, self.T, self.q[l], self.out[l], None, self.ws, None, stream)
+
+    def unit_bytes(self, i: int) -> int:
+        return algorithmic_bytes(self.cfgs[i], self.T, self.rows)
 
     def decode_layer(self, l: int, stream):
         if self.mixed[l] is not None:  # its pairs' caches side by side (fork / join on side streams)
@@ -279,7 +299,7 @@ class Model:
                 self.decode(i, stream)
 
     def decode_bytes(self):
-        return sum(algorithmic_bytes(c, self.T) for c in self.cfgs)
+        return sum(self.unit_bytes(i) for i in range(len(self.cfgs)))
 
     def launches_per_step(self):
         """Kernel launches of one step: per decode unit the 1-token append's
@@ -288,8 +308,8 @@ class Model:
         n = 0
         for c in self.cfgs:
             n += 1  # fp16 window copy of the appended token
-            if window_counts(c, self.T)[1] > window_counts(c, self.T - 1)[1]:
-                n += 1  # the append flushes one 32-token group
+            if any(window_counts(c, t)[1] > window_counts(c, t - 1)[1] for t in (self.rows or [self.T])):
+                n += 1  # the append flushes one 32-token group (of some row)
             n += 1  # decode
         return n
 
@@ -426,7 +446,7 @@ def _time_mixed_layers(model, stream, steps: int, warmup: int):
         e1.record(stream)
     torch.cuda.synchronize()
     layer_ms = e0.elapsed_time(e1) / (steps * model.L)
-    b = [algorithmic_bytes(c, model.T) for c in model.cfgs]
+    b = [model.unit_bytes(i) for i in range(len(model.cfgs))]
     lb = [0] * model.L
     for i, l in enumerate(model.unit_layer):
         lb[l] += b[i]
@@ -620,6 +640,18 @@ def _oracle_streams(name: str):
     return _ORACLE_STREAMS[name]
 
 
+def _ragged_scale(name: str):
+    """(factor, note) turning a full-context stream decode into the mean row's
+    of a ragged workload (the oracle's decode time grows linearly with T)."""
+    from bit_kv_cache_07_gb300 import workloads
+    rows = workloads.row_tokens(name)
+    if rows is None:
+        return 1.0, ""
+    T = workloads.WORKLOADS[name]["tokens"]
+    f = statistics.mean(rows) / T
+    return f, f"; rows of different lengths: the full-context stream time scaled by their mean length / T = {f:.3f}"
+
+
 def oracle_sample(name: str, seconds: float, layer_count: int | None = None):
     """Time the CPU oracle (single thread, as written) decoding whole streams of
     layer 0 at the workload's context until ~seconds have passed; scale the
@@ -637,14 +669,15 @@ def oracle_sample(name: str, seconds: float, layer_count: int | None = None):
         spent += time.perf_counter() - t0
         n += 1
     streams_per_step = w["layers"] * w["batch"] * w["n_kv_heads"]
+    rf, rnote = _ragged_scale(name)
     per_stream = spent / n
     return {
         "streams": n, "seconds": spent,
-        "value": per_stream * streams_per_step * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "value": per_stream * rf * streams_per_step * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
         "sample": f"fp64 oracle decode of {n} (batch row, KV head) streams of layer 0 at T={T} "
                   f"(cycling over {nstore} prebuilt streams), "
                   f"{per_stream * 1e3:.1f} ms each, scaled x{streams_per_step / n:.0f} to one "
-                  f"{w['layers']}-layer step; cache build not timed",
+                  f"{w['layers']}-layer step; cache build not timed" + rnote,
     }
 
 
@@ -694,11 +727,12 @@ def oracle_sample_all_cores(name: str, seconds: float, procs: int | None = None)
     n = sum(r[0] for r in res)
     wall = max(r[1] for r in res)
     streams_per_step = w["layers"] * w["batch"] * w["n_kv_heads"]
+    rf, rnote = _ragged_scale(name)
     return {
-        "value": wall / n * streams_per_step * 1e6, "unit": UNIT, "cores": procs, "kind": "oracle",
+        "value": wall / n * rf * streams_per_step * 1e6, "unit": UNIT, "cores": procs, "kind": "oracle",
         "sample": f"{procs} spawned processes, each decoding one prebuilt stream of layer 0 at "
                   f"T={w['tokens']} for ~{seconds:.0f} s: {n} streams in {wall:.1f} s of wall time, "
-                  f"scaled to one {w['layers']}-layer step; cache build not timed",
+                  f"scaled to one {w['layers']}-layer step; cache build not timed" + rnote,
     }
 
 
@@ -758,7 +792,7 @@ def decode_roofline(model, per_layer_ms, peak, peak_kind, workload):
     """Roofline object of the decode launches of one step (in-graph times),
     plus a per-(K, V)-pair breakdown when the layers differ."""
     names = model.kernel_names()
-    layer_bytes = [algorithmic_bytes(c, model.T) for c in model.cfgs]
+    layer_bytes = [model.unit_bytes(i) for i in range(len(model.cfgs))]
     total_b, total_ms = sum(layer_bytes), sum(per_layer_ms)
     achieved = total_b / (total_ms * 1e-3) / 1e9
     traffic = [ncu_traffic(f"decode:{workload}:{_pair_name(c)}") for c in model.cfgs]
@@ -830,6 +864,7 @@ def main():
     e2e_ms = max_over_ranks(e2e_ms)
     launches = model.launches_per_step() * args.steps
     model_layers, model_T = model.L, model.T
+    model_kernels, model_rows = sorted(set(model.kernel_names())), model.rows
     head_pairs = model.head_pairs or None
     del model
     torch.cuda.empty_cache()
@@ -866,12 +901,16 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16xf16->f32 (tensor cores) on u8-packed codes", "data": "synthetic",
+        "vs_baseline": None, "data": "synthetic",
+        "dtype": ("f32 (CUDA cores) on u8-packed codes" if all(k.startswith("decode_kernel<") for k in model_kernels)
+                  else "f16xf16->f32 (tensor cores) on u8-packed codes"),
         "config": {"workload": args.workload, "layers": model_layers, "batch": w["batch"],
                    "q_heads": w["n_q_heads"], "kv_heads": w["n_kv_heads"], "head_dim": w["head_dim"],
                    "context": model_T, "cache": w["pairs"], "n_sink": w["n_sink"], "n_recent": w["n_recent"],
                    "l2": "inputs larger than L2: %.2f GB of cache read per step" % (dec_bytes / 1e9),
-                   "step": "per layer: kvq_append of 1 token + kvq_decode_attn",
+                   "step": ("per layer: kvq_append_ragged of 1 token per row + kvq_decode_attn_ragged"
+                            if model_rows else "per layer: kvq_append of 1 token + kvq_decode_attn"),
+                   "rows": ({"lengths": model_rows, "mean": statistics.mean(model_rows)} if model_rows else None),
                    "timing": (f"one step captured in a CUDA graph; median over {rounds} timed rounds of "
                               f"exactly {args.steps} replays" if g_ms is not None else
                               "eager launches (" + str(g_err) + ")")},

@@ -46,18 +46,19 @@ class kvq_region(C.Structure):
 
 _REGIONS_HEAD = ["k_codes", "k_scales", "v_codes", "v_scales", "k_sink", "v_sink", "k_ring", "v_ring",
                  "k_csr_rowptr", "k_csr_col", "k_csr_val", "v_csr_rowptr", "v_csr_col", "v_csr_val"]
-REGIONS = _REGIONS_HEAD + ["k_norm"]
+REGIONS = _REGIONS_HEAD + ["k_norm", "rows"]
 
 
 class kvq_layout(C.Structure):
     _fields_ = [(n, kvq_region) for n in _REGIONS_HEAD] + [
         ("layer_bytes", C.c_uint64), ("workspace_bytes", C.c_uint64), ("max_splits", C.c_int32),
-        ("ring_slots", C.c_int32), ("q_cap", C.c_int32), ("k_norm", kvq_region)]
+        ("ring_slots", C.c_int32), ("q_cap", C.c_int32), ("k_norm", kvq_region), ("rows", kvq_region)]
 
 
 EXPORTS = ["kvq_layout_query", "kvq_append", "kvq_decode_attn", "kvq_decode_plan",
            "kvq_decode_path", "kvq_status_string", "kvq_decode_attn_noalloc", "kvq_context_shard",
-           "kvq_merge_attn", "kvq_fit_nuq_lut", "kvq_measure_distortion", "kvq_rate_allocate"]
+           "kvq_merge_attn", "kvq_fit_nuq_lut", "kvq_measure_distortion", "kvq_rate_allocate",
+           "kvq_append_ragged", "kvq_decode_attn_ragged"]
 NUQ_FIT_WORKSPACE_BYTES = 3 * 65538 * 8
 
 _lib = None
@@ -105,6 +106,11 @@ def lib():
         L.kvq_rate_allocate.restype = C.c_int
         L.kvq_decode_attn_noalloc.argtypes = [C.POINTER(kvq_config), vp, C.c_int32, u16p, u16p, vp, vp]
         L.kvq_decode_attn_noalloc.restype = C.c_int
+        i32p = C.POINTER(C.c_int32)
+        L.kvq_append_ragged.argtypes = [C.POINTER(kvq_config), vp, i32p, i32p, u16p, u16p, C.c_int32, vp]
+        L.kvq_append_ragged.restype = C.c_int
+        L.kvq_decode_attn_ragged.argtypes = [C.POINTER(kvq_config), vp, i32p, u16p, u16p, vp, vp, C.c_uint64, vp]
+        L.kvq_decode_attn_ragged.restype = C.c_int
         L.kvq_status_string.argtypes = [C.c_int]
         L.kvq_status_string.restype = C.c_char_p
         _lib = L
@@ -243,6 +249,46 @@ def kvq_decode_attn(cfg, layer_buf, tokens: int, q, out, lse=None, workspace=Non
     _check("kvq_decode_attn", st)
 
 
+def _rows(values, batch: int, what: str):
+    """A host int32 array of one value per batch row."""
+    vals = [int(v) for v in values]
+    if len(vals) != batch:
+        raise ValueError(f"{what}: one value per batch row ({batch}), got {len(vals)}")
+    return (C.c_int32 * batch)(*vals)
+
+
+def kvq_append_ragged(cfg, layer_buf, tokens_before, n_new, k_new, v_new, stream=None):
+    """Row b appends n_new[b] tokens (the first of its k_new / v_new rows,
+    [B, Hkv, n_stride, d]) after tokens_before[b]."""
+    import torch
+    c = _cfg(cfg)
+    lay = kvq_layout_query(c)
+    n_stride = int(k_new.shape[2])
+    row = c.batch * _totals(c)[0] * n_stride * c.head_dim * 2
+    st = lib().kvq_append_ragged(C.byref(c), _ptr(layer_buf, "layer_buf", numel=lay.layer_bytes),
+                                 _rows(tokens_before, c.batch, "tokens_before"), _rows(n_new, c.batch, "n_new"),
+                                 _ptr(k_new, "k_new", torch.float16, row), _ptr(v_new, "v_new", torch.float16, row),
+                                 n_stride, _stream(stream))
+    _check("kvq_append_ragged", st)
+
+
+def kvq_decode_attn_ragged(cfg, layer_buf, tokens, q, out, lse=None, workspace=None, ws_bytes=None, stream=None):
+    """Attention of batch row b over its own tokens[b] tokens."""
+    import torch
+    c = _cfg(cfg)
+    lay = kvq_layout_query(c)
+    hq = _totals(c)[1]
+    nq = c.batch * hq * c.head_dim * 2
+    if ws_bytes is None:
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().kvq_decode_attn_ragged(
+        C.byref(c), _ptr(layer_buf, "layer_buf", numel=lay.layer_bytes), _rows(tokens, c.batch, "tokens"),
+        _ptr(q, "q", torch.float16, nq), _ptr(out, "out", torch.float16, nq),
+        _ptr(lse, "lse", torch.float32, c.batch * hq * 4, allow_none=True),
+        _ptr(workspace, "workspace", allow_none=True), int(ws_bytes), _stream(stream))
+    _check("kvq_decode_attn_ragged", st)
+
+
 def kvq_decode_attn_noalloc(cfg, layer_buf, tokens: int, q, out, lse=None, stream=None):
     """kvq_decode_attn for callers that cannot allocate: the split-K scratch
     is the library's own fixed 8 MiB device array (see include/kvq.h)."""
@@ -370,6 +416,12 @@ class Layer:
 
     def decode(self, tokens: int, q, out, lse=None, workspace=None, stream=None):
         kvq_decode_attn(self.cfg, self.buf, tokens, q, out, lse, workspace, None, stream)
+
+    def append_ragged(self, tokens_before, n_new, k_new, v_new, stream=None):
+        kvq_append_ragged(self.cfg, self.buf, tokens_before, n_new, k_new, v_new, stream)
+
+    def decode_ragged(self, tokens, q, out, lse=None, workspace=None, stream=None):
+        kvq_decode_attn_ragged(self.cfg, self.buf, tokens, q, out, lse, workspace, None, stream)
 
 
 def new_workspace(cfg, device="cuda"):

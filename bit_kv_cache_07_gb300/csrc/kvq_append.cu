@@ -16,6 +16,8 @@
 // The fp32 quantizer is evaluated with explicitly rounded intrinsics
 // (__fsub_rn, __fdiv_rn, rintf) so that no operation is contracted or
 // approximated: codes and scales are bit-reproducible.
+#include <cstring>
+
 #include "kvq_internal.cuh"
 
 namespace kvq {
@@ -314,8 +316,10 @@ __device__ __forceinline__ void pack_rows(const uint8_t (*codes)[kHeadDim], int 
 template <int KM, int KB, int VB>
 __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_constant__ AppendParams p) {
   const Geometry& G = p.geo;
-  const int grp = p.first_group + blockIdx.x;
   const int s = blockIdx.y;
+  const RowAppend ra = row_append(p, s);
+  if ((int)blockIdx.x >= (ra.nq_after - ra.nq_before) / kGroupTokens) return;  // (ragged) no such group here
+  const int grp = ra.first_group + blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
 
   __shared__ __align__(16) uint16_t sK[kGroupTokens][kRowHalves];
@@ -336,8 +340,8 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
       const int r = idx / kRowVec, ch = idx % kRowVec;
       const int t = G.S + grp * kGroupTokens + r;
       const uint16_t *srck, *srcv;
-      if (t >= p.tokens_before) {
-        const size_t off = (in_stream(G, s) * p.n_new + (t - p.tokens_before)) * kRowHalves;
+      if (t >= ra.before) {
+        const size_t off = (in_stream(G, s) * p.n_new + (t - ra.before)) * kRowHalves;
         srck = p.k_new + off;
         srcv = p.v_new + off;
       } else {
@@ -478,17 +482,24 @@ __global__ void __launch_bounds__(kThreads) append_quantize_kernel(const __grid_
 // stream) fold the block's max |K_c| into the stream's slot with an integer
 // atomic max (non-negative floats order like their bit patterns: the max is
 // exact in any order), then one thread per (stream, channel) turns the max
-// into the power of two, in place.  The slots start at zero (memset).
+// into the power of two, in place.  The slots start at zero.  Only streams
+// whose row appends into an empty cache take part (every stream but for a
+// ragged append).
 __device__ __forceinline__ __half2 u32_as_half2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
 // In the max pass thread t reads 16-byte pieces (channels 8 (t mod 16) ..
 // + 7) of every 8th row from row t / 16 on, keeps the maxima of |x| as fp16
 // pairs (exact), and the 8 row slots of a channel meet in shared memory.
 constexpr int kNormTokens = 256;  // tokens per CTA of the max pass
+__global__ void __launch_bounds__(kHeadDim) key_norm_zero_kernel(const __grid_constant__ AppendParams p) {
+  if (row_append(p, blockIdx.x).before == 0) p.L.k_norm[(size_t)blockIdx.x * kHeadDim + threadIdx.x] = 0.0f;
+}
 __global__ void __launch_bounds__(kHeadDim) key_norm_max_kernel(const __grid_constant__ AppendParams p) {
   __shared__ float part[8][kHeadDim];
   const int s = blockIdx.y, tid = threadIdx.x, piece = tid & 15, row = tid >> 4;
-  const int t0 = blockIdx.x * kNormTokens, t1 = min(p.n_new, t0 + kNormTokens);
+  const RowAppend ra = row_append(p, s);
+  if (ra.before != 0) return;
+  const int t0 = blockIdx.x * kNormTokens, t1 = min(ra.n, t0 + kNormTokens);
   const uint4* k = reinterpret_cast<const uint4*>(p.k_new + in_stream(p.geo, s) * p.n_new * kRowHalves) + piece;
   __half2 m[4];
 #pragma unroll
@@ -514,6 +525,7 @@ __global__ void __launch_bounds__(kHeadDim) key_norm_max_kernel(const __grid_con
   atomicMax(reinterpret_cast<unsigned int*>(&p.L.k_norm[(size_t)s * kHeadDim + tid]), __float_as_uint(mc));
 }
 __global__ void __launch_bounds__(kHeadDim) key_norm_pow2_kernel(const __grid_constant__ AppendParams p) {
+  if (row_append(p, blockIdx.x).before != 0) return;
   float* slot = &p.L.k_norm[(size_t)blockIdx.x * kHeadDim + threadIdx.x];
   const float m = *slot;
   float n = 1.0f;
@@ -530,23 +542,10 @@ __global__ void __launch_bounds__(kHeadDim) key_norm_pow2_kernel(const __grid_co
 // window) into their slots.  One thread per 16-byte chunk of a K or V row,
 // over those tokens only: the call's tokens j < a (sinks; every token of an
 // fp16 cache) and j >= b (past the quantized part).
-__host__ __device__ __forceinline__ void window_split(const AppendParams& p, int* a, int* b) {
-  const Geometry& G = p.geo;
-  if (G.fp16_mode) {
-    *a = *b = p.n_new;
-    return;
-  }
-  auto clamp = [](int x, int lo, int hi) { return x < lo ? lo : x > hi ? hi : x; };
-  *a = clamp(G.S - p.tokens_before, 0, p.n_new);
-  *b = clamp(G.S + p.nq_after - p.tokens_before, *a, p.n_new);
-}
-__global__ void __launch_bounds__(256) append_window_kernel(const __grid_constant__ AppendParams p) {
+__global__ void __launch_bounds__(256) append_window_kernel(const __grid_constant__ AppendParams p, int ncopy) {
   const Geometry& G = p.geo;
   grid_dep_wait();     // earlier kernels may still read the ring slots written here
   grid_dep_trigger();  // the decode that follows may set up meanwhile
-  int a, b;
-  window_split(p, &a, &b);
-  const int ncopy = a + (p.n_new - b);
   const size_t total = (size_t)G.NS * ncopy * (2 * kRowVec);
   for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (size_t)gridDim.x * blockDim.x) {
@@ -555,8 +554,12 @@ __global__ void __launch_bounds__(256) append_window_kernel(const __grid_constan
     const size_t rest = idx / (2 * kRowVec);
     const int jc = (int)(rest % ncopy);
     const int s = (int)(rest / ncopy);
+    const RowAppend ra = row_append(p, s);
+    int a, b;
+    window_split(p, ra, &a, &b);
+    if (jc >= a + (ra.n - b)) continue;  // (ragged) this row copies fewer
     const int j = jc < a ? jc : b + (jc - a);
-    const int pos = p.tokens_before + j;
+    const int pos = ra.before + j;
     uint16_t* dst;
     if (G.fp16_mode) {
       dst = (isv ? p.L.v_ring : p.L.k_ring) + ((size_t)s * G.ring + pos) * kRowHalves;
@@ -923,8 +926,47 @@ cudaError_t launch_append_quantize(const AppendParams& p, int n_groups, cudaStre
   return done ? cudaGetLastError() : cudaErrorInvalidValue;
 }
 
+// A ragged append's per-row counts into the layer buffer's rows region
+// (read by the append kernels that follow on the stream).
+struct AppendRows {
+  int before[kMaxRaggedRows];
+  int n[kMaxRaggedRows];
+};
+__global__ void append_rows_kernel(const __grid_constant__ AppendRows r, int rows, int* dst) {
+  const int b = threadIdx.x;
+  if (b < rows) {
+    dst[b] = r.before[b];
+    dst[kMaxRaggedRows + b] = r.n[b];
+  }
+}
+cudaError_t launch_append_rows(const int32_t* before, const int32_t* n, int rows, int* dst, cudaStream_t st) {
+  AppendRows r;
+  std::memset(&r, 0, sizeof(r));
+  for (int b = 0; b < rows; ++b) {
+    r.before[b] = before[b];
+    r.n[b] = n[b];
+  }
+  append_rows_kernel<<<1, kMaxRaggedRows, 0, st>>>(r, rows, dst);
+  return cudaGetLastError();
+}
+
+// A ragged decode's row tables into the workspace (read by the decode that
+// follows on the stream, after its dependent-launch wait).
+__global__ void ragged_tables_kernel(const __grid_constant__ RaggedTables t, RaggedTables* dst) {
+  for (int i = threadIdx.x; i < kMaxRaggedRows + 1; i += blockDim.x) {
+    if (i < kMaxRaggedRows) dst->tokens[i] = t.tokens[i];
+    dst->j0[i] = t.j0[i];
+    dst->x0[i] = t.x0[i];
+  }
+}
+cudaError_t launch_ragged_tables(const RaggedTables& t, RaggedTables* dst, cudaStream_t st) {
+  ragged_tables_kernel<<<1, kMaxRaggedRows, 0, st>>>(t, dst);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_key_norm(const AppendParams& p, cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(p.L.k_norm, 0, sizeof(float) * (size_t)p.geo.NS * kHeadDim, st);
+  key_norm_zero_kernel<<<p.geo.NS, kHeadDim, 0, st>>>(p);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   key_norm_max_kernel<<<dim3((p.n_new + kNormTokens - 1) / kNormTokens, p.geo.NS), kHeadDim, 0, st>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -932,14 +974,12 @@ cudaError_t launch_key_norm(const AppendParams& p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_append_window(const AppendParams& p, cudaStream_t st) {
-  int a, b;
-  window_split(p, &a, &b);
-  const size_t total = (size_t)p.geo.NS * (a + (p.n_new - b)) * (2 * kRowVec);
+cudaError_t launch_append_window(const AppendParams& p, int ncopy, cudaStream_t st) {
+  const size_t total = (size_t)p.geo.NS * ncopy * (2 * kRowVec);
   size_t blocks = (total + 255) / 256;
   if (blocks > 152 * 64) blocks = 152 * 64;
   if (blocks < 1) blocks = 1;  // nothing to copy: the launch still keeps the dependent-launch chain
-  return launch_dependent(append_window_kernel, dim3((unsigned)blocks), dim3(256), 0, st, p);
+  return launch_dependent(append_window_kernel, dim3((unsigned)blocks), dim3(256), 0, st, p, ncopy);
 }
 
 }  // namespace kvq

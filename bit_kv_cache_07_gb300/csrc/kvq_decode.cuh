@@ -361,22 +361,27 @@ __device__ __forceinline__ void v_accumulate(const DecodeParams& p, DecodeSmem<G
 
 // fp16 token of index k in this split's fp16 token list -> (row pointer
 // offset in halves, absolute position).
-__device__ __forceinline__ size_t fp16_row(const DecodeParams& p, int s, int k, bool* in_sink, int* pos) {
+// S_eff, Nq: the stream's sinks present and quantized tokens.
+__device__ __forceinline__ size_t fp16_row_at(const DecodeParams& p, int s, int k, int S_eff, int Nq, bool* in_sink,
+                                              int* pos) {
   const Geometry& G = p.geo;
   if (G.fp16_mode) {
     *in_sink = false;
     *pos = k;
     return ((size_t)s * G.ring + k) * kHeadDim;
   }
-  if (k < p.S_eff) {
+  if (k < S_eff) {
     *in_sink = true;
     *pos = k;
     return ((size_t)s * G.S + k) * kHeadDim;
   }
-  const int ps = G.S + p.Nq + (k - p.S_eff);
+  const int ps = G.S + Nq + (k - S_eff);
   *in_sink = false;
   *pos = ps;
   return ((size_t)s * G.ring + (ps - G.S) % G.ring) * kHeadDim;
+}
+__device__ __forceinline__ size_t fp16_row(const DecodeParams& p, int s, int k, bool* in_sink, int* pos) {
+  return fp16_row_at(p, s, k, p.S_eff, p.Nq, in_sink, pos);
 }
 
 // One 32-token chunk of fp16 tokens (sinks / window, or an fp16 cache) for
@@ -387,7 +392,7 @@ __device__ __forceinline__ size_t fp16_row(const DecodeParams& p, int s, int k, 
 // compiles the RoPE path out (callers that never see pre-RoPE keys).
 template <int GQ, int KBATCH = 8, int VBATCH = 8, bool ROPE = true>
 __device__ __forceinline__ void fp16_chunk(const DecodeParams& p, const float (*sq)[kHeadDim],
-                                           float (*pbuf)[GQ], int s, int k0, int k1, int lane,
+                                           float (*pbuf)[GQ], int s, int k0, int k1, int se, int nq, int lane,
                                            float (&m)[GQ], float (&lsum)[GQ], float (&acc)[GQ][4],
                                            float (&macc)[GQ]) {
   const Geometry& G = p.geo;
@@ -398,7 +403,7 @@ __device__ __forceinline__ void fp16_chunk(const DecodeParams& p, const float (*
   if (k < k1) {
     bool sink;
     int pos;
-    const size_t off = fp16_row(p, s, k, &sink, &pos);
+    const size_t off = fp16_row_at(p, s, k, se, nq, &sink, &pos);
     const uint4* krow = reinterpret_cast<const uint4*>((sink ? p.L.k_sink : p.L.k_ring) + off);
 #pragma unroll
     for (int r = 0; r < GQ; ++r) z[r] = 0.0f;
@@ -463,7 +468,7 @@ __device__ __forceinline__ void fp16_chunk(const DecodeParams& p, const float (*
       if (t0 + i < n) {
         bool sink;
         int pos;
-        const size_t off = fp16_row(p, s, k0 + t0 + i, &sink, &pos);
+        const size_t off = fp16_row_at(p, s, k0 + t0 + i, se, nq, &sink, &pos);
         u[i] = __ldg(reinterpret_cast<const uint2*>((sink ? p.L.v_sink : p.L.v_ring) + off) + lane);
       }
     }
@@ -770,6 +775,12 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int sp = blockIdx.x, s = blockIdx.y;
   const int b = s / G.Hkv, hk = s % G.Hkv, g = G.g;
+  // this stream's tokens: the call's T, or its batch row's in a ragged call
+  int T_s = p.T, S_eff = p.S_eff, Nq = p.Nq, Wn = p.W;
+  if (p.ragged) {
+    T_s = p.row_tokens[b];
+    window_counts(G, T_s, &S_eff, &Nq, &Wn);
+  }
 
   for (int idx = tid; idx < GQ * kHeadDim; idx += kThreads) {
     const int r = idx / kHeadDim, c = idx % kHeadDim;
@@ -834,7 +845,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
 
   if constexpr (KB == 3) if (quant_split) {
     // staged: group grp + 4 (this warp's next) streams in while grp is computed
-    const int ngroups = p.Nq / kGroupTokens;
+    const int ngroups = Nq / kGroupTokens;
     const int g0 = sp * p.gps;
     const int g1 = min(ngroups, g0 + p.gps);
     const int sb = NuqStage::bytes(G.nout);
@@ -867,7 +878,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     cp_async_wait<0>();
   }
   if constexpr (KB != 16 && KB != 3) if (quant_split) {
-    const int ngroups = p.Nq / kGroupTokens;
+    const int ngroups = Nq / kGroupTokens;
     const int g0 = sp * p.gps;
     const int g1 = min(ngroups, g0 + p.gps);
     for (int grp = g0 + w; grp < g1; grp += 4) {
@@ -885,13 +896,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     int k0, k1;
     if (G.fp16_mode) {
       k0 = sp * p.fp16_tokens_per_split;
-      k1 = min(p.T, k0 + p.fp16_tokens_per_split);
+      k1 = min(T_s, k0 + p.fp16_tokens_per_split);
     } else {
       k0 = 0;
-      k1 = p.S_eff + p.W;
+      k1 = S_eff + Wn;
     }
     for (int c0 = k0 + 32 * w; c0 < k1; c0 += 32 * 4)
-      fp16_chunk<GQ>(p, sm.q, sm.p[w], s, c0, k1, lane, m, lsum, acc, macc);
+      fp16_chunk<GQ>(p, sm.q, sm.p[w], s, c0, k1, S_eff, Nq, lane, m, lsum, acc, macc);
   }
 
   // ---- combine the 4 warps of this CTA

@@ -877,7 +877,7 @@ __device__ __forceinline__ void process_group(const float (*qw)[kHeadDim], MmaWa
 // swizzled: K chunk c of row t at c ^ 4(t & 1) (the fragment loads of a
 // quarter warp read rows 2i, 2i+1), V chunk c at c ^ (t & 7) (ldmatrix
 // reads one chunk of 8 consecutive rows).
-constexpr int kF16Tokens = 8;
+constexpr int kF16Tokens = kPersistF16Tokens;
 
 struct F16Geom {
   static constexpr int KC = 0;
@@ -903,7 +903,8 @@ __device__ __forceinline__ void mma1688(float (&d)[4], uint32_t a0, uint32_t a1,
 // Queue the copies of fp16 item (stream s, first fp16 token kk0; tokens at
 // or past k1 are zero-filled).  Lanes 0-15 copy the even tokens' rows,
 // lanes 16-31 the odd ones', one 16-byte chunk of K and of V each.
-__device__ __forceinline__ void issue_f16(const DecodeParams& p, int s, int kk0, int k1, uint32_t dst, int lane) {
+__device__ __forceinline__ void issue_f16(const DecodeParams& p, int s, int kk0, int k1, int S_eff, int Nq,
+                                          uint32_t dst, int lane) {
   const int c = lane & 15;
 #pragma unroll
   for (int n = 0; n < kF16Tokens / 2; ++n) {
@@ -912,7 +913,7 @@ __device__ __forceinline__ void issue_f16(const DecodeParams& p, int s, int kk0,
     const bool valid = kk < k1;
     bool sink;
     int pos;
-    const size_t off = fp16_row(p, s, valid ? kk : kk0, &sink, &pos);
+    const size_t off = fp16_row_at(p, s, valid ? kk : kk0, S_eff, Nq, &sink, &pos);
     const uint16_t* kr = (sink ? p.L.k_sink : p.L.k_ring) + off;
     const uint16_t* vr = (sink ? p.L.v_sink : p.L.v_ring) + off;
     cp_async16_zfill(dst + F16Geom::KC + kf16_off(t, c), kr + 8 * c, valid);

@@ -288,6 +288,7 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT, IQ>::kCtaThreads
 
   const int gw = blockIdx.x * LY::kWarps + w;  // global warp index
   if (gw >= p.nwarps) return;
+  if (p.ragged) grid_dep_wait();  // the row tables were written by the kernel before
   const long long j0 = first_item_at(p, warp_x(p, gw));
   const long long j1 = first_item_at(p, warp_x(p, gw + 1));
   if (j0 >= j1) return;
@@ -310,25 +311,27 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT, IQ>::kCtaThreads
   };
   reset();
 
-  const int n_items = p.n_items, ng = LY::kQuant ? p.ng : 0;
-  const int k1 = p.S_eff + p.W;  // fp16 tokens of a stream
-  // current item (s, k) and the next item to queue (is, ik, ij); all advance incrementally
-  int s = (int)idiv(j0, n_items, p.fd_n_items);
-  int k = (int)(j0 - (long long)s * n_items);
+  // current item (s, k) and the next item to queue (is, ik, ij); all advance
+  // incrementally, each with its stream's counts (sp, isp: quantized groups,
+  // items, fp16 tokens), refreshed when it moves to the next stream
+  int s, k;
+  locate_item(p, j0, &s, &k);
+  StreamSpan sp = stream_span(p, s);
   int is = s, ik = k;
+  StreamSpan isp = sp;
   long long ij = j0;
   auto issue_next = [&](int stage) {
     if (ij < j1) {
       const uint32_t dst = st0_s + stage * LY::kStageBytes;
+      const int ng = LY::kQuant ? isp.ng : 0;
       if (LY::kQuant && ik < ng) {
         if constexpr (LY::kQuant) issue_group<KBq, VBq, IQ>(p, is, ik, dst, lane);
       } else {
-        issue_f16(p, is, kF16Tokens * (ik - ng), k1, dst, lane);
+        issue_f16(p, is, kF16Tokens * (ik - ng), isp.k1, isp.S_eff, isp.Nq, dst, lane);
       }
-      ++ij;
-      if (++ik == n_items) {
+      if (++ij < j1 && ++ik == isp.n_items) {
         ik = 0;
-        ++is;
+        isp = stream_span(p, ++is);
       }
     }
     cp_async_commit();
@@ -352,9 +355,9 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT, IQ>::kCtaThreads
   auto finish = [&](int sf) {
     if (has_q) stage_quant<VBq, NT, GT, JC>(p, sO, sML, g, lane, O, macc, m_used, lsum);
     staged = staged || has_q;
-    const long long first = (long long)sf * n_items;
-    const int wf = owner_of(p, item_pos(p, first));
-    const int wl = owner_of(p, item_pos(p, first + n_items - 1));
+    const StreamSpan fs = stream_span(p, sf);
+    const int wf = owner_of(p, item_pos(p, fs.first));
+    const int wl = owner_of(p, item_pos(p, fs.first + fs.n_items - 1));
     finalize_stream<NT, GT>(p, gw + sf, sf, wf, wl - wf + 1, sO, sML, staged, lane, O, m_used, lsum);
     reset();
     has_q = staged = bq_f16 = false;
@@ -394,6 +397,7 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT, IQ>::kCtaThreads
     cp_async_wait<LY::kStages - 1>();
     __syncwarp();
     const unsigned char* stc = st0 + cur * LY::kStageBytes;
+    const int ng = LY::kQuant ? sp.ng : 0;
     if (LY::kQuant && k < ng) {
       if constexpr (LY::kQuant) {
         process_group<KB, VB, NT, JC, GT, IQ>(qw, sm, iq, stc, g, lane, O, macc, m_used, lsum);
@@ -410,13 +414,14 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT, IQ>::kCtaThreads
           staged = true;
         }
       }
-      process_f16<NT>(sm, stc, g, lane, kF16Tokens * (k - ng), k1, O, m_used, lsum);
+      process_f16<NT>(sm, stc, g, lane, kF16Tokens * (k - ng), sp.k1, O, m_used, lsum);
     }
     __syncwarp();
     cur = (cur + 1 == LY::kStages) ? 0 : cur + 1;
-    if (++k == n_items) {
+    if (++k == sp.n_items) {
       k = 0;
       ++s;
+      if (j + 1 < j1) sp = stream_span(p, s);
     }
   }
   cp_async_wait<0>();

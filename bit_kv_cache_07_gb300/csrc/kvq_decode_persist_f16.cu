@@ -56,6 +56,9 @@ cudaError_t plan_persist(DecodeParams& p, uint64_t* ws_need) {
   p.wt = (long long)mma::kF16Tokens * kHeadDim * 2 * 2;
   p.wstream = (long long)p.ng * p.wq + (long long)p.nt * p.wt;
   p.wtot = (long long)G.NS * p.wstream;
+  long long items = (long long)G.NS * p.n_items;
+  bool any_groups = p.ng > 0;
+  if (p.ragged) plan_rows(p, &items, &any_groups);
   int sms = 0, occ = 0;
   cudaError_t e = device_sm_count(&sms);
   if (e != cudaSuccess) return e;
@@ -64,12 +67,11 @@ cudaError_t plan_persist(DecodeParams& p, uint64_t* ws_need) {
   if (e != cudaSuccess) return e;
   if (occ < 1) occ = 1;
   long long nw = (long long)sms * occ;  // occ: resident warps per SM
-  const long long items = (long long)G.NS * p.n_items;
   if (nw > items) nw = items;
   if (nw > (long long)kMaxQSplits * G.NS) nw = (long long)kMaxQSplits * G.NS;
   // every warp's weight range must hold at least one item start, so that the
   // warps counted for a stream are exactly the ones that work on it
-  const long long wmax = p.ng > 0 && p.wq > p.wt ? p.wq : p.wt;
+  const long long wmax = any_groups && p.wq > p.wt ? p.wq : p.wt;
   if (nw > p.wtot / wmax) nw = p.wtot / wmax;
   if (nw < 1) nw = 1;
   p.nwarps = (int)nw;

@@ -135,18 +135,7 @@ kvq_status make_geometry(const kvq_config* c, Geometry* g) {
 }
 
 // Sink tokens present, quantized tokens and window tokens at T tokens.
-void counts(const Geometry& g, int T, int* S_eff, int* Nq, int* W) {
-  if (g.fp16_mode) {
-    *S_eff = 0;
-    *Nq = 0;
-    *W = T;
-    return;
-  }
-  *S_eff = T < g.S ? T : g.S;
-  const int rest = T - g.S - g.R;
-  *Nq = rest > 0 ? kGroupTokens * (rest / kGroupTokens) : 0;
-  *W = T - *S_eff - *Nq;
-}
+void counts(const Geometry& g, int T, int* S_eff, int* Nq, int* W) { window_counts(g, T, S_eff, Nq, W); }
 
 kvq_status build_layout(const kvq_config* c, const Geometry& g, kvq_layout* L) {
   std::memset(L, 0, sizeof(*L));
@@ -174,12 +163,15 @@ kvq_status build_layout(const kvq_config* c, const Geometry& g, kvq_layout* L) {
   put(L->v_csr_col, nuq ? NS * Q * k : 0);
   put(L->v_csr_val, nuq ? NS * Q * k * 2 : 0);
   put(L->k_norm, g.knorm ? NS * d * 4 : 0);
+  put(L->rows, 2 * kMaxRaggedRows * 4);  // a ragged append's per-row counts
   L->layer_bytes = off;
   L->max_splits = kMaxQSplits + 1;
   L->ring_slots = g.ring;
   L->q_cap = g.qcap;
-  const uint64_t ws = align_up(NS * 4) + align_up(NS * (uint64_t)L->max_splits * g.g * 2 * 4) +
-                      NS * (uint64_t)L->max_splits * g.g * d * 4;
+  // split counters, partial (m, l) and accumulators, then a ragged decode's row tables
+  const uint64_t ws = align_up(align_up(NS * 4) + align_up(NS * (uint64_t)L->max_splits * g.g * 2 * 4) +
+                               NS * (uint64_t)L->max_splits * g.g * d * 4) +
+                      kRaggedTableBytes;
   L->workspace_bytes = ws;
   (void)c;
   return KVQ_OK;
@@ -202,6 +194,7 @@ void layer_ptrs(const kvq_layout& L, void* base, LayerPtrs* P) {
   P->v_col = (uint8_t*)at(L.v_csr_col);
   P->v_val = (uint16_t*)at(L.v_csr_val);
   P->k_norm = (float*)at(L.k_norm);
+  P->rows = (int*)at(L.rows);
 }
 
 // Split plan: how many splits cover `ngroups` 32-token groups of NS streams.
@@ -502,8 +495,108 @@ kvq_status kvq_append(const kvq_config* cfg, void* layer_buf, int32_t tokens_bef
   if (n_groups > 0) {
     if (launch_append_quantize(p, n_groups, cs) != cudaSuccess) return KVQ_ERR_CUDA;
   }
-  if (launch_append_window(p, cs) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (launch_append_window(p, window_copies_max(p), cs) != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
+}
+
+kvq_status kvq_append_ragged(const kvq_config* cfg, void* layer_buf, const int32_t* tokens_before,
+                             const int32_t* n_new, const uint16_t* k_new, const uint16_t* v_new, int32_t n_stride,
+                             kvq_stream_t stream) {
+  Geometry g;
+  kvq_status st = make_geometry(cfg, &g);
+  if (st != KVQ_OK) return st;
+  if (!layer_buf || !k_new || !v_new || !tokens_before || !n_new) return KVQ_ERR_INVALID_ARG;
+  if (g.B > kMaxRaggedRows) return KVQ_ERR_UNSUPPORTED;
+  if (n_stride < 1) return KVQ_ERR_INVALID_ARG;
+  int most = 0;
+  for (int b = 0; b < g.B; ++b) {
+    if (tokens_before[b] < 0 || n_new[b] < 0 || n_new[b] > n_stride) return KVQ_ERR_INVALID_ARG;
+    if ((int64_t)tokens_before[b] + n_new[b] > cfg->max_tokens) return KVQ_ERR_CAPACITY;
+    most = n_new[b] > most ? n_new[b] : most;
+  }
+  if (((uintptr_t)k_new | (uintptr_t)v_new | (uintptr_t)layer_buf) % 16) return KVQ_ERR_INVALID_ARG;
+  kvq_layout L;
+  build_layout(cfg, g, &L);
+
+  AppendParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.geo = g;
+  layer_ptrs(L, layer_buf, &p.L);
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.n_new = n_stride;
+  p.ragged = 1;
+  // plan on the host arrays, launch on their device copy in the layer buffer
+  p.row_before = tokens_before;
+  p.row_new = n_new;
+  bool any_first = false;
+  int n_groups = 0;
+  for (int b = 0; b < g.B; ++b) {
+    any_first = any_first || tokens_before[b] == 0;
+    const RowAppend ra = row_append(p, b * g.Hkv);
+    const int ng = (ra.nq_after - ra.nq_before) / kGroupTokens;
+    n_groups = ng > n_groups ? ng : n_groups;
+  }
+  const int ncopy = window_copies_max(p);
+  p.hadamard_c = (float)(1.0 / std::sqrt((double)kHeadDim));
+  for (int i = 0; i < 8; ++i) {
+    p.k_lut[i] = cfg->k_lut[i];
+    p.v_lut[i] = cfg->v_lut[i];
+  }
+  if (most == 0) return KVQ_OK;  // no row appends anything
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_append_rows(tokens_before, n_new, g.B, p.L.rows, cs) != cudaSuccess) return KVQ_ERR_CUDA;
+  p.row_before = p.L.rows;
+  p.row_new = p.L.rows + kMaxRaggedRows;
+  // InnerQ key normalisation of the rows that append into an empty cache
+  if (g.knorm && any_first && launch_key_norm(p, cs) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (n_groups > 0 && launch_append_quantize(p, n_groups, cs) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (launch_append_window(p, ncopy, cs) != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+kvq_status kvq_decode_attn_ragged(const kvq_config* cfg, const void* layer_buf, const int32_t* tokens,
+                                  const uint16_t* q, uint16_t* out, float* lse, void* workspace, uint64_t ws_bytes,
+                                  kvq_stream_t stream) {
+  if (!cfg || !tokens) return KVQ_ERR_INVALID_ARG;
+  if (cfg->batch < 1) return KVQ_ERR_INVALID_ARG;
+  if (cfg->batch > kMaxRaggedRows) return KVQ_ERR_UNSUPPORTED;
+  int T = 0;
+  for (int b = 0; b < cfg->batch; ++b) {
+    if (tokens[b] < 1) return KVQ_ERR_INVALID_ARG;
+    if (tokens[b] > cfg->max_tokens) return KVQ_ERR_CAPACITY;
+    T = tokens[b] > T ? tokens[b] : T;
+  }
+  DecodeParams p;
+  bool persistent = false;
+  uint64_t layout_ws = 0;
+  kvq_status st = decode_setup(cfg, layer_buf, T, q, out, lse, &p, &persistent, &layout_ws);
+  if (st != KVQ_OK) return st;
+  // the same kernel as kvq_decode_attn: the persistent schedule lays every
+  // stream's own items end to end; the split kernel is planned for the
+  // longest row and every stream takes its row's counts
+  // plan on host tables, launch on their copy in the workspace (behind the
+  // scratch the plan needs)
+  RaggedTables ht;
+  std::memset(&ht, 0, sizeof(ht));
+  for (int b = 0; b < cfg->batch; ++b) ht.tokens[b] = tokens[b];
+  p.ragged = 1;
+  p.row_tokens = ht.tokens;
+  p.row_j0 = ht.j0;
+  p.row_x0 = ht.x0;
+  if (!workspace || ws_bytes < layout_ws || ((uintptr_t)workspace % 16)) return KVQ_ERR_WORKSPACE;
+  uint64_t need = 0;
+  st = decode_plan_device(&p, persistent, &need);
+  if (st != KVQ_OK) return st;
+  const uint64_t tab_off = align_up(need);
+  if (ws_bytes < tab_off + kRaggedTableBytes) return KVQ_ERR_WORKSPACE;
+  RaggedTables* dt = reinterpret_cast<RaggedTables*>(static_cast<char*>(workspace) + tab_off);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_ragged_tables(ht, dt, cs) != cudaSuccess) return KVQ_ERR_CUDA;
+  p.row_tokens = dt->tokens;
+  p.row_j0 = dt->j0;
+  p.row_x0 = dt->x0;
+  return decode_launch(&p, persistent, workspace, cs);
 }
 
 kvq_status kvq_decode_attn(const kvq_config* cfg, const void* layer_buf, int32_t tokens,

@@ -19,6 +19,9 @@ constexpr int kMaxQSplits = 64;    // quantized split-K chunks per stream (decod
 constexpr int kMaxOutliers = 8;    // non-uniform outliers per vector
 constexpr int kMaxGQA = 8;         // query heads per KV head
 constexpr int kThreads = 128;      // threads per CTA of the append and split-decode kernels
+// Sequences of different lengths in one call (kvq_decode_attn_ragged,
+// kvq_append_ragged): at most this many batch rows.
+constexpr int kMaxRaggedRows = 256;
 
 // Geometry derived once on the host from a kvq_config.
 struct Geometry {
@@ -68,7 +71,25 @@ struct LayerPtrs {
   uint8_t* v_col;
   uint16_t* v_val;
   float* k_norm;        // [NS][d] InnerQ key normalisation
+  int* rows;            // [2][kMaxRaggedRows] a ragged append's per-row tokens before / appended
 };
+
+// Window rule at T tokens (host and device): sinks present, quantized
+// tokens (whole 32-token groups past the sinks, leaving at least R), and the
+// fp16 window; an fp16 cache keeps every token in its window.
+__host__ __device__ inline void window_counts(const Geometry& g, int T, int* S_eff, int* Nq, int* W) {
+  if (g.fp16_mode) {
+    *S_eff = 0;
+    *Nq = 0;
+    *W = T;
+    return;
+  }
+  *S_eff = T < g.S ? T : g.S;
+  const int rest = T - g.S - g.R;
+  *Nq = rest > 0 ? kGroupTokens * (rest / kGroupTokens) : 0;
+  *W = T - *S_eff - *Nq;
+}
+
 
 struct AppendParams {
   Geometry geo;
@@ -83,7 +104,65 @@ struct AppendParams {
   float hadamard_c;       // fp32(1/sqrt(d))
   float k_lut[8];
   float v_lut[8];
+  // ragged append: batch row b appends row_new[b] tokens (the first of its
+  // n_new input rows) after row_before[b] (device copies in the layer
+  // buffer at launch; host arrays while the host plans); n_new is then the
+  // inputs' token stride
+  int ragged;
+  const int* row_before;
+  const int* row_new;
 };
+
+// The append of batch row b (stream s = b Hkv + h): tokens before, tokens
+// appended, quantized tokens before and after, first group flushed.
+struct RowAppend {
+  int before, n, nq_before, nq_after, first_group;
+};
+__host__ __device__ inline RowAppend row_append(const AppendParams& p, int s) {
+  RowAppend r;
+  if (!p.ragged) {
+    r.before = p.tokens_before;
+    r.n = p.n_new;
+    r.nq_before = p.nq_before;
+    r.nq_after = p.nq_after;
+    r.first_group = p.first_group;
+    return r;
+  }
+  const int b = s / p.geo.Hkv;
+  r.before = p.row_before[b];
+  r.n = p.row_new[b];
+  int se, w;
+  window_counts(p.geo, r.before, &se, &r.nq_before, &w);
+  window_counts(p.geo, r.before + r.n, &se, &r.nq_after, &w);
+  r.first_group = r.nq_before / kGroupTokens;
+  return r;
+}
+
+// fp16 tokens a stream's append copies into sink / window slots: the call's
+// tokens j < a (sinks; every token of an fp16 cache) and j >= b (past the
+// quantized part).
+__host__ __device__ inline void window_split(const AppendParams& p, const RowAppend& ra, int* a, int* b) {
+  const Geometry& G = p.geo;
+  if (G.fp16_mode) {
+    *a = *b = ra.n;
+    return;
+  }
+  auto clamp = [](int x, int lo, int hi) { return x < lo ? lo : x > hi ? hi : x; };
+  *a = clamp(G.S - ra.before, 0, ra.n);
+  *b = clamp(G.S + ra.nq_after - ra.before, *a, ra.n);
+}
+// The most tokens any stream copies (the grid's token extent).
+__host__ __device__ inline int window_copies_max(const AppendParams& p) {
+  int most = 0;
+  const int rows = p.ragged ? p.geo.B : 1;
+  for (int r = 0; r < rows; ++r) {
+    const RowAppend ra = row_append(p, r * p.geo.Hkv);
+    int a, b;
+    window_split(p, ra, &a, &b);
+    most = max(most, a + (ra.n - b));
+  }
+  return most;
+}
 
 // Division by a divisor that is fixed for a launch, without a hardware
 // divide: floor(x / d) = (x * m) >> sh for 0 <= x < 2^56, where
@@ -146,7 +225,80 @@ struct DecodeParams {
   int nwarps;
   long long wq, wt, wstream, wtot;
   FastDiv fd_n_items, fd_wq, fd_wt, fd_wstream, fd_wtot, fd_nwarps;  // for idiv
+  // ragged decode: tokens of batch row b (T = their maximum); for the
+  // persistent schedule, the first item and the first weight position of
+  // row b's first stream (entry B: the totals).  Device copies in the
+  // workspace at launch (RaggedTables), host arrays while the host plans.
+  int ragged;
+  const int* row_tokens;
+  long long* row_j0;
+  long long* row_x0;
 };
+
+// A ragged decode's per-row tables, as the host builds them and as a copy
+// kernel writes them into the workspace (behind the split counters and
+// partial results).
+struct RaggedTables {
+  int tokens[kMaxRaggedRows];
+  long long j0[kMaxRaggedRows + 1];
+  long long x0[kMaxRaggedRows + 1];
+};
+constexpr uint64_t kRaggedTableBytes = (sizeof(RaggedTables) + 255) / 256 * 256;
+
+constexpr int kPersistF16Tokens = 8;  // fp16 tokens per item of the persistent schedule
+
+// One stream's part of the persistent schedule: its first item and weight
+// position, quantized groups, fp16 items and tokens, and the window counts
+// its fp16 tokens are addressed with.  Uniform calls: the same for every
+// stream; ragged ones: from the stream's batch row.
+struct StreamSpan {
+  long long first, x0, wstream;
+  int ng, nt, n_items, k1, S_eff, Nq;
+};
+__host__ __device__ inline StreamSpan row_span(const DecodeParams& p, int b) {
+  StreamSpan r;
+  int W;
+  window_counts(p.geo, p.row_tokens[b], &r.S_eff, &r.Nq, &W);
+  r.k1 = r.S_eff + W;
+  r.ng = p.geo.fp16_mode ? 0 : r.Nq / kGroupTokens;
+  r.nt = (r.k1 + kPersistF16Tokens - 1) / kPersistF16Tokens;
+  r.n_items = r.ng + r.nt;
+  r.wstream = (long long)r.ng * p.wq + (long long)r.nt * p.wt;
+  r.first = p.row_j0[b];
+  r.x0 = p.row_x0[b];
+  return r;
+}
+__host__ __device__ inline StreamSpan stream_span(const DecodeParams& p, int s) {
+  if (!p.ragged) {
+    StreamSpan r;
+    r.first = (long long)s * p.n_items;
+    r.x0 = (long long)s * p.wstream;
+    r.wstream = p.wstream;
+    r.ng = p.ng;
+    r.nt = p.nt;
+    r.n_items = p.n_items;
+    r.k1 = p.S_eff + p.W;
+    r.S_eff = p.S_eff;
+    r.Nq = p.Nq;
+    return r;
+  }
+  const int b = s / p.geo.Hkv, h = s - b * p.geo.Hkv;
+  StreamSpan r = row_span(p, b);
+  r.first += (long long)h * r.n_items;
+  r.x0 += (long long)h * r.wstream;
+  return r;
+}
+// Ragged schedule: the last row whose first entry in `tab` (row_j0 or
+// row_x0) is <= v (rows of a ragged call hold at least one item each).
+__host__ __device__ inline int row_at(const long long* tab, int rows, long long v) {
+  int lo = 0, hi = rows - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tab[mid] <= v) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
 
 // floor(x / d) for 0 <= x < 2^56: the device multiplies and shifts (a
 // 64-bit integer division is a long serial emulation there, and fp64 is a
@@ -161,14 +313,61 @@ __host__ __device__ inline long long idiv(long long x, long long d, const FastDi
 #endif
 }
 
+// Ragged persistent schedule (host): every row's first item and weight
+// position, the totals, and whether any stream holds quantized groups.
+inline void plan_rows(DecodeParams& p, long long* items, bool* any_groups) {
+  p.row_j0[0] = p.row_x0[0] = 0;
+  *any_groups = false;
+  for (int b = 0; b < p.geo.B; ++b) {
+    const StreamSpan r = row_span(p, b);
+    p.row_j0[b + 1] = p.row_j0[b] + (long long)p.geo.Hkv * r.n_items;
+    p.row_x0[b + 1] = p.row_x0[b] + (long long)p.geo.Hkv * r.wstream;
+    *any_groups = *any_groups || r.ng > 0;
+  }
+  *items = p.row_j0[p.geo.B];
+  p.wtot = p.row_x0[p.geo.B];
+}
+
 // Persistent-schedule arithmetic shared by host and device.
 // (Dividends stay below 2^56: plan_persist checks (wtot + 1) (nwarps + 1) < 2^56.)
+// Item j's stream s and index k within it.
+__host__ __device__ inline void locate_item(const DecodeParams& p, long long j, int* s, int* k) {
+  if (!p.ragged) {
+    const long long ss = idiv(j, p.n_items, p.fd_n_items);
+    *s = (int)ss;
+    *k = (int)(j - ss * p.n_items);
+    return;
+  }
+  const int b = row_at(p.row_j0, p.geo.B, j);
+  const StreamSpan r = row_span(p, b);
+  const long long h = (j - r.first) / r.n_items;
+  *s = b * p.geo.Hkv + (int)h;
+  *k = (int)(j - r.first - h * r.n_items);
+}
 __host__ __device__ inline long long item_pos(const DecodeParams& p, long long j) {
+  if (p.ragged) {
+    int s, k;
+    locate_item(p, j, &s, &k);
+    const StreamSpan r = stream_span(p, s);
+    return r.x0 + (k <= r.ng ? k * p.wq : r.ng * p.wq + (k - r.ng) * p.wt);
+  }
   const long long s = idiv(j, p.n_items, p.fd_n_items), k = j - s * p.n_items;
   return s * p.wstream + (k <= p.ng ? k * p.wq : p.ng * p.wq + (k - p.ng) * p.wt);
 }
 // First item whose start weight is >= x (x in [0, wtot]).
 __host__ __device__ inline long long first_item_at(const DecodeParams& p, long long x) {
+  if (p.ragged) {
+    if (x >= p.wtot) return p.row_j0[p.geo.B];
+    const int b = row_at(p.row_x0, p.geo.B, x);
+    const StreamSpan r = row_span(p, b);
+    const long long h = (x - r.x0) / r.wstream, rem = x - r.x0 - h * r.wstream;
+    const long long f = r.first + h * r.n_items;  // the stream's first item
+    if (rem == 0) return f;
+    long long k;
+    if (rem <= (long long)r.ng * p.wq) k = (rem + p.wq - 1) / p.wq;
+    else k = r.ng + (rem - (long long)r.ng * p.wq + p.wt - 1) / p.wt;
+    return f + k;  // k == n_items: the next stream's first item
+  }
   long long s = idiv(x, p.wstream, p.fd_wstream), rem = x - s * p.wstream, k;
   if (rem == 0) return s * p.n_items;
   if (rem <= p.ng * p.wq) k = idiv(rem + p.wq - 1, p.wq, p.fd_wq);
@@ -230,9 +429,9 @@ __host__ __device__ inline float anchor_turns(const float4& v, float c0, int g) 
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" :::); }
 
-template <typename Param>
-inline cudaError_t launch_dependent(void (*kernel)(Param), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                                    const Param& arg) {
+template <typename... Params, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                    const Args&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -243,7 +442,7 @@ inline cudaError_t launch_dependent(void (*kernel)(Param), dim3 grid, dim3 block
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, arg);
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 // Split kernel: raise the quantized splits (n_qsplit of n_split per stream,
@@ -339,7 +538,9 @@ cudaError_t launch_merge_attn(int n_parts, long long rows, const uint16_t* outs,
                               uint16_t* out, float* lse_out, cudaStream_t st);
 cudaError_t launch_append_quantize(const AppendParams& p, int n_groups, cudaStream_t st);
 cudaError_t launch_key_norm(const AppendParams& p, cudaStream_t st);
-cudaError_t launch_append_window(const AppendParams& p, cudaStream_t st);
+cudaError_t launch_append_window(const AppendParams& p, int ncopy, cudaStream_t st);
+cudaError_t launch_append_rows(const int32_t* before, const int32_t* n, int rows, int* dst, cudaStream_t st);
+cudaError_t launch_ragged_tables(const RaggedTables& t, RaggedTables* dst, cudaStream_t st);
 // Split-K decode; with occ != nullptr it only reports the kernel's resident
 // CTAs per SM (for sizing the grid) and launches nothing.
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, int* occ = nullptr);

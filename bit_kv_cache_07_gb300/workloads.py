@@ -64,6 +64,13 @@ WORKLOADS = {
         _BASE, layers=32, batch=16, n_q_heads=32, n_kv_heads=8, tokens=32768,
         pairs="rateq", rateq_avg_bits=4.0, rateq_calib_tokens=2048, n_sink=4, n_recent=128, head_spread=4.0,
         k_dist="normal", k_outlier_channels="random3", k_outlier_scale=8.0, v_dist="laplace"),
+    # sequences of different lengths in one batch (a serving batch of
+    # requests at different positions): KV4 at the Llama-3-8B shape, batch
+    # row b at its own length drawn uniformly from [8192, 32768]
+    "llama3_8b_kv4_ragged_t32k": dict(
+        _BASE, layers=32, batch=16, n_q_heads=32, n_kv_heads=8, tokens=32768,
+        pairs="KV4", n_sink=4, n_recent=128, ragged_min_tokens=8192,
+        k_dist="normal", k_outlier_channels="random3", k_outlier_scale=8.0, v_dist="laplace"),
     "llama7b_nuq3_t1m": dict(
         _BASE, layers=1, batch=1, n_q_heads=32, n_kv_heads=32, tokens=1048576,
         pairs="NUQ3", k_pre_rope=1, outliers_per_vector=2, lut="fitted", lut_calib_tokens=2048,
@@ -73,7 +80,7 @@ WORKLOADS = {
 # order of the workloads as listed with the method's benchmark
 WORKLOAD_ORDER = ["toy_k4v2_t1k", "llama2_7b_kv4_t4k", "llama3_8b_mixed_t32k",
                   "qwen_gqa_hadamard_t8k", "llama7b_nuq3_t1m", "llama3_8b_innerq_kv4_t32k",
-                  "llama3_8b_rateq_t32k", "llama3_8b_mixed_innerq_t32k"]
+                  "llama3_8b_rateq_t32k", "llama3_8b_mixed_innerq_t32k", "llama3_8b_kv4_ragged_t32k"]
 
 
 def layer_pairs(name: str) -> list[str]:
@@ -112,6 +119,21 @@ def layer_config(name: str, layer: int, max_tokens: int | None = None,
     cfg["k_lut"] = list(k_lut) if k_lut is not None else [0.0] * 8
     cfg["v_lut"] = list(v_lut) if v_lut is not None else [0.0] * 8
     return cfg
+
+
+def row_tokens(name: str, tokens: int | None = None) -> list[int] | None:
+    """Per batch row lengths of a ragged workload at its decode step (the
+    longest row has `tokens`, default the workload's context; the others are
+    drawn uniformly from [ragged_min_tokens scaled alike, tokens] by
+    numpy default_rng(1)), or None for a uniform workload."""
+    w = WORKLOADS[name]
+    if "ragged_min_tokens" not in w:
+        return None
+    T = w["tokens"] if tokens is None else tokens
+    lo = max(1, w["ragged_min_tokens"] * T // w["tokens"])
+    rows = np.random.default_rng(1).integers(lo, T + 1, w["batch"])
+    rows[0] = T
+    return [int(r) for r in rows]
 
 
 def fp16_baseline_config(cfg: dict) -> dict:

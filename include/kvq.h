@@ -200,6 +200,7 @@ typedef struct kvq_layout {
     int32_t ring_slots;       /* RING                                           */
     int32_t q_cap;            /* Qcap                                           */
     kvq_region k_norm;        /* InnerQ key normalisation (0 bytes if unused)   */
+    kvq_region rows;          /* a ragged append's per-row counts (2 KB)        */
 } kvq_layout;
 
 /* kvq_layout_query -- host only, no CUDA call.
@@ -275,6 +276,38 @@ kvq_status kvq_decode_plan(const kvq_config *cfg, int32_t tokens, int32_t *split
  * KV head the kernel is instantiated for (1, 2, 4 or 8).
  * Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CAPACITY. */
 kvq_status kvq_decode_path(const kvq_config *cfg, int32_t tokens, int32_t *persistent, int32_t *gq_slots);
+
+/* kvq_append_ragged -- kvq_append for sequences of different lengths.
+ * The pages attend one context length per call; a batch of sequences at
+ * different positions (requests that started at different times, prompts
+ * of different lengths) takes this call instead.  Batch row b appends
+ * n_new[b] tokens after tokens_before[b] (0 = empty row; n_new[b] = 0 leaves
+ * the row as it is); each row follows the same window rule as kvq_append.
+ *   tokens_before, n_new  host int32 [batch]; tokens_before[b] >= 0,
+ *                         0 <= n_new[b] <= n_stride,
+ *                         tokens_before[b] + n_new[b] <= max_tokens
+ *   k_new, v_new          device fp16 [B][Hkv][n_stride][d]: row b's tokens
+ *                         are the first n_new[b] of its n_stride slots
+ *   n_stride              >= 1, the inputs' token dimension
+ * InnerQ key normalisation (k_channel_norm) is fixed per row by the row's
+ * first append into its empty cache (tokens_before[b] = 0).
+ * Errors: as kvq_append; KVQ_ERR_UNSUPPORTED when batch > 256. */
+kvq_status kvq_append_ragged(const kvq_config *cfg, void *layer_buf, const int32_t *tokens_before,
+                             const int32_t *n_new, const uint16_t *k_new, const uint16_t *v_new,
+                             int32_t n_stride, kvq_stream_t stream);
+
+/* kvq_decode_attn_ragged -- kvq_decode_attn for sequences of different
+ * lengths: batch row b attends over its own tokens[b] tokens.
+ *   tokens     host int32 [batch], 1 <= tokens[b] <= max_tokens
+ *   other arguments as kvq_decode_attn.
+ * Runs the kernel kvq_decode_attn would: the persistent kernel lays every
+ * stream's own work items end to end and cuts them into equal byte ranges;
+ * the split-K kernel is planned for the longest row (a stream's splits past
+ * its own tokens contribute nothing).
+ * Errors: as kvq_decode_attn; KVQ_ERR_UNSUPPORTED when batch > 256. */
+kvq_status kvq_decode_attn_ragged(const kvq_config *cfg, const void *layer_buf, const int32_t *tokens,
+                                  const uint16_t *q, uint16_t *out, float *lse,
+                                  void *workspace, uint64_t ws_bytes, kvq_stream_t stream);
 
 /* kvq_decode_attn_noalloc -- kvq_decode_attn without a caller workspace.
  * The pages have no counterpart: this exists for callers that cannot

@@ -1,7 +1,8 @@
 // Host-side check of the persistent decode's work schedule: every item has
 // exactly one owner warp, no warp range is empty under the launch cap, the
 // owner formula agrees with the ranges, and the (warp, stream) slots are
-// distinct and in bounds.  Also checks the device's division by a launch
+// distinct and in bounds -- for batches of one length and for ragged ones
+// (rows of different lengths).  Also checks the device's division by a launch
 // constant (fastdiv_mulshift: multiply by a rounded-up reciprocal, shift)
 // against exact integer division, and the fp32 RoPE group anchors
 // (anchor_turns) against the fp64 angle.  Built and run by
@@ -40,6 +41,81 @@ int main() {
         int wf = owner_of(p, item_pos(p, (long long)s * p.n_items)), wl = owner_of(p, item_pos(p, (long long)s * p.n_items + p.n_items - 1));
         if ((int)ws.size() != wl - wf + 1) { printf("count mismatch s=%d\n", s); ++bad; }
         for (int w : ws) { if (!slots.insert(w + s).second) { printf("slot clash\n"); ++bad; } if (w + s >= nw + NS) ++bad; }
+      }
+    }
+  }
+  // ragged batches: rows of different lengths, every row's streams laid end
+  // to end with their own item counts; the same properties per stream
+  {
+    unsigned long long rs = 1234567ull;
+    auto rr = [&]() { rs ^= rs << 13; rs ^= rs >> 7; rs ^= rs << 17; return rs; };
+    for (int trial = 0; trial < 400; ++trial) {
+      DecodeParams p{};
+      static RaggedTables tab;
+      p.ragged = 1;
+      p.row_tokens = tab.tokens;
+      p.row_j0 = tab.j0;
+      p.row_x0 = tab.x0;
+      p.geo.B = 1 + (int)(rr() % 40);
+      p.geo.Hkv = 1 + (int)(rr() % 8);
+      p.geo.NS = p.geo.B * p.geo.Hkv;
+      p.geo.fp16_mode = trial % 7 == 0;
+      p.geo.S = p.geo.fp16_mode ? 0 : (int)(rr() % 5);
+      p.geo.R = p.geo.fp16_mode ? 0 : (int)(rr() % 70);
+      p.wq = (trial & 1) ? 5376 : 9984;
+      p.wt = 8 * 128 * 4;
+      const int tmax = 1 + (int)(rr() % (trial % 3 == 0 ? 5000 : 300));
+      for (int b = 0; b < p.geo.B; ++b) tab.tokens[b] = 1 + (int)(rr() % tmax);
+      long long items;
+      bool any_groups;
+      plan_rows(p, &items, &any_groups);
+      const int NS = p.geo.NS;
+      long long nw = 1 + (long long)(rr() % 3000);
+      if (nw > items) nw = items;
+      if (nw > 64LL * NS) nw = 64LL * NS;
+      const long long wmax = any_groups && p.wq > p.wt ? p.wq : p.wt;
+      if (nw > p.wtot / wmax) nw = p.wtot / wmax;
+      if (nw < 1) nw = 1;
+      p.nwarps = (int)nw;
+      p.fd_nwarps = make_fastdiv(p.nwarps);
+      p.fd_wtot = make_fastdiv(p.wtot);
+      ++cases;
+      // items of every stream: their count and positions from the stream's own length
+      long long j = 0;
+      for (int s = 0; s < NS; ++s) {
+        const StreamSpan sp = stream_span(p, s);
+        int se, nq, w;
+        window_counts(p.geo, p.row_tokens[s / p.geo.Hkv], &se, &nq, &w);
+        if (sp.first != j || sp.ng != (p.geo.fp16_mode ? 0 : nq / 32) || sp.nt != (se + w + 7) / 8) {
+          printf("ragged span s=%d\n", s);
+          ++bad;
+        }
+        for (int k = 0; k < sp.n_items; ++k, ++j) {
+          int s2, k2;
+          locate_item(p, j, &s2, &k2);
+          if (s2 != s || k2 != k) { printf("ragged locate j=%lld\n", j); ++bad; }
+          if (item_pos(p, j) != sp.x0 + (k <= sp.ng ? k * p.wq : sp.ng * p.wq + (k - sp.ng) * p.wt)) ++bad;
+        }
+      }
+      if (j != items) ++bad;
+      std::vector<int> own(items, -1);
+      for (int i = 0; i < nw; ++i) {
+        const long long j0 = first_item_at(p, warp_x(p, i)), j1 = first_item_at(p, warp_x(p, i + 1));
+        if (j0 >= j1) { printf("ragged empty range trial=%d i=%d\n", trial, i); ++bad; }
+        for (long long jj = j0; jj < j1; ++jj) { if (own[jj] != -1) ++bad; own[jj] = i; }
+      }
+      std::set<long long> slots;
+      for (long long jj = 0; jj < items; ++jj) {
+        if (own[jj] < 0) { printf("ragged unowned item\n"); ++bad; continue; }
+        if (owner_of(p, item_pos(p, jj)) != own[jj]) { printf("ragged owner mismatch\n"); ++bad; }
+      }
+      for (int s = 0; s < NS; ++s) {
+        const StreamSpan sp = stream_span(p, s);
+        std::set<int> ws;
+        for (int k = 0; k < sp.n_items; ++k) ws.insert(own[sp.first + k]);
+        const int wf = owner_of(p, item_pos(p, sp.first)), wl = owner_of(p, item_pos(p, sp.first + sp.n_items - 1));
+        if ((int)ws.size() != wl - wf + 1) { printf("ragged count mismatch s=%d\n", s); ++bad; }
+        for (int w : ws) { if (!slots.insert(w + s).second) ++bad; if (w + s >= nw + NS) ++bad; }
       }
     }
   }

@@ -49,3 +49,18 @@ def test_fp16_cache_bytes():
     NS = cfg["batch"] * cfg["n_kv_heads"]
     qo = cfg["batch"] * cfg["n_q_heads"] * D * 2 * 2
     assert bench.algorithmic_bytes(cfg, 1000) == NS * 1000 * D * 2 * 2 + qo
+
+
+def test_ragged_bytes_sum_the_rows():
+    """A ragged batch's bytes are its rows' bytes at their own lengths: equal
+    rows give the uniform count, and each row adds what a one-row batch at
+    its length reads."""
+    cfg = workloads.layer_config("llama3_8b_kv4_ragged_t32k", 0, batch=3, max_tokens=4096)
+    assert bench.algorithmic_bytes(cfg, 2000, [2000] * 3) == bench.algorithmic_bytes(cfg, 2000)
+    one = dict(cfg, batch=1)
+    rows = [2000, 37, 1500]
+    assert bench.algorithmic_bytes(cfg, 2000, rows) == sum(bench.algorithmic_bytes(one, t) for t in rows)
+    lengths = workloads.row_tokens("llama3_8b_kv4_ragged_t32k")
+    w = workloads.WORKLOADS["llama3_8b_kv4_ragged_t32k"]
+    assert len(lengths) == w["batch"] and max(lengths) == w["tokens"]
+    assert min(lengths) >= w["ragged_min_tokens"]

@@ -132,3 +132,33 @@ def test_decode_path(B):
     assert B.decode_kernel_name(base(k_pre_rope=1), 900) == "decode_kernel<4, 2, 4>"
     with pytest.raises(B.KvqError):
         B.kvq_decode_path(base(), 1001)
+
+
+def test_ragged_entry_points_reject_before_launch(B):
+    """The ragged calls validate every row before any launch: lengths,
+    capacity, stride, alignment, the workspace and the batch limit."""
+    import ctypes as C
+    c = B.make_config(base())
+    L = B.lib()
+    fake = 1 << 20
+    rows = lambda *v: (C.c_int32 * len(v))(*v)
+    # append: null arrays, negative counts, a row past its stride or capacity, misalignment
+    assert L.kvq_append_ragged(c, fake, None, rows(1, 1), fake, fake, 4, None) == -1
+    assert L.kvq_append_ragged(c, fake, rows(0, -1), rows(1, 1), fake, fake, 4, None) == -1
+    assert L.kvq_append_ragged(c, fake, rows(0, 0), rows(5, 1), fake, fake, 4, None) == -1
+    assert L.kvq_append_ragged(c, fake, rows(0, 0), rows(1, 1), fake, fake, 0, None) == -1
+    assert L.kvq_append_ragged(c, fake, rows(0, 998), rows(1, 3), fake, fake, 4, None) == -3
+    assert L.kvq_append_ragged(c, fake + 8, rows(0, 0), rows(1, 1), fake, fake, 4, None) == -1
+    # nothing to append in any row: success without a launch
+    assert L.kvq_append_ragged(c, fake, rows(10, 20), rows(0, 0), fake, fake, 4, None) == 0
+    # decode: a row of zero tokens or past capacity, null q, null lengths
+    assert L.kvq_decode_attn_ragged(c, fake, rows(5, 0), fake, fake, None, None, 0, None) == -1
+    assert L.kvq_decode_attn_ragged(c, fake, rows(5, 1001), fake, fake, None, None, 0, None) == -3
+    assert L.kvq_decode_attn_ragged(c, fake, rows(5, 7), None, fake, None, None, 0, None) == -1
+    assert L.kvq_decode_attn_ragged(c, fake, None, fake, fake, None, None, 0, None) == -1
+    # the persistent kernel needs its workspace; more than 256 rows
+    assert L.kvq_decode_attn_ragged(c, fake, rows(500, 7), fake, fake, None, None, 0, None) == -4
+    big = B.make_config(base(batch=257))
+    many = (C.c_int32 * 257)(*([5] * 257))
+    assert L.kvq_decode_attn_ragged(big, fake, many, fake, fake, None, None, 0, None) == -2
+    assert L.kvq_append_ragged(big, fake, many, many, fake, fake, 8, None) == -2
