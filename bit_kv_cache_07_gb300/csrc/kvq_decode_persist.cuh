@@ -267,7 +267,41 @@ __device__ __forceinline__ void finalize_stream(const DecodeParams& p, int slot,
   if (lane == 0) p.counters[s] = 0u;
 }
 
-template <int KB, int VB, int NT, int GT, bool IQ = false>
+// The counts of the stream a walker (the issue side or the processing side
+// of a warp's range) is in: quantized groups, items, fp16 tokens and the
+// window counts that address them.  Uniform calls read them from the launch
+// parameters (every stream alike); ragged ones keep the current stream's.
+template <bool RG>
+struct Walk {
+  __device__ __forceinline__ void set(const DecodeParams&, int) {}
+  __device__ __forceinline__ int ng(const DecodeParams& p) const { return p.ng; }
+  __device__ __forceinline__ int n_items(const DecodeParams& p) const { return p.n_items; }
+  __device__ __forceinline__ int k1(const DecodeParams& p) const { return p.S_eff + p.W; }
+  __device__ __forceinline__ int S_eff(const DecodeParams& p) const { return p.S_eff; }
+  __device__ __forceinline__ int Nq(const DecodeParams& p) const { return p.Nq; }
+};
+template <>
+struct Walk<true> {
+  int ng_, n_, k1_, se_, nq_;
+  __device__ __forceinline__ void set(const DecodeParams& p, int s) {
+    const StreamSpan r = stream_span_t<true>(p, s);
+    ng_ = r.ng;
+    n_ = r.n_items;
+    k1_ = r.k1;
+    se_ = r.S_eff;
+    nq_ = r.Nq;
+  }
+  __device__ __forceinline__ int ng(const DecodeParams&) const { return ng_; }
+  __device__ __forceinline__ int n_items(const DecodeParams&) const { return n_; }
+  __device__ __forceinline__ int k1(const DecodeParams&) const { return k1_; }
+  __device__ __forceinline__ int S_eff(const DecodeParams&) const { return se_; }
+  __device__ __forceinline__ int Nq(const DecodeParams&) const { return nq_; }
+};
+
+// RG: a ragged call (every stream at its batch row's length; the row tables
+// in the workspace), compiled separately so that the uniform schedule
+// carries none of it.
+template <int KB, int VB, int NT, int GT, bool IQ = false, bool RG = false>
 __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT, IQ>::kCtaThreads, 1)
     decode_persist_kernel(const __grid_constant__ DecodeParams p) {
   using LY = PersistLayout<KB, VB, NT, GT, IQ>;
@@ -288,9 +322,9 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT, IQ>::kCtaThreads
 
   const int gw = blockIdx.x * LY::kWarps + w;  // global warp index
   if (gw >= p.nwarps) return;
-  if (p.ragged) grid_dep_wait();  // the row tables were written by the kernel before
-  const long long j0 = first_item_at(p, warp_x(p, gw));
-  const long long j1 = first_item_at(p, warp_x(p, gw + 1));
+  if constexpr (RG) grid_dep_wait();  // the row tables were written by the kernel before
+  const long long j0 = first_item_at_t<RG>(p, warp_x(p, gw));
+  const long long j1 = first_item_at_t<RG>(p, warp_x(p, gw + 1));
   if (j0 >= j1) return;
 
   float O[8][o_tiles<NT>()][4], macc[NT][kNVG], m_used[NT], lsum[NT];
@@ -315,23 +349,28 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT, IQ>::kCtaThreads
   // incrementally, each with its stream's counts (sp, isp: quantized groups,
   // items, fp16 tokens), refreshed when it moves to the next stream
   int s, k;
-  locate_item(p, j0, &s, &k);
-  StreamSpan sp = stream_span(p, s);
+  locate_item_t<RG>(p, j0, &s, &k);
+  Walk<RG> sw;
+  sw.set(p, s);
   int is = s, ik = k;
-  StreamSpan isp = sp;
+  Walk<RG> isw = sw;
   long long ij = j0;
   auto issue_next = [&](int stage) {
     if (ij < j1) {
       const uint32_t dst = st0_s + stage * LY::kStageBytes;
-      const int ng = LY::kQuant ? isp.ng : 0;
+      const int ng = LY::kQuant ? isw.ng(p) : 0;
       if (LY::kQuant && ik < ng) {
         if constexpr (LY::kQuant) issue_group<KBq, VBq, IQ>(p, is, ik, dst, lane);
       } else {
-        issue_f16(p, is, kF16Tokens * (ik - ng), isp.k1, isp.S_eff, isp.Nq, dst, lane);
+        issue_f16(p, is, kF16Tokens * (ik - ng), isw.k1(p), isw.S_eff(p), isw.Nq(p), dst, lane);
       }
-      if (++ij < j1 && ++ik == isp.n_items) {
+      ++ij;
+      if (++ik == isw.n_items(p)) {
         ik = 0;
-        isp = stream_span(p, ++is);
+        ++is;
+        if constexpr (RG) {
+          if (ij < j1) isw.set(p, is);
+        }
       }
     }
     cp_async_commit();
@@ -355,9 +394,9 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT, IQ>::kCtaThreads
   auto finish = [&](int sf) {
     if (has_q) stage_quant<VBq, NT, GT, JC>(p, sO, sML, g, lane, O, macc, m_used, lsum);
     staged = staged || has_q;
-    const StreamSpan fs = stream_span(p, sf);
-    const int wf = owner_of(p, item_pos(p, fs.first));
-    const int wl = owner_of(p, item_pos(p, fs.first + fs.n_items - 1));
+    const StreamSpan fs = stream_span_t<RG>(p, sf);
+    const int wf = owner_of(p, item_pos_t<RG>(p, fs.first));
+    const int wl = owner_of(p, item_pos_t<RG>(p, fs.first + fs.n_items - 1));
     finalize_stream<NT, GT>(p, gw + sf, sf, wf, wl - wf + 1, sO, sML, staged, lane, O, m_used, lsum);
     reset();
     has_q = staged = bq_f16 = false;
@@ -397,7 +436,7 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT, IQ>::kCtaThreads
     cp_async_wait<LY::kStages - 1>();
     __syncwarp();
     const unsigned char* stc = st0 + cur * LY::kStageBytes;
-    const int ng = LY::kQuant ? sp.ng : 0;
+    const int ng = LY::kQuant ? sw.ng(p) : 0;
     if (LY::kQuant && k < ng) {
       if constexpr (LY::kQuant) {
         process_group<KB, VB, NT, JC, GT, IQ>(qw, sm, iq, stc, g, lane, O, macc, m_used, lsum);
@@ -414,14 +453,16 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT, IQ>::kCtaThreads
           staged = true;
         }
       }
-      process_f16<NT>(sm, stc, g, lane, kF16Tokens * (k - ng), sp.k1, O, m_used, lsum);
+      process_f16<NT>(sm, stc, g, lane, kF16Tokens * (k - ng), sw.k1(p), O, m_used, lsum);
     }
     __syncwarp();
     cur = (cur + 1 == LY::kStages) ? 0 : cur + 1;
-    if (++k == sp.n_items) {
+    if (++k == sw.n_items(p)) {
       k = 0;
       ++s;
-      if (j + 1 < j1) sp = stream_span(p, s);
+      if constexpr (RG) {
+        if (j + 1 < j1) sw.set(p, s);
+      }
     }
   }
   cp_async_wait<0>();
@@ -439,10 +480,17 @@ cudaError_t launch_t(const DecodeParams& p, cudaStream_t st) {
   constexpr int NT = GT <= 4 ? 1 : 2;
   using LY = PersistLayout<KB, VB, NT, GT, IQ>;
   const int smem = LY::kBytes;
+  const int ctas = (p.nwarps + LY::kWarps - 1) / LY::kWarps;
+  if (p.ragged) {
+    static std::atomic<long long> smem_memo_rg[kMemoDevices];
+    cudaError_t e = ensure_smem_limit(decode_persist_kernel<KB, VB, NT, GT, IQ, true>, smem_memo_rg, smem);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(decode_persist_kernel<KB, VB, NT, GT, IQ, true>, dim3(ctas), dim3(LY::kCtaThreads),
+                            smem, st, p);
+  }
   static std::atomic<long long> smem_memo[kMemoDevices];
   cudaError_t e = ensure_smem_limit(decode_persist_kernel<KB, VB, NT, GT, IQ>, smem_memo, smem);
   if (e != cudaSuccess) return e;
-  const int ctas = (p.nwarps + LY::kWarps - 1) / LY::kWarps;
   return launch_dependent(decode_persist_kernel<KB, VB, NT, GT, IQ>, dim3(ctas), dim3(LY::kCtaThreads), smem, st,
                           p);
 }

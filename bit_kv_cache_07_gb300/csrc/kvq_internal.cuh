@@ -268,8 +268,10 @@ __host__ __device__ inline StreamSpan row_span(const DecodeParams& p, int b) {
   r.x0 = p.row_x0[b];
   return r;
 }
-__host__ __device__ inline StreamSpan stream_span(const DecodeParams& p, int s) {
-  if (!p.ragged) {
+// RG: the ragged schedule (compile-time in the kernel, p.ragged on the host)
+template <bool RG>
+__host__ __device__ inline StreamSpan stream_span_t(const DecodeParams& p, int s) {
+  if constexpr (!RG) {
     StreamSpan r;
     r.first = (long long)s * p.n_items;
     r.x0 = (long long)s * p.wstream;
@@ -287,6 +289,9 @@ __host__ __device__ inline StreamSpan stream_span(const DecodeParams& p, int s) 
   r.first += (long long)h * r.n_items;
   r.x0 += (long long)h * r.wstream;
   return r;
+}
+__host__ __device__ inline StreamSpan stream_span(const DecodeParams& p, int s) {
+  return p.ragged ? stream_span_t<true>(p, s) : stream_span_t<false>(p, s);
 }
 // Ragged schedule: the last row whose first entry in `tab` (row_j0 or
 // row_x0) is <= v (rows of a ragged call hold at least one item each).
@@ -328,35 +333,41 @@ inline void plan_rows(DecodeParams& p, long long* items, bool* any_groups) {
   p.wtot = p.row_x0[p.geo.B];
 }
 
-// Persistent-schedule arithmetic shared by host and device.
+// Persistent-schedule arithmetic shared by host and device: items laid
+// stream after stream, weighted by their bytes; RG selects the ragged
+// schedule at compile time (the wrappers below take p.ragged).
 // (Dividends stay below 2^56: plan_persist checks (wtot + 1) (nwarps + 1) < 2^56.)
 // Item j's stream s and index k within it.
-__host__ __device__ inline void locate_item(const DecodeParams& p, long long j, int* s, int* k) {
-  if (!p.ragged) {
+template <bool RG>
+__host__ __device__ inline void locate_item_t(const DecodeParams& p, long long j, int* s, int* k) {
+  if constexpr (!RG) {
     const long long ss = idiv(j, p.n_items, p.fd_n_items);
     *s = (int)ss;
     *k = (int)(j - ss * p.n_items);
-    return;
+  } else {
+    const int b = row_at(p.row_j0, p.geo.B, j);
+    const StreamSpan r = row_span(p, b);
+    const long long h = (j - r.first) / r.n_items;
+    *s = b * p.geo.Hkv + (int)h;
+    *k = (int)(j - r.first - h * r.n_items);
   }
-  const int b = row_at(p.row_j0, p.geo.B, j);
-  const StreamSpan r = row_span(p, b);
-  const long long h = (j - r.first) / r.n_items;
-  *s = b * p.geo.Hkv + (int)h;
-  *k = (int)(j - r.first - h * r.n_items);
 }
-__host__ __device__ inline long long item_pos(const DecodeParams& p, long long j) {
-  if (p.ragged) {
+template <bool RG>
+__host__ __device__ inline long long item_pos_t(const DecodeParams& p, long long j) {
+  if constexpr (RG) {
     int s, k;
-    locate_item(p, j, &s, &k);
-    const StreamSpan r = stream_span(p, s);
+    locate_item_t<true>(p, j, &s, &k);
+    const StreamSpan r = stream_span_t<true>(p, s);
     return r.x0 + (k <= r.ng ? k * p.wq : r.ng * p.wq + (k - r.ng) * p.wt);
+  } else {
+    const long long s = idiv(j, p.n_items, p.fd_n_items), k = j - s * p.n_items;
+    return s * p.wstream + (k <= p.ng ? k * p.wq : p.ng * p.wq + (k - p.ng) * p.wt);
   }
-  const long long s = idiv(j, p.n_items, p.fd_n_items), k = j - s * p.n_items;
-  return s * p.wstream + (k <= p.ng ? k * p.wq : p.ng * p.wq + (k - p.ng) * p.wt);
 }
 // First item whose start weight is >= x (x in [0, wtot]).
-__host__ __device__ inline long long first_item_at(const DecodeParams& p, long long x) {
-  if (p.ragged) {
+template <bool RG>
+__host__ __device__ inline long long first_item_at_t(const DecodeParams& p, long long x) {
+  if constexpr (RG) {
     if (x >= p.wtot) return p.row_j0[p.geo.B];
     const int b = row_at(p.row_x0, p.geo.B, x);
     const StreamSpan r = row_span(p, b);
@@ -367,13 +378,24 @@ __host__ __device__ inline long long first_item_at(const DecodeParams& p, long l
     if (rem <= (long long)r.ng * p.wq) k = (rem + p.wq - 1) / p.wq;
     else k = r.ng + (rem - (long long)r.ng * p.wq + p.wt - 1) / p.wt;
     return f + k;  // k == n_items: the next stream's first item
+  } else {
+    long long s = idiv(x, p.wstream, p.fd_wstream), rem = x - s * p.wstream, k;
+    if (rem == 0) return s * p.n_items;
+    if (rem <= p.ng * p.wq) k = idiv(rem + p.wq - 1, p.wq, p.fd_wq);
+    else k = p.ng + idiv(rem - p.ng * p.wq + p.wt - 1, p.wt, p.fd_wt);
+    if (k >= p.n_items) return (s + 1) * p.n_items;
+    return s * p.n_items + k;
   }
-  long long s = idiv(x, p.wstream, p.fd_wstream), rem = x - s * p.wstream, k;
-  if (rem == 0) return s * p.n_items;
-  if (rem <= p.ng * p.wq) k = idiv(rem + p.wq - 1, p.wq, p.fd_wq);
-  else k = p.ng + idiv(rem - p.ng * p.wq + p.wt - 1, p.wt, p.fd_wt);
-  if (k >= p.n_items) return (s + 1) * p.n_items;
-  return s * p.n_items + k;
+}
+__host__ __device__ inline void locate_item(const DecodeParams& p, long long j, int* s, int* k) {
+  if (p.ragged) locate_item_t<true>(p, j, s, k);
+  else locate_item_t<false>(p, j, s, k);
+}
+__host__ __device__ inline long long item_pos(const DecodeParams& p, long long j) {
+  return p.ragged ? item_pos_t<true>(p, j) : item_pos_t<false>(p, j);
+}
+__host__ __device__ inline long long first_item_at(const DecodeParams& p, long long x) {
+  return p.ragged ? first_item_at_t<true>(p, x) : first_item_at_t<false>(p, x);
 }
 // Warp i covers weight [x_i, x_{i+1}), x_i = floor(i * wtot / nwarps).
 __host__ __device__ inline long long warp_x(const DecodeParams& p, long long i) {
