@@ -290,7 +290,9 @@ kvq_status kvq_decode_path(const kvq_config *cfg, int32_t tokens, int32_t *persi
  *                         are the first n_new[b] of its n_stride slots
  *   n_stride              >= 1, the inputs' token dimension
  * InnerQ key normalisation (k_channel_norm) is fixed per row by the row's
- * first append into its empty cache (tokens_before[b] = 0).
+ * first append into its empty cache (tokens_before[b] = 0).  The per-row
+ * counts are copied into the layer buffer's `rows` region (a small kernel
+ * on `stream`) for the append kernels that follow.
  * Errors: as kvq_append; KVQ_ERR_UNSUPPORTED when batch > 256. */
 kvq_status kvq_append_ragged(const kvq_config *cfg, void *layer_buf, const int32_t *tokens_before,
                              const int32_t *n_new, const uint16_t *k_new, const uint16_t *v_new,
@@ -299,6 +301,8 @@ kvq_status kvq_append_ragged(const kvq_config *cfg, void *layer_buf, const int32
 /* kvq_decode_attn_ragged -- kvq_decode_attn for sequences of different
  * lengths: batch row b attends over its own tokens[b] tokens.
  *   tokens     host int32 [batch], 1 <= tokens[b] <= max_tokens
+ *   workspace  always required, ws_bytes >= layout.workspace_bytes: the row
+ *              tables are copied into its end (a small kernel on `stream`)
  *   other arguments as kvq_decode_attn.
  * Runs the kernel kvq_decode_attn would: the persistent kernel lays every
  * stream's own work items end to end and cuts them into equal byte ranges;
