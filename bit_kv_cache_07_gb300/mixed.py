@@ -80,13 +80,25 @@ class MixedLayer:
         for _, _, layer in self.parts:
             layer.append(tokens_before, k_new, v_new, stream)
 
+    def append_ragged(self, tokens_before, n_new, k_new, v_new, stream=None):
+        """Batch row b appends n_new[b] tokens after tokens_before[b] (every part)."""
+        for _, _, layer in self.parts:
+            layer.append_ragged(tokens_before, n_new, k_new, v_new, stream)
+
     def decode(self, tokens: int, q, out, lse=None, workspace=None, stream=None):
         """Attention over the layer's cache into out (all heads); each part
         uses its own workspace (`workspace` is not used)."""
+        self._side_by_side(lambda layer, ws, s: layer.decode(tokens, q, out, lse, ws, s), stream)
+
+    def decode_ragged(self, tokens, q, out, lse=None, workspace=None, stream=None):
+        """decode with batch row b attending over its own tokens[b] tokens."""
+        self._side_by_side(lambda layer, ws, s: layer.decode_ragged(tokens, q, out, lse, ws, s), stream)
+
+    def _side_by_side(self, call, stream):
         import torch
         main = stream if stream is not None else torch.cuda.current_stream()
         if len(self.parts) == 1:
-            self.parts[0][2].decode(tokens, q, out, lse, self.ws[0], main)
+            call(self.parts[0][2], self.ws[0], main)
             return
         fork = torch.cuda.Event()
         fork.record(main)
@@ -95,7 +107,7 @@ class MixedLayer:
             s = main if i == 0 else self.side[i - 1]
             if i:
                 s.wait_event(fork)
-            layer.decode(tokens, q, out, lse, self.ws[i], s)
+            call(layer, self.ws[i], s)
             if i:
                 e = torch.cuda.Event()
                 e.record(s)

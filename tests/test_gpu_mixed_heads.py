@@ -73,6 +73,37 @@ def test_mixed_pairs_match_the_oracle(B, kind):
                 assert np.allclose(lse[b, h * g:(h + 1) * g].cpu().numpy(), rlse, rtol=1e-4, atol=1e-3)
 
 
+def test_mixed_pairs_with_ragged_rows(B):
+    """Per-head pairs and rows of different lengths together: every part
+    takes the ragged calls over its heads; each (row, head) matches the
+    oracle built from that row's tokens at that head's pair."""
+    from bit_kv_cache_07_gb300 import mixed, synth
+    lengths = [700, 133, 2]
+    cfg, pairs = base_cfg(3, 8, 4, max(lengths)), [(8, 4), (2, 2), (4, 4), (2, 2)]
+    K, V = synth.random_kv(3, 4, max(lengths), seed=51, device="cuda")
+    layer = mixed.MixedLayer(cfg, pairs)
+    layer.append_ragged([0, 0, 0], lengths, K, V)
+    q = synth.random_q(3, 8, seed=52, device="cuda")
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device="cuda")
+    layer.decode_ragged(lengths, q, out, lse)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    Kh, Vh, qh = K.cpu().numpy(), V.cpu().numpy(), q.cpu().numpy()
+    g = 2
+    for pair, heads, sub in layer.parts:
+        pc = dict(cfg, k_bits=pair[0], v_bits=pair[1])
+        for b, T in enumerate(lengths):
+            for i, h in enumerate(heads):
+                st = O.build_stream(pc, Kh[b, h, :T], Vh[b, h, :T])
+                assert_store_equal(gpu_store(sub, b * len(heads) + i, T, O.layout_counts(pc, T)), st,
+                                   where=f"{pair} b{b} h{h}")
+                ref, rlse = O.decode_stream(pc, T, st, qh[b, h * g:(h + 1) * g])
+                err = normwise_err(out[b, h * g:(h + 1) * g].float().cpu().numpy(), ref).max()
+                assert err < TOL, (pair, b, h, err)
+                assert np.allclose(lse[b, h * g:(h + 1) * g].cpu().numpy(), rlse, rtol=1e-4, atol=1e-3)
+
+
 @pytest.mark.parametrize("kind", ["per_channel", "hadamard_hybrid", "innerq_norm"])
 def test_distortion_matches_the_oracle(B, kind):
     from bit_kv_cache_07_gb300 import synth
