@@ -158,6 +158,42 @@ def test_ragged_equal_lengths_match_the_uniform_calls(B):
     assert normwise_err(out_u.cpu().numpy(), out_r.cpu().numpy().astype(np.float64)).max() < TOL
 
 
+def test_ragged_innerq_row_starts_later(B):
+    """InnerQ key normalisation with rows that start at different calls: a
+    row still empty after the first ragged append gets its normalisation
+    from its own first append, while the other rows keep theirs."""
+    from bit_kv_cache_07_gb300 import synth
+    rows, Hkv, Hq = 3, 2, 8
+    cfg = cfg_of(4, 4, rows, Hq, Hkv, 400, k_group_channels=64, hybrid_groups=1, k_channel_norm=1)
+    K, V = synth.random_kv(rows, Hkv, 300, seed=23, device="cuda")
+    layer = B.Layer(cfg)
+    first = [200, 0, 150]   # row 1 stays empty
+    layer.append_ragged([0, 0, 0], first, K, V)
+    more = [40, 260, 0]     # row 1 starts now; row 2 appends nothing
+    k2 = torch.stack([K[b, :, first[b]:first[b] + 260] if first[b] + 260 <= 300 else
+                      torch.cat([K[b, :, first[b]:], K[b, :, :first[b] + 260 - 300]], 1) for b in range(rows)]).contiguous()
+    v2 = torch.stack([V[b, :, first[b]:first[b] + 260] if first[b] + 260 <= 300 else
+                      torch.cat([V[b, :, first[b]:], V[b, :, :first[b] + 260 - 300]], 1) for b in range(rows)]).contiguous()
+    layer.append_ragged(first, more, k2, v2)
+    torch.cuda.synchronize()
+    lengths = [f + m for f, m in zip(first, more)]
+    Kh, Vh = K.cpu().numpy(), V.cpu().numpy()
+    # each row's tokens in order: its first slice, then the first `more` rows of its second input
+    k2h, v2h = k2.cpu().numpy(), v2.cpu().numpy()
+    refs = []
+    for s in range(rows * Hkv):
+        b, h = divmod(s, Hkv)
+        kt = np.concatenate([Kh[b, h, :first[b]], k2h[b, h, :more[b]]], 0)
+        vt = np.concatenate([Vh[b, h, :first[b]], v2h[b, h, :more[b]]], 0)
+        norm_from = first[b] if first[b] > 0 else more[b]
+        c = dict(cfg, norm_tokens=norm_from)
+        ref = O.build_stream(c, kt, vt)
+        assert_store_equal(gpu_store(layer, s, lengths[b], O.layout_counts(cfg, lengths[b])), ref,
+                           where=f"stream {s} (T={lengths[b]})")
+        refs.append(ref)
+    check_ragged_decode(B, layer, cfg, lengths, refs, seed=4)
+
+
 def test_ragged_innerq_append_and_decode(B):
     """InnerQ keys with key normalisation: each row's normalisation comes
     from its own first append, and the ragged decode (persistent kernel,
