@@ -38,12 +38,16 @@ constexpr int kRowVec = kRowHalves * 2 / 16;  // 16 x 16-byte chunks per row
 // and its rounding in [0, qmax]: the clamp of the definition never binds;
 // qa - rint(qa) is exact, and its magnitude exceeds 0.4999 exactly when qa
 // lies within 1e-4 of a half-integer.)
+// rint(d / scale) by the IEEE division, out of line: the rare path of the
+// codes below, kept out of their unrolled loops.
+__device__ __noinline__ float rint_div(float d, float scale) { return rintf(__fdiv_rn(d, scale)); }
+
 __device__ __forceinline__ uint32_t uniform_code(float x, float mn, float scale, float rs) {
   if (scale == 0.0f) return 0u;
   const float d = __fsub_rn(x, mn);
   const float qa = __fmul_rn(d, rs);
   float r = rintf(qa);
-  if (fabsf(__fsub_rn(qa, r)) > 0.4999f) r = rintf(__fdiv_rn(d, scale));
+  if (fabsf(__fsub_rn(qa, r)) > 0.4999f) r = rint_div(d, scale);
   return (uint32_t)r;
 }
 
@@ -110,7 +114,7 @@ __device__ __forceinline__ GroupQ group_params(float mn, float mx, long long sum
 __device__ __forceinline__ uint32_t sym_code(float x, float scale, float rs, int bits) {
   const float qa = __fmul_rn(x, rs);
   float r = rintf(qa);
-  if (fabsf(__fsub_rn(qa, r)) > 0.4999f) r = rintf(__fdiv_rn(x, scale));
+  if (fabsf(__fsub_rn(qa, r)) > 0.4999f) r = rint_div(x, scale);
   const float qs = (float)((1 << (bits - 1)) - 1);
   r = fminf(fmaxf(r, -qs), qs);
   return (uint32_t)((int)r + (1 << (bits - 1)));
