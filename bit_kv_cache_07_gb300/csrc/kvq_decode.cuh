@@ -69,6 +69,16 @@ __host__ __device__ constexpr size_t decode_smem_fixed() {
 // adjacent (a lane reads both with one 16-byte load), lanes l consecutive.
 __host__ __device__ __forceinline__ int rope_tab_index(int j, int l) { return (((j >> 1) * 32 + l) << 1) | (j & 1); }
 
+// RoPE region of the dynamic shared memory: the offset table over 32 token
+// offsets, or, for non-uniform codes with one query head, the query-folded
+// table over 16 offsets followed by each warp's second anchor set (the
+// anchors of offsets 16..31, see k_logits_nuq_st).
+template <int KB, int GQ>
+__host__ __device__ constexpr int rope_region_bytes() {
+  return (KB == 3 && GQ == 1) ? 16 * (kHeadDim / 2) * 8 + 4 * (kHeadDim / 2) * 8
+                              : kGroupTokens * (kHeadDim / 2) * 8;
+}
+
 // 16-byte asynchronous global -> shared copies (cp.async, completion by group)
 __device__ __forceinline__ void cp_async16(uint32_t smem, const void* gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem), "l"(gmem));
@@ -508,31 +518,37 @@ __device__ __forceinline__ void warp_fwht(float (&v)[4], float c, int lane) {
 }
 
 // ------------------------------------------------------ staged NUQ groups
-// For the non-uniform (3-bit) cache every warp double-buffers its groups in
+// For the non-uniform (3-bit) cache every warp streams its groups into
 // shared memory with cp.async: while it computes group i, group i + 4 (its
-// next one) streams in.  A stage holds one 32-token group of one stream:
-// K and V code rows (48 bytes each), the per-token {min, s} words, and the
-// group's CSR outlier entries -- exactly k per row (the append writes k
-// entries for every row), so a group's entries are the k*32 consecutive
-// ones starting at row * k and the row pointers are not needed here.
+// next one) streams in.  The K code rows (48 bytes per token) go to one
+// buffer per warp: the lanes take their rows into registers before the
+// next group's rows are issued into it.  Everything else is double-buffered
+// in stages: V code rows, the per-token {min, s} words, and the group's CSR
+// outlier entries -- exactly k per row (the append writes k entries for
+// every row), so a group's entries are the k*32 consecutive ones starting
+// at row * k and the row pointers are not needed here.
 struct NuqStage {
-  static constexpr int KC = 0, VC = kGroupTokens * 48, KMS = 2 * kGroupTokens * 48;
+  static constexpr int KBUF = kGroupTokens * 48;  // the per-warp K code buffer
+  static constexpr int VC = 0, KMS = kGroupTokens * 48;
   static constexpr int VMS = KMS + kGroupTokens * 4, CSR = VMS + kGroupTokens * 4;
   static __host__ __device__ constexpr int kcol(int k) { return CSR; }
   static __host__ __device__ constexpr int kval(int k) { return CSR + 32 * k; }
   static __host__ __device__ constexpr int vcol(int k) { return CSR + 96 * k; }
   static __host__ __device__ constexpr int vval(int k) { return CSR + 128 * k; }
   static __host__ __device__ constexpr int bytes(int k) { return (CSR + 192 * k + 127) / 128 * 128; }
+  // one warp's K buffer and two stages
+  static __host__ __device__ constexpr int warp_bytes(int k) { return KBUF + 2 * bytes(k); }
 };
 
-__device__ __forceinline__ void issue_nuq(const DecodeParams& p, int s, int grp, uint32_t dst, int lane) {
+__device__ __forceinline__ void issue_nuq(const DecodeParams& p, int s, int grp, uint32_t kdst, uint32_t dst,
+                                          int lane) {
   const Geometry& G = p.geo;
   const int k = G.nout;
   const size_t i0 = (size_t)s * G.qcap + (size_t)grp * kGroupTokens;  // first row of the group
   const uint8_t* kc = p.L.k_codes + i0 * 48;
   const uint8_t* vc = p.L.v_codes + i0 * 48;
   for (int c = lane; c < kGroupTokens * 48 / 16; c += 32) {
-    cp_async16(dst + NuqStage::KC + 16 * c, kc + 16 * c);
+    cp_async16(kdst + 16 * c, kc + 16 * c);
     cp_async16(dst + NuqStage::VC + 16 * c, vc + 16 * c);
   }
   if (lane < 8) {
@@ -553,41 +569,84 @@ __device__ __forceinline__ void issue_nuq(const DecodeParams& p, int s, int grp,
 // 3-bit code c of a 48-byte row held in 12 (+1 zero) registers.
 __device__ __forceinline__ uint32_t code3(const uint32_t (&w)[13], int c) { return code_at<3>(w, c); }
 
+// Pair tables: the level values of two adjacent 3-bit codes with one 8-byte
+// load.  Entry f = c0 | c1 << 3 holds (L[c0], L[c1]); each entry is stored
+// 16 times, copy i at bank pair i, and lane l reads copy l & 15, so the
+// 16 lanes of a half-warp never meet in a bank whatever their codes.
+// Byte offset of entry f, copy i: f * 128 + i * 8.
+constexpr int kPairEntries = 64, kPairCopies = 16;
+constexpr int kPairTableBytes = kPairEntries * kPairCopies * 8;
+
+// Dynamic shared memory of a split-kernel launch: DecodeSmem (up to `work`
+// for non-uniform codes), for non-uniform codes the K and V pair tables (at
+// a fixed offset, so their loads take it as an immediate), the RoPE region,
+// and for non-uniform codes the warps' K buffers and stages and their
+// outlier buffers.
+template <int KB, int GQ>
+__host__ __device__ constexpr size_t decode_smem_bytes(bool pre_rope, int nout) {
+  return decode_smem_fixed<KB, GQ>() + (KB == 3 ? 2 * kPairTableBytes : 0) +
+         (pre_rope ? rope_region_bytes<KB, GQ>() : 0) +
+         (KB == 3 ? 4 * (size_t)NuqStage::warp_bytes(nout) + 4 * GQ * kHeadDim * sizeof(float) : 0);
+}
+
+// (L[c], L[c+1]) for codes c, c+1 (c even) of a 48-byte row in registers;
+// loff = (lane & 15) * 8.  The 6-bit field at bit 3c is shifted to bits
+// 7..12 of x, which makes it the entry's byte offset.
+__device__ __forceinline__ float2 pair_levels(const unsigned char* tab, const uint32_t (&w)[13], int c, uint32_t loff) {
+  const int bp = 3 * c;
+  uint32_t x;
+  if (bp < 7) {
+    x = w[0] << (7 - bp);
+  } else {
+    const int sft = bp - 7, w0 = sft >> 5, sh = sft & 31;
+    x = sh <= 19 ? (w[w0] >> sh) : __funnelshift_r(w[w0], w[w0 + 1], sh);
+  }
+  return *reinterpret_cast<const float2*>(tab + ((x & 0x1F80u) | loff));
+}
+
 // K logits of one staged NUQ group, lane = token.
 //  no RoPE:    z = min * sum(q) + s * sum_c q_c L'_code, plus outlier terms
-//  RoPE, GQ=1: z = sum_j Re[W_{j,lane} * A_j * (k_j + i k_{j+64})], with
-//              W_{j,d} = conj(q_j + i q_{j+64}) e^{i theta_j d} (table, per
-//              CTA) and A_j = e^{i theta_j t0} (group anchor): two complex
-//              products per channel pair instead of rotating q or k
+//  RoPE, GQ=1: z = sum_j Re[W_{j,d} * A_j * (k_j + i k_{j+64})] for the
+//              lane's offset lane = 16 h + d, with
+//              W_{j,d} = conj(q_j + i q_{j+64}) e^{i theta_j d}, d < 16
+//              (table, per CTA) and A_j = e^{i theta_j (t0 + 16 h)} (anchor
+//              set h of the group): two complex products per channel pair
+//              instead of rotating q or k; lanes d and 16 + d read the same
+//              table entry
 //  RoPE, GQ>1: rotate each key pair once by A_j e^{i theta_j lane}, dot with
 //              every head
 // Group anchors of a warp that visits groups g, g + 4, g + 8, ...: lane j
 // keeps pairs j and j + 32; the anchor moves by e^{i theta_j 128} per visit
 // (`step`, from an fp64 angle) and is recomputed exactly (anchor_expi) every
 // kAnchorEvery visits, so fp32 rounding of the products stays within that
-// many complex multiplications.
+// many complex multiplications.  The second set is the first times
+// e^{i theta_j 16} (`half`, from an fp64 angle).
 constexpr int kAnchorEvery = 16;
 struct AnchorWalk {
-  float2 a[2], step[2];
+  float2 a[2], step[2], half[2];
   int left;  // visits before the next exact anchor
 };
 
+// A lane's K code row (48 bytes, token = lane) from the warp's K buffer.
+__device__ __forceinline__ void load_code_row(const unsigned char* kbuf, int lane, uint32_t (&wd)[13]) {
+  const uint4* row = reinterpret_cast<const uint4*>(kbuf + 48 * lane);
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    const uint4 u = row[i];
+    wd[4 * i] = u.x; wd[4 * i + 1] = u.y; wd[4 * i + 2] = u.z; wd[4 * i + 3] = u.w;
+  }
+  wd[12] = 0;
+}
+
+// tab: the RoPE region (for GQ = 1 the folded 16-offset table, then the
+// second anchor sets of the 4 warps)
 template <int GQ>
 __device__ __forceinline__ void k_logits_nuq_st(const DecodeParams& p, DecodeSmem<GQ>& sm,
-                                                const float2* __restrict__ tab, const unsigned char* st,
-                                                int grp, int lane, int w, float (&z)[GQ], AnchorWalk& aw) {
+                                                const float2* tab, const unsigned char* ptab_k,
+                                                const uint32_t (&wd)[13], const unsigned char* st, int grp,
+                                                int lane, int w, float (&z)[GQ], AnchorWalk& aw) {
   const Geometry& G = p.geo;
   const int k = G.nout;
-  uint32_t wd[13];
-  {
-    const uint4* row = reinterpret_cast<const uint4*>(st + NuqStage::KC + 48 * lane);
-#pragma unroll
-    for (int i = 0; i < 3; ++i) {
-      const uint4 u = row[i];
-      wd[4 * i] = u.x; wd[4 * i + 1] = u.y; wd[4 * i + 2] = u.z; wd[4 * i + 3] = u.w;
-    }
-    wd[12] = 0;
-  }
   const float2 ms = unpack_min_scale(reinterpret_cast<const uint32_t*>(st + NuqStage::KMS)[lane]);
   const uint8_t* ocol = st + NuqStage::kcol(k) + k * lane;
   const uint16_t* oval = reinterpret_cast<const uint16_t*>(st + NuqStage::kval(k)) + k * lane;
@@ -620,8 +679,11 @@ __device__ __forceinline__ void k_logits_nuq_st(const DecodeParams& p, DecodeSme
   }
   // group anchor e^{i t0 theta_j}
   if constexpr (GQ == 1) {
-    // anchors of pairs 2i, 2i+1 as (x_2i, x_2i+1, y_2i, y_2i+1): fp32x2 operands without shuffling
-    float* ap = reinterpret_cast<float*>(&sm.anchor[w][0]);
+    // anchors of pairs 2i, 2i+1 as (x_2i, x_2i+1, y_2i, y_2i+1): fp32x2
+    // operands without shuffling; set 0 (offsets 0..15) in sm.anchor, set 1
+    // (offsets 16..31) after the folded table
+    float* ap0 = reinterpret_cast<float*>(&sm.anchor[w][0]);
+    float* ap1 = reinterpret_cast<float*>(const_cast<float2*>(tab) + 16 * (kHeadDim / 2) + w * (kHeadDim / 2));
     if (aw.left == 0) {
       aw.a[0] = anchor_expi<GQ>(p, sm, lane, grp);
       aw.a[1] = anchor_expi<GQ>(p, sm, lane + 32, grp);
@@ -630,26 +692,29 @@ __device__ __forceinline__ void k_logits_nuq_st(const DecodeParams& p, DecodeSme
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int j = lane + 32 * h;
-      ap[(j >> 1) * 4 + (j & 1)] = aw.a[h].x;
-      ap[(j >> 1) * 4 + 2 + (j & 1)] = aw.a[h].y;
+      const float2 a1 = cmul(aw.a[h], aw.half[h]);
+      ap0[(j >> 1) * 4 + (j & 1)] = aw.a[h].x;
+      ap0[(j >> 1) * 4 + 2 + (j & 1)] = aw.a[h].y;
+      ap1[(j >> 1) * 4 + (j & 1)] = a1.x;
+      ap1[(j >> 1) * 4 + 2 + (j & 1)] = a1.y;
       aw.a[h] = cmul(aw.a[h], aw.step[h]);  // the anchor of this warp's next group
     }
     --aw.left;
     __syncwarp();
     // two channel pairs at a time in packed fp32x2 arithmetic (W laid out like the anchors)
-    const float4* tab4 = reinterpret_cast<const float4*>(tab);
-    const float4* anc4 = reinterpret_cast<const float4*>(ap);
+    const float4* tab4 = reinterpret_cast<const float4*>(tab) + (lane & 15);
+    const float4* anc4 = reinterpret_cast<const float4*>(lane < 16 ? ap0 : ap1);
     const float2 S2 = make_float2(ms.y, ms.y), M2 = make_float2(ms.x, ms.x);
+    const uint32_t loff = (uint32_t)(lane & 15) * 8u;
     float2 z2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < kHeadDim / 2; j += 2) {
       const float4 A4 = anc4[j >> 1];
-      const float4 W4 = tab4[(j >> 1) * kGroupTokens + lane];
+      const float4 W4 = tab4[(j >> 1) * 16];
       const float2 Ax = make_float2(A4.x, A4.y), Ay = make_float2(A4.z, A4.w);
       const float2 Wx = make_float2(W4.x, W4.y), Wy = make_float2(W4.z, W4.w);
-      const float2 a2 = __ffma2_rn(S2, make_float2(sm.lut_k[code3(wd, j)], sm.lut_k[code3(wd, j + 1)]), M2);
-      const float2 b2 = __ffma2_rn(
-          S2, make_float2(sm.lut_k[code3(wd, j + kHeadDim / 2)], sm.lut_k[code3(wd, j + 1 + kHeadDim / 2)]), M2);
+      const float2 a2 = __ffma2_rn(S2, pair_levels(ptab_k, wd, j, loff), M2);
+      const float2 b2 = __ffma2_rn(S2, pair_levels(ptab_k, wd, j + kHeadDim / 2, loff), M2);
       const float2 cx = __ffma2_rn(Ax, a2, __fmul2_rn(make_float2(-Ay.x, -Ay.y), b2));  // ax a - ay b
       const float2 cy = __ffma2_rn(Ax, b2, __fmul2_rn(Ay, a2));                          // ax b + ay a
       z2 = __ffma2_rn(Wx, cx, __ffma2_rn(make_float2(-Wy.x, -Wy.y), cy, z2));           // Re[W c]
@@ -662,7 +727,7 @@ __device__ __forceinline__ void k_logits_nuq_st(const DecodeParams& p, DecodeSme
       // W and the anchor of pair j as 16-byte loads: the W rows of a lane are
       // 16 bytes apart from its neighbours' whatever their columns (no bank
       // conflicts); pick the pair's components
-      const float4 W4 = tab4[(j >> 1) * kGroupTokens + lane];
+      const float4 W4 = tab4[(j >> 1) * 16];
       const float4 A4 = anc4[j >> 1];
       const bool odd = (j & 1) != 0;
       const float2 WA = cmul(make_float2(odd ? W4.y : W4.x, odd ? W4.w : W4.z),
@@ -703,7 +768,8 @@ __device__ __forceinline__ void k_logits_nuq_st(const DecodeParams& p, DecodeSme
 // shared-memory atomics), folded into the accumulators afterwards.
 template <int GQ>
 __device__ __forceinline__ void v_accumulate_nuq_st(const DecodeParams& p, DecodeSmem<GQ>& sm,
-                                                    const unsigned char* st, float* obuf, int lane, int w,
+                                                    const unsigned char* st, const unsigned char* ptab_v,
+                                                    float* obuf, int lane, int w,
                                                     float (&acc)[GQ][4], float (&macc)[GQ]) {
   const int k = p.geo.nout;
   const uint32_t* vms = reinterpret_cast<const uint32_t*>(st + NuqStage::VMS);
@@ -720,20 +786,21 @@ __device__ __forceinline__ void v_accumulate_nuq_st(const DecodeParams& p, Decod
     }
     __syncwarp();
   }
+  const uint32_t loff = (uint32_t)(lane & 15) * 8u;
 #pragma unroll 4
   for (int t = 0; t < kGroupTokens; ++t) {
+    // this lane's 12 bits (word wi + 1 of the last row is the next region's
+    // first word: in the stage, and shifted out)
     const uint32_t* rw = reinterpret_cast<const uint32_t*>(st + NuqStage::VC + 48 * t);
-    uint32_t u = rw[wi] >> sh;
-    if (sh > 20) u |= rw[wi + 1] << (32 - sh);
-    float cv[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) cv[e] = sm.lut_v[(u >> (3 * e)) & 7u];
+    const uint32_t u = __funnelshift_r(rw[wi], rw[wi + 1], sh);
+    const float2 c01 = *reinterpret_cast<const float2*>(ptab_v + (((u << 7) & 0x1F80u) | loff));
+    const float2 c23 = *reinterpret_cast<const float2*>(ptab_v + (((u << 1) & 0x1F80u) | loff));
 #pragma unroll
     for (int r = 0; r < GQ; ++r) {
       const float pp = sm.pv[w][t][r];
       const float2 pp2 = make_float2(pp, pp);
-      const float2 a01 = __ffma2_rn(pp2, make_float2(cv[0], cv[1]), make_float2(acc[r][0], acc[r][1]));
-      const float2 a23 = __ffma2_rn(pp2, make_float2(cv[2], cv[3]), make_float2(acc[r][2], acc[r][3]));
+      const float2 a01 = __ffma2_rn(pp2, c01, make_float2(acc[r][0], acc[r][1]));
+      const float2 a23 = __ffma2_rn(pp2, c23, make_float2(acc[r][2], acc[r][3]));
       acc[r][0] = a01.x;
       acc[r][1] = a01.y;
       acc[r][2] = a23.x;
@@ -770,7 +837,9 @@ template <int KB, int VB, int GQ>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   DecodeSmem<GQ>& sm = *reinterpret_cast<DecodeSmem<GQ>*>(smem_raw);
-  float2* rope_e = reinterpret_cast<float2*>(smem_raw + decode_smem_fixed<KB, GQ>());
+  // NUQ: K and V pair tables first
+  unsigned char* nuq_ptab = smem_raw + decode_smem_fixed<KB, GQ>();
+  float2* rope_e = reinterpret_cast<float2*>(nuq_ptab + (KB == 3 ? 2 * kPairTableBytes : 0));
   const Geometry& G = p.geo;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int sp = blockIdx.x, s = blockIdx.y;
@@ -796,7 +865,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     for (int j = tid; j < kHeadDim / 2; j += kThreads)
       anchor_step(p.theta[j], (long long)G.pos_offset + G.S, &sm.anc_v[j], &sm.anc_c0[j]);
   const bool quant_split = sp < p.n_qsplit;
-  if (G.pre_rope && quant_split) {
+  constexpr bool kFolded = KB == 3 && GQ == 1;  // query-folded 16-offset table (built below)
+  if (!kFolded && G.pre_rope && quant_split) {
     // e^{i l theta_j} at [j][l]: a warp reads one j for its 32 token offsets l,
     // 32 consecutive entries (no bank conflicts)
     for (int idx = tid; idx < kGroupTokens * (kHeadDim / 2); idx += kThreads) {
@@ -804,24 +874,31 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
       rope_e[rope_tab_index(j, l)] = expi((double)l * p.theta[j]);
     }
   }
-  // NUQ: per-warp stages, then per-warp outlier buffers (zeroed)
+  // NUQ: per-warp K buffers and stages, then per-warp outlier buffers (zeroed)
   unsigned char* nuq_stages = reinterpret_cast<unsigned char*>(rope_e) +
-                              (G.pre_rope ? sizeof(float2) * kGroupTokens * (kHeadDim / 2) : 0);
-  float* nuq_obuf = reinterpret_cast<float*>(nuq_stages + (KB == 3 ? 8 * NuqStage::bytes(G.nout) : 0));
-  if constexpr (KB == 3)
+                              (G.pre_rope ? rope_region_bytes<KB, GQ>() : 0);
+  float* nuq_obuf = reinterpret_cast<float*>(nuq_stages + (KB == 3 ? 4 * NuqStage::warp_bytes(G.nout) : 0));
+  if constexpr (KB == 3) {
     for (int idx = tid; idx < 4 * GQ * kHeadDim; idx += kThreads) nuq_obuf[idx] = 0.0f;
+    for (int idx = tid; idx < 2 * kPairEntries * kPairCopies; idx += kThreads) {
+      const int f = (idx / kPairCopies) % kPairEntries;
+      const float* L = idx < kPairEntries * kPairCopies ? p.k_lut_off : p.v_lut_off;
+      reinterpret_cast<float2*>(nuq_ptab)[idx] = make_float2(L[f & 7], L[f >> 3]);
+    }
+  }
   __syncthreads();
   if constexpr (KB == 3 && GQ == 1) {
-    // one query head: fold the query into the offset table, W_{j,l} = conj(q_j + i q_{j+64}) e^{i l theta_j}
+    // one query head: the offset table with the query folded in,
+    // W_{j,l} = conj(q_j + i q_{j+64}) e^{i l theta_j}, offsets l < 16
     if (G.pre_rope && quant_split) {
       // W of pairs 2i, 2i+1 for offset l as (x_2i, x_2i+1, y_2i, y_2i+1)
       float4* tab4 = reinterpret_cast<float4*>(rope_e);
-      for (int idx = tid; idx < kGroupTokens * (kHeadDim / 4); idx += kThreads) {
-        const int jp = idx / kGroupTokens, l = idx % kGroupTokens, j = 2 * jp;
-        const float4 e4 = tab4[jp * kGroupTokens + l];  // E_j, E_{j+1} (rope_tab_index layout)
-        const float2 w0 = cmul(make_float2(sm.q[0][j], -sm.q[0][j + kHeadDim / 2]), make_float2(e4.x, e4.y));
-        const float2 w1 = cmul(make_float2(sm.q[0][j + 1], -sm.q[0][j + 1 + kHeadDim / 2]), make_float2(e4.z, e4.w));
-        tab4[jp * kGroupTokens + l] = make_float4(w0.x, w1.x, w0.y, w1.y);
+      for (int idx = tid; idx < 16 * (kHeadDim / 4); idx += kThreads) {
+        const int jp = idx / 16, l = idx % 16, j = 2 * jp;
+        const float2 w0 = cmul(make_float2(sm.q[0][j], -sm.q[0][j + kHeadDim / 2]), expi((double)l * p.theta[j]));
+        const float2 w1 =
+            cmul(make_float2(sm.q[0][j + 1], -sm.q[0][j + 1 + kHeadDim / 2]), expi((double)l * p.theta[j + 1]));
+        tab4[jp * 16 + l] = make_float4(w0.x, w1.x, w0.y, w1.y);
       }
       __syncthreads();
     }
@@ -849,8 +926,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     const int g0 = sp * p.gps;
     const int g1 = min(ngroups, g0 + p.gps);
     const int sb = NuqStage::bytes(G.nout);
-    unsigned char* stw = nuq_stages + w * 2 * sb;
-    const uint32_t stw_s = smem_u32(stw);
+    unsigned char* kbw = nuq_stages + w * NuqStage::warp_bytes(G.nout);  // this warp's K buffer
+    unsigned char* stw = kbw + NuqStage::KBUF;                           // and its two stages
+    const uint32_t kbw_s = smem_u32(kbw), stw_s = smem_u32(stw);
     float* obuf = nuq_obuf + w * GQ * kHeadDim;
     int cur = 0;
     AnchorWalk aw;
@@ -858,20 +936,28 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     if (G.pre_rope) {
       // e^{i theta_j 4 G_K}: a warp's consecutive groups are 4 apart
 #pragma unroll
-      for (int h = 0; h < 2; ++h) aw.step[h] = expi(4.0 * kGroupTokens * p.theta[lane + 32 * h]);
+      for (int h = 0; h < 2; ++h) {
+        aw.step[h] = expi(4.0 * kGroupTokens * p.theta[lane + 32 * h]);
+        aw.half[h] = expi(16.0 * p.theta[lane + 32 * h]);
+      }
     }
-    if (g0 + w < g1) issue_nuq(p, s, g0 + w, stw_s, lane);
+    if (g0 + w < g1) issue_nuq(p, s, g0 + w, kbw_s, stw_s, lane);
     cp_async_commit();
     for (int grp = g0 + w; grp < g1; grp += 4) {
-      if (grp + 4 < g1) issue_nuq(p, s, grp + 4, stw_s + (cur ^ 1) * sb, lane);
-      cp_async_commit();
-      cp_async_wait<1>();
+      cp_async_wait<0>();
       __syncwarp();
+      // this group's K rows into registers; then the next group streams in
+      // (K rows into the freed buffer, the rest into the other stage)
+      uint32_t wd[13];
+      load_code_row(kbw, lane, wd);
+      __syncwarp();
+      if (grp + 4 < g1) issue_nuq(p, s, grp + 4, kbw_s, stw_s + (cur ^ 1) * sb, lane);
+      cp_async_commit();
       const unsigned char* stc = stw + cur * sb;
       float z[GQ];
-      k_logits_nuq_st<GQ>(p, sm, rope_e, stc, grp, lane, w, z, aw);
+      k_logits_nuq_st<GQ>(p, sm, rope_e, nuq_ptab, wd, stc, grp, lane, w, z, aw);
       softmax_update<GQ>(z, m, lsum, acc, macc, sm.p[w], lane);
-      v_accumulate_nuq_st<GQ>(p, sm, stc, obuf, lane, w, acc, macc);
+      v_accumulate_nuq_st<GQ>(p, sm, stc, nuq_ptab + kPairTableBytes, obuf, lane, w, acc, macc);
       __syncwarp();
       cur ^= 1;
     }
@@ -924,7 +1010,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   float (*stage)[GQ][kHeadDim] = reinterpret_cast<float (*)[GQ][kHeadDim]>(
       KB == 3 ? reinterpret_cast<float*>(nuq_stages) : &sm.work[0][0][0]);
   static_assert(sizeof(sm.work) >= 4 * GQ * kHeadDim * sizeof(float), "merge staging");
-  static_assert(KB != 3 || 8 * NuqStage::bytes(0) >= 4 * GQ * kHeadDim * (int)sizeof(float), "merge staging");
+  static_assert(KB != 3 || 4 * NuqStage::warp_bytes(0) >= 4 * GQ * kHeadDim * (int)sizeof(float), "merge staging");
 #pragma unroll
   for (int r = 0; r < GQ; ++r)
 #pragma unroll
@@ -1032,9 +1118,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
 
 template <int KB, int VB, int GQ>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t st, int* occ) {
-  size_t smem = decode_smem_fixed<KB, GQ>();
-  if (p.geo.pre_rope) smem += sizeof(float2) * kGroupTokens * (kHeadDim / 2);
-  if (KB == 3) smem += 8 * (size_t)NuqStage::bytes(p.geo.nout) + 4 * GQ * kHeadDim * sizeof(float);
+  const size_t smem = decode_smem_bytes<KB, GQ>(p.geo.pre_rope != 0, p.geo.nout);
   static std::atomic<long long> smem_memo[kMemoDevices], occ_memo[kMemoDevices];
   const cudaError_t e = ensure_smem_limit(decode_kernel<KB, VB, GQ>, smem_memo, (int)smem);
   if (e != cudaSuccess) return e;
