@@ -105,6 +105,13 @@ CASES = {
     "nuq_norope_sinks": (3, 3, 1, 8, 2, 777, dict(S=4, R=32, nout=2)),
     "nuq_no_outliers": (3, 3, 1, 2, 2, 300, dict(nout=0)),
     "nuq_hadamard_k4": (3, 3, 1, 1, 1, 333, dict(nout=4, had=1)),
+    # one query head with pre-RoPE keys (the query-folded 16-offset table,
+    # two anchor sets) at 1, 3, 4 and 8 outliers per vector (from 3 on: 3 CTAs
+    # per SM)
+    "nuq_rope_k1": (3, 3, 2, 2, 2, 611, dict(rope=1, nout=1, S=4, R=16)),
+    "nuq_rope_k3": (3, 3, 1, 3, 3, 450, dict(rope=1, nout=3)),
+    "nuq_rope_k4_hadamard": (3, 3, 1, 2, 2, 389, dict(rope=1, nout=4, had=1)),
+    "nuq_rope_k8": (3, 3, 1, 1, 1, 300, dict(rope=1, nout=8)),
     "k8v4_rope": (8, 4, 1, 4, 1, 500, dict(S=4, R=16, rope=1)),
     "k2v2_rope_g8": (2, 2, 1, 8, 1, 300, dict(S=0, R=8, rope=1)),
     "fp16": (16, 16, 2, 8, 2, 777, dict()),
