@@ -41,6 +41,8 @@ constexpr int kRowVec = kRowHalves * 2 / 16;  // 16 x 16-byte chunks per row
 // rint(d / scale) by the IEEE division, out of line: the rare path of the
 // codes below, kept out of their unrolled loops.
 __device__ __noinline__ float rint_div(float d, float scale) { return rintf(__fdiv_rn(d, scale)); }
+// d / s by the IEEE division, out of line (the non-uniform codes' rare path).
+__device__ __noinline__ float div_rn(float d, float s) { return __fdiv_rn(d, s); }
 
 __device__ __forceinline__ uint32_t uniform_code(float x, float mn, float scale, float rs) {
   if (scale == 0.0f) return 0u;
@@ -131,6 +133,20 @@ __device__ __forceinline__ void nuq_midpoints(const float* lut, float (&tau)[7])
   for (int i = 0; i < 7; ++i) tau[i] = __fsub_rn(__fmul_rn(__fadd_rn(lut[i], lut[i + 1]), 0.5f), lut[0]);
 }
 
+// Minimum and maximum of the dense (non-outlier) values of a warp's vector.
+__device__ __forceinline__ void dense_min_max(const float (&v)[4], const bool (&is_out)[4], float& mn, float& mx) {
+  mn = INFINITY;
+  mx = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (!is_out[q]) { mn = fminf(mn, v[q]); mx = fmaxf(mx, v[q]); }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+}
+
 // The k largest |v| of a token vector held by a warp (lane l: channels
 // 4l..4l+3), ties to the lower channel: is_out marks this lane's outliers,
 // sel[j] is the channel of the j-th largest (past k: a value that sorts
@@ -162,16 +178,39 @@ __device__ __forceinline__ void nuq_outliers(const float (&v)[4], int k, int lan
     for (int q = 0; q < 4; ++q)
       if (bi == 4 * lane + q) is_out[q] = true;
   }
-  mn = INFINITY;
-  mx = -INFINITY;
+  dense_min_max(v, is_out, mn, mx);
+}
+
+// The same selection for fp16 values h (v their fp32 widenings), one
+// warp-wide integer maximum per outlier: the key (|h| << 16) | (0xFFFF - c)
+// orders by magnitude (fp16 magnitude bits order like the magnitudes, for
+// finite values) and then by the lower channel c, so its maximum is the
+// largest |x| with ties to the lower channel.
+__device__ __forceinline__ void nuq_outliers_h(const float (&v)[4], const uint16_t (&h)[4], int k, int lane,
+                                               bool (&is_out)[4], int (&sel)[kMaxOutliers], float& mn,
+                                               float& mx) {
+  uint32_t key[4];
 #pragma unroll
-  for (int q = 0; q < 4; ++q)
-    if (!is_out[q]) { mn = fminf(mn, v[q]); mx = fmaxf(mx, v[q]); }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  for (int q = 0; q < 4; ++q) {
+    is_out[q] = false;
+    key[q] = ((uint32_t)(h[q] & 0x7FFFu) << 16) | (0xFFFFu - (uint32_t)(4 * lane + q));
   }
+#pragma unroll
+  for (int j = 0; j < kMaxOutliers; ++j) {
+    sel[j] = 1 << 30;  // past k: sorts last, never written
+    if (j >= k) continue;
+    uint32_t b = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (!is_out[q]) b = max(b, key[q]);
+    b = __reduce_max_sync(0xffffffffu, b);
+    const int bi = (int)(0xFFFFu - (b & 0xFFFFu));
+    sel[j] = bi;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (bi == 4 * lane + q) is_out[q] = true;
+  }
+  dense_min_max(v, is_out, mn, mx);
 }
 
 // Non-uniform (LUT) encoding of one 128-channel token vector held by a warp
@@ -185,12 +224,16 @@ __device__ void nuq_encode_row(const uint16_t* __restrict__ xrow, const float* l
                                uint8_t* __restrict__ code_row, uint32_t* minsc_out,
                                uint8_t* col_out, uint16_t* val_out, int lane) {
   float v[4];
+  uint16_t hb[4];
   bool is_out[4];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) v[q] = half_bits_to_float(xrow[4 * lane + q]);
+  for (int q = 0; q < 4; ++q) {
+    hb[q] = xrow[4 * lane + q];
+    v[q] = half_bits_to_float(hb[q]);
+  }
   int sel[kMaxOutliers];
   float mn, mx;
-  nuq_outliers(v, k, lane, is_out, sel, mn, mx);
+  nuq_outliers_h(v, hb, k, lane, is_out, sel, mn, mx);
   const float s = __fdiv_rn(__fsub_rn(mx, mn), __fsub_rn(lut[7], lut[0]));
   const float rs = s != 0.0f ? __frcp_rn(s) : 0.0f;
 #pragma unroll
@@ -203,7 +246,7 @@ __device__ void nuq_encode_row(const uint16_t* __restrict__ xrow, const float* l
       bool near = false;
 #pragma unroll
       for (int i = 0; i < 7; ++i) near |= fabsf(__fsub_rn(u, tau[i])) <= band;
-      if (near) u = __fdiv_rn(d, s);
+      if (near) u = div_rn(d, s);
 #pragma unroll
       for (int i = 0; i < 7; ++i) c += (u > tau[i]) ? 1u : 0u;
     }

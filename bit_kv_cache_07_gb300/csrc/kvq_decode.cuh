@@ -390,9 +390,6 @@ __device__ __forceinline__ size_t fp16_row_at(const DecodeParams& p, int s, int 
   *pos = ps;
   return ((size_t)s * G.ring + (ps - G.S) % G.ring) * kHeadDim;
 }
-__device__ __forceinline__ size_t fp16_row(const DecodeParams& p, int s, int k, bool* in_sink, int* pos) {
-  return fp16_row_at(p, s, k, p.S_eff, p.Nq, in_sink, pos);
-}
 
 // One 32-token chunk of fp16 tokens (sinks / window, or an fp16 cache) for
 // one warp: lane = token for q.k, lane = 4 channels for p.v.  sq is the
