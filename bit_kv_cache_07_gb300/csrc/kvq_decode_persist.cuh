@@ -322,9 +322,18 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT, IQ>::kCtaThreads
 
   const int gw = blockIdx.x * LY::kWarps + w;  // global warp index
   if (gw >= p.nwarps) return;
-  if constexpr (RG) grid_dep_wait();  // the row tables were written by the kernel before
-  const long long j0 = first_item_at_t<RG>(p, warp_x(p, gw));
-  const long long j1 = first_item_at_t<RG>(p, warp_x(p, gw + 1));
+  long long j0, j1;
+  if constexpr (RG) {
+    grid_dep_wait();  // the row tables were written by the kernel before
+    // the rows of this warp's range by a warp-wide search of the row tables
+    const long long x0 = warp_x(p, gw), x1 = warp_x(p, gw + 1);
+    const int b0 = row_at_warp(p.row_x0, G.B, x0, lane), b1 = row_at_warp(p.row_x0, G.B, x1, lane);
+    j0 = x0 >= p.wtot ? p.row_j0[G.B] : first_item_in_row(p, x0, b0);
+    j1 = x1 >= p.wtot ? p.row_j0[G.B] : first_item_in_row(p, x1, b1);
+  } else {
+    j0 = first_item_at_t<false>(p, warp_x(p, gw));
+    j1 = first_item_at_t<false>(p, warp_x(p, gw + 1));
+  }
   if (j0 >= j1) return;
 
   float O[8][o_tiles<NT>()][4], macc[NT][kNVG], m_used[NT], lsum[NT];
@@ -349,7 +358,8 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT, IQ>::kCtaThreads
   // incrementally, each with its stream's counts (sp, isp: quantized groups,
   // items, fp16 tokens), refreshed when it moves to the next stream
   int s, k;
-  locate_item_t<RG>(p, j0, &s, &k);
+  if constexpr (RG) locate_in_row(p, j0, row_at_warp(p.row_j0, G.B, j0, lane), &s, &k);
+  else locate_item_t<false>(p, j0, &s, &k);
   Walk<RG> sw;
   sw.set(p, s);
   int is = s, ik = k;
@@ -395,8 +405,8 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT, IQ>::kCtaThreads
     if (has_q) stage_quant<VBq, NT, GT, JC>(p, sO, sML, g, lane, O, macc, m_used, lsum);
     staged = staged || has_q;
     const StreamSpan fs = stream_span_t<RG>(p, sf);
-    const int wf = owner_of(p, item_pos_t<RG>(p, fs.first));
-    const int wl = owner_of(p, item_pos_t<RG>(p, fs.first + fs.n_items - 1));
+    const int wf = owner_of(p, item_pos_in(p, fs, 0));
+    const int wl = owner_of(p, item_pos_in(p, fs, fs.n_items - 1));
     finalize_stream<NT, GT>(p, gw + sf, sf, wf, wl - wf + 1, sO, sML, staged, lane, O, m_used, lsum);
     reset();
     has_q = staged = bq_f16 = false;

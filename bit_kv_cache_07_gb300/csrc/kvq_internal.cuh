@@ -305,6 +305,20 @@ __host__ __device__ inline int row_at(const long long* tab, int rows, long long 
   return lo;
 }
 
+#ifdef __CUDACC__
+// row_at by a whole warp (every lane calls it with the same arguments): each
+// lane tests up to 8 rows (rows <= 256) with independent loads, and the rows
+// at or below v are counted by ballot (the entries increase strictly).
+__device__ __forceinline__ int row_at_warp(const long long* tab, int rows, long long v, int lane) {
+  int cnt = 0;
+  for (int r0 = 0; r0 < rows; r0 += 32) {
+    const int r = r0 + lane;
+    cnt += __popc(__ballot_sync(0xffffffffu, r < rows && tab[r] <= v));
+  }
+  return cnt - 1;
+}
+#endif
+
 // floor(x / d) for 0 <= x < 2^56: the device multiplies and shifts (a
 // 64-bit integer division is a long serial emulation there, and fp64 is a
 // narrow pipe on this GPU); the host divides exactly.
@@ -316,6 +330,13 @@ __host__ __device__ inline long long idiv(long long x, long long d, const FastDi
   (void)f;
   return x / d;
 #endif
+}
+
+// floor(x / d) for 0 <= x, 0 < d: in 32 bits when both fit (the usual case;
+// a 64-bit integer division is a long serial emulation on the device).
+__host__ __device__ inline long long udiv(long long x, long long d) {
+  if (((unsigned long long)x | (unsigned long long)d) >> 32 == 0) return (long long)((unsigned)x / (unsigned)d);
+  return x / d;
 }
 
 // Ragged persistent schedule (host): every row's first item and weight
@@ -337,6 +358,13 @@ inline void plan_rows(DecodeParams& p, long long* items, bool* any_groups) {
 // stream after stream, weighted by their bytes; RG selects the ragged
 // schedule at compile time (the wrappers below take p.ragged).
 // (Dividends stay below 2^56: plan_persist checks (wtot + 1) (nwarps + 1) < 2^56.)
+// Ragged schedule, item j of batch row b: its stream s and index k.
+__host__ __device__ inline void locate_in_row(const DecodeParams& p, long long j, int b, int* s, int* k) {
+  const StreamSpan r = row_span(p, b);
+  const long long h = udiv(j - r.first, r.n_items);
+  *s = b * p.geo.Hkv + (int)h;
+  *k = (int)(j - r.first - h * r.n_items);
+}
 // Item j's stream s and index k within it.
 template <bool RG>
 __host__ __device__ inline void locate_item_t(const DecodeParams& p, long long j, int* s, int* k) {
@@ -345,11 +373,7 @@ __host__ __device__ inline void locate_item_t(const DecodeParams& p, long long j
     *s = (int)ss;
     *k = (int)(j - ss * p.n_items);
   } else {
-    const int b = row_at(p.row_j0, p.geo.B, j);
-    const StreamSpan r = row_span(p, b);
-    const long long h = (j - r.first) / r.n_items;
-    *s = b * p.geo.Hkv + (int)h;
-    *k = (int)(j - r.first - h * r.n_items);
+    locate_in_row(p, j, row_at(p.row_j0, p.geo.B, j), s, k);
   }
 }
 template <bool RG>
@@ -364,20 +388,29 @@ __host__ __device__ inline long long item_pos_t(const DecodeParams& p, long long
     return s * p.wstream + (k <= p.ng ? k * p.wq : p.ng * p.wq + (k - p.ng) * p.wt);
   }
 }
+// Start weight of item k of the stream whose span is r (item_pos_t of the
+// stream's first item + k, without locating the stream).
+__host__ __device__ inline long long item_pos_in(const DecodeParams& p, const StreamSpan& r, int k) {
+  return r.x0 + (k <= r.ng ? (long long)k * p.wq : (long long)r.ng * p.wq + (long long)(k - r.ng) * p.wt);
+}
+// Ragged schedule: the first item whose start weight is >= x, for x in
+// batch row b's weights [row_x0[b], row_x0[b + 1]).
+__host__ __device__ inline long long first_item_in_row(const DecodeParams& p, long long x, int b) {
+  const StreamSpan r = row_span(p, b);
+  const long long h = udiv(x - r.x0, r.wstream), rem = x - r.x0 - h * r.wstream;
+  const long long f = r.first + h * r.n_items;  // the stream's first item
+  if (rem == 0) return f;
+  long long k;
+  if (rem <= (long long)r.ng * p.wq) k = udiv(rem + p.wq - 1, p.wq);
+  else k = r.ng + udiv(rem - (long long)r.ng * p.wq + p.wt - 1, p.wt);
+  return f + k;  // k == n_items: the next stream's first item
+}
 // First item whose start weight is >= x (x in [0, wtot]).
 template <bool RG>
 __host__ __device__ inline long long first_item_at_t(const DecodeParams& p, long long x) {
   if constexpr (RG) {
     if (x >= p.wtot) return p.row_j0[p.geo.B];
-    const int b = row_at(p.row_x0, p.geo.B, x);
-    const StreamSpan r = row_span(p, b);
-    const long long h = (x - r.x0) / r.wstream, rem = x - r.x0 - h * r.wstream;
-    const long long f = r.first + h * r.n_items;  // the stream's first item
-    if (rem == 0) return f;
-    long long k;
-    if (rem <= (long long)r.ng * p.wq) k = (rem + p.wq - 1) / p.wq;
-    else k = r.ng + (rem - (long long)r.ng * p.wq + p.wt - 1) / p.wt;
-    return f + k;  // k == n_items: the next stream's first item
+    return first_item_in_row(p, x, row_at(p.row_x0, p.geo.B, x));
   } else {
     long long s = idiv(x, p.wstream, p.fd_wstream), rem = x - s * p.wstream, k;
     if (rem == 0) return s * p.n_items;
