@@ -208,3 +208,20 @@ def test_ragged_innerq_append_and_decode(B):
     torch.cuda.synchronize()
     refs = check_rows(layer, cfg, lengths, K.cpu().numpy(), V.cpu().numpy(), norm_tokens=lengths)
     check_ragged_decode(B, layer, cfg, lengths, refs, seed=1)
+
+
+@pytest.mark.parametrize("rows,hi", [(70, 300), (256, 80)])
+def test_ragged_many_rows(B, rows, hi):
+    """More batch rows than a warp has lanes (the decode finds a warp's rows
+    by a ballot over 32 rows at a time), up to the 256-row limit; rows from
+    one token to a few groups, many with no quantized group at all."""
+    from bit_kv_cache_07_gb300 import synth
+    rng = np.random.default_rng(rows)
+    lengths = [int(x) for x in rng.integers(1, hi + 1, rows)]
+    cfg = cfg_of(4, 4, rows, 2, 1, hi + 8, n_sink=4, n_recent=16)
+    K, V = synth.random_kv(rows, 1, hi, seed=rows, device="cuda")
+    layer = B.Layer(cfg)
+    layer.append_ragged([0] * rows, lengths, K, V)
+    torch.cuda.synchronize()
+    refs = check_rows(layer, cfg, lengths, K.cpu().numpy(), V.cpu().numpy())
+    check_ragged_decode(B, layer, cfg, lengths, refs, seed=rows + 1)
