@@ -39,6 +39,9 @@ int main() {
         std::set<int> ws;
         for (int k = 0; k < p.n_items; ++k) ws.insert(own[(long long)s * p.n_items + k]);
         int wf = owner_of(p, item_pos(p, (long long)s * p.n_items)), wl = owner_of(p, item_pos(p, (long long)s * p.n_items + p.n_items - 1));
+        const StreamSpan sp = stream_span(p, s);  // positions from the stream's span (the kernel's stream ends)
+        for (int k = 0; k < p.n_items; ++k)
+          if (item_pos_in(p, sp, k) != item_pos(p, (long long)s * p.n_items + k)) { printf("span position\n"); ++bad; }
         if ((int)ws.size() != wl - wf + 1) { printf("count mismatch s=%d\n", s); ++bad; }
         for (int w : ws) { if (!slots.insert(w + s).second) { printf("slot clash\n"); ++bad; } if (w + s >= nw + NS) ++bad; }
       }
@@ -95,9 +98,17 @@ int main() {
           locate_item(p, j, &s2, &k2);
           if (s2 != s || k2 != k) { printf("ragged locate j=%lld\n", j); ++bad; }
           if (item_pos(p, j) != sp.x0 + (k <= sp.ng ? k * p.wq : sp.ng * p.wq + (k - sp.ng) * p.wt)) ++bad;
+          if (item_pos_in(p, sp, k) != item_pos(p, j)) { printf("ragged span position\n"); ++bad; }
         }
       }
       if (j != items) ++bad;
+      // the device's warp search: (rows with an entry <= v) - 1 is row_at
+      for (int t = 0; t < 64; ++t) {
+        const long long vx = (long long)(rr() % (unsigned long long)p.wtot), vj = (long long)(rr() % (unsigned long long)items);
+        int cx = 0, cj = 0;
+        for (int r = 0; r < p.geo.B; ++r) { cx += p.row_x0[r] <= vx; cj += p.row_j0[r] <= vj; }
+        if (cx - 1 != row_at(p.row_x0, p.geo.B, vx) || cj - 1 != row_at(p.row_j0, p.geo.B, vj)) { printf("row count\n"); ++bad; }
+      }
       std::vector<int> own(items, -1);
       for (int i = 0; i < nw; ++i) {
         const long long j0 = first_item_at(p, warp_x(p, i)), j1 = first_item_at(p, warp_x(p, i + 1));
@@ -117,6 +128,16 @@ int main() {
         if ((int)ws.size() != wl - wf + 1) { printf("ragged count mismatch s=%d\n", s); ++bad; }
         for (int w : ws) { if (!slots.insert(w + s).second) ++bad; if (w + s >= nw + NS) ++bad; }
       }
+    }
+  }
+  // udiv: 32-bit when both operands fit, exact either way
+  {
+    unsigned long long us = 0x9E3779B97F4A7C15ull;
+    auto ur = [&]() { us ^= us << 13; us ^= us >> 7; us ^= us << 17; return us; };
+    for (int t = 0; t < 200000; ++t) {
+      const int sx = (int)(ur() % 60), sd = (int)(ur() % 40);
+      const long long x = (long long)(ur() >> (64 - 1 - sx) >> 1), d = (long long)(ur() >> (64 - 1 - sd) >> 1) + 1;
+      if (udiv(x, d) != x / d) { printf("udiv %lld %lld\n", x, d); ++bad; break; }
     }
   }
   // multiply-shift division: exact for 0 <= x < 2^56, any d >= 1
