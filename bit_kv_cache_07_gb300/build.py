@@ -17,7 +17,9 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkvq.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", *ARCH]
+# hidden symbol visibility: the library exports only the C ABI (KVQ_API in
+# include/kvq.h), so its template instances and kernels stay private to it
+NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden", *ARCH]
 
 
 def _nvcc() -> str:
@@ -32,7 +34,8 @@ def sources() -> list[str]:
 
 
 def _deps() -> list[str]:
-    return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + [os.path.join(ROOT, "include", "kvq.h")]
+    return (sources() + glob.glob(os.path.join(CSRC, "*.cuh")) +
+            [os.path.join(ROOT, "include", "kvq.h"), os.path.abspath(__file__)])  # this file: the flags
 
 
 def up_to_date() -> bool:

@@ -36,6 +36,15 @@
 
 #include <stdint.h>
 
+/* The library is built with hidden symbol visibility: only the calls below
+ * are exported (so that two builds loaded into one process do not bind to
+ * each other's internal symbols). */
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -208,7 +217,7 @@ typedef struct kvq_layout {
  * buffer size and the decode workspace size for `cfg`.
  * Returns KVQ_ERR_INVALID_ARG for null pointers or inconsistent sizes,
  * KVQ_ERR_UNSUPPORTED for combinations the kernels are not built for. */
-kvq_status kvq_layout_query(const kvq_config *cfg, kvq_layout *out);
+KVQ_API kvq_status kvq_layout_query(const kvq_config *cfg, kvq_layout *out);
 
 /* kvq_append -- write n_new tokens per sequence into the cache.
  * ("KVTuner" review, online quantization at the fixed per-layer pair;
@@ -228,7 +237,7 @@ kvq_status kvq_layout_query(const kvq_config *cfg, kvq_layout *out);
  * groups are flushed, then one copy kernel for the fp16 tokens.
  * Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CAPACITY,
  * KVQ_ERR_CUDA. */
-kvq_status kvq_append(const kvq_config *cfg, void *layer_buf, int32_t tokens_before,
+KVQ_API kvq_status kvq_append(const kvq_config *cfg, void *layer_buf, int32_t tokens_before,
                       const uint16_t *k_new, const uint16_t *v_new, int32_t n_new,
                       kvq_stream_t stream);
 
@@ -256,7 +265,7 @@ kvq_status kvq_append(const kvq_config *cfg, void *layer_buf, int32_t tokens_bef
  * Hadamard rotation to the quantized part.
  * Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CAPACITY,
  * KVQ_ERR_WORKSPACE, KVQ_ERR_CUDA. */
-kvq_status kvq_decode_attn(const kvq_config *cfg, const void *layer_buf, int32_t tokens,
+KVQ_API kvq_status kvq_decode_attn(const kvq_config *cfg, const void *layer_buf, int32_t tokens,
                            const uint16_t *q, uint16_t *out, float *lse,
                            void *workspace, uint64_t ws_bytes, kvq_stream_t stream);
 
@@ -265,7 +274,7 @@ kvq_status kvq_decode_attn(const kvq_config *cfg, const void *layer_buf, int32_t
  * groups; host only, for measurement.  With split_tokens = 0 the decode
  * itself may raise the quantized splits (up to 64) so that its grid fills
  * whole waves of the kernel's resident CTAs on the device it runs on. */
-kvq_status kvq_decode_plan(const kvq_config *cfg, int32_t tokens, int32_t *splits_per_stream,
+KVQ_API kvq_status kvq_decode_plan(const kvq_config *cfg, int32_t tokens, int32_t *splits_per_stream,
                            int32_t *quantized_splits);
 
 /* Which decode kernel kvq_decode_attn launches for `tokens` (host only, for
@@ -275,7 +284,7 @@ kvq_status kvq_decode_plan(const kvq_config *cfg, int32_t tokens, int32_t *split
  * pre-RoPE K, 32- or 128-channel V groups).  *gq_slots = query-head slots per
  * KV head the kernel is instantiated for (1, 2, 4 or 8).
  * Errors: KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CAPACITY. */
-kvq_status kvq_decode_path(const kvq_config *cfg, int32_t tokens, int32_t *persistent, int32_t *gq_slots);
+KVQ_API kvq_status kvq_decode_path(const kvq_config *cfg, int32_t tokens, int32_t *persistent, int32_t *gq_slots);
 
 /* kvq_append_ragged -- kvq_append for sequences of different lengths.
  * The pages attend one context length per call; a batch of sequences at
@@ -294,7 +303,7 @@ kvq_status kvq_decode_path(const kvq_config *cfg, int32_t tokens, int32_t *persi
  * counts are copied into the layer buffer's `rows` region (a small kernel
  * on `stream`) for the append kernels that follow.
  * Errors: as kvq_append; KVQ_ERR_UNSUPPORTED when batch > 256. */
-kvq_status kvq_append_ragged(const kvq_config *cfg, void *layer_buf, const int32_t *tokens_before,
+KVQ_API kvq_status kvq_append_ragged(const kvq_config *cfg, void *layer_buf, const int32_t *tokens_before,
                              const int32_t *n_new, const uint16_t *k_new, const uint16_t *v_new,
                              int32_t n_stride, kvq_stream_t stream);
 
@@ -309,7 +318,7 @@ kvq_status kvq_append_ragged(const kvq_config *cfg, void *layer_buf, const int32
  * the split-K kernel is planned for the longest row (a stream's splits past
  * its own tokens contribute nothing).
  * Errors: as kvq_decode_attn; KVQ_ERR_UNSUPPORTED when batch > 256. */
-kvq_status kvq_decode_attn_ragged(const kvq_config *cfg, const void *layer_buf, const int32_t *tokens,
+KVQ_API kvq_status kvq_decode_attn_ragged(const kvq_config *cfg, const void *layer_buf, const int32_t *tokens,
                                   const uint16_t *q, uint16_t *out, float *lse,
                                   void *workspace, uint64_t ws_bytes, kvq_stream_t stream);
 
@@ -334,7 +343,7 @@ kvq_status kvq_decode_attn_ragged(const kvq_config *cfg, const void *layer_buf, 
  *   (kvq_decode_plan) is used as is.
  * Errors: as kvq_decode_attn; KVQ_ERR_WORKSPACE when this call's scratch
  * (split counters + per-split partials) would exceed 8 MiB. */
-kvq_status kvq_decode_attn_noalloc(const kvq_config *cfg, const void *layer_buf, int32_t tokens,
+KVQ_API kvq_status kvq_decode_attn_noalloc(const kvq_config *cfg, const void *layer_buf, int32_t tokens,
                                    const uint16_t *q, uint16_t *out, float *lse,
                                    kvq_stream_t stream);
 
@@ -368,7 +377,7 @@ kvq_status kvq_decode_attn_noalloc(const kvq_config *cfg, const void *layer_buf,
  * Three launches on `stream` (a memset and two kernels).  Errors:
  * KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_WORKSPACE, KVQ_ERR_CUDA. */
 #define KVQ_NUQ_FIT_WORKSPACE_BYTES (3ull * 65538ull * 8ull)
-kvq_status kvq_fit_nuq_lut(const uint16_t *x, int64_t n_vectors, int32_t head_dim, int32_t outliers,
+KVQ_API kvq_status kvq_fit_nuq_lut(const uint16_t *x, int64_t n_vectors, int32_t head_dim, int32_t outliers,
                            int32_t hadamard, int32_t max_iters, void *workspace, uint64_t ws_bytes,
                            float *lut_out, int32_t *info_out, kvq_stream_t stream);
 
@@ -394,7 +403,7 @@ kvq_status kvq_fit_nuq_lut(const uint16_t *x, int64_t n_vectors, int32_t head_di
  * cfg's k_bits / v_bits are ignored (bits applies); non-uniform and fp16
  * configs are not supported.  Errors: KVQ_ERR_INVALID_ARG,
  * KVQ_ERR_UNSUPPORTED, KVQ_ERR_WORKSPACE, KVQ_ERR_CUDA. */
-kvq_status kvq_measure_distortion(const kvq_config *cfg, const uint16_t *k, const uint16_t *v, int32_t n_tokens,
+KVQ_API kvq_status kvq_measure_distortion(const kvq_config *cfg, const uint16_t *k, const uint16_t *v, int32_t n_tokens,
                                   int32_t bits, void *workspace, uint64_t ws_bytes, double *mse_out,
                                   kvq_stream_t stream);
 
@@ -410,7 +419,7 @@ kvq_status kvq_measure_distortion(const kvq_config *cfg, const uint16_t *k, cons
  * (the continuous reverse water-filling optimum b_i with sum b_i =
  * total_bits, from w_i alpha_i ln(beta_i) beta_i^-b_i equal for all i) may
  * be NULL.  Errors: KVQ_ERR_INVALID_ARG. */
-kvq_status kvq_rate_allocate(int32_t n, const double *distortion, const double *weights, int32_t total_bits,
+KVQ_API kvq_status kvq_rate_allocate(int32_t n, const double *distortion, const double *weights, int32_t total_bits,
                              int32_t *bits_out, double *alpha_out, double *beta_out, double *waterfill_out);
 
 /* Context-parallel decode (KVQuant summary, abstract and main results: a
@@ -434,7 +443,7 @@ kvq_status kvq_rate_allocate(int32_t n, const double *distortion, const double *
  * takes part in the merge as an empty part, lse = -inf, and is not decoded).
  * Errors: KVQ_ERR_INVALID_ARG (n_shards < 1 or > 65536, shard out of range,
  * tokens < 1), KVQ_ERR_CAPACITY, and the config errors of kvq_layout_query. */
-kvq_status kvq_context_shard(const kvq_config *cfg, int32_t tokens, int32_t n_shards, int32_t shard,
+KVQ_API kvq_status kvq_context_shard(const kvq_config *cfg, int32_t tokens, int32_t n_shards, int32_t shard,
                              kvq_config *shard_cfg, int32_t *first_token, int32_t *shard_tokens);
 
 /* kvq_merge_attn -- attention over the union of n_parts disjoint parts of a
@@ -449,11 +458,11 @@ kvq_status kvq_context_shard(const kvq_config *cfg, int32_t tokens, int32_t n_sh
  * rows = batch * n_q_heads; head_dim = 128.  One launch, fp32 arithmetic.
  * Errors: KVQ_ERR_INVALID_ARG (n_parts < 1, rows < 0, null or misaligned
  * pointers), KVQ_ERR_UNSUPPORTED (head_dim), KVQ_ERR_CUDA. */
-kvq_status kvq_merge_attn(int32_t n_parts, int64_t rows, int32_t head_dim, const uint16_t *outs,
+KVQ_API kvq_status kvq_merge_attn(int32_t n_parts, int64_t rows, int32_t head_dim, const uint16_t *outs,
                           const float *lses, uint16_t *out, float *lse_out, kvq_stream_t stream);
 
 /* Static string naming a status code. */
-const char *kvq_status_string(kvq_status status);
+KVQ_API const char *kvq_status_string(kvq_status status);
 
 #ifdef __cplusplus
 }
