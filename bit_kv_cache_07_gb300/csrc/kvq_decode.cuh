@@ -844,7 +844,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
   // this stream's tokens: the call's T, or its batch row's in a ragged call
   int T_s = p.T, S_eff = p.S_eff, Nq = p.Nq, Wn = p.W;
   if (p.ragged) {
-    T_s = p.row_tokens[b];
+    T_s = rows_tokens(p)[b];
     window_counts(G, T_s, &S_eff, &Nq, &Wn);
   }
 

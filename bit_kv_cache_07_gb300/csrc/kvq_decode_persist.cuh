@@ -324,12 +324,14 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT, IQ>::kCtaThreads
   if (gw >= p.nwarps) return;
   long long j0, j1;
   if constexpr (RG) {
-    grid_dep_wait();  // the row tables were written by the kernel before
+    // tables in the workspace were written by the kernel before; inline
+    // ones need nothing earlier (the schedule overlaps that kernel)
+    if (!p.rows_inline) grid_dep_wait();
     // the rows of this warp's range by a warp-wide search of the row tables
     const long long x0 = warp_x(p, gw), x1 = warp_x(p, gw + 1);
-    const int b0 = row_at_warp(p.row_x0, G.B, x0, lane), b1 = row_at_warp(p.row_x0, G.B, x1, lane);
-    j0 = x0 >= p.wtot ? p.row_j0[G.B] : first_item_in_row(p, x0, b0);
-    j1 = x1 >= p.wtot ? p.row_j0[G.B] : first_item_in_row(p, x1, b1);
+    const int b0 = row_at_warp(rows_x0(p), G.B, x0, lane), b1 = row_at_warp(rows_x0(p), G.B, x1, lane);
+    j0 = x0 >= p.wtot ? rows_j0(p)[G.B] : first_item_in_row(p, x0, b0);
+    j1 = x1 >= p.wtot ? rows_j0(p)[G.B] : first_item_in_row(p, x1, b1);
   } else {
     j0 = first_item_at_t<false>(p, warp_x(p, gw));
     j1 = first_item_at_t<false>(p, warp_x(p, gw + 1));
@@ -358,7 +360,7 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT, IQ>::kCtaThreads
   // incrementally, each with its stream's counts (sp, isp: quantized groups,
   // items, fp16 tokens), refreshed when it moves to the next stream
   int s, k;
-  if constexpr (RG) locate_in_row(p, j0, row_at_warp(p.row_j0, G.B, j0, lane), &s, &k);
+  if constexpr (RG) locate_in_row(p, j0, row_at_warp(rows_j0(p), G.B, j0, lane), &s, &k);
   else locate_item_t<false>(p, j0, &s, &k);
   Walk<RG> sw;
   sw.set(p, s);

@@ -590,12 +590,22 @@ kvq_status kvq_decode_attn_ragged(const kvq_config* cfg, const void* layer_buf, 
   if (st != KVQ_OK) return st;
   const uint64_t tab_off = align_up(need);
   if (ws_bytes < tab_off + kRaggedTableBytes) return KVQ_ERR_WORKSPACE;
-  RaggedTables* dt = reinterpret_cast<RaggedTables*>(static_cast<char*>(workspace) + tab_off);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (launch_ragged_tables(ht, dt, cs) != cudaSuccess) return KVQ_ERR_CUDA;
-  p.row_tokens = dt->tokens;
-  p.row_j0 = dt->j0;
-  p.row_x0 = dt->x0;
+  if (cfg->batch <= kInlineRows) {
+    // few rows: the tables travel in the launch parameters
+    for (int b = 0; b <= cfg->batch; ++b) {
+      if (b < cfg->batch) p.in_tokens[b] = ht.tokens[b];
+      p.in_j0[b] = ht.j0[b];
+      p.in_x0[b] = ht.x0[b];
+    }
+    p.rows_inline = 1;
+  } else {
+    RaggedTables* dt = reinterpret_cast<RaggedTables*>(static_cast<char*>(workspace) + tab_off);
+    if (launch_ragged_tables(ht, dt, cs) != cudaSuccess) return KVQ_ERR_CUDA;
+    p.row_tokens = dt->tokens;
+    p.row_j0 = dt->j0;
+    p.row_x0 = dt->x0;
+  }
   return decode_launch(&p, persistent, workspace, cs);
 }
 

@@ -22,6 +22,9 @@ constexpr int kThreads = 128;      // threads per CTA of the append and split-de
 // Sequences of different lengths in one call (kvq_decode_attn_ragged,
 // kvq_append_ragged): at most this many batch rows.
 constexpr int kMaxRaggedRows = 256;
+// Ragged decodes of at most this many rows carry their row tables in the
+// launch parameters (no copy kernel ahead of the decode).
+constexpr int kInlineRows = 16;
 
 // Geometry derived once on the host from a kvq_config.
 struct Geometry {
@@ -233,7 +236,24 @@ struct DecodeParams {
   const int* row_tokens;
   long long* row_j0;
   long long* row_x0;
+  // ragged decode of at most kInlineRows rows: the same tables inline (the
+  // kernels read them from the parameters; the pointers above stay the
+  // host's)
+  int rows_inline;
+  int in_tokens[kInlineRows];
+  long long in_j0[kInlineRows + 1], in_x0[kInlineRows + 1];
 };
+
+// The row tables a ragged decode reads: inline or through the pointers.
+__host__ __device__ inline const int* rows_tokens(const DecodeParams& p) {
+  return p.rows_inline ? p.in_tokens : p.row_tokens;
+}
+__host__ __device__ inline const long long* rows_j0(const DecodeParams& p) {
+  return p.rows_inline ? p.in_j0 : p.row_j0;
+}
+__host__ __device__ inline const long long* rows_x0(const DecodeParams& p) {
+  return p.rows_inline ? p.in_x0 : p.row_x0;
+}
 
 // A ragged decode's per-row tables, as the host builds them and as a copy
 // kernel writes them into the workspace (behind the split counters and
@@ -258,14 +278,14 @@ struct StreamSpan {
 __host__ __device__ inline StreamSpan row_span(const DecodeParams& p, int b) {
   StreamSpan r;
   int W;
-  window_counts(p.geo, p.row_tokens[b], &r.S_eff, &r.Nq, &W);
+  window_counts(p.geo, rows_tokens(p)[b], &r.S_eff, &r.Nq, &W);
   r.k1 = r.S_eff + W;
   r.ng = p.geo.fp16_mode ? 0 : r.Nq / kGroupTokens;
   r.nt = (r.k1 + kPersistF16Tokens - 1) / kPersistF16Tokens;
   r.n_items = r.ng + r.nt;
   r.wstream = (long long)r.ng * p.wq + (long long)r.nt * p.wt;
-  r.first = p.row_j0[b];
-  r.x0 = p.row_x0[b];
+  r.first = rows_j0(p)[b];
+  r.x0 = rows_x0(p)[b];
   return r;
 }
 // RG: the ragged schedule (compile-time in the kernel, p.ragged on the host)
@@ -373,7 +393,7 @@ __host__ __device__ inline void locate_item_t(const DecodeParams& p, long long j
     *s = (int)ss;
     *k = (int)(j - ss * p.n_items);
   } else {
-    locate_in_row(p, j, row_at(p.row_j0, p.geo.B, j), s, k);
+    locate_in_row(p, j, row_at(rows_j0(p), p.geo.B, j), s, k);
   }
 }
 template <bool RG>
@@ -409,8 +429,8 @@ __host__ __device__ inline long long first_item_in_row(const DecodeParams& p, lo
 template <bool RG>
 __host__ __device__ inline long long first_item_at_t(const DecodeParams& p, long long x) {
   if constexpr (RG) {
-    if (x >= p.wtot) return p.row_j0[p.geo.B];
-    return first_item_in_row(p, x, row_at(p.row_x0, p.geo.B, x));
+    if (x >= p.wtot) return rows_j0(p)[p.geo.B];
+    return first_item_in_row(p, x, row_at(rows_x0(p), p.geo.B, x));
   } else {
     long long s = idiv(x, p.wstream, p.fd_wstream), rem = x - s * p.wstream, k;
     if (rem == 0) return s * p.n_items;

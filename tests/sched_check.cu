@@ -83,6 +83,35 @@ int main() {
       p.fd_nwarps = make_fastdiv(p.nwarps);
       p.fd_wtot = make_fastdiv(p.wtot);
       ++cases;
+      if (p.geo.B <= kInlineRows) {
+        // the same schedule from inline tables (the pointers aimed at zeros)
+        static RaggedTables zero;
+        DecodeParams q = p;
+        q.rows_inline = 1;
+        for (int b = 0; b <= p.geo.B; ++b) {
+          if (b < p.geo.B) q.in_tokens[b] = tab.tokens[b];
+          q.in_j0[b] = tab.j0[b];
+          q.in_x0[b] = tab.x0[b];
+        }
+        q.row_tokens = zero.tokens;
+        q.row_j0 = zero.j0;
+        q.row_x0 = zero.x0;
+        for (long long i = 0; i <= nw; ++i)
+          if (first_item_at(q, warp_x(q, i)) != first_item_at(p, warp_x(p, i))) { printf("inline range\n"); ++bad; }
+        for (int s = 0; s < NS; ++s) {
+          const StreamSpan a = stream_span(p, s), c = stream_span(q, s);
+          if (a.first != c.first || a.x0 != c.x0 || a.n_items != c.n_items || a.ng != c.ng || a.k1 != c.k1) {
+            printf("inline span\n");
+            ++bad;
+          }
+        }
+        for (long long jj = 0; jj < items; ++jj) {
+          int s1, k1, s2, k2;
+          locate_item(p, jj, &s1, &k1);
+          locate_item(q, jj, &s2, &k2);
+          if (s1 != s2 || k1 != k2) { printf("inline locate\n"); ++bad; }
+        }
+      }
       // items of every stream: their count and positions from the stream's own length
       long long j = 0;
       for (int s = 0; s < NS; ++s) {
