@@ -310,8 +310,10 @@ KVQ_API kvq_status kvq_append_ragged(const kvq_config *cfg, void *layer_buf, con
 /* kvq_decode_attn_ragged -- kvq_decode_attn for sequences of different
  * lengths: batch row b attends over its own tokens[b] tokens.
  *   tokens     host int32 [batch], 1 <= tokens[b] <= max_tokens
- *   workspace  always required, ws_bytes >= layout.workspace_bytes: the row
- *              tables are copied into its end (a small kernel on `stream`)
+ *   workspace  always required, ws_bytes >= layout.workspace_bytes: with
+ *              more than 16 rows the row tables are copied into its end (a
+ *              small kernel on `stream`); up to 16 rows they travel in the
+ *              launch parameters
  *   other arguments as kvq_decode_attn.
  * Runs the kernel kvq_decode_attn would: the persistent kernel lays every
  * stream's own work items end to end and cuts them into equal byte ranges;
