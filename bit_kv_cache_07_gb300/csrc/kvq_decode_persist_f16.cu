@@ -49,11 +49,17 @@ cudaError_t plan_persist(DecodeParams& p, uint64_t* ws_need) {
   p.ng = G.fp16_mode ? 0 : p.Nq / kGroupTokens;
   p.nt = (p.S_eff + p.W + mma::kF16Tokens - 1) / mma::kF16Tokens;
   p.n_items = p.ng + p.nt;
-  // bytes an item reads: a quantized group (codes, K scales, V scales) or an fp16 item's K and V rows
-  p.wq = G.fp16_mode ? 1
-                     : (long long)kGroupTokens * (G.krow + G.vrow) + (G.gkc ? kGroupTokens * G.nkg * 4 : kHeadDim * 4) +
-                           kGroupTokens * G.nvg * 4;
-  p.wt = (long long)mma::kF16Tokens * kHeadDim * 2 * 2;
+  // item weights the warps' ranges are cut by.  fp16 cache: an item's bytes.
+  // Quantized cache: every item weighs the bytes of a quantized group (its
+  // codes, K scales and V scales), the fp16 items of the sinks and window
+  // included: measured per warp, an 8-token fp16 item takes about as long as
+  // a 32-token group at any bit width (both bound by per-item work), and with
+  // byte weights the warps holding a stream's fp16 items (and its end)
+  // finished last: the 32k mixed-pair step took 2.7 % longer
+  const long long wgroup = (long long)kGroupTokens * (G.krow + G.vrow) +
+                           (G.gkc ? kGroupTokens * G.nkg * 4 : kHeadDim * 4) + kGroupTokens * G.nvg * 4;
+  p.wq = G.fp16_mode ? 1 : wgroup;
+  p.wt = G.fp16_mode ? (long long)mma::kF16Tokens * kHeadDim * 2 * 2 : wgroup;
   p.wstream = (long long)p.ng * p.wq + (long long)p.nt * p.wt;
   p.wtot = (long long)G.NS * p.wstream;
   long long items = (long long)G.NS * p.n_items;
