@@ -146,7 +146,8 @@ __device__ __forceinline__ void stage_quant(const DecodeParams& p, float* sO, fl
 // End of this warp's piece of stream s: combine the staged quantized part
 // (if any) with the fp16 part held in O (plain channel order), store the
 // slot, take a ticket, and merge the stream if this was the last piece.
-template <int NT, int GT>
+// PAIR: merge two heads at a time (see below)
+template <int NT, int GT, bool PAIR>
 __device__ __forceinline__ void finalize_stream(const DecodeParams& p, int slot, int s, int wf, int count, float* sO,
                                                 float* sML, bool staged, int lane,
                                                 const float (&O)[8][o_tiles<NT>()][4],
@@ -208,61 +209,97 @@ __device__ __forceinline__ void finalize_stream(const DecodeParams& p, int slot,
   // Lane q reads slot q's (m, l); the first kMB slots' accumulators are read
   // in the same round trip (4 channels per lane), later ones kMB at a time.
   // Single-head streams have ~10 slots and registers to spare at this point
-  // (measured: 16 at a time is faster there, 8 for larger groups).
+  // (measured: 16 at a time is faster there, 8 for larger groups).  With
+  // PAIR, heads are merged two at a time so that their reads share the
+  // round trips: one head after the other, the merges of a 4-head stream's
+  // ~14 slots were the last ~8 µs of a 32k layer.  Measured per layer kind,
+  // pairing is faster for 8-bit keys, InnerQ keys and 8 head slots, and
+  // slower (the kernel around it compiles differently) for the 2- and
+  // 4-bit per-channel-key layers with 4 head slots.
   constexpr int kMB = GT == 1 ? 16 : 8;
+  constexpr int H = PAIR && GT > 1 ? 2 : 1;
   const int b = s / G.Hkv, hk = s % G.Hkv;
   const size_t slot0 = (size_t)(wf + s);
-  for (int r = 0; r < g; ++r) {
-    auto acc_at = [&](int q) {
-      return __ldcg(reinterpret_cast<const float4*>(&p.part_acc[((slot0 + q) * g + r) * kHeadDim + 4 * lane]));
-    };
-    float mq = -INFINITY, lq = 0.0f;
-    if (lane < count) {
-      mq = __ldcg(&p.part_ml[((slot0 + lane) * g + r) * 2]);
-      lq = __ldcg(&p.part_ml[((slot0 + lane) * g + r) * 2 + 1]);
-    }
-    float4 a[kMB];
+  for (int r0 = 0; r0 < g; r0 += H) {
+    bool live[H];
 #pragma unroll
-    for (int u = 0; u < kMB; ++u) a[u] = u < count ? acc_at(u) : make_float4(0.f, 0.f, 0.f, 0.f);
-    float M = mq;
-    for (int q0 = lane + 32; q0 < count; q0 += 32) M = fmaxf(M, __ldcg(&p.part_ml[((slot0 + q0) * g + r) * 2]));
-    M = warp_max(M);
-    float L = 0.0f, v[4] = {0, 0, 0, 0};
+    for (int h = 0; h < H; ++h) live[h] = r0 + h < g;  // warp-uniform
+    auto acc_at = [&](int h, int q) {
+      return __ldcg(reinterpret_cast<const float4*>(&p.part_acc[((slot0 + q) * g + r0 + h) * kHeadDim + 4 * lane]));
+    };
+    auto ml_at = [&](int h, int q, int i) { return __ldcg(&p.part_ml[((slot0 + q) * g + r0 + h) * 2 + i]); };
+    float mq[H], lq[H];
+    float4 a[H][kMB];
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+      mq[h] = -INFINITY;
+      lq[h] = 0.0f;
+      if (live[h] && lane < count) {
+        mq[h] = ml_at(h, lane, 0);
+        lq[h] = ml_at(h, lane, 1);
+      }
+#pragma unroll
+      for (int u = 0; u < kMB; ++u) a[h][u] = live[h] && u < count ? acc_at(h, u) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float M[H], L[H], v[H][4];
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+      M[h] = mq[h];
+      if (live[h])
+        for (int q0 = lane + 32; q0 < count; q0 += 32) M[h] = fmaxf(M[h], ml_at(h, q0, 0));
+      M[h] = warp_max(M[h]);
+      L[h] = 0.0f;
+      v[h][0] = v[h][1] = v[h][2] = v[h][3] = 0.0f;
+    }
     for (int c0 = 0; c0 < count; c0 += 32) {
       // lane q: weight of slot c0 + q
-      if (c0 > 0 && c0 + lane < count) {
-        mq = __ldcg(&p.part_ml[((slot0 + c0 + lane) * g + r) * 2]);
-        lq = __ldcg(&p.part_ml[((slot0 + c0 + lane) * g + r) * 2 + 1]);
-      }
-      float e = 0.0f;
-      if (c0 + lane < count) {
-        e = (mq == -INFINITY) ? 0.0f : exp2f(mq - M);
-        L += e * lq;
+      float e[H];
+#pragma unroll
+      for (int h = 0; h < H; ++h) {
+        if (c0 > 0 && live[h] && c0 + lane < count) {
+          mq[h] = ml_at(h, c0 + lane, 0);
+          lq[h] = ml_at(h, c0 + lane, 1);
+        }
+        e[h] = 0.0f;
+        if (c0 + lane < count) {
+          e[h] = (mq[h] == -INFINITY) ? 0.0f : exp2f(mq[h] - M[h]);
+          L[h] += e[h] * lq[h];
+        }
       }
       const int n = min(32, count - c0);
       for (int q = 0; q < n; q += kMB) {
         if (c0 + q > 0) {
 #pragma unroll
-          for (int u = 0; u < kMB; ++u) a[u] = q + u < n ? acc_at(c0 + q + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int h = 0; h < H; ++h)
+#pragma unroll
+            for (int u = 0; u < kMB; ++u)
+              a[h][u] = live[h] && q + u < n ? acc_at(h, c0 + q + u) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int u = 0; u < kMB; ++u) {
-          const float eq = __shfl_sync(0xffffffffu, e, (q + u) & 31);  // 0 past the last slot
-          v[0] = fmaf(eq, a[u].x, v[0]);
-          v[1] = fmaf(eq, a[u].y, v[1]);
-          v[2] = fmaf(eq, a[u].z, v[2]);
-          v[3] = fmaf(eq, a[u].w, v[3]);
-        }
+        for (int u = 0; u < kMB; ++u)
+#pragma unroll
+          for (int h = 0; h < H; ++h) {
+            const float eq = __shfl_sync(0xffffffffu, e[h], (q + u) & 31);  // 0 past the last slot
+            v[h][0] = fmaf(eq, a[h][u].x, v[h][0]);
+            v[h][1] = fmaf(eq, a[h][u].y, v[h][1]);
+            v[h][2] = fmaf(eq, a[h][u].z, v[h][2]);
+            v[h][3] = fmaf(eq, a[h][u].w, v[h][3]);
+          }
       }
     }
-    L = warp_sum(L);
-    const size_t o = q_row(G, b, hk, r) * kHeadDim + 4 * lane;
-    const __half2 h0 = __floats2half2_rn(v[0] / L, v[1] / L), h1 = __floats2half2_rn(v[2] / L, v[3] / L);
-    uint2 stv;
-    stv.x = h2_as_u32(h0);
-    stv.y = h2_as_u32(h1);
-    *reinterpret_cast<uint2*>(p.out + o) = stv;
-    if (p.lse && lane == 0) p.lse[q_row(G, b, hk, r)] = (M + log2f(L)) * 0.6931471805599453f;
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+      if (!live[h]) continue;
+      const int r = r0 + h;
+      const float Lh = warp_sum(L[h]);
+      const size_t o = q_row(G, b, hk, r) * kHeadDim + 4 * lane;
+      const __half2 h0 = __floats2half2_rn(v[h][0] / Lh, v[h][1] / Lh), h1 = __floats2half2_rn(v[h][2] / Lh, v[h][3] / Lh);
+      uint2 stv;
+      stv.x = h2_as_u32(h0);
+      stv.y = h2_as_u32(h1);
+      *reinterpret_cast<uint2*>(p.out + o) = stv;
+      if (p.lse && lane == 0) p.lse[q_row(G, b, hk, r)] = (M[h] + log2f(Lh)) * 0.6931471805599453f;
+    }
   }
   if (lane == 0) p.counters[s] = 0u;
 }
@@ -409,7 +446,8 @@ __global__ void __launch_bounds__(PersistLayout<KB, VB, NT, GT, IQ>::kCtaThreads
     const StreamSpan fs = stream_span_t<RG>(p, sf);
     const int wf = owner_of(p, item_pos_in(p, fs, 0));
     const int wl = owner_of(p, item_pos_in(p, fs, fs.n_items - 1));
-    finalize_stream<NT, GT>(p, gw + sf, sf, wf, wl - wf + 1, sO, sML, staged, lane, O, m_used, lsum);
+    finalize_stream<NT, GT, (KB == 8 || IQ || GT == 8)>(p, gw + sf, sf, wf, wl - wf + 1, sO, sML, staged, lane, O,
+                                                         m_used, lsum);
     reset();
     has_q = staged = bq_f16 = false;
   };
