@@ -223,7 +223,8 @@ struct DecodeParams {
   double theta[kHeadDim / 2];  // RoPE frequencies rope_theta^(-2i/d), fp64
   // persistent schedule (tensor-core / fp16 kernels): the streams' work items
   // -- ng quantized 32-token groups, then nt fp16 items of a few tokens each --
-  // laid end to end, weighted by their bytes, cut into nwarps equal ranges.
+  // laid end to end, weighted (wq, wt: see plan_persist), cut into nwarps
+  // equal ranges.
   int ng, nt, n_items;
   int nwarps;
   long long wq, wt, wstream, wtot;
@@ -375,7 +376,7 @@ inline void plan_rows(DecodeParams& p, long long* items, bool* any_groups) {
 }
 
 // Persistent-schedule arithmetic shared by host and device: items laid
-// stream after stream, weighted by their bytes; RG selects the ragged
+// stream after stream, weighted by wq and wt; RG selects the ragged
 // schedule at compile time (the wrappers below take p.ragged).
 // (Dividends stay below 2^56: plan_persist checks (wtot + 1) (nwarps + 1) < 2^56.)
 // Ragged schedule, item j of batch row b: its stream s and index k.

@@ -316,7 +316,7 @@ KVQ_API kvq_status kvq_append_ragged(const kvq_config *cfg, void *layer_buf, con
  *              launch parameters
  *   other arguments as kvq_decode_attn.
  * Runs the kernel kvq_decode_attn would: the persistent kernel lays every
- * stream's own work items end to end and cuts them into equal byte ranges;
+ * stream's own work items end to end and cuts them into equal ranges;
  * the split-K kernel is planned for the longest row (a stream's splits past
  * its own tokens contribute nothing).
  * Errors: as kvq_decode_attn; KVQ_ERR_UNSUPPORTED when batch > 256. */
