@@ -15,7 +15,8 @@
 using namespace kvq;
 int main() {
   int bad = 0, cases = 0;
-  for (int NS : {1, 2, 7, 32, 256}) for (int ng : {0, 1, 3, 31, 125}) for (int nt : {0, 1, 3, 12}) for (long long wq : {3328LL, 5376LL, 9984LL}) for (long long wt : {4096LL, 16384LL}) {
+  for (int NS : {1, 2, 7, 32, 256}) for (int ng : {0, 1, 3, 31, 125}) for (int nt : {0, 1, 3, 12}) for (long long wq : {3328LL, 5376LL, 9984LL}) for (long long wt : {4096LL, 16384LL, 0LL}) {
+    if (wt == 0) wt = wq;  // every item one group's weight (the quantized cache's schedule)
     if (ng + nt == 0) continue;
     DecodeParams p{}; p.ng = ng; p.nt = nt; p.n_items = ng + nt; p.wq = wq; p.wt = wt;
     p.wstream = ng * wq + nt * p.wt; p.wtot = NS * p.wstream;
@@ -66,7 +67,7 @@ int main() {
       p.geo.S = p.geo.fp16_mode ? 0 : (int)(rr() % 5);
       p.geo.R = p.geo.fp16_mode ? 0 : (int)(rr() % 70);
       p.wq = (trial & 1) ? 5376 : 9984;
-      p.wt = 8 * 128 * 4;
+      p.wt = trial % 3 == 1 ? p.wq : 8 * 128 * 4;  // equal item weights, or an fp16 item's bytes
       const int tmax = 1 + (int)(rr() % (trial % 3 == 0 ? 5000 : 300));
       for (int b = 0; b < p.geo.B; ++b) tab.tokens[b] = 1 + (int)(rr() % tmax);
       long long items;
