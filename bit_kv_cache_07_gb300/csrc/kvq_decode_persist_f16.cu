@@ -58,8 +58,11 @@ cudaError_t plan_persist(DecodeParams& p, uint64_t* ws_need) {
   // finished last: the 32k mixed-pair step took 2.7 % longer
   const long long wgroup = (long long)kGroupTokens * (G.krow + G.vrow) +
                            (G.gkc ? kGroupTokens * G.nkg * 4 : kHeadDim * 4) + kGroupTokens * G.nvg * 4;
+  // (with 5-8 query heads per KV head an fp16 item weighs 5/4 of a group:
+  // its 8 tokens carry every head's scores and products on the tensor cores
+  // at half-filled tiles, and those warps still finished ~4 % late)
   p.wq = G.fp16_mode ? 1 : wgroup;
-  p.wt = G.fp16_mode ? (long long)mma::kF16Tokens * kHeadDim * 2 * 2 : wgroup;
+  p.wt = G.fp16_mode ? (long long)mma::kF16Tokens * kHeadDim * 2 * 2 : (G.g > 4 ? wgroup * 5 / 4 : wgroup);
   p.wstream = (long long)p.ng * p.wq + (long long)p.nt * p.wt;
   p.wtot = (long long)G.NS * p.wstream;
   long long items = (long long)G.NS * p.n_items;
